@@ -1,0 +1,542 @@
+/*
+ * ezoracle.c -- plain CPU reference of the lossless BF16 exponent codecs.
+ *
+ * TEST INFRASTRUCTURE.  Only the tests, the smoke check and the benchmark's
+ * CPU-baseline leg use this file.  It is deliberately slow and literal: one
+ * value at a time, in value order, no blocking and no fusion, so that each
+ * step can be checked against the pages by eye.  It shares no code, header,
+ * table or constant with the CUDA library.
+ *
+ * Byte layouts (all integers little-endian, all padding bytes zero):
+ *
+ * BF16 split [CIERA, exponent-reuse paragraph; ZIP 3.1]
+ *   h = 16 bits: sign s = h>>15, exponent E = (h>>7)&0xFF, mantissa m = h&0x7F.
+ *   sign+mantissa byte SM = (s<<7)|m.  merge(SM,E) = ((SM&0x80)<<8)|(E<<7)|(SM&0x7F).
+ *
+ * Shards / per-peer chunks
+ *   L = 128 * ceil(ceil(n/W)/128); shard r covers [r*L, min((r+1)*L, n)).
+ *
+ * code3 chunk [ZIP 3.1 code and layout; 3.2 AllGather/AlltoAll]
+ *   header 128 B: "EZC3", u8 version=1, u8 E0, u16 0, u64 n_c, u64 n_esc,
+ *                 u64 chunk_bytes, u32 chunk index, u32 W, zeros
+ *   SM    : n_c bytes, padded to 128
+ *   P0..P2: ceil(n_c/8) bytes each, padded to 128; bit p of code(j) is bit
+ *           (j&7) of byte (j>>3) of plane p
+ *   ESC   : n_esc raw exponent bytes in value order, padded to 128
+ *   code(j) = E-E0+1 when E0 <= E <= E0+6, else 0 (escape)
+ *
+ * reuse payload [CIERA, exponent-reuse and gain-formula paragraphs]
+ *   header 64 B: "EZRU", u8 version=1, u8 flags (bit0 exponents code3-coded,
+ *                bit1 cold), u8 E0, u8 0, u32 B, u32 shard index, u64 n_s,
+ *                u64 n_changed, u64 m, u64 n_esc, u64 total_bytes, u64 0
+ *   BM : ceil(nb/8) bytes, nb = ceil(n_s/B); bit k = block k changed, bit
+ *        (k&7) of byte (k>>3); padded to 16
+ *   SM : n_s bytes, padded to 16
+ *   EXP: raw  -> the m exponent bytes of the changed blocks, block order
+ *        coded-> planes P0..P2 of the code3 code of those m exponents (each
+ *               ceil(m/8) bytes padded to 16), then n_esc escape bytes
+ *   total padded to 128.
+ */
+#include "ezoracle.h"
+
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ------------------------------------------------------------------ split */
+
+static uint8_t bf16_exp(uint16_t h) { return (uint8_t)((h >> 7) & 0xFF); }
+static uint8_t bf16_sm(uint16_t h) { return (uint8_t)(((h >> 8) & 0x80) | (h & 0x7F)); }
+static uint16_t bf16_merge(uint8_t sm, uint8_t e)
+{
+    return (uint16_t)(((uint16_t)(sm & 0x80) << 8) | ((uint16_t)e << 7) | (sm & 0x7F));
+}
+
+static uint64_t ceil_div(uint64_t a, uint64_t b) { return (a + b - 1) / b; }
+static uint64_t round_up(uint64_t a, uint64_t b) { return ceil_div(a, b) * b; }
+
+uint64_t orc_shard_len(uint64_t n, uint32_t W)
+{
+    return round_up(ceil_div(n, W), 128);
+}
+
+uint64_t orc_shard_count(uint64_t n, uint32_t W, uint32_t r)
+{
+    uint64_t L = orc_shard_len(n, W);
+    uint64_t a = (uint64_t)r * L;
+    if (a >= n) return 0;
+    return (n - a < L) ? n - a : L;
+}
+
+/* little-endian field access */
+static void put_u32(uint8_t* p, uint32_t v)
+{
+    for (int i = 0; i < 4; i++) p[i] = (uint8_t)(v >> (8 * i));
+}
+static void put_u64(uint8_t* p, uint64_t v)
+{
+    for (int i = 0; i < 8; i++) p[i] = (uint8_t)(v >> (8 * i));
+}
+static uint32_t get_u32(const uint8_t* p)
+{
+    uint32_t v = 0;
+    for (int i = 3; i >= 0; i--) v = (v << 8) | p[i];
+    return v;
+}
+static uint64_t get_u64(const uint8_t* p)
+{
+    uint64_t v = 0;
+    for (int i = 7; i >= 0; i--) v = (v << 8) | p[i];
+    return v;
+}
+
+/* ------------------------------------------------------------ big integer */
+/* Non-negative integers of 768 bits, used only to sum the moments exactly. */
+
+#define BIG_LIMBS 24
+typedef struct { uint32_t w[BIG_LIMBS]; } big_t;
+
+static void big_add_pow2(big_t* a, unsigned pos)
+{
+    unsigned i = pos / 32;
+    uint32_t add = 1u << (pos % 32);
+    while (i < BIG_LIMBS) {
+        uint32_t old = a->w[i];
+        a->w[i] = old + add;
+        if (a->w[i] >= old) return;   /* no carry out */
+        add = 1;
+        i++;
+    }
+    abort();                          /* cannot happen for n < 2**40 */
+}
+
+/* a += v * 2**sh, one set bit of v at a time */
+static void big_add_shifted(big_t* a, uint64_t v, unsigned sh)
+{
+    for (unsigned i = 0; i < 64; i++)
+        if ((v >> i) & 1u) big_add_pow2(a, sh + i);
+}
+
+static int big_cmp(const big_t* a, const big_t* b)
+{
+    for (int i = BIG_LIMBS - 1; i >= 0; i--) {
+        if (a->w[i] != b->w[i]) return a->w[i] > b->w[i] ? 1 : -1;
+    }
+    return 0;
+}
+
+/* a -= b, requires a >= b */
+static void big_sub(big_t* a, const big_t* b)
+{
+    uint32_t borrow = 0;
+    for (int i = 0; i < BIG_LIMBS; i++) {
+        uint64_t ai = a->w[i], bi = (uint64_t)b->w[i] + borrow;
+        a->w[i] = (uint32_t)(ai - bi);
+        borrow = ai < bi;
+    }
+}
+
+static int big_bit(const big_t* a, int pos)
+{
+    return (a->w[pos / 32] >> (pos % 32)) & 1u;
+}
+
+static int big_bitlen(const big_t* a)
+{
+    for (int pos = 32 * BIG_LIMBS - 1; pos >= 0; pos--)
+        if (big_bit(a, pos)) return pos + 1;
+    return 0;
+}
+
+/* a * 2**scale rounded to the nearest double, ties to even */
+static double big_round(const big_t* a, int scale)
+{
+    int L = big_bitlen(a);
+    if (L == 0) return 0.0;
+    uint64_t q = 0;
+    if (L <= 53) {
+        for (int i = L - 1; i >= 0; i--) q = 2 * q + (uint64_t)big_bit(a, i);
+        return ldexp((double)q, scale);
+    }
+    for (int i = L - 1; i >= L - 53; i--) q = 2 * q + (uint64_t)big_bit(a, i);
+    int half = big_bit(a, L - 54);
+    int sticky = 0;
+    for (int i = L - 55; i >= 0; i--) sticky |= big_bit(a, i);
+    if (half && (sticky || (q & 1u))) q++;
+    return ldexp((double)q, L - 53 + scale);
+}
+
+/* ------------------------------------------------------------ statistics */
+
+/* K = 16383 / (14 ln 2): sigma^2 >= K * 2^(2k-1)  <=>  x_opt + 1/2 >= k,
+ * with x_opt = log2(sigma) + (1/2) log2(14 ln 2 / 16383)  [ZIP 3.1, Eq. for
+ * x_opt].  So the integer nearest x_opt (ties up) is the largest such k. */
+double orc_window_K(void)
+{
+    return 16383.0 / (14.0 * log(2.0));
+}
+
+uint32_t orc_window_from_var(double var)
+{
+    double K = orc_window_K();
+    uint32_t E0 = 0;
+    for (int e = 1; e <= 249; e++) {       /* E0 = 127 + x0, clamped to 0..249 */
+        int k = e - 127;
+        if (var >= ldexp(K, 2 * k - 1)) E0 = (uint32_t)e;
+    }
+    return E0;
+}
+
+int orc_stats_compute(const uint16_t* x, uint64_t n, orc_stats* st)
+{
+    int64_t S1[256];
+    uint64_t S2[256];
+    memset(st, 0, sizeof(*st));
+    memset(S1, 0, sizeof(S1));
+    memset(S2, 0, sizeof(S2));
+    st->n = n;
+    /* exact per-exponent moments of v = (-1)^s * M * 2^(k(E)),
+     * M = E ? 128+m : m, k(E) = (E ? E : 1) - 134 */
+    for (uint64_t i = 0; i < n; i++) {
+        uint16_t h = x[i];
+        unsigned E = bf16_exp(h);
+        st->hist[E]++;
+        if (E == 255) continue;            /* Inf / NaN stay out of sigma */
+        st->n_finite++;
+        int64_t M = (E ? 128 : 0) + (h & 0x7F);
+        S1[E] += (h & 0x8000) ? -M : M;
+        S2[E] += (uint64_t)(M * M);
+    }
+    /* s1 = sum_E S1[E] * 2^(k(E)), exactly, as (P - Q) * 2^-133 */
+    big_t P, Q, R;
+    memset(&P, 0, sizeof(P));
+    memset(&Q, 0, sizeof(Q));
+    memset(&R, 0, sizeof(R));
+    for (unsigned E = 0; E < 255; E++) {
+        unsigned sh = (E ? E : 1) - 1;     /* k(E) + 133 */
+        if (S1[E] >= 0) big_add_shifted(&P, (uint64_t)S1[E], sh);
+        else big_add_shifted(&Q, (uint64_t)(-S1[E]), sh);
+        big_add_shifted(&R, S2[E], 2 * sh);  /* s2 = R * 2^-266 */
+    }
+    if (big_cmp(&P, &Q) >= 0) {
+        big_sub(&P, &Q);
+        st->s1 = big_round(&P, -133);
+    } else {
+        big_sub(&Q, &P);
+        st->s1 = -big_round(&Q, -133);
+    }
+    st->s2 = big_round(&R, -266);
+    st->K = orc_window_K();
+    st->rule = 1;
+    if (st->n_finite >= 2) {
+        double N = (double)st->n_finite;
+        double var = (st->s2 - st->s1 * (st->s1 / N)) / (N - 1.0);
+        st->var = var;
+        if (var > 0 && isfinite(var)) {
+            st->sigma = sqrt(var);
+            st->E0 = orc_window_from_var(var);
+            st->rule = 0;
+        }
+    }
+    if (st->rule == 1) {
+        /* fallback: the 7 consecutive exponent bins with the most values */
+        uint64_t best = 0;
+        uint32_t best_b = 0;
+        for (uint32_t b = 0; b <= 249; b++) {
+            uint64_t c = 0;
+            for (uint32_t E = b; E <= b + 6; E++) c += st->hist[E];
+            if (c > best) { best = c; best_b = b; }
+        }
+        st->E0 = best_b;
+    }
+    uint64_t in_window = 0;
+    for (uint32_t E = st->E0; E <= st->E0 + 6; E++) in_window += st->hist[E];
+    st->n_escape = n - in_window;
+    return 0;
+}
+
+/* ------------------------------------------------------------------ code3 */
+
+static unsigned code_of(unsigned E, unsigned E0)
+{
+    return (E >= E0 && E <= E0 + 6) ? E - E0 + 1 : 0;
+}
+
+uint64_t orc_code3_chunk_bytes(uint64_t n_c, uint64_t n_esc)
+{
+    return 128 + round_up(n_c, 128) + 3 * round_up(ceil_div(n_c, 8), 128)
+           + round_up(n_esc, 128);
+}
+
+uint64_t orc_code3_slot_bytes(uint64_t n, uint32_t W)
+{
+    uint64_t L = orc_shard_len(n, W);
+    return orc_code3_chunk_bytes(L, L);
+}
+
+int orc_code3_encode(const uint16_t* x, uint64_t n, uint32_t W, uint32_t E0,
+                     uint8_t* out, uint64_t slot_bytes, uint64_t* sizes)
+{
+    if (W == 0 || E0 > 249) return -1;
+    uint64_t L = orc_shard_len(n, W);
+    for (uint32_t c = 0; c < W; c++) {
+        uint64_t n_c = orc_shard_count(n, W, c);
+        const uint16_t* xc = x + (uint64_t)c * L;
+        uint8_t* o = out + (uint64_t)c * slot_bytes;
+        uint64_t n_esc = 0;
+        for (uint64_t j = 0; j < n_c; j++)
+            if (code_of(bf16_exp(xc[j]), E0) == 0) n_esc++;
+        uint64_t bytes = orc_code3_chunk_bytes(n_c, n_esc);
+        if (bytes > slot_bytes) return -2;
+        memset(o, 0, bytes);
+        o[0] = 'E'; o[1] = 'Z'; o[2] = 'C'; o[3] = '3';
+        o[4] = 1;
+        o[5] = (uint8_t)E0;
+        put_u64(o + 8, n_c);
+        put_u64(o + 16, n_esc);
+        put_u64(o + 24, bytes);
+        put_u32(o + 32, c);
+        put_u32(o + 36, W);
+        uint64_t off_sm = 128;
+        uint64_t plane = round_up(ceil_div(n_c, 8), 128);
+        uint64_t off_p = off_sm + round_up(n_c, 128);
+        uint64_t off_e = off_p + 3 * plane;
+        uint64_t k = 0;
+        for (uint64_t j = 0; j < n_c; j++) {
+            uint16_t h = xc[j];
+            unsigned E = bf16_exp(h);
+            unsigned code = code_of(E, E0);
+            o[off_sm + j] = bf16_sm(h);
+            for (unsigned p = 0; p < 3; p++)
+                if ((code >> p) & 1u) o[off_p + p * plane + j / 8] |= (uint8_t)(1u << (j % 8));
+            if (code == 0) o[off_e + k++] = (uint8_t)E;
+        }
+        sizes[c] = bytes;
+    }
+    return 0;
+}
+
+uint32_t orc_code3_decode(const uint8_t* in, const uint64_t* offsets,
+                          uint64_t n, uint32_t W, uint16_t* out)
+{
+    uint32_t status = 0;
+    uint64_t L = orc_shard_len(n, W);
+    for (uint32_t c = 0; c < W; c++) {
+        uint64_t n_c = orc_shard_count(n, W, c);
+        if (offsets[c + 1] < offsets[c]) { status |= ORC_BAD_SIZE; continue; }
+        uint64_t avail = offsets[c + 1] - offsets[c];
+        if (avail < 128) { status |= ORC_BAD_SIZE; continue; }
+        const uint8_t* p = in + offsets[c];
+        if (!(p[0] == 'E' && p[1] == 'Z' && p[2] == 'C' && p[3] == '3') || p[4] != 1
+            || p[5] > 249 || get_u64(p + 8) != n_c || get_u32(p + 32) != c
+            || get_u32(p + 36) != W) {
+            status |= ORC_BAD_HEADER;
+            continue;
+        }
+        unsigned E0 = p[5];
+        uint64_t n_esc = get_u64(p + 16);
+        if (n_esc > n_c) { status |= ORC_BAD_COUNT; continue; }
+        uint64_t bytes = get_u64(p + 24);
+        if (bytes != orc_code3_chunk_bytes(n_c, n_esc) || bytes > avail) {
+            status |= ORC_BAD_SIZE;
+            continue;
+        }
+        uint64_t plane = round_up(ceil_div(n_c, 8), 128);
+        const uint8_t* sm = p + 128;
+        const uint8_t* pl = sm + round_up(n_c, 128);
+        const uint8_t* esc = pl + 3 * plane;
+        uint16_t* oc = out + (uint64_t)c * L;
+        uint64_t k = 0;
+        for (uint64_t j = 0; j < n_c; j++) {
+            unsigned code = 0;
+            for (unsigned b = 0; b < 3; b++)
+                code |= ((pl[b * plane + j / 8] >> (j % 8)) & 1u) << b;
+            unsigned E;
+            if (code) {
+                E = E0 + code - 1;
+            } else if (k < n_esc) {
+                E = esc[k++];
+            } else {
+                status |= ORC_BAD_COUNT;
+                E = 0;
+            }
+            oc[j] = bf16_merge(sm[j], (uint8_t)E);
+        }
+        if (k != n_esc) status |= ORC_BAD_COUNT;
+    }
+    return status;
+}
+
+/* ------------------------------------------------------------------ reuse */
+
+uint64_t orc_reuse_bytes(uint64_t n_s, uint32_t B, uint64_t m, int coded,
+                         uint64_t n_esc)
+{
+    uint64_t nb = ceil_div(n_s, B);
+    uint64_t exp_bytes = coded ? 3 * round_up(ceil_div(m, 8), 16) + n_esc : m;
+    return round_up(64 + round_up(ceil_div(nb, 8), 16) + round_up(n_s, 16) + exp_bytes, 128);
+}
+
+uint64_t orc_reuse_slot_bytes(uint64_t n, uint32_t W, uint32_t B, int coded)
+{
+    uint64_t L = orc_shard_len(n, W);
+    return orc_reuse_bytes(L, B, L, coded, coded ? L : 0);
+}
+
+int orc_reuse_encode(const uint16_t* shard, uint64_t n_s, uint32_t B,
+                     uint32_t shard_index, uint8_t* send_cache, int cold,
+                     int coded, orc_stats* st, uint8_t* out, uint64_t cap,
+                     uint64_t* size)
+{
+    if (B == 0) return -1;
+    uint64_t nb = ceil_div(n_s, B);
+    uint8_t* changed = (uint8_t*)calloc(nb ? nb : 1, 1);
+    uint8_t* exps = (uint8_t*)malloc(n_s ? n_s : 1);
+    if (!changed || !exps) { free(changed); free(exps); return -3; }
+    /* changed_k = cold or some exponent differs from the sender's cache */
+    uint64_t n_changed = 0, m = 0;
+    for (uint64_t k = 0; k < nb; k++) {
+        uint64_t a = k * B, b = (k + 1) * B < n_s ? (k + 1) * B : n_s;
+        int ch = cold;
+        for (uint64_t i = a; i < b; i++)
+            if (bf16_exp(shard[i]) != send_cache[i]) ch = 1;
+        changed[k] = (uint8_t)ch;
+        if (ch) {
+            n_changed++;
+            for (uint64_t i = a; i < b; i++) exps[m++] = bf16_exp(shard[i]);
+        }
+    }
+    uint32_t E0 = 0;
+    uint64_t n_esc = 0;
+    if (coded) {
+        /* the code window comes from this shard's sigma [ZIP 3.1] */
+        orc_stats local;
+        orc_stats* s = st ? st : &local;
+        orc_stats_compute(shard, n_s, s);
+        E0 = s->E0;
+        for (uint64_t j = 0; j < m; j++)
+            if (code_of(exps[j], E0) == 0) n_esc++;
+    }
+    uint64_t total = orc_reuse_bytes(n_s, B, m, coded, n_esc);
+    if (total > cap) { free(changed); free(exps); return -2; }
+    memset(out, 0, total);
+    out[0] = 'E'; out[1] = 'Z'; out[2] = 'R'; out[3] = 'U';
+    out[4] = 1;
+    out[5] = (uint8_t)((coded ? 1 : 0) | (cold ? 2 : 0));
+    out[6] = (uint8_t)E0;
+    put_u32(out + 8, B);
+    put_u32(out + 12, shard_index);
+    put_u64(out + 16, n_s);
+    put_u64(out + 24, n_changed);
+    put_u64(out + 32, m);
+    put_u64(out + 40, n_esc);
+    put_u64(out + 48, total);
+    uint64_t off_bm = 64;
+    uint64_t off_sm = off_bm + round_up(ceil_div(nb, 8), 16);
+    uint64_t off_x = off_sm + round_up(n_s, 16);
+    for (uint64_t k = 0; k < nb; k++)
+        if (changed[k]) out[off_bm + k / 8] |= (uint8_t)(1u << (k % 8));
+    for (uint64_t i = 0; i < n_s; i++) out[off_sm + i] = bf16_sm(shard[i]);
+    if (!coded) {
+        for (uint64_t j = 0; j < m; j++) out[off_x + j] = exps[j];
+    } else {
+        uint64_t plane = round_up(ceil_div(m, 8), 16);
+        uint64_t off_e = off_x + 3 * plane, k = 0;
+        for (uint64_t j = 0; j < m; j++) {
+            unsigned code = code_of(exps[j], E0);
+            for (unsigned p = 0; p < 3; p++)
+                if ((code >> p) & 1u) out[off_x + p * plane + j / 8] |= (uint8_t)(1u << (j % 8));
+            if (code == 0) out[off_e + k++] = exps[j];
+        }
+    }
+    /* the sender's cache now holds this iteration's exponents */
+    for (uint64_t k = 0; k < nb; k++) {
+        if (!changed[k]) continue;
+        uint64_t a = k * B, b = (k + 1) * B < n_s ? (k + 1) * B : n_s;
+        for (uint64_t i = a; i < b; i++) send_cache[i] = bf16_exp(shard[i]);
+    }
+    *size = total;
+    free(changed);
+    free(exps);
+    return 0;
+}
+
+uint32_t orc_reuse_decode(const uint8_t* p, uint64_t avail, uint64_t n_s,
+                          uint32_t B, uint32_t shard_index,
+                          uint8_t* recv_cache, uint16_t* out)
+{
+    if (avail < 64) return ORC_BAD_SIZE;
+    if (!(p[0] == 'E' && p[1] == 'Z' && p[2] == 'R' && p[3] == 'U') || p[4] != 1
+        || (p[5] & ~3u) != 0 || p[7] != 0 || get_u32(p + 8) != B
+        || get_u32(p + 12) != shard_index || get_u64(p + 16) != n_s)
+        return ORC_BAD_HEADER;
+    int coded = p[5] & 1;
+    unsigned E0 = p[6];
+    uint64_t n_changed = get_u64(p + 24), m = get_u64(p + 32);
+    uint64_t n_esc = get_u64(p + 40), total = get_u64(p + 48);
+    if (coded ? E0 > 249 : (E0 != 0 || n_esc != 0)) return ORC_BAD_HEADER;
+    uint64_t nb = ceil_div(n_s, B);
+    if (n_changed > nb || m > n_s || n_esc > m) return ORC_BAD_COUNT;
+    if (total != orc_reuse_bytes(n_s, B, m, coded, n_esc) || total > avail)
+        return ORC_BAD_SIZE;
+    uint64_t off_bm = 64;
+    uint64_t off_sm = off_bm + round_up(ceil_div(nb, 8), 16);
+    uint64_t off_x = off_sm + round_up(n_s, 16);
+    const uint8_t* bm = p + off_bm;
+    const uint8_t* sm = p + off_sm;
+    /* the bitmap must agree with the declared counts before anything is
+     * written to the receiver's cache */
+    uint64_t cnt = 0, len = 0;
+    for (uint64_t k = 0; k < nb; k++) {
+        if ((bm[k / 8] >> (k % 8)) & 1u) {
+            uint64_t a = k * B, b = (k + 1) * B < n_s ? (k + 1) * B : n_s;
+            cnt++;
+            len += b - a;
+        }
+    }
+    if (cnt != n_changed || len != m) return ORC_BAD_COUNT;
+    uint32_t status = 0;
+    uint64_t plane = round_up(ceil_div(m, 8), 16);
+    const uint8_t* esc = p + off_x + 3 * plane;
+    uint64_t j = 0, k_esc = 0;
+    for (uint64_t k = 0; k < nb; k++) {
+        uint64_t a = k * B, b = (k + 1) * B < n_s ? (k + 1) * B : n_s;
+        int ch = (bm[k / 8] >> (k % 8)) & 1u;
+        for (uint64_t i = a; i < b; i++) {
+            if (ch) {
+                unsigned E;
+                if (!coded) {
+                    E = p[off_x + j];
+                } else {
+                    unsigned code = 0;
+                    for (unsigned q = 0; q < 3; q++)
+                        code |= ((p[off_x + q * plane + j / 8] >> (j % 8)) & 1u) << q;
+                    if (code) E = E0 + code - 1;
+                    else if (k_esc < n_esc) E = esc[k_esc++];
+                    else { status |= ORC_BAD_COUNT; E = 0; }
+                }
+                j++;
+                recv_cache[i] = (uint8_t)E;   /* ExpCache takes the new block */
+            }
+            out[i] = bf16_merge(sm[i], recv_cache[i]);
+        }
+    }
+    if (coded && k_esc != n_esc) status |= ORC_BAD_COUNT;
+    return status;
+}
+
+uint32_t orc_gather_decode_reuse(const uint8_t* recv, const uint64_t* offsets,
+                                 uint64_t n, uint32_t W, uint32_t B,
+                                 uint8_t* recv_cache, uint16_t* out)
+{
+    uint32_t status = 0;
+    uint64_t L = orc_shard_len(n, W);
+    for (uint32_t r = 0; r < W; r++) {
+        uint64_t n_r = orc_shard_count(n, W, r);
+        if (offsets[r + 1] < offsets[r]) { status |= ORC_BAD_SIZE; continue; }
+        status |= orc_reuse_decode(recv + offsets[r], offsets[r + 1] - offsets[r],
+                                   n_r, B, r, recv_cache + (uint64_t)r * L,
+                                   out + (uint64_t)r * L);
+    }
+    return status;
+}
