@@ -1,0 +1,454 @@
+#!/usr/bin/env python
+"""Benchmark of the lossless BF16 exponent-codec hot path on one GB300.
+
+Workload: the ZipCCL 3-bit exponent codec tensor (2^26 BF16 values from
+N(0, 0.02), 0.5% of entries x100, 0.1% set to +0; W = 8 per-peer chunks).
+One step takes iteration t of that tensor (exponent flips at c = 0.003 per
+element per iteration, the per-element change rate quoted on the CIERA page)
+through every row of the hot path:
+
+  a1 stats + window -> a2 code3 encode -> a6/a5 code3 gather-decode
+  a3 reuse encode (B = 256, warm cache) -> a4/a5 reuse gather-decode
+  a3 reuse encode with 3-bit-coded exponents -> a5 gather-decode
+
+`value` = codec passes x uncompressed BF16 bytes / step time (six codec
+passes per step: three encodes and three gather-decodes; the stats pass is
+timed as part of the code3 encode).  Inputs are resident in HBM; L2 is
+flushed (a 512 MiB write) before every op, outside the op's timer.
+
+`--impl reference` times the CPU oracle on a bounded sample of the same
+workload (the reference arm of this build).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+N_VALUES = 1 << 26
+W_CHUNKS = 8
+B_BLOCK = 256
+FLIP_RATE = 0.003
+WORKLOAD = "zipccl_code3_64M_w8+ciera_reuse_b256_flip0.003"
+METRIC = "codec GB/s (uncompressed BF16) and % of HBM roofline; compression ratio"
+UNIT = "GB/s"
+PASSES = 6
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=60)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ dist
+
+def init_dist(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def reduce_max(world, v: float) -> float:
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64,
+                     device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi samples of the SM clock and throttle reasons while the
+    timed region runs."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.proc = None
+        self.path = os.path.join("/tmp", f"ez_clocks_{os.getpid()}.csv")
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(index), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------ ours
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs)"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback 6.8 TB/s"
+
+
+def make_chain(count: int):
+    import synth
+    xs = [synth.config2(N_VALUES, device="cuda")]
+    for t in range(1, count):
+        xs.append(synth.scale_drift_bench(xs[-1], t, rate=FLIP_RATE))
+    torch.cuda.synchronize()
+    return xs
+
+
+def run_ours(args, world, rank, local):
+    from lossless_bf16_exponent_codec_gb300 import binding as Bd
+    from lossless_bf16_exponent_codec_gb300 import build
+    from lossless_bf16_exponent_codec_gb300.codec import Codec
+    build.build()
+    n, W, B = N_VALUES, W_CHUNKS, B_BLOCK
+    K, Wm = args.steps, args.warmup
+    xs = make_chain(K + Wm + 1)
+    c3 = Codec(n, W)
+    ru = Codec(n, W, B, Bd.EZ_CODEC_REUSE)
+    rc = Codec(n, W, B, Bd.EZ_CODEC_REUSE_CODE3)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    s = torch.cuda.current_stream()
+    # iteration 0 primes the caches (cold)
+    ru.encode_reuse(xs[0], cold=True)
+    ru.gather_decode()
+    rc.encode_reuse(xs[0], cold=True)
+    rc.gather_decode()
+    ops = ["stats", "code3_encode", "code3_decode", "reuse_encode", "reuse_decode",
+           "reuse_code3_encode", "reuse_code3_decode"]
+
+    def step(x, evs):
+        def op(i, fn):
+            flush.zero_()
+            evs[i][0].record(s)
+            fn()
+            evs[i][1].record(s)
+        op(0, lambda: c3.stats(x))
+        op(1, lambda: c3.encode_code3(x))
+        op(2, lambda: c3.gather_decode())
+        op(3, lambda: ru.encode_reuse(x))
+        op(4, lambda: ru.gather_decode())
+        op(5, lambda: rc.encode_reuse(x))
+        op(6, lambda: rc.gather_decode())
+
+    def mk():
+        return [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in ops]
+
+    for i in range(Wm):
+        step(xs[1 + i], mk())
+    torch.cuda.synchronize()
+    for cdc in (c3, ru, rc):
+        assert cdc.status_word() == 0, "warm-up status"
+    # ---- timed region
+    all_evs = [mk() for _ in range(K)]
+    barrier(world)
+    torch.cuda.synchronize()
+    clk = ClockSampler(local)
+    time.sleep(0.25)
+    t_wall = time.perf_counter()
+    for k in range(K):
+        step(xs[1 + Wm + k], all_evs[k])
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall
+    barrier(world)
+    clocks = clk.stop()
+    op_ms = [0.0] * len(ops)
+    for evs in all_evs:
+        for i, (a, b) in enumerate(evs):
+            op_ms[i] += a.elapsed_time(b)
+    op_ms = [v / K for v in op_ms]
+    step_ms = sum(op_ms)
+    step_ms_max = reduce_max(world, step_ms)
+    # ---- verification of the last step (outside the timed region)
+    xl = xs[Wm + K]
+    ok = all(cdc.status_word() == 0 for cdc in (c3, ru, rc))
+    ok = ok and torch.equal(c3.full[:n], xl) and torch.equal(ru.full[:n], xl) \
+        and torch.equal(rc.full[:n], xl)
+    sz = {name: int(cdc.sizes.sum().item()) for name, cdc in
+          (("code3", c3), ("reuse", ru), ("reuse_code3", rc))}
+    # changed exponents in the last step, for the algorithmic byte counts
+    m_tot = 0
+    for r in range(W):
+        hdr = ru.out[r * ru.slot:r * ru.slot + 64].cpu().numpy()
+        m_tot += int(hdr[32:40].view(np.uint64)[0])
+    n_esc = sum(int(c3.out[r * c3.slot + 16:r * c3.slot + 24].cpu().numpy().view(np.uint64)[0])
+                for r in range(W))
+    peak, peak_src = measured_peak()
+    raw = 2 * n
+    alg = {   # algorithmic bytes per launch (read + write)
+        "stats": raw,
+        "code3_encode": raw + sz["code3"],
+        "code3_decode": sz["code3"] + raw,
+        "reuse_encode": raw + n + sz["reuse"] + m_tot,
+        "reuse_decode": sz["reuse"] + (n - m_tot) + raw + m_tot,
+        "reuse_code3_encode": raw + n + sz["reuse_code3"] + m_tot,
+        "reuse_code3_decode": sz["reuse_code3"] + (n - m_tot) + raw + m_tot,
+    }
+    per_op = {}
+    for i, name in enumerate(ops):
+        gbs = alg[name] / (op_ms[i] * 1e-3) / 1e9
+        per_op[name] = {"ms": round(op_ms[i], 4), "alg_bytes": alg[name],
+                        "hbm_GBs": round(gbs, 1), "frac": round(gbs / peak, 3),
+                        "uncompressed_GBs": round(raw / (op_ms[i] * 1e-3) / 1e9, 1)}
+    top = max(range(len(ops)), key=lambda i: op_ms[i])
+    ach = alg[ops[top]] / (op_ms[top] * 1e-3) / 1e9
+    roof = {"bound": "hbm", "kernel": ops[top], "achieved": round(ach, 1), "peak": peak,
+            "peak_source": peak_src, "unit": "GB/s", "frac": round(ach / peak, 3),
+            "traffic": None}
+    ratios = {k: round(raw / v, 4) for k, v in sz.items()}
+
+    def g(name):
+        return raw / (op_ms[ops.index(name)] * 1e-3) / 1e9
+
+    from lossless_bf16_exponent_codec_gb300 import breakeven as be
+    enc3 = raw / ((op_ms[0] + op_ms[1]) * 1e-3) / 1e9
+    bstar = {
+        "code3": be.break_even_allgather(sz["code3"] / raw, enc3, g("code3_decode"), W),
+        "reuse": be.break_even_allgather(sz["reuse"] / raw, g("reuse_encode"), g("reuse_decode"), W),
+        "reuse_code3": be.break_even_allgather(sz["reuse_code3"] / raw, g("reuse_code3_encode"),
+                                               g("reuse_code3_decode"), W),
+    }
+    value = world * PASSES * raw / (step_ms_max * 1e-3) / 1e9
+    e2e = None if args.no_e2e else run_e2e(args, world, xs, c3, ru, rc, s)
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+        "steps": K, "warmup": Wm, "ms_per_step": round(step_ms_max, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u16",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "n": n, "W": W, "B": B, "flip_rate": FLIP_RATE,
+                   "codec_passes_per_step": PASSES, "bytes_per_pass": raw,
+                   "l2": "512 MiB flush before every op, outside the op timers",
+                   "wall_ms_per_step_incl_flush": round(1e3 * t_wall / K, 3)},
+        "roofline": roof,
+        "ops": per_op,
+        "compression_ratio": ratios,
+        "break_even_allgather_GBs": {k: round(v, 1) for k, v in bstar.items()},
+        "verified": bool(ok),
+        "gpu_launches": 8 * K,
+        "clocks": clocks,
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    return line, (rank == 0)
+
+
+def run_e2e(args, world, xs, c3, ru, rc, s):
+    """Same metric through the public calls with host inputs: each step copies
+    the iteration's tensor from pinned host memory, runs the six passes and
+    reads back the three size tables and status words."""
+    K = min(args.steps, 20)
+    n = N_VALUES
+    start = len(xs) - K - 1
+    hosts = [xs[start + 1 + k].cpu().pin_memory() for k in range(K)]
+    dev = torch.empty_like(xs[0])
+    # prime the caches with the iteration before
+    ru.encode_reuse(xs[start])
+    ru.gather_decode()
+    rc.encode_reuse(xs[start])
+    rc.gather_decode()
+    out_sizes = torch.empty(3 * W_CHUNKS + 3, dtype=torch.int64).pin_memory()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    for k in range(K):
+        dev.copy_(hosts[k], non_blocking=True)
+        c3.stats(dev)
+        c3.encode_code3(dev)
+        c3.gather_decode()
+        ru.encode_reuse(dev)
+        ru.gather_decode()
+        rc.encode_reuse(dev)
+        rc.gather_decode()
+        res = torch.cat([c3.sizes, ru.sizes, rc.sizes, c3.status.long(), ru.status.long(),
+                         rc.status.long()])
+        out_sizes.copy_(res, non_blocking=True)
+    e1.record(s)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / K
+    ms = reduce_max(world, ms)
+    barrier(world)
+    return {"value": round(world * PASSES * 2 * n / (ms * 1e-3) / 1e9, 1), "unit": UNIT,
+            "ms_per_step": round(ms, 4), "h2d_bytes_per_step": 2 * n,
+            "d2h_bytes_per_step": int(out_sizes.numel() * 8)}
+
+
+# ------------------------------------------------------------------ oracle
+
+def oracle_sample(seconds: float, n_sample: int = 1 << 22):
+    """The CPU oracle, single-threaded, on the first n_sample values of the
+    workload (W = 8), through the same six passes, iteration after iteration
+    until `seconds` of oracle work.  Drawing each iteration's flips is not
+    timed.  Returns (iterations, seconds, n_sample)."""
+    import oracle
+    import synth
+    oracle.build()
+    W, B = W_CHUNKS, B_BLOCK
+    cur = synth.config2(n_sample)
+    caches = {c: (np.zeros(n_sample, np.uint8), np.zeros(n_sample, np.uint8)) for c in (False, True)}
+    x0 = cur.numpy().view(np.uint16)
+    for coded, (send, recv) in caches.items():          # cold iteration, untimed
+        sl, sz, slot, _ = oracle.reuse_encode_all(x0, W, B, send, cold=True, coded=coded)
+        rb, of = oracle.compact(sl, sz, slot)
+        oracle.gather_decode_reuse(rb, of, n_sample, W, B, recv)
+    iters, busy = 0, 0.0
+    while busy < seconds:
+        cur = synth.scale_drift_bench(cur, iters + 1, rate=FLIP_RATE)
+        xn = cur.numpy().view(np.uint16)
+        t = time.perf_counter()
+        st = oracle.stats(xn)
+        sl, sz, slot = oracle.code3_encode(xn, W, st["E0"])
+        rb, of = oracle.compact(sl, sz, slot)
+        oracle.code3_decode(rb, of, n_sample, W)
+        for coded, (send, recv) in caches.items():
+            sl, sz, slot, _ = oracle.reuse_encode_all(xn, W, B, send, coded=coded)
+            rb, of = oracle.compact(sl, sz, slot)
+            oracle.gather_decode_reuse(rb, of, n_sample, W, B, recv)
+        busy += time.perf_counter() - t
+        iters += 1
+    return iters, busy, n_sample
+
+
+def cpu_baseline(seconds: float) -> dict:
+    iters, elapsed, ns = oracle_sample(seconds)
+    gbs = PASSES * 2 * ns * iters / elapsed / 1e9
+    return {"value": round(gbs, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"first {ns} values of the workload (W=8, B=256), {iters} iterations "
+                      f"through the six passes, {elapsed:.1f} s of oracle time"}
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return None
+    # every step is a bounded sample: 2^22 values through the six passes
+    import oracle
+    import synth
+    oracle.build()
+    ns = 1 << 22
+    W, B = W_CHUNKS, B_BLOCK
+    x = synth.config2(ns)
+    xs = [x]
+    for t in range(1, args.steps + args.warmup + 1):
+        xs.append(synth.scale_drift_bench(xs[-1], t, rate=FLIP_RATE))
+    xs = [t.numpy().view(np.uint16) for t in xs]
+    caches = {c: (np.zeros(ns, np.uint8), np.zeros(ns, np.uint8)) for c in (False, True)}
+
+    def step(xn, cold=False):
+        st = oracle.stats(xn)
+        sl, sz, slot = oracle.code3_encode(xn, W, st["E0"])
+        rb, of = oracle.compact(sl, sz, slot)
+        oracle.code3_decode(rb, of, ns, W)
+        for coded, (send, recv) in caches.items():
+            sl, sz, slot, _ = oracle.reuse_encode_all(xn, W, B, send, cold=cold, coded=coded)
+            rb, of = oracle.compact(sl, sz, slot)
+            oracle.gather_decode_reuse(rb, of, ns, W, B, recv)
+
+    step(xs[0], cold=True)
+    for i in range(args.warmup):
+        step(xs[1 + i])
+    t0 = time.perf_counter()
+    for k in range(args.steps):
+        step(xs[1 + args.warmup + k])
+    dt = (time.perf_counter() - t0) / args.steps
+    value = PASSES * 2 * ns / dt / 1e9
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "u16", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "n": N_VALUES, "W": W, "B": B,
+                       "flip_rate": FLIP_RATE, "codec_passes_per_step": PASSES,
+                       "sample_values_per_step": ns},
+            "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1,
+                             "kind": "oracle",
+                             "sample": f"first {ns} values of the workload per step"},
+            "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    world, rank, local = init_dist(args)
+    if args.impl == "reference":
+        line = run_reference(args, world, rank)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+    line, is_root = run_ours(args, world, rank, local)
+    if is_root:
+        if world == 1 and not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()
+    if int(os.environ.get("WORLD_SIZE", "1")) > 1:
+        import torch.distributed as dist
+        if dist.is_initialized():
+            dist.destroy_process_group()

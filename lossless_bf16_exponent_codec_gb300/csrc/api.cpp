@@ -1,0 +1,268 @@
+// api.cpp -- the C ABI of libexpzip: plans, argument checks, workspace
+// layout, and kernel launches.  See include/expzip.h for the contract.
+#include <cstdint>
+#include <cstring>
+#include <new>
+
+#include "ez_internal.h"
+
+namespace {
+
+constexpr uint64_t kTileValues = 8192;   // ez::kTile
+constexpr uint64_t kMaxN = 1ull << 40;
+
+uint64_t cdiv(uint64_t a, uint64_t b) { return (a + b - 1) / b; }
+uint64_t rup(uint64_t a, uint64_t b) { return cdiv(a, b) * b; }
+bool al(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// bytes of the per-shard records and of StatsBins (must match the device types)
+constexpr uint64_t kShardInfoBytes = 64;
+constexpr uint64_t kStatsBinsBytes = 5 * 256 * 8 + 256;
+
+bool is_reuse(const ez_plan_s* p) { return p->codec != EZ_CODEC_CODE3; }
+
+ez_status cuda_status(cudaError_t e) { return e == cudaSuccess ? EZ_OK : EZ_ERR_CUDA; }
+
+// Clear [0, bytes) of the workspace on the stream.
+ez_status clear_ws(void* ws, uint64_t bytes, cudaStream_t s)
+{
+    if (!bytes) return EZ_OK;
+    return cuda_status(cudaMemsetAsync(ws, 0, bytes, s));
+}
+
+ez_status check_ws(const ez_plan_s* p, const void* ws, uint64_t ws_bytes)
+{
+    if (!ws || !al(ws, 256)) return EZ_ERR_ARG;
+    if (ws_bytes < p->ws_bytes) return EZ_ERR_CAPACITY;
+    return EZ_OK;
+}
+
+}  // namespace
+
+namespace ezk {
+
+WsView ws_view(const ez_plan_s* p, void* ws)
+{
+    uint8_t* b = static_cast<uint8_t*>(ws);
+    WsView v;
+    v.counters = reinterpret_cast<uint32_t*>(b);
+    v.info = reinterpret_cast<ShardInfo*>(b + p->off_info);
+    v.shard_stats = reinterpret_cast<ez_stats_t*>(b + p->off_shard_stats);
+    v.bins = b + p->off_bins;
+    v.state_a = reinterpret_cast<unsigned long long*>(b + p->off_state_a);
+    v.state_b = reinterpret_cast<unsigned long long*>(b + p->off_state_b);
+    v.expbuf = b + p->off_expbuf;
+    return v;
+}
+
+}  // namespace ezk
+
+extern "C" {
+
+ez_status ez_plan_create(ez_plan* out, const ez_plan_desc* d)
+{
+    if (!out || !d) return EZ_ERR_ARG;
+    *out = nullptr;
+    if (d->flags != 0 || d->W == 0 || d->W > 65536 || d->n > kMaxN) return EZ_ERR_ARG;
+    if (d->codec < EZ_CODEC_CODE3 || d->codec > EZ_CODEC_REUSE_CODE3) return EZ_ERR_ARG;
+    const bool reuse = d->codec != EZ_CODEC_CODE3;
+    if (reuse) {
+        if (d->B == 0) return EZ_ERR_ARG;
+        if (d->B < 8 || d->B > 1024 || (d->B & (d->B - 1))) return EZ_ERR_UNSUPPORTED;
+    }
+    ez_plan_s* p = new (std::nothrow) ez_plan_s();
+    if (!p) return EZ_ERR_ARG;
+    p->n = d->n;
+    p->W = d->W;
+    p->B = reuse ? d->B : 0;
+    p->codec = d->codec;
+    p->L = rup(cdiv(d->n, d->W), 128);
+    const uint64_t tpc = p->L ? cdiv(p->L, kTileValues) : 1;
+    p->tpc = (uint32_t)tpc;
+    const uint64_t L = p->L;
+    if (!reuse) {
+        p->slot_bytes = 128 + L + 3 * rup(cdiv(L, 8), 128) + L;
+    } else {
+        const uint64_t nb = cdiv(L, p->B);
+        const uint64_t head = 64 + rup(cdiv(nb, 8), 16) + rup(L, 16);
+        const uint64_t exp = (d->codec == EZ_CODEC_REUSE_CODE3) ? 3 * rup(cdiv(L, 8), 16) + L : L;
+        p->slot_bytes = rup(head + exp, 128);
+    }
+    p->K = 16383.0 / (14.0 * 0.6931471805599453);
+    const uint64_t W = d->W;
+    const bool coded = d->codec == EZ_CODEC_REUSE_CODE3;
+    p->n_bins = coded ? d->W : 1;
+    uint64_t off = 256;                                   // 8 tile counters
+    p->off_info = off;
+    off = rup(off + W * kShardInfoBytes, 256);
+    p->off_shard_stats = off;
+    off = rup(off + (coded ? W * sizeof(ez_stats_t) : 0), 256);
+    p->off_bins = off;
+    off = rup(off + p->n_bins * kStatsBinsBytes, 256);
+    p->off_state_a = off;
+    off = rup(off + W * tpc * 8, 256);
+    p->off_state_b = off;
+    off = rup(off + (reuse ? W * tpc * 8 : 0), 256);
+    p->zero_bytes = off;
+    p->off_expbuf = off;
+    off = rup(off + (coded ? W * L : 0), 256);
+    p->ws_bytes = off;
+    *out = p;
+    return EZ_OK;
+}
+
+ez_status ez_plan_destroy(ez_plan p)
+{
+    delete p;
+    return EZ_OK;
+}
+
+ez_status ez_plan_sizes(ez_plan p, ez_sizes* out)
+{
+    if (!p || !out) return EZ_ERR_ARG;
+    out->shard_len = p->L;
+    out->slot_bytes = p->slot_bytes;
+    out->workspace_bytes = p->ws_bytes;
+    out->cache_bytes = is_reuse(p) ? p->n : 0;
+    out->tile_values = kTileValues;
+    return EZ_OK;
+}
+
+ez_status ez_stats(ez_plan p, const uint16_t* d_x, uint64_t n_values, ez_stats_t* d_stats,
+                   void* d_ws, uint64_t ws_bytes, void* stream)
+{
+    if (!p || !d_stats || !al(d_stats, 8) || n_values > kMaxN) return EZ_ERR_ARG;
+    if (n_values && (!d_x || !al(d_x, 16))) return EZ_ERR_ARG;
+    ez_status s = check_ws(p, d_ws, ws_bytes);
+    if (s != EZ_OK) return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    s = clear_ws(d_ws, p->off_state_a, st);
+    if (s != EZ_OK) return s;
+    return cuda_status(ezk::launch_stats(p, d_x, n_values, d_stats, ezk::ws_view(p, d_ws), st));
+}
+
+ez_status ez_encode_code3(ez_plan p, const uint16_t* d_x, uint32_t first, uint32_t count,
+                          const ez_stats_t* d_stats, uint8_t* d_out, uint64_t out_bytes,
+                          uint64_t* d_sizes, uint32_t* d_status, void* d_ws, uint64_t ws_bytes,
+                          void* stream)
+{
+    if (!p || p->codec != EZ_CODEC_CODE3) return EZ_ERR_ARG;
+    if (count == 0 || first >= p->W || count > p->W - first) return EZ_ERR_ARG;
+    if (!d_stats || !al(d_stats, 8) || !d_out || !al(d_out, 16) || !d_sizes || !al(d_sizes, 8) ||
+        !d_status || !al(d_status, 4))
+        return EZ_ERR_ARG;
+    if (p->n && (!d_x || !al(d_x, 16))) return EZ_ERR_ARG;
+    if (out_bytes / p->slot_bytes < count) return EZ_ERR_CAPACITY;
+    ez_status s = check_ws(p, d_ws, ws_bytes);
+    if (s != EZ_OK) return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    s = clear_ws(d_ws, p->off_state_a + (uint64_t)count * p->tpc * 8, st);
+    if (s != EZ_OK) return s;
+    return cuda_status(ezk::launch_code3_encode(p, d_x, first, count, d_stats, d_out, d_sizes,
+                                                d_status, ezk::ws_view(p, d_ws), st));
+}
+
+ez_status ez_decode_code3(ez_plan p, const uint8_t* d_in, const uint64_t* d_offsets, uint32_t first,
+                          uint32_t count, uint16_t* d_out, uint32_t* d_status, void* d_ws,
+                          uint64_t ws_bytes, void* stream)
+{
+    if (!p || p->codec != EZ_CODEC_CODE3) return EZ_ERR_ARG;
+    if (count == 0 || first >= p->W || count > p->W - first) return EZ_ERR_ARG;
+    if (!d_in || !al(d_in, 16) || !d_offsets || !al(d_offsets, 8) || !d_status || !al(d_status, 4))
+        return EZ_ERR_ARG;
+    if (p->n && (!d_out || !al(d_out, 16))) return EZ_ERR_ARG;
+    ez_status s = check_ws(p, d_ws, ws_bytes);
+    if (s != EZ_OK) return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    s = clear_ws(d_ws, p->off_state_a + (uint64_t)count * p->tpc * 8, st);
+    if (s != EZ_OK) return s;
+    return cuda_status(ezk::launch_code3_decode(p, d_in, d_offsets, first, count, d_out, d_status,
+                                                ezk::ws_view(p, d_ws), st));
+}
+
+ez_status ez_encode_reuse(ez_plan p, const uint16_t* d_x, uint32_t first, uint32_t count,
+                          uint8_t* d_send_cache, int cold, uint8_t* d_out, uint64_t out_bytes,
+                          uint64_t* d_sizes, ez_stats_t* d_stats, uint32_t* d_status, void* d_ws,
+                          uint64_t ws_bytes, void* stream)
+{
+    if (!p || !is_reuse(p)) return EZ_ERR_ARG;
+    if (count == 0 || first >= p->W || count > p->W - first) return EZ_ERR_ARG;
+    if (!d_out || !al(d_out, 16) || !d_sizes || !al(d_sizes, 8) || !d_status || !al(d_status, 4))
+        return EZ_ERR_ARG;
+    if (p->n && (!d_x || !al(d_x, 16) || !d_send_cache || !al(d_send_cache, 16))) return EZ_ERR_ARG;
+    if (d_stats && !al(d_stats, 8)) return EZ_ERR_ARG;
+    if (out_bytes / p->slot_bytes < count) return EZ_ERR_CAPACITY;
+    ez_status s = check_ws(p, d_ws, ws_bytes);
+    if (s != EZ_OK) return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const bool coded = p->codec == EZ_CODEC_REUSE_CODE3;
+    const uint64_t clear = coded ? p->off_state_b + (uint64_t)count * p->tpc * 8
+                                 : p->off_state_a + (uint64_t)count * p->tpc * 8;
+    s = clear_ws(d_ws, clear, st);
+    if (s != EZ_OK) return s;
+    return cuda_status(ezk::launch_reuse_encode(p, d_x, first, count, d_send_cache, cold, d_out,
+                                                d_sizes, d_stats, d_status, ezk::ws_view(p, d_ws),
+                                                st));
+}
+
+ez_status ez_decode_reuse(ez_plan p, const uint8_t* d_payload, uint64_t payload_bytes, uint32_t shard,
+                          uint8_t* d_recv_cache, uint16_t* d_out, uint32_t* d_status, void* d_ws,
+                          uint64_t ws_bytes, void* stream)
+{
+    if (!p || !is_reuse(p) || shard >= p->W) return EZ_ERR_ARG;
+    if (!d_payload || !al(d_payload, 16) || !d_status || !al(d_status, 4)) return EZ_ERR_ARG;
+    if (p->n && (!d_recv_cache || !al(d_recv_cache, 16) || !d_out || !al(d_out, 16)))
+        return EZ_ERR_ARG;
+    ez_status s = check_ws(p, d_ws, ws_bytes);
+    if (s != EZ_OK) return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    s = clear_ws(d_ws, p->off_state_b + (uint64_t)p->tpc * 8, st);
+    if (s != EZ_OK) return s;
+    return cuda_status(ezk::launch_reuse_decode(p, d_payload, nullptr, payload_bytes, shard, 1,
+                                                d_recv_cache, d_out, d_status,
+                                                ezk::ws_view(p, d_ws), st));
+}
+
+ez_status ez_gather_decode(ez_plan p, const uint8_t* d_recv, const uint64_t* d_offsets,
+                           uint8_t* d_recv_cache, uint16_t* d_full_out, uint32_t* d_status, void* d_ws,
+                           uint64_t ws_bytes, void* stream)
+{
+    if (!p) return EZ_ERR_ARG;
+    if (!d_recv || !al(d_recv, 16) || !d_offsets || !al(d_offsets, 8) || !d_status ||
+        !al(d_status, 4))
+        return EZ_ERR_ARG;
+    if (p->n && (!d_full_out || !al(d_full_out, 16))) return EZ_ERR_ARG;
+    if (is_reuse(p) && p->n && (!d_recv_cache || !al(d_recv_cache, 16))) return EZ_ERR_ARG;
+    ez_status s = check_ws(p, d_ws, ws_bytes);
+    if (s != EZ_OK) return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const ezk::WsView w = ezk::ws_view(p, d_ws);
+    if (!is_reuse(p)) {
+        s = clear_ws(d_ws, p->off_state_a + (uint64_t)p->W * p->tpc * 8, st);
+        if (s != EZ_OK) return s;
+        return cuda_status(
+            ezk::launch_code3_decode(p, d_recv, d_offsets, 0, p->W, d_full_out, d_status, w, st));
+    }
+    s = clear_ws(d_ws, p->off_state_b + (uint64_t)p->W * p->tpc * 8, st);
+    if (s != EZ_OK) return s;
+    return cuda_status(ezk::launch_reuse_decode(p, d_recv, d_offsets, 0, 0, p->W, d_recv_cache,
+                                                d_full_out, d_status, w, st));
+}
+
+const char* ez_status_str(ez_status s)
+{
+    switch (s) {
+        case EZ_OK: return "ok";
+        case EZ_ERR_ARG: return "invalid argument";
+        case EZ_ERR_CUDA: return "CUDA error";
+        case EZ_ERR_CAPACITY: return "buffer or workspace too small";
+        case EZ_ERR_CORRUPT: return "corrupt payload";
+        case EZ_ERR_TIMEOUT: return "timed out";
+        case EZ_ERR_UNSUPPORTED: return "unsupported";
+    }
+    return "unknown status";
+}
+
+uint32_t ez_version(void) { return 0x000100u; }
+
+}  // extern "C"

@@ -1,0 +1,209 @@
+// ez_common.cuh -- tile geometry and device helpers shared by the kernels of
+// libexpzip (sm_103a).
+//
+// Every kernel works on tiles of kTile = 8192 values.  A CTA of 256 threads
+// takes one tile; thread t owns four "groups" of 8 consecutive values, group
+// g at tile value 8*(g*256 + t), so each warp load or store of a group is one
+// contiguous run (512 B of BF16, 256 B of sign+mantissa bytes, 32 B of a code
+// plane).  Tiles never straddle a shard: shard i owns tiles
+// [i*tpc, (i+1)*tpc) with tpc = max(1, ceil(L/kTile)).
+//
+// Order-preserving compaction (escapes, changed blocks) uses a decoupled
+// look-back scan over tile aggregates (Merrill & Garland, "Single-pass
+// parallel prefix scan with decoupled look-back", 2016).  Tile ids are taken
+// from an atomic counter, so a tile only waits on tiles whose CTAs are
+// already running.  Every wait is bounded; a wait that gives up sets a flag
+// the caller turns into EZ_DSTAT_TIMEOUT.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "expzip.h"
+
+namespace ez {
+
+constexpr int kThreads = 256;
+constexpr int kGroups = 4;
+constexpr int kTile = kThreads * kGroups * 8;      // 8192 values
+constexpr uint32_t kFull = 0xffffffffu;
+constexpr uint32_t kSpinLimit = 1u << 21;          // ~0.1-0.3 s of polling
+
+constexpr unsigned long long kFlagAgg = 1ull << 62;
+constexpr unsigned long long kFlagIncl = 2ull << 62;
+constexpr unsigned long long kValMask = (1ull << 62) - 1;
+
+__host__ __device__ __forceinline__ uint64_t cdiv(uint64_t a, uint64_t b) { return (a + b - 1) / b; }
+__host__ __device__ __forceinline__ uint64_t rup(uint64_t a, uint64_t b) { return cdiv(a, b) * b; }
+__host__ __device__ __forceinline__ uint64_t umin64(uint64_t a, uint64_t b) { return a < b ? a : b; }
+
+// values of shard r (r counted over the whole plan)
+__host__ __device__ __forceinline__ uint64_t shard_values(uint64_t n, uint64_t L, uint32_t r)
+{
+    uint64_t a = (uint64_t)r * L;
+    if (a >= n) return 0;
+    return (n - a < L) ? n - a : L;
+}
+
+// ---- BF16 fields (CIERA split; ZipCCL 3.1) ---------------------------------
+__device__ __forceinline__ uint32_t exp_of(uint32_t h) { return (h >> 7) & 0xFFu; }
+__device__ __forceinline__ uint32_t sm_of(uint32_t h) { return ((h >> 8) & 0x80u) | (h & 0x7Fu); }
+__device__ __forceinline__ uint32_t merge_of(uint32_t sm, uint32_t e)
+{
+    return ((sm & 0x80u) << 8) | (e << 7) | (sm & 0x7Fu);
+}
+// value i (0..7) of a 16-byte group held as uint4
+__device__ __forceinline__ uint32_t half_of(const uint4& w, int i)
+{
+    uint32_t word = (i < 2) ? w.x : (i < 4) ? w.y : (i < 6) ? w.z : w.w;
+    return (i & 1) ? (word >> 16) : (word & 0xFFFFu);
+}
+
+// ---- memory helpers ----------------------------------------------------------
+__device__ __forceinline__ uint4 ld_v4_nc(const void* p)
+{
+    uint4 r;
+    asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+    return r;
+}
+__device__ __forceinline__ void st_v4(void* p, const uint4& v)
+{
+    asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};"
+                 :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+}
+__device__ __forceinline__ unsigned long long ld_relaxed(const unsigned long long* p)
+{
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_relaxed(unsigned long long* p, unsigned long long v)
+{
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" :: "l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+    return v;
+}
+
+// Exclusive prefix of tile t over [seg_first, t).  One full warp calls it.
+// Returns the prefix; *stuck is set (uniformly) if a predecessor never
+// published within the spin limit.
+__device__ __forceinline__ uint32_t ld_relaxed32(const uint32_t* p)
+{
+    uint32_t v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// `abort` (per launch, zeroed with the tile states) is raised by the first
+// wait that gives up; every other wait then stops at once, so a broken chain
+// costs one spin limit, not one per tile.
+static __device__ __noinline__ unsigned long long lookback(unsigned long long* st, long long t,
+                                                    long long seg_first, bool* stuck,
+                                                    uint32_t* abort)
+{
+    const int lane = threadIdx.x & 31;
+    unsigned long long prefix = 0;
+    long long pos = t - 1;
+    *stuck = false;
+    while (pos >= seg_first) {
+        const long long idx = pos - lane;
+        const bool valid = idx >= seg_first;
+        unsigned long long w = 0;
+        if (valid) {
+            w = ld_relaxed(st + idx);
+            uint32_t spins = 0;
+            while ((w >> 62) == 0 && spins < kSpinLimit) {
+                __nanosleep(40);
+                w = ld_relaxed(st + idx);
+                if ((++spins & 63u) == 0 && ld_relaxed32(abort)) break;
+            }
+        }
+        __syncwarp();
+        if (__any_sync(kFull, valid && (w >> 62) == 0)) {
+            *stuck = true;
+            if ((threadIdx.x & 31) == 0) atomicExch(abort, 1u);
+            return prefix;
+        }
+        const uint32_t incl = __ballot_sync(kFull, valid && (w >> 62) == 2);
+        unsigned long long v = valid ? (w & kValMask) : 0ull;
+        if (incl) {
+            const int j = __ffs(incl) - 1;     // nearest predecessor with a full prefix
+            if (lane > j) v = 0;
+            return prefix + warp_sum_u64(v);
+        }
+        prefix += warp_sum_u64(v);
+        pos -= 32;
+    }
+    return prefix;
+}
+
+// Block-wide exclusive scan of a 64-bit value over 256 threads.  s_warp holds
+// 8 entries; a __syncthreads() is needed before s_warp is reused.
+__device__ __forceinline__ unsigned long long block_excl_scan(unsigned long long v,
+                                                              unsigned long long* s_warp,
+                                                              unsigned long long* total)
+{
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    unsigned long long x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        unsigned long long y = __shfl_up_sync(kFull, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) s_warp[wid] = x;
+    __syncthreads();
+    unsigned long long pre = 0, tot = 0;
+#pragma unroll
+    for (int i = 0; i < kThreads / 32; i++) {
+        unsigned long long s = s_warp[i];
+        if (i < wid) pre += s;
+        tot += s;
+    }
+    *total = tot;
+    return pre + x - v;
+}
+
+// Tile id from the per-launch counter, broadcast to the CTA.
+__device__ __forceinline__ uint32_t next_tile(uint32_t* counter, uint32_t* s_tile)
+{
+    if (threadIdx.x == 0) *s_tile = atomicAdd(counter, 1u);
+    __syncthreads();
+    return *s_tile;
+}
+
+// Publish a tile's aggregate, look back, publish its inclusive prefix.  All
+// threads call it; returns the exclusive prefix to every thread.
+__device__ __forceinline__ unsigned long long tile_prefix(unsigned long long* st, uint32_t tile,
+                                                          uint32_t seg_first,
+                                                          unsigned long long agg,
+                                                          unsigned long long* s_prefix,
+                                                          uint32_t* dstatus, uint32_t* abort)
+{
+    if (tile == seg_first) {
+        if (threadIdx.x == 0) {
+            st_relaxed(st + tile, kFlagIncl | agg);
+            *s_prefix = 0;
+        }
+    } else {
+        if (threadIdx.x == 0) st_relaxed(st + tile, kFlagAgg | agg);
+        if (threadIdx.x < 32) {
+            bool stuck;
+            unsigned long long p = lookback(st, tile, seg_first, &stuck, abort);
+            if (threadIdx.x == 0) {
+                if (stuck) atomicOr(dstatus, EZ_DSTAT_TIMEOUT);
+                st_relaxed(st + tile, kFlagIncl | ((p + agg) & kValMask));
+                *s_prefix = p;
+            }
+        }
+    }
+    __syncthreads();
+    return *s_prefix;
+}
+
+}  // namespace ez

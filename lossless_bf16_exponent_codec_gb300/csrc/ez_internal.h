@@ -1,0 +1,66 @@
+// ez_internal.h -- plan object and kernel launchers of libexpzip (host side).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "expzip.h"
+
+struct ez_plan_s {
+    uint64_t n;
+    uint32_t W, B, codec;
+    uint64_t L;              // shard length
+    uint32_t tpc;            // tiles per shard
+    uint64_t slot_bytes;     // worst-case payload per shard
+    double K;                // 16383 / (14 ln 2)
+    // workspace layout (byte offsets); [0, zero_bytes) is cleared per call
+    uint64_t off_info, off_shard_stats, off_bins, off_state_a, off_state_b, off_expbuf;
+    uint64_t zero_bytes, ws_bytes;
+    uint32_t n_bins;
+};
+
+namespace ezk {
+
+// Per-shard scratch record of the two-pass reuse+code3 encoder.
+struct ShardInfo {
+    unsigned long long m;          // exponents in the changed blocks
+    unsigned long long n_changed;  // changed blocks
+    unsigned int E0;               // window of the shard
+    unsigned int pad[11];
+};
+
+struct WsView {
+    uint32_t* counters;            // 8 tile counters
+    ShardInfo* info;               // W records
+    ez_stats_t* shard_stats;       // W records (reuse+code3 without caller stats)
+    unsigned long long* state_a;
+    unsigned long long* state_b;
+    void* bins;                    // StatsBins[n_bins]
+    uint8_t* expbuf;               // W * L bytes (reuse+code3 only)
+};
+
+WsView ws_view(const ez_plan_s* p, void* ws);
+
+cudaError_t launch_stats(const ez_plan_s* p, const uint16_t* x, uint64_t n, ez_stats_t* out,
+                         const WsView& w, cudaStream_t s);
+
+cudaError_t launch_code3_encode(const ez_plan_s* p, const uint16_t* x, uint32_t first,
+                                uint32_t count, const ez_stats_t* st, uint8_t* out,
+                                uint64_t* sizes, uint32_t* dstatus, const WsView& w,
+                                cudaStream_t s);
+
+cudaError_t launch_code3_decode(const ez_plan_s* p, const uint8_t* in, const uint64_t* offsets,
+                                uint32_t first, uint32_t count, uint16_t* out,
+                                uint32_t* dstatus, const WsView& w, cudaStream_t s);
+
+cudaError_t launch_reuse_encode(const ez_plan_s* p, const uint16_t* x, uint32_t first,
+                                uint32_t count, uint8_t* cache, int cold, uint8_t* out,
+                                uint64_t* sizes, ez_stats_t* st, uint32_t* dstatus,
+                                const WsView& w, cudaStream_t s);
+
+cudaError_t launch_reuse_decode(const ez_plan_s* p, const uint8_t* in, const uint64_t* offsets,
+                                uint64_t single_avail, uint32_t first, uint32_t count,
+                                uint8_t* cache, uint16_t* out, uint32_t* dstatus,
+                                const WsView& w, cudaStream_t s);
+
+}  // namespace ezk

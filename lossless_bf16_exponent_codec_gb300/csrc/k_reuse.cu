@@ -1,0 +1,742 @@
+// k_reuse.cu -- a3 / a4 / a5: CIERA cross-iteration exponent reuse
+// ("CIERA: Cross-Iteration Exponent Reuse for Lossless Allgather in Sharded
+// MoE Training", exponent-reuse and gain-formula paragraphs).
+//
+// Sender (k_reuse_encode): per block of B values, the block is "changed" when
+// one of its exponents differs from the sender's cache of the previous
+// iteration (or the call is cold).  The payload carries a changed-block
+// bitmap, the sign+mantissa byte of every value and the exponents of the
+// changed blocks packed in block order; the cache then takes the new
+// exponents.  The pages detect changes with a 128-bit block hash compared to
+// a hash cache; comparing the cached exponents directly gives the same
+// bitmap (minus hash collisions) in one pass.  A changed block's position in
+// the exponent section is (changed blocks before it) * B: a decoupled
+// look-back gives each tile the count of changed blocks in earlier tiles.
+//
+// Coded variant (EZ_CODEC_REUSE_CODE3): the changed exponents are coded with
+// the 3-bit code of ZipCCL (research digest 3.1) instead of nvCOMP's ANS,
+// whose window comes from the shard's sigma, accumulated in the same pass.
+// Pass 1 stages the raw exponent stream in the workspace; pass 2
+// (k_reuse_code3) codes it into planes + escapes inside the payload.
+//
+// Receiver (k_reuse_decode): for W payloads in one launch, each tile reads
+// its slice of the bitmap, looks back for the changed-block prefix, takes
+// unchanged exponents from its exponent cache (ExpCache) and changed ones
+// from the payload, writes them back into the cache and stores the merged
+// BF16 values straight into the gathered full buffer.
+#include "ez_internal.h"
+#include "ez_stats.cuh"
+
+namespace ezk {
+using namespace ez;
+
+struct RuEnc {
+    const uint16_t* x;
+    uint8_t* cache;
+    uint8_t* out;
+    uint64_t slot;
+    uint64_t* sizes;
+    uint32_t* dstatus;
+    uint64_t n, L;
+    uint32_t W, B, log2B, first, tpc;
+    int cold;
+    unsigned long long* state;
+    uint32_t* counter;
+    uint32_t* abort;
+    // coded variant
+    uint8_t* expbuf;
+    ShardInfo* info;
+    StatsBins* bins;
+    ez_stats_t* stats;    // per shard record (caller's or workspace)
+    double K;
+};
+
+struct RuC3 {
+    uint8_t* out;
+    uint64_t slot;
+    uint64_t* sizes;
+    uint32_t* dstatus;
+    uint64_t n, L;
+    uint32_t W, B, first, tpc;
+    int cold;
+    unsigned long long* state;
+    uint32_t* counter;
+    uint32_t* abort;
+    const uint8_t* expbuf;
+    const ShardInfo* info;
+    const ez_stats_t* stats;
+};
+
+struct RuDec {
+    const uint8_t* in;
+    const uint64_t* offsets;   // NULL: one payload at `in` with single_avail bytes
+    uint64_t single_avail;
+    uint8_t* cache;
+    uint16_t* out;
+    uint32_t* dstatus;
+    uint64_t n, L;
+    uint32_t W, B, log2B, first, tpc;
+    unsigned long long* state_a;
+    unsigned long long* state_b;
+    uint32_t* counter;
+    uint32_t* abort;
+};
+
+__device__ __forceinline__ uint64_t ru_off_sm(uint64_t n_s, uint32_t B)
+{
+    return 64 + rup(cdiv(cdiv(n_s, B), 8), 16);
+}
+__device__ __forceinline__ uint64_t ru_off_exp(uint64_t n_s, uint32_t B)
+{
+    return ru_off_sm(n_s, B) + rup(n_s, 16);
+}
+__device__ __forceinline__ uint64_t ru_bytes(uint64_t n_s, uint32_t B, uint64_t m, bool coded,
+                                             uint64_t n_esc)
+{
+    return rup(ru_off_exp(n_s, B) + (coded ? 3 * rup(cdiv(m, 8), 16) + n_esc : m), 128);
+}
+
+__device__ __forceinline__ uint32_t lb8(uint64_t v, int k) { return (uint32_t)(v >> (8 * k)) & 0xFFu; }
+
+__device__ __forceinline__ uint32_t ru_header_byte(int b, uint32_t flags, uint32_t E0, uint32_t B,
+                                                   uint32_t shard, uint64_t n_s, uint64_t n_changed,
+                                                   uint64_t m, uint64_t n_esc, uint64_t total)
+{
+    switch (b) {
+        case 0: return 'E';
+        case 1: return 'Z';
+        case 2: return 'R';
+        case 3: return 'U';
+        case 4: return 1;
+        case 5: return flags;
+        case 6: return E0;
+        case 7: return 0;
+        default: break;
+    }
+    if (b < 12) return lb8(B, b - 8);
+    if (b < 16) return lb8(shard, b - 12);
+    if (b < 24) return lb8(n_s, b - 16);
+    if (b < 32) return lb8(n_changed, b - 24);
+    if (b < 40) return lb8(m, b - 32);
+    if (b < 48) return lb8(n_esc, b - 40);
+    if (b < 56) return lb8(total, b - 48);
+    return 0;
+}
+
+__device__ __forceinline__ uint4 ld_group16(const uint16_t* p, uint32_t v, uint32_t nv)
+{
+    if (v + 8 <= nv) return ld_v4_nc(p + v);
+    uint32_t h[8];
+#pragma unroll
+    for (int i = 0; i < 8; i++) h[i] = (v + i < nv) ? (uint32_t)p[v + i] : 0u;
+    return make_uint4(h[0] | h[1] << 16, h[2] | h[3] << 16, h[4] | h[5] << 16, h[6] | h[7] << 16);
+}
+__device__ __forceinline__ unsigned long long ld_group8(const uint8_t* p, uint32_t v, uint32_t nv)
+{
+    if (v + 8 <= nv) return __ldg(reinterpret_cast<const unsigned long long*>(p + v));
+    unsigned long long r = 0;
+    for (uint32_t i = 0; v + i < nv && i < 8; i++) r |= (unsigned long long)p[v + i] << (8 * i);
+    return r;
+}
+__device__ __forceinline__ void st_group8(uint8_t* p, uint32_t v, uint32_t nv, unsigned long long x)
+{
+    if (v + 8 <= nv) {
+        *reinterpret_cast<unsigned long long*>(p + v) = x;
+    } else {
+        for (uint32_t i = 0; v + i < nv && i < 8; i++) p[v + i] = (uint8_t)(x >> (8 * i));
+    }
+}
+__device__ __forceinline__ uint32_t vmask_of(uint32_t v, uint32_t nv)
+{
+    return v >= nv ? 0u : (nv - v >= 8 ? 0xFFu : ((1u << (nv - v)) - 1u));
+}
+__device__ __forceinline__ unsigned long long bytemask_of(uint32_t vm)
+{
+    unsigned long long r = 0;
+#pragma unroll
+    for (int i = 0; i < 8; i++) r |= ((vm >> i) & 1u) ? (0xFFull << (8 * i)) : 0ull;
+    return r;
+}
+
+// Tile bitmap (up to 1024 blocks) from the 1024 group-lane changed bits held
+// in s_gl (word w = group-lanes 32w..32w+31), built by warp 0 into s_bm; the
+// exclusive per-word popcount prefix goes to s_pre.  Returns the changed
+// block count of the tile (warp 0 only).
+__device__ __forceinline__ uint32_t build_bitmap(const uint32_t* s_gl, uint32_t* s_bm, uint32_t* s_pre,
+                                                 uint32_t log2B)
+{
+    const int lane = threadIdx.x & 31;
+    const uint32_t word = s_gl[lane];
+    const uint32_t s = 1u << (log2B - 3);   // group-lanes per block
+    if (s <= 32) {
+        const uint32_t per = 32u / s;
+        const uint32_t bmask = (s == 32) ? 0xffffffffu : ((1u << s) - 1u);
+        uint32_t bits = 0;
+        for (uint32_t b = 0; b < per; b++)
+            if ((word >> (b * s)) & bmask) bits |= 1u << b;
+        const uint32_t pos = (uint32_t)lane * per;
+        atomicOr(&s_bm[pos >> 5], bits << (pos & 31));
+    } else {
+        const uint32_t k = ((uint32_t)lane * 32u) / s;
+        if (word) atomicOr(&s_bm[k >> 5], 1u << (k & 31));
+    }
+    __syncwarp();
+    const uint32_t c = __popc(s_bm[lane]);
+    uint32_t x = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(kFull, x, o);
+        if (lane >= o) x += y;
+    }
+    s_pre[lane] = x - c;
+    return __shfl_sync(kFull, x, 31);
+}
+
+__device__ __forceinline__ bool block_changed(const uint32_t* s_bm, uint32_t k)
+{
+    return (s_bm[k >> 5] >> (k & 31)) & 1u;
+}
+__device__ __forceinline__ uint32_t block_rank(const uint32_t* s_bm, const uint32_t* s_pre, uint32_t k)
+{
+    return s_pre[k >> 5] + __popc(s_bm[k >> 5] & ((1u << (k & 31)) - 1u));
+}
+
+template <bool kCoded>
+__global__ void __launch_bounds__(kThreads) k_reuse_encode(RuEnc a)
+{
+    __shared__ uint32_t s_tile;
+    __shared__ uint32_t s_gl[32], s_bm[32], s_pre[32];
+    __shared__ uint32_t s_agg;
+    __shared__ unsigned long long s_prefix;
+    extern __shared__ __align__(16) unsigned char dyn[];
+    const int t = threadIdx.x, lane = t & 31, wid = t >> 5;
+    const uint32_t tile = next_tile(a.counter, &s_tile);
+    const uint32_t ci = tile / a.tpc, lt = tile - ci * a.tpc;
+    const uint32_t r = a.first + ci;
+    const uint64_t n_s = shard_values(a.n, a.L, r);
+    const uint64_t v0 = (uint64_t)lt * kTile;
+    const uint32_t nv = v0 < n_s ? (uint32_t)umin64(kTile, n_s - v0) : 0u;
+    const uint32_t B = a.B, log2B = a.log2B;
+    const uint64_t nb = cdiv(n_s, B);
+    const uint64_t bm_bytes = cdiv(nb, 8);
+    const uint64_t off_sm = ru_off_sm(n_s, B), off_exp = ru_off_exp(n_s, B);
+    const uint16_t* xt = a.x + (uint64_t)ci * a.L + v0;
+    uint8_t* ct = a.cache + (uint64_t)ci * a.L + v0;
+    uint8_t* o = a.out + (uint64_t)ci * a.slot;
+    const uint32_t fin_tile = n_s ? (uint32_t)((n_s - 1) / kTile) : 0u;
+
+    if (t < 32) {
+        s_gl[t] = 0;
+        s_bm[t] = 0;
+    }
+    uint4 w[kGroups];
+    unsigned long long cv[kGroups];
+#pragma unroll
+    for (int g = 0; g < kGroups; g++) {
+        const uint32_t v = 8u * (uint32_t)(g * kThreads + t);
+        w[g] = ld_group16(xt, v, nv);
+        cv[g] = (v < nv && !a.cold) ? ld_group8(ct, v, nv) : 0ull;
+    }
+
+    StatsSmem* S = reinterpret_cast<StatsSmem*>(dyn);
+    unsigned long long acc2 = 0;
+    if (kCoded) st_begin(*S, (8u * (uint32_t)t < nv) ? half_of(w[0], 0) : 0xFFFFFFFFu);
+    else __syncthreads();
+
+    unsigned long long e8[kGroups];
+#pragma unroll
+    for (int g = 0; g < kGroups; g++) {
+        const uint32_t v = 8u * (uint32_t)(g * kThreads + t);
+        const uint32_t vm = vmask_of(v, nv);
+        unsigned long long e = 0, smw = 0;
+#pragma unroll
+        for (int i = 0; i < 8; i++) {
+            const uint32_t h = half_of(w[g], i);
+            e |= (unsigned long long)exp_of(h) << (8 * i);
+            smw |= (unsigned long long)sm_of(h) << (8 * i);
+        }
+        const unsigned long long bmask = bytemask_of(vm);
+        e &= bmask;
+        e8[g] = e;
+        const bool ch = vm && (a.cold || ((e ^ cv[g]) & bmask) != 0ull);
+        const uint32_t bal = __ballot_sync(kFull, ch);
+        if (lane == 0) s_gl[g * (kThreads / 32) + wid] = bal;
+        if (vm) st_group8(o + off_sm + v0, v, nv, smw & bmask);
+        if (kCoded && vm) {
+            uint32_t* cell = &S->cells[wid][0][lane];
+            const uint32_t elo = S->elo;
+#pragma unroll
+            for (int i = 0; i < 8; i++)
+                if ((vm >> i) & 1u) st_add(half_of(w[g], i), elo, cell, acc2, *S);
+        }
+    }
+    __syncthreads();
+    if (t < 32) {
+        const uint32_t agg = build_bitmap(s_gl, s_bm, s_pre, log2B);
+        if (t == 0) s_agg = agg;
+    }
+    __syncthreads();
+    const unsigned long long agg = s_agg;
+    const unsigned long long P = tile_prefix(a.state, tile, ci * a.tpc, agg, &s_prefix, a.dstatus, a.abort);
+
+    // bitmap bytes of this tile
+    const uint32_t nbt = (uint32_t)kTile >> log2B;
+    const uint64_t bm0 = (uint64_t)lt * (nbt / 8);
+    if ((uint32_t)t < nbt / 8 && bm0 + t < bm_bytes)
+        o[64 + bm0 + t] = reinterpret_cast<const uint8_t*>(s_bm)[t];
+
+    // changed exponents into the payload (or the staging stream) and cache
+#pragma unroll
+    for (int g = 0; g < kGroups; g++) {
+        const uint32_t v = 8u * (uint32_t)(g * kThreads + t);
+        if (v >= nv) continue;
+        const uint32_t k = v >> log2B;
+        if (!block_changed(s_bm, k)) continue;
+        const uint64_t pos = (P + block_rank(s_bm, s_pre, k)) * B + (v - (k << log2B));
+        if (kCoded) st_group8(a.expbuf + (uint64_t)ci * a.L + pos, 0u, nv - v, e8[g]);
+        else st_group8(o + off_exp + pos, 0u, nv - v, e8[g]);
+        st_group8(ct, v, nv, e8[g]);
+    }
+
+    if (kCoded) {
+        if (st_end(*S, acc2, a.bins + ci, a.tpc)) {
+            st_finalize(a.bins + ci, n_s, a.K, a.stats + ci);
+        }
+    }
+
+    if (lt == fin_tile) {
+        const uint64_t n_changed = P + agg;
+        bool last_changed = false;
+        if (n_s) {
+            const uint32_t klast = (uint32_t)((n_s - 1 - v0) >> log2B);
+            last_changed = block_changed(s_bm, klast);
+        }
+        const uint64_t m = n_changed * B - (last_changed ? nb * B - n_s : 0);
+        if (t < 16 && rup(bm_bytes, 16) > bm_bytes + t) o[64 + bm_bytes + t] = 0;
+        if (t < 16 && rup(n_s, 16) > n_s + t) o[off_sm + n_s + t] = 0;
+        if (kCoded) {
+            if (t == 0) {
+                a.info[ci].m = m;
+                a.info[ci].n_changed = n_changed;
+            }
+        } else {
+            const uint64_t total = ru_bytes(n_s, B, m, false, 0);
+            if (t < 64)
+                o[t] = (uint8_t)ru_header_byte(t, a.cold ? 2u : 0u, 0u, B, r, n_s, n_changed, m, 0, total);
+            if (t < 128 && off_exp + m + t < total) o[off_exp + m + t] = 0;
+            if (t == 0) a.sizes[ci] = total;
+        }
+    }
+}
+
+// Pass 2 of the coded variant: 3-bit code of the staged exponent stream.
+__global__ void __launch_bounds__(kThreads) k_reuse_code3(RuC3 a)
+{
+    __shared__ uint32_t s_tile;
+    __shared__ unsigned long long s_warp[kThreads / 32];
+    __shared__ unsigned long long s_prefix;
+    const int t = threadIdx.x;
+    const uint32_t tile = next_tile(a.counter, &s_tile);
+    const uint32_t ci = tile / a.tpc, lt = tile - ci * a.tpc;
+    const uint32_t r = a.first + ci;
+    const uint64_t n_s = shard_values(a.n, a.L, r);
+    const uint64_t m = a.info[ci].m;
+    const uint64_t n_changed = a.info[ci].n_changed;
+    const uint64_t v0 = (uint64_t)lt * kTile;
+    const uint32_t nv = v0 < m ? (uint32_t)umin64(kTile, m - v0) : 0u;
+    uint32_t E0 = a.stats[ci].E0;
+    if (E0 > 249u) {
+        if (t == 0) atomicOr(a.dstatus, EZ_DSTAT_BAD_STATS);
+        E0 = 0;
+    }
+    const uint64_t off_exp = ru_off_exp(n_s, a.B);
+    const uint64_t plane = rup(cdiv(m, 8), 16);
+    uint8_t* o = a.out + (uint64_t)ci * a.slot;
+    uint8_t* pl = o + off_exp;
+    uint8_t* esc_sec = pl + 3 * plane;
+    const uint8_t* es = a.expbuf + (uint64_t)ci * a.L + v0;
+    const uint32_t fin_tile = m ? (uint32_t)((m - 1) / kTile) : 0u;
+
+    unsigned long long e8[kGroups];
+    uint32_t emask[kGroups];
+    unsigned long long packed = 0;
+#pragma unroll
+    for (int g = 0; g < kGroups; g++) {
+        const uint32_t j = (uint32_t)(g * kThreads + t);
+        const uint32_t v = 8u * j;
+        e8[g] = v < nv ? ld_group8(es, v, nv) : 0ull;
+    }
+#pragma unroll
+    for (int g = 0; g < kGroups; g++) {
+        const uint32_t j = (uint32_t)(g * kThreads + t);
+        const uint32_t v = 8u * j;
+        const uint32_t vm = vmask_of(v, nv);
+        emask[g] = 0;
+        if (!vm) continue;
+        uint32_t p0 = 0, p1 = 0, p2 = 0, esc = 0;
+#pragma unroll
+        for (int i = 0; i < 8; i++) {
+            const uint32_t d = (uint32_t)((e8[g] >> (8 * i)) & 0xFFu) - E0;
+            const uint32_t code = d < 7u ? d + 1u : 0u;
+            p0 |= (code & 1u) << i;
+            p1 |= ((code >> 1) & 1u) << i;
+            p2 |= (code >> 2) << i;
+            esc |= (code == 0u ? 1u : 0u) << i;
+        }
+        const uint64_t pb = v0 / 8 + j;
+        pl[pb] = (uint8_t)(p0 & vm);
+        pl[plane + pb] = (uint8_t)(p1 & vm);
+        pl[2 * plane + pb] = (uint8_t)(p2 & vm);
+        emask[g] = esc & vm;
+        packed |= (unsigned long long)__popc(emask[g]) << (16 * g);
+    }
+    unsigned long long total;
+    const unsigned long long excl = block_excl_scan(packed, s_warp, &total);
+    const unsigned long long agg = (total & 0xFFFFull) + ((total >> 16) & 0xFFFFull) +
+                                   ((total >> 32) & 0xFFFFull) + (total >> 48);
+    const unsigned long long P = tile_prefix(a.state, tile, ci * a.tpc, agg, &s_prefix, a.dstatus, a.abort);
+    unsigned long long gbase = 0;
+#pragma unroll
+    for (int g = 0; g < kGroups; g++) {
+        uint32_t mm = emask[g];
+        unsigned long long q = P + gbase + ((excl >> (16 * g)) & 0xFFFFull);
+        while (mm) {
+            const int i = __ffs(mm) - 1;
+            mm &= mm - 1;
+            esc_sec[q++] = (uint8_t)(e8[g] >> (8 * i));
+        }
+        gbase += (total >> (16 * g)) & 0xFFFFull;
+    }
+    if (lt == fin_tile) {
+        const uint64_t n_esc = P + agg;
+        const uint64_t tot = ru_bytes(n_s, a.B, m, true, n_esc);
+        if (t < 64)
+            o[t] = (uint8_t)ru_header_byte(t, 1u | (a.cold ? 2u : 0u), E0, a.B, r, n_s, n_changed, m,
+                                           n_esc, tot);
+        const uint64_t pbytes = cdiv(m, 8);
+        if (t < 16 && pbytes + t < plane) {
+            pl[pbytes + t] = 0;
+            pl[plane + pbytes + t] = 0;
+            pl[2 * plane + pbytes + t] = 0;
+        }
+        if (t < 128 && off_exp + 3 * plane + n_esc + t < tot) o[off_exp + 3 * plane + n_esc + t] = 0;
+        if (t == 0) a.sizes[ci] = tot;
+    }
+}
+
+__device__ __forceinline__ uint64_t rd64(const uint8_t* p)
+{
+    uint64_t v = 0;
+#pragma unroll
+    for (int k = 7; k >= 0; k--) v = (v << 8) | p[k];
+    return v;
+}
+__device__ __forceinline__ uint32_t rd32(const uint8_t* p)
+{
+    return (uint32_t)p[0] | (uint32_t)p[1] << 8 | (uint32_t)p[2] << 16 | (uint32_t)p[3] << 24;
+}
+
+template <bool kCoded>
+__global__ void __launch_bounds__(kThreads) k_reuse_decode(RuDec a)
+{
+    __shared__ uint32_t s_tile, s_bad, s_E0;
+    __shared__ unsigned long long s_hdr[4];   // n_changed, m, n_esc
+    __shared__ uint32_t s_bm[32], s_pre[32], s_agg;
+    __shared__ unsigned long long s_warp[kThreads / 32];
+    __shared__ unsigned long long s_prefix;
+    const int t = threadIdx.x;
+    const uint32_t tile = next_tile(a.counter, &s_tile);
+    const uint32_t ci = tile / a.tpc, lt = tile - ci * a.tpc;
+    const uint32_t r = a.first + ci;
+    const uint64_t n_s = shard_values(a.n, a.L, r);
+    const uint64_t v0 = (uint64_t)lt * kTile;
+    const uint32_t nv = v0 < n_s ? (uint32_t)umin64(kTile, n_s - v0) : 0u;
+    const uint32_t B = a.B, log2B = a.log2B;
+    const uint64_t nb = cdiv(n_s, B);
+    const uint64_t bm_bytes = cdiv(nb, 8);
+    const uint32_t fin_tile = n_s ? (uint32_t)((n_s - 1) / kTile) : 0u;
+    const uint64_t off = a.offsets ? a.offsets[ci] : 0ull;
+    const uint8_t* p = a.in + off;
+    if (t == 0) {
+        uint32_t bad = 0;
+        uint64_t avail = 0;
+        if (a.offsets) {
+            const uint64_t end = a.offsets[ci + 1];
+            avail = end >= off ? end - off : 0;
+            if (end < off) bad = EZ_DSTAT_BAD_SIZE;
+        } else {
+            avail = a.single_avail;
+        }
+        if (!bad && (off & 15u)) bad = EZ_DSTAT_MISALIGNED;
+        if (!bad && avail < 64) bad = EZ_DSTAT_BAD_SIZE;
+        if (!bad) {
+            const uint32_t flags = p[5], E0 = p[6];
+            const uint64_t n_changed = rd64(p + 24), m = rd64(p + 32), n_esc = rd64(p + 40),
+                           total = rd64(p + 48);
+            const bool coded = flags & 1u;
+            if (!(p[0] == 'E' && p[1] == 'Z' && p[2] == 'R' && p[3] == 'U') || p[4] != 1 ||
+                (flags & ~3u) || p[7] != 0 || rd32(p + 8) != B || rd32(p + 12) != r ||
+                rd64(p + 16) != n_s || coded != kCoded)
+                bad = EZ_DSTAT_BAD_HEADER;
+            else if (coded ? E0 > 249 : (E0 != 0 || n_esc != 0))
+                bad = EZ_DSTAT_BAD_HEADER;
+            else if (n_changed > nb || m > n_s || n_esc > m)
+                bad = EZ_DSTAT_BAD_COUNT;
+            else if (total != ru_bytes(n_s, B, m, coded, n_esc) || total > avail)
+                bad = EZ_DSTAT_BAD_SIZE;
+            s_E0 = E0;
+            s_hdr[0] = n_changed;
+            s_hdr[1] = m;
+            s_hdr[2] = n_esc;
+        }
+        s_bad = bad;
+    }
+    if (t < 32) s_bm[t] = 0;
+    __syncthreads();
+    if (s_bad) {
+        if (lt == fin_tile && t == 0) atomicOr(a.dstatus, s_bad);
+        return;
+    }
+    const uint64_t n_changed = s_hdr[0], m = s_hdr[1], n_esc = s_hdr[2];
+    const uint32_t E0 = s_E0;
+    const uint64_t off_sm = ru_off_sm(n_s, B), off_exp = ru_off_exp(n_s, B);
+    const uint8_t* sm_t = p + off_sm + v0;
+    const uint8_t* ex = p + off_exp;
+    uint8_t* ct = a.cache + (uint64_t)ci * a.L + v0;
+    uint16_t* ot = a.out + (uint64_t)ci * a.L + v0;
+
+    // this tile's slice of the bitmap (bits past nb ignored)
+    const uint32_t nbt = (uint32_t)kTile >> log2B;
+    const uint64_t bm0 = (uint64_t)lt * (nbt / 8);
+    if ((uint32_t)t < nbt / 8) {
+        uint32_t b = 0;
+        if (bm0 + t < bm_bytes) {
+            b = p[64 + bm0 + t];
+            if (bm0 + t == bm_bytes - 1 && (nb & 7)) b &= (1u << (nb & 7)) - 1u;
+        }
+        if (b) atomicOr(&s_bm[t >> 2], b << (8 * (t & 3)));
+    }
+    __syncthreads();
+    if (t < 32) {
+        const uint32_t c = __popc(s_bm[t]);
+        uint32_t x = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(kFull, x, o);
+            if (t >= o) x += y;
+        }
+        s_pre[t] = x - c;
+        if (t == 31) s_agg = x;
+    }
+    __syncthreads();
+    const unsigned long long agg = s_agg;
+
+    // loads that do not depend on the prefix
+    unsigned long long smv[kGroups], ev[kGroups];
+    bool chg[kGroups];
+#pragma unroll
+    for (int g = 0; g < kGroups; g++) {
+        const uint32_t v = 8u * (uint32_t)(g * kThreads + t);
+        chg[g] = v < nv && block_changed(s_bm, v >> log2B);
+        smv[g] = v < nv ? ld_group8(sm_t, v, nv) : 0ull;
+        ev[g] = (v < nv && !chg[g]) ? ld_group8(ct, v, nv) : 0ull;
+    }
+    const unsigned long long P = tile_prefix(a.state_a, tile, ci * a.tpc, agg, &s_prefix, a.dstatus, a.abort);
+    bool bad_count = false;
+    if (lt == fin_tile && t == 0) {
+        bool last_changed = false;
+        if (n_s) last_changed = block_changed(s_bm, (uint32_t)((n_s - 1 - v0) >> log2B));
+        const uint64_t want_m = (P + agg) * B - (last_changed ? nb * B - n_s : 0);
+        if (P + agg != n_changed || want_m != m) bad_count = true;
+    }
+
+    if (!kCoded) {
+#pragma unroll
+        for (int g = 0; g < kGroups; g++) {
+            if (!chg[g]) continue;
+            const uint32_t v = 8u * (uint32_t)(g * kThreads + t);
+            const uint32_t k = v >> log2B;
+            const uint64_t pos = (P + block_rank(s_bm, s_pre, k)) * B + (v - (k << log2B));
+            const uint32_t cnt = min(8u, nv - v);
+            if (pos + cnt <= m) {
+                ev[g] = ld_group8(ex + pos, 0u, cnt);
+            } else {
+                ev[g] = 0;
+                bad_count = true;
+            }
+        }
+    } else {
+        // planes of this tile's changed exponents, then the escape prefix
+        const uint64_t plane = rup(cdiv(m, 8), 16);
+        const uint8_t* esc_sec = ex + 3 * plane;
+        uint32_t codes[kGroups], emask[kGroups];
+        unsigned long long packed = 0;
+        uint64_t pos[kGroups];
+#pragma unroll
+        for (int g = 0; g < kGroups; g++) {
+            codes[g] = 0;
+            emask[g] = 0;
+            pos[g] = 0;
+            if (!chg[g]) continue;
+            const uint32_t v = 8u * (uint32_t)(g * kThreads + t);
+            const uint32_t k = v >> log2B;
+            pos[g] = (P + block_rank(s_bm, s_pre, k)) * B + (v - (k << log2B));
+            const uint32_t cnt = min(8u, nv - v);
+            if (pos[g] + cnt > m) {
+                bad_count = true;
+                chg[g] = false;     // treated as a bad block: value left as cache contents
+                continue;
+            }
+            const uint64_t pb = pos[g] >> 3;
+            codes[g] = (uint32_t)ex[pb] | (uint32_t)ex[plane + pb] << 8 | (uint32_t)ex[2 * plane + pb] << 16;
+            const uint32_t vm = cnt >= 8 ? 0xFFu : ((1u << cnt) - 1u);
+            emask[g] = ~(codes[g] | codes[g] >> 8 | codes[g] >> 16) & vm;
+            packed |= (unsigned long long)__popc(emask[g]) << (16 * g);
+        }
+        unsigned long long total;
+        const unsigned long long excl = block_excl_scan(packed, s_warp, &total);
+        const unsigned long long agg2 = (total & 0xFFFFull) + ((total >> 16) & 0xFFFFull) +
+                                        ((total >> 32) & 0xFFFFull) + (total >> 48);
+        __syncthreads();   // s_prefix is reused
+        const unsigned long long Q = tile_prefix(a.state_b, tile, ci * a.tpc, agg2, &s_prefix, a.dstatus, a.abort);
+        if (lt == fin_tile && t == 0 && Q + agg2 != n_esc) bad_count = true;
+        unsigned long long gbase = 0;
+#pragma unroll
+        for (int g = 0; g < kGroups; g++) {
+            unsigned long long q = Q + gbase + ((excl >> (16 * g)) & 0xFFFFull);
+            gbase += (total >> (16 * g)) & 0xFFFFull;
+            if (!chg[g]) continue;
+            unsigned long long e = 0;
+#pragma unroll
+            for (int i = 0; i < 8; i++) {
+                const uint32_t cb = codes[g] >> i;
+                const uint32_t code = (cb & 1u) | ((cb >> 7) & 2u) | ((cb >> 14) & 4u);
+                uint32_t E = 0;
+                if (code) {
+                    E = E0 + code - 1;
+                } else if ((emask[g] >> i) & 1u) {
+                    if (q < n_esc) E = esc_sec[q];
+                    else bad_count = true;
+                    q++;
+                }
+                e |= (unsigned long long)E << (8 * i);
+            }
+            ev[g] = e;
+        }
+    }
+
+#pragma unroll
+    for (int g = 0; g < kGroups; g++) {
+        const uint32_t v = 8u * (uint32_t)(g * kThreads + t);
+        if (v >= nv) continue;
+        if (chg[g]) st_group8(ct, v, nv, ev[g]);
+        uint32_t h[8];
+#pragma unroll
+        for (int i = 0; i < 8; i++)
+            h[i] = merge_of((uint32_t)(smv[g] >> (8 * i)) & 0xFFu, (uint32_t)(ev[g] >> (8 * i)) & 0xFFu);
+        if (v + 8 <= nv) {
+            st_v4(ot + v, make_uint4(h[0] | h[1] << 16, h[2] | h[3] << 16, h[4] | h[5] << 16,
+                                     h[6] | h[7] << 16));
+        } else {
+            for (uint32_t i = 0; i < nv - v; i++) ot[v + i] = (uint16_t)h[i];
+        }
+    }
+    if (bad_count) atomicOr(a.dstatus, EZ_DSTAT_BAD_COUNT);
+}
+
+static uint32_t ilog2(uint32_t v)
+{
+    uint32_t r = 0;
+    while ((1u << r) < v) r++;
+    return r;
+}
+
+cudaError_t launch_reuse_encode(const ez_plan_s* p, const uint16_t* x, uint32_t first,
+                                uint32_t count, uint8_t* cache, int cold, uint8_t* out,
+                                uint64_t* sizes, ez_stats_t* st, uint32_t* dstatus,
+                                const WsView& w, cudaStream_t s)
+{
+    const bool coded = p->codec == EZ_CODEC_REUSE_CODE3;
+    RuEnc a;
+    a.x = x;
+    a.cache = cache;
+    a.out = out;
+    a.slot = p->slot_bytes;
+    a.sizes = sizes;
+    a.dstatus = dstatus;
+    a.n = p->n;
+    a.L = p->L;
+    a.W = p->W;
+    a.B = p->B;
+    a.log2B = ilog2(p->B);
+    a.first = first;
+    a.tpc = p->tpc;
+    a.cold = cold ? 1 : 0;
+    a.state = w.state_a;
+    a.counter = w.counters + 0;
+    a.abort = w.counters + 7;
+    a.expbuf = w.expbuf;
+    a.info = w.info;
+    a.bins = (StatsBins*)w.bins;
+    a.stats = st ? st : w.shard_stats;
+    a.K = p->K;
+    const unsigned tiles = (unsigned)((uint64_t)count * p->tpc);
+    if (!coded) {
+        k_reuse_encode<false><<<tiles, kThreads, 0, s>>>(a);
+        return cudaGetLastError();
+    }
+    k_reuse_encode<true><<<tiles, kThreads, sizeof(StatsSmem), s>>>(a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    RuC3 b;
+    b.out = out;
+    b.slot = p->slot_bytes;
+    b.sizes = sizes;
+    b.dstatus = dstatus;
+    b.n = p->n;
+    b.L = p->L;
+    b.W = p->W;
+    b.B = p->B;
+    b.first = first;
+    b.tpc = p->tpc;
+    b.cold = a.cold;
+    b.state = w.state_b;
+    b.counter = w.counters + 2;
+    b.abort = w.counters + 7;
+    b.expbuf = w.expbuf;
+    b.info = w.info;
+    b.stats = a.stats;
+    k_reuse_code3<<<tiles, kThreads, 0, s>>>(b);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_reuse_decode(const ez_plan_s* p, const uint8_t* in, const uint64_t* offsets,
+                                uint64_t single_avail, uint32_t first, uint32_t count,
+                                uint8_t* cache, uint16_t* out, uint32_t* dstatus,
+                                const WsView& w, cudaStream_t s)
+{
+    RuDec a;
+    a.in = in;
+    a.offsets = offsets;
+    a.single_avail = single_avail;
+    a.cache = cache;
+    a.out = out;
+    a.dstatus = dstatus;
+    a.n = p->n;
+    a.L = p->L;
+    a.W = p->W;
+    a.B = p->B;
+    a.log2B = ilog2(p->B);
+    a.first = first;
+    a.tpc = p->tpc;
+    a.state_a = w.state_a;
+    a.state_b = w.state_b;
+    a.counter = w.counters + 3;
+    a.abort = w.counters + 7;
+    const unsigned tiles = (unsigned)((uint64_t)count * p->tpc);
+    if (p->codec == EZ_CODEC_REUSE_CODE3) k_reuse_decode<true><<<tiles, kThreads, 0, s>>>(a);
+    else k_reuse_decode<false><<<tiles, kThreads, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace ezk
