@@ -17,7 +17,7 @@ bool al(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (
 
 // bytes of the per-shard records and of StatsBins (must match the device types)
 constexpr uint64_t kShardInfoBytes = 64;
-constexpr uint64_t kStatsBinsBytes = 5 * 256 * 8 + 256;
+constexpr uint64_t kStatsBinsBytes = 3 * 256 * 8 + 256;
 
 bool is_reuse(const ez_plan_s* p) { return p->codec != EZ_CODEC_CODE3; }
 
@@ -46,6 +46,7 @@ WsView ws_view(const ez_plan_s* p, void* ws)
     uint8_t* b = static_cast<uint8_t*>(ws);
     WsView v;
     v.counters = reinterpret_cast<uint32_t*>(b);
+    v.shard_ctr = reinterpret_cast<uint32_t*>(b + p->off_ctr);
     v.info = reinterpret_cast<ShardInfo*>(b + p->off_info);
     v.shard_stats = reinterpret_cast<ez_stats_t*>(b + p->off_shard_stats);
     v.bins = b + p->off_bins;
@@ -93,6 +94,8 @@ ez_status ez_plan_create(ez_plan* out, const ez_plan_desc* d)
     const bool coded = d->codec == EZ_CODEC_REUSE_CODE3;
     p->n_bins = coded ? d->W : 1;
     uint64_t off = 256;                                   // 8 tile counters
+    p->off_ctr = off;
+    off = rup(off + W * 4, 256);                          // per-shard tile counters
     p->off_info = off;
     off = rup(off + W * kShardInfoBytes, 256);
     p->off_shard_stats = off;

@@ -1,0 +1,104 @@
+// ez_bytes.cuh -- branch-light byte compaction and expansion for escapes.
+//
+// A group of 8 values has an 8-bit escape mask m.  The encoder must append
+// the escaping exponent bytes, in value order, to the tile's escape list; the
+// decoder must put the next popc(m) bytes of that list back at the set bits
+// of m.  Both are byte permutations that depend only on m, so they are done
+// with PRMT (__byte_perm) and selectors from compile-time tables indexed by m
+// instead of a per-escape loop.
+#pragma once
+
+#include <cstdint>
+
+namespace ez {
+
+struct ByteTables {
+    uint32_t comp_lo[256];   // PRMT selector: selected bytes 0..3 of (lo, hi)
+    uint32_t comp_hi[256];   // selected bytes 4..7
+    uint32_t exp_lo[256];    // PRMT selector: byte i (0..3) <- compact byte rank(i)
+    uint32_t exp_hi[256];    // byte i (4..7)
+    unsigned long long bmask[256];    // 0xFF in byte i where bit i of m is set
+    unsigned long long spread[256];   // bit i of b -> bit 8i
+};
+
+constexpr ByteTables make_byte_tables()
+{
+    ByteTables t{};
+    for (int m = 0; m < 256; m++) {
+        uint32_t clo = 0, chi = 0, elo = 0, ehi = 0;
+        unsigned long long bm = 0, sp = 0;
+        int rank = 0;
+        for (int i = 0; i < 8; i++) {
+            if ((m >> i) & 1) {
+                if (rank < 4) clo |= (uint32_t)i << (4 * rank);
+                else chi |= (uint32_t)i << (4 * (rank - 4));
+                if (i < 4) elo |= (uint32_t)rank << (4 * i);
+                else ehi |= (uint32_t)rank << (4 * (i - 4));
+                bm |= 0xFFull << (8 * i);
+                sp |= 1ull << (8 * i);
+                rank++;
+            }
+        }
+        t.comp_lo[m] = clo;
+        t.comp_hi[m] = chi;
+        t.exp_lo[m] = elo;
+        t.exp_hi[m] = ehi;
+        t.bmask[m] = bm;
+        t.spread[m] = sp;
+    }
+    return t;
+}
+
+__device__ const ByteTables kByteTables = make_byte_tables();
+
+// Append the bytes of (lo, hi) selected by m to s[r ...].  kmax is the
+// largest popc(m) over the warp (warp-uniform), so the store loop does not
+// diverge.
+__device__ __forceinline__ void stage_selected(uint8_t* s, uint32_t r, uint32_t m, uint32_t lo,
+                                               uint32_t hi, uint32_t kmax)
+{
+    const uint32_t c_lo = __byte_perm(lo, hi, __ldg(&kByteTables.comp_lo[m]));
+    const uint32_t c_hi = __byte_perm(lo, hi, __ldg(&kByteTables.comp_hi[m]));
+    const uint32_t cnt = __popc(m);
+#pragma unroll
+    for (uint32_t k = 0; k < 8; k++) {
+        if (k >= kmax) break;
+        if (k < cnt) s[r + k] = (uint8_t)((k < 4 ? c_lo >> (8 * k) : c_hi >> (8 * (k - 4))) & 0xFFu);
+    }
+}
+
+// The 8 bytes starting at byte offset r of a 4-byte-aligned shared buffer
+// (which must extend 12 bytes past the last byte read).
+__device__ __forceinline__ void load_unaligned8(const uint32_t* s32, uint32_t r, uint32_t& lo,
+                                                uint32_t& hi)
+{
+    const uint32_t q = r >> 2, o = r & 3u;
+    const uint32_t sel = 0x3210u + 0x1111u * o;
+    const uint32_t w0 = s32[q], w1 = s32[q + 1], w2 = s32[q + 2];
+    lo = __byte_perm(w0, w1, sel);
+    hi = __byte_perm(w1, w2, sel);
+}
+
+// e8 with the bytes at the set bits of m replaced, in order, by the compact
+// bytes (c_lo, c_hi).
+__device__ __forceinline__ unsigned long long insert_selected(unsigned long long e8, uint32_t m,
+                                                              uint32_t c_lo, uint32_t c_hi)
+{
+    const unsigned long long x =
+        (unsigned long long)__byte_perm(c_lo, c_hi, __ldg(&kByteTables.exp_hi[m])) << 32 |
+        __byte_perm(c_lo, c_hi, __ldg(&kByteTables.exp_lo[m]));
+    const unsigned long long bm = __ldg(&kByteTables.bmask[m]);
+    return (e8 & ~bm) | (x & bm);
+}
+
+__device__ __forceinline__ unsigned long long spread_bits(uint32_t b)
+{
+    return __ldg(&kByteTables.spread[b]);
+}
+
+__device__ __forceinline__ unsigned long long byte_mask(uint32_t m)
+{
+    return __ldg(&kByteTables.bmask[m]);
+}
+
+}  // namespace ez

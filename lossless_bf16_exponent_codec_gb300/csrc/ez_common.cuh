@@ -59,6 +59,48 @@ __device__ __forceinline__ uint32_t half_of(const uint4& w, int i)
     return (i & 1) ? (word >> 16) : (word & 0xFFFFu);
 }
 
+// ---- SWAR helpers: two BF16 values per 32-bit word --------------------------
+// Sign+mantissa bytes of the 4 values in words a (values 0,1) and b (2,3):
+// per 16-bit half, ((h >> 8) & 0x80) | (h & 0x7F), then bytes 0 and 2 of each.
+__device__ __forceinline__ uint32_t sm4_of(uint32_t a, uint32_t b)
+{
+    const uint32_t pa = ((a >> 8) & 0x00800080u) | (a & 0x007F007Fu);
+    const uint32_t pb = ((b >> 8) & 0x00800080u) | (b & 0x007F007Fu);
+    return __byte_perm(pa, pb, 0x6420);
+}
+// Exponent bytes of the 4 values in words a, b.
+__device__ __forceinline__ uint32_t exp4_of(uint32_t a, uint32_t b)
+{
+    return __byte_perm(a >> 7, b >> 7, 0x6420);
+}
+// Two output words (values 0,1 and 2,3) from 4 sign+mantissa bytes and 4
+// exponent bytes: per value ((sm & 0x80) << 8) | (E << 7) | (sm & 0x7F).
+__device__ __forceinline__ void merge4(uint32_t sm4, uint32_t e4, uint32_t& lo, uint32_t& hi)
+{
+    // X halves = E << 8 | sm ; then pick E << 7 from X >> 1, mantissa from X,
+    // sign from X << 8
+    const uint32_t x0 = __byte_perm(sm4, e4, 0x5140);
+    const uint32_t x1 = __byte_perm(sm4, e4, 0x7362);
+    lo = ((x0 >> 1) & 0x7F807F80u) | (x0 & 0x007F007Fu) | ((x0 << 8) & 0x80008000u);
+    hi = ((x1 >> 1) & 0x7F807F80u) | (x1 & 0x007F007Fu) | ((x1 << 8) & 0x80008000u);
+}
+
+// ---- tile order ----------------------------------------------------------------
+// Tile ids are dealt round-robin over the `count` shards of a launch, so the
+// shards' look-back chains advance side by side; state index is
+// shard-contiguous (shard ci owns [ci*tpc, (ci+1)*tpc)).
+struct TilePos {
+    uint32_t ci, lt, state;
+};
+__device__ __forceinline__ TilePos tile_pos(uint32_t id, uint32_t count, uint32_t tpc)
+{
+    TilePos p;
+    p.ci = id % count;
+    p.lt = id / count;
+    p.state = p.ci * tpc + p.lt;
+    return p;
+}
+
 // ---- memory helpers ----------------------------------------------------------
 __device__ __forceinline__ uint4 ld_v4_nc(const void* p)
 {
@@ -100,45 +142,72 @@ __device__ __forceinline__ uint32_t ld_relaxed32(const uint32_t* p)
     return v;
 }
 
+// Exclusive prefix of tile t over [seg_first, t).  One full warp calls it.
+// Each pass reads a window of 128 predecessors (4 per lane, nearest first) in
+// one round trip to L2, so the inclusive-prefix front advances 128 tiles per
+// round trip -- faster than tiles complete at HBM speed.  Entries before
+// seg_first act as an inclusive prefix of 0.
 // `abort` (per launch, zeroed with the tile states) is raised by the first
 // wait that gives up; every other wait then stops at once, so a broken chain
-// costs one spin limit, not one per tile.
+// costs one spin limit, not one per tile.  *stuck is set uniformly on a
+// give-up.
+constexpr int kLookPerLane = 4;
+
 static __device__ __noinline__ unsigned long long lookback(unsigned long long* st, long long t,
-                                                    long long seg_first, bool* stuck,
-                                                    uint32_t* abort)
+                                                           long long seg_first, bool* stuck,
+                                                           uint32_t* abort)
 {
     const int lane = threadIdx.x & 31;
     unsigned long long prefix = 0;
     long long pos = t - 1;
     *stuck = false;
     while (pos >= seg_first) {
-        const long long idx = pos - lane;
-        const bool valid = idx >= seg_first;
-        unsigned long long w = 0;
-        if (valid) {
-            w = ld_relaxed(st + idx);
+        unsigned long long w[kLookPerLane];
+#pragma unroll
+        for (int k = 0; k < kLookPerLane; k++) {
+            const long long idx = pos - (long long)(kLookPerLane * lane + k);
+            w[k] = idx >= seg_first ? ld_relaxed(st + idx) : kFlagIncl;
+        }
+        bool empty = false;
+#pragma unroll
+        for (int k = 0; k < kLookPerLane; k++) {
+            const long long idx = pos - (long long)(kLookPerLane * lane + k);
             uint32_t spins = 0;
-            while ((w >> 62) == 0 && spins < kSpinLimit) {
-                __nanosleep(40);
-                w = ld_relaxed(st + idx);
+            while ((w[k] >> 62) == 0 && spins < kSpinLimit) {
+                __nanosleep(32);
+                w[k] = ld_relaxed(st + idx);
                 if ((++spins & 63u) == 0 && ld_relaxed32(abort)) break;
             }
+            empty |= (w[k] >> 62) == 0;
         }
         __syncwarp();
-        if (__any_sync(kFull, valid && (w >> 62) == 0)) {
+        if (__any_sync(kFull, empty)) {
             *stuck = true;
-            if ((threadIdx.x & 31) == 0) atomicExch(abort, 1u);
+            if (lane == 0) atomicExch(abort, 1u);
             return prefix;
         }
-        const uint32_t incl = __ballot_sync(kFull, valid && (w >> 62) == 2);
-        unsigned long long v = valid ? (w & kValMask) : 0ull;
+        int kf = kLookPerLane;            // nearest inclusive entry of this lane
+        unsigned long long all = 0, part = 0;
+#pragma unroll
+        for (int k = kLookPerLane - 1; k >= 0; k--) {
+            const unsigned long long v = w[k] & kValMask;
+            all += v;
+            if ((w[k] >> 62) == 2) {
+                kf = k;
+                part = 0;
+            }
+            part += v;
+        }
+        // part = sum of entries 0..kf when kf < kLookPerLane
+        if (kf == kLookPerLane) part = all;
+        const uint32_t incl = __ballot_sync(kFull, kf < kLookPerLane);
         if (incl) {
-            const int j = __ffs(incl) - 1;     // nearest predecessor with a full prefix
-            if (lane > j) v = 0;
+            const int j = __ffs(incl) - 1;
+            const unsigned long long v = lane < j ? all : (lane == j ? part : 0ull);
             return prefix + warp_sum_u64(v);
         }
-        prefix += warp_sum_u64(v);
-        pos -= 32;
+        prefix += warp_sum_u64(all);
+        pos -= 32 * kLookPerLane;
     }
     return prefix;
 }
@@ -161,6 +230,86 @@ __device__ __forceinline__ unsigned long long block_excl_scan(unsigned long long
     unsigned long long pre = 0, tot = 0;
 #pragma unroll
     for (int i = 0; i < kThreads / 32; i++) {
+        unsigned long long s = s_warp[i];
+        if (i < wid) pre += s;
+        tot += s;
+    }
+    *total = tot;
+    return pre + x - v;
+}
+
+// ---- persistent, warp-specialised launches ----------------------------------
+// A CTA has kCompute threads (8 compute warps) plus one chain warp.  Compute
+// warps synchronise among themselves with named barrier 1; the chain warp
+// never joins it.  Slots of a small shared-memory ring pass tiles between the
+// two roles; every wait on a slot flag is bounded.
+constexpr int kCompute = kThreads;            // 256 compute threads
+constexpr int kPThreads = kCompute + 32;      // + the chain warp
+constexpr int kSlots = 4;
+
+__device__ __forceinline__ void compute_sync()
+{
+    asm volatile("bar.sync 1, %0;" :: "r"(kCompute) : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_volatile_s32(const volatile uint32_t* p) { return *p; }
+
+// Wait until *flag >= want (bounded); returns false if the wait gave up.
+__device__ __forceinline__ bool wait_flag(const volatile uint32_t* flag, uint32_t want, uint32_t* abort)
+{
+    uint32_t spins = 0;
+    while (ld_volatile_s32(flag) < want) {
+        if (++spins > kSpinLimit) return false;
+        if ((spins & 63u) == 0 && ld_relaxed32(abort)) return false;
+        __nanosleep(20);
+    }
+    return true;
+}
+
+// Shards served by CTA `c` of `G` persistent CTAs: with count <= G each shard
+// gets G/count CTAs (shard c % count); otherwise CTA c serves c, c+G, ...
+struct ShardIter {
+    uint32_t next, step, count;
+    __device__ __forceinline__ ShardIter(uint32_t c, uint32_t G, uint32_t count_)
+    {
+        count = count_;
+        if (count <= G) {
+            const uint32_t per = G / count;
+            next = (c < per * count) ? c % count : count;
+            step = count;   // one shard only
+        } else {
+            next = c;
+            step = G;
+        }
+    }
+    __device__ __forceinline__ bool valid() const { return next < count; }
+    __device__ __forceinline__ void advance() { next = (step == count) ? count : next + step; }
+};
+
+// CTAs serving shard s (for the count <= G case; 1 otherwise)
+__device__ __forceinline__ uint32_t servers_of(uint32_t G, uint32_t count)
+{
+    return count <= G ? G / count : 1u;
+}
+
+// Exclusive scan over the kCompute compute threads (named barrier 1); s_warp
+// holds 8 entries and must not be reused before the next compute_sync().
+__device__ __forceinline__ unsigned long long compute_excl_scan(unsigned long long v,
+                                                                unsigned long long* s_warp,
+                                                                unsigned long long* total)
+{
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    unsigned long long x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        unsigned long long y = __shfl_up_sync(kFull, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) s_warp[wid] = x;
+    compute_sync();
+    unsigned long long pre = 0, tot = 0;
+#pragma unroll
+    for (int i = 0; i < kCompute / 32; i++) {
         unsigned long long s = s_warp[i];
         if (i < wid) pre += s;
         tot += s;
@@ -204,6 +353,20 @@ __device__ __forceinline__ unsigned long long tile_prefix(unsigned long long* st
     }
     __syncthreads();
     return *s_prefix;
+}
+
+// Grid of a persistent kernel: resident CTAs per SM (from the occupancy
+// calculator) times the SM count of the current device.
+template <typename K>
+inline unsigned persistent_grid(K kernel, int threads, size_t dyn_smem = 0)
+{
+    int dev = 0, sms = 0, per = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, kernel, threads, dyn_smem);
+    if (per < 1) per = 1;
+    if (sms < 1) sms = 1;
+    return (unsigned)(sms * per);
 }
 
 }  // namespace ez

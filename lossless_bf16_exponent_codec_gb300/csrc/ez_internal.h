@@ -14,7 +14,7 @@ struct ez_plan_s {
     uint64_t slot_bytes;     // worst-case payload per shard
     double K;                // 16383 / (14 ln 2)
     // workspace layout (byte offsets); [0, zero_bytes) is cleared per call
-    uint64_t off_info, off_shard_stats, off_bins, off_state_a, off_state_b, off_expbuf;
+    uint64_t off_ctr, off_info, off_shard_stats, off_bins, off_state_a, off_state_b, off_expbuf;
     uint64_t zero_bytes, ws_bytes;
     uint32_t n_bins;
 };
@@ -31,6 +31,7 @@ struct ShardInfo {
 
 struct WsView {
     uint32_t* counters;            // 8 tile counters
+    uint32_t* shard_ctr;           // W per-shard tile counters
     ShardInfo* info;               // W records
     ez_stats_t* shard_stats;       // W records (reuse+code3 without caller stats)
     unsigned long long* state_a;

@@ -7,20 +7,17 @@
 //
 //   v = (-1)^s * M * 2^(E-134),  M = 128 + mantissa  (E >= 1)
 //
-// Per value the hot loop does integer work only.  A CTA picks a 16-binade
-// window [Elo, Elo+16) around the mode of a sample of its exponents.  Values
-// inside it add
-//   * (count, sum of +-M) into a lane-private shared-memory cell of their
-//     exponent: cell += 2^22 + 256 +- M (count in bits 22..31, sum + 256*count
-//     in bits 0..21; at most 1023 values per cell before a flush), and
-//   * (M << (E-Elo))^2 < 2^46 into a per-thread 64-bit fixed-point sum of
-//     squares.
-// Values outside the window (and zeros, subnormals, Inf/NaN) go to exact
-// per-exponent bins with shared-memory atomics.  At the end of a tile the
-// CTA folds everything into per-shard global bins (64-bit atomics; the
-// window sums into a 128-bit slot per Elo).  The last CTA of the shard turns
-// the bins into one big integer per sum, rounds it to nearest-even double,
-// and derives var, sigma and the window base E0.
+// so s1 and s2 follow from per-exponent integer sums of +-M and M^2.  Per
+// value the hot loop is integer work on shared memory only.  A CTA picks a
+// 16-binade window [Elo, Elo+16) around the mode of a sample of its
+// exponents.  A value inside it adds 2^22 + M to the lane-private cell of
+// (sign, E) -- count in bits 22..31, sum of M in bits 0..21 -- and M^2 to the
+// lane-private square cell of E; lane-private cells never conflict.  Values
+// outside the window (and zeros, subnormals, Inf/NaN) go to per-exponent
+// bins with shared-memory atomics.  At the end of a tile the CTA folds
+// everything into per-shard global bins (64-bit atomics); the last CTA of the
+// shard turns the bins into one big integer per sum, rounds it to nearest
+// even, and derives var, sigma and the window base E0.
 #pragma once
 
 #include "ez_common.cuh"
@@ -30,26 +27,27 @@ namespace ez {
 struct StatsBins {                 // per shard, in the workspace (zeroed per call)
     unsigned long long hist[256];
     unsigned long long s1[256];    // two's-complement int64 sums of +-M
-    unsigned long long s2[256];    // sums of M^2 of out-of-window values
-    unsigned long long s2w_lo[256];// 128-bit window sums of (M << (E-Elo))^2, by Elo
-    unsigned long long s2w_hi[256];
+    unsigned long long s2[256];    // sums of M^2
     unsigned int done;             // CTAs that have flushed
     unsigned int pad[63];
 };
 
+// Per-CTA accumulators (dynamic shared memory).  A CTA adds at most 32768
+// values per tile (at most 128 per lane), so no cell or bin can overflow:
+// 1023 values per packed cell, 128 * 65025 < 2^32 per square cell, and
+// 32768 * 65025 < 2^32 per square bin.
 struct StatsSmem {
-    uint32_t cells[kThreads / 32][16][32];
-    unsigned long long cnt[256];
-    unsigned long long s1[256];
-    unsigned long long s2[256];
-    unsigned long long red_lo[kThreads / 32];
-    unsigned long long red_hi[kThreads / 32];
+    uint32_t cells[kThreads / 32][32][32];   // [warp][sign*16 + d][lane]
+    uint32_t sq[kThreads / 32][16][32];      // [warp][d][lane]
+    uint32_t cnt[256];
+    int s1[256];
+    uint32_t s2[256];
     uint32_t sample[256];
     uint32_t elo;
     uint32_t last;
 };
 
-constexpr uint32_t kCellOne = (1u << 22) | 256u;
+constexpr uint32_t kCellOne = 1u << 22;
 
 // Zero the CTA's accumulators and choose Elo from one exponent per thread
 // (h0 = that thread's first value, or 0xFFFFFFFF for none).
@@ -60,8 +58,9 @@ __device__ __forceinline__ void st_begin(StatsSmem& S, uint32_t h0)
     S.s1[t] = 0;
     S.s2[t] = 0;
     S.sample[t] = 0;
-    uint32_t* c = &S.cells[0][0][0];
-    for (int i = t; i < (kThreads / 32) * 16 * 32; i += kThreads) c[i] = 0;
+    uint4* c = reinterpret_cast<uint4*>(&S.cells[0][0][0]);
+    constexpr int kVec = (int)((sizeof(S.cells) + sizeof(S.sq)) / 16);
+    for (int i = t; i < kVec; i += kThreads) c[i] = make_uint4(0, 0, 0, 0);
     __syncthreads();
     if (h0 != 0xFFFFFFFFu) atomicAdd(&S.sample[exp_of(h0)], 1u);
     __syncthreads();
@@ -88,79 +87,58 @@ __device__ __forceinline__ void st_begin(StatsSmem& S, uint32_t h0)
     __syncthreads();
 }
 
-__device__ __forceinline__ void st_add(uint32_t h, uint32_t elo, uint32_t* cell,
-                                       unsigned long long& acc2, StatsSmem& S)
+// One value h (16 bits).  `cell` = &S.cells[warp][0][lane], `sq` = &S.sq[warp][0][lane].
+__device__ __forceinline__ void st_add(uint32_t h, uint32_t elo, uint32_t* cell, uint32_t* sq,
+                                       StatsSmem& S)
 {
-    const uint32_t E = exp_of(h);
-    const uint32_t d = E - elo;
-    if (d < 16u) {
-        const uint32_t M = (h & 0x7Fu) | 0x80u;
-        cell[d * 32] += (h & 0x8000u) ? (kCellOne - M) : (kCellOne + M);
-        const uint32_t V = M << d;
-        acc2 += (unsigned long long)V * V;
+    // v = sign*256 + E - Elo; in the window iff its low byte is below 16
+    // (Elo <= 239 keeps E = 255 and E < Elo outside)
+    const uint32_t v = (h >> 7) - elo;
+    if ((v & 0xF0u) == 0) {
+        const uint32_t k = (v & 0xFu) | ((v >> 4) & 0x10u);     // sign*16 + d
+        const uint32_t m = h & 0x7Fu;
+        atomicAdd(cell + 32 * k, kCellOne | 0x80u | m);
+        atomicAdd(sq + 32 * (v & 0xFu), (m | 0x80u) * (m | 0x80u));
     } else {
-        atomicAdd(&S.cnt[E], 1ull);
+        const uint32_t E = exp_of(h);
+        atomicAdd(&S.cnt[E], 1u);
         if (E != 255u) {
             const uint32_t M = (E ? 128u : 0u) | (h & 0x7Fu);
-            const long long sM = (h & 0x8000u) ? -(long long)M : (long long)M;
-            atomicAdd(&S.s1[E], (unsigned long long)sM);
-            atomicAdd(&S.s2[E], (unsigned long long)(M * M));
+            atomicAdd(&S.s1[E], (h & 0x8000u) ? -(int)M : (int)M);
+            atomicAdd(&S.s2[E], M * M);
         }
     }
 }
 
 // Fold the CTA into the global bins; returns true in every thread of the CTA
 // that is the `expected`-th to finish (it must then call st_finalize).
-__device__ __forceinline__ bool st_end(StatsSmem& S, unsigned long long acc2, StatsBins* G,
-                                       uint32_t expected)
+__device__ __forceinline__ bool st_end(StatsSmem& S, StatsBins* G, uint32_t expected)
 {
     const int t = threadIdx.x, lane = t & 31, wid = t >> 5;
     const uint32_t elo = S.elo;
+    __syncthreads();
     // lane-private cells -> per-exponent CTA bins
 #pragma unroll 4
     for (int d = 0; d < 16; d++) {
-        const uint32_t c = S.cells[wid][d][lane];
-        const uint32_t cnt = c >> 22;
-        const int s1 = (int)(c & 0x3FFFFFu) - 256 * (int)cnt;
+        const uint32_t cp = S.cells[wid][d][lane];
+        const uint32_t cn = S.cells[wid][16 + d][lane];
+        const uint32_t q = S.sq[wid][d][lane];
+        const uint32_t cnt = (cp >> 22) + (cn >> 22);
+        const int s1 = (int)(cp & 0x3FFFFFu) - (int)(cn & 0x3FFFFFu);
         const uint32_t wc = __reduce_add_sync(kFull, cnt);
         const int ws = __reduce_add_sync(kFull, s1);
+        const uint32_t wq = __reduce_add_sync(kFull, q);
         if (lane == 0 && wc) {
-            atomicAdd(&S.cnt[elo + d], (unsigned long long)wc);
-            atomicAdd(&S.s1[elo + d], (unsigned long long)(long long)ws);
+            atomicAdd(&S.cnt[elo + d], wc);
+            atomicAdd(&S.s1[elo + d], ws);
+            atomicAdd(&S.s2[elo + d], wq);
         }
-    }
-    // 128-bit sum of the window squares
-    unsigned long long lo = acc2, hi = 0;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const unsigned long long l2 = __shfl_xor_sync(kFull, lo, o);
-        const unsigned long long h2 = __shfl_xor_sync(kFull, hi, o);
-        const unsigned long long s = lo + l2;
-        hi = hi + h2 + (s < lo ? 1ull : 0ull);
-        lo = s;
-    }
-    if (lane == 0) {
-        S.red_lo[wid] = lo;
-        S.red_hi[wid] = hi;
     }
     __syncthreads();
-    if (t == 0) {
-        unsigned long long L = 0, H = 0;
-        for (int i = 0; i < kThreads / 32; i++) {
-            const unsigned long long s = L + S.red_lo[i];
-            H += S.red_hi[i] + (s < L ? 1ull : 0ull);
-            L = s;
-        }
-        if (L | H) {
-            const unsigned long long old = atomicAdd(&G->s2w_lo[elo], L);
-            const unsigned long long carry = (old + L < old) ? 1ull : 0ull;
-            if (H + carry) atomicAdd(&G->s2w_hi[elo], H + carry);
-        }
-    }
     // per-exponent bins -> global
-    if (S.cnt[t]) atomicAdd(&G->hist[t], S.cnt[t]);
-    if (S.s1[t]) atomicAdd(&G->s1[t], S.s1[t]);
-    if (S.s2[t]) atomicAdd(&G->s2[t], S.s2[t]);
+    if (S.cnt[t]) atomicAdd(&G->hist[t], (unsigned long long)S.cnt[t]);
+    if (S.s1[t]) atomicAdd(&G->s1[t], (unsigned long long)(long long)S.s1[t]);
+    if (S.s2[t]) atomicAdd(&G->s2[t], (unsigned long long)S.s2[t]);
     __threadfence();
     __syncthreads();
     if (t == 0) S.last = (atomicAdd(&G->done, 1u) == expected - 1) ? 1u : 0u;
@@ -259,32 +237,39 @@ __device__ __forceinline__ uint32_t window_base(double var, double K)
     return (uint32_t)lo;
 }
 
-// One thread of the last CTA finalises; every thread copies the histogram.
-static __device__ void st_finalize(const StatsBins* G, uint64_t n, double K, ez_stats_t* out)
+// The last CTA finalises: all its threads load the bins into shared memory
+// (reusing the cell area), thread 0 does the exact arithmetic from there.
+struct FinSmem {
+    unsigned long long h[256];
+    unsigned long long s1[256];
+    unsigned long long s2[256];
+};
+static_assert(sizeof(FinSmem) <= sizeof(StatsSmem::cells), "finalise scratch fits the cells");
+
+static __device__ void st_finalize(const StatsBins* G, uint64_t n, double K, ez_stats_t* out,
+                                   StatsSmem& S)
 {
     const int t = threadIdx.x;
-    out->hist[t] = __ldcg(&G->hist[t]);
+    FinSmem& F = *reinterpret_cast<FinSmem*>(&S.cells[0][0][0]);
+    __syncthreads();
+    const unsigned long long h = __ldcg(&G->hist[t]);
+    F.h[t] = h;
+    F.s1[t] = __ldcg(&G->s1[t]);
+    F.s2[t] = __ldcg(&G->s2[t]);
+    out->hist[t] = h;
+    __syncthreads();
     if (t != 0) return;
     Big P, Q, R;
     for (int i = 0; i < 24; i++) { P.w[i] = 0; Q.w[i] = 0; R.w[i] = 0; }
     unsigned long long n_fin = 0;
-    for (int E = 0; E < 256; E++) {
-        const unsigned long long c = __ldcg(&G->hist[E]);
-        if (E != 255) n_fin += c;
-        if (E == 255) continue;
+    for (int E = 0; E < 255; E++) {
+        n_fin += F.h[E];
+        if (!F.h[E]) continue;
         const int sh = (E ? E : 1) - 1;     // v * 2^133 = +-M * 2^sh
-        const long long s1 = (long long)__ldcg(&G->s1[E]);
+        const long long s1 = (long long)F.s1[E];
         if (s1 > 0) big_add_shl(P, (unsigned long long)s1, sh);
         else if (s1 < 0) big_add_shl(Q, (unsigned long long)(-s1), sh);
-        const unsigned long long s2 = __ldcg(&G->s2[E]);
-        if (s2) big_add_shl(R, s2, 2 * sh);
-        if (E >= 1) {
-            const unsigned long long wl = __ldcg(&G->s2w_lo[E]);
-            const unsigned long long wh = __ldcg(&G->s2w_hi[E]);
-            // window sums at Elo = E: v^2 * 2^266 = (M<<d)^2 * 2^(2(E-1))
-            if (wl) big_add_shl(R, wl, 2 * (E - 1));
-            if (wh) big_add_shl(R, wh, 2 * (E - 1) + 64);
-        }
+        if (F.s2[E]) big_add_shl(R, F.s2[E], 2 * sh);   // v^2 * 2^266 = M^2 * 2^(2 sh)
     }
     double s1d;
     if (big_cmp(P, Q) >= 0) {
@@ -309,16 +294,16 @@ static __device__ void st_finalize(const StatsBins* G, uint64_t n, double K, ez_
     if (rule == 1) {
         // the densest run of 7 exponent bins, ties to the lowest base
         unsigned long long run = 0, best = 0;
-        for (int E = 0; E < 7; E++) run += __ldcg(&G->hist[E]);
+        for (int E = 0; E < 7; E++) run += F.h[E];
         best = run;
         E0 = 0;
         for (int b = 1; b <= 249; b++) {
-            run += __ldcg(&G->hist[b + 6]) - __ldcg(&G->hist[b - 1]);
+            run += F.h[b + 6] - F.h[b - 1];
             if (run > best) { best = run; E0 = (uint32_t)b; }
         }
     }
     unsigned long long inwin = 0;
-    for (uint32_t E = E0; E <= E0 + 6; E++) inwin += __ldcg(&G->hist[E]);
+    for (uint32_t E = E0; E <= E0 + 6; E++) inwin += F.h[E];
     out->n = n;
     out->n_finite = n_fin;
     out->s1 = s1d;

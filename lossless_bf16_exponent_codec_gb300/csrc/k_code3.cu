@@ -15,6 +15,8 @@
 // chunk writes the header, the zero padding and the chunk size.
 #include "ez_internal.h"
 #include "ez_common.cuh"
+#include "ez_bytes.cuh"
+#include "ez_tma.cuh"
 
 namespace ezk {
 using namespace ez;
@@ -27,10 +29,11 @@ struct C3Enc {
     const ez_stats_t* st;
     uint32_t* dstatus;
     uint64_t n, L;
-    uint32_t W, first, tpc;
+    uint32_t W, first, count, tpc;
     unsigned long long* state;
     uint32_t* counter;
     uint32_t* abort;
+    uint32_t* shard_ctr;
 };
 
 struct C3Dec {
@@ -39,7 +42,7 @@ struct C3Dec {
     uint16_t* out;
     uint32_t* dstatus;
     uint64_t n, L;
-    uint32_t W, first, tpc;
+    uint32_t W, first, count, tpc;
     unsigned long long* state;
     uint32_t* counter;
     uint32_t* abort;
@@ -83,109 +86,276 @@ __device__ __forceinline__ uint4 load_group(const uint16_t* p, uint32_t v, uint3
     return make_uint4(h[0] | h[1] << 16, h[2] | h[3] << 16, h[4] | h[5] << 16, h[6] | h[7] << 16);
 }
 
-__global__ void __launch_bounds__(kThreads) k_code3_encode(C3Enc a)
+// Per exponent value e, the code's three plane bits spread to bits 0, 8 and 16
+// and the escape flag at bit 24: adding lut[E_i] << i over the 8 values of a
+// group yields plane bytes 0..2 and the escape mask in one register.
+__device__ __forceinline__ uint32_t c3_lut_entry(uint32_t e, uint32_t E0)
 {
-    __shared__ uint32_t s_tile;
-    __shared__ unsigned long long s_warp[kThreads / 32];
-    __shared__ unsigned long long s_prefix;
+    const uint32_t d = e - E0;
+    const uint32_t code = d < 7u ? d + 1u : 0u;
+    return (code & 1u) | ((code & 2u) << 7) | ((code & 4u) << 14) | (code ? 0u : (1u << 24));
+}
+
+__device__ __forceinline__ uint32_t lut_at(const uint32_t* lut, uint32_t byte_off)
+{
+    return *reinterpret_cast<const uint32_t*>(reinterpret_cast<const char*>(lut) + byte_off);
+}
+
+__device__ __forceinline__ uint32_t group_codes(const uint32_t* lut, const uint4& w)
+{
+    uint32_t acc = 0;
+    acc += lut_at(lut, (w.x >> 5) & 0x3FCu);
+    acc += lut_at(lut, (w.x >> 21) & 0x3FCu) << 1;
+    acc += lut_at(lut, (w.y >> 5) & 0x3FCu) << 2;
+    acc += lut_at(lut, (w.y >> 21) & 0x3FCu) << 3;
+    acc += lut_at(lut, (w.z >> 5) & 0x3FCu) << 4;
+    acc += lut_at(lut, (w.z >> 21) & 0x3FCu) << 5;
+    acc += lut_at(lut, (w.w >> 5) & 0x3FCu) << 6;
+    acc += lut_at(lut, (w.w >> 21) & 0x3FCu) << 7;
+    return acc;
+}
+
+__device__ __forceinline__ uint32_t byte_of(uint32_t lo, uint32_t hi, int i)
+{
+    return ((i < 4 ? lo : hi) >> (8 * (i & 3))) & 0xFFu;
+}
+
+constexpr uint32_t kEndMark = 0xFFFFFFFFu;
+constexpr int kStages = 4;                       // input ring depth (16 KB per stage)
+constexpr int kEncThreads = kCompute + 64;       // + chain warp + producer warp
+
+struct EncSmem {
+    __align__(128) uint8_t in[kStages][kTile * 2];
+    __align__(16) uint8_t esc[kSlots][kTile + 16];
+};
+
+__device__ __forceinline__ uint4 lds128(const uint8_t* p)
+{
+    return *reinterpret_cast<const uint4*>(p);
+}
+
+// Persistent, warp-specialised:
+//  * producer warp: takes the next tile of a chunk this CTA serves and starts
+//    a bulk copy of its BF16 values into a ring stage;
+//  * 8 compute warps: code the tile from shared memory, store sign+mantissa
+//    bytes and planes, stage the escapes in an escape slot, publish the
+//    tile's escape count;
+//  * chain warp: resolves each tile's escape prefix in order (decoupled
+//    look-back), writes the escapes, and on a chunk's last tile its header,
+//    padding and size.
+__global__ void __launch_bounds__(kEncThreads, 2) k_code3_encode(C3Enc a)
+{
+    extern __shared__ __align__(128) unsigned char dyn[];
+    EncSmem& S = *reinterpret_cast<EncSmem*>(dyn);
+    __shared__ unsigned long long s_full[kStages];
+    __shared__ uint32_t s_ici[kStages], s_ilt[kStages], s_empty[kStages];
+    __shared__ uint32_t s_lut[256];
+    __shared__ uint32_t s_sci[kSlots], s_slt[kSlots], s_sagg[kSlots];
+    __shared__ uint32_t s_efull[kSlots], s_edone[kSlots];
+    __shared__ unsigned long long s_warp[kCompute / 32];
     const int t = threadIdx.x;
-    const uint32_t tile = next_tile(a.counter, &s_tile);
-    const uint32_t ci = tile / a.tpc, lt = tile - ci * a.tpc;
-    const uint32_t c = a.first + ci;
-    const uint64_t n_c = shard_values(a.n, a.L, c);
-    const uint64_t v0 = (uint64_t)lt * kTile;
-    const uint32_t nv = v0 < n_c ? (uint32_t)umin64(kTile, n_c - v0) : 0u;
     uint32_t E0 = __ldg(&a.st->E0);
     if (E0 > 249u) {
         if (t == 0) atomicOr(a.dstatus, EZ_DSTAT_BAD_STATS);
         E0 = 0;
     }
-    const uint16_t* xt = a.x + (uint64_t)ci * a.L + v0;
-    uint8_t* o = a.out + (uint64_t)ci * a.slot;
-    const uint64_t plane = rup(cdiv(n_c, 8), 128);
-    uint8_t* sm_sec = o + 128;
-    uint8_t* pl_sec = sm_sec + rup(n_c, 128);
-    uint8_t* esc_sec = pl_sec + 3 * plane;
-    uint8_t* pl_t = pl_sec + v0 / 8;
+    if (t < 256) s_lut[t] = c3_lut_entry((uint32_t)t, E0);
+    if (t < kStages) {
+        mbar_init(&s_full[t], 1);
+        s_empty[t] = 0;
+    }
+    if (t < kSlots) {
+        s_efull[t] = 0;
+        s_edone[t] = 0;
+    }
+    mbar_fence_init();
+    __syncthreads();
+    volatile uint32_t* vempty = s_empty;
+    volatile uint32_t* vefull = s_efull;
+    volatile uint32_t* vedone = s_edone;
 
-    uint4 w[kGroups];
-#pragma unroll
-    for (int g = 0; g < kGroups; g++) w[g] = load_group(xt, 8u * (uint32_t)(g * kThreads + t), nv);
-
-    uint32_t emask[kGroups];
-    unsigned long long packed = 0;
-#pragma unroll
-    for (int g = 0; g < kGroups; g++) {
-        const uint32_t j = (uint32_t)(g * kThreads + t);
-        const uint32_t v = 8u * j;
-        emask[g] = 0;
-        if (v < nv) {
-            const uint32_t vmask = (nv - v >= 8) ? 0xFFu : ((1u << (nv - v)) - 1u);
-            uint32_t p0 = 0, p1 = 0, p2 = 0, esc = 0, s_lo = 0, s_hi = 0;
-#pragma unroll
-            for (int i = 0; i < 8; i++) {
-                const uint32_t h = half_of(w[g], i);
-                const uint32_t d = exp_of(h) - E0;
-                const uint32_t code = d < 7u ? d + 1u : 0u;
-                p0 |= (code & 1u) << i;
-                p1 |= ((code >> 1) & 1u) << i;
-                p2 |= (code >> 2) << i;
-                esc |= (code == 0u ? 1u : 0u) << i;
-                if (i < 4) s_lo |= sm_of(h) << (8 * i);
-                else s_hi |= sm_of(h) << (8 * (i - 4));
+    if (t >= kCompute + 32) {
+        // ---- producer warp (one lane)
+        if (t != kCompute + 32) return;
+        uint32_t it = 0;
+        for (ShardIter sh(blockIdx.x, gridDim.x, a.count); sh.valid(); sh.advance()) {
+            const uint32_t ci = sh.next;
+            const uint64_t n_c = shard_values(a.n, a.L, a.first + ci);
+            for (;; it++) {
+                const uint32_t s = it % kStages, round = it / kStages;
+                if (!wait_flag(&vempty[s], round, a.abort)) atomicOr(a.dstatus, EZ_DSTAT_TIMEOUT);
+                const uint32_t lt = atomicAdd(&a.shard_ctr[ci], 1u);
+                if (lt >= a.tpc) break;
+                const uint64_t v0 = (uint64_t)lt * kTile;
+                const uint32_t nv = v0 < n_c ? (uint32_t)umin64(kTile, n_c - v0) : 0u;
+                const uint32_t bytes = (nv & ~7u) * 2u;
+                s_ici[s] = ci;
+                s_ilt[s] = lt;
+                mbar_arrive_expect_tx(&s_full[s], bytes);
+                if (bytes) bulk_g2s(S.in[s], a.x + (uint64_t)ci * a.L + v0, bytes, &s_full[s]);
             }
-            p0 &= vmask;
-            p1 &= vmask;
-            p2 &= vmask;
-            esc &= vmask;
-            if (vmask == 0xFFu) {
-                *reinterpret_cast<uint2*>(sm_sec + v0 + v) = make_uint2(s_lo, s_hi);
-            } else {
-                for (uint32_t i = 0; i < nv - v; i++)
-                    sm_sec[v0 + v + i] = (uint8_t)((i < 4 ? s_lo >> (8 * i) : s_hi >> (8 * (i - 4))) & 0xFFu);
-            }
-            pl_t[j] = (uint8_t)p0;
-            pl_t[plane + j] = (uint8_t)p1;
-            pl_t[2 * plane + j] = (uint8_t)p2;
-            emask[g] = esc;
-            packed |= (unsigned long long)__popc(esc) << (16 * g);
         }
+        const uint32_t s = it % kStages, round = it / kStages;
+        if (!wait_flag(&vempty[s], round, a.abort)) atomicOr(a.dstatus, EZ_DSTAT_TIMEOUT);
+        s_ici[s] = kEndMark;
+        mbar_arrive(&s_full[s]);
+        return;
     }
 
-    unsigned long long total;
-    const unsigned long long excl = block_excl_scan(packed, s_warp, &total);
-    const unsigned long long agg = (total & 0xFFFFull) + ((total >> 16) & 0xFFFFull) +
-                                   ((total >> 32) & 0xFFFFull) + (total >> 48);
-    const unsigned long long P = tile_prefix(a.state, tile, ci * a.tpc, agg, &s_prefix, a.dstatus, a.abort);
+    if (t < kCompute) {
+        // ---- compute warps
+        uint32_t it = 0;
+        for (;; it++) {
+            const uint32_t s = it % kStages;
+            if (!mbar_wait(&s_full[s], (it / kStages) & 1u, a.abort)) {
+                // give up on the pipeline, but let a copy still in flight land
+                // before this CTA leaves
+                if (t == 0) {
+                    atomicOr(a.dstatus, EZ_DSTAT_TIMEOUT);
+                    atomicExch(a.abort, 1u);
+                }
+                uint32_t zero = 0;
+                mbar_wait(&s_full[s], (it / kStages) & 1u, &zero);
+                break;
+            }
+            const uint32_t ci = s_ici[s];
+            if (ci == kEndMark) break;
+            const uint32_t lt = s_ilt[s];
+            const uint32_t es = it % kSlots, eround = it / kSlots;
+            const uint32_t c = a.first + ci;
+            const uint64_t n_c = shard_values(a.n, a.L, c);
+            const uint64_t v0 = (uint64_t)lt * kTile;
+            const uint32_t nv = v0 < n_c ? (uint32_t)umin64(kTile, n_c - v0) : 0u;
+            uint8_t* o = a.out + (uint64_t)ci * a.slot;
+            const uint64_t plane = rup(cdiv(n_c, 8), 128);
+            uint8_t* sm_sec = o + 128;
+            uint8_t* pl_t = sm_sec + rup(n_c, 128) + v0 / 8;
+            const uint16_t* xt = a.x + (uint64_t)ci * a.L + v0;
 
-    unsigned long long gbase = 0;
+            uint4 w[kGroups];
 #pragma unroll
-    for (int g = 0; g < kGroups; g++) {
-        uint32_t m = emask[g];
-        unsigned long long r = P + gbase + ((excl >> (16 * g)) & 0xFFFFull);
-        while (m) {
-            const int i = __ffs(m) - 1;
-            m &= m - 1;
-            esc_sec[r++] = (uint8_t)exp_of(half_of(w[g], i));
+            for (int g = 0; g < kGroups; g++) {
+                const uint32_t v = 8u * (uint32_t)(g * kCompute + t);
+                w[g] = (v + 8 <= nv) ? lds128(S.in[s] + 2 * v) : load_group(xt, v, nv);
+            }
+            uint32_t emasks = 0;
+            unsigned long long packed = 0;
+#pragma unroll
+            for (int g = 0; g < kGroups; g++) {
+                const uint32_t j = (uint32_t)(g * kCompute + t);
+                const uint32_t v = 8u * j;
+                if (v >= nv) continue;
+                uint32_t acc = group_codes(s_lut, w[g]);
+                const uint32_t sm_lo = sm4_of(w[g].x, w[g].y), sm_hi = sm4_of(w[g].z, w[g].w);
+                if (nv - v >= 8) {
+                    *reinterpret_cast<uint2*>(sm_sec + v0 + v) = make_uint2(sm_lo, sm_hi);
+                } else {
+                    const uint32_t vm = (1u << (nv - v)) - 1u;
+                    acc &= vm * 0x01010101u;
+                    for (uint32_t i = 0; i < nv - v; i++)
+                        sm_sec[v0 + v + i] = (uint8_t)byte_of(sm_lo, sm_hi, (int)i);
+                }
+                pl_t[j] = (uint8_t)acc;
+                pl_t[plane + j] = (uint8_t)(acc >> 8);
+                pl_t[2 * plane + j] = (uint8_t)(acc >> 16);
+                const uint32_t esc = acc >> 24;
+                emasks |= esc << (8 * g);
+                packed |= (unsigned long long)__popc(esc) << (16 * g);
+            }
+            if (t == 0 && !wait_flag(&vedone[es], eround, a.abort)) atomicOr(a.dstatus, EZ_DSTAT_TIMEOUT);
+            unsigned long long total;
+            const unsigned long long excl = compute_excl_scan(packed, s_warp, &total);
+            if (t == 0) {
+                __threadfence_block();
+                vempty[s] = (it / kStages) + 1;     // every compute thread has read the stage
+            }
+            const unsigned long long agg = (total & 0xFFFFull) + ((total >> 16) & 0xFFFFull) +
+                                           ((total >> 32) & 0xFFFFull) + (total >> 48);
+            uint32_t gbase = 0;
+#pragma unroll
+            for (int g = 0; g < kGroups; g++) {
+                const uint32_t m = (emasks >> (8 * g)) & 0xFFu;
+                const uint32_t kmax = __reduce_max_sync(kFull, (uint32_t)__popc(m));
+                if (kmax) {
+                    const uint32_t r = gbase + (uint32_t)((excl >> (16 * g)) & 0xFFFFull);
+                    stage_selected(S.esc[es], r, m, exp4_of(w[g].x, w[g].y), exp4_of(w[g].z, w[g].w),
+                                   kmax);
+                }
+                gbase += (uint32_t)((total >> (16 * g)) & 0xFFFFull);
+            }
+            compute_sync();    // staging complete; s_warp free
+            if (t == 0) {
+                st_relaxed(a.state + ci * a.tpc + lt, (lt == 0 ? kFlagIncl : kFlagAgg) | agg);
+                s_sci[es] = ci;
+                s_slt[es] = lt;
+                s_sagg[es] = (uint32_t)agg;
+                __threadfence_block();
+                vefull[es] = eround + 1;
+            }
         }
-        gbase += (total >> (16 * g)) & 0xFFFFull;
+        if (t == 0) {
+            const uint32_t es = it % kSlots, eround = it / kSlots;
+            if (!wait_flag(&vedone[es], eround, a.abort)) atomicOr(a.dstatus, EZ_DSTAT_TIMEOUT);
+            s_sci[es] = kEndMark;
+            __threadfence_block();
+            vefull[es] = eround + 1;
+        }
+        return;
     }
 
-    if (lt == a.tpc - 1) {
-        const uint64_t n_esc = P + agg;
-        const uint64_t bytes = c3_bytes(n_c, n_esc);
-        if (t < 128) {
-            o[t] = (uint8_t)c3_header_byte(t, E0, n_c, n_esc, bytes, c, a.W);
-            if (n_c + t < rup(n_c, 128)) sm_sec[n_c + t] = 0;
+    // ---- chain warp
+    const int lane = t & 31;
+    for (uint32_t it = 0;; it++) {
+        const uint32_t s = it % kSlots, round = it / kSlots;
+        bool ok = true;
+        if (lane == 0) ok = wait_flag(&vefull[s], round + 1, a.abort);
+        ok = __shfl_sync(kFull, ok, 0);
+        __threadfence_block();
+        if (!ok) {
+            if (lane == 0) atomicOr(a.dstatus, EZ_DSTAT_TIMEOUT);
+            break;
+        }
+        const uint32_t ci = s_sci[s];
+        if (ci == kEndMark) break;
+        const uint32_t lt = s_slt[s], agg = s_sagg[s];
+        const uint32_t c = a.first + ci;
+        const uint64_t n_c = shard_values(a.n, a.L, c);
+        uint8_t* o = a.out + (uint64_t)ci * a.slot;
+        const uint64_t plane = rup(cdiv(n_c, 8), 128);
+        uint8_t* sm_sec = o + 128;
+        uint8_t* pl_sec = sm_sec + rup(n_c, 128);
+        uint8_t* esc_sec = pl_sec + 3 * plane;
+        unsigned long long P = 0;
+        if (lt != 0) {
+            bool stuck;
+            P = lookback(a.state, ci * a.tpc + lt, ci * a.tpc, &stuck, a.abort);
+            if (lane == 0) {
+                if (stuck) atomicOr(a.dstatus, EZ_DSTAT_TIMEOUT);
+                st_relaxed(a.state + ci * a.tpc + lt, kFlagIncl | ((P + agg) & kValMask));
+            }
+        }
+        for (uint32_t b = (uint32_t)lane; b < agg; b += 32) esc_sec[P + b] = S.esc[s][b];
+        if (lt == a.tpc - 1) {
+            const uint64_t n_esc = P + agg;
+            const uint64_t bytes = c3_bytes(n_c, n_esc);
             const uint64_t pb = cdiv(n_c, 8);
-            if (pb + t < plane) {
-                pl_sec[pb + t] = 0;
-                pl_sec[plane + pb + t] = 0;
-                pl_sec[2 * plane + pb + t] = 0;
+            for (int q = lane; q < 128; q += 32) {
+                o[q] = (uint8_t)c3_header_byte(q, E0, n_c, n_esc, bytes, c, a.W);
+                if (n_c + q < rup(n_c, 128)) sm_sec[n_c + q] = 0;
+                if (pb + q < plane) {
+                    pl_sec[pb + q] = 0;
+                    pl_sec[plane + pb + q] = 0;
+                    pl_sec[2 * plane + pb + q] = 0;
+                }
+                if (n_esc + q < rup(n_esc, 128)) esc_sec[n_esc + q] = 0;
             }
-            if (n_esc + t < rup(n_esc, 128)) esc_sec[n_esc + t] = 0;
+            if (lane == 0) a.sizes[ci] = bytes;
         }
-        if (t == 0) a.sizes[ci] = bytes;
+        __syncwarp();
+        if (lane == 0) {
+            __threadfence_block();
+            vedone[s] = round + 1;
+        }
     }
 }
 
@@ -201,15 +371,27 @@ __device__ __forceinline__ uint32_t rd_u32(const uint8_t* p)
     return (uint32_t)p[0] | (uint32_t)p[1] << 8 | (uint32_t)p[2] << 16 | (uint32_t)p[3] << 24;
 }
 
+// Exponent bytes of a group from its code bytes (1..7 -> E0+code-1); the
+// bytes of escapes are placeholders.
+__device__ __forceinline__ unsigned long long codes_to_exps(unsigned long long c8, uint32_t E0)
+{
+    if (E0 == 0) return ((c8 | 0x8080808080808080ull) - 0x0101010101010101ull) & 0x7F7F7F7F7F7F7F7Full;
+    return c8 + (unsigned long long)(E0 - 1) * 0x0101010101010101ull;
+}
+
 __global__ void __launch_bounds__(kThreads) k_code3_decode(C3Dec a)
 {
     __shared__ uint32_t s_tile, s_bad, s_E0;
     __shared__ unsigned long long s_nesc;
+    __shared__ unsigned long long s_spread[256];
     __shared__ unsigned long long s_warp[kThreads / 32];
     __shared__ unsigned long long s_prefix;
+    __shared__ __align__(16) uint32_t s_esc32[(kTile + 16) / 4];
+    uint8_t* s_esc = reinterpret_cast<uint8_t*>(s_esc32);
     const int t = threadIdx.x;
-    const uint32_t tile = next_tile(a.counter, &s_tile);
-    const uint32_t ci = tile / a.tpc, lt = tile - ci * a.tpc;
+    s_spread[t] = spread_bits((uint32_t)t);
+    const TilePos tp = tile_pos(next_tile(a.counter, &s_tile), a.count, a.tpc);
+    const uint32_t ci = tp.ci, lt = tp.lt;
     const uint32_t c = a.first + ci;
     const uint64_t n_c = shard_values(a.n, a.L, c);
     const uint64_t v0 = (uint64_t)lt * kTile;
@@ -252,16 +434,17 @@ __global__ void __launch_bounds__(kThreads) k_code3_decode(C3Dec a)
     const uint8_t* esc_sec = pl_sec + 3 * plane;
     const uint8_t* pl_t = pl_sec + v0 / 8;
     uint16_t* ot = a.out + (uint64_t)ci * a.L + v0;
+    const bool full = nv == (uint32_t)kTile;
 
     uint2 smv[kGroups];
-    uint32_t codes[kGroups];   // plane bytes p0 | p1 << 8 | p2 << 16
+    uint32_t pb[kGroups];    // plane bytes p0 | p1 << 8 | p2 << 16
 #pragma unroll
     for (int g = 0; g < kGroups; g++) {
         const uint32_t j = (uint32_t)(g * kThreads + t);
         const uint32_t v = 8u * j;
         smv[g] = make_uint2(0, 0);
-        codes[g] = 0;
-        if (v + 8 <= nv) {
+        pb[g] = 0;
+        if (full || v + 8 <= nv) {
             smv[g] = __ldg(reinterpret_cast<const uint2*>(sm_sec + v0 + v));
         } else if (v < nv) {
             uint32_t lo = 0, hi = 0;
@@ -272,61 +455,59 @@ __global__ void __launch_bounds__(kThreads) k_code3_decode(C3Dec a)
             }
             smv[g] = make_uint2(lo, hi);
         }
-        if (v < nv)
-            codes[g] = (uint32_t)__ldg(pl_t + j) | (uint32_t)__ldg(pl_t + plane + j) << 8 |
-                       (uint32_t)__ldg(pl_t + 2 * plane + j) << 16;
+        if (full || v < nv)
+            pb[g] = (uint32_t)__ldg(pl_t + j) | (uint32_t)__ldg(pl_t + plane + j) << 8 |
+                    (uint32_t)__ldg(pl_t + 2 * plane + j) << 16;
     }
-    uint32_t emask[kGroups];
+    uint32_t emasks = 0;
     unsigned long long packed = 0;
 #pragma unroll
     for (int g = 0; g < kGroups; g++) {
         const uint32_t v = 8u * (uint32_t)(g * kThreads + t);
-        const uint32_t vmask = v >= nv ? 0u : (nv - v >= 8 ? 0xFFu : ((1u << (nv - v)) - 1u));
-        const uint32_t any = (codes[g] | codes[g] >> 8 | codes[g] >> 16) & 0xFFu;
-        emask[g] = ~any & vmask;
-        packed |= (unsigned long long)__popc(emask[g]) << (16 * g);
+        const uint32_t vmask = full ? 0xFFu : (v >= nv ? 0u : (nv - v >= 8 ? 0xFFu : ((1u << (nv - v)) - 1u)));
+        const uint32_t esc = ~(pb[g] | pb[g] >> 8 | pb[g] >> 16) & vmask;
+        emasks |= esc << (8 * g);
+        packed |= (unsigned long long)__popc(esc) << (16 * g);
     }
     unsigned long long total;
     const unsigned long long excl = block_excl_scan(packed, s_warp, &total);
     const unsigned long long agg = (total & 0xFFFFull) + ((total >> 16) & 0xFFFFull) +
                                    ((total >> 32) & 0xFFFFull) + (total >> 48);
-    const unsigned long long P = tile_prefix(a.state, tile, ci * a.tpc, agg, &s_prefix, a.dstatus, a.abort);
-    if (lt == a.tpc - 1 && t == 0 && P + agg != n_esc) atomicOr(a.dstatus, EZ_DSTAT_BAD_COUNT);
+    const unsigned long long P = tile_prefix(a.state, tp.state, ci * a.tpc, agg, &s_prefix,
+                                             a.dstatus, a.abort);
+    // this tile's escapes, staged in shared memory (never read past n_esc)
+    const unsigned long long have = P >= n_esc ? 0ull : (n_esc - P < agg ? n_esc - P : agg);
+    for (uint32_t b = (uint32_t)t; b < (uint32_t)have; b += kThreads) s_esc[b] = esc_sec[P + b];
+    if (t == 0 && (have < agg || (lt == a.tpc - 1 && P + agg != n_esc)))
+        atomicOr(a.dstatus, EZ_DSTAT_BAD_COUNT);
+    __syncthreads();
 
-    unsigned long long gbase = 0;
-    bool overrun = false;
+    uint32_t gbase = 0;
 #pragma unroll
     for (int g = 0; g < kGroups; g++) {
         const uint32_t v = 8u * (uint32_t)(g * kThreads + t);
-        unsigned long long r = P + gbase + ((excl >> (16 * g)) & 0xFFFFull);
-        gbase += (total >> (16 * g)) & 0xFFFFull;
-        if (v >= nv) continue;
-        uint32_t h[8];
-#pragma unroll
-        for (int i = 0; i < 8; i++) {
-            const uint32_t cb = codes[g] >> i;
-            const uint32_t code = (cb & 1u) | ((cb >> 7) & 2u) | ((cb >> 14) & 4u);
-            uint32_t E;
-            if (code) {
-                E = E0 + code - 1;
-            } else if ((emask[g] >> i) & 1u) {
-                if (r < n_esc) E = esc_sec[r];
-                else { E = 0; overrun = true; }
-                r++;
-            } else {
-                E = 0;   // past the end of the chunk
-            }
-            const uint32_t sm = ((i < 4 ? smv[g].x >> (8 * i) : smv[g].y >> (8 * (i - 4)))) & 0xFFu;
-            h[i] = merge_of(sm, E);
+        const uint32_t r = gbase + (uint32_t)((excl >> (16 * g)) & 0xFFFFull);
+        gbase += (uint32_t)((total >> (16 * g)) & 0xFFFFull);
+        if (!full && v >= nv) continue;
+        const unsigned long long c8 = s_spread[pb[g] & 0xFFu] | (s_spread[(pb[g] >> 8) & 0xFFu] << 1) |
+                                      (s_spread[(pb[g] >> 16) & 0xFFu] << 2);
+        unsigned long long e8 = codes_to_exps(c8, E0);
+        const uint32_t m = (emasks >> (8 * g)) & 0xFFu;
+        if (m) {
+            uint32_t c_lo, c_hi;
+            load_unaligned8(s_esc32, r, c_lo, c_hi);
+            e8 = insert_selected(e8, m, c_lo, c_hi);
         }
-        if (v + 8 <= nv) {
-            st_v4(ot + v, make_uint4(h[0] | h[1] << 16, h[2] | h[3] << 16, h[4] | h[5] << 16,
-                                     h[6] | h[7] << 16));
+        uint4 o4;
+        merge4(smv[g].x, (uint32_t)e8, o4.x, o4.y);
+        merge4(smv[g].y, (uint32_t)(e8 >> 32), o4.z, o4.w);
+        if (full || v + 8 <= nv) {
+            st_v4(ot + v, o4);
         } else {
-            for (uint32_t i = 0; i < nv - v; i++) ot[v + i] = (uint16_t)h[i];
+            const uint32_t hw[4] = {o4.x, o4.y, o4.z, o4.w};
+            for (uint32_t i = 0; i < nv - v; i++) ot[v + i] = (uint16_t)(hw[i >> 1] >> (16 * (i & 1)));
         }
     }
-    if (overrun) atomicOr(a.dstatus, EZ_DSTAT_BAD_COUNT);
 }
 
 cudaError_t launch_code3_encode(const ez_plan_s* p, const uint16_t* x, uint32_t first,
@@ -344,12 +525,17 @@ cudaError_t launch_code3_encode(const ez_plan_s* p, const uint16_t* x, uint32_t 
     a.L = p->L;
     a.W = p->W;
     a.first = first;
+    a.count = count;
     a.tpc = p->tpc;
     a.state = w.state_a;
     a.counter = w.counters + 0;
     a.abort = w.counters + 7;
-    const uint64_t tiles = (uint64_t)count * p->tpc;
-    k_code3_encode<<<(unsigned)tiles, kThreads, 0, s>>>(a);
+    a.shard_ctr = w.shard_ctr;
+    static const cudaError_t attr = cudaFuncSetAttribute(
+        k_code3_encode, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(EncSmem));
+    if (attr != cudaSuccess) return attr;
+    k_code3_encode<<<persistent_grid(k_code3_encode, kEncThreads, sizeof(EncSmem)), kEncThreads,
+                     sizeof(EncSmem), s>>>(a);
     return cudaGetLastError();
 }
 
@@ -366,6 +552,7 @@ cudaError_t launch_code3_decode(const ez_plan_s* p, const uint8_t* in, const uin
     a.L = p->L;
     a.W = p->W;
     a.first = first;
+    a.count = count;
     a.tpc = p->tpc;
     a.state = w.state_a;
     a.counter = w.counters + 1;

@@ -26,6 +26,7 @@
 // BF16 values straight into the gathered full buffer.
 #include "ez_internal.h"
 #include "ez_stats.cuh"
+#include "ez_bytes.cuh"
 
 namespace ezk {
 using namespace ez;
@@ -38,7 +39,7 @@ struct RuEnc {
     uint64_t* sizes;
     uint32_t* dstatus;
     uint64_t n, L;
-    uint32_t W, B, log2B, first, tpc;
+    uint32_t W, B, log2B, first, count, tpc;
     int cold;
     unsigned long long* state;
     uint32_t* counter;
@@ -57,7 +58,7 @@ struct RuC3 {
     uint64_t* sizes;
     uint32_t* dstatus;
     uint64_t n, L;
-    uint32_t W, B, first, tpc;
+    uint32_t W, B, first, count, tpc;
     int cold;
     unsigned long long* state;
     uint32_t* counter;
@@ -75,7 +76,7 @@ struct RuDec {
     uint16_t* out;
     uint32_t* dstatus;
     uint64_t n, L;
-    uint32_t W, B, log2B, first, tpc;
+    uint32_t W, B, log2B, first, count, tpc;
     unsigned long long* state_a;
     unsigned long long* state_b;
     uint32_t* counter;
@@ -210,8 +211,12 @@ __global__ void __launch_bounds__(kThreads) k_reuse_encode(RuEnc a)
     __shared__ unsigned long long s_prefix;
     extern __shared__ __align__(16) unsigned char dyn[];
     const int t = threadIdx.x, lane = t & 31, wid = t >> 5;
-    const uint32_t tile = next_tile(a.counter, &s_tile);
-    const uint32_t ci = tile / a.tpc, lt = tile - ci * a.tpc;
+    if (t < 32) {
+        s_gl[t] = 0;
+        s_bm[t] = 0;
+    }
+    const TilePos tp = tile_pos(next_tile(a.counter, &s_tile), a.count, a.tpc);
+    const uint32_t ci = tp.ci, lt = tp.lt;
     const uint32_t r = a.first + ci;
     const uint64_t n_s = shard_values(a.n, a.L, r);
     const uint64_t v0 = (uint64_t)lt * kTile;
@@ -225,10 +230,6 @@ __global__ void __launch_bounds__(kThreads) k_reuse_encode(RuEnc a)
     uint8_t* o = a.out + (uint64_t)ci * a.slot;
     const uint32_t fin_tile = n_s ? (uint32_t)((n_s - 1) / kTile) : 0u;
 
-    if (t < 32) {
-        s_gl[t] = 0;
-        s_bm[t] = 0;
-    }
     uint4 w[kGroups];
     unsigned long long cv[kGroups];
 #pragma unroll
@@ -239,35 +240,40 @@ __global__ void __launch_bounds__(kThreads) k_reuse_encode(RuEnc a)
     }
 
     StatsSmem* S = reinterpret_cast<StatsSmem*>(dyn);
-    unsigned long long acc2 = 0;
-    if (kCoded) st_begin(*S, (8u * (uint32_t)t < nv) ? half_of(w[0], 0) : 0xFFFFFFFFu);
-    else __syncthreads();
+    if (kCoded) st_begin(*S, (8u * (uint32_t)t < nv) ? (w[0].x & 0xFFFFu) : 0xFFFFFFFFu);
 
     unsigned long long e8[kGroups];
 #pragma unroll
     for (int g = 0; g < kGroups; g++) {
         const uint32_t v = 8u * (uint32_t)(g * kThreads + t);
         const uint32_t vm = vmask_of(v, nv);
-        unsigned long long e = 0, smw = 0;
-#pragma unroll
-        for (int i = 0; i < 8; i++) {
-            const uint32_t h = half_of(w[g], i);
-            e |= (unsigned long long)exp_of(h) << (8 * i);
-            smw |= (unsigned long long)sm_of(h) << (8 * i);
-        }
-        const unsigned long long bmask = bytemask_of(vm);
-        e &= bmask;
+        const unsigned long long bmask = vm == 0xFFu ? ~0ull : bytemask_of(vm);
+        const unsigned long long e = ((unsigned long long)exp4_of(w[g].z, w[g].w) << 32 |
+                                      exp4_of(w[g].x, w[g].y)) & bmask;
         e8[g] = e;
         const bool ch = vm && (a.cold || ((e ^ cv[g]) & bmask) != 0ull);
         const uint32_t bal = __ballot_sync(kFull, ch);
         if (lane == 0) s_gl[g * (kThreads / 32) + wid] = bal;
-        if (vm) st_group8(o + off_sm + v0, v, nv, smw & bmask);
+        if (vm) {
+            const unsigned long long smw = (unsigned long long)sm4_of(w[g].z, w[g].w) << 32 |
+                                           sm4_of(w[g].x, w[g].y);
+            st_group8(o + off_sm + v0, v, nv, smw);
+        }
         if (kCoded && vm) {
             uint32_t* cell = &S->cells[wid][0][lane];
+            uint32_t* sq = &S->sq[wid][0][lane];
             const uint32_t elo = S->elo;
+            if (vm == 0xFFu) {
+                const uint32_t ws[4] = {w[g].x, w[g].y, w[g].z, w[g].w};
 #pragma unroll
-            for (int i = 0; i < 8; i++)
-                if ((vm >> i) & 1u) st_add(half_of(w[g], i), elo, cell, acc2, *S);
+                for (int q = 0; q < 4; q++) {
+                    st_add(ws[q] & 0xFFFFu, elo, cell, sq, *S);
+                    st_add(ws[q] >> 16, elo, cell, sq, *S);
+                }
+            } else {
+                for (int i = 0; i < 8; i++)
+                    if ((vm >> i) & 1u) st_add(half_of(w[g], i), elo, cell, sq, *S);
+            }
         }
     }
     __syncthreads();
@@ -277,7 +283,8 @@ __global__ void __launch_bounds__(kThreads) k_reuse_encode(RuEnc a)
     }
     __syncthreads();
     const unsigned long long agg = s_agg;
-    const unsigned long long P = tile_prefix(a.state, tile, ci * a.tpc, agg, &s_prefix, a.dstatus, a.abort);
+    const unsigned long long P = tile_prefix(a.state, tp.state, ci * a.tpc, agg, &s_prefix,
+                                             a.dstatus, a.abort);
 
     // bitmap bytes of this tile
     const uint32_t nbt = (uint32_t)kTile >> log2B;
@@ -285,7 +292,7 @@ __global__ void __launch_bounds__(kThreads) k_reuse_encode(RuEnc a)
     if ((uint32_t)t < nbt / 8 && bm0 + t < bm_bytes)
         o[64 + bm0 + t] = reinterpret_cast<const uint8_t*>(s_bm)[t];
 
-    // changed exponents into the payload (or the staging stream) and cache
+    // changed exponents into the payload (or the staging stream) and the cache
 #pragma unroll
     for (int g = 0; g < kGroups; g++) {
         const uint32_t v = 8u * (uint32_t)(g * kThreads + t);
@@ -299,9 +306,7 @@ __global__ void __launch_bounds__(kThreads) k_reuse_encode(RuEnc a)
     }
 
     if (kCoded) {
-        if (st_end(*S, acc2, a.bins + ci, a.tpc)) {
-            st_finalize(a.bins + ci, n_s, a.K, a.stats + ci);
-        }
+        if (st_end(*S, a.bins + ci, a.tpc)) st_finalize(a.bins + ci, n_s, a.K, a.stats + ci, *S);
     }
 
     if (lt == fin_tile) {
@@ -329,15 +334,43 @@ __global__ void __launch_bounds__(kThreads) k_reuse_encode(RuEnc a)
     }
 }
 
+// 3-bit code plane bits / escape flag per exponent value (see k_code3.cu)
+__device__ __forceinline__ uint32_t ru_lut_entry(uint32_t e, uint32_t E0)
+{
+    const uint32_t d = e - E0;
+    const uint32_t code = d < 7u ? d + 1u : 0u;
+    return (code & 1u) | ((code & 2u) << 7) | ((code & 4u) << 14) | (code ? 0u : (1u << 24));
+}
+__device__ __forceinline__ uint32_t lut_b(const uint32_t* lut, uint32_t byte_off)
+{
+    return *reinterpret_cast<const uint32_t*>(reinterpret_cast<const char*>(lut) + byte_off);
+}
+// plane bytes 0..2 and escape mask (byte 3) of 8 exponent bytes
+__device__ __forceinline__ uint32_t codes_of_bytes(const uint32_t* lut, uint32_t lo, uint32_t hi)
+{
+    uint32_t acc = 0;
+    acc += lut_b(lut, (lo << 2) & 0x3FCu);
+    acc += lut_b(lut, (lo >> 6) & 0x3FCu) << 1;
+    acc += lut_b(lut, (lo >> 14) & 0x3FCu) << 2;
+    acc += lut_b(lut, (lo >> 22) & 0x3FCu) << 3;
+    acc += lut_b(lut, (hi << 2) & 0x3FCu) << 4;
+    acc += lut_b(lut, (hi >> 6) & 0x3FCu) << 5;
+    acc += lut_b(lut, (hi >> 14) & 0x3FCu) << 6;
+    acc += lut_b(lut, (hi >> 22) & 0x3FCu) << 7;
+    return acc;
+}
+
 // Pass 2 of the coded variant: 3-bit code of the staged exponent stream.
 __global__ void __launch_bounds__(kThreads) k_reuse_code3(RuC3 a)
 {
     __shared__ uint32_t s_tile;
+    __shared__ uint32_t s_lut[256];
     __shared__ unsigned long long s_warp[kThreads / 32];
     __shared__ unsigned long long s_prefix;
+    __shared__ __align__(16) uint8_t s_esc[kTile + 16];
     const int t = threadIdx.x;
-    const uint32_t tile = next_tile(a.counter, &s_tile);
-    const uint32_t ci = tile / a.tpc, lt = tile - ci * a.tpc;
+    const TilePos tp = tile_pos(next_tile(a.counter, &s_tile), a.count, a.tpc);
+    const uint32_t ci = tp.ci, lt = tp.lt;
     const uint32_t r = a.first + ci;
     const uint64_t n_s = shard_values(a.n, a.L, r);
     const uint64_t m = a.info[ci].m;
@@ -349,6 +382,7 @@ __global__ void __launch_bounds__(kThreads) k_reuse_code3(RuC3 a)
         if (t == 0) atomicOr(a.dstatus, EZ_DSTAT_BAD_STATS);
         E0 = 0;
     }
+    s_lut[t] = ru_lut_entry((uint32_t)t, E0);
     const uint64_t off_exp = ru_off_exp(n_s, a.B);
     const uint64_t plane = rup(cdiv(m, 8), 16);
     uint8_t* o = a.out + (uint64_t)ci * a.slot;
@@ -358,55 +392,48 @@ __global__ void __launch_bounds__(kThreads) k_reuse_code3(RuC3 a)
     const uint32_t fin_tile = m ? (uint32_t)((m - 1) / kTile) : 0u;
 
     unsigned long long e8[kGroups];
-    uint32_t emask[kGroups];
+#pragma unroll
+    for (int g = 0; g < kGroups; g++) {
+        const uint32_t v = 8u * (uint32_t)(g * kThreads + t);
+        e8[g] = v < nv ? ld_group8(es, v, nv) : 0ull;
+    }
+    __syncthreads();   // lut
+    uint32_t emasks = 0;
     unsigned long long packed = 0;
 #pragma unroll
     for (int g = 0; g < kGroups; g++) {
         const uint32_t j = (uint32_t)(g * kThreads + t);
         const uint32_t v = 8u * j;
-        e8[g] = v < nv ? ld_group8(es, v, nv) : 0ull;
-    }
-#pragma unroll
-    for (int g = 0; g < kGroups; g++) {
-        const uint32_t j = (uint32_t)(g * kThreads + t);
-        const uint32_t v = 8u * j;
         const uint32_t vm = vmask_of(v, nv);
-        emask[g] = 0;
         if (!vm) continue;
-        uint32_t p0 = 0, p1 = 0, p2 = 0, esc = 0;
-#pragma unroll
-        for (int i = 0; i < 8; i++) {
-            const uint32_t d = (uint32_t)((e8[g] >> (8 * i)) & 0xFFu) - E0;
-            const uint32_t code = d < 7u ? d + 1u : 0u;
-            p0 |= (code & 1u) << i;
-            p1 |= ((code >> 1) & 1u) << i;
-            p2 |= (code >> 2) << i;
-            esc |= (code == 0u ? 1u : 0u) << i;
-        }
+        const uint32_t acc = codes_of_bytes(s_lut, (uint32_t)e8[g], (uint32_t)(e8[g] >> 32)) &
+                             (vm * 0x01010101u);
         const uint64_t pb = v0 / 8 + j;
-        pl[pb] = (uint8_t)(p0 & vm);
-        pl[plane + pb] = (uint8_t)(p1 & vm);
-        pl[2 * plane + pb] = (uint8_t)(p2 & vm);
-        emask[g] = esc & vm;
-        packed |= (unsigned long long)__popc(emask[g]) << (16 * g);
+        pl[pb] = (uint8_t)acc;
+        pl[plane + pb] = (uint8_t)(acc >> 8);
+        pl[2 * plane + pb] = (uint8_t)(acc >> 16);
+        const uint32_t esc = acc >> 24;
+        emasks |= esc << (8 * g);
+        packed |= (unsigned long long)__popc(esc) << (16 * g);
     }
     unsigned long long total;
     const unsigned long long excl = block_excl_scan(packed, s_warp, &total);
     const unsigned long long agg = (total & 0xFFFFull) + ((total >> 16) & 0xFFFFull) +
                                    ((total >> 32) & 0xFFFFull) + (total >> 48);
-    const unsigned long long P = tile_prefix(a.state, tile, ci * a.tpc, agg, &s_prefix, a.dstatus, a.abort);
-    unsigned long long gbase = 0;
+    uint32_t gbase = 0;
 #pragma unroll
     for (int g = 0; g < kGroups; g++) {
-        uint32_t mm = emask[g];
-        unsigned long long q = P + gbase + ((excl >> (16 * g)) & 0xFFFFull);
-        while (mm) {
-            const int i = __ffs(mm) - 1;
-            mm &= mm - 1;
-            esc_sec[q++] = (uint8_t)(e8[g] >> (8 * i));
+        const uint32_t mm = (emasks >> (8 * g)) & 0xFFu;
+        const uint32_t kmax = __reduce_max_sync(kFull, (uint32_t)__popc(mm));
+        if (kmax) {
+            const uint32_t q = gbase + (uint32_t)((excl >> (16 * g)) & 0xFFFFull);
+            stage_selected(s_esc, q, mm, (uint32_t)e8[g], (uint32_t)(e8[g] >> 32), kmax);
         }
-        gbase += (total >> (16 * g)) & 0xFFFFull;
+        gbase += (uint32_t)((total >> (16 * g)) & 0xFFFFull);
     }
+    const unsigned long long P = tile_prefix(a.state, tp.state, ci * a.tpc, agg, &s_prefix,
+                                             a.dstatus, a.abort);
+    for (uint32_t b = (uint32_t)t; b < (uint32_t)agg; b += kThreads) esc_sec[P + b] = s_esc[b];
     if (lt == fin_tile) {
         const uint64_t n_esc = P + agg;
         const uint64_t tot = ru_bytes(n_s, a.B, m, true, n_esc);
@@ -444,9 +471,14 @@ __global__ void __launch_bounds__(kThreads) k_reuse_decode(RuDec a)
     __shared__ uint32_t s_bm[32], s_pre[32], s_agg;
     __shared__ unsigned long long s_warp[kThreads / 32];
     __shared__ unsigned long long s_prefix;
+    __shared__ unsigned long long s_spread[kCoded ? 256 : 1];
+    __shared__ __align__(16) uint32_t s_esc32[kCoded ? (kTile + 16) / 4 : 4];
+    uint8_t* s_esc = reinterpret_cast<uint8_t*>(s_esc32);
     const int t = threadIdx.x;
-    const uint32_t tile = next_tile(a.counter, &s_tile);
-    const uint32_t ci = tile / a.tpc, lt = tile - ci * a.tpc;
+    if (kCoded) s_spread[t] = spread_bits((uint32_t)t);
+    if (t < 32) s_bm[t] = 0;
+    const TilePos tp = tile_pos(next_tile(a.counter, &s_tile), a.count, a.tpc);
+    const uint32_t ci = tp.ci, lt = tp.lt;
     const uint32_t r = a.first + ci;
     const uint64_t n_s = shard_values(a.n, a.L, r);
     const uint64_t v0 = (uint64_t)lt * kTile;
@@ -491,7 +523,6 @@ __global__ void __launch_bounds__(kThreads) k_reuse_decode(RuDec a)
         }
         s_bad = bad;
     }
-    if (t < 32) s_bm[t] = 0;
     __syncthreads();
     if (s_bad) {
         if (lt == fin_tile && t == 0) atomicOr(a.dstatus, s_bad);
@@ -541,7 +572,8 @@ __global__ void __launch_bounds__(kThreads) k_reuse_decode(RuDec a)
         smv[g] = v < nv ? ld_group8(sm_t, v, nv) : 0ull;
         ev[g] = (v < nv && !chg[g]) ? ld_group8(ct, v, nv) : 0ull;
     }
-    const unsigned long long P = tile_prefix(a.state_a, tile, ci * a.tpc, agg, &s_prefix, a.dstatus, a.abort);
+    const unsigned long long P = tile_prefix(a.state_a, tp.state, ci * a.tpc, agg, &s_prefix,
+                                             a.dstatus, a.abort);
     bool bad_count = false;
     if (lt == fin_tile && t == 0) {
         bool last_changed = false;
@@ -569,59 +601,60 @@ __global__ void __launch_bounds__(kThreads) k_reuse_decode(RuDec a)
         // planes of this tile's changed exponents, then the escape prefix
         const uint64_t plane = rup(cdiv(m, 8), 16);
         const uint8_t* esc_sec = ex + 3 * plane;
-        uint32_t codes[kGroups], emask[kGroups];
+        uint32_t pbs[kGroups];
+        uint32_t emasks = 0;
         unsigned long long packed = 0;
-        uint64_t pos[kGroups];
 #pragma unroll
         for (int g = 0; g < kGroups; g++) {
-            codes[g] = 0;
-            emask[g] = 0;
-            pos[g] = 0;
+            pbs[g] = 0;
             if (!chg[g]) continue;
             const uint32_t v = 8u * (uint32_t)(g * kThreads + t);
             const uint32_t k = v >> log2B;
-            pos[g] = (P + block_rank(s_bm, s_pre, k)) * B + (v - (k << log2B));
+            const uint64_t pos = (P + block_rank(s_bm, s_pre, k)) * B + (v - (k << log2B));
             const uint32_t cnt = min(8u, nv - v);
-            if (pos[g] + cnt > m) {
+            if (pos + cnt > m) {
                 bad_count = true;
-                chg[g] = false;     // treated as a bad block: value left as cache contents
+                chg[g] = false;     // a corrupt block: its values are left as cache contents
                 continue;
             }
-            const uint64_t pb = pos[g] >> 3;
-            codes[g] = (uint32_t)ex[pb] | (uint32_t)ex[plane + pb] << 8 | (uint32_t)ex[2 * plane + pb] << 16;
+            const uint64_t pb = pos >> 3;
+            pbs[g] = (uint32_t)ex[pb] | (uint32_t)ex[plane + pb] << 8 | (uint32_t)ex[2 * plane + pb] << 16;
             const uint32_t vm = cnt >= 8 ? 0xFFu : ((1u << cnt) - 1u);
-            emask[g] = ~(codes[g] | codes[g] >> 8 | codes[g] >> 16) & vm;
-            packed |= (unsigned long long)__popc(emask[g]) << (16 * g);
+            const uint32_t esc = ~(pbs[g] | pbs[g] >> 8 | pbs[g] >> 16) & vm;
+            emasks |= esc << (8 * g);
+            packed |= (unsigned long long)__popc(esc) << (16 * g);
         }
         unsigned long long total;
         const unsigned long long excl = block_excl_scan(packed, s_warp, &total);
         const unsigned long long agg2 = (total & 0xFFFFull) + ((total >> 16) & 0xFFFFull) +
                                         ((total >> 32) & 0xFFFFull) + (total >> 48);
         __syncthreads();   // s_prefix is reused
-        const unsigned long long Q = tile_prefix(a.state_b, tile, ci * a.tpc, agg2, &s_prefix, a.dstatus, a.abort);
-        if (lt == fin_tile && t == 0 && Q + agg2 != n_esc) bad_count = true;
-        unsigned long long gbase = 0;
+        const unsigned long long Q = tile_prefix(a.state_b, tp.state, ci * a.tpc, agg2, &s_prefix,
+                                                 a.dstatus, a.abort);
+        const unsigned long long have = Q >= n_esc ? 0ull : (n_esc - Q < agg2 ? n_esc - Q : agg2);
+        for (uint32_t b = (uint32_t)t; b < (uint32_t)have; b += kThreads) s_esc[b] = esc_sec[Q + b];
+        if (t == 0 && (have < agg2 || (lt == fin_tile && Q + agg2 != n_esc))) bad_count = true;
+        __syncthreads();
+        uint32_t gbase = 0;
 #pragma unroll
         for (int g = 0; g < kGroups; g++) {
-            unsigned long long q = Q + gbase + ((excl >> (16 * g)) & 0xFFFFull);
-            gbase += (total >> (16 * g)) & 0xFFFFull;
+            const uint32_t q = gbase + (uint32_t)((excl >> (16 * g)) & 0xFFFFull);
+            gbase += (uint32_t)((total >> (16 * g)) & 0xFFFFull);
             if (!chg[g]) continue;
-            unsigned long long e = 0;
-#pragma unroll
-            for (int i = 0; i < 8; i++) {
-                const uint32_t cb = codes[g] >> i;
-                const uint32_t code = (cb & 1u) | ((cb >> 7) & 2u) | ((cb >> 14) & 4u);
-                uint32_t E = 0;
-                if (code) {
-                    E = E0 + code - 1;
-                } else if ((emask[g] >> i) & 1u) {
-                    if (q < n_esc) E = esc_sec[q];
-                    else bad_count = true;
-                    q++;
-                }
-                e |= (unsigned long long)E << (8 * i);
+            const unsigned long long c8 = s_spread[pbs[g] & 0xFFu] |
+                                          (s_spread[(pbs[g] >> 8) & 0xFFu] << 1) |
+                                          (s_spread[(pbs[g] >> 16) & 0xFFu] << 2);
+            unsigned long long e = (E0 == 0)
+                ? ((c8 | 0x8080808080808080ull) - 0x0101010101010101ull) & 0x7F7F7F7F7F7F7F7Full
+                : c8 + (unsigned long long)(E0 - 1) * 0x0101010101010101ull;
+            const uint32_t mm = (emasks >> (8 * g)) & 0xFFu;
+            if (mm) {
+                uint32_t c_lo, c_hi;
+                load_unaligned8(s_esc32, q, c_lo, c_hi);
+                e = insert_selected(e, mm, c_lo, c_hi);
             }
-            ev[g] = e;
+            const uint32_t cnt = min(8u, nv - (8u * (uint32_t)(g * kThreads + t)));
+            ev[g] = cnt >= 8 ? e : (e & byte_mask((1u << cnt) - 1u));
         }
     }
 
@@ -630,15 +663,14 @@ __global__ void __launch_bounds__(kThreads) k_reuse_decode(RuDec a)
         const uint32_t v = 8u * (uint32_t)(g * kThreads + t);
         if (v >= nv) continue;
         if (chg[g]) st_group8(ct, v, nv, ev[g]);
-        uint32_t h[8];
-#pragma unroll
-        for (int i = 0; i < 8; i++)
-            h[i] = merge_of((uint32_t)(smv[g] >> (8 * i)) & 0xFFu, (uint32_t)(ev[g] >> (8 * i)) & 0xFFu);
+        uint4 o4;
+        merge4((uint32_t)smv[g], (uint32_t)ev[g], o4.x, o4.y);
+        merge4((uint32_t)(smv[g] >> 32), (uint32_t)(ev[g] >> 32), o4.z, o4.w);
         if (v + 8 <= nv) {
-            st_v4(ot + v, make_uint4(h[0] | h[1] << 16, h[2] | h[3] << 16, h[4] | h[5] << 16,
-                                     h[6] | h[7] << 16));
+            st_v4(ot + v, o4);
         } else {
-            for (uint32_t i = 0; i < nv - v; i++) ot[v + i] = (uint16_t)h[i];
+            const uint32_t hw[4] = {o4.x, o4.y, o4.z, o4.w};
+            for (uint32_t i = 0; i < nv - v; i++) ot[v + i] = (uint16_t)(hw[i >> 1] >> (16 * (i & 1)));
         }
     }
     if (bad_count) atomicOr(a.dstatus, EZ_DSTAT_BAD_COUNT);
@@ -670,6 +702,7 @@ cudaError_t launch_reuse_encode(const ez_plan_s* p, const uint16_t* x, uint32_t 
     a.B = p->B;
     a.log2B = ilog2(p->B);
     a.first = first;
+    a.count = count;
     a.tpc = p->tpc;
     a.cold = cold ? 1 : 0;
     a.state = w.state_a;
@@ -685,6 +718,9 @@ cudaError_t launch_reuse_encode(const ez_plan_s* p, const uint16_t* x, uint32_t 
         k_reuse_encode<false><<<tiles, kThreads, 0, s>>>(a);
         return cudaGetLastError();
     }
+    static const cudaError_t attr = cudaFuncSetAttribute(
+        k_reuse_encode<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(StatsSmem));
+    if (attr != cudaSuccess) return attr;
     k_reuse_encode<true><<<tiles, kThreads, sizeof(StatsSmem), s>>>(a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -698,6 +734,7 @@ cudaError_t launch_reuse_encode(const ez_plan_s* p, const uint16_t* x, uint32_t 
     b.W = p->W;
     b.B = p->B;
     b.first = first;
+    b.count = count;
     b.tpc = p->tpc;
     b.cold = a.cold;
     b.state = w.state_b;
@@ -728,6 +765,7 @@ cudaError_t launch_reuse_decode(const ez_plan_s* p, const uint8_t* in, const uin
     a.B = p->B;
     a.log2B = ilog2(p->B);
     a.first = first;
+    a.count = count;
     a.tpc = p->tpc;
     a.state_a = w.state_a;
     a.state_b = w.state_b;

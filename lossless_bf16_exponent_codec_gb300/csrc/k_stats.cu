@@ -11,7 +11,7 @@
 namespace ezk {
 using namespace ez;
 
-static_assert(sizeof(StatsBins) == 5 * 256 * 8 + 256, "StatsBins layout (api.cpp sizes it)");
+static_assert(sizeof(StatsBins) == 3 * 256 * 8 + 256, "StatsBins layout (api.cpp sizes it)");
 static_assert(sizeof(ShardInfo) == 64, "ShardInfo layout (api.cpp sizes it)");
 static_assert(sizeof(ez_stats_t) == 2120, "ez_stats_t layout");
 
@@ -21,16 +21,17 @@ constexpr uint32_t kStatsTile = kThreads * kStatsLoads * 8;   // 32768 values
 __global__ void __launch_bounds__(kThreads)
 k_stats(const uint16_t* __restrict__ x, uint64_t n, StatsBins* G, ez_stats_t* out, double K)
 {
-    __shared__ StatsSmem S;
+    extern __shared__ __align__(16) unsigned char dyn[];
+    StatsSmem& S = *reinterpret_cast<StatsSmem*>(dyn);
     const uint64_t base = (uint64_t)blockIdx.x * kStatsTile;
     const uint32_t nv = base < n ? (uint32_t)umin64(kStatsTile, n - base) : 0u;
     const uint16_t* xt = x + base;
     const int t = threadIdx.x;
     const int lane = t & 31;
     uint32_t* cell = &S.cells[t >> 5][0][lane];
+    uint32_t* sq = &S.sq[t >> 5][0][lane];
     st_begin(S, (uint32_t)(8 * t) < nv ? (uint32_t)xt[8 * t] : 0xFFFFFFFFu);
     const uint32_t elo = S.elo;
-    unsigned long long acc2 = 0;
 #pragma unroll 1
     for (int g0 = 0; g0 < kStatsLoads; g0 += 4) {
         uint4 w[4];
@@ -51,16 +52,19 @@ k_stats(const uint16_t* __restrict__ x, uint64_t n, StatsBins* G, ez_stats_t* ou
         for (int k = 0; k < 4; k++) {
             const uint32_t v = 8u * (uint32_t)((g0 + k) * kThreads + t);
             if (v + 8 <= nv) {
+                const uint32_t ws[4] = {w[k].x, w[k].y, w[k].z, w[k].w};
 #pragma unroll
-                for (int i = 0; i < 8; i++) st_add(half_of(w[k], i), elo, cell, acc2, S);
+                for (int q = 0; q < 4; q++) {
+                    st_add(ws[q] & 0xFFFFu, elo, cell, sq, S);
+                    st_add(ws[q] >> 16, elo, cell, sq, S);
+                }
             } else if (v < nv) {
                 for (int i = 0; i < 8; i++)
-                    if (v + i < nv) st_add(half_of(w[k], i), elo, cell, acc2, S);
+                    if (v + i < nv) st_add(half_of(w[k], i), elo, cell, sq, S);
             }
         }
     }
-    __syncwarp();
-    if (st_end(S, acc2, G, gridDim.x)) st_finalize(G, n, K, out);
+    if (st_end(S, G, gridDim.x)) st_finalize(G, n, K, out, S);
 }
 
 cudaError_t launch_stats(const ez_plan_s* p, const uint16_t* x, uint64_t n, ez_stats_t* out,
@@ -68,7 +72,10 @@ cudaError_t launch_stats(const ez_plan_s* p, const uint16_t* x, uint64_t n, ez_s
 {
     const uint64_t tiles = n ? cdiv(n, kStatsTile) : 1;
     if (tiles > 0x7fffffffull) return cudaErrorInvalidValue;
-    k_stats<<<(unsigned)tiles, kThreads, 0, s>>>(x, n, (StatsBins*)w.bins, out, p->K);
+    static const cudaError_t attr = cudaFuncSetAttribute(
+        k_stats, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(StatsSmem));
+    if (attr != cudaSuccess) return attr;
+    k_stats<<<(unsigned)tiles, kThreads, sizeof(StatsSmem), s>>>(x, n, (StatsBins*)w.bins, out, p->K);
     return cudaGetLastError();
 }
 
