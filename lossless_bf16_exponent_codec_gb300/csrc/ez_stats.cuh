@@ -8,16 +8,16 @@
 //   v = (-1)^s * M * 2^(E-134),  M = 128 + mantissa  (E >= 1)
 //
 // so s1 and s2 follow from per-exponent integer sums of +-M and M^2.  Per
-// value the hot loop is integer work on shared memory only.  A CTA picks a
-// 16-binade window [Elo, Elo+16) around the mode of a sample of its
-// exponents.  A value inside it adds 2^22 + M to the lane-private cell of
-// (sign, E) -- count in bits 22..31, sum of M in bits 0..21 -- and M^2 to the
-// lane-private square cell of E; lane-private cells never conflict.  Values
-// outside the window (and zeros, subnormals, Inf/NaN) go to per-exponent
-// bins with shared-memory atomics.  At the end of a tile the CTA folds
-// everything into per-shard global bins (64-bit atomics); the last CTA of the
-// shard turns the bins into one big integer per sum, rounds it to nearest
-// even, and derives var, sigma and the window base E0.
+// value the hot loop is one shared-memory atomic.  A CTA picks a 16-binade
+// window [Elo, Elo+16) around the mode of a sample of its exponents; a value
+// inside it increments the count of its (d = E - Elo, sign|mantissa byte)
+// cell of a 16 x 256 histogram.  Since a cell fixes sign and M, the cell
+// counts determine the window's exact per-exponent count, sum of +-M and
+// sum of M^2; they are folded once per tile.  Values outside the window
+// (and zeros, subnormals, Inf/NaN) go straight to per-exponent bins.  The
+// CTA then adds its bins to per-shard global bins (64-bit atomics); the last
+// CTA of the shard turns the bins into one big integer per sum, rounds it to
+// nearest even, and derives var, sigma and the window base E0.
 #pragma once
 
 #include "ez_common.cuh"
@@ -32,22 +32,20 @@ struct StatsBins {                 // per shard, in the workspace (zeroed per ca
     unsigned int pad[63];
 };
 
-// Per-CTA accumulators (dynamic shared memory).  A CTA adds at most 32768
-// values per tile (at most 128 per lane), so no cell or bin can overflow:
-// 1023 values per packed cell, 128 * 65025 < 2^32 per square cell, and
-// 32768 * 65025 < 2^32 per square bin.
+// Per-CTA accumulators (dynamic shared memory).  A CTA adds at most
+// kStatsMaxValues values before it flushes, so no cell or bin can overflow:
+// counts <= 2^23, |sum +-M| <= 2^23 * 255 < 2^31, and sums of M^2 are 64-bit.
+constexpr int kStatsWin = 16;                  // binades in a CTA's window
+constexpr uint32_t kStatsMaxValues = 1u << 23;
 struct StatsSmem {
-    uint32_t cells[kThreads / 32][32][32];   // [warp][sign*16 + d][lane]
-    uint32_t sq[kThreads / 32][16][32];      // [warp][d][lane]
+    uint32_t hist[kStatsWin * 256];            // [d][sign << 7 | mantissa]
+    unsigned long long s2[256];
     uint32_t cnt[256];
     int s1[256];
-    uint32_t s2[256];
     uint32_t sample[256];
     uint32_t elo;
     uint32_t last;
 };
-
-constexpr uint32_t kCellOne = 1u << 22;
 
 // Zero the CTA's accumulators and choose Elo from one exponent per thread
 // (h0 = that thread's first value, or 0xFFFFFFFF for none).
@@ -58,8 +56,8 @@ __device__ __forceinline__ void st_begin(StatsSmem& S, uint32_t h0)
     S.s1[t] = 0;
     S.s2[t] = 0;
     S.sample[t] = 0;
-    uint4* c = reinterpret_cast<uint4*>(&S.cells[0][0][0]);
-    constexpr int kVec = (int)((sizeof(S.cells) + sizeof(S.sq)) / 16);
+    uint4* c = reinterpret_cast<uint4*>(S.hist);
+    constexpr int kVec = (int)(sizeof(S.hist) / 16);
     for (int i = t; i < kVec; i += kThreads) c[i] = make_uint4(0, 0, 0, 0);
     __syncthreads();
     if (h0 != 0xFFFFFFFFu) atomicAdd(&S.sample[exp_of(h0)], 1u);
@@ -87,26 +85,48 @@ __device__ __forceinline__ void st_begin(StatsSmem& S, uint32_t h0)
     __syncthreads();
 }
 
-// One value h (16 bits).  `cell` = &S.cells[warp][0][lane], `sq` = &S.sq[warp][0][lane].
-__device__ __forceinline__ void st_add(uint32_t h, uint32_t elo, uint32_t* cell, uint32_t* sq,
-                                       StatsSmem& S)
+// A value outside the window: straight into the per-exponent bins.
+static __device__ __noinline__ void st_add_slow(uint32_t h, StatsSmem& S)
+{
+    const uint32_t E = exp_of(h);
+    atomicAdd(&S.cnt[E], 1u);
+    if (E != 255u) {
+        const uint32_t M = (E ? 128u : 0u) | (h & 0x7Fu);
+        atomicAdd(&S.s1[E], (h & 0x8000u) ? -(int)M : (int)M);
+        atomicAdd(&S.s2[E], (unsigned long long)(M * M));
+    }
+}
+
+// One value h (16 bits).
+__device__ __forceinline__ void st_add(uint32_t h, uint32_t elo, StatsSmem& S)
 {
     // v = sign*256 + E - Elo; in the window iff its low byte is below 16
     // (Elo <= 239 keeps E = 255 and E < Elo outside)
     const uint32_t v = (h >> 7) - elo;
     if ((v & 0xF0u) == 0) {
-        const uint32_t k = (v & 0xFu) | ((v >> 4) & 0x10u);     // sign*16 + d
-        const uint32_t m = h & 0x7Fu;
-        atomicAdd(cell + 32 * k, kCellOne | 0x80u | m);
-        atomicAdd(sq + 32 * (v & 0xFu), (m | 0x80u) * (m | 0x80u));
+        const uint32_t sm = (h & 0x7Fu) | ((h >> 8) & 0x80u);
+        atomicAdd(&S.hist[((v & 0xFu) << 8) | sm], 1u);
     } else {
-        const uint32_t E = exp_of(h);
-        atomicAdd(&S.cnt[E], 1u);
-        if (E != 255u) {
-            const uint32_t M = (E ? 128u : 0u) | (h & 0x7Fu);
-            atomicAdd(&S.s1[E], (h & 0x8000u) ? -(int)M : (int)M);
-            atomicAdd(&S.s2[E], M * M);
-        }
+        st_add_slow(h, S);
+    }
+}
+
+// The two values of a 32-bit word.  bias2 = (0x8000 - Elo) * 0x10001: each
+// 16-bit lane of w2 = 0x8000 + (sign*256 + E) - Elo, so its low byte is
+// E - Elo for a value in the window and no lane borrows from the other.
+__device__ __forceinline__ uint32_t st_bias2(uint32_t elo) { return (0x8000u - elo) * 0x10001u; }
+
+__device__ __forceinline__ void st_add2(uint32_t x, uint32_t bias2, uint32_t elo, StatsSmem& S)
+{
+    const uint32_t w2 = ((x >> 7) & 0x01FF01FFu) + bias2;
+    if ((w2 & 0x00F000F0u) == 0) {
+        const uint32_t i0 = ((w2 & 0xFu) << 8) | (x & 0x7Fu) | ((x >> 8) & 0x80u);
+        const uint32_t i1 = ((w2 >> 8) & 0xF00u) | ((x >> 16) & 0x7Fu) | (x >> 24 & 0x80u);
+        atomicAdd(&S.hist[i0], 1u);
+        atomicAdd(&S.hist[i1], 1u);
+    } else {
+        st_add(x & 0xFFFFu, elo, S);
+        st_add(x >> 16, elo, S);
     }
 }
 
@@ -114,31 +134,45 @@ __device__ __forceinline__ void st_add(uint32_t h, uint32_t elo, uint32_t* cell,
 // that is the `expected`-th to finish (it must then call st_finalize).
 __device__ __forceinline__ bool st_end(StatsSmem& S, StatsBins* G, uint32_t expected)
 {
-    const int t = threadIdx.x, lane = t & 31, wid = t >> 5;
+    const int t = threadIdx.x;
     const uint32_t elo = S.elo;
     __syncthreads();
-    // lane-private cells -> per-exponent CTA bins
-#pragma unroll 4
-    for (int d = 0; d < 16; d++) {
-        const uint32_t cp = S.cells[wid][d][lane];
-        const uint32_t cn = S.cells[wid][16 + d][lane];
-        const uint32_t q = S.sq[wid][d][lane];
-        const uint32_t cnt = (cp >> 22) + (cn >> 22);
-        const int s1 = (int)(cp & 0x3FFFFFu) - (int)(cn & 0x3FFFFFu);
-        const uint32_t wc = __reduce_add_sync(kFull, cnt);
-        const int ws = __reduce_add_sync(kFull, s1);
-        const uint32_t wq = __reduce_add_sync(kFull, q);
-        if (lane == 0 && wc) {
-            atomicAdd(&S.cnt[elo + d], wc);
-            atomicAdd(&S.s1[elo + d], ws);
-            atomicAdd(&S.s2[elo + d], wq);
+    // histogram row d (16 threads per row, 16 cells each; one sign per thread)
+    {
+        const uint32_t d = (uint32_t)t >> 4, part = (uint32_t)t & 15u;
+        const uint4* row = reinterpret_cast<const uint4*>(&S.hist[(d << 8) | (part << 4)]);
+        uint32_t c = 0, s1 = 0;
+        unsigned long long s2 = 0;
+        uint32_t M = 128u + ((part & 7u) << 4);
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+            const uint4 x = row[q];
+            const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+            for (int i = 0; i < 4; i++, M++) {
+                c += xs[i];
+                s1 += xs[i] * M;
+                s2 += (unsigned long long)xs[i] * (M * M);
+            }
+        }
+#pragma unroll
+        for (int o = 1; o < 8; o <<= 1) {
+            c += __shfl_xor_sync(kFull, c, o);
+            s1 += __shfl_xor_sync(kFull, s1, o);
+            s2 += __shfl_xor_sync(kFull, s2, o);
+        }
+        if ((part & 7u) == 0 && c) {
+            const uint32_t E = elo + d;
+            atomicAdd(&S.cnt[E], c);
+            atomicAdd(&S.s1[E], (part & 8u) ? -(int)s1 : (int)s1);
+            atomicAdd(&S.s2[E], s2);
         }
     }
     __syncthreads();
     // per-exponent bins -> global
     if (S.cnt[t]) atomicAdd(&G->hist[t], (unsigned long long)S.cnt[t]);
     if (S.s1[t]) atomicAdd(&G->s1[t], (unsigned long long)(long long)S.s1[t]);
-    if (S.s2[t]) atomicAdd(&G->s2[t], (unsigned long long)S.s2[t]);
+    if (S.s2[t]) atomicAdd(&G->s2[t], S.s2[t]);
     __threadfence();
     __syncthreads();
     if (t == 0) S.last = (atomicAdd(&G->done, 1u) == expected - 1) ? 1u : 0u;
@@ -153,24 +187,6 @@ __device__ __forceinline__ bool st_end(StatsSmem& S, StatsBins* G, uint32_t expe
 struct Big {
     uint32_t w[24];   // 768-bit non-negative integer, little-endian limbs
 };
-
-__device__ __forceinline__ void big_add_at(Big& b, unsigned long long x, int limb)
-{
-    unsigned long long c = x;
-    for (int i = limb; i < 24 && c; i++) {
-        const unsigned long long s = (unsigned long long)b.w[i] + (c & 0xffffffffull);
-        b.w[i] = (uint32_t)s;
-        c = (c >> 32) + (s >> 32);
-    }
-}
-
-// b += v * 2^sh
-__device__ __forceinline__ void big_add_shl(Big& b, unsigned long long v, int sh)
-{
-    const int limb = sh >> 5, bit = sh & 31;
-    big_add_at(b, (v & 0xffffffffull) << bit, limb);
-    big_add_at(b, (v >> 32) << bit, limb + 1);
-}
 
 __device__ __forceinline__ int big_cmp(const Big& a, const Big& b)
 {
@@ -237,40 +253,70 @@ __device__ __forceinline__ uint32_t window_base(double var, double K)
     return (uint32_t)lo;
 }
 
-// The last CTA finalises: all its threads load the bins into shared memory
-// (reusing the cell area), thread 0 does the exact arithmetic from there.
+// The last CTA finalises.  Every thread takes one exponent bin and adds its
+// terms, split into 32-bit pieces, to per-limb 64-bit accumulators of the
+// three big sums (positive and negative parts of s1, and s2) with
+// shared-memory atomics; one thread then propagates the carries and does the
+// rounding.  A limb accumulator receives at most 3 * 255 pieces < 2^42.
+constexpr int kLimbs = 24;
 struct FinSmem {
     unsigned long long h[256];
-    unsigned long long s1[256];
-    unsigned long long s2[256];
+    unsigned long long acc[3][kLimbs + 2];     // P, Q, R
+    unsigned long long n_fin;
 };
-static_assert(sizeof(FinSmem) <= sizeof(StatsSmem::cells), "finalise scratch fits the cells");
+static_assert(sizeof(FinSmem) <= sizeof(StatsSmem::hist), "finalise scratch fits the histogram");
 
-static __device__ void st_finalize(const StatsBins* G, uint64_t n, double K, ez_stats_t* out,
+// acc += v * 2^sh, as three 32-bit pieces
+__device__ __forceinline__ void acc_add_shl(unsigned long long* acc, unsigned long long v, int sh)
+{
+    const int limb = sh >> 5, bit = sh & 31;
+    const uint32_t p0 = (uint32_t)(v << bit);
+    const uint32_t p1 = (uint32_t)(bit ? (v >> (32 - bit)) : (v >> 32));
+    const uint32_t p2 = (uint32_t)(bit ? (v >> (64 - bit)) : 0ull);
+    if (p0) atomicAdd(&acc[limb], (unsigned long long)p0);
+    if (p1) atomicAdd(&acc[limb + 1], (unsigned long long)p1);
+    if (p2) atomicAdd(&acc[limb + 2], (unsigned long long)p2);
+}
+
+__device__ __forceinline__ void acc_to_big(const unsigned long long* acc, Big& b)
+{
+    unsigned long long carry = 0;
+    for (int i = 0; i < kLimbs; i++) {
+        const unsigned long long x = acc[i] + carry;
+        b.w[i] = (uint32_t)x;
+        carry = x >> 32;
+    }
+}
+
+static __device__ __noinline__ void st_finalize(const StatsBins* G, uint64_t n, double K, ez_stats_t* out,
                                    StatsSmem& S)
 {
     const int t = threadIdx.x;
-    FinSmem& F = *reinterpret_cast<FinSmem*>(&S.cells[0][0][0]);
+    FinSmem& F = *reinterpret_cast<FinSmem*>(S.hist);
     __syncthreads();
+    unsigned long long* accz = &F.acc[0][0];
+    for (int i = t; i < 3 * (kLimbs + 2); i += kThreads) accz[i] = 0;
+    if (t == 0) F.n_fin = 0;
     const unsigned long long h = __ldcg(&G->hist[t]);
+    const long long s1 = (long long)__ldcg(&G->s1[t]);
+    const unsigned long long s2 = __ldcg(&G->s2[t]);
     F.h[t] = h;
-    F.s1[t] = __ldcg(&G->s1[t]);
-    F.s2[t] = __ldcg(&G->s2[t]);
     out->hist[t] = h;
+    __syncthreads();
+    if (t < 255 && h) {
+        const int sh = (t ? t : 1) - 1;     // v * 2^133 = +-M * 2^sh
+        if (s1 > 0) acc_add_shl(F.acc[0], (unsigned long long)s1, sh);
+        else if (s1 < 0) acc_add_shl(F.acc[1], (unsigned long long)(-s1), sh);
+        if (s2) acc_add_shl(F.acc[2], s2, 2 * sh);   // v^2 * 2^266 = M^2 * 2^(2 sh)
+        atomicAdd(&F.n_fin, h);
+    }
     __syncthreads();
     if (t != 0) return;
     Big P, Q, R;
-    for (int i = 0; i < 24; i++) { P.w[i] = 0; Q.w[i] = 0; R.w[i] = 0; }
-    unsigned long long n_fin = 0;
-    for (int E = 0; E < 255; E++) {
-        n_fin += F.h[E];
-        if (!F.h[E]) continue;
-        const int sh = (E ? E : 1) - 1;     // v * 2^133 = +-M * 2^sh
-        const long long s1 = (long long)F.s1[E];
-        if (s1 > 0) big_add_shl(P, (unsigned long long)s1, sh);
-        else if (s1 < 0) big_add_shl(Q, (unsigned long long)(-s1), sh);
-        if (F.s2[E]) big_add_shl(R, F.s2[E], 2 * sh);   // v^2 * 2^266 = M^2 * 2^(2 sh)
-    }
+    acc_to_big(F.acc[0], P);
+    acc_to_big(F.acc[1], Q);
+    acc_to_big(F.acc[2], R);
+    const unsigned long long n_fin = F.n_fin;
     double s1d;
     if (big_cmp(P, Q) >= 0) {
         big_sub(P, Q);

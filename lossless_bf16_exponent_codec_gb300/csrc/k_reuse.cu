@@ -203,7 +203,7 @@ __device__ __forceinline__ uint32_t block_rank(const uint32_t* s_bm, const uint3
 }
 
 template <bool kCoded>
-__global__ void __launch_bounds__(kThreads) k_reuse_encode(RuEnc a)
+__global__ void __launch_bounds__(kThreads, 4) k_reuse_encode(RuEnc a)
 {
     __shared__ uint32_t s_tile;
     __shared__ uint32_t s_gl[32], s_bm[32], s_pre[32];
@@ -260,19 +260,14 @@ __global__ void __launch_bounds__(kThreads) k_reuse_encode(RuEnc a)
             st_group8(o + off_sm + v0, v, nv, smw);
         }
         if (kCoded && vm) {
-            uint32_t* cell = &S->cells[wid][0][lane];
-            uint32_t* sq = &S->sq[wid][0][lane];
             const uint32_t elo = S->elo;
             if (vm == 0xFFu) {
                 const uint32_t ws[4] = {w[g].x, w[g].y, w[g].z, w[g].w};
 #pragma unroll
-                for (int q = 0; q < 4; q++) {
-                    st_add(ws[q] & 0xFFFFu, elo, cell, sq, *S);
-                    st_add(ws[q] >> 16, elo, cell, sq, *S);
-                }
+                for (int q = 0; q < 4; q++) st_add2(ws[q], st_bias2(elo), elo, *S);
             } else {
                 for (int i = 0; i < 8; i++)
-                    if ((vm >> i) & 1u) st_add(half_of(w[g], i), elo, cell, sq, *S);
+                    if ((vm >> i) & 1u) st_add(half_of(w[g], i), elo, *S);
             }
         }
     }

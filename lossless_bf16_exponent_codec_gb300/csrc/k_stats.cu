@@ -1,10 +1,9 @@
 // k_stats.cu -- a1: statistics and window of one BF16 tensor (ZipCCL digest
 // 3.1, "one call of torch.std gives sigma, and the code table follows").
 //
-// One CTA reads a tile of 32768 values with 16-byte loads (4 loads in flight
-// per thread), adds each value into the exact accumulators of ez_stats.cuh,
-// and folds them into the global bins; the last CTA to finish computes s1,
-// s2, var, sigma and E0 and writes the ez_stats_t record.
+// Each CTA adds a tile of values into the exact accumulators of
+// ez_stats.cuh and folds them into the global bins; the last CTA to finish
+// computes s1, s2, var, sigma and E0 and writes the ez_stats_t record.
 #include "ez_internal.h"
 #include "ez_stats.cuh"
 
@@ -18,7 +17,10 @@ static_assert(sizeof(ez_stats_t) == 2120, "ez_stats_t layout");
 constexpr int kStatsLoads = 16;                             // 16-B loads per thread
 constexpr uint32_t kStatsTile = kThreads * kStatsLoads * 8;   // 32768 values
 
-__global__ void __launch_bounds__(kThreads)
+// One CTA per tile of 32768 values, 6 resident CTAs per SM; every thread
+// keeps four 16-byte loads in flight and adds their 32 values to the CTA's
+// histogram.
+__global__ void __launch_bounds__(kThreads, 6)
 k_stats(const uint16_t* __restrict__ x, uint64_t n, StatsBins* G, ez_stats_t* out, double K)
 {
     extern __shared__ __align__(16) unsigned char dyn[];
@@ -27,9 +29,6 @@ k_stats(const uint16_t* __restrict__ x, uint64_t n, StatsBins* G, ez_stats_t* ou
     const uint32_t nv = base < n ? (uint32_t)umin64(kStatsTile, n - base) : 0u;
     const uint16_t* xt = x + base;
     const int t = threadIdx.x;
-    const int lane = t & 31;
-    uint32_t* cell = &S.cells[t >> 5][0][lane];
-    uint32_t* sq = &S.sq[t >> 5][0][lane];
     st_begin(S, (uint32_t)(8 * t) < nv ? (uint32_t)xt[8 * t] : 0xFFFFFFFFu);
     const uint32_t elo = S.elo;
 #pragma unroll 1
@@ -55,12 +54,12 @@ k_stats(const uint16_t* __restrict__ x, uint64_t n, StatsBins* G, ez_stats_t* ou
                 const uint32_t ws[4] = {w[k].x, w[k].y, w[k].z, w[k].w};
 #pragma unroll
                 for (int q = 0; q < 4; q++) {
-                    st_add(ws[q] & 0xFFFFu, elo, cell, sq, S);
-                    st_add(ws[q] >> 16, elo, cell, sq, S);
+                    st_add(ws[q] & 0xFFFFu, elo, S);
+                    st_add(ws[q] >> 16, elo, S);
                 }
             } else if (v < nv) {
                 for (int i = 0; i < 8; i++)
-                    if (v + i < nv) st_add(half_of(w[k], i), elo, cell, sq, S);
+                    if (v + i < nv) st_add(half_of(w[k], i), elo, S);
             }
         }
     }
@@ -75,7 +74,8 @@ cudaError_t launch_stats(const ez_plan_s* p, const uint16_t* x, uint64_t n, ez_s
     static const cudaError_t attr = cudaFuncSetAttribute(
         k_stats, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(StatsSmem));
     if (attr != cudaSuccess) return attr;
-    k_stats<<<(unsigned)tiles, kThreads, sizeof(StatsSmem), s>>>(x, n, (StatsBins*)w.bins, out, p->K);
+    k_stats<<<(unsigned)tiles, kThreads, sizeof(StatsSmem), s>>>(x, n, (StatsBins*)w.bins, out,
+                                                               p->K);
     return cudaGetLastError();
 }
 
