@@ -44,19 +44,25 @@
  * the cache and send the next iteration cold.
  *
  * Byte formats (little-endian; all padding bytes are zero):
- *  code3 chunk: 128-B header {"EZC3", u8 version 1, u8 E0, u16 0, u64 n_c,
+ *  code3 chunk: 128-B header {"EZC3", u8 version 2, u8 E0, u16 0, u64 n_c,
  *    u64 n_esc, u64 chunk_bytes, u32 chunk index, u32 W, zeros}; SM bytes
  *    (n_c, padded to 128); planes P0,P1,P2 (ceil(n_c/8) bytes each, padded
  *    to 128; bit p of code j is bit (j&7) of byte (j>>3) of plane p);
- *    escapes (n_esc raw exponents in value order, padded to 128).
+ *    escape index (u64 per 8192 values: escapes among the values before
+ *    that point; ceil(n_c/8192) entries, padded to 128); escapes (n_esc raw
+ *    exponents in value order, padded to 128).
  *    code = E-E0+1 for E0 <= E <= E0+6, else 0.
- *  reuse payload: 64-B header {"EZRU", u8 version 1, u8 flags (bit0 coded,
+ *  reuse payload: 64-B header {"EZRU", u8 version 2, u8 flags (bit0 coded,
  *    bit1 cold), u8 E0, u8 0, u32 B, u32 shard, u64 n_s, u64 n_changed,
  *    u64 m, u64 n_esc, u64 total_bytes, u64 0}; bitmap (ceil(nb/8) bytes,
  *    block k = bit (k&7) of byte (k>>3), padded to 16); SM bytes (n_s,
- *    padded to 16); EXP = the m exponents of the changed blocks in block
- *    order, or (coded) their 3 code planes (ceil(m/8) bytes each, padded to
- *    16) followed by n_esc escapes; total padded to 128.
+ *    padded to 16); index (per 8192 values: u64 changed blocks before that
+ *    point and, coded, u64 escapes among their exponents; padded to 16);
+ *    EXP = the m exponents of the changed blocks in block order, or (coded)
+ *    their 3 code planes (ceil(m/8) bytes each, padded to 16) followed by
+ *    n_esc escapes; total padded to 128.
+ *  The indices let a decoder place every 8192-value span independently;
+ *  decoders check each entry against the span's own counts.
  */
 #ifndef EXPZIP_H
 #define EXPZIP_H

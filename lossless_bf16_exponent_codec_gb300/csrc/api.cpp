@@ -81,11 +81,13 @@ ez_status ez_plan_create(ez_plan* out, const ez_plan_desc* d)
     const uint64_t tpc = p->L ? cdiv(p->L, kTileValues) : 1;
     p->tpc = (uint32_t)tpc;
     const uint64_t L = p->L;
+    const uint64_t spans = cdiv(L, kTileValues);   // index entries per shard
     if (!reuse) {
-        p->slot_bytes = 128 + L + 3 * rup(cdiv(L, 8), 128) + L;
+        p->slot_bytes = 128 + L + 3 * rup(cdiv(L, 8), 128) + rup(8 * spans, 128) + L;
     } else {
         const uint64_t nb = cdiv(L, p->B);
-        const uint64_t head = 64 + rup(cdiv(nb, 8), 16) + rup(L, 16);
+        const uint64_t idx = rup((d->codec == EZ_CODEC_REUSE_CODE3 ? 16 : 8) * spans, 16);
+        const uint64_t head = 64 + rup(cdiv(nb, 8), 16) + rup(L, 16) + idx;
         const uint64_t exp = (d->codec == EZ_CODEC_REUSE_CODE3) ? 3 * rup(cdiv(L, 8), 16) + L : L;
         p->slot_bytes = rup(head + exp, 128);
     }
@@ -177,8 +179,6 @@ ez_status ez_decode_code3(ez_plan p, const uint8_t* d_in, const uint64_t* d_offs
     ez_status s = check_ws(p, d_ws, ws_bytes);
     if (s != EZ_OK) return s;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    s = clear_ws(d_ws, p->off_state_a + (uint64_t)count * p->tpc * 8, st);
-    if (s != EZ_OK) return s;
     return cuda_status(ezk::launch_code3_decode(p, d_in, d_offsets, first, count, d_out, d_status,
                                                 ezk::ws_view(p, d_ws), st));
 }
@@ -219,8 +219,6 @@ ez_status ez_decode_reuse(ez_plan p, const uint8_t* d_payload, uint64_t payload_
     ez_status s = check_ws(p, d_ws, ws_bytes);
     if (s != EZ_OK) return s;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    s = clear_ws(d_ws, p->off_state_b + (uint64_t)p->tpc * 8, st);
-    if (s != EZ_OK) return s;
     return cuda_status(ezk::launch_reuse_decode(p, d_payload, nullptr, payload_bytes, shard, 1,
                                                 d_recv_cache, d_out, d_status,
                                                 ezk::ws_view(p, d_ws), st));
@@ -240,14 +238,9 @@ ez_status ez_gather_decode(ez_plan p, const uint8_t* d_recv, const uint64_t* d_o
     if (s != EZ_OK) return s;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const ezk::WsView w = ezk::ws_view(p, d_ws);
-    if (!is_reuse(p)) {
-        s = clear_ws(d_ws, p->off_state_a + (uint64_t)p->W * p->tpc * 8, st);
-        if (s != EZ_OK) return s;
+    if (!is_reuse(p))
         return cuda_status(
             ezk::launch_code3_decode(p, d_recv, d_offsets, 0, p->W, d_full_out, d_status, w, st));
-    }
-    s = clear_ws(d_ws, p->off_state_b + (uint64_t)p->W * p->tpc * 8, st);
-    if (s != EZ_OK) return s;
     return cuda_status(ezk::launch_reuse_decode(p, d_recv, d_offsets, 0, 0, p->W, d_recv_cache,
                                                 d_full_out, d_status, w, st));
 }
@@ -266,6 +259,6 @@ const char* ez_status_str(ez_status s)
     return "unknown status";
 }
 
-uint32_t ez_version(void) { return 0x000100u; }
+uint32_t ez_version(void) { return 0x000200u; }
 
 }  // extern "C"

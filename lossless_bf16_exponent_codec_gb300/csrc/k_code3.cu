@@ -48,10 +48,16 @@ struct C3Dec {
     uint32_t* abort;
 };
 
+// Escape index: one u64 per kTile (8192) values of the chunk, the number of
+// escapes among the values before it.
+__device__ __forceinline__ uint64_t c3_idx_bytes(uint64_t n_c) { return rup(8 * cdiv(n_c, kTile), 128); }
+
 __device__ __forceinline__ uint64_t c3_bytes(uint64_t n_c, uint64_t n_esc)
 {
-    return 128 + rup(n_c, 128) + 3 * rup(cdiv(n_c, 8), 128) + rup(n_esc, 128);
+    return 128 + rup(n_c, 128) + 3 * rup(cdiv(n_c, 8), 128) + c3_idx_bytes(n_c) + rup(n_esc, 128);
 }
+
+__device__ __forceinline__ uint64_t v0_of(uint32_t lt) { return (uint64_t)lt * kTile; }
 
 __device__ __forceinline__ uint32_t le_byte(uint64_t v, int k) { return (uint32_t)(v >> (8 * k)) & 0xFFu; }
 
@@ -63,7 +69,7 @@ __device__ __forceinline__ uint32_t c3_header_byte(int b, uint32_t E0, uint64_t 
         case 1: return 'Z';
         case 2: return 'C';
         case 3: return '3';
-        case 4: return 1;
+        case 4: return 2;
         case 5: return E0;
         default: break;
     }
@@ -324,7 +330,8 @@ __global__ void __launch_bounds__(kEncThreads, 2) k_code3_encode(C3Enc a)
         const uint64_t plane = rup(cdiv(n_c, 8), 128);
         uint8_t* sm_sec = o + 128;
         uint8_t* pl_sec = sm_sec + rup(n_c, 128);
-        uint8_t* esc_sec = pl_sec + 3 * plane;
+        uint8_t* idx_sec = pl_sec + 3 * plane;
+        uint8_t* esc_sec = idx_sec + c3_idx_bytes(n_c);
         unsigned long long P = 0;
         if (lt != 0) {
             bool stuck;
@@ -334,11 +341,14 @@ __global__ void __launch_bounds__(kEncThreads, 2) k_code3_encode(C3Enc a)
                 st_relaxed(a.state + ci * a.tpc + lt, kFlagIncl | ((P + agg) & kValMask));
             }
         }
+        if (lane == 0 && v0_of(lt) < n_c)
+            *reinterpret_cast<unsigned long long*>(idx_sec + 8ull * lt) = P;
         for (uint32_t b = (uint32_t)lane; b < agg; b += 32) esc_sec[P + b] = S.esc[s][b];
         if (lt == a.tpc - 1) {
             const uint64_t n_esc = P + agg;
             const uint64_t bytes = c3_bytes(n_c, n_esc);
             const uint64_t pb = cdiv(n_c, 8);
+            const uint64_t ib = 8 * cdiv(n_c, kTile);
             for (int q = lane; q < 128; q += 32) {
                 o[q] = (uint8_t)c3_header_byte(q, E0, n_c, n_esc, bytes, c, a.W);
                 if (n_c + q < rup(n_c, 128)) sm_sec[n_c + q] = 0;
@@ -347,6 +357,7 @@ __global__ void __launch_bounds__(kEncThreads, 2) k_code3_encode(C3Enc a)
                     pl_sec[plane + pb + q] = 0;
                     pl_sec[2 * plane + pb + q] = 0;
                 }
+                if (ib + q < c3_idx_bytes(n_c)) idx_sec[ib + q] = 0;
                 if (n_esc + q < rup(n_esc, 128)) esc_sec[n_esc + q] = 0;
             }
             if (lane == 0) a.sizes[ci] = bytes;
@@ -359,18 +370,6 @@ __global__ void __launch_bounds__(kEncThreads, 2) k_code3_encode(C3Enc a)
     }
 }
 
-__device__ __forceinline__ uint64_t rd_u64(const uint8_t* p)
-{
-    uint64_t v = 0;
-#pragma unroll
-    for (int k = 7; k >= 0; k--) v = (v << 8) | p[k];
-    return v;
-}
-__device__ __forceinline__ uint32_t rd_u32(const uint8_t* p)
-{
-    return (uint32_t)p[0] | (uint32_t)p[1] << 8 | (uint32_t)p[2] << 16 | (uint32_t)p[3] << 24;
-}
-
 // Exponent bytes of a group from its code bytes (1..7 -> E0+code-1); the
 // bytes of escapes are placeholders.
 __device__ __forceinline__ unsigned long long codes_to_exps(unsigned long long c8, uint32_t E0)
@@ -379,85 +378,107 @@ __device__ __forceinline__ unsigned long long codes_to_exps(unsigned long long c
     return c8 + (unsigned long long)(E0 - 1) * 0x0101010101010101ull;
 }
 
+__device__ __forceinline__ uint4 ld_v4_plain(const void* p)
+{
+    return *reinterpret_cast<const uint4*>(p);
+}
+
+// One CTA per tile of 8192 values, no inter-tile dependence: the tile's
+// escape prefix is the chunk's index entry.  Every thread reads the chunk's
+// offsets, issues its sign+mantissa, plane and index loads as soon as the
+// fixed sections are known to lie inside the payload, and only then waits
+// for thread 0's header checks (in the oracle's order).  The index is
+// checked against the tile's own escape count (entry 0 must be 0, each entry
+// plus the tile's count must equal the next entry, the last one n_esc), so
+// the escapes read are always inside the escape section.
 __global__ void __launch_bounds__(kThreads) k_code3_decode(C3Dec a)
 {
-    __shared__ uint32_t s_tile, s_bad, s_E0;
+    __shared__ uint32_t s_bad, s_E0;
     __shared__ unsigned long long s_nesc;
     __shared__ unsigned long long s_spread[256];
     __shared__ unsigned long long s_warp[kThreads / 32];
-    __shared__ unsigned long long s_prefix;
-    __shared__ __align__(16) uint32_t s_esc32[(kTile + 16) / 4];
-    uint8_t* s_esc = reinterpret_cast<uint8_t*>(s_esc32);
+    __shared__ __align__(16) uint32_t s_esc32[(kTile + 32) / 4];
     const int t = threadIdx.x;
     s_spread[t] = spread_bits((uint32_t)t);
-    const TilePos tp = tile_pos(next_tile(a.counter, &s_tile), a.count, a.tpc);
-    const uint32_t ci = tp.ci, lt = tp.lt;
+    const uint32_t ci = blockIdx.x / a.tpc, lt = blockIdx.x % a.tpc;
     const uint32_t c = a.first + ci;
     const uint64_t n_c = shard_values(a.n, a.L, c);
     const uint64_t v0 = (uint64_t)lt * kTile;
     const uint32_t nv = v0 < n_c ? (uint32_t)umin64(kTile, n_c - v0) : 0u;
-    const uint64_t off = a.offsets[ci];
+    const uint64_t off = __ldg(a.offsets + ci), end = __ldg(a.offsets + ci + 1);
+    const uint64_t avail = end >= off ? end - off : 0ull;
     const uint8_t* p = a.in + off;
+    const uint64_t plane = rup(cdiv(n_c, 8), 128);
+    const uint64_t sec_pl = 128 + rup(n_c, 128);
+    const uint64_t sec_idx = sec_pl + 3 * plane;
+    const uint64_t sec_esc = sec_idx + c3_idx_bytes(n_c);
+    const uint64_t n_idx = cdiv(n_c, kTile);
+    // all fixed sections inside the payload: safe to read before the header
+    const bool fixed_ok = (off & 15u) == 0 && end >= off && avail >= sec_esc;
+    const uint8_t* sm_t = p + 128 + v0;
+    const uint8_t* pl_t = p + sec_pl + v0 / 8;
+    const bool full = nv == (uint32_t)kTile;
+
+    uint2 smv[kGroups];
+    uint32_t pb[kGroups];    // plane bytes p0 | p1 << 8 | p2 << 16
+    unsigned long long idx_here = 0, idx_next = 0;
+    if (fixed_ok) {
+#pragma unroll
+        for (int g = 0; g < kGroups; g++) {
+            const uint32_t j = (uint32_t)(g * kThreads + t);
+            const uint32_t v = 8u * j;
+            smv[g] = make_uint2(0, 0);
+            pb[g] = 0;
+            if (full || v + 8 <= nv) {
+                smv[g] = __ldg(reinterpret_cast<const uint2*>(sm_t + v));
+            } else if (v < nv) {
+                uint32_t lo = 0, hi = 0;
+                for (uint32_t i = 0; i < nv - v; i++) {
+                    const uint32_t b = sm_t[v + i];
+                    if (i < 4) lo |= b << (8 * i);
+                    else hi |= b << (8 * (i - 4));
+                }
+                smv[g] = make_uint2(lo, hi);
+            }
+            if (full || v < nv)
+                pb[g] = (uint32_t)__ldg(pl_t + j) | (uint32_t)__ldg(pl_t + plane + j) << 8 |
+                        (uint32_t)__ldg(pl_t + 2 * plane + j) << 16;
+        }
+        if (lt < n_idx) idx_here = __ldg(reinterpret_cast<const unsigned long long*>(p + sec_idx) + lt);
+        if (lt + 1 < n_idx) idx_next = __ldg(reinterpret_cast<const unsigned long long*>(p + sec_idx) + lt + 1);
+    } else {
+#pragma unroll
+        for (int g = 0; g < kGroups; g++) {
+            smv[g] = make_uint2(0, 0);
+            pb[g] = 0;
+        }
+    }
     if (t == 0) {
         // the oracle's order of checks
         uint32_t bad = 0;
-        const uint64_t end = a.offsets[ci + 1];
+        s_E0 = 0;
+        s_nesc = 0;
         if (off & 15u) {
             bad = EZ_DSTAT_MISALIGNED;
-        } else if (end < off || end - off < 128) {
+        } else if (end < off || avail < 128) {
             bad = EZ_DSTAT_BAD_SIZE;
         } else {
-            const uint64_t avail = end - off;
-            const uint64_t n_esc = rd_u64(p + 16), bytes = rd_u64(p + 24);
-            if (!(p[0] == 'E' && p[1] == 'Z' && p[2] == 'C' && p[3] == '3') || p[4] != 1 ||
-                p[5] > 249 || rd_u64(p + 8) != n_c || rd_u32(p + 32) != c || rd_u32(p + 36) != a.W)
+            const uint4 h0 = ld_v4_plain(p), h1 = ld_v4_plain(p + 16), h2 = ld_v4_plain(p + 32);
+            const uint64_t n_hdr = (uint64_t)h0.z | (uint64_t)h0.w << 32;
+            const uint64_t n_esc = (uint64_t)h1.x | (uint64_t)h1.y << 32;
+            const uint64_t bytes = (uint64_t)h1.z | (uint64_t)h1.w << 32;
+            const uint32_t E0 = (h0.y >> 8) & 0xFFu;
+            if (h0.x != 0x33435A45u || (h0.y & 0xFFu) != 2u || E0 > 249 || n_hdr != n_c ||
+                h2.x != c || h2.y != a.W)
                 bad = EZ_DSTAT_BAD_HEADER;
             else if (n_esc > n_c)
                 bad = EZ_DSTAT_BAD_COUNT;
             else if (bytes != c3_bytes(n_c, n_esc) || bytes > avail)
                 bad = EZ_DSTAT_BAD_SIZE;
-            s_E0 = p[5];
+            s_E0 = E0;
             s_nesc = n_esc;
         }
         s_bad = bad;
-    }
-    __syncthreads();
-    if (s_bad) {
-        if (lt == a.tpc - 1 && t == 0) atomicOr(a.dstatus, s_bad);
-        return;
-    }
-    const uint32_t E0 = s_E0;
-    const uint64_t n_esc = s_nesc;
-    const uint64_t plane = rup(cdiv(n_c, 8), 128);
-    const uint8_t* sm_sec = p + 128;
-    const uint8_t* pl_sec = sm_sec + rup(n_c, 128);
-    const uint8_t* esc_sec = pl_sec + 3 * plane;
-    const uint8_t* pl_t = pl_sec + v0 / 8;
-    uint16_t* ot = a.out + (uint64_t)ci * a.L + v0;
-    const bool full = nv == (uint32_t)kTile;
-
-    uint2 smv[kGroups];
-    uint32_t pb[kGroups];    // plane bytes p0 | p1 << 8 | p2 << 16
-#pragma unroll
-    for (int g = 0; g < kGroups; g++) {
-        const uint32_t j = (uint32_t)(g * kThreads + t);
-        const uint32_t v = 8u * j;
-        smv[g] = make_uint2(0, 0);
-        pb[g] = 0;
-        if (full || v + 8 <= nv) {
-            smv[g] = __ldg(reinterpret_cast<const uint2*>(sm_sec + v0 + v));
-        } else if (v < nv) {
-            uint32_t lo = 0, hi = 0;
-            for (uint32_t i = 0; i < nv - v; i++) {
-                const uint32_t b = sm_sec[v0 + v + i];
-                if (i < 4) lo |= b << (8 * i);
-                else hi |= b << (8 * (i - 4));
-            }
-            smv[g] = make_uint2(lo, hi);
-        }
-        if (full || v < nv)
-            pb[g] = (uint32_t)__ldg(pl_t + j) | (uint32_t)__ldg(pl_t + plane + j) << 8 |
-                    (uint32_t)__ldg(pl_t + 2 * plane + j) << 16;
     }
     uint32_t emasks = 0;
     unsigned long long packed = 0;
@@ -470,18 +491,34 @@ __global__ void __launch_bounds__(kThreads) k_code3_decode(C3Dec a)
         packed |= (unsigned long long)__popc(esc) << (16 * g);
     }
     unsigned long long total;
-    const unsigned long long excl = block_excl_scan(packed, s_warp, &total);
+    const unsigned long long excl = block_excl_scan(packed, s_warp, &total);   // also publishes s_bad
+    const uint32_t bad = s_bad;
+    if (bad) {
+        if (lt == 0 && t == 0) atomicOr(a.dstatus, bad);
+        return;
+    }
+    const uint32_t E0 = s_E0;
+    const unsigned long long n_esc = s_nesc;
     const unsigned long long agg = (total & 0xFFFFull) + ((total >> 16) & 0xFFFFull) +
                                    ((total >> 32) & 0xFFFFull) + (total >> 48);
-    const unsigned long long P = tile_prefix(a.state, tp.state, ci * a.tpc, agg, &s_prefix,
-                                             a.dstatus, a.abort);
-    // this tile's escapes, staged in shared memory (never read past n_esc)
-    const unsigned long long have = P >= n_esc ? 0ull : (n_esc - P < agg ? n_esc - P : agg);
-    for (uint32_t b = (uint32_t)t; b < (uint32_t)have; b += kThreads) s_esc[b] = esc_sec[P + b];
-    if (t == 0 && (have < agg || (lt == a.tpc - 1 && P + agg != n_esc)))
-        atomicOr(a.dstatus, EZ_DSTAT_BAD_COUNT);
+    // index checks (tiles past the chunk's end carry no entry and no escapes)
+    const unsigned long long P = lt < n_idx ? idx_here : n_esc;
+    const unsigned long long want = lt + 1 < n_idx ? idx_next : n_esc;
+    const bool idx_ok = (lt != 0 || n_idx == 0 || P == 0) && P <= n_esc && agg <= n_esc - P &&
+                        (lt >= n_idx || P + agg == want);
+    if (!idx_ok) {
+        if (t == 0) atomicOr(a.dstatus, EZ_DSTAT_BAD_COUNT);
+        return;
+    }
+    // this tile's escapes as aligned words: byte q of the tile is byte q + (P & 3)
+    const uint8_t* esc_w = p + sec_esc + (P & ~3ull);
+    const uint32_t sh = (uint32_t)(P & 3ull);
+    const uint32_t words = (uint32_t)((agg + sh + 3) >> 2);
+    for (uint32_t i = (uint32_t)t; i < words; i += kThreads)
+        s_esc32[i] = __ldg(reinterpret_cast<const uint32_t*>(esc_w) + i);
     __syncthreads();
 
+    uint16_t* ot = a.out + (uint64_t)ci * a.L + v0;
     uint32_t gbase = 0;
 #pragma unroll
     for (int g = 0; g < kGroups; g++) {
@@ -495,7 +532,7 @@ __global__ void __launch_bounds__(kThreads) k_code3_decode(C3Dec a)
         const uint32_t m = (emasks >> (8 * g)) & 0xFFu;
         if (m) {
             uint32_t c_lo, c_hi;
-            load_unaligned8(s_esc32, r, c_lo, c_hi);
+            load_unaligned8(s_esc32, r + sh, c_lo, c_hi);
             e8 = insert_selected(e8, m, c_lo, c_hi);
         }
         uint4 o4;

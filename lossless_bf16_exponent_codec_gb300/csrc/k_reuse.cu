@@ -83,18 +83,31 @@ struct RuDec {
     uint32_t* abort;
 };
 
+// Payload sections: header 64 | bitmap | SM | index | EXP.  The index holds
+// one entry per kTile (8192) values of the shard: u64 changed blocks before
+// it, and for the coded variant a second u64, the escapes among the EXP
+// exponents of those blocks.
 __device__ __forceinline__ uint64_t ru_off_sm(uint64_t n_s, uint32_t B)
 {
     return 64 + rup(cdiv(cdiv(n_s, B), 8), 16);
 }
-__device__ __forceinline__ uint64_t ru_off_exp(uint64_t n_s, uint32_t B)
+__device__ __forceinline__ uint64_t ru_off_idx(uint64_t n_s, uint32_t B)
 {
     return ru_off_sm(n_s, B) + rup(n_s, 16);
+}
+__device__ __forceinline__ uint32_t ru_idx_stride(bool coded) { return coded ? 16u : 8u; }
+__device__ __forceinline__ uint64_t ru_idx_bytes(uint64_t n_s, bool coded)
+{
+    return rup(ru_idx_stride(coded) * cdiv(n_s, kTile), 16);
+}
+__device__ __forceinline__ uint64_t ru_off_exp(uint64_t n_s, uint32_t B, bool coded)
+{
+    return ru_off_idx(n_s, B) + ru_idx_bytes(n_s, coded);
 }
 __device__ __forceinline__ uint64_t ru_bytes(uint64_t n_s, uint32_t B, uint64_t m, bool coded,
                                              uint64_t n_esc)
 {
-    return rup(ru_off_exp(n_s, B) + (coded ? 3 * rup(cdiv(m, 8), 16) + n_esc : m), 128);
+    return rup(ru_off_exp(n_s, B, coded) + (coded ? 3 * rup(cdiv(m, 8), 16) + n_esc : m), 128);
 }
 
 __device__ __forceinline__ uint32_t lb8(uint64_t v, int k) { return (uint32_t)(v >> (8 * k)) & 0xFFu; }
@@ -108,7 +121,7 @@ __device__ __forceinline__ uint32_t ru_header_byte(int b, uint32_t flags, uint32
         case 1: return 'Z';
         case 2: return 'R';
         case 3: return 'U';
-        case 4: return 1;
+        case 4: return 2;
         case 5: return flags;
         case 6: return E0;
         case 7: return 0;
@@ -224,7 +237,8 @@ __global__ void __launch_bounds__(kThreads, 4) k_reuse_encode(RuEnc a)
     const uint32_t B = a.B, log2B = a.log2B;
     const uint64_t nb = cdiv(n_s, B);
     const uint64_t bm_bytes = cdiv(nb, 8);
-    const uint64_t off_sm = ru_off_sm(n_s, B), off_exp = ru_off_exp(n_s, B);
+    const uint64_t off_sm = ru_off_sm(n_s, B), off_idx = ru_off_idx(n_s, B);
+    const uint64_t off_exp = ru_off_exp(n_s, B, kCoded);
     const uint16_t* xt = a.x + (uint64_t)ci * a.L + v0;
     uint8_t* ct = a.cache + (uint64_t)ci * a.L + v0;
     uint8_t* o = a.out + (uint64_t)ci * a.slot;
@@ -281,6 +295,9 @@ __global__ void __launch_bounds__(kThreads, 4) k_reuse_encode(RuEnc a)
     const unsigned long long P = tile_prefix(a.state, tp.state, ci * a.tpc, agg, &s_prefix,
                                              a.dstatus, a.abort);
 
+    // index entry: changed blocks before this tile
+    if (t == 0 && v0 < n_s)
+        *reinterpret_cast<unsigned long long*>(o + off_idx + (uint64_t)ru_idx_stride(kCoded) * lt) = P;
     // bitmap bytes of this tile
     const uint32_t nbt = (uint32_t)kTile >> log2B;
     const uint64_t bm0 = (uint64_t)lt * (nbt / 8);
@@ -314,6 +331,8 @@ __global__ void __launch_bounds__(kThreads, 4) k_reuse_encode(RuEnc a)
         const uint64_t m = n_changed * B - (last_changed ? nb * B - n_s : 0);
         if (t < 16 && rup(bm_bytes, 16) > bm_bytes + t) o[64 + bm_bytes + t] = 0;
         if (t < 16 && rup(n_s, 16) > n_s + t) o[off_sm + n_s + t] = 0;
+        const uint64_t ib = (uint64_t)ru_idx_stride(kCoded) * cdiv(n_s, kTile);
+        if (t < 16 && ib + t < ru_idx_bytes(n_s, kCoded)) o[off_idx + ib + t] = 0;
         if (kCoded) {
             if (t == 0) {
                 a.info[ci].m = m;
@@ -356,6 +375,12 @@ __device__ __forceinline__ uint32_t codes_of_bytes(const uint32_t* lut, uint32_t
 }
 
 // Pass 2 of the coded variant: 3-bit code of the staged exponent stream.
+// One CTA per kTile span of the shard's values: it codes the stream
+// exponents of the span's changed blocks, [q0, q1) with q = (changed blocks
+// before the span) * B taken from the index that pass 1 wrote, so its
+// escape prefix -- from a look-back over the spans -- is the span's second
+// index entry.  q0 is a multiple of B >= 8, so the span's plane bytes start
+// on a byte.
 __global__ void __launch_bounds__(kThreads) k_reuse_code3(RuC3 a)
 {
     __shared__ uint32_t s_tile;
@@ -370,21 +395,32 @@ __global__ void __launch_bounds__(kThreads) k_reuse_code3(RuC3 a)
     const uint64_t n_s = shard_values(a.n, a.L, r);
     const uint64_t m = a.info[ci].m;
     const uint64_t n_changed = a.info[ci].n_changed;
-    const uint64_t v0 = (uint64_t)lt * kTile;
-    const uint32_t nv = v0 < m ? (uint32_t)umin64(kTile, m - v0) : 0u;
+    const uint64_t spans = cdiv(n_s, kTile);
     uint32_t E0 = a.stats[ci].E0;
     if (E0 > 249u) {
         if (t == 0) atomicOr(a.dstatus, EZ_DSTAT_BAD_STATS);
         E0 = 0;
     }
     s_lut[t] = ru_lut_entry((uint32_t)t, E0);
-    const uint64_t off_exp = ru_off_exp(n_s, a.B);
+    const uint64_t off_idx = ru_off_idx(n_s, a.B), off_exp = ru_off_exp(n_s, a.B, true);
     const uint64_t plane = rup(cdiv(m, 8), 16);
     uint8_t* o = a.out + (uint64_t)ci * a.slot;
     uint8_t* pl = o + off_exp;
     uint8_t* esc_sec = pl + 3 * plane;
-    const uint8_t* es = a.expbuf + (uint64_t)ci * a.L + v0;
-    const uint32_t fin_tile = m ? (uint32_t)((m - 1) / kTile) : 0u;
+    unsigned long long* idx = reinterpret_cast<unsigned long long*>(o + off_idx);
+    // the span's slice of the stream
+    uint64_t q0 = 0, q1 = 0;
+    if (lt < spans) {
+        q0 = idx[2 * lt] * a.B;
+        q1 = lt + 1 < spans ? idx[2 * (lt + 1)] * a.B : m;
+        if (q1 < q0 || q1 > m || q1 - q0 > kTile) {
+            if (t == 0) atomicOr(a.dstatus, EZ_DSTAT_BAD_COUNT);
+            q1 = q0 = 0;
+        }
+    }
+    const uint32_t nv = (uint32_t)(q1 - q0);
+    const uint8_t* es = a.expbuf + (uint64_t)ci * a.L + q0;
+    const uint32_t fin_tile = (uint32_t)(a.tpc - 1);
 
     unsigned long long e8[kGroups];
 #pragma unroll
@@ -403,7 +439,7 @@ __global__ void __launch_bounds__(kThreads) k_reuse_code3(RuC3 a)
         if (!vm) continue;
         const uint32_t acc = codes_of_bytes(s_lut, (uint32_t)e8[g], (uint32_t)(e8[g] >> 32)) &
                              (vm * 0x01010101u);
-        const uint64_t pb = v0 / 8 + j;
+        const uint64_t pb = q0 / 8 + j;
         pl[pb] = (uint8_t)acc;
         pl[plane + pb] = (uint8_t)(acc >> 8);
         pl[2 * plane + pb] = (uint8_t)(acc >> 16);
@@ -428,6 +464,7 @@ __global__ void __launch_bounds__(kThreads) k_reuse_code3(RuC3 a)
     }
     const unsigned long long P = tile_prefix(a.state, tp.state, ci * a.tpc, agg, &s_prefix,
                                              a.dstatus, a.abort);
+    if (t == 0 && lt < spans) idx[2 * lt + 1] = P;
     for (uint32_t b = (uint32_t)t; b < (uint32_t)agg; b += kThreads) esc_sec[P + b] = s_esc[b];
     if (lt == fin_tile) {
         const uint64_t n_esc = P + agg;
@@ -446,34 +483,28 @@ __global__ void __launch_bounds__(kThreads) k_reuse_code3(RuC3 a)
     }
 }
 
-__device__ __forceinline__ uint64_t rd64(const uint8_t* p)
-{
-    uint64_t v = 0;
-#pragma unroll
-    for (int k = 7; k >= 0; k--) v = (v << 8) | p[k];
-    return v;
-}
-__device__ __forceinline__ uint32_t rd32(const uint8_t* p)
-{
-    return (uint32_t)p[0] | (uint32_t)p[1] << 8 | (uint32_t)p[2] << 16 | (uint32_t)p[3] << 24;
-}
+__device__ __forceinline__ uint4 ld16_plain(const void* p) { return *reinterpret_cast<const uint4*>(p); }
 
+// One CTA per kTile span of one payload, no inter-tile dependence.  The
+// span's index entry gives the changed blocks (and, coded, the escapes)
+// before it; it is checked against the span's own counts -- entry 0 must be
+// 0, entry + count must equal the next entry, the last one n_changed (n_esc)
+// -- so the exponents read always lie inside the EXP section.  Every thread
+// reads the payload offsets, then the bitmap slice, sign+mantissa bytes and
+// index entries are loaded before thread 0's header checks complete.
 template <bool kCoded>
 __global__ void __launch_bounds__(kThreads) k_reuse_decode(RuDec a)
 {
-    __shared__ uint32_t s_tile, s_bad, s_E0;
+    __shared__ uint32_t s_bad, s_E0;
     __shared__ unsigned long long s_hdr[4];   // n_changed, m, n_esc
     __shared__ uint32_t s_bm[32], s_pre[32], s_agg;
     __shared__ unsigned long long s_warp[kThreads / 32];
-    __shared__ unsigned long long s_prefix;
     __shared__ unsigned long long s_spread[kCoded ? 256 : 1];
-    __shared__ __align__(16) uint32_t s_esc32[kCoded ? (kTile + 16) / 4 : 4];
-    uint8_t* s_esc = reinterpret_cast<uint8_t*>(s_esc32);
+    __shared__ __align__(16) uint32_t s_esc32[kCoded ? (kTile + 32) / 4 : 4];
     const int t = threadIdx.x;
     if (kCoded) s_spread[t] = spread_bits((uint32_t)t);
     if (t < 32) s_bm[t] = 0;
-    const TilePos tp = tile_pos(next_tile(a.counter, &s_tile), a.count, a.tpc);
-    const uint32_t ci = tp.ci, lt = tp.lt;
+    const uint32_t ci = blockIdx.x / a.tpc, lt = blockIdx.x % a.tpc;
     const uint32_t r = a.first + ci;
     const uint64_t n_s = shard_values(a.n, a.L, r);
     const uint64_t v0 = (uint64_t)lt * kTile;
@@ -481,29 +512,69 @@ __global__ void __launch_bounds__(kThreads) k_reuse_decode(RuDec a)
     const uint32_t B = a.B, log2B = a.log2B;
     const uint64_t nb = cdiv(n_s, B);
     const uint64_t bm_bytes = cdiv(nb, 8);
-    const uint32_t fin_tile = n_s ? (uint32_t)((n_s - 1) / kTile) : 0u;
-    const uint64_t off = a.offsets ? a.offsets[ci] : 0ull;
+    const uint64_t spans = cdiv(n_s, kTile);
+    const uint64_t off = a.offsets ? __ldg(a.offsets + ci) : 0ull;
+    uint64_t avail = a.single_avail;
+    bool order_bad = false;
+    if (a.offsets) {
+        const uint64_t end = __ldg(a.offsets + ci + 1);
+        order_bad = end < off;
+        avail = order_bad ? 0ull : end - off;
+    }
     const uint8_t* p = a.in + off;
+    const uint64_t off_sm = ru_off_sm(n_s, B), off_idx = ru_off_idx(n_s, B);
+    const uint64_t off_exp = ru_off_exp(n_s, B, kCoded);
+    const uint32_t stride = ru_idx_stride(kCoded);
+    const bool fixed_ok = !order_bad && (off & 15u) == 0 && avail >= off_exp;
+
+    // loads that need only the fixed sections
+    const uint32_t nbt = (uint32_t)kTile >> log2B;
+    const uint64_t bm0 = (uint64_t)lt * (nbt / 8);
+    uint32_t bmb = 0;
+    unsigned long long smv[kGroups];
+    unsigned long long ib_here = 0, ib_next = 0, ie_here = 0, ie_next = 0;
+#pragma unroll
+    for (int g = 0; g < kGroups; g++) smv[g] = 0;
+    if (fixed_ok) {
+        if ((uint32_t)t < nbt / 8 && bm0 + t < bm_bytes) {
+            bmb = p[64 + bm0 + t];
+            if (bm0 + t == bm_bytes - 1 && (nb & 7)) bmb &= (1u << (nb & 7)) - 1u;
+        }
+        const uint8_t* sm_t = p + off_sm + v0;
+#pragma unroll
+        for (int g = 0; g < kGroups; g++) {
+            const uint32_t v = 8u * (uint32_t)(g * kThreads + t);
+            if (v < nv) smv[g] = ld_group8(sm_t, v, nv);
+        }
+        const unsigned long long* idx = reinterpret_cast<const unsigned long long*>(p + off_idx);
+        const uint32_t sw = stride / 8;
+        if (lt < spans) {
+            ib_here = __ldg(idx + sw * lt);
+            if (kCoded) ie_here = __ldg(idx + sw * lt + 1);
+        }
+        if (lt + 1 < spans) {
+            ib_next = __ldg(idx + sw * (lt + 1));
+            if (kCoded) ie_next = __ldg(idx + sw * (lt + 1) + 1);
+        }
+    }
     if (t == 0) {
         uint32_t bad = 0;
-        uint64_t avail = 0;
-        if (a.offsets) {
-            const uint64_t end = a.offsets[ci + 1];
-            avail = end >= off ? end - off : 0;
-            if (end < off) bad = EZ_DSTAT_BAD_SIZE;
-        } else {
-            avail = a.single_avail;
-        }
+        s_E0 = 0;
+        if (order_bad) bad = EZ_DSTAT_BAD_SIZE;
         if (!bad && (off & 15u)) bad = EZ_DSTAT_MISALIGNED;
         if (!bad && avail < 64) bad = EZ_DSTAT_BAD_SIZE;
         if (!bad) {
-            const uint32_t flags = p[5], E0 = p[6];
-            const uint64_t n_changed = rd64(p + 24), m = rd64(p + 32), n_esc = rd64(p + 40),
-                           total = rd64(p + 48);
+            const uint4 h0 = ld16_plain(p), h1 = ld16_plain(p + 16), h2 = ld16_plain(p + 32),
+                        h3 = ld16_plain(p + 48);
+            const uint32_t flags = (h0.y >> 8) & 0xFFu, E0 = (h0.y >> 16) & 0xFFu;
+            const uint64_t n_hdr = (uint64_t)h1.x | (uint64_t)h1.y << 32;
+            const uint64_t n_changed = (uint64_t)h1.z | (uint64_t)h1.w << 32;
+            const uint64_t m = (uint64_t)h2.x | (uint64_t)h2.y << 32;
+            const uint64_t n_esc = (uint64_t)h2.z | (uint64_t)h2.w << 32;
+            const uint64_t total = (uint64_t)h3.x | (uint64_t)h3.y << 32;
             const bool coded = flags & 1u;
-            if (!(p[0] == 'E' && p[1] == 'Z' && p[2] == 'R' && p[3] == 'U') || p[4] != 1 ||
-                (flags & ~3u) || p[7] != 0 || rd32(p + 8) != B || rd32(p + 12) != r ||
-                rd64(p + 16) != n_s || coded != kCoded)
+            if (h0.x != 0x55525A45u || (h0.y & 0xFFu) != 2u || (flags & ~3u) || (h0.y >> 24) != 0 ||
+                h0.z != B || h0.w != r || n_hdr != n_s || coded != kCoded)
                 bad = EZ_DSTAT_BAD_HEADER;
             else if (coded ? E0 > 249 : (E0 != 0 || n_esc != 0))
                 bad = EZ_DSTAT_BAD_HEADER;
@@ -518,31 +589,12 @@ __global__ void __launch_bounds__(kThreads) k_reuse_decode(RuDec a)
         }
         s_bad = bad;
     }
+    if (bmb) atomicOr(&s_bm[t >> 2], bmb << (8 * (t & 3)));
     __syncthreads();
     if (s_bad) {
-        if (lt == fin_tile && t == 0) atomicOr(a.dstatus, s_bad);
+        if (lt == 0 && t == 0) atomicOr(a.dstatus, s_bad);
         return;
     }
-    const uint64_t n_changed = s_hdr[0], m = s_hdr[1], n_esc = s_hdr[2];
-    const uint32_t E0 = s_E0;
-    const uint64_t off_sm = ru_off_sm(n_s, B), off_exp = ru_off_exp(n_s, B);
-    const uint8_t* sm_t = p + off_sm + v0;
-    const uint8_t* ex = p + off_exp;
-    uint8_t* ct = a.cache + (uint64_t)ci * a.L + v0;
-    uint16_t* ot = a.out + (uint64_t)ci * a.L + v0;
-
-    // this tile's slice of the bitmap (bits past nb ignored)
-    const uint32_t nbt = (uint32_t)kTile >> log2B;
-    const uint64_t bm0 = (uint64_t)lt * (nbt / 8);
-    if ((uint32_t)t < nbt / 8) {
-        uint32_t b = 0;
-        if (bm0 + t < bm_bytes) {
-            b = p[64 + bm0 + t];
-            if (bm0 + t == bm_bytes - 1 && (nb & 7)) b &= (1u << (nb & 7)) - 1u;
-        }
-        if (b) atomicOr(&s_bm[t >> 2], b << (8 * (t & 3)));
-    }
-    __syncthreads();
     if (t < 32) {
         const uint32_t c = __popc(s_bm[t]);
         uint32_t x = c;
@@ -556,44 +608,47 @@ __global__ void __launch_bounds__(kThreads) k_reuse_decode(RuDec a)
     }
     __syncthreads();
     const unsigned long long agg = s_agg;
+    const uint64_t n_changed = s_hdr[0], m = s_hdr[1], n_esc = s_hdr[2];
+    const uint32_t E0 = s_E0;
+    // index checks on the changed-block prefix
+    const unsigned long long P = lt < spans ? ib_here : n_changed;
+    bool ok = (lt != 0 || spans == 0 || P == 0) && P <= n_changed && agg <= n_changed - P &&
+              (lt >= spans || P + agg == (lt + 1 < spans ? ib_next : n_changed));
+    if (ok && lt + 1 == spans) {
+        const bool last_changed = block_changed(s_bm, (uint32_t)((n_s - 1 - v0) >> log2B));
+        ok = (P + agg) * B - (last_changed ? nb * B - n_s : 0) == m;
+    }
+    if (!ok) {
+        if (t == 0) atomicOr(a.dstatus, EZ_DSTAT_BAD_COUNT);
+        return;
+    }
+    const uint8_t* ex = p + off_exp;
+    uint8_t* ct = a.cache + (uint64_t)ci * a.L + v0;
+    uint16_t* ot = a.out + (uint64_t)ci * a.L + v0;
 
-    // loads that do not depend on the prefix
-    unsigned long long smv[kGroups], ev[kGroups];
+    unsigned long long ev[kGroups];
     bool chg[kGroups];
+    uint64_t pos[kGroups];
+    bool in_range = true;
 #pragma unroll
     for (int g = 0; g < kGroups; g++) {
         const uint32_t v = 8u * (uint32_t)(g * kThreads + t);
-        chg[g] = v < nv && block_changed(s_bm, v >> log2B);
-        smv[g] = v < nv ? ld_group8(sm_t, v, nv) : 0ull;
-        ev[g] = (v < nv && !chg[g]) ? ld_group8(ct, v, nv) : 0ull;
-    }
-    const unsigned long long P = tile_prefix(a.state_a, tp.state, ci * a.tpc, agg, &s_prefix,
-                                             a.dstatus, a.abort);
-    bool bad_count = false;
-    if (lt == fin_tile && t == 0) {
-        bool last_changed = false;
-        if (n_s) last_changed = block_changed(s_bm, (uint32_t)((n_s - 1 - v0) >> log2B));
-        const uint64_t want_m = (P + agg) * B - (last_changed ? nb * B - n_s : 0);
-        if (P + agg != n_changed || want_m != m) bad_count = true;
-    }
-
-    if (!kCoded) {
-#pragma unroll
-        for (int g = 0; g < kGroups; g++) {
-            if (!chg[g]) continue;
-            const uint32_t v = 8u * (uint32_t)(g * kThreads + t);
-            const uint32_t k = v >> log2B;
-            const uint64_t pos = (P + block_rank(s_bm, s_pre, k)) * B + (v - (k << log2B));
-            const uint32_t cnt = min(8u, nv - v);
-            if (pos + cnt <= m) {
-                ev[g] = ld_group8(ex + pos, 0u, cnt);
-            } else {
-                ev[g] = 0;
-                bad_count = true;
-            }
+        const uint32_t k = v >> log2B;
+        chg[g] = v < nv && block_changed(s_bm, k);
+        pos[g] = (P + block_rank(s_bm, s_pre, k)) * B + (v - (k << log2B));
+        ev[g] = 0;
+        if (v < nv && !chg[g]) ev[g] = ld_group8(ct, v, nv);
+        if (chg[g] && pos[g] + min(8u, nv - v) > m) {
+            // an m smaller than the bitmap says: never read past the section
+            in_range = false;
+            chg[g] = false;
         }
-    } else {
-        // planes of this tile's changed exponents, then the escape prefix
+        if (!kCoded && chg[g]) ev[g] = ld_group8(ex + pos[g], 0u, min(8u, nv - v));
+    }
+    if (!in_range) atomicOr(a.dstatus, EZ_DSTAT_BAD_COUNT);
+
+    if (kCoded) {
+        // planes of this span's changed exponents; escapes from the index
         const uint64_t plane = rup(cdiv(m, 8), 16);
         const uint8_t* esc_sec = ex + 3 * plane;
         uint32_t pbs[kGroups];
@@ -604,15 +659,8 @@ __global__ void __launch_bounds__(kThreads) k_reuse_decode(RuDec a)
             pbs[g] = 0;
             if (!chg[g]) continue;
             const uint32_t v = 8u * (uint32_t)(g * kThreads + t);
-            const uint32_t k = v >> log2B;
-            const uint64_t pos = (P + block_rank(s_bm, s_pre, k)) * B + (v - (k << log2B));
             const uint32_t cnt = min(8u, nv - v);
-            if (pos + cnt > m) {
-                bad_count = true;
-                chg[g] = false;     // a corrupt block: its values are left as cache contents
-                continue;
-            }
-            const uint64_t pb = pos >> 3;
+            const uint64_t pb = pos[g] >> 3;
             pbs[g] = (uint32_t)ex[pb] | (uint32_t)ex[plane + pb] << 8 | (uint32_t)ex[2 * plane + pb] << 16;
             const uint32_t vm = cnt >= 8 ? 0xFFu : ((1u << cnt) - 1u);
             const uint32_t esc = ~(pbs[g] | pbs[g] >> 8 | pbs[g] >> 16) & vm;
@@ -623,12 +671,21 @@ __global__ void __launch_bounds__(kThreads) k_reuse_decode(RuDec a)
         const unsigned long long excl = block_excl_scan(packed, s_warp, &total);
         const unsigned long long agg2 = (total & 0xFFFFull) + ((total >> 16) & 0xFFFFull) +
                                         ((total >> 32) & 0xFFFFull) + (total >> 48);
-        __syncthreads();   // s_prefix is reused
-        const unsigned long long Q = tile_prefix(a.state_b, tp.state, ci * a.tpc, agg2, &s_prefix,
-                                                 a.dstatus, a.abort);
-        const unsigned long long have = Q >= n_esc ? 0ull : (n_esc - Q < agg2 ? n_esc - Q : agg2);
-        for (uint32_t b = (uint32_t)t; b < (uint32_t)have; b += kThreads) s_esc[b] = esc_sec[Q + b];
-        if (t == 0 && (have < agg2 || (lt == fin_tile && Q + agg2 != n_esc))) bad_count = true;
+        const unsigned long long Q = lt < spans ? ie_here : n_esc;
+        const bool eok = (lt != 0 || spans == 0 || Q == 0) && Q <= n_esc && agg2 <= n_esc - Q &&
+                         (lt >= spans || Q + agg2 == (lt + 1 < spans ? ie_next : n_esc));
+        if (!eok) {
+            if (t == 0) atomicOr(a.dstatus, EZ_DSTAT_BAD_COUNT);
+            return;
+        }
+        const uint8_t* esc_w = esc_sec + (Q & ~3ull);
+        const uint32_t sh = (uint32_t)(Q & 3ull);
+        const uint32_t words = (uint32_t)((agg2 + sh + 3) >> 2);
+        // the escape section starts on a 16-byte boundary (EXP section and
+        // planes are multiples of 16), so whole words up to rup(n_esc, 4)
+        // stay inside the padded payload
+        for (uint32_t i = (uint32_t)t; i < words; i += kThreads)
+            s_esc32[i] = __ldg(reinterpret_cast<const uint32_t*>(esc_w) + i);
         __syncthreads();
         uint32_t gbase = 0;
 #pragma unroll
@@ -645,7 +702,7 @@ __global__ void __launch_bounds__(kThreads) k_reuse_decode(RuDec a)
             const uint32_t mm = (emasks >> (8 * g)) & 0xFFu;
             if (mm) {
                 uint32_t c_lo, c_hi;
-                load_unaligned8(s_esc32, q, c_lo, c_hi);
+                load_unaligned8(s_esc32, q + sh, c_lo, c_hi);
                 e = insert_selected(e, mm, c_lo, c_hi);
             }
             const uint32_t cnt = min(8u, nv - (8u * (uint32_t)(g * kThreads + t)));
@@ -668,7 +725,6 @@ __global__ void __launch_bounds__(kThreads) k_reuse_decode(RuDec a)
             for (uint32_t i = 0; i < nv - v; i++) ot[v + i] = (uint16_t)(hw[i >> 1] >> (16 * (i & 1)));
         }
     }
-    if (bad_count) atomicOr(a.dstatus, EZ_DSTAT_BAD_COUNT);
 }
 
 static uint32_t ilog2(uint32_t v)

@@ -16,22 +16,29 @@
  * Shards / per-peer chunks
  *   L = 128 * ceil(ceil(n/W)/128); shard r covers [r*L, min((r+1)*L, n)).
  *
- * code3 chunk [ZIP 3.1 code and layout; 3.2 AllGather/AlltoAll]
- *   header 128 B: "EZC3", u8 version=1, u8 E0, u16 0, u64 n_c, u64 n_esc,
+ * code3 chunk [ZIP 3.1 code and layout; 3.2 AllGather/AlltoAll; 3.1 measured
+ * size: "padding, indices"]
+ *   header 128 B: "EZC3", u8 version=2, u8 E0, u16 0, u64 n_c, u64 n_esc,
  *                 u64 chunk_bytes, u32 chunk index, u32 W, zeros
  *   SM    : n_c bytes, padded to 128
  *   P0..P2: ceil(n_c/8) bytes each, padded to 128; bit p of code(j) is bit
  *           (j&7) of byte (j>>3) of plane p
+ *   IDX   : u64 per 8192 values, T = ceil(n_c/8192) entries; IDX[k] = number
+ *           of escapes among values [0, 8192k); padded to 128
  *   ESC   : n_esc raw exponent bytes in value order, padded to 128
  *   code(j) = E-E0+1 when E0 <= E <= E0+6, else 0 (escape)
  *
  * reuse payload [CIERA, exponent-reuse and gain-formula paragraphs]
- *   header 64 B: "EZRU", u8 version=1, u8 flags (bit0 exponents code3-coded,
+ *   header 64 B: "EZRU", u8 version=2, u8 flags (bit0 exponents code3-coded,
  *                bit1 cold), u8 E0, u8 0, u32 B, u32 shard index, u64 n_s,
  *                u64 n_changed, u64 m, u64 n_esc, u64 total_bytes, u64 0
  *   BM : ceil(nb/8) bytes, nb = ceil(n_s/B); bit k = block k changed, bit
  *        (k&7) of byte (k>>3); padded to 16
  *   SM : n_s bytes, padded to 16
+ *   IDX: per 8192 values, T = ceil(n_s/8192) entries: u64 number of changed
+ *        blocks among blocks [0, 8192k/B), and, when coded, a second u64:
+ *        number of escapes among the EXP exponents of those blocks; padded
+ *        to 16 (B divides 8192, so no block straddles an entry)
  *   EXP: raw  -> the m exponent bytes of the changed blocks, block order
  *        coded-> planes P0..P2 of the code3 code of those m exponents (each
  *               ceil(m/8) bytes padded to 16), then n_esc escape bytes
@@ -262,10 +269,12 @@ static unsigned code_of(unsigned E, unsigned E0)
     return (E >= E0 && E <= E0 + 6) ? E - E0 + 1 : 0;
 }
 
+#define IDX_SPAN 8192u
+
 uint64_t orc_code3_chunk_bytes(uint64_t n_c, uint64_t n_esc)
 {
     return 128 + round_up(n_c, 128) + 3 * round_up(ceil_div(n_c, 8), 128)
-           + round_up(n_esc, 128);
+           + round_up(8 * ceil_div(n_c, IDX_SPAN), 128) + round_up(n_esc, 128);
 }
 
 uint64_t orc_code3_slot_bytes(uint64_t n, uint32_t W)
@@ -290,7 +299,7 @@ int orc_code3_encode(const uint16_t* x, uint64_t n, uint32_t W, uint32_t E0,
         if (bytes > slot_bytes) return -2;
         memset(o, 0, bytes);
         o[0] = 'E'; o[1] = 'Z'; o[2] = 'C'; o[3] = '3';
-        o[4] = 1;
+        o[4] = 2;
         o[5] = (uint8_t)E0;
         put_u64(o + 8, n_c);
         put_u64(o + 16, n_esc);
@@ -300,10 +309,12 @@ int orc_code3_encode(const uint16_t* x, uint64_t n, uint32_t W, uint32_t E0,
         uint64_t off_sm = 128;
         uint64_t plane = round_up(ceil_div(n_c, 8), 128);
         uint64_t off_p = off_sm + round_up(n_c, 128);
-        uint64_t off_e = off_p + 3 * plane;
+        uint64_t off_i = off_p + 3 * plane;
+        uint64_t off_e = off_i + round_up(8 * ceil_div(n_c, IDX_SPAN), 128);
         uint64_t k = 0;
         for (uint64_t j = 0; j < n_c; j++) {
             uint16_t h = xc[j];
+            if (j % IDX_SPAN == 0) put_u64(o + off_i + 8 * (j / IDX_SPAN), k);
             unsigned E = bf16_exp(h);
             unsigned code = code_of(E, E0);
             o[off_sm + j] = bf16_sm(h);
@@ -327,7 +338,7 @@ uint32_t orc_code3_decode(const uint8_t* in, const uint64_t* offsets,
         uint64_t avail = offsets[c + 1] - offsets[c];
         if (avail < 128) { status |= ORC_BAD_SIZE; continue; }
         const uint8_t* p = in + offsets[c];
-        if (!(p[0] == 'E' && p[1] == 'Z' && p[2] == 'C' && p[3] == '3') || p[4] != 1
+        if (!(p[0] == 'E' && p[1] == 'Z' && p[2] == 'C' && p[3] == '3') || p[4] != 2
             || p[5] > 249 || get_u64(p + 8) != n_c || get_u32(p + 32) != c
             || get_u32(p + 36) != W) {
             status |= ORC_BAD_HEADER;
@@ -344,10 +355,14 @@ uint32_t orc_code3_decode(const uint8_t* in, const uint64_t* offsets,
         uint64_t plane = round_up(ceil_div(n_c, 8), 128);
         const uint8_t* sm = p + 128;
         const uint8_t* pl = sm + round_up(n_c, 128);
-        const uint8_t* esc = pl + 3 * plane;
+        const uint8_t* idx = pl + 3 * plane;
+        const uint8_t* esc = idx + round_up(8 * ceil_div(n_c, IDX_SPAN), 128);
         uint16_t* oc = out + (uint64_t)c * L;
         uint64_t k = 0;
         for (uint64_t j = 0; j < n_c; j++) {
+            /* the index must hold the escape count of the values before */
+            if (j % IDX_SPAN == 0 && get_u64(idx + 8 * (j / IDX_SPAN)) != k)
+                status |= ORC_BAD_COUNT;
             unsigned code = 0;
             for (unsigned b = 0; b < 3; b++)
                 code |= ((pl[b * plane + j / 8] >> (j % 8)) & 1u) << b;
@@ -369,12 +384,18 @@ uint32_t orc_code3_decode(const uint8_t* in, const uint64_t* offsets,
 
 /* ------------------------------------------------------------------ reuse */
 
+static uint64_t reuse_idx_bytes(uint64_t n_s, int coded)
+{
+    return round_up((coded ? 16 : 8) * ceil_div(n_s, IDX_SPAN), 16);
+}
+
 uint64_t orc_reuse_bytes(uint64_t n_s, uint32_t B, uint64_t m, int coded,
                          uint64_t n_esc)
 {
     uint64_t nb = ceil_div(n_s, B);
     uint64_t exp_bytes = coded ? 3 * round_up(ceil_div(m, 8), 16) + n_esc : m;
-    return round_up(64 + round_up(ceil_div(nb, 8), 16) + round_up(n_s, 16) + exp_bytes, 128);
+    return round_up(64 + round_up(ceil_div(nb, 8), 16) + round_up(n_s, 16)
+                    + reuse_idx_bytes(n_s, coded) + exp_bytes, 128);
 }
 
 uint64_t orc_reuse_slot_bytes(uint64_t n, uint32_t W, uint32_t B, int coded)
@@ -421,7 +442,7 @@ int orc_reuse_encode(const uint16_t* shard, uint64_t n_s, uint32_t B,
     if (total > cap) { free(changed); free(exps); return -2; }
     memset(out, 0, total);
     out[0] = 'E'; out[1] = 'Z'; out[2] = 'R'; out[3] = 'U';
-    out[4] = 1;
+    out[4] = 2;
     out[5] = (uint8_t)((coded ? 1 : 0) | (cold ? 2 : 0));
     out[6] = (uint8_t)E0;
     put_u32(out + 8, B);
@@ -433,10 +454,28 @@ int orc_reuse_encode(const uint16_t* shard, uint64_t n_s, uint32_t B,
     put_u64(out + 48, total);
     uint64_t off_bm = 64;
     uint64_t off_sm = off_bm + round_up(ceil_div(nb, 8), 16);
-    uint64_t off_x = off_sm + round_up(n_s, 16);
+    uint64_t off_i = off_sm + round_up(n_s, 16);
+    uint64_t off_x = off_i + reuse_idx_bytes(n_s, coded);
     for (uint64_t k = 0; k < nb; k++)
         if (changed[k]) out[off_bm + k / 8] |= (uint8_t)(1u << (k % 8));
     for (uint64_t i = 0; i < n_s; i++) out[off_sm + i] = bf16_sm(shard[i]);
+    /* index: changed blocks (and escapes among their exponents) before
+     * each multiple of 8192 values */
+    {
+        uint64_t k = 0, before = 0, q = 0, esc_before = 0;
+        for (uint64_t t = 0; t < ceil_div(n_s, IDX_SPAN); t++) {
+            /* walk the blocks that lie before value t*8192 */
+            for (; k < t * IDX_SPAN / B; k++) {
+                if (!changed[k]) continue;
+                before++;
+                uint64_t a = k * B, b = (k + 1) * B < n_s ? (k + 1) * B : n_s;
+                for (uint64_t i = a; i < b; i++, q++)
+                    if (coded && code_of(exps[q], E0) == 0) esc_before++;
+            }
+            put_u64(out + off_i + (coded ? 16 : 8) * t, before);
+            if (coded) put_u64(out + off_i + 16 * t + 8, esc_before);
+        }
+    }
     if (!coded) {
         for (uint64_t j = 0; j < m; j++) out[off_x + j] = exps[j];
     } else {
@@ -466,7 +505,7 @@ uint32_t orc_reuse_decode(const uint8_t* p, uint64_t avail, uint64_t n_s,
                           uint8_t* recv_cache, uint16_t* out)
 {
     if (avail < 64) return ORC_BAD_SIZE;
-    if (!(p[0] == 'E' && p[1] == 'Z' && p[2] == 'R' && p[3] == 'U') || p[4] != 1
+    if (!(p[0] == 'E' && p[1] == 'Z' && p[2] == 'R' && p[3] == 'U') || p[4] != 2
         || (p[5] & ~3u) != 0 || p[7] != 0 || get_u32(p + 8) != B
         || get_u32(p + 12) != shard_index || get_u64(p + 16) != n_s)
         return ORC_BAD_HEADER;
@@ -481,9 +520,12 @@ uint32_t orc_reuse_decode(const uint8_t* p, uint64_t avail, uint64_t n_s,
         return ORC_BAD_SIZE;
     uint64_t off_bm = 64;
     uint64_t off_sm = off_bm + round_up(ceil_div(nb, 8), 16);
-    uint64_t off_x = off_sm + round_up(n_s, 16);
+    uint64_t off_i = off_sm + round_up(n_s, 16);
+    uint64_t off_x = off_i + reuse_idx_bytes(n_s, coded);
     const uint8_t* bm = p + off_bm;
     const uint8_t* sm = p + off_sm;
+    const uint8_t* idx = p + off_i;
+    const uint64_t stride = coded ? 16 : 8;
     /* the bitmap must agree with the declared counts before anything is
      * written to the receiver's cache */
     uint64_t cnt = 0, len = 0;
@@ -498,10 +540,17 @@ uint32_t orc_reuse_decode(const uint8_t* p, uint64_t avail, uint64_t n_s,
     uint32_t status = 0;
     uint64_t plane = round_up(ceil_div(m, 8), 16);
     const uint8_t* esc = p + off_x + 3 * plane;
-    uint64_t j = 0, k_esc = 0;
+    uint64_t j = 0, k_esc = 0, blocks_before = 0;
     for (uint64_t k = 0; k < nb; k++) {
         uint64_t a = k * B, b = (k + 1) * B < n_s ? (k + 1) * B : n_s;
         int ch = (bm[k / 8] >> (k % 8)) & 1u;
+        /* the index must hold the changed blocks (and escapes) before */
+        if (a % IDX_SPAN == 0) {
+            const uint8_t* e = idx + stride * (a / IDX_SPAN);
+            if (get_u64(e) != blocks_before || (coded && get_u64(e + 8) != k_esc))
+                status |= ORC_BAD_COUNT;
+        }
+        blocks_before += (uint64_t)ch;
         for (uint64_t i = a; i < b; i++) {
             if (ch) {
                 unsigned E;

@@ -51,7 +51,7 @@ def test_plan_validation(B):
         with pytest.raises(E) as ei:
             B.ez_plan_create(1000, 2, bb, B.EZ_CODEC_REUSE)
         assert ei.value.status == B.EZ_ERR_UNSUPPORTED
-    assert B.ez_version() == 0x000100
+    assert B.ez_version() == 0x000200
     assert B.status_str(0) == "ok"
 
 

@@ -63,7 +63,7 @@ def check_sizes(c, res, B):
     sizes = c.sizes.cpu().tolist()
     for r, (ns, nc, m) in enumerate(res):
         nb = cdiv(ns, B)
-        raw = rup(64 + rup(cdiv(nb, 8), 16) + rup(ns, 16) + m, 128)
+        raw = rup(64 + rup(cdiv(nb, 8), 16) + rup(ns, 16) + rup(8 * cdiv(ns, 8192), 16) + m, 128)
         assert sizes[r] == raw, (r, sizes[r], raw)
 
 

@@ -131,7 +131,7 @@ def test_all_patterns_coded_and_raw(ez, orc):
 
 def _payload_cases(pay: np.ndarray):
     cases = [("magic", lambda b: b.__setitem__(0, b[0] ^ 1), None),
-             ("version", lambda b: b.__setitem__(4, 2), None),
+             ("version", lambda b: b.__setitem__(4, 1), None),
              ("shard", lambda b: b.__setitem__(12, 3), None),
              ("total", lambda b: b.__setitem__(48, b[48] ^ 0x80), None),
              ("bitmap", lambda b: b.__setitem__(64, b[64] ^ 1), None),

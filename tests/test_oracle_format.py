@@ -33,16 +33,22 @@ def exps(x):
 
 
 def load_examples():
+    """Scalar rows by key; image rows (<name>_fill off len hex, <name>_bytes
+    off hex...) by image name, in file order."""
     rows = {}
-    byte_rows = {"code3_bytes": [], "reuse_bytes": []}
+    byte_rows = {}
     with open(os.path.join(HERE, "golden", "format_examples.txt")) as f:
         for line in f:
             line = line.split("#")[0].strip()
             if not line:
                 continue
             key, *vals = line.split()
-            if key in byte_rows:
-                byte_rows[key].append((int(vals[0]), bytes(int(v, 16) for v in vals[1:])))
+            if key.endswith("_bytes"):
+                byte_rows.setdefault(key[:-6], []).append(
+                    (int(vals[0]), bytes(int(v, 16) for v in vals[1:])))
+            elif key.endswith("_fill"):
+                byte_rows.setdefault(key[:-5], []).append(
+                    (int(vals[0]), bytes([int(vals[2], 16)]) * int(vals[1])))
             else:
                 rows[key] = vals
     return rows, byte_rows
@@ -55,6 +61,14 @@ def expected_image(total, byte_rows):
     return bytes(img)
 
 
+def multi_input(rows):
+    x = np.full(int(rows["multi_n"][0]), 0x3C00, dtype=np.uint16)
+    for item in rows["multi_special"]:
+        j, bits = item.split(":")
+        x[int(j)] = int(bits, 16)
+    return x
+
+
 def test_code3_golden_example(orc):
     rows, byte_rows = load_examples()
     x = np.array([int(v, 16) for v in rows["input"]], dtype=np.uint16)
@@ -62,7 +76,7 @@ def test_code3_golden_example(orc):
     slots, sizes, slot = orc.code3_encode(x, 1, E0)
     total = int(rows["code3_total"][0])
     assert int(sizes[0]) == total
-    assert bytes(slots[:total]) == expected_image(total, byte_rows["code3_bytes"])
+    assert bytes(slots[:total]) == expected_image(total, byte_rows["code3"])
     out, st = orc.code3_decode(slots, np.array([0, slot], np.uint64), x.size, 1)
     assert st == 0 and np.array_equal(out, x)
 
@@ -77,10 +91,57 @@ def test_reuse_golden_example(orc):
     pay, _ = orc.reuse_encode(x, B, 0, cache)
     total = int(rows["reuse_total"][0])
     assert pay.size == total
-    assert bytes(pay) == expected_image(total, byte_rows["reuse_bytes"])
+    assert bytes(pay) == expected_image(total, byte_rows["reuse"])
     assert np.array_equal(cache, exps(x))
     out, st = orc.reuse_decode(pay, x.size, B, 0, recv_cache)
     assert st == 0 and np.array_equal(out, x) and np.array_equal(recv_cache, exps(x))
+
+
+def test_code3_golden_index_example(orc):
+    """Three 8192-value index entries, worked by hand."""
+    rows, byte_rows = load_examples()
+    x = multi_input(rows)
+    slots, sizes, slot = orc.code3_encode(x, 1, int(rows["code3m_E0"][0]))
+    total = int(rows["code3m_total"][0])
+    assert int(sizes[0]) == total
+    assert bytes(slots[:total]) == expected_image(total, byte_rows["code3m"])
+    out, st = orc.code3_decode(slots, np.array([0, slot], np.uint64), x.size, 1)
+    assert st == 0 and np.array_equal(out, x)
+
+
+def test_reuse_golden_index_example(orc):
+    rows, byte_rows = load_examples()
+    x = np.full(int(rows["multi_n"][0]), 0x3C00, dtype=np.uint16)
+    B = int(rows["reuse" + "m_B"][0])
+    cache = exps(x).copy()
+    cache[[int(v) for v in rows["reusem_prev0"]]] = 0
+    recv_cache = cache.copy()
+    pay, _ = orc.reuse_encode(x, B, 0, cache)
+    total = int(rows["reusem_total"][0])
+    assert pay.size == total
+    assert bytes(pay) == expected_image(total, byte_rows["reusem"])
+    out, st = orc.reuse_decode(pay, x.size, B, 0, recv_cache)
+    assert st == 0 and np.array_equal(out, x) and np.array_equal(recv_cache, exps(x))
+
+
+def test_index_entries_are_checked(orc):
+    """A decoder that finds an index entry different from the count it
+    derives itself reports a count error (code3 and reuse)."""
+    rows, _ = load_examples()
+    x = multi_input(rows)
+    slots, sizes, slot = orc.code3_encode(x, 1, 120)
+    bad = slots.copy()
+    bad[23168 + 8] ^= 1
+    _, st = orc.code3_decode(bad, np.array([0, slot], np.uint64), x.size, 1)
+    assert st == orc.BAD_COUNT
+    y = np.full(x.size, 0x3C00, dtype=np.uint16)
+    cache = exps(y).copy()
+    cache[[3, 8190]] = 0
+    pay, _ = orc.reuse_encode(y, 8, 0, cache.copy())
+    bad = pay.copy()
+    bad[16736 + 16] ^= 1
+    _, st = orc.reuse_decode(bad, y.size, 8, 0, cache.copy())
+    assert st == orc.BAD_COUNT
 
 
 @pytest.mark.parametrize("W", [1, 3, 8])
@@ -132,7 +193,7 @@ def test_reuse_all_patterns(orc, B, coded):
     for r in range(W):
         n_r = orc.shard_count(n, W, r)
         nb = cdiv(n_r, B)
-        raw = 64 + rup(cdiv(nb, 8), 16) + rup(n_r, 16) + n_r
+        raw = 64 + rup(cdiv(nb, 8), 16) + rup(n_r, 16) + rup(8 * cdiv(n_r, 8192), 16) + n_r
         if not coded:
             assert int(sizes[r]) == rup(raw, 128)
     # warm: another permutation of all patterns
@@ -153,7 +214,8 @@ def test_unchanged_iteration_sends_no_exponents(orc):
     hdr = pay[:64]
     assert int(hdr[24:32].view(np.uint64)[0]) == 0          # n_changed
     nb = cdiv(5000, 64)
-    assert pay.size == rup(64 + rup(cdiv(nb, 8), 16) + rup(5000, 16), 128)
+    assert pay.size == rup(64 + rup(cdiv(nb, 8), 16) + rup(5000, 16) + rup(8 * cdiv(5000, 8192), 16),
+                           128)
 
 
 def test_composed_matches_code3_of_exp_stream(orc):
@@ -173,7 +235,8 @@ def test_composed_matches_code3_of_exp_stream(orc):
     assert st["E0"] == orc.stats(x1)["E0"]
     m = int(raw[32:40].view(np.uint64)[0])
     nb = cdiv(x1.size, B)
-    off_x = 64 + rup(cdiv(nb, 8), 16) + rup(x1.size, 16)
+    off_x = 64 + rup(cdiv(nb, 8), 16) + rup(x1.size, 16) + rup(8 * cdiv(x1.size, 8192), 16)
+    off_c = 64 + rup(cdiv(nb, 8), 16) + rup(x1.size, 16) + rup(16 * cdiv(x1.size, 8192), 16)
     stream = raw[off_x:off_x + m]
     # a BF16 tensor whose exponents are the stream (sign+mantissa zero)
     xs = (stream.astype(np.uint16) << 7)
@@ -182,13 +245,14 @@ def test_composed_matches_code3_of_exp_stream(orc):
     p128 = rup(cdiv(m, 8), 128)
     base3 = 128 + rup(m, 128)
     for p in range(3):
-        got = cod[off_x + p * plane:off_x + p * plane + (m + 7) // 8]
+        got = cod[off_c + p * plane:off_c + p * plane + (m + 7) // 8]
         want = slots[base3 + p * p128:base3 + p * p128 + (m + 7) // 8]
         assert np.array_equal(got, want)
     n_esc = int(cod[40:48].view(np.uint64)[0])
     assert n_esc == int(slots[16:24].view(np.uint64)[0])
-    esc_c3 = slots[base3 + 3 * p128:base3 + 3 * p128 + n_esc]
-    assert np.array_equal(cod[off_x + 3 * plane:off_x + 3 * plane + n_esc], esc_c3)
+    esc3 = base3 + 3 * p128 + rup(8 * cdiv(m, 8192), 128)
+    esc_c3 = slots[esc3:esc3 + n_esc]
+    assert np.array_equal(cod[off_c + 3 * plane:off_c + 3 * plane + n_esc], esc_c3)
     # and both decode to x1
     r1 = exps(x0).copy()
     r2 = exps(x0).copy()

@@ -58,7 +58,8 @@ def test_bruteforce_all_subsets(orc, n, B):
                 for k in range(nb)]
         assert bitmap_bits(pay, nb) == want
         changed_len = sum(min((k + 1) * B, n) - k * B for k in range(nb) if want[k])
-        assert pay.size == rup(64 + rup(cdiv(nb, 8), 16) + rup(n, 16) + changed_len, 128)
+        assert pay.size == rup(64 + rup(cdiv(nb, 8), 16) + rup(n, 16) + rup(8 * cdiv(n, 8192), 16)
+                               + changed_len, 128)
         assert np.array_equal(send, exps(cur))
         out, st = orc.reuse_decode(pay, n, B, 0, recv)
         assert st == 0 and np.array_equal(out, cur) and np.array_equal(recv, exps(cur))
@@ -151,7 +152,7 @@ def test_corrupt_reuse_payloads(orc, coded):
     assert st == 0 and np.array_equal(ok, cur)
     cases = []
     bad = pay.copy(); bad[0] ^= 1; cases.append((bad, None, orc.BAD_HEADER))
-    bad = pay.copy(); bad[4] = 2; cases.append((bad, None, orc.BAD_HEADER))
+    bad = pay.copy(); bad[4] = 1; cases.append((bad, None, orc.BAD_HEADER))
     bad = pay.copy(); bad[12] = 3; cases.append((bad, None, orc.BAD_HEADER))
     bad = pay.copy(); cases.append((bad, pay.size - 128, orc.BAD_SIZE))   # truncated
     bad = pay.copy(); bad[48] ^= 0x80; cases.append((bad, None, orc.BAD_SIZE))
