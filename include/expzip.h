@@ -210,34 +210,33 @@ ez_status ez_gather_decode(ez_plan p, const uint8_t* d_recv, const uint64_t* d_o
                            void* d_ws, uint64_t ws_bytes, void* stream);
 
 /* Bytes of the library's fixed device scratch array used by
- * ez_gather_decode_noalloc (one array per device). */
+ * ez_encode_code3_noalloc (one array per device). */
 #define EZ_NOALLOC_SCRATCH_BYTES (4u * 1024u * 1024u)
 
-/* ez_gather_decode without a caller workspace: the same decode and the same
- * results, with its scratch (tile counters and look-back state) taken from a
- * fixed array inside the library instead of d_ws.  No counterpart in the
- * papers: it exists for callers that cannot allocate device memory at the
- * point where they decode -- a communication runtime's progress path or a
- * non-blocking host thread, where cudaMalloc/cudaFree could synchronize the
- * device and stall against communication kernels still waiting on peers,
- * or an application whose memory belongs to a pooling allocator.  The call
- * allocates nothing (no cudaMalloc, no cudaFree, no allocating library).
- * Limit: the plan's decode scratch -- about 8 bytes per 8192 values (16 for
- * the reuse codecs) plus per-shard records of 64 B, and for
- * EZ_CODEC_REUSE_CODE3 about 4.4 KB more per shard -- must fit in
- * EZ_NOALLOC_SCRATCH_BYTES, else EZ_ERR_CAPACITY and nothing is launched
- * (4 MiB covers e.g. 2^31 values with code3, or 2^30 with a reuse codec,
- * in 8 shards).
+/* ez_encode_code3 without a caller workspace: the same encode and the same
+ * results, with its scratch (tile counters, per-chunk tile counters and
+ * look-back state) taken from a fixed array inside the library instead of
+ * d_ws.  No counterpart in the papers: it exists for callers that cannot
+ * allocate device memory at the point where they compress -- a
+ * communication runtime's send path or a non-blocking host thread, where
+ * cudaMalloc/cudaFree could synchronize the device and stall against
+ * communication kernels still waiting on peers, or an application whose
+ * memory belongs to a pooling allocator.  The call allocates nothing (no
+ * cudaMalloc, no cudaFree, no allocating library).
+ * Limit: the plan's encode scratch -- 8 bytes per 8192 values of the
+ * encoded chunks plus about 3.5 KB of counters and records for 8 chunks --
+ * must fit in EZ_NOALLOC_SCRATCH_BYTES, else EZ_ERR_CAPACITY and nothing is
+ * launched (4 MiB covers e.g. 2^31 values in 8 chunks).
  * The first call on a device, with that device current, looks up the
  * array's device address (cudaGetSymbolAddress); make that first call before
  * any stream capture.  Each call clears the scratch it needs on `stream`
  * before its launch; every call on a device shares the one array, so calls
  * whose work overlaps on the GPU (unordered streams) race and must not be
  * issued.  Devices with ordinal >= 64 give EZ_ERR_UNSUPPORTED.  Arguments
- * and device status bits as ez_gather_decode. */
-ez_status ez_gather_decode_noalloc(ez_plan p, const uint8_t* d_recv, const uint64_t* d_offsets,
-                                   uint8_t* d_recv_cache, uint16_t* d_full_out,
-                                   uint32_t* d_status, void* stream);
+ * and device status bits as ez_encode_code3. */
+ez_status ez_encode_code3_noalloc(ez_plan p, const uint16_t* d_x, uint32_t first, uint32_t count,
+                                  const ez_stats_t* d_stats, uint8_t* d_out, uint64_t out_bytes,
+                                  uint64_t* d_sizes, uint32_t* d_status, void* stream);
 
 /* Static text for a status code. */
 const char* ez_status_str(ez_status s);

@@ -26,7 +26,7 @@ NOALLOC_SCRATCH_BYTES = 4 << 20   # EZ_NOALLOC_SCRATCH_BYTES
 
 ENTRY_POINTS = ("ez_plan_create", "ez_plan_destroy", "ez_plan_sizes", "ez_stats",
                 "ez_encode_code3", "ez_decode_code3", "ez_encode_reuse", "ez_decode_reuse",
-                "ez_gather_decode", "ez_gather_decode_noalloc", "ez_status_str", "ez_version")
+                "ez_gather_decode", "ez_encode_code3_noalloc", "ez_status_str", "ez_version")
 
 
 class EzError(RuntimeError):
@@ -67,7 +67,7 @@ def lib():
             "ez_encode_reuse": [vp, vp, u32, u32, vp, i32, vp, u64, vp, vp, vp, vp, u64, vp],
             "ez_decode_reuse": [vp, vp, u64, u32, vp, vp, vp, vp, u64, vp],
             "ez_gather_decode": [vp, vp, vp, vp, vp, vp, vp, u64, vp],
-            "ez_gather_decode_noalloc": [vp, vp, vp, vp, vp, vp, vp],
+            "ez_encode_code3_noalloc": [vp, vp, u32, u32, vp, vp, u64, vp, vp, vp],
         }
         for name, args in sig.items():
             f = getattr(L, name)
@@ -169,11 +169,11 @@ def ez_gather_decode(plan, recv, offsets, recv_cache, full_out, status, ws, ws_b
                                                       _stream(stream)))
 
 
-def ez_gather_decode_noalloc(plan, recv, offsets, recv_cache, full_out, status,
-                             stream=None) -> None:
-    _check("ez_gather_decode_noalloc",
-           lib().ez_gather_decode_noalloc(plan, _ptr(recv), _ptr(offsets), _ptr(recv_cache),
-                                          _ptr(full_out), _ptr(status), _stream(stream)))
+def ez_encode_code3_noalloc(plan, x, first: int, count: int, stats, out, out_bytes: int, sizes,
+                            status, stream=None) -> None:
+    _check("ez_encode_code3_noalloc",
+           lib().ez_encode_code3_noalloc(plan, _ptr(x), first, count, _ptr(stats), _ptr(out),
+                                         out_bytes, _ptr(sizes), _ptr(status), _stream(stream)))
 
 
 def ez_version() -> int:

@@ -1,20 +1,21 @@
-// k_noalloc.cu -- gather-decode whose scratch memory is a fixed device array
+// k_noalloc.cu -- code3 encode whose scratch memory is a fixed device array
 // of this library, so that the call allocates nothing.
 //
-// Who needs it: a caller that decodes received payloads from inside a
-// communication runtime's progress path, a host thread that must not block,
-// or an application whose device memory is owned by a pooling allocator it
-// cannot call into.  cudaMalloc and cudaFree may synchronize the whole device
-// and take driver locks, which can stall or deadlock against communication
-// kernels that are still waiting on peers; and a pooled application has no
-// raw cudaMalloc budget to spare.  Such a caller cannot hand the ordinary
-// gather-decode a workspace, so this variant uses the array below instead.
+// Who needs it: a caller that compresses on a communication runtime's send
+// path, from a host thread that must not block, or inside an application
+// whose device memory is owned by a pooling allocator it cannot call into.
+// cudaMalloc and cudaFree may synchronize the whole device and take driver
+// locks, which can stall or deadlock against communication kernels that are
+// still waiting on peers; and a pooled application has no raw cudaMalloc
+// budget to spare.  Such a caller cannot hand the ordinary encoder a
+// workspace, so this variant uses the array below instead.
 //
 // The array is shared by every call on a device and keeps the previous
 // call's contents; each call clears the part that must start at zero (tile
-// counters and look-back state) on its own stream before the launch.  Two
-// calls on one device whose work overlaps on the GPU (different streams, no
-// ordering between them) race on the array and give undefined results.
+// counters, per-chunk tile counters and look-back state) on its own stream
+// before the launch.  Two calls on one device whose work overlaps on the GPU
+// (different streams, no ordering between them) race on the array and give
+// undefined results.
 #include <atomic>
 #include <cstdint>
 #include <mutex>
@@ -32,13 +33,11 @@ std::mutex g_setup_mutex;
 
 bool al(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
-// Bytes of scratch the gather-decode of plan p touches: the zeroed prefix of
-// the plan's workspace up to the end of the look-back state it uses.  The
-// later regions (encoder-only exponent buffer) are never read by a decoder.
-uint64_t scratch_needed(const ez_plan_s* p)
+// Bytes of scratch a code3 encode of `count` chunks touches: the plan's
+// workspace prefix up to the end of the look-back state of those chunks.
+uint64_t scratch_needed(const ez_plan_s* p, uint32_t count)
 {
-    const uint64_t state = (uint64_t)p->W * p->tpc * 8;
-    return p->codec == EZ_CODEC_CODE3 ? p->off_state_a + state : p->off_state_b + state;
+    return p->off_state_a + (uint64_t)count * p->tpc * 8;
 }
 
 // Device address of this device's array; looked up once per device, with
@@ -61,19 +60,19 @@ ez_status scratch_of(int dev, void** out)
 
 }  // namespace
 
-extern "C" ez_status ez_gather_decode_noalloc(ez_plan p, const uint8_t* d_recv,
-                                              const uint64_t* d_offsets, uint8_t* d_recv_cache,
-                                              uint16_t* d_full_out, uint32_t* d_status,
-                                              void* stream)
+extern "C" ez_status ez_encode_code3_noalloc(ez_plan p, const uint16_t* d_x, uint32_t first,
+                                             uint32_t count, const ez_stats_t* d_stats,
+                                             uint8_t* d_out, uint64_t out_bytes,
+                                             uint64_t* d_sizes, uint32_t* d_status, void* stream)
 {
-    if (!p) return EZ_ERR_ARG;
-    if (!d_recv || !al(d_recv, 16) || !d_offsets || !al(d_offsets, 8) || !d_status ||
-        !al(d_status, 4))
+    if (!p || p->codec != EZ_CODEC_CODE3) return EZ_ERR_ARG;
+    if (count == 0 || first >= p->W || count > p->W - first) return EZ_ERR_ARG;
+    if (!d_stats || !al(d_stats, 8) || !d_out || !al(d_out, 16) || !d_sizes || !al(d_sizes, 8) ||
+        !d_status || !al(d_status, 4))
         return EZ_ERR_ARG;
-    const bool reuse = p->codec != EZ_CODEC_CODE3;
-    if (p->n && (!d_full_out || !al(d_full_out, 16))) return EZ_ERR_ARG;
-    if (reuse && p->n && (!d_recv_cache || !al(d_recv_cache, 16))) return EZ_ERR_ARG;
-    const uint64_t need = scratch_needed(p);
+    if (p->n && (!d_x || !al(d_x, 16))) return EZ_ERR_ARG;
+    if (out_bytes / p->slot_bytes < count) return EZ_ERR_CAPACITY;
+    const uint64_t need = scratch_needed(p, count);
     if (need > (uint64_t)EZ_NOALLOC_SCRATCH_BYTES) return EZ_ERR_CAPACITY;
 
     int dev = -1;
@@ -85,11 +84,7 @@ extern "C" ez_status ez_gather_decode_noalloc(ez_plan p, const uint8_t* d_recv,
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (cudaMemsetAsync(ws, 0, need, st) != cudaSuccess) return EZ_ERR_CUDA;
-    const ezk::WsView w = ezk::ws_view(p, ws);
-    const cudaError_t e =
-        reuse ? ezk::launch_reuse_decode(p, d_recv, d_offsets, 0, 0, p->W, d_recv_cache,
-                                         d_full_out, d_status, w, st)
-              : ezk::launch_code3_decode(p, d_recv, d_offsets, 0, p->W, d_full_out, d_status, w,
-                                         st);
+    const cudaError_t e = ezk::launch_code3_encode(p, d_x, first, count, d_stats, d_out, d_sizes,
+                                                   d_status, ezk::ws_view(p, ws), st);
     return e == cudaSuccess ? EZ_OK : EZ_ERR_CUDA;
 }

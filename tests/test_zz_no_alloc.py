@@ -1,10 +1,10 @@
-"""ez_gather_decode_noalloc: the gather-decode whose scratch is the library's
+"""ez_encode_code3_noalloc: the code3 encode whose scratch is the library's
 fixed device array instead of a caller workspace.
 
-On the GPU it must give the same decoded tensor, receiver cache and status as
-ez_gather_decode on the same payloads, for two calls in a row whose inputs
+On the GPU it must give the same payload bytes, sizes and status as
+ez_encode_code3 on the same input, for two calls in a row whose inputs
 differ (the second call runs on scratch the first one left behind).  On the
-host, plans whose decode scratch exceeds the array are rejected before any
+host, plans whose encode scratch exceeds the array are rejected before any
 CUDA call.  This file is collected last so that its first call may come
 either in a fresh process or after every other test."""
 import pytest
@@ -21,60 +21,37 @@ def ez():
     return binding, codec
 
 
-def payloads(c, xs, reuse):
-    """Encode each tensor with the workspace entry points (the first one
-    cold) and lay its payloads out as an allgather would deliver them."""
-    out = []
-    for it, x in enumerate(xs):
-        if reuse:
-            c.encode_reuse(x, cold=it == 0)
-        else:
-            c.stats(x)
-            c.encode_code3(x)
-        torch.cuda.synchronize()
-        assert c.status_word() == 0
-        out.append(c.exchange())
-    return out
-
-
 @pytest.mark.gpu
-@pytest.mark.parametrize("codec_id", [1, 2, 3])
-@pytest.mark.parametrize("n,W,B", [(200_003, 4, 64), ((1 << 22) + 77, 8, 256)])
-def test_noalloc_matches_workspace_gather(ez, codec_id, n, W, B):
+@pytest.mark.parametrize("n,W", [(200_003, 4), ((1 << 22) + 77, 8), (40_000, 1)])
+def test_noalloc_matches_workspace_encode(ez, n, W):
     binding, codec = ez
-    reuse = codec_id != binding.EZ_CODEC_CODE3
-    c = codec.Codec(n, W, B if reuse else 0, codec_id)
+    c = codec.Codec(n, W)
     x0 = synth.config2(n, device="cuda")
     x1 = synth.scale_drift_bench(x0, 1, rate=0.01)
-    got = payloads(c, [x0, x1], reuse)
-
-    def fresh():
-        return torch.zeros(max(n, 8), dtype=torch.uint8, device="cuda") if reuse else None
-
-    # expected: the workspace gather-decode, iteration by iteration
-    ref_cache = fresh()
-    ref_out = []
-    for recv, offs in got:
-        o = torch.full((n,), -1, dtype=torch.int16, device="cuda")
+    # expected: the workspace encoder, one input after the other
+    ref = []
+    for x in (x0, x1):
+        c.stats(x)
         c.clear_status()
-        c.gather_decode(recv, offs, ref_cache, o)
+        c.out.zero_()
+        c.encode_code3(x)
         torch.cuda.synchronize()
         assert c.status_word() == 0
-        ref_out.append(o)
-    assert torch.equal(ref_out[0], x0) and torch.equal(ref_out[1], x1)
-
+        st = c.stats_buf[:binding.STATS_BYTES].clone()
+        ref.append((c.out.clone(), c.sizes.clone(), st))
     # the no-alloc entry point: two calls in a row, no synchronisation between
-    cache = fresh()
+    outs = [torch.zeros_like(c.out) for _ in ref]
+    sizes = [torch.zeros_like(c.sizes) for _ in ref]
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
-    outs = [torch.full((n,), -1, dtype=torch.int16, device="cuda") for _ in got]
-    for (recv, offs), o in zip(got, outs):
-        binding.ez_gather_decode_noalloc(c.plan, recv, offs, cache, o, status)
+    for (o_ref, s_ref, st), o, sz, x in zip(ref, outs, sizes, (x0, x1)):
+        binding.ez_encode_code3_noalloc(c.plan, x, 0, W, st, o, o.numel(), sz, status)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
-    for o, r in zip(outs, ref_out):
-        assert torch.equal(o, r)
-    if reuse:
-        assert torch.equal(cache, ref_cache)
+    for (o_ref, s_ref, _), o, sz in zip(ref, outs, sizes):
+        assert torch.equal(sz, s_ref)
+        for r in range(W):
+            k = int(s_ref[r].item())
+            assert torch.equal(o[r * c.slot:r * c.slot + k], o_ref[r * c.slot:r * c.slot + k])
 
 
 def test_noalloc_rejects_oversized_plans(ez):
@@ -83,20 +60,22 @@ def test_noalloc_rejects_oversized_plans(ez):
     dereferenced on that path (this test runs without a GPU)."""
     binding, _ = ez
     fake = 1 << 20
-    for n, W, B, cid in [(1 << 40, 8, 0, 1),            # 1 GiB of look-back state
-                         (1 << 31, 8, 256, 2),          # two 2 MiB state arrays
-                         (1 << 20, 65536, 64, 3)]:      # per-shard records
-        plan = binding.ez_plan_create(n, W, B, cid)
+    for n, W in [(1 << 40, 8),          # 1 GiB of look-back state
+                 (1 << 33, 1),          # one chunk of 2^33 values: 8 MiB
+                 (1 << 20, 65536)]:     # per-chunk counters and records
+        plan = binding.ez_plan_create(n, W, 0, binding.EZ_CODEC_CODE3)
         try:
+            slot = binding.ez_plan_sizes(plan)["slot_bytes"]
             with pytest.raises(binding.EzError) as ei:
-                binding.ez_gather_decode_noalloc(plan, fake, fake, fake, fake, fake, 0)
+                binding.ez_encode_code3_noalloc(plan, fake, 0, W, fake, fake, slot * W, fake,
+                                                fake, 0)
             assert ei.value.status == binding.EZ_ERR_CAPACITY
         finally:
             binding.ez_plan_destroy(plan)
-    plan = binding.ez_plan_create(1000, 2, 0, 1)
+    plan = binding.ez_plan_create(1000, 2, 0, binding.EZ_CODEC_CODE3)
     try:
         with pytest.raises(binding.EzError) as ei:
-            binding.ez_gather_decode_noalloc(plan, None, fake, None, fake, fake, 0)
+            binding.ez_encode_code3_noalloc(plan, fake, 0, 2, None, fake, 1 << 30, fake, fake, 0)
         assert ei.value.status == binding.EZ_ERR_ARG
     finally:
         binding.ez_plan_destroy(plan)
