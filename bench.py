@@ -161,6 +161,22 @@ def make_chain(count: int):
     return xs
 
 
+def measured_traffic(op):
+    """DRAM bytes (read + write) of one call of `op`, from the committed ncu
+    summary of this workload; None when no capture of the current kernels
+    exists."""
+    path = os.path.join(ROOT, "profiles", "traffic_bench_64M_w8.json")
+    try:
+        with open(path) as f:
+            t = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if t.get("workload") != WORKLOAD:
+        return None
+    e = t.get("ops", {}).get(op)
+    return int(e["dram_bytes"]) if e else None
+
+
 def run_ours(args, world, rank, local):
     from lossless_bf16_exponent_codec_gb300 import binding as Bd
     from lossless_bf16_exponent_codec_gb300 import build
@@ -260,7 +276,7 @@ def run_ours(args, world, rank, local):
     ach = alg[ops[top]] / (op_ms[top] * 1e-3) / 1e9
     roof = {"bound": "hbm", "kernel": ops[top], "achieved": round(ach, 1), "peak": peak,
             "peak_source": peak_src, "unit": "GB/s", "frac": round(ach / peak, 3),
-            "traffic": None}
+            "traffic": measured_traffic(ops[top])}
     ratios = {k: round(raw / v, 4) for k, v in sz.items()}
 
     def g(name):
