@@ -45,6 +45,11 @@ WsView ws_view(const ez_plan_s* p, void* ws);
 cudaError_t launch_stats(const ez_plan_s* p, const uint16_t* x, uint64_t n, ez_stats_t* out,
                          const WsView& w, cudaStream_t s);
 
+// Statistics of shards [first, first+count) of the plan (values at x + i*L),
+// one record per shard.
+cudaError_t launch_shard_stats(const ez_plan_s* p, const uint16_t* x, uint32_t first, uint32_t count,
+                               ez_stats_t* out, const WsView& w, cudaStream_t s);
+
 cudaError_t launch_code3_encode(const ez_plan_s* p, const uint16_t* x, uint32_t first,
                                 uint32_t count, const ez_stats_t* st, uint8_t* out,
                                 uint64_t* sizes, uint32_t* dstatus, const WsView& w,

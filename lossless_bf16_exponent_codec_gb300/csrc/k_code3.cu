@@ -391,7 +391,7 @@ __device__ __forceinline__ uint4 ld_v4_plain(const void* p)
 // checked against the tile's own escape count (entry 0 must be 0, each entry
 // plus the tile's count must equal the next entry, the last one n_esc), so
 // the escapes read are always inside the escape section.
-__global__ void __launch_bounds__(kThreads) k_code3_decode(C3Dec a)
+__global__ void __launch_bounds__(kThreads, 6) k_code3_decode(C3Dec a)
 {
     __shared__ uint32_t s_bad, s_E0;
     __shared__ unsigned long long s_nesc;

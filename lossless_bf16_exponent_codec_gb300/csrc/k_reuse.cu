@@ -15,9 +15,10 @@
 //
 // Coded variant (EZ_CODEC_REUSE_CODE3): the changed exponents are coded with
 // the 3-bit code of ZipCCL (research digest 3.1) instead of nvCOMP's ANS,
-// whose window comes from the shard's sigma, accumulated in the same pass.
-// Pass 1 stages the raw exponent stream in the workspace; pass 2
-// (k_reuse_code3) codes it into planes + escapes inside the payload.
+// whose window comes from the shard's sigma (k_stats over each shard, a
+// launch of its own).  Pass 1 stages the raw exponent stream in the
+// workspace; pass 2 (k_reuse_code3) codes it into planes + escapes inside the
+// payload.
 //
 // Receiver (k_reuse_decode): for W payloads in one launch, each tile reads
 // its slice of the bitmap, looks back for the changed-block prefix, takes
@@ -222,7 +223,6 @@ __global__ void __launch_bounds__(kThreads, 4) k_reuse_encode(RuEnc a)
     __shared__ uint32_t s_gl[32], s_bm[32], s_pre[32];
     __shared__ uint32_t s_agg;
     __shared__ unsigned long long s_prefix;
-    extern __shared__ __align__(16) unsigned char dyn[];
     const int t = threadIdx.x, lane = t & 31, wid = t >> 5;
     if (t < 32) {
         s_gl[t] = 0;
@@ -253,8 +253,6 @@ __global__ void __launch_bounds__(kThreads, 4) k_reuse_encode(RuEnc a)
         cv[g] = (v < nv && !a.cold) ? ld_group8(ct, v, nv) : 0ull;
     }
 
-    StatsSmem* S = reinterpret_cast<StatsSmem*>(dyn);
-    if (kCoded) st_begin(*S, (8u * (uint32_t)t < nv) ? (w[0].x & 0xFFFFu) : 0xFFFFFFFFu);
 
     unsigned long long e8[kGroups];
 #pragma unroll
@@ -272,17 +270,6 @@ __global__ void __launch_bounds__(kThreads, 4) k_reuse_encode(RuEnc a)
             const unsigned long long smw = (unsigned long long)sm4_of(w[g].z, w[g].w) << 32 |
                                            sm4_of(w[g].x, w[g].y);
             st_group8(o + off_sm + v0, v, nv, smw);
-        }
-        if (kCoded && vm) {
-            const uint32_t elo = S->elo;
-            if (vm == 0xFFu) {
-                const uint32_t ws[4] = {w[g].x, w[g].y, w[g].z, w[g].w};
-#pragma unroll
-                for (int q = 0; q < 4; q++) st_add2(ws[q], st_bias2(elo), elo, *S);
-            } else {
-                for (int i = 0; i < 8; i++)
-                    if ((vm >> i) & 1u) st_add(half_of(w[g], i), elo, *S);
-            }
         }
     }
     __syncthreads();
@@ -317,9 +304,6 @@ __global__ void __launch_bounds__(kThreads, 4) k_reuse_encode(RuEnc a)
         st_group8(ct, v, nv, e8[g]);
     }
 
-    if (kCoded) {
-        if (st_end(*S, a.bins + ci, a.tpc)) st_finalize(a.bins + ci, n_s, a.K, a.stats + ci, *S);
-    }
 
     if (lt == fin_tile) {
         const uint64_t n_changed = P + agg;
@@ -493,7 +477,7 @@ __device__ __forceinline__ uint4 ld16_plain(const void* p) { return *reinterpret
 // reads the payload offsets, then the bitmap slice, sign+mantissa bytes and
 // index entries are loaded before thread 0's header checks complete.
 template <bool kCoded>
-__global__ void __launch_bounds__(kThreads) k_reuse_decode(RuDec a)
+__global__ void __launch_bounds__(kThreads, 6) k_reuse_decode(RuDec a)
 {
     __shared__ uint32_t s_bad, s_E0;
     __shared__ unsigned long long s_hdr[4];   // n_changed, m, n_esc
@@ -769,11 +753,12 @@ cudaError_t launch_reuse_encode(const ez_plan_s* p, const uint16_t* x, uint32_t 
         k_reuse_encode<false><<<tiles, kThreads, 0, s>>>(a);
         return cudaGetLastError();
     }
-    static const cudaError_t attr = cudaFuncSetAttribute(
-        k_reuse_encode<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(StatsSmem));
-    if (attr != cudaSuccess) return attr;
-    k_reuse_encode<true><<<tiles, kThreads, sizeof(StatsSmem), s>>>(a);
-    cudaError_t e = cudaGetLastError();
+    // the shards' windows first (their own pass over the values), then the
+    // split and the staged exponent stream, then the code
+    cudaError_t e = launch_shard_stats(p, x, first, count, a.stats, w, s);
+    if (e != cudaSuccess) return e;
+    k_reuse_encode<true><<<tiles, kThreads, 0, s>>>(a);
+    e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     RuC3 b;
     b.out = out;

@@ -17,17 +17,22 @@ static_assert(sizeof(ez_stats_t) == 2120, "ez_stats_t layout");
 constexpr int kStatsLoads = 16;                             // 16-B loads per thread
 constexpr uint32_t kStatsTile = kThreads * kStatsLoads * 8;   // 32768 values
 
-// One CTA per tile of 32768 values, 6 resident CTAs per SM; every thread
-// keeps four 16-byte loads in flight and adds their 32 values to the CTA's
-// histogram.
+// One CTA per tile of 32768 values of one shard, 6 resident CTAs per SM;
+// every thread keeps four 16-byte loads in flight and adds their 32 values to
+// the CTA's histogram.  Shard ci = tile / tps holds values [ci*L, ci*L + n_s)
+// of x; its CTAs fold into bins G[ci], and the last of them writes out[ci].
+// The a1 statistics of a whole tensor are the case of one shard.
 __global__ void __launch_bounds__(kThreads, 6)
-k_stats(const uint16_t* __restrict__ x, uint64_t n, StatsBins* G, ez_stats_t* out, double K)
+k_stats(const uint16_t* __restrict__ x, uint64_t n, uint64_t L, uint32_t first, uint32_t W,
+        uint32_t tps, StatsBins* G, ez_stats_t* out, double K)
 {
     extern __shared__ __align__(16) unsigned char dyn[];
     StatsSmem& S = *reinterpret_cast<StatsSmem*>(dyn);
-    const uint64_t base = (uint64_t)blockIdx.x * kStatsTile;
-    const uint32_t nv = base < n ? (uint32_t)umin64(kStatsTile, n - base) : 0u;
-    const uint16_t* xt = x + base;
+    const uint32_t ci = blockIdx.x / tps, lt = blockIdx.x % tps;
+    const uint64_t n_s = W ? shard_values(n, L, first + ci) : n;
+    const uint64_t base = (uint64_t)lt * kStatsTile;
+    const uint32_t nv = base < n_s ? (uint32_t)umin64(kStatsTile, n_s - base) : 0u;
+    const uint16_t* xt = x + (uint64_t)ci * L + base;
     const int t = threadIdx.x;
     st_begin(S, (uint32_t)(8 * t) < nv ? (uint32_t)xt[8 * t] : 0xFFFFFFFFu);
     const uint32_t elo = S.elo;
@@ -63,20 +68,34 @@ k_stats(const uint16_t* __restrict__ x, uint64_t n, StatsBins* G, ez_stats_t* ou
             }
         }
     }
-    if (st_end(S, G, gridDim.x)) st_finalize(G, n, K, out, S);
+    if (st_end(S, G + ci, tps)) st_finalize(G + ci, n_s, K, out + ci, S);
+}
+
+static cudaError_t stats_launch(const uint16_t* x, uint64_t n, uint64_t L, uint32_t first,
+                                uint32_t W, uint32_t count, uint64_t per_shard, StatsBins* G,
+                                ez_stats_t* out, double K, cudaStream_t s)
+{
+    const uint64_t tps = per_shard ? cdiv(per_shard, kStatsTile) : 1;
+    const uint64_t tiles = tps * count;
+    if (tiles > 0x7fffffffull) return cudaErrorInvalidValue;
+    static const cudaError_t attr = cudaFuncSetAttribute(
+        k_stats, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(StatsSmem));
+    if (attr != cudaSuccess) return attr;
+    k_stats<<<(unsigned)tiles, kThreads, sizeof(StatsSmem), s>>>(x, n, L, first, W, (uint32_t)tps,
+                                                               G, out, K);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_stats(const ez_plan_s* p, const uint16_t* x, uint64_t n, ez_stats_t* out,
                          const WsView& w, cudaStream_t s)
 {
-    const uint64_t tiles = n ? cdiv(n, kStatsTile) : 1;
-    if (tiles > 0x7fffffffull) return cudaErrorInvalidValue;
-    static const cudaError_t attr = cudaFuncSetAttribute(
-        k_stats, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(StatsSmem));
-    if (attr != cudaSuccess) return attr;
-    k_stats<<<(unsigned)tiles, kThreads, sizeof(StatsSmem), s>>>(x, n, (StatsBins*)w.bins, out,
-                                                               p->K);
-    return cudaGetLastError();
+    return stats_launch(x, n, n, 0, 0, 1, n, (StatsBins*)w.bins, out, p->K, s);
+}
+
+cudaError_t launch_shard_stats(const ez_plan_s* p, const uint16_t* x, uint32_t first, uint32_t count,
+                               ez_stats_t* out, const WsView& w, cudaStream_t s)
+{
+    return stats_launch(x, p->n, p->L, first, p->W, count, p->L, (StatsBins*)w.bins, out, p->K, s);
 }
 
 }  // namespace ezk
