@@ -52,7 +52,6 @@ WsView ws_view(const ez_plan_s* p, void* ws)
     v.bins = b + p->off_bins;
     v.state_a = reinterpret_cast<unsigned long long*>(b + p->off_state_a);
     v.state_b = reinterpret_cast<unsigned long long*>(b + p->off_state_b);
-    v.expbuf = b + p->off_expbuf;
     return v;
 }
 
@@ -109,8 +108,6 @@ ez_status ez_plan_create(ez_plan* out, const ez_plan_desc* d)
     p->off_state_b = off;
     off = rup(off + (reuse ? W * tpc * 8 : 0), 256);
     p->zero_bytes = off;
-    p->off_expbuf = off;
-    off = rup(off + (coded ? W * L : 0), 256);
     p->ws_bytes = off;
     *out = p;
     return EZ_OK;

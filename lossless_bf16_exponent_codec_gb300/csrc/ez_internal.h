@@ -14,14 +14,14 @@ struct ez_plan_s {
     uint64_t slot_bytes;     // worst-case payload per shard
     double K;                // 16383 / (14 ln 2)
     // workspace layout (byte offsets); [0, zero_bytes) is cleared per call
-    uint64_t off_ctr, off_info, off_shard_stats, off_bins, off_state_a, off_state_b, off_expbuf;
+    uint64_t off_ctr, off_info, off_shard_stats, off_bins, off_state_a, off_state_b;
     uint64_t zero_bytes, ws_bytes;
     uint32_t n_bins;
 };
 
 namespace ezk {
 
-// Per-shard scratch record of the two-pass reuse+code3 encoder.
+// Per-shard totals of the reuse split, summed with atomics by its tiles.
 struct ShardInfo {
     unsigned long long m;          // exponents in the changed blocks
     unsigned long long n_changed;  // changed blocks
@@ -37,7 +37,6 @@ struct WsView {
     unsigned long long* state_a;
     unsigned long long* state_b;
     void* bins;                    // StatsBins[n_bins]
-    uint8_t* expbuf;               // W * L bytes (reuse+code3 only)
 };
 
 WsView ws_view(const ez_plan_s* p, void* ws);

@@ -45,26 +45,23 @@ struct RuEnc {
     unsigned long long* state;
     uint32_t* counter;
     uint32_t* abort;
-    // coded variant
-    uint8_t* expbuf;
-    ShardInfo* info;
-    StatsBins* bins;
-    ez_stats_t* stats;    // per shard record (caller's or workspace)
-    double K;
+    ShardInfo* info;      // per-shard totals (changed blocks, m)
+    ez_stats_t* stats;    // per shard record (caller's or workspace), coded only
 };
 
 struct RuC3 {
+    const uint8_t* cache;
     uint8_t* out;
     uint64_t slot;
     uint64_t* sizes;
     uint32_t* dstatus;
     uint64_t n, L;
-    uint32_t W, B, first, count, tpc;
+    uint32_t W, B, log2B, first, count, tpc;
     int cold;
-    unsigned long long* state;
+    unsigned long long* state_a;   // the split's changed-block aggregates
+    unsigned long long* state;     // escape aggregates of this pass
     uint32_t* counter;
     uint32_t* abort;
-    const uint8_t* expbuf;
     const ShardInfo* info;
     const ez_stats_t* stats;
 };
@@ -216,19 +213,46 @@ __device__ __forceinline__ uint32_t block_rank(const uint32_t* s_bm, const uint3
     return s_pre[k >> 5] + __popc(s_bm[k >> 5] & ((1u << (k & 31)) - 1u));
 }
 
-template <bool kCoded>
-__global__ void __launch_bounds__(kThreads, 4) k_reuse_encode(RuEnc a)
+// Tile prefix of an aggregate another launch has already published at
+// st[tile] (every earlier aggregate of the segment is present, so the
+// look-back never waits): the exclusive prefix, published as inclusive.
+__device__ __forceinline__ unsigned long long known_prefix(unsigned long long* st, uint32_t tile,
+                                                           uint32_t seg_first,
+                                                           unsigned long long agg,
+                                                           unsigned long long* s_prefix,
+                                                           uint32_t* dstatus, uint32_t* abort)
 {
-    __shared__ uint32_t s_tile;
+    if (tile == seg_first) {
+        if (threadIdx.x == 0) *s_prefix = 0;
+    } else if (threadIdx.x < 32) {
+        bool stuck;
+        const unsigned long long p = lookback(st, tile, seg_first, &stuck, abort);
+        if (threadIdx.x == 0) {
+            if (stuck) atomicOr(dstatus, EZ_DSTAT_TIMEOUT);
+            st_relaxed(st + tile, kFlagIncl | ((p + agg) & kValMask));
+            *s_prefix = p;
+        }
+    }
+    __syncthreads();
+    return *s_prefix;
+}
+
+// Step A of both reuse encoders, one CTA per 8192-value tile with no
+// inter-tile dependence: compare the exponents with the sender cache, store
+// the sign+mantissa bytes, build the tile's slice of the changed-block bitmap
+// (one ballot per 8-value group), write the changed blocks' exponents into
+// the cache, and publish the tile's changed-block count as its look-back
+// aggregate.  The updated cache then holds every current exponent at its own
+// position, so the later steps read the changed exponents from it.
+__global__ void __launch_bounds__(kThreads, 5) k_reuse_split(RuEnc a)
+{
     __shared__ uint32_t s_gl[32], s_bm[32], s_pre[32];
-    __shared__ uint32_t s_agg;
-    __shared__ unsigned long long s_prefix;
     const int t = threadIdx.x, lane = t & 31, wid = t >> 5;
     if (t < 32) {
         s_gl[t] = 0;
         s_bm[t] = 0;
     }
-    const TilePos tp = tile_pos(next_tile(a.counter, &s_tile), a.count, a.tpc);
+    const TilePos tp = tile_pos(blockIdx.x, a.count, a.tpc);
     const uint32_t ci = tp.ci, lt = tp.lt;
     const uint32_t r = a.first + ci;
     const uint64_t n_s = shard_values(a.n, a.L, r);
@@ -237,12 +261,10 @@ __global__ void __launch_bounds__(kThreads, 4) k_reuse_encode(RuEnc a)
     const uint32_t B = a.B, log2B = a.log2B;
     const uint64_t nb = cdiv(n_s, B);
     const uint64_t bm_bytes = cdiv(nb, 8);
-    const uint64_t off_sm = ru_off_sm(n_s, B), off_idx = ru_off_idx(n_s, B);
-    const uint64_t off_exp = ru_off_exp(n_s, B, kCoded);
+    const uint64_t off_sm = ru_off_sm(n_s, B);
     const uint16_t* xt = a.x + (uint64_t)ci * a.L + v0;
     uint8_t* ct = a.cache + (uint64_t)ci * a.L + v0;
     uint8_t* o = a.out + (uint64_t)ci * a.slot;
-    const uint32_t fin_tile = n_s ? (uint32_t)((n_s - 1) / kTile) : 0u;
 
     uint4 w[kGroups];
     unsigned long long cv[kGroups];
@@ -252,8 +274,6 @@ __global__ void __launch_bounds__(kThreads, 4) k_reuse_encode(RuEnc a)
         w[g] = ld_group16(xt, v, nv);
         cv[g] = (v < nv && !a.cold) ? ld_group8(ct, v, nv) : 0ull;
     }
-
-
     unsigned long long e8[kGroups];
 #pragma unroll
     for (int g = 0; g < kGroups; g++) {
@@ -273,25 +293,99 @@ __global__ void __launch_bounds__(kThreads, 4) k_reuse_encode(RuEnc a)
         }
     }
     __syncthreads();
+    const uint32_t fin_tile = n_s ? (uint32_t)((n_s - 1) / kTile) : 0u;
     if (t < 32) {
         const uint32_t agg = build_bitmap(s_gl, s_bm, s_pre, log2B);
-        if (t == 0) s_agg = agg;
+        if (t == 0) {
+            st_relaxed(a.state + tp.state, (lt == 0 ? kFlagIncl : kFlagAgg) | agg);
+            // per-shard totals: changed blocks and stream length m
+            uint64_t len = (uint64_t)agg * B;
+            if (lt == fin_tile && n_s && block_changed(s_bm, (uint32_t)((n_s - 1 - v0) >> log2B)))
+                len -= nb * B - n_s;
+            if (agg) {
+                atomicAdd(&a.info[ci].n_changed, (unsigned long long)agg);
+                atomicAdd(&a.info[ci].m, (unsigned long long)len);
+            }
+        }
     }
     __syncthreads();
-    const unsigned long long agg = s_agg;
-    const unsigned long long P = tile_prefix(a.state, tp.state, ci * a.tpc, agg, &s_prefix,
-                                             a.dstatus, a.abort);
-
-    // index entry: changed blocks before this tile
-    if (t == 0 && v0 < n_s)
-        *reinterpret_cast<unsigned long long*>(o + off_idx + (uint64_t)ru_idx_stride(kCoded) * lt) = P;
-    // bitmap bytes of this tile
     const uint32_t nbt = (uint32_t)kTile >> log2B;
     const uint64_t bm0 = (uint64_t)lt * (nbt / 8);
     if ((uint32_t)t < nbt / 8 && bm0 + t < bm_bytes)
         o[64 + bm0 + t] = reinterpret_cast<const uint8_t*>(s_bm)[t];
+#pragma unroll
+    for (int g = 0; g < kGroups; g++) {
+        const uint32_t v = 8u * (uint32_t)(g * kThreads + t);
+        if (v < nv && block_changed(s_bm, v >> log2B)) st_group8(ct, v, nv, e8[g]);
+    }
+    if (lt == fin_tile) {
+        if (t < 16 && rup(bm_bytes, 16) > bm_bytes + t) o[64 + bm_bytes + t] = 0;
+        if (t < 16 && rup(n_s, 16) > n_s + t) o[off_sm + n_s + t] = 0;
+    }
+}
 
-    // changed exponents into the payload (or the staging stream) and the cache
+// This tile's slice of the bitmap, read back from the payload: s_bm, the
+// per-word exclusive popcounts s_pre and the changed-block count (returned
+// in every thread).  Bits past nb are ignored.
+__device__ __forceinline__ uint32_t load_bitmap(const uint8_t* o, uint32_t lt, uint64_t nb,
+                                                uint32_t log2B, uint32_t* s_bm, uint32_t* s_pre,
+                                                uint32_t* s_agg)
+{
+    const int t = threadIdx.x;
+    const uint64_t bm_bytes = cdiv(nb, 8);
+    const uint32_t nbt = (uint32_t)kTile >> log2B;
+    const uint64_t bm0 = (uint64_t)lt * (nbt / 8);
+    if ((uint32_t)t < nbt / 8) {
+        uint32_t b = 0;
+        if (bm0 + t < bm_bytes) {
+            b = o[64 + bm0 + t];
+            if (bm0 + t == bm_bytes - 1 && (nb & 7)) b &= (1u << (nb & 7)) - 1u;
+        }
+        if (b) atomicOr(&s_bm[t >> 2], b << (8 * (t & 3)));
+    }
+    __syncthreads();
+    if (t < 32) {
+        const uint32_t c = __popc(s_bm[t]);
+        uint32_t x = c;
+#pragma unroll
+        for (int q = 1; q < 32; q <<= 1) {
+            const uint32_t y = __shfl_up_sync(kFull, x, q);
+            if (t >= q) x += y;
+        }
+        s_pre[t] = x - c;
+        if (t == 31) *s_agg = x;
+    }
+    __syncthreads();
+    return *s_agg;
+}
+
+// Step B of the raw reuse encoder: place each tile's changed exponents.  The
+// tile's changed-block prefix comes from a look-back over the aggregates the
+// split published (all present: no wait); the exponents come from the cache.
+// The index entry is the prefix; the tile holding the shard's last value
+// writes the header, the padding and the size.
+__global__ void __launch_bounds__(kThreads, 6) k_reuse_place(RuEnc a)
+{
+    __shared__ uint32_t s_bm[32], s_pre[32], s_agg;
+    __shared__ unsigned long long s_prefix;
+    const int t = threadIdx.x;
+    if (t < 32) s_bm[t] = 0;
+    const TilePos tp = tile_pos(blockIdx.x, a.count, a.tpc);
+    const uint32_t ci = tp.ci, lt = tp.lt;
+    const uint32_t r = a.first + ci;
+    const uint64_t n_s = shard_values(a.n, a.L, r);
+    const uint64_t v0 = (uint64_t)lt * kTile;
+    const uint32_t nv = v0 < n_s ? (uint32_t)umin64(kTile, n_s - v0) : 0u;
+    const uint32_t B = a.B, log2B = a.log2B;
+    const uint64_t nb = cdiv(n_s, B);
+    const uint64_t off_idx = ru_off_idx(n_s, B), off_exp = ru_off_exp(n_s, B, false);
+    const uint8_t* ct = a.cache + (uint64_t)ci * a.L + v0;
+    uint8_t* o = a.out + (uint64_t)ci * a.slot;
+    __syncthreads();
+    const unsigned long long agg = load_bitmap(o, lt, nb, log2B, s_bm, s_pre, &s_agg);
+    const unsigned long long P = known_prefix(a.state, tp.state, ci * a.tpc, agg, &s_prefix,
+                                              a.dstatus, a.abort);
+    if (t == 0 && v0 < n_s) *reinterpret_cast<unsigned long long*>(o + off_idx + 8ull * lt) = P;
 #pragma unroll
     for (int g = 0; g < kGroups; g++) {
         const uint32_t v = 8u * (uint32_t)(g * kThreads + t);
@@ -299,36 +393,21 @@ __global__ void __launch_bounds__(kThreads, 4) k_reuse_encode(RuEnc a)
         const uint32_t k = v >> log2B;
         if (!block_changed(s_bm, k)) continue;
         const uint64_t pos = (P + block_rank(s_bm, s_pre, k)) * B + (v - (k << log2B));
-        if (kCoded) st_group8(a.expbuf + (uint64_t)ci * a.L + pos, 0u, nv - v, e8[g]);
-        else st_group8(o + off_exp + pos, 0u, nv - v, e8[g]);
-        st_group8(ct, v, nv, e8[g]);
+        st_group8(o + off_exp + pos, 0u, nv - v, ld_group8(ct, v, nv));
     }
-
-
+    const uint32_t fin_tile = n_s ? (uint32_t)((n_s - 1) / kTile) : 0u;
     if (lt == fin_tile) {
         const uint64_t n_changed = P + agg;
         bool last_changed = false;
-        if (n_s) {
-            const uint32_t klast = (uint32_t)((n_s - 1 - v0) >> log2B);
-            last_changed = block_changed(s_bm, klast);
-        }
+        if (n_s) last_changed = block_changed(s_bm, (uint32_t)((n_s - 1 - v0) >> log2B));
         const uint64_t m = n_changed * B - (last_changed ? nb * B - n_s : 0);
-        if (t < 16 && rup(bm_bytes, 16) > bm_bytes + t) o[64 + bm_bytes + t] = 0;
-        if (t < 16 && rup(n_s, 16) > n_s + t) o[off_sm + n_s + t] = 0;
-        const uint64_t ib = (uint64_t)ru_idx_stride(kCoded) * cdiv(n_s, kTile);
-        if (t < 16 && ib + t < ru_idx_bytes(n_s, kCoded)) o[off_idx + ib + t] = 0;
-        if (kCoded) {
-            if (t == 0) {
-                a.info[ci].m = m;
-                a.info[ci].n_changed = n_changed;
-            }
-        } else {
-            const uint64_t total = ru_bytes(n_s, B, m, false, 0);
-            if (t < 64)
-                o[t] = (uint8_t)ru_header_byte(t, a.cold ? 2u : 0u, 0u, B, r, n_s, n_changed, m, 0, total);
-            if (t < 128 && off_exp + m + t < total) o[off_exp + m + t] = 0;
-            if (t == 0) a.sizes[ci] = total;
-        }
+        const uint64_t total = ru_bytes(n_s, B, m, false, 0);
+        if (t < 64)
+            o[t] = (uint8_t)ru_header_byte(t, a.cold ? 2u : 0u, 0u, B, r, n_s, n_changed, m, 0, total);
+        if (t < 128 && off_exp + m + t < total) o[off_exp + m + t] = 0;
+        const uint64_t ib = 8 * cdiv(n_s, kTile);
+        if (t < 16 && ib + t < ru_idx_bytes(n_s, false)) o[off_idx + ib + t] = 0;
+        if (t == 0) a.sizes[ci] = total;
     }
 }
 
@@ -358,83 +437,83 @@ __device__ __forceinline__ uint32_t codes_of_bytes(const uint32_t* lut, uint32_t
     return acc;
 }
 
-// Pass 2 of the coded variant: 3-bit code of the staged exponent stream.
-// One CTA per kTile span of the shard's values: it codes the stream
-// exponents of the span's changed blocks, [q0, q1) with q = (changed blocks
-// before the span) * B taken from the index that pass 1 wrote, so its
-// escape prefix -- from a look-back over the spans -- is the span's second
-// index entry.  q0 is a multiple of B >= 8, so the span's plane bytes start
-// on a byte.
+// Coded variant, step B: one CTA per 8192-value span.  The span's
+// changed-block prefix comes from the split's aggregates (no wait); its
+// changed exponents, read from the cache, are coded with the shard's window
+// into the planes at stream position (prefix + rank) * B + offset (a
+// multiple of 8, so plane bytes are whole); the escapes are compacted in
+// value order and placed by a second look-back over the spans.  Both
+// prefixes are the span's index entries; the tile holding the shard's last
+// value writes the header, the padding and the size.
 __global__ void __launch_bounds__(kThreads) k_reuse_code3(RuC3 a)
 {
     __shared__ uint32_t s_tile;
     __shared__ uint32_t s_lut[256];
+    __shared__ uint32_t s_bm[32], s_pre[32], s_agg;
     __shared__ unsigned long long s_warp[kThreads / 32];
     __shared__ unsigned long long s_prefix;
     __shared__ __align__(16) uint8_t s_esc[kTile + 16];
     const int t = threadIdx.x;
+    if (t < 32) s_bm[t] = 0;
     const TilePos tp = tile_pos(next_tile(a.counter, &s_tile), a.count, a.tpc);
     const uint32_t ci = tp.ci, lt = tp.lt;
     const uint32_t r = a.first + ci;
     const uint64_t n_s = shard_values(a.n, a.L, r);
-    const uint64_t m = a.info[ci].m;
-    const uint64_t n_changed = a.info[ci].n_changed;
-    const uint64_t spans = cdiv(n_s, kTile);
+    const uint64_t v0 = (uint64_t)lt * kTile;
+    const uint32_t nv = v0 < n_s ? (uint32_t)umin64(kTile, n_s - v0) : 0u;
+    const uint32_t B = a.B, log2B = a.log2B;
+    const uint64_t nb = cdiv(n_s, B);
     uint32_t E0 = a.stats[ci].E0;
     if (E0 > 249u) {
         if (t == 0) atomicOr(a.dstatus, EZ_DSTAT_BAD_STATS);
         E0 = 0;
     }
     s_lut[t] = ru_lut_entry((uint32_t)t, E0);
-    const uint64_t off_idx = ru_off_idx(n_s, a.B), off_exp = ru_off_exp(n_s, a.B, true);
-    const uint64_t plane = rup(cdiv(m, 8), 16);
+    const uint64_t off_idx = ru_off_idx(n_s, B), off_exp = ru_off_exp(n_s, B, true);
+    const uint8_t* ct = a.cache + (uint64_t)ci * a.L + v0;
     uint8_t* o = a.out + (uint64_t)ci * a.slot;
+    unsigned long long* idx = reinterpret_cast<unsigned long long*>(o + off_idx);
+    const unsigned long long agg = load_bitmap(o, lt, nb, log2B, s_bm, s_pre, &s_agg);
+    const unsigned long long P = known_prefix(a.state_a, tp.state, ci * a.tpc, agg, &s_prefix,
+                                              a.dstatus, a.abort);
+    // the stream length m follows from the totals, known to every span only
+    // through the last one; plane offsets need the plane size, so m is taken
+    // from the split's per-shard total instead
+    const uint64_t n_changed_all = a.info[ci].n_changed;
+    const uint64_t m = a.info[ci].m;
+    const uint64_t plane = rup(cdiv(m, 8), 16);
     uint8_t* pl = o + off_exp;
     uint8_t* esc_sec = pl + 3 * plane;
-    unsigned long long* idx = reinterpret_cast<unsigned long long*>(o + off_idx);
-    // the span's slice of the stream
-    uint64_t q0 = 0, q1 = 0;
-    if (lt < spans) {
-        q0 = idx[2 * lt] * a.B;
-        q1 = lt + 1 < spans ? idx[2 * (lt + 1)] * a.B : m;
-        if (q1 < q0 || q1 > m || q1 - q0 > kTile) {
-            if (t == 0) atomicOr(a.dstatus, EZ_DSTAT_BAD_COUNT);
-            q1 = q0 = 0;
-        }
-    }
-    const uint32_t nv = (uint32_t)(q1 - q0);
-    const uint8_t* es = a.expbuf + (uint64_t)ci * a.L + q0;
-    const uint32_t fin_tile = (uint32_t)(a.tpc - 1);
 
     unsigned long long e8[kGroups];
-#pragma unroll
-    for (int g = 0; g < kGroups; g++) {
-        const uint32_t v = 8u * (uint32_t)(g * kThreads + t);
-        e8[g] = v < nv ? ld_group8(es, v, nv) : 0ull;
-    }
-    __syncthreads();   // lut
     uint32_t emasks = 0;
     unsigned long long packed = 0;
 #pragma unroll
     for (int g = 0; g < kGroups; g++) {
-        const uint32_t j = (uint32_t)(g * kThreads + t);
-        const uint32_t v = 8u * j;
+        const uint32_t v = 8u * (uint32_t)(g * kThreads + t);
+        e8[g] = 0;
+        if (v >= nv) continue;
+        const uint32_t k = v >> log2B;
+        if (!block_changed(s_bm, k)) continue;
+        e8[g] = ld_group8(ct, v, nv);
+        const uint64_t pos = (P + block_rank(s_bm, s_pre, k)) * B + (v - (k << log2B));
         const uint32_t vm = vmask_of(v, nv);
-        if (!vm) continue;
         const uint32_t acc = codes_of_bytes(s_lut, (uint32_t)e8[g], (uint32_t)(e8[g] >> 32)) &
                              (vm * 0x01010101u);
-        const uint64_t pb = q0 / 8 + j;
-        pl[pb] = (uint8_t)acc;
-        pl[plane + pb] = (uint8_t)(acc >> 8);
-        pl[2 * plane + pb] = (uint8_t)(acc >> 16);
+        const uint64_t pb = pos >> 3;
+        if (pos + 8 <= rup(m, 8)) {
+            pl[pb] = (uint8_t)acc;
+            pl[plane + pb] = (uint8_t)(acc >> 8);
+            pl[2 * plane + pb] = (uint8_t)(acc >> 16);
+        }
         const uint32_t esc = acc >> 24;
         emasks |= esc << (8 * g);
         packed |= (unsigned long long)__popc(esc) << (16 * g);
     }
     unsigned long long total;
     const unsigned long long excl = block_excl_scan(packed, s_warp, &total);
-    const unsigned long long agg = (total & 0xFFFFull) + ((total >> 16) & 0xFFFFull) +
-                                   ((total >> 32) & 0xFFFFull) + (total >> 48);
+    const unsigned long long agg2 = (total & 0xFFFFull) + ((total >> 16) & 0xFFFFull) +
+                                    ((total >> 32) & 0xFFFFull) + (total >> 48);
     uint32_t gbase = 0;
 #pragma unroll
     for (int g = 0; g < kGroups; g++) {
@@ -446,16 +525,21 @@ __global__ void __launch_bounds__(kThreads) k_reuse_code3(RuC3 a)
         }
         gbase += (uint32_t)((total >> (16 * g)) & 0xFFFFull);
     }
-    const unsigned long long P = tile_prefix(a.state, tp.state, ci * a.tpc, agg, &s_prefix,
+    __syncthreads();   // s_prefix is reused
+    const unsigned long long Q = tile_prefix(a.state, tp.state, ci * a.tpc, agg2, &s_prefix,
                                              a.dstatus, a.abort);
-    if (t == 0 && lt < spans) idx[2 * lt + 1] = P;
-    for (uint32_t b = (uint32_t)t; b < (uint32_t)agg; b += kThreads) esc_sec[P + b] = s_esc[b];
+    if (t == 0 && v0 < n_s) {
+        idx[2 * lt] = P;
+        idx[2 * lt + 1] = Q;
+    }
+    for (uint32_t b = (uint32_t)t; b < (uint32_t)agg2; b += kThreads) esc_sec[Q + b] = s_esc[b];
+    const uint32_t fin_tile = n_s ? (uint32_t)((n_s - 1) / kTile) : 0u;
     if (lt == fin_tile) {
-        const uint64_t n_esc = P + agg;
-        const uint64_t tot = ru_bytes(n_s, a.B, m, true, n_esc);
+        const uint64_t n_esc = Q + agg2;
+        const uint64_t tot = ru_bytes(n_s, B, m, true, n_esc);
         if (t < 64)
-            o[t] = (uint8_t)ru_header_byte(t, 1u | (a.cold ? 2u : 0u), E0, a.B, r, n_s, n_changed, m,
-                                           n_esc, tot);
+            o[t] = (uint8_t)ru_header_byte(t, 1u | (a.cold ? 2u : 0u), E0, B, r, n_s, n_changed_all,
+                                           m, n_esc, tot);
         const uint64_t pbytes = cdiv(m, 8);
         if (t < 16 && pbytes + t < plane) {
             pl[pbytes + t] = 0;
@@ -463,6 +547,8 @@ __global__ void __launch_bounds__(kThreads) k_reuse_code3(RuC3 a)
             pl[2 * plane + pbytes + t] = 0;
         }
         if (t < 128 && off_exp + 3 * plane + n_esc + t < tot) o[off_exp + 3 * plane + n_esc + t] = 0;
+        const uint64_t ib = 16 * cdiv(n_s, kTile);
+        if (t < 16 && ib + t < ru_idx_bytes(n_s, true)) o[off_idx + ib + t] = 0;
         if (t == 0) a.sizes[ci] = tot;
     }
 }
@@ -743,24 +829,24 @@ cudaError_t launch_reuse_encode(const ez_plan_s* p, const uint16_t* x, uint32_t 
     a.state = w.state_a;
     a.counter = w.counters + 0;
     a.abort = w.counters + 7;
-    a.expbuf = w.expbuf;
     a.info = w.info;
-    a.bins = (StatsBins*)w.bins;
     a.stats = st ? st : w.shard_stats;
-    a.K = p->K;
     const unsigned tiles = (unsigned)((uint64_t)count * p->tpc);
-    if (!coded) {
-        k_reuse_encode<false><<<tiles, kThreads, 0, s>>>(a);
-        return cudaGetLastError();
+    cudaError_t e;
+    if (coded) {
+        // the shards' windows (a pass over the values of their own)
+        e = launch_shard_stats(p, x, first, count, a.stats, w, s);
+        if (e != cudaSuccess) return e;
     }
-    // the shards' windows first (their own pass over the values), then the
-    // split and the staged exponent stream, then the code
-    cudaError_t e = launch_shard_stats(p, x, first, count, a.stats, w, s);
-    if (e != cudaSuccess) return e;
-    k_reuse_encode<true><<<tiles, kThreads, 0, s>>>(a);
+    k_reuse_split<<<tiles, kThreads, 0, s>>>(a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+    if (!coded) {
+        k_reuse_place<<<tiles, kThreads, 0, s>>>(a);
+        return cudaGetLastError();
+    }
     RuC3 b;
+    b.cache = cache;
     b.out = out;
     b.slot = p->slot_bytes;
     b.sizes = sizes;
@@ -769,14 +855,15 @@ cudaError_t launch_reuse_encode(const ez_plan_s* p, const uint16_t* x, uint32_t 
     b.L = p->L;
     b.W = p->W;
     b.B = p->B;
+    b.log2B = a.log2B;
     b.first = first;
     b.count = count;
     b.tpc = p->tpc;
     b.cold = a.cold;
+    b.state_a = w.state_a;
     b.state = w.state_b;
     b.counter = w.counters + 2;
     b.abort = w.counters + 7;
-    b.expbuf = w.expbuf;
     b.info = w.info;
     b.stats = a.stats;
     k_reuse_code3<<<tiles, kThreads, 0, s>>>(b);
