@@ -50,6 +50,10 @@ WsView ws_view(const ez_plan_s* p, void* ws)
     v.info = reinterpret_cast<ShardInfo*>(b + p->off_info);
     v.shard_stats = reinterpret_cast<ez_stats_t*>(b + p->off_shard_stats);
     v.bins = b + p->off_bins;
+    v.escbuf = p->off_escbuf ? b + p->off_escbuf : nullptr;
+    const uint64_t segs = tile_scan_segments(p->tpc) * p->W;
+    v.seg_a = reinterpret_cast<unsigned long long*>(b + p->off_seg);
+    v.seg_b = v.seg_a + segs;
     v.state_a = reinterpret_cast<unsigned long long*>(b + p->off_state_a);
     v.state_b = reinterpret_cast<unsigned long long*>(b + p->off_state_b);
     return v;
@@ -106,8 +110,13 @@ ez_status ez_plan_create(ez_plan* out, const ez_plan_desc* d)
     p->off_state_a = off;
     off = rup(off + W * tpc * 8, 256);
     p->off_state_b = off;
-    off = rup(off + (reuse ? W * tpc * 8 : 0), 256);
+    off = rup(off + (coded ? W * tpc * 8 : 0), 256);
+    p->off_seg = off;                                     // two arrays of scan-segment states
+    off = rup(off + 2 * W * ezk::tile_scan_segments(tpc) * 8, 256);
     p->zero_bytes = off;
+    // coded reuse: each span's escapes staged at its own offset
+    p->off_escbuf = coded ? off : 0;
+    off = rup(off + (coded ? W * L : 0), 256);
     p->ws_bytes = off;
     *out = p;
     return EZ_OK;
@@ -158,7 +167,7 @@ ez_status ez_encode_code3(ez_plan p, const uint16_t* d_x, uint32_t first, uint32
     ez_status s = check_ws(p, d_ws, ws_bytes);
     if (s != EZ_OK) return s;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    s = clear_ws(d_ws, p->off_state_a + (uint64_t)count * p->tpc * 8, st);
+    s = clear_ws(d_ws, p->zero_bytes, st);
     if (s != EZ_OK) return s;
     return cuda_status(ezk::launch_code3_encode(p, d_x, first, count, d_stats, d_out, d_sizes,
                                                 d_status, ezk::ws_view(p, d_ws), st));
@@ -195,10 +204,7 @@ ez_status ez_encode_reuse(ez_plan p, const uint16_t* d_x, uint32_t first, uint32
     ez_status s = check_ws(p, d_ws, ws_bytes);
     if (s != EZ_OK) return s;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const bool coded = p->codec == EZ_CODEC_REUSE_CODE3;
-    const uint64_t clear = coded ? p->off_state_b + (uint64_t)count * p->tpc * 8
-                                 : p->off_state_a + (uint64_t)count * p->tpc * 8;
-    s = clear_ws(d_ws, clear, st);
+    s = clear_ws(d_ws, p->zero_bytes, st);
     if (s != EZ_OK) return s;
     return cuda_status(ezk::launch_reuse_encode(p, d_x, first, count, d_send_cache, cold, d_out,
                                                 d_sizes, d_stats, d_status, ezk::ws_view(p, d_ws),

@@ -14,7 +14,7 @@ struct ez_plan_s {
     uint64_t slot_bytes;     // worst-case payload per shard
     double K;                // 16383 / (14 ln 2)
     // workspace layout (byte offsets); [0, zero_bytes) is cleared per call
-    uint64_t off_ctr, off_info, off_shard_stats, off_bins, off_state_a, off_state_b;
+    uint64_t off_ctr, off_info, off_shard_stats, off_bins, off_state_a, off_state_b, off_seg, off_escbuf;
     uint64_t zero_bytes, ws_bytes;
     uint32_t n_bins;
 };
@@ -37,9 +37,20 @@ struct WsView {
     unsigned long long* state_a;
     unsigned long long* state_b;
     void* bins;                    // StatsBins[n_bins]
+    uint8_t* escbuf;               // W * L bytes of staged escapes (coded reuse) or NULL
+    unsigned long long* seg_a;     // scan-segment states, two arrays of W * segments
+    unsigned long long* seg_b;
 };
 
 WsView ws_view(const ez_plan_s* p, void* ws);
+
+// Scan segments per chunk of tpc tiles (k_scan.cu).
+uint64_t tile_scan_segments(uint64_t tpc);
+
+// Inclusive prefixes, per chunk, of the per-tile counts in st[count * tpc].
+cudaError_t launch_tile_scan(const ez_plan_s* p, unsigned long long* st, uint32_t count,
+                             unsigned long long* seg_st, uint32_t* counter, uint32_t* abort,
+                             uint32_t* dstatus, cudaStream_t s);
 
 cudaError_t launch_stats(const ez_plan_s* p, const uint16_t* x, uint64_t n, ez_stats_t* out,
                          const WsView& w, cudaStream_t s);

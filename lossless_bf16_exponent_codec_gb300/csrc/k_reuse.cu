@@ -51,6 +51,7 @@ struct RuEnc {
 
 struct RuC3 {
     const uint8_t* cache;
+    uint8_t* escbuf;               // W*L-byte stream, span t's escapes at t*kTile
     uint8_t* out;
     uint64_t slot;
     uint64_t* sizes;
@@ -213,30 +214,6 @@ __device__ __forceinline__ uint32_t block_rank(const uint32_t* s_bm, const uint3
     return s_pre[k >> 5] + __popc(s_bm[k >> 5] & ((1u << (k & 31)) - 1u));
 }
 
-// Tile prefix of an aggregate another launch has already published at
-// st[tile] (every earlier aggregate of the segment is present, so the
-// look-back never waits): the exclusive prefix, published as inclusive.
-__device__ __forceinline__ unsigned long long known_prefix(unsigned long long* st, uint32_t tile,
-                                                           uint32_t seg_first,
-                                                           unsigned long long agg,
-                                                           unsigned long long* s_prefix,
-                                                           uint32_t* dstatus, uint32_t* abort)
-{
-    if (tile == seg_first) {
-        if (threadIdx.x == 0) *s_prefix = 0;
-    } else if (threadIdx.x < 32) {
-        bool stuck;
-        const unsigned long long p = lookback(st, tile, seg_first, &stuck, abort);
-        if (threadIdx.x == 0) {
-            if (stuck) atomicOr(dstatus, EZ_DSTAT_TIMEOUT);
-            st_relaxed(st + tile, kFlagIncl | ((p + agg) & kValMask));
-            *s_prefix = p;
-        }
-    }
-    __syncthreads();
-    return *s_prefix;
-}
-
 // Step A of both reuse encoders, one CTA per 8192-value tile with no
 // inter-tile dependence: compare the exponents with the sender cache, store
 // the sign+mantissa bytes, build the tile's slice of the changed-block bitmap
@@ -359,15 +336,14 @@ __device__ __forceinline__ uint32_t load_bitmap(const uint8_t* o, uint32_t lt, u
     return *s_agg;
 }
 
-// Step B of the raw reuse encoder: place each tile's changed exponents.  The
-// tile's changed-block prefix comes from a look-back over the aggregates the
-// split published (all present: no wait); the exponents come from the cache.
-// The index entry is the prefix; the tile holding the shard's last value
-// writes the header, the padding and the size.
+// Step B of the raw reuse encoder, after the tile scan turned the split's
+// changed-block counts into inclusive prefixes: the tile's changed exponents,
+// read from the cache, go to EXP at (prefix + rank) * B + offset.  The index
+// entry is the prefix; the tile holding the shard's last value writes the
+// header, the padding and the size (totals from the split's shard record).
 __global__ void __launch_bounds__(kThreads, 6) k_reuse_place(RuEnc a)
 {
     __shared__ uint32_t s_bm[32], s_pre[32], s_agg;
-    __shared__ unsigned long long s_prefix;
     const int t = threadIdx.x;
     if (t < 32) s_bm[t] = 0;
     const TilePos tp = tile_pos(blockIdx.x, a.count, a.tpc);
@@ -381,11 +357,19 @@ __global__ void __launch_bounds__(kThreads, 6) k_reuse_place(RuEnc a)
     const uint64_t off_idx = ru_off_idx(n_s, B), off_exp = ru_off_exp(n_s, B, false);
     const uint8_t* ct = a.cache + (uint64_t)ci * a.L + v0;
     uint8_t* o = a.out + (uint64_t)ci * a.slot;
+    const unsigned long long* sc = a.state + (uint64_t)ci * a.tpc;
+    // every group's cache bytes, loaded with the bitmap and the prefix
+    unsigned long long ev[kGroups];
+#pragma unroll
+    for (int g = 0; g < kGroups; g++) {
+        const uint32_t v = 8u * (uint32_t)(g * kThreads + t);
+        ev[g] = v < nv ? ld_group8(ct, v, nv) : 0ull;
+    }
+    const unsigned long long P = lt ? ld_relaxed(sc + lt - 1) : 0ull;
     __syncthreads();
-    const unsigned long long agg = load_bitmap(o, lt, nb, log2B, s_bm, s_pre, &s_agg);
-    const unsigned long long P = known_prefix(a.state, tp.state, ci * a.tpc, agg, &s_prefix,
-                                              a.dstatus, a.abort);
+    load_bitmap(o, lt, nb, log2B, s_bm, s_pre, &s_agg);
     if (t == 0 && v0 < n_s) *reinterpret_cast<unsigned long long*>(o + off_idx + 8ull * lt) = P;
+    const uint64_t m = a.info[ci].m;
 #pragma unroll
     for (int g = 0; g < kGroups; g++) {
         const uint32_t v = 8u * (uint32_t)(g * kThreads + t);
@@ -393,14 +377,12 @@ __global__ void __launch_bounds__(kThreads, 6) k_reuse_place(RuEnc a)
         const uint32_t k = v >> log2B;
         if (!block_changed(s_bm, k)) continue;
         const uint64_t pos = (P + block_rank(s_bm, s_pre, k)) * B + (v - (k << log2B));
-        st_group8(o + off_exp + pos, 0u, nv - v, ld_group8(ct, v, nv));
+        const uint32_t cnt = min(8u, nv - v);
+        if (pos + cnt <= m) st_group8(o + off_exp + pos, 0u, cnt, ev[g]);
     }
     const uint32_t fin_tile = n_s ? (uint32_t)((n_s - 1) / kTile) : 0u;
     if (lt == fin_tile) {
-        const uint64_t n_changed = P + agg;
-        bool last_changed = false;
-        if (n_s) last_changed = block_changed(s_bm, (uint32_t)((n_s - 1 - v0) >> log2B));
-        const uint64_t m = n_changed * B - (last_changed ? nb * B - n_s : 0);
+        const uint64_t n_changed = a.info[ci].n_changed;
         const uint64_t total = ru_bytes(n_s, B, m, false, 0);
         if (t < 64)
             o[t] = (uint8_t)ru_header_byte(t, a.cold ? 2u : 0u, 0u, B, r, n_s, n_changed, m, 0, total);
@@ -437,25 +419,22 @@ __device__ __forceinline__ uint32_t codes_of_bytes(const uint32_t* lut, uint32_t
     return acc;
 }
 
-// Coded variant, step B: one CTA per 8192-value span.  The span's
-// changed-block prefix comes from the split's aggregates (no wait); its
-// changed exponents, read from the cache, are coded with the shard's window
-// into the planes at stream position (prefix + rank) * B + offset (a
-// multiple of 8, so plane bytes are whole); the escapes are compacted in
-// value order and placed by a second look-back over the spans.  Both
-// prefixes are the span's index entries; the tile holding the shard's last
-// value writes the header, the padding and the size.
-__global__ void __launch_bounds__(kThreads) k_reuse_code3(RuC3 a)
+// Coded variant, step B (after the tile scan of the split's counts): one CTA
+// per 8192-value span codes the span's changed exponents, read from the
+// cache, with the shard's window into the planes at stream position
+// (prefix + rank) * B + offset (a multiple of 8: plane bytes are whole),
+// writes the span's escapes (value order) as whole words at the span's own
+// offset of the escape stream, and publishes its escape count.
+__global__ void __launch_bounds__(kThreads, 5) k_reuse_code3(RuC3 a)
 {
-    __shared__ uint32_t s_tile;
     __shared__ uint32_t s_lut[256];
     __shared__ uint32_t s_bm[32], s_pre[32], s_agg;
     __shared__ unsigned long long s_warp[kThreads / 32];
-    __shared__ unsigned long long s_prefix;
-    __shared__ __align__(16) uint8_t s_esc[kTile + 16];
+    __shared__ __align__(16) uint32_t s_esc32[(kTile + 16) / 4];
+    uint8_t* s_esc = reinterpret_cast<uint8_t*>(s_esc32);
     const int t = threadIdx.x;
     if (t < 32) s_bm[t] = 0;
-    const TilePos tp = tile_pos(next_tile(a.counter, &s_tile), a.count, a.tpc);
+    const TilePos tp = tile_pos(blockIdx.x, a.count, a.tpc);
     const uint32_t ci = tp.ci, lt = tp.lt;
     const uint32_t r = a.first + ci;
     const uint64_t n_s = shard_values(a.n, a.L, r);
@@ -465,25 +444,20 @@ __global__ void __launch_bounds__(kThreads) k_reuse_code3(RuC3 a)
     const uint64_t nb = cdiv(n_s, B);
     uint32_t E0 = a.stats[ci].E0;
     if (E0 > 249u) {
-        if (t == 0) atomicOr(a.dstatus, EZ_DSTAT_BAD_STATS);
+        if (t == 0 && lt == 0) atomicOr(a.dstatus, EZ_DSTAT_BAD_STATS);
         E0 = 0;
     }
     s_lut[t] = ru_lut_entry((uint32_t)t, E0);
-    const uint64_t off_idx = ru_off_idx(n_s, B), off_exp = ru_off_exp(n_s, B, true);
+    const uint64_t off_exp = ru_off_exp(n_s, B, true);
     const uint8_t* ct = a.cache + (uint64_t)ci * a.L + v0;
     uint8_t* o = a.out + (uint64_t)ci * a.slot;
-    unsigned long long* idx = reinterpret_cast<unsigned long long*>(o + off_idx);
-    const unsigned long long agg = load_bitmap(o, lt, nb, log2B, s_bm, s_pre, &s_agg);
-    const unsigned long long P = known_prefix(a.state_a, tp.state, ci * a.tpc, agg, &s_prefix,
-                                              a.dstatus, a.abort);
-    // the stream length m follows from the totals, known to every span only
-    // through the last one; plane offsets need the plane size, so m is taken
-    // from the split's per-shard total instead
-    const uint64_t n_changed_all = a.info[ci].n_changed;
+    const unsigned long long* sc = a.state_a + (uint64_t)ci * a.tpc;
+    const unsigned long long P = lt ? ld_relaxed(sc + lt - 1) : 0ull;
+    __syncthreads();   // s_bm cleared, s_lut written
+    load_bitmap(o, lt, nb, log2B, s_bm, s_pre, &s_agg);
     const uint64_t m = a.info[ci].m;
     const uint64_t plane = rup(cdiv(m, 8), 16);
     uint8_t* pl = o + off_exp;
-    uint8_t* esc_sec = pl + 3 * plane;
 
     unsigned long long e8[kGroups];
     uint32_t emasks = 0;
@@ -495,25 +469,25 @@ __global__ void __launch_bounds__(kThreads) k_reuse_code3(RuC3 a)
         if (v >= nv) continue;
         const uint32_t k = v >> log2B;
         if (!block_changed(s_bm, k)) continue;
-        e8[g] = ld_group8(ct, v, nv);
         const uint64_t pos = (P + block_rank(s_bm, s_pre, k)) * B + (v - (k << log2B));
+        if (pos + min(8u, nv - v) > m) continue;   // inconsistent totals: nothing past EXP
+        e8[g] = ld_group8(ct, v, nv);
         const uint32_t vm = vmask_of(v, nv);
         const uint32_t acc = codes_of_bytes(s_lut, (uint32_t)e8[g], (uint32_t)(e8[g] >> 32)) &
                              (vm * 0x01010101u);
         const uint64_t pb = pos >> 3;
-        if (pos + 8 <= rup(m, 8)) {
-            pl[pb] = (uint8_t)acc;
-            pl[plane + pb] = (uint8_t)(acc >> 8);
-            pl[2 * plane + pb] = (uint8_t)(acc >> 16);
-        }
+        pl[pb] = (uint8_t)acc;
+        pl[plane + pb] = (uint8_t)(acc >> 8);
+        pl[2 * plane + pb] = (uint8_t)(acc >> 16);
         const uint32_t esc = acc >> 24;
         emasks |= esc << (8 * g);
         packed |= (unsigned long long)__popc(esc) << (16 * g);
     }
     unsigned long long total;
     const unsigned long long excl = block_excl_scan(packed, s_warp, &total);
-    const unsigned long long agg2 = (total & 0xFFFFull) + ((total >> 16) & 0xFFFFull) +
-                                    ((total >> 32) & 0xFFFFull) + (total >> 48);
+    const uint32_t agg2 = (uint32_t)((total & 0xFFFFull) + ((total >> 16) & 0xFFFFull) +
+                                     ((total >> 32) & 0xFFFFull) + (total >> 48));
+    if (t == 0) st_relaxed(a.state + tp.state, (unsigned long long)agg2);
     uint32_t gbase = 0;
 #pragma unroll
     for (int g = 0; g < kGroups; g++) {
@@ -525,21 +499,72 @@ __global__ void __launch_bounds__(kThreads) k_reuse_code3(RuC3 a)
         }
         gbase += (uint32_t)((total >> (16 * g)) & 0xFFFFull);
     }
-    __syncthreads();   // s_prefix is reused
-    const unsigned long long Q = tile_prefix(a.state, tp.state, ci * a.tpc, agg2, &s_prefix,
-                                             a.dstatus, a.abort);
+    __syncthreads();
+    uint32_t* dst = reinterpret_cast<uint32_t*>(a.escbuf + (uint64_t)ci * a.L + v0);
+    for (uint32_t i = (uint32_t)t; i < (agg2 + 3) / 4; i += kThreads) dst[i] = s_esc32[i];
+}
+
+// Bytes [b, b+16) of a run of `len` bytes at dst, from d (bytes past len
+// are not written).
+constexpr uint32_t kSpecBytes = 2048;
+
+__device__ __forceinline__ void store_run16(uint8_t* dst, uint32_t b, uint32_t len, const uint4& d)
+{
+    if (b >= len) return;
+    const uint32_t ws[4] = {d.x, d.y, d.z, d.w};
+#pragma unroll
+    for (uint32_t i = 0; i < 16; i++)
+        if (b + i < len) dst[b + i] = (uint8_t)(ws[i >> 2] >> (8 * (i & 3)));
+}
+
+// Coded variant, step C (after the tile scan of the escape counts): both
+// index entries of the span, its escapes copied from the stream into place,
+// and on the tile holding the shard's last value the header, the padding and
+// the size.
+__global__ void __launch_bounds__(kThreads, 8) k_reuse_place_esc(RuC3 a)
+{
+    const int t = threadIdx.x;
+    const TilePos tp = tile_pos(blockIdx.x, a.count, a.tpc);
+    const uint32_t ci = tp.ci, lt = tp.lt;
+    const uint32_t r = a.first + ci;
+    const uint64_t n_s = shard_values(a.n, a.L, r);
+    const uint64_t v0 = (uint64_t)lt * kTile;
+    const uint32_t B = a.B;
+    const uint64_t off_idx = ru_off_idx(n_s, B), off_exp = ru_off_exp(n_s, B, true);
+    uint8_t* o = a.out + (uint64_t)ci * a.slot;
+    const uint64_t m = a.info[ci].m;
+    const uint64_t plane = rup(cdiv(m, 8), 16);
+    uint8_t* pl = o + off_exp;
+    uint8_t* esc_sec = pl + 3 * plane;
+    const unsigned long long* sa = a.state_a + (uint64_t)ci * a.tpc;
+    const unsigned long long* sb = a.state + (uint64_t)ci * a.tpc;
+    const uint8_t* src = a.escbuf + (uint64_t)ci * a.L + v0;
+    // a speculative 2 KB window of the staged bytes, loaded with the
+    // prefixes; longer runs (rare) finish with a byte loop
+    uint4 d0 = make_uint4(0, 0, 0, 0);
+    const uint32_t b0 = 16u * (uint32_t)t;
+    if (b0 < kSpecBytes && v0 + b0 + 16 <= a.L) d0 = ld_v4_nc(src + b0);
+    const unsigned long long P = lt ? ld_relaxed(sa + lt - 1) : 0ull;
+    const unsigned long long Q = lt ? ld_relaxed(sb + lt - 1) : 0ull;
+    const unsigned long long Qend = ld_relaxed(sb + lt);
+    const uint32_t agg2 = Qend >= Q && Qend - Q <= kTile ? (uint32_t)(Qend - Q) : 0u;
     if (t == 0 && v0 < n_s) {
+        unsigned long long* idx = reinterpret_cast<unsigned long long*>(o + off_idx);
         idx[2 * lt] = P;
         idx[2 * lt + 1] = Q;
     }
-    for (uint32_t b = (uint32_t)t; b < (uint32_t)agg2; b += kThreads) esc_sec[Q + b] = s_esc[b];
+    if (b0 < kSpecBytes) store_run16(esc_sec + Q, b0, agg2, d0);
+    for (uint32_t b = kSpecBytes + (uint32_t)t; b < agg2; b += kThreads) esc_sec[Q + b] = src[b];
     const uint32_t fin_tile = n_s ? (uint32_t)((n_s - 1) / kTile) : 0u;
     if (lt == fin_tile) {
-        const uint64_t n_esc = Q + agg2;
+        uint32_t E0 = a.stats[ci].E0;
+        if (E0 > 249u) E0 = 0;
+        const uint64_t n_esc = ld_relaxed(sb + a.tpc - 1);
+        const uint64_t n_changed = a.info[ci].n_changed;
         const uint64_t tot = ru_bytes(n_s, B, m, true, n_esc);
         if (t < 64)
-            o[t] = (uint8_t)ru_header_byte(t, 1u | (a.cold ? 2u : 0u), E0, B, r, n_s, n_changed_all,
-                                           m, n_esc, tot);
+            o[t] = (uint8_t)ru_header_byte(t, 1u | (a.cold ? 2u : 0u), E0, B, r, n_s, n_changed, m,
+                                           n_esc, tot);
         const uint64_t pbytes = cdiv(m, 8);
         if (t < 16 && pbytes + t < plane) {
             pl[pbytes + t] = 0;
@@ -841,6 +866,8 @@ cudaError_t launch_reuse_encode(const ez_plan_s* p, const uint16_t* x, uint32_t 
     k_reuse_split<<<tiles, kThreads, 0, s>>>(a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+    e = launch_tile_scan(p, w.state_a, count, w.seg_a, w.counters + 4, w.counters + 7, dstatus, s);
+    if (e != cudaSuccess) return e;
     if (!coded) {
         k_reuse_place<<<tiles, kThreads, 0, s>>>(a);
         return cudaGetLastError();
@@ -866,7 +893,13 @@ cudaError_t launch_reuse_encode(const ez_plan_s* p, const uint16_t* x, uint32_t 
     b.abort = w.counters + 7;
     b.info = w.info;
     b.stats = a.stats;
+    b.escbuf = w.escbuf;
     k_reuse_code3<<<tiles, kThreads, 0, s>>>(b);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    e = launch_tile_scan(p, w.state_b, count, w.seg_b, w.counters + 5, w.counters + 7, dstatus, s);
+    if (e != cudaSuccess) return e;
+    k_reuse_place_esc<<<tiles, kThreads, 0, s>>>(b);
     return cudaGetLastError();
 }
 

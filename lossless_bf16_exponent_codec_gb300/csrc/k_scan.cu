@@ -1,0 +1,70 @@
+// k_scan.cu -- prefix sums of per-tile counts, between the split and place
+// steps of the encoders.
+//
+// A split launch publishes one count per 8192-value tile (escapes, changed
+// blocks) in a tile-state array, chunk-major: st[c * tpc + t], the value in
+// the low 62 bits.  This launch replaces every entry by the inclusive prefix
+// of its chunk (flag bits cleared), so tile t of chunk c starts at
+// st[c*tpc + t - 1] (0 for t = 0) and the chunk's total is st[c*tpc + tpc-1].
+// One CTA scans a segment of kScanSpan entries of one chunk (8 per thread,
+// one block scan); segments of a chunk are chained by a decoupled look-back
+// over per-segment states (ids from an atomic counter, so a segment waits
+// only on running ones; every wait bounded).
+#include "ez_internal.h"
+#include "ez_common.cuh"
+
+namespace ezk {
+using namespace ez;
+
+constexpr uint32_t kScanPer = 8;
+constexpr uint32_t kScanSpan = kThreads * kScanPer;   // 2048 tile entries per CTA
+
+__global__ void __launch_bounds__(kThreads) k_tile_scan(unsigned long long* st, uint32_t count,
+                                                        uint32_t tpc, uint32_t spc,
+                                                        unsigned long long* seg_st,
+                                                        uint32_t* counter, uint32_t* abort,
+                                                        uint32_t* dstatus)
+{
+    __shared__ uint32_t s_tile;
+    __shared__ unsigned long long s_warp[kThreads / 32];
+    __shared__ unsigned long long s_prefix;
+    const int t = threadIdx.x;
+    const uint32_t id = next_tile(counter, &s_tile);
+    const uint32_t c = id / spc, sg = id % spc;   // segments of a chunk in order
+    if (c >= count) return;
+    unsigned long long* sc = st + (uint64_t)c * tpc;
+    const uint32_t base = sg * kScanSpan + (uint32_t)t * kScanPer;
+    unsigned long long v[kScanPer];
+    unsigned long long sum = 0;
+#pragma unroll
+    for (uint32_t i = 0; i < kScanPer; i++) {
+        v[i] = base + i < tpc ? (ld_relaxed(sc + base + i) & kValMask) : 0ull;
+        sum += v[i];
+    }
+    unsigned long long total;
+    const unsigned long long excl = block_excl_scan(sum, s_warp, &total);
+    const unsigned long long P = tile_prefix(seg_st, c * spc + sg, c * spc, total, &s_prefix,
+                                             dstatus, abort);
+    unsigned long long run = P + excl;
+#pragma unroll
+    for (uint32_t i = 0; i < kScanPer; i++) {
+        run += v[i];
+        if (base + i < tpc) st_relaxed(sc + base + i, run);
+    }
+}
+
+cudaError_t launch_tile_scan(const ez_plan_s* p, unsigned long long* st, uint32_t count,
+                             unsigned long long* seg_st, uint32_t* counter, uint32_t* abort,
+                             uint32_t* dstatus, cudaStream_t s)
+{
+    const uint32_t spc = (uint32_t)cdiv(p->tpc, kScanSpan);
+    const uint64_t ctas = (uint64_t)count * spc;
+    if (ctas > 0x7fffffffull) return cudaErrorInvalidValue;
+    k_tile_scan<<<(unsigned)ctas, kThreads, 0, s>>>(st, count, p->tpc, spc, seg_st, counter,
+                                                    abort, dstatus);
+    return cudaGetLastError();
+}
+
+uint64_t tile_scan_segments(uint64_t tpc) { return cdiv(tpc, kScanSpan); }
+
+}  // namespace ezk
