@@ -86,7 +86,7 @@ __device__ __forceinline__ void st_begin(StatsSmem& S, uint32_t h0)
 }
 
 // A value outside the window: straight into the per-exponent bins.
-static __device__ __noinline__ void st_add_slow(uint32_t h, StatsSmem& S)
+__device__ __forceinline__ void st_add_slow(uint32_t h, StatsSmem& S)
 {
     const uint32_t E = exp_of(h);
     atomicAdd(&S.cnt[E], 1u);
@@ -173,9 +173,13 @@ __device__ __forceinline__ bool st_end(StatsSmem& S, StatsBins* G, uint32_t expe
     if (S.cnt[t]) atomicAdd(&G->hist[t], (unsigned long long)S.cnt[t]);
     if (S.s1[t]) atomicAdd(&G->s1[t], (unsigned long long)(long long)S.s1[t]);
     if (S.s2[t]) atomicAdd(&G->s2[t], S.s2[t]);
-    __threadfence();
+    // the barrier orders every thread's bin atomics before thread 0's fence
+    // (fences are cumulative), which orders them before the completion count
     __syncthreads();
-    if (t == 0) S.last = (atomicAdd(&G->done, 1u) == expected - 1) ? 1u : 0u;
+    if (t == 0) {
+        __threadfence();
+        S.last = (atomicAdd(&G->done, 1u) == expected - 1) ? 1u : 0u;
+    }
     __syncthreads();
     const bool last = S.last != 0;
     if (last) __threadfence();
@@ -184,30 +188,34 @@ __device__ __forceinline__ bool st_end(StatsSmem& S, StatsBins* G, uint32_t expe
 
 // ---- exact rounding of big sums --------------------------------------------
 
-struct Big {
-    uint32_t w[24];   // 768-bit non-negative integer, little-endian limbs
-};
+constexpr int kLimbs = 24;   // 768-bit non-negative integers, little-endian 32-bit limbs
 
-__device__ __forceinline__ int big_cmp(const Big& a, const Big& b)
+__device__ __forceinline__ int big_cmp(const uint32_t* a, const uint32_t* b)
 {
-    for (int i = 23; i >= 0; i--)
-        if (a.w[i] != b.w[i]) return a.w[i] > b.w[i] ? 1 : -1;
+    for (int i = kLimbs - 1; i >= 0; i--)
+        if (a[i] != b[i]) return a[i] > b[i] ? 1 : -1;
     return 0;
 }
 
-__device__ __forceinline__ void big_sub(Big& a, const Big& b)   // a >= b
+__device__ __forceinline__ void big_sub(uint32_t* a, const uint32_t* b)   // a >= b
 {
     unsigned long long borrow = 0;
-    for (int i = 0; i < 24; i++) {
-        const unsigned long long bi = (unsigned long long)b.w[i] + borrow;
-        borrow = (unsigned long long)a.w[i] < bi ? 1ull : 0ull;
-        a.w[i] = (uint32_t)((unsigned long long)a.w[i] - bi);
+    for (int i = 0; i < kLimbs; i++) {
+        const unsigned long long bi = (unsigned long long)b[i] + borrow;
+        borrow = (unsigned long long)a[i] < bi ? 1ull : 0ull;
+        a[i] = (uint32_t)((unsigned long long)a[i] - bi);
     }
 }
 
-__device__ __forceinline__ uint32_t big_bit(const Big& b, int pos)
+__device__ __forceinline__ uint32_t limb(const uint32_t* w, int i) { return (i >= 0 && i < kLimbs) ? w[i] : 0u; }
+
+// Bits [pos, pos + 64) of the number (pos >= 0).
+__device__ __forceinline__ unsigned long long bits64(const uint32_t* w, int pos)
 {
-    return (pos < 0) ? 0u : (b.w[pos >> 5] >> (pos & 31)) & 1u;
+    const int i = pos >> 5, sh = pos & 31;
+    const unsigned long long lo = (unsigned long long)limb(w, i) | (unsigned long long)limb(w, i + 1) << 32;
+    if (!sh) return lo;
+    return (lo >> sh) | ((unsigned long long)limb(w, i + 2) << (64 - sh));
 }
 
 // 2^e as a double, e in the normal range
@@ -216,38 +224,47 @@ __device__ __forceinline__ double pow2d(int e)
     return __longlong_as_double((long long)(e + 1023) << 52);
 }
 
-// b * 2^scale to the nearest double, ties to even
-static __device__ double big_round(const Big& b, int scale)
+// w * 2^scale to the nearest double, ties to even: the top 53 bits, the next
+// bit and whether any bit below it is set, taken a word at a time.
+static __device__ __noinline__ double big_round(const uint32_t* w, int scale)
 {
     int top = -1;
-    for (int i = 23; i >= 0; i--) {
-        if (b.w[i]) { top = i; break; }
+    for (int i = kLimbs - 1; i >= 0; i--) {
+        if (w[i]) { top = i; break; }
     }
     if (top < 0) return 0.0;
-    const int L = top * 32 + (32 - __clz(b.w[top]));
-    unsigned long long q = 0;
-    const int keep = L < 53 ? L : 53;
-    for (int i = L - 1; i >= L - keep; i--) q = (q << 1) | big_bit(b, i);
-    int e = L - keep + scale;
-    if (L > 53) {
-        const uint32_t half = big_bit(b, L - 54);
-        uint32_t sticky = 0;
-        const int below = L - 54;          // bits [0, below) are the sticky bits
-        for (int i = 0; i < (below >> 5); i++) sticky |= b.w[i];
-        if (below & 31) sticky |= b.w[below >> 5] & ((1u << (below & 31)) - 1u);
-        if (half && (sticky || (q & 1ull))) q++;
+    const int L = top * 32 + (32 - __clz(w[top]));     // bit length
+    if (L <= 53)                                       // exact: at most two limbs
+        return __dmul_rn((double)((unsigned long long)w[0] | (unsigned long long)limb(w, 1) << 32),
+                         pow2d(scale));
+    unsigned long long top64;                          // bits [L-64, L), zero-filled below 0
+    bool sticky = false;
+    if (L >= 64) {
+        top64 = bits64(w, L - 64);
+        const int below = L - 64;                      // bits [0, below) feed the sticky bit
+        for (int i = 0; i < (below >> 5); i++) sticky |= w[i] != 0;
+        if (below & 31) sticky |= (w[below >> 5] & ((1u << (below & 31)) - 1u)) != 0;
+    } else {
+        top64 = bits64(w, 0) << (64 - L);
     }
-    return __dmul_rn((double)q, pow2d(e));
+    unsigned long long q = top64 >> 11;                // the top 53 bits
+    const bool half = (top64 >> 10) & 1ull;
+    sticky |= (top64 & 0x3FFull) != 0;
+    if (half && (sticky || (q & 1ull))) q++;           // 2^53 stays exact
+    return __dmul_rn((double)q, pow2d(L - 53 + scale));
 }
 
 // Window base from the variance: the largest e in 1..249 with
-// var >= K * 2^(2(e-127)-1), else 0.
+// var >= K * 2^(2(e-127)-1), else 0.  K * 2^j is K with j added to its
+// exponent field (exact: every threshold is a normal double), and positive
+// doubles order as their bit patterns, so the search needs no FP64 multiply.
 __device__ __forceinline__ uint32_t window_base(double var, double K)
 {
+    const long long vb = __double_as_longlong(var), kb = __double_as_longlong(K);
     int lo = 0, hi = 249;
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if (var >= __dmul_rn(K, pow2d(2 * mid - 255))) lo = mid;
+        if (vb >= kb + ((long long)(2 * mid - 255) << 52)) lo = mid;
         else hi = mid - 1;
     }
     return (uint32_t)lo;
@@ -256,12 +273,13 @@ __device__ __forceinline__ uint32_t window_base(double var, double K)
 // The last CTA finalises.  Every thread takes one exponent bin and adds its
 // terms, split into 32-bit pieces, to per-limb 64-bit accumulators of the
 // three big sums (positive and negative parts of s1, and s2) with
-// shared-memory atomics; one thread then propagates the carries and does the
-// rounding.  A limb accumulator receives at most 3 * 255 pieces < 2^42.
-constexpr int kLimbs = 24;
+// shared-memory atomics; three threads propagate the carries into 32-bit
+// limbs, and thread 0 does the rounding.  A limb accumulator receives at most
+// 3 * 256 pieces < 2^42.
 struct FinSmem {
     unsigned long long h[256];
     unsigned long long acc[3][kLimbs + 2];     // P, Q, R
+    uint32_t w[3][kLimbs];
     unsigned long long n_fin;
 };
 static_assert(sizeof(FinSmem) <= sizeof(StatsSmem::hist), "finalise scratch fits the histogram");
@@ -278,18 +296,8 @@ __device__ __forceinline__ void acc_add_shl(unsigned long long* acc, unsigned lo
     if (p2) atomicAdd(&acc[limb + 2], (unsigned long long)p2);
 }
 
-__device__ __forceinline__ void acc_to_big(const unsigned long long* acc, Big& b)
-{
-    unsigned long long carry = 0;
-    for (int i = 0; i < kLimbs; i++) {
-        const unsigned long long x = acc[i] + carry;
-        b.w[i] = (uint32_t)x;
-        carry = x >> 32;
-    }
-}
-
 static __device__ __noinline__ void st_finalize(const StatsBins* G, uint64_t n, double K, ez_stats_t* out,
-                                   StatsSmem& S)
+                                                StatsSmem& S)
 {
     const int t = threadIdx.x;
     FinSmem& F = *reinterpret_cast<FinSmem*>(S.hist);
@@ -303,19 +311,27 @@ static __device__ __noinline__ void st_finalize(const StatsBins* G, uint64_t n, 
     F.h[t] = h;
     out->hist[t] = h;
     __syncthreads();
-    if (t < 255 && h) {
+    if (t < 255 && (s1 || s2)) {
         const int sh = (t ? t : 1) - 1;     // v * 2^133 = +-M * 2^sh
         if (s1 > 0) acc_add_shl(F.acc[0], (unsigned long long)s1, sh);
         else if (s1 < 0) acc_add_shl(F.acc[1], (unsigned long long)(-s1), sh);
         if (s2) acc_add_shl(F.acc[2], s2, 2 * sh);   // v^2 * 2^266 = M^2 * 2^(2 sh)
-        atomicAdd(&F.n_fin, h);
+    }
+    if (t < 255 && h) atomicAdd(&F.n_fin, h);
+    __syncthreads();
+    if (t < 3) {
+        unsigned long long carry = 0;
+        for (int i = 0; i < kLimbs; i++) {
+            const unsigned long long x = F.acc[t][i] + carry;
+            F.w[t][i] = (uint32_t)x;
+            carry = x >> 32;
+        }
     }
     __syncthreads();
     if (t != 0) return;
-    Big P, Q, R;
-    acc_to_big(F.acc[0], P);
-    acc_to_big(F.acc[1], Q);
-    acc_to_big(F.acc[2], R);
+    uint32_t* P = F.w[0];
+    uint32_t* Q = F.w[1];
+    const uint32_t* R = F.w[2];
     const unsigned long long n_fin = F.n_fin;
     double s1d;
     if (big_cmp(P, Q) >= 0) {

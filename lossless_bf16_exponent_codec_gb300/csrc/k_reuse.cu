@@ -26,7 +26,7 @@
 // from the payload, writes them back into the cache and stores the merged
 // BF16 values straight into the gathered full buffer.
 #include "ez_internal.h"
-#include "ez_stats.cuh"
+#include "ez_common.cuh"
 #include "ez_bytes.cuh"
 
 namespace ezk {

@@ -36,6 +36,26 @@ k_stats(const uint16_t* __restrict__ x, uint64_t n, uint64_t L, uint32_t first, 
     const int t = threadIdx.x;
     st_begin(S, (uint32_t)(8 * t) < nv ? (uint32_t)xt[8 * t] : 0xFFFFFFFFu);
     const uint32_t elo = S.elo;
+    if (nv == kStatsTile) {
+        // full tile: no per-group bounds
+#pragma unroll 1
+        for (int g0 = 0; g0 < kStatsLoads; g0 += 4) {
+            uint4 w[4];
+#pragma unroll
+            for (int k = 0; k < 4; k++) w[k] = ld_v4_nc(xt + 8u * (uint32_t)((g0 + k) * kThreads + t));
+#pragma unroll
+            for (int k = 0; k < 4; k++) {
+                const uint32_t ws[4] = {w[k].x, w[k].y, w[k].z, w[k].w};
+#pragma unroll
+                for (int q = 0; q < 4; q++) {
+                    st_add(ws[q] & 0xFFFFu, elo, S);
+                    st_add(ws[q] >> 16, elo, S);
+                }
+            }
+        }
+        if (st_end(S, G + ci, tps)) st_finalize(G + ci, n_s, K, out + ci, S);
+        return;
+    }
 #pragma unroll 1
     for (int g0 = 0; g0 < kStatsLoads; g0 += 4) {
         uint4 w[4];
