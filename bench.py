@@ -192,6 +192,7 @@ def run_ours(args, world, rank, local):
     ru = Codec(n, W, B, Bd.EZ_CODEC_REUSE)
     rc = Codec(n, W, B, Bd.EZ_CODEC_REUSE_CODE3)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    hosts, start = (None, None) if args.no_e2e else pinned_inputs(args, xs)
     s = torch.cuda.current_stream()
     # iteration 0 primes the caches (cold)
     ru.encode_reuse(xs[0], cold=True)
@@ -309,7 +310,7 @@ def run_ours(args, world, rank, local):
                                                g("reuse_code3_decode"), W),
     }
     value = world * PASSES * raw / (step_ms_max * 1e-3) / 1e9
-    e2e = None if args.no_e2e else run_e2e(args, world, xs, c3, ru, rc, s)
+    e2e = None if args.no_e2e else run_e2e(args, world, xs, hosts, start, c3, ru, rc, s)
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
         "steps": K, "warmup": Wm, "ms_per_step": round(step_ms_max, 4),
@@ -332,45 +333,66 @@ def run_ours(args, world, rank, local):
     return line, (rank == 0)
 
 
-def run_e2e(args, world, xs, c3, ru, rc, s):
-    """Same metric through the public calls with host inputs: each step copies
-    the iteration's tensor from pinned host memory, runs the six passes and
-    reads back the three size tables and status words."""
+def pinned_inputs(args, xs):
+    """The e2e inputs in pinned host memory, made once before any timing and
+    touched twice by the device (a pipeline reuses its pinned staging
+    buffers; the first device accesses to a new pinned buffer run at a
+    fraction of the link's rate)."""
     K = min(args.steps, 20)
-    n = N_VALUES
     start = len(xs) - K - 1
     hosts = [xs[start + 1 + k].cpu().pin_memory() for k in range(K)]
     dev = torch.empty_like(xs[0])
-    # prime the caches with the iteration before
-    ru.encode_reuse(xs[start])
-    ru.gather_decode()
-    rc.encode_reuse(xs[start])
-    rc.gather_decode()
+    for _ in range(2):
+        for h in hosts:
+            dev.copy_(h, non_blocking=True)
+    torch.cuda.synchronize()
+    return hosts, start
+
+
+def run_e2e(args, world, xs, hosts, start, c3, ru, rc, s):
+    """Same metric through the public calls with host inputs: each step copies
+    the iteration's tensor from pinned host memory, runs the six passes and
+    reads back the three size tables and status words.  One untimed pass over
+    the K steps warms the host-to-device path (it runs far below the link's
+    rate after a stretch without host traffic); the median of the next three
+    passes is reported (the caches are re-primed before each pass)."""
+    K = len(hosts)
+    n = N_VALUES
+    dev = torch.empty_like(xs[0])
     out_sizes = torch.empty(3 * W_CHUNKS + 3, dtype=torch.int64).pin_memory()
-    torch.cuda.synchronize()
-    barrier(world)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(s)
-    for k in range(K):
-        dev.copy_(hosts[k], non_blocking=True)
-        c3.stats(dev)
-        c3.encode_code3(dev)
-        c3.gather_decode()
-        ru.encode_reuse(dev)
+    times = []
+    for rep in range(4):   # pass 0: untimed warm-up of the host-to-device path
+        # prime the caches with the iteration before
+        ru.encode_reuse(xs[start])
         ru.gather_decode()
-        rc.encode_reuse(dev)
+        rc.encode_reuse(xs[start])
         rc.gather_decode()
-        res = torch.cat([c3.sizes, ru.sizes, rc.sizes, c3.status.long(), ru.status.long(),
-                         rc.status.long()])
-        out_sizes.copy_(res, non_blocking=True)
-    e1.record(s)
-    torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / K
-    ms = reduce_max(world, ms)
+        torch.cuda.synchronize()
+        barrier(world)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        for k in range(K):
+            dev.copy_(hosts[k], non_blocking=True)
+            c3.stats(dev)
+            c3.encode_code3(dev)
+            c3.gather_decode()
+            ru.encode_reuse(dev)
+            ru.gather_decode()
+            rc.encode_reuse(dev)
+            rc.gather_decode()
+            res = torch.cat([c3.sizes, ru.sizes, rc.sizes, c3.status.long(), ru.status.long(),
+                             rc.status.long()])
+            out_sizes.copy_(res, non_blocking=True)
+        e1.record(s)
+        torch.cuda.synchronize()
+        if rep:
+            times.append(e0.elapsed_time(e1) / K)
+    ms = reduce_max(world, statistics.median(times))
     barrier(world)
     return {"value": round(world * PASSES * 2 * n / (ms * 1e-3) / 1e9, 1), "unit": UNIT,
             "ms_per_step": round(ms, 4), "h2d_bytes_per_step": 2 * n,
-            "d2h_bytes_per_step": int(out_sizes.numel() * 8)}
+            "d2h_bytes_per_step": int(out_sizes.numel() * 8),
+            "passes_ms_per_step": [round(t, 4) for t in times]}
 
 
 # ------------------------------------------------------------------ oracle
