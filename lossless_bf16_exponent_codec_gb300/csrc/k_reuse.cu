@@ -452,6 +452,13 @@ __global__ void __launch_bounds__(kThreads, 5) k_reuse_code3(RuC3 a)
     const uint8_t* ct = a.cache + (uint64_t)ci * a.L + v0;
     uint8_t* o = a.out + (uint64_t)ci * a.slot;
     const unsigned long long* sc = a.state_a + (uint64_t)ci * a.tpc;
+    // every group's cache bytes, loaded with the bitmap and the prefix
+    unsigned long long e8[kGroups];
+#pragma unroll
+    for (int g = 0; g < kGroups; g++) {
+        const uint32_t v = 8u * (uint32_t)(g * kThreads + t);
+        e8[g] = v < nv ? ld_group8(ct, v, nv) : 0ull;
+    }
     const unsigned long long P = lt ? ld_relaxed(sc + lt - 1) : 0ull;
     __syncthreads();   // s_bm cleared, s_lut written
     load_bitmap(o, lt, nb, log2B, s_bm, s_pre, &s_agg);
@@ -459,19 +466,16 @@ __global__ void __launch_bounds__(kThreads, 5) k_reuse_code3(RuC3 a)
     const uint64_t plane = rup(cdiv(m, 8), 16);
     uint8_t* pl = o + off_exp;
 
-    unsigned long long e8[kGroups];
     uint32_t emasks = 0;
     unsigned long long packed = 0;
 #pragma unroll
     for (int g = 0; g < kGroups; g++) {
         const uint32_t v = 8u * (uint32_t)(g * kThreads + t);
-        e8[g] = 0;
         if (v >= nv) continue;
         const uint32_t k = v >> log2B;
-        if (!block_changed(s_bm, k)) continue;
+        if (!block_changed(s_bm, k)) { e8[g] = 0; continue; }
         const uint64_t pos = (P + block_rank(s_bm, s_pre, k)) * B + (v - (k << log2B));
-        if (pos + min(8u, nv - v) > m) continue;   // inconsistent totals: nothing past EXP
-        e8[g] = ld_group8(ct, v, nv);
+        if (pos + min(8u, nv - v) > m) { e8[g] = 0; continue; }   // inconsistent totals: nothing past EXP
         const uint32_t vm = vmask_of(v, nv);
         const uint32_t acc = codes_of_bytes(s_lut, (uint32_t)e8[g], (uint32_t)(e8[g] >> 32)) &
                              (vm * 0x01010101u);
