@@ -206,7 +206,7 @@ def run_ours(args, world, rank, local):
     launches = {"stats": 1, "code3_encode": 1, "code3_decode": 1,
                 "reuse_encode": 3,            # split, tile scan, place
                 "reuse_decode": 1,
-                "reuse_code3_encode": 6,      # shard stats, split, scan, code, scan, place
+                "reuse_code3_encode": 5,      # shard stats, split, two scans, place
                 "reuse_code3_decode": 1}
 
     def step(x, evs):

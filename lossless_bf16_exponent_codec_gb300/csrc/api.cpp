@@ -51,6 +51,7 @@ WsView ws_view(const ez_plan_s* p, void* ws)
     v.shard_stats = reinterpret_cast<ez_stats_t*>(b + p->off_shard_stats);
     v.bins = b + p->off_bins;
     v.escbuf = p->off_escbuf ? b + p->off_escbuf : nullptr;
+    v.plbuf = p->off_plbuf ? b + p->off_plbuf : nullptr;
     const uint64_t segs = tile_scan_segments(p->tpc) * p->W;
     v.seg_a = reinterpret_cast<unsigned long long*>(b + p->off_seg);
     v.seg_b = v.seg_a + segs;
@@ -114,9 +115,12 @@ ez_status ez_plan_create(ez_plan* out, const ez_plan_desc* d)
     p->off_seg = off;                                     // two arrays of scan-segment states
     off = rup(off + 2 * W * ezk::tile_scan_segments(tpc) * 8, 256);
     p->zero_bytes = off;
-    // coded reuse: each span's escapes staged at its own offset
+    // coded reuse: each tile's escapes staged at its own offset, its planes
+    // in 3 KB per tile
     p->off_escbuf = coded ? off : 0;
     off = rup(off + (coded ? W * L : 0), 256);
+    p->off_plbuf = coded ? off : 0;
+    off = rup(off + (coded ? W * tpc * 3 * (kTileValues / 8) : 0), 256);
     p->ws_bytes = off;
     *out = p;
     return EZ_OK;

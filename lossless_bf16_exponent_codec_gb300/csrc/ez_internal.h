@@ -14,7 +14,7 @@ struct ez_plan_s {
     uint64_t slot_bytes;     // worst-case payload per shard
     double K;                // 16383 / (14 ln 2)
     // workspace layout (byte offsets); [0, zero_bytes) is cleared per call
-    uint64_t off_ctr, off_info, off_shard_stats, off_bins, off_state_a, off_state_b, off_seg, off_escbuf;
+    uint64_t off_ctr, off_info, off_shard_stats, off_bins, off_state_a, off_state_b, off_seg, off_escbuf, off_plbuf;
     uint64_t zero_bytes, ws_bytes;
     uint32_t n_bins;
 };
@@ -38,6 +38,7 @@ struct WsView {
     unsigned long long* state_b;
     void* bins;                    // StatsBins[n_bins]
     uint8_t* escbuf;               // W * L bytes of staged escapes (coded reuse) or NULL
+    uint8_t* plbuf;                // 3 KB of staged planes per tile (coded reuse) or NULL
     unsigned long long* seg_a;     // scan-segment states, two arrays of W * segments
     unsigned long long* seg_b;
 };

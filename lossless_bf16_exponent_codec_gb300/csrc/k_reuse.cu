@@ -16,9 +16,8 @@
 // Coded variant (EZ_CODEC_REUSE_CODE3): the changed exponents are coded with
 // the 3-bit code of ZipCCL (research digest 3.1) instead of nvCOMP's ANS,
 // whose window comes from the shard's sigma (k_stats over each shard, a
-// launch of its own).  Pass 1 stages the raw exponent stream in the
-// workspace; pass 2 (k_reuse_code3) codes it into planes + escapes inside the
-// payload.
+// launch of its own).  The split codes each tile's changed exponents and
+// stages its planes and escapes; the place step moves them into the payload.
 //
 // Receiver (k_reuse_decode): for W payloads in one launch, each tile reads
 // its slice of the bitmap, looks back for the changed-block prefix, takes
@@ -47,25 +46,13 @@ struct RuEnc {
     uint32_t* abort;
     ShardInfo* info;      // per-shard totals (changed blocks, m)
     ez_stats_t* stats;    // per shard record (caller's or workspace), coded only
+    // coded only: staged planes (3 x 1 KB per tile), staged escapes (the
+    // tile's own kTile bytes of a W*L stream), escape-count tile states
+    uint8_t* plbuf;
+    uint8_t* escbuf;
+    unsigned long long* state_b;
 };
 
-struct RuC3 {
-    const uint8_t* cache;
-    uint8_t* escbuf;               // W*L-byte stream, span t's escapes at t*kTile
-    uint8_t* out;
-    uint64_t slot;
-    uint64_t* sizes;
-    uint32_t* dstatus;
-    uint64_t n, L;
-    uint32_t W, B, log2B, first, count, tpc;
-    int cold;
-    unsigned long long* state_a;   // the split's changed-block aggregates
-    unsigned long long* state;     // escape aggregates of this pass
-    uint32_t* counter;
-    uint32_t* abort;
-    const ShardInfo* info;
-    const ez_stats_t* stats;
-};
 
 struct RuDec {
     const uint8_t* in;
@@ -214,6 +201,32 @@ __device__ __forceinline__ uint32_t block_rank(const uint32_t* s_bm, const uint3
     return s_pre[k >> 5] + __popc(s_bm[k >> 5] & ((1u << (k & 31)) - 1u));
 }
 
+// 3-bit code plane bits / escape flag per exponent value (see k_code3.cu)
+__device__ __forceinline__ uint32_t ru_lut_entry(uint32_t e, uint32_t E0)
+{
+    const uint32_t d = e - E0;
+    const uint32_t code = d < 7u ? d + 1u : 0u;
+    return (code & 1u) | ((code & 2u) << 7) | ((code & 4u) << 14) | (code ? 0u : (1u << 24));
+}
+__device__ __forceinline__ uint32_t lut_b(const uint32_t* lut, uint32_t byte_off)
+{
+    return *reinterpret_cast<const uint32_t*>(reinterpret_cast<const char*>(lut) + byte_off);
+}
+// plane bytes 0..2 and escape mask (byte 3) of 8 exponent bytes
+__device__ __forceinline__ uint32_t codes_of_bytes(const uint32_t* lut, uint32_t lo, uint32_t hi)
+{
+    uint32_t acc = 0;
+    acc += lut_b(lut, (lo << 2) & 0x3FCu);
+    acc += lut_b(lut, (lo >> 6) & 0x3FCu) << 1;
+    acc += lut_b(lut, (lo >> 14) & 0x3FCu) << 2;
+    acc += lut_b(lut, (lo >> 22) & 0x3FCu) << 3;
+    acc += lut_b(lut, (hi << 2) & 0x3FCu) << 4;
+    acc += lut_b(lut, (hi >> 6) & 0x3FCu) << 5;
+    acc += lut_b(lut, (hi >> 14) & 0x3FCu) << 6;
+    acc += lut_b(lut, (hi >> 22) & 0x3FCu) << 7;
+    return acc;
+}
+
 // Step A of both reuse encoders, one CTA per 8192-value tile with no
 // inter-tile dependence: compare the exponents with the sender cache, store
 // the sign+mantissa bytes, build the tile's slice of the changed-block bitmap
@@ -221,9 +234,13 @@ __device__ __forceinline__ uint32_t block_rank(const uint32_t* s_bm, const uint3
 // the cache, and publish the tile's changed-block count as its look-back
 // aggregate.  The updated cache then holds every current exponent at its own
 // position, so the later steps read the changed exponents from it.
-__global__ void __launch_bounds__(kThreads, 5) k_reuse_split(RuEnc a)
+template <bool kCoded>
+__global__ void __launch_bounds__(kThreads, kCoded ? 4 : 5) k_reuse_split(RuEnc a)
 {
     __shared__ uint32_t s_gl[32], s_bm[32], s_pre[32];
+    __shared__ uint32_t s_lut[kCoded ? 256 : 1];
+    __shared__ unsigned long long s_warp[kCoded ? kThreads / 32 : 1];
+    __shared__ __align__(16) uint32_t s_esc32[kCoded ? (kTile + 16) / 4 : 4];
     const int t = threadIdx.x, lane = t & 31, wid = t >> 5;
     if (t < 32) {
         s_gl[t] = 0;
@@ -231,6 +248,14 @@ __global__ void __launch_bounds__(kThreads, 5) k_reuse_split(RuEnc a)
     }
     const TilePos tp = tile_pos(blockIdx.x, a.count, a.tpc);
     const uint32_t ci = tp.ci, lt = tp.lt;
+    if (kCoded) {
+        uint32_t E0 = a.stats[ci].E0;
+        if (E0 > 249u) {
+            if (t == 0 && lt == 0) atomicOr(a.dstatus, EZ_DSTAT_BAD_STATS);
+            E0 = 0;
+        }
+        s_lut[t] = ru_lut_entry((uint32_t)t, E0);
+    }
     const uint32_t r = a.first + ci;
     const uint64_t n_s = shard_values(a.n, a.L, r);
     const uint64_t v0 = (uint64_t)lt * kTile;
@@ -299,6 +324,50 @@ __global__ void __launch_bounds__(kThreads, 5) k_reuse_split(RuEnc a)
         if (t < 16 && rup(bm_bytes, 16) > bm_bytes + t) o[64 + bm_bytes + t] = 0;
         if (t < 16 && rup(n_s, 16) > n_s + t) o[off_sm + n_s + t] = 0;
     }
+    if (!kCoded) return;
+    // coded: the changed exponents' 3-bit code at tile-local stream positions
+    // (rank of the block among the tile's changed blocks * B + offset), the
+    // planes and the escapes staged for the place step
+    uint8_t* pst = a.plbuf + (uint64_t)tp.state * 3 * (kTile / 8);
+    uint32_t emasks = 0;
+    unsigned long long packed = 0;
+#pragma unroll
+    for (int g = 0; g < kGroups; g++) {
+        const uint32_t v = 8u * (uint32_t)(g * kThreads + t);
+        if (v >= nv) continue;
+        const uint32_t k = v >> log2B;
+        if (!block_changed(s_bm, k)) continue;
+        const uint32_t local = block_rank(s_bm, s_pre, k) * B + (v - (k << log2B));
+        const uint32_t acc = codes_of_bytes(s_lut, (uint32_t)e8[g], (uint32_t)(e8[g] >> 32)) &
+                             (vmask_of(v, nv) * 0x01010101u);
+        const uint32_t pb = local >> 3;
+        pst[pb] = (uint8_t)acc;
+        pst[kTile / 8 + pb] = (uint8_t)(acc >> 8);
+        pst[2 * (kTile / 8) + pb] = (uint8_t)(acc >> 16);
+        const uint32_t esc = acc >> 24;
+        emasks |= esc << (8 * g);
+        packed |= (unsigned long long)__popc(esc) << (16 * g);
+    }
+    unsigned long long total;
+    const unsigned long long excl = block_excl_scan(packed, s_warp, &total);
+    const uint32_t agg2 = (uint32_t)((total & 0xFFFFull) + ((total >> 16) & 0xFFFFull) +
+                                     ((total >> 32) & 0xFFFFull) + (total >> 48));
+    if (t == 0) st_relaxed(a.state_b + tp.state, (unsigned long long)agg2);
+    uint8_t* s_esc = reinterpret_cast<uint8_t*>(s_esc32);
+    uint32_t gbase = 0;
+#pragma unroll
+    for (int g = 0; g < kGroups; g++) {
+        const uint32_t mm = (emasks >> (8 * g)) & 0xFFu;
+        const uint32_t kmax = __reduce_max_sync(kFull, (uint32_t)__popc(mm));
+        if (kmax) {
+            const uint32_t q = gbase + (uint32_t)((excl >> (16 * g)) & 0xFFFFull);
+            stage_selected(s_esc, q, mm, (uint32_t)e8[g], (uint32_t)(e8[g] >> 32), kmax);
+        }
+        gbase += (uint32_t)((total >> (16 * g)) & 0xFFFFull);
+    }
+    __syncthreads();
+    uint32_t* dst = reinterpret_cast<uint32_t*>(a.escbuf + (uint64_t)ci * a.L + v0);
+    for (uint32_t i = (uint32_t)t; i < (agg2 + 3) / 4; i += kThreads) dst[i] = s_esc32[i];
 }
 
 // This tile's slice of the bitmap, read back from the payload: s_bm, the
@@ -393,121 +462,6 @@ __global__ void __launch_bounds__(kThreads, 6) k_reuse_place(RuEnc a)
     }
 }
 
-// 3-bit code plane bits / escape flag per exponent value (see k_code3.cu)
-__device__ __forceinline__ uint32_t ru_lut_entry(uint32_t e, uint32_t E0)
-{
-    const uint32_t d = e - E0;
-    const uint32_t code = d < 7u ? d + 1u : 0u;
-    return (code & 1u) | ((code & 2u) << 7) | ((code & 4u) << 14) | (code ? 0u : (1u << 24));
-}
-__device__ __forceinline__ uint32_t lut_b(const uint32_t* lut, uint32_t byte_off)
-{
-    return *reinterpret_cast<const uint32_t*>(reinterpret_cast<const char*>(lut) + byte_off);
-}
-// plane bytes 0..2 and escape mask (byte 3) of 8 exponent bytes
-__device__ __forceinline__ uint32_t codes_of_bytes(const uint32_t* lut, uint32_t lo, uint32_t hi)
-{
-    uint32_t acc = 0;
-    acc += lut_b(lut, (lo << 2) & 0x3FCu);
-    acc += lut_b(lut, (lo >> 6) & 0x3FCu) << 1;
-    acc += lut_b(lut, (lo >> 14) & 0x3FCu) << 2;
-    acc += lut_b(lut, (lo >> 22) & 0x3FCu) << 3;
-    acc += lut_b(lut, (hi << 2) & 0x3FCu) << 4;
-    acc += lut_b(lut, (hi >> 6) & 0x3FCu) << 5;
-    acc += lut_b(lut, (hi >> 14) & 0x3FCu) << 6;
-    acc += lut_b(lut, (hi >> 22) & 0x3FCu) << 7;
-    return acc;
-}
-
-// Coded variant, step B (after the tile scan of the split's counts): one CTA
-// per 8192-value span codes the span's changed exponents, read from the
-// cache, with the shard's window into the planes at stream position
-// (prefix + rank) * B + offset (a multiple of 8: plane bytes are whole),
-// writes the span's escapes (value order) as whole words at the span's own
-// offset of the escape stream, and publishes its escape count.
-__global__ void __launch_bounds__(kThreads, 5) k_reuse_code3(RuC3 a)
-{
-    __shared__ uint32_t s_lut[256];
-    __shared__ uint32_t s_bm[32], s_pre[32], s_agg;
-    __shared__ unsigned long long s_warp[kThreads / 32];
-    __shared__ __align__(16) uint32_t s_esc32[(kTile + 16) / 4];
-    uint8_t* s_esc = reinterpret_cast<uint8_t*>(s_esc32);
-    const int t = threadIdx.x;
-    if (t < 32) s_bm[t] = 0;
-    const TilePos tp = tile_pos(blockIdx.x, a.count, a.tpc);
-    const uint32_t ci = tp.ci, lt = tp.lt;
-    const uint32_t r = a.first + ci;
-    const uint64_t n_s = shard_values(a.n, a.L, r);
-    const uint64_t v0 = (uint64_t)lt * kTile;
-    const uint32_t nv = v0 < n_s ? (uint32_t)umin64(kTile, n_s - v0) : 0u;
-    const uint32_t B = a.B, log2B = a.log2B;
-    const uint64_t nb = cdiv(n_s, B);
-    uint32_t E0 = a.stats[ci].E0;
-    if (E0 > 249u) {
-        if (t == 0 && lt == 0) atomicOr(a.dstatus, EZ_DSTAT_BAD_STATS);
-        E0 = 0;
-    }
-    s_lut[t] = ru_lut_entry((uint32_t)t, E0);
-    const uint64_t off_exp = ru_off_exp(n_s, B, true);
-    const uint8_t* ct = a.cache + (uint64_t)ci * a.L + v0;
-    uint8_t* o = a.out + (uint64_t)ci * a.slot;
-    const unsigned long long* sc = a.state_a + (uint64_t)ci * a.tpc;
-    // every group's cache bytes, loaded with the bitmap and the prefix
-    unsigned long long e8[kGroups];
-#pragma unroll
-    for (int g = 0; g < kGroups; g++) {
-        const uint32_t v = 8u * (uint32_t)(g * kThreads + t);
-        e8[g] = v < nv ? ld_group8(ct, v, nv) : 0ull;
-    }
-    const unsigned long long P = lt ? ld_relaxed(sc + lt - 1) : 0ull;
-    __syncthreads();   // s_bm cleared, s_lut written
-    load_bitmap(o, lt, nb, log2B, s_bm, s_pre, &s_agg);
-    const uint64_t m = a.info[ci].m;
-    const uint64_t plane = rup(cdiv(m, 8), 16);
-    uint8_t* pl = o + off_exp;
-
-    uint32_t emasks = 0;
-    unsigned long long packed = 0;
-#pragma unroll
-    for (int g = 0; g < kGroups; g++) {
-        const uint32_t v = 8u * (uint32_t)(g * kThreads + t);
-        if (v >= nv) continue;
-        const uint32_t k = v >> log2B;
-        if (!block_changed(s_bm, k)) { e8[g] = 0; continue; }
-        const uint64_t pos = (P + block_rank(s_bm, s_pre, k)) * B + (v - (k << log2B));
-        if (pos + min(8u, nv - v) > m) { e8[g] = 0; continue; }   // inconsistent totals: nothing past EXP
-        const uint32_t vm = vmask_of(v, nv);
-        const uint32_t acc = codes_of_bytes(s_lut, (uint32_t)e8[g], (uint32_t)(e8[g] >> 32)) &
-                             (vm * 0x01010101u);
-        const uint64_t pb = pos >> 3;
-        pl[pb] = (uint8_t)acc;
-        pl[plane + pb] = (uint8_t)(acc >> 8);
-        pl[2 * plane + pb] = (uint8_t)(acc >> 16);
-        const uint32_t esc = acc >> 24;
-        emasks |= esc << (8 * g);
-        packed |= (unsigned long long)__popc(esc) << (16 * g);
-    }
-    unsigned long long total;
-    const unsigned long long excl = block_excl_scan(packed, s_warp, &total);
-    const uint32_t agg2 = (uint32_t)((total & 0xFFFFull) + ((total >> 16) & 0xFFFFull) +
-                                     ((total >> 32) & 0xFFFFull) + (total >> 48));
-    if (t == 0) st_relaxed(a.state + tp.state, (unsigned long long)agg2);
-    uint32_t gbase = 0;
-#pragma unroll
-    for (int g = 0; g < kGroups; g++) {
-        const uint32_t mm = (emasks >> (8 * g)) & 0xFFu;
-        const uint32_t kmax = __reduce_max_sync(kFull, (uint32_t)__popc(mm));
-        if (kmax) {
-            const uint32_t q = gbase + (uint32_t)((excl >> (16 * g)) & 0xFFFFull);
-            stage_selected(s_esc, q, mm, (uint32_t)e8[g], (uint32_t)(e8[g] >> 32), kmax);
-        }
-        gbase += (uint32_t)((total >> (16 * g)) & 0xFFFFull);
-    }
-    __syncthreads();
-    uint32_t* dst = reinterpret_cast<uint32_t*>(a.escbuf + (uint64_t)ci * a.L + v0);
-    for (uint32_t i = (uint32_t)t; i < (agg2 + 3) / 4; i += kThreads) dst[i] = s_esc32[i];
-}
-
 // Bytes [b, b+16) of a run of `len` bytes at dst, from d (bytes past len
 // are not written).
 constexpr uint32_t kSpecBytes = 2048;
@@ -515,17 +469,22 @@ constexpr uint32_t kSpecBytes = 2048;
 __device__ __forceinline__ void store_run16(uint8_t* dst, uint32_t b, uint32_t len, const uint4& d)
 {
     if (b >= len) return;
+    if (b + 16 <= len && (reinterpret_cast<uintptr_t>(dst + b) & 15u) == 0) {
+        *reinterpret_cast<uint4*>(dst + b) = d;   // a whole aligned 16-byte piece
+        return;
+    }
     const uint32_t ws[4] = {d.x, d.y, d.z, d.w};
 #pragma unroll
     for (uint32_t i = 0; i < 16; i++)
         if (b + i < len) dst[b + i] = (uint8_t)(ws[i >> 2] >> (8 * (i & 3)));
 }
 
-// Coded variant, step C (after the tile scan of the escape counts): both
-// index entries of the span, its escapes copied from the stream into place,
-// and on the tile holding the shard's last value the header, the padding and
-// the size.
-__global__ void __launch_bounds__(kThreads, 8) k_reuse_place_esc(RuC3 a)
+// Coded variant, place step (after the scans of the changed-block and the
+// escape counts): the tile's staged plane bytes go to stream byte
+// (prefix * B) / 8 of each plane, its staged escapes to their prefix; both
+// prefixes are the span's index entries; the tile holding the shard's last
+// value writes the header, the padding and the size.
+__global__ void __launch_bounds__(kThreads, 8) k_reuse_place_coded(RuEnc a)
 {
     const int t = threadIdx.x;
     const TilePos tp = tile_pos(blockIdx.x, a.count, a.tpc);
@@ -534,31 +493,43 @@ __global__ void __launch_bounds__(kThreads, 8) k_reuse_place_esc(RuC3 a)
     const uint64_t n_s = shard_values(a.n, a.L, r);
     const uint64_t v0 = (uint64_t)lt * kTile;
     const uint32_t B = a.B;
+    const uint64_t spans = cdiv(n_s, kTile);
     const uint64_t off_idx = ru_off_idx(n_s, B), off_exp = ru_off_exp(n_s, B, true);
     uint8_t* o = a.out + (uint64_t)ci * a.slot;
     const uint64_t m = a.info[ci].m;
     const uint64_t plane = rup(cdiv(m, 8), 16);
     uint8_t* pl = o + off_exp;
     uint8_t* esc_sec = pl + 3 * plane;
-    const unsigned long long* sa = a.state_a + (uint64_t)ci * a.tpc;
-    const unsigned long long* sb = a.state + (uint64_t)ci * a.tpc;
-    const uint8_t* src = a.escbuf + (uint64_t)ci * a.L + v0;
-    // a speculative 2 KB window of the staged bytes, loaded with the
-    // prefixes; longer runs (rare) finish with a byte loop
-    uint4 d0 = make_uint4(0, 0, 0, 0);
+    const unsigned long long* sa = a.state + (uint64_t)ci * a.tpc;
+    const unsigned long long* sb = a.state_b + (uint64_t)ci * a.tpc;
+    // staged planes (3 KB) and a 2 KB window of staged escapes, loaded with
+    // the prefixes
+    const uint8_t* pst = a.plbuf + (uint64_t)tp.state * 3 * (kTile / 8);
+    const uint8_t* est = a.escbuf + (uint64_t)ci * a.L + v0;
     const uint32_t b0 = 16u * (uint32_t)t;
-    if (b0 < kSpecBytes && v0 + b0 + 16 <= a.L) d0 = ld_v4_nc(src + b0);
+    uint4 dp = make_uint4(0, 0, 0, 0), de = make_uint4(0, 0, 0, 0);
+    if (b0 < 3 * (kTile / 8)) dp = ld_v4_nc(pst + b0);
+    if (b0 < kSpecBytes && v0 + b0 + 16 <= a.L) de = ld_v4_nc(est + b0);
     const unsigned long long P = lt ? ld_relaxed(sa + lt - 1) : 0ull;
+    const unsigned long long Pend = ld_relaxed(sa + lt);
     const unsigned long long Q = lt ? ld_relaxed(sb + lt - 1) : 0ull;
     const unsigned long long Qend = ld_relaxed(sb + lt);
+    // this span's stream slice [P*B, end): whole blocks, the last span up to m
+    uint64_t start = P * B, end = lt + 1 < spans ? Pend * B : m;
+    if (lt >= spans || end < start || end > m || end - start > kTile) end = start = 0;
+    const uint32_t nbytes = (uint32_t)cdiv(end - start, 8);
     const uint32_t agg2 = Qend >= Q && Qend - Q <= kTile ? (uint32_t)(Qend - Q) : 0u;
     if (t == 0 && v0 < n_s) {
         unsigned long long* idx = reinterpret_cast<unsigned long long*>(o + off_idx);
         idx[2 * lt] = P;
         idx[2 * lt + 1] = Q;
     }
-    if (b0 < kSpecBytes) store_run16(esc_sec + Q, b0, agg2, d0);
-    for (uint32_t b = kSpecBytes + (uint32_t)t; b < agg2; b += kThreads) esc_sec[Q + b] = src[b];
+    if (b0 < 3 * (kTile / 8)) {
+        const uint32_t p = b0 / (kTile / 8), off = b0 % (kTile / 8);
+        store_run16(pl + (uint64_t)p * plane + start / 8, off, nbytes, dp);
+    }
+    if (b0 < kSpecBytes) store_run16(esc_sec + Q, b0, agg2, de);
+    for (uint32_t b = kSpecBytes + (uint32_t)t; b < agg2; b += kThreads) esc_sec[Q + b] = est[b];
     const uint32_t fin_tile = n_s ? (uint32_t)((n_s - 1) / kTile) : 0u;
     if (lt == fin_tile) {
         uint32_t E0 = a.stats[ci].E0;
@@ -867,43 +838,26 @@ cudaError_t launch_reuse_encode(const ez_plan_s* p, const uint16_t* x, uint32_t 
         e = launch_shard_stats(p, x, first, count, a.stats, w, s);
         if (e != cudaSuccess) return e;
     }
-    k_reuse_split<<<tiles, kThreads, 0, s>>>(a);
+    if (!coded) {
+        k_reuse_split<false><<<tiles, kThreads, 0, s>>>(a);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        e = launch_tile_scan(p, w.state_a, count, w.seg_a, w.counters + 4, w.counters + 7, dstatus, s);
+        if (e != cudaSuccess) return e;
+        k_reuse_place<<<tiles, kThreads, 0, s>>>(a);
+        return cudaGetLastError();
+    }
+    a.plbuf = w.plbuf;
+    a.escbuf = w.escbuf;
+    a.state_b = w.state_b;
+    k_reuse_split<true><<<tiles, kThreads, 0, s>>>(a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     e = launch_tile_scan(p, w.state_a, count, w.seg_a, w.counters + 4, w.counters + 7, dstatus, s);
     if (e != cudaSuccess) return e;
-    if (!coded) {
-        k_reuse_place<<<tiles, kThreads, 0, s>>>(a);
-        return cudaGetLastError();
-    }
-    RuC3 b;
-    b.cache = cache;
-    b.out = out;
-    b.slot = p->slot_bytes;
-    b.sizes = sizes;
-    b.dstatus = dstatus;
-    b.n = p->n;
-    b.L = p->L;
-    b.W = p->W;
-    b.B = p->B;
-    b.log2B = a.log2B;
-    b.first = first;
-    b.count = count;
-    b.tpc = p->tpc;
-    b.cold = a.cold;
-    b.state_a = w.state_a;
-    b.state = w.state_b;
-    b.counter = w.counters + 2;
-    b.abort = w.counters + 7;
-    b.info = w.info;
-    b.stats = a.stats;
-    b.escbuf = w.escbuf;
-    k_reuse_code3<<<tiles, kThreads, 0, s>>>(b);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
     e = launch_tile_scan(p, w.state_b, count, w.seg_b, w.counters + 5, w.counters + 7, dstatus, s);
     if (e != cudaSuccess) return e;
-    k_reuse_place_esc<<<tiles, kThreads, 0, s>>>(b);
+    k_reuse_place_coded<<<tiles, kThreads, 0, s>>>(a);
     return cudaGetLastError();
 }
 
