@@ -91,6 +91,22 @@ __device__ __forceinline__ unsigned long long insert_selected(unsigned long long
     return (e8 & ~bm) | (x & bm);
 }
 
+// insert_selected with the expansion selectors in shared memory (s_elo/s_ehi
+// = ByteTables::exp_lo/exp_hi) and the byte mask made from the bit spread
+// s_spread[m] (bit i -> bit 8i): mask = spread * 255.
+__device__ __forceinline__ unsigned long long insert_selected_s(unsigned long long e8, uint32_t m,
+                                                                uint32_t c_lo, uint32_t c_hi,
+                                                                const uint32_t* s_elo,
+                                                                const uint32_t* s_ehi,
+                                                                const unsigned long long* s_spread)
+{
+    const unsigned long long x = (unsigned long long)__byte_perm(c_lo, c_hi, s_ehi[m]) << 32 |
+                                 __byte_perm(c_lo, c_hi, s_elo[m]);
+    const unsigned long long sp = s_spread[m];
+    const unsigned long long bm = (sp << 8) - sp;
+    return (e8 & ~bm) | (x & bm);
+}
+
 __device__ __forceinline__ unsigned long long spread_bits(uint32_t b)
 {
     return __ldg(&kByteTables.spread[b]);

@@ -396,10 +396,13 @@ __global__ void __launch_bounds__(kThreads, 6) k_code3_decode(C3Dec a)
     __shared__ uint32_t s_bad, s_E0;
     __shared__ unsigned long long s_nesc;
     __shared__ unsigned long long s_spread[256];
-    __shared__ unsigned long long s_warp[kThreads / 32];
+    __shared__ uint32_t s_elo[256], s_ehi[256];
+    __shared__ uint32_t s_warp32[kThreads / 32];
     __shared__ __align__(16) uint32_t s_esc32[(kTile + 32) / 4];
     const int t = threadIdx.x;
     s_spread[t] = spread_bits((uint32_t)t);
+    s_elo[t] = kByteTables.exp_lo[t];
+    s_ehi[t] = kByteTables.exp_hi[t];
     const uint32_t ci = blockIdx.x / a.tpc, lt = blockIdx.x % a.tpc;
     const uint32_t c = a.first + ci;
     const uint64_t n_c = shard_values(a.n, a.L, c);
@@ -415,43 +418,35 @@ __global__ void __launch_bounds__(kThreads, 6) k_code3_decode(C3Dec a)
     const uint64_t n_idx = cdiv(n_c, kTile);
     // all fixed sections inside the payload: safe to read before the header
     const bool fixed_ok = (off & 15u) == 0 && end >= off && avail >= sec_esc;
-    const uint8_t* sm_t = p + 128 + v0;
-    const uint8_t* pl_t = p + sec_pl + v0 / 8;
-    const bool full = nv == (uint32_t)kTile;
-
-    uint2 smv[kGroups];
-    uint32_t pb[kGroups];    // plane bytes p0 | p1 << 8 | p2 << 16
+    // thread t owns the 32 consecutive values [32t, 32t + 32) of the tile:
+    // 32 sign+mantissa bytes, one 32-bit word of each plane
+    const uint32_t tv = 32u * (uint32_t)t;
+    const uint32_t cnt_v = tv < nv ? umin64(32u, nv - tv) : 0u;   // values of this thread
+    const uint8_t* sm_t = p + 128 + v0 + tv;
+    const uint8_t* pl_t = p + sec_pl + v0 / 8 + tv / 8;
+    uint4 smw[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+    uint32_t p0 = 0, p1 = 0, p2 = 0;
     unsigned long long idx_here = 0, idx_next = 0;
     if (fixed_ok) {
-#pragma unroll
-        for (int g = 0; g < kGroups; g++) {
-            const uint32_t j = (uint32_t)(g * kThreads + t);
-            const uint32_t v = 8u * j;
-            smv[g] = make_uint2(0, 0);
-            pb[g] = 0;
-            if (full || v + 8 <= nv) {
-                smv[g] = __ldg(reinterpret_cast<const uint2*>(sm_t + v));
-            } else if (v < nv) {
-                uint32_t lo = 0, hi = 0;
-                for (uint32_t i = 0; i < nv - v; i++) {
-                    const uint32_t b = sm_t[v + i];
-                    if (i < 4) lo |= b << (8 * i);
-                    else hi |= b << (8 * (i - 4));
-                }
-                smv[g] = make_uint2(lo, hi);
+        if (cnt_v == 32) {
+            smw[0] = ld_v4_nc(sm_t);
+            smw[1] = ld_v4_nc(sm_t + 16);
+            p0 = __ldg(reinterpret_cast<const uint32_t*>(pl_t));
+            p1 = __ldg(reinterpret_cast<const uint32_t*>(pl_t + plane));
+            p2 = __ldg(reinterpret_cast<const uint32_t*>(pl_t + 2 * plane));
+        } else if (cnt_v) {
+            uint32_t w8[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+            for (uint32_t i = 0; i < cnt_v; i++) w8[i >> 2] |= (uint32_t)sm_t[i] << (8 * (i & 3));
+            smw[0] = make_uint4(w8[0], w8[1], w8[2], w8[3]);
+            smw[1] = make_uint4(w8[4], w8[5], w8[6], w8[7]);
+            for (uint32_t i = 0; i < cdiv(cnt_v, 8); i++) {
+                p0 |= (uint32_t)pl_t[i] << (8 * i);
+                p1 |= (uint32_t)pl_t[plane + i] << (8 * i);
+                p2 |= (uint32_t)pl_t[2 * plane + i] << (8 * i);
             }
-            if (full || v < nv)
-                pb[g] = (uint32_t)__ldg(pl_t + j) | (uint32_t)__ldg(pl_t + plane + j) << 8 |
-                        (uint32_t)__ldg(pl_t + 2 * plane + j) << 16;
         }
         if (lt < n_idx) idx_here = __ldg(reinterpret_cast<const unsigned long long*>(p + sec_idx) + lt);
         if (lt + 1 < n_idx) idx_next = __ldg(reinterpret_cast<const unsigned long long*>(p + sec_idx) + lt + 1);
-    } else {
-#pragma unroll
-        for (int g = 0; g < kGroups; g++) {
-            smv[g] = make_uint2(0, 0);
-            pb[g] = 0;
-        }
     }
     if (t == 0) {
         // the oracle's order of checks
@@ -480,18 +475,28 @@ __global__ void __launch_bounds__(kThreads, 6) k_code3_decode(C3Dec a)
         }
         s_bad = bad;
     }
-    uint32_t emasks = 0;
-    unsigned long long packed = 0;
+    // escapes of the thread's 32 values: code 0 in all three planes
+    const uint32_t vmask = cnt_v >= 32 ? 0xFFFFFFFFu : ((1u << cnt_v) - 1u);
+    const uint32_t esc = ~(p0 | p1 | p2) & vmask;
+    const uint32_t my = __popc(esc);
+    // block exclusive scan of one count per thread
+    const int lane = t & 31, wid = t >> 5;
+    uint32_t x = my;
 #pragma unroll
-    for (int g = 0; g < kGroups; g++) {
-        const uint32_t v = 8u * (uint32_t)(g * kThreads + t);
-        const uint32_t vmask = full ? 0xFFu : (v >= nv ? 0u : (nv - v >= 8 ? 0xFFu : ((1u << (nv - v)) - 1u)));
-        const uint32_t esc = ~(pb[g] | pb[g] >> 8 | pb[g] >> 16) & vmask;
-        emasks |= esc << (8 * g);
-        packed |= (unsigned long long)__popc(esc) << (16 * g);
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(kFull, x, o);
+        if (lane >= o) x += y;
     }
-    unsigned long long total;
-    const unsigned long long excl = block_excl_scan(packed, s_warp, &total);   // also publishes s_bad
+    if (lane == 31) s_warp32[wid] = x;
+    __syncthreads();   // also publishes s_bad
+    uint32_t wpre = 0, agg32 = 0;
+#pragma unroll
+    for (int i = 0; i < kThreads / 32; i++) {
+        const uint32_t v = s_warp32[i];
+        wpre += i < wid ? v : 0u;
+        agg32 += v;
+    }
+    const uint32_t excl = wpre + x - my;
     const uint32_t bad = s_bad;
     if (bad) {
         if (lt == 0 && t == 0) atomicOr(a.dstatus, bad);
@@ -499,8 +504,7 @@ __global__ void __launch_bounds__(kThreads, 6) k_code3_decode(C3Dec a)
     }
     const uint32_t E0 = s_E0;
     const unsigned long long n_esc = s_nesc;
-    const unsigned long long agg = (total & 0xFFFFull) + ((total >> 16) & 0xFFFFull) +
-                                   ((total >> 32) & 0xFFFFull) + (total >> 48);
+    const unsigned long long agg = agg32;
     // index checks (tiles past the chunk's end carry no entry and no escapes)
     const unsigned long long P = lt < n_idx ? idx_here : n_esc;
     const unsigned long long want = lt + 1 < n_idx ? idx_next : n_esc;
@@ -517,32 +521,30 @@ __global__ void __launch_bounds__(kThreads, 6) k_code3_decode(C3Dec a)
     for (uint32_t i = (uint32_t)t; i < words; i += kThreads)
         s_esc32[i] = __ldg(reinterpret_cast<const uint32_t*>(esc_w) + i);
     __syncthreads();
-
-    uint16_t* ot = a.out + (uint64_t)ci * a.L + v0;
-    uint32_t gbase = 0;
+    if (!cnt_v) return;
+    uint16_t* ot = a.out + (uint64_t)ci * a.L + v0 + tv;
+    const uint32_t smv[8] = {smw[0].x, smw[0].y, smw[0].z, smw[0].w, smw[1].x, smw[1].y, smw[1].z, smw[1].w};
 #pragma unroll
-    for (int g = 0; g < kGroups; g++) {
-        const uint32_t v = 8u * (uint32_t)(g * kThreads + t);
-        const uint32_t r = gbase + (uint32_t)((excl >> (16 * g)) & 0xFFFFull);
-        gbase += (uint32_t)((total >> (16 * g)) & 0xFFFFull);
-        if (!full && v >= nv) continue;
-        const unsigned long long c8 = s_spread[pb[g] & 0xFFu] | (s_spread[(pb[g] >> 8) & 0xFFu] << 1) |
-                                      (s_spread[(pb[g] >> 16) & 0xFFu] << 2);
+    for (int g = 0; g < 4; g++) {
+        const uint32_t b0 = (p0 >> (8 * g)) & 0xFFu, b1 = (p1 >> (8 * g)) & 0xFFu, b2 = (p2 >> (8 * g)) & 0xFFu;
+        const unsigned long long c8 = s_spread[b0] | (s_spread[b1] << 1) | (s_spread[b2] << 2);
         unsigned long long e8 = codes_to_exps(c8, E0);
-        const uint32_t m = (emasks >> (8 * g)) & 0xFFu;
+        const uint32_t m = (esc >> (8 * g)) & 0xFFu;
         if (m) {
+            const uint32_t r = excl + __popc(esc & ((1u << (8 * g)) - 1u));
             uint32_t c_lo, c_hi;
             load_unaligned8(s_esc32, r + sh, c_lo, c_hi);
-            e8 = insert_selected(e8, m, c_lo, c_hi);
+            e8 = insert_selected_s(e8, m, c_lo, c_hi, s_elo, s_ehi, s_spread);
         }
         uint4 o4;
-        merge4(smv[g].x, (uint32_t)e8, o4.x, o4.y);
-        merge4(smv[g].y, (uint32_t)(e8 >> 32), o4.z, o4.w);
-        if (full || v + 8 <= nv) {
+        merge4(smv[2 * g], (uint32_t)e8, o4.x, o4.y);
+        merge4(smv[2 * g + 1], (uint32_t)(e8 >> 32), o4.z, o4.w);
+        const uint32_t v = 8u * (uint32_t)g;
+        if (v + 8 <= cnt_v) {
             st_v4(ot + v, o4);
-        } else {
+        } else if (v < cnt_v) {
             const uint32_t hw[4] = {o4.x, o4.y, o4.z, o4.w};
-            for (uint32_t i = 0; i < nv - v; i++) ot[v + i] = (uint16_t)(hw[i >> 1] >> (16 * (i & 1)));
+            for (uint32_t i = 0; i < cnt_v - v; i++) ot[v + i] = (uint16_t)(hw[i >> 1] >> (16 * (i & 1)));
         }
     }
 }

@@ -570,9 +570,14 @@ __global__ void __launch_bounds__(kThreads, 6) k_reuse_decode(RuDec a)
     __shared__ uint32_t s_bm[32], s_pre[32], s_agg;
     __shared__ unsigned long long s_warp[kThreads / 32];
     __shared__ unsigned long long s_spread[kCoded ? 256 : 1];
+    __shared__ uint32_t s_elo[kCoded ? 256 : 1], s_ehi[kCoded ? 256 : 1];
     __shared__ __align__(16) uint32_t s_esc32[kCoded ? (kTile + 32) / 4 : 4];
     const int t = threadIdx.x;
-    if (kCoded) s_spread[t] = spread_bits((uint32_t)t);
+    if (kCoded) {
+        s_spread[t] = spread_bits((uint32_t)t);
+        s_elo[t] = kByteTables.exp_lo[t];
+        s_ehi[t] = kByteTables.exp_hi[t];
+    }
     if (t < 32) s_bm[t] = 0;
     const uint32_t ci = blockIdx.x / a.tpc, lt = blockIdx.x % a.tpc;
     const uint32_t r = a.first + ci;
@@ -773,7 +778,7 @@ __global__ void __launch_bounds__(kThreads, 6) k_reuse_decode(RuDec a)
             if (mm) {
                 uint32_t c_lo, c_hi;
                 load_unaligned8(s_esc32, q + sh, c_lo, c_hi);
-                e = insert_selected(e, mm, c_lo, c_hi);
+                e = insert_selected_s(e, mm, c_lo, c_hi, s_elo, s_ehi, s_spread);
             }
             const uint32_t cnt = min(8u, nv - (8u * (uint32_t)(g * kThreads + t)));
             ev[g] = cnt >= 8 ? e : (e & byte_mask((1u << cnt) - 1u));
