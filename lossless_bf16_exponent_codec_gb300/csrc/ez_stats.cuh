@@ -14,7 +14,13 @@
 // cell of a 16 x 256 histogram.  Since a cell fixes sign and M, the cell
 // counts determine the window's exact per-exponent count, sum of +-M and
 // sum of M^2; they are folded once per tile.  Values outside the window
-// (and zeros, subnormals, Inf/NaN) go straight to per-exponent bins.  The
+// (and zeros, subnormals, Inf/NaN) go straight to per-exponent bins.
+//
+// The cell of an in-window value is s << 11 | d << 7 | m (sign, binade
+// offset, mantissa).  With y = (h | 0x8000) - Elo * 128, a 16-bit lane holds
+// 1 << 15 | d << 7 | m and has bits 11..14 clear exactly when the value lies
+// in the window, so the cell is one PRMT (the sign, replicated) and one LOP3
+// away from y; the cell increment is a predicated shared reduction.  The
 // CTA then adds its bins to per-shard global bins (64-bit atomics); the last
 // CTA of the shard turns the bins into one big integer per sum, rounds it to
 // nearest even, and derives var, sigma and the window base E0.
@@ -38,7 +44,7 @@ struct StatsBins {                 // per shard, in the workspace (zeroed per ca
 constexpr int kStatsWin = 16;                  // binades in a CTA's window
 constexpr uint32_t kStatsMaxValues = 1u << 23;
 struct StatsSmem {
-    uint32_t hist[kStatsWin * 256];            // [d][sign << 7 | mantissa]
+    uint32_t hist[2 * kStatsWin * 128];        // [sign][d][mantissa]
     unsigned long long s2[256];
     uint32_t cnt[256];
     int s1[256];
@@ -85,48 +91,87 @@ __device__ __forceinline__ void st_begin(StatsSmem& S, uint32_t h0)
     __syncthreads();
 }
 
-// A value outside the window: straight into the per-exponent bins.
+// A value outside the window: straight into the per-exponent bins (a zero
+// only counts).
 __device__ __forceinline__ void st_add_slow(uint32_t h, StatsSmem& S)
 {
     const uint32_t E = exp_of(h);
     atomicAdd(&S.cnt[E], 1u);
-    if (E != 255u) {
-        const uint32_t M = (E ? 128u : 0u) | (h & 0x7Fu);
+    const uint32_t M = (E ? 128u : 0u) | (h & 0x7Fu);
+    if (E != 255u && M) {
         atomicAdd(&S.s1[E], (h & 0x8000u) ? -(int)M : (int)M);
         atomicAdd(&S.s2[E], (unsigned long long)(M * M));
     }
 }
 
-// One value h (16 bits).
+// One value h (16 bits), any value.
 __device__ __forceinline__ void st_add(uint32_t h, uint32_t elo, StatsSmem& S)
 {
     // v = sign*256 + E - Elo; in the window iff its low byte is below 16
     // (Elo <= 239 keeps E = 255 and E < Elo outside)
     const uint32_t v = (h >> 7) - elo;
     if ((v & 0xF0u) == 0) {
-        const uint32_t sm = (h & 0x7Fu) | ((h >> 8) & 0x80u);
-        atomicAdd(&S.hist[((v & 0xFu) << 8) | sm], 1u);
+        atomicAdd(&S.hist[((h >> 4) & 0x800u) | ((v & 0xFu) << 7) | (h & 0x7Fu)], 1u);
     } else {
         st_add_slow(h, S);
     }
 }
 
-// The two values of a 32-bit word.  bias2 = (0x8000 - Elo) * 0x10001: each
-// 16-bit lane of w2 = 0x8000 + (sign*256 + E) - Elo, so its low byte is
-// E - Elo for a value in the window and no lane borrows from the other.
-__device__ __forceinline__ uint32_t st_bias2(uint32_t elo) { return (0x8000u - elo) * 0x10001u; }
+// Lane-exact window offsets of the two values of word x: y = (x | 0x8000) -
+// Elo * 0x00800080 (e7 = (Elo << 7) * 0x10001).  Setting the low lane's sign
+// bit keeps it from borrowing out of the high lane.
+__device__ __forceinline__ uint32_t st_y(uint32_t x, uint32_t e7) { return (x | 0x8000u) - e7; }
 
-__device__ __forceinline__ void st_add2(uint32_t x, uint32_t bias2, uint32_t elo, StatsSmem& S)
+// Cell of one lane: t = that lane's y in bits 0..15 (bits above don't
+// matter), m = its sign replicated over bits 8..15 of a word otherwise zero.
+// Bits 0..10 and 12..14 come from t, bit 11 is ~t & m = the sign (bit 11 of
+// an in-window t is clear), bit 15 and up give ~t & m = 0.
+__device__ __forceinline__ uint32_t st_cell(uint32_t t, uint32_t m)
 {
-    const uint32_t w2 = ((x >> 7) & 0x01FF01FFu) + bias2;
-    if ((w2 & 0x00F000F0u) == 0) {
-        const uint32_t i0 = ((w2 & 0xFu) << 8) | (x & 0x7Fu) | ((x >> 8) & 0x80u);
-        const uint32_t i1 = ((w2 >> 8) & 0xF00u) | ((x >> 16) & 0x7Fu) | (x >> 24 & 0x80u);
-        atomicAdd(&S.hist[i0], 1u);
-        atomicAdd(&S.hist[i1], 1u);
-    } else {
-        st_add(x & 0xFFFFu, elo, S);
-        st_add(x >> 16, elo, S);
+    uint32_t r;
+    asm("lop3.b32 %0, %1, %2, %3, 0xC2;" : "=r"(r) : "r"(t), "r"(0x77FFu), "r"(m));
+    return r;
+}
+__device__ __forceinline__ uint32_t st_sign_lo(uint32_t x)
+{
+    uint32_t r;
+    asm("prmt.b32 %0, %1, 0, 0x4494;" : "=r"(r) : "r"(x));
+    return r;
+}
+__device__ __forceinline__ uint32_t st_sign_hi(uint32_t x)
+{
+    uint32_t r;
+    asm("prmt.b32 %0, %1, 0, 0x44B4;" : "=r"(r) : "r"(x));
+    return r;
+}
+
+// hist[cell] += 1 when (y & mask) == 0 (the lane is in the window); addr is
+// the cell's shared-memory address.
+__device__ __forceinline__ void st_red_if_in(uint32_t addr, uint32_t y, uint32_t mask)
+{
+    asm volatile("{ .reg .pred q; .reg .b32 t; and.b32 t, %1, %2; setp.eq.u32 q, t, 0;"
+                 " @q red.shared.add.u32 [%0], 1; }"
+                 :: "r"(addr), "r"(y), "r"(mask) : "memory");
+}
+
+// Eight values (one 16-byte load): in-window values take their cell, the
+// others (rare) the per-exponent bins.
+__device__ __forceinline__ void st_add8(const uint4& w, uint32_t e7, uint32_t hist_base, StatsSmem& S)
+{
+    const uint32_t xs[4] = {w.x, w.y, w.z, w.w};
+    uint32_t y[4];
+#pragma unroll
+    for (int q = 0; q < 4; q++) {
+        y[q] = st_y(xs[q], e7);
+        st_red_if_in(hist_base + 4u * st_cell(y[q], st_sign_lo(xs[q])), y[q], 0x7800u);
+        st_red_if_in(hist_base + 4u * st_cell(y[q] >> 16, st_sign_hi(xs[q])), y[q], 0x78000000u);
+    }
+    if ((y[0] | y[1] | y[2] | y[3]) & 0x78007800u) {
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+            if (y[q] & 0x7800u) st_add_slow(xs[q] & 0xFFFFu, S);
+            if (y[q] & 0x78000000u) st_add_slow(xs[q] >> 16, S);
+        }
     }
 }
 
@@ -137,13 +182,13 @@ __device__ __forceinline__ bool st_end(StatsSmem& S, StatsBins* G, uint32_t expe
     const int t = threadIdx.x;
     const uint32_t elo = S.elo;
     __syncthreads();
-    // histogram row d (16 threads per row, 16 cells each; one sign per thread)
+    // cells [s][d][m]: 8 threads per (s, d) row, 16 mantissas each
     {
-        const uint32_t d = (uint32_t)t >> 4, part = (uint32_t)t & 15u;
-        const uint4* row = reinterpret_cast<const uint4*>(&S.hist[(d << 8) | (part << 4)]);
+        const uint32_t s = (uint32_t)t >> 7, d = ((uint32_t)t >> 3) & 15u, part = (uint32_t)t & 7u;
+        const uint4* row = reinterpret_cast<const uint4*>(&S.hist[(s << 11) | (d << 7) | (part << 4)]);
         uint32_t c = 0, s1 = 0;
         unsigned long long s2 = 0;
-        uint32_t M = 128u + ((part & 7u) << 4);
+        uint32_t M = 128u + (part << 4);
 #pragma unroll
         for (int q = 0; q < 4; q++) {
             const uint4 x = row[q];
@@ -161,10 +206,10 @@ __device__ __forceinline__ bool st_end(StatsSmem& S, StatsBins* G, uint32_t expe
             s1 += __shfl_xor_sync(kFull, s1, o);
             s2 += __shfl_xor_sync(kFull, s2, o);
         }
-        if ((part & 7u) == 0 && c) {
+        if (part == 0 && c) {
             const uint32_t E = elo + d;
             atomicAdd(&S.cnt[E], c);
-            atomicAdd(&S.s1[E], (part & 8u) ? -(int)s1 : (int)s1);
+            atomicAdd(&S.s1[E], s ? -(int)s1 : (int)s1);
             atomicAdd(&S.s2[E], s2);
         }
     }

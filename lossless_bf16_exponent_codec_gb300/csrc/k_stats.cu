@@ -17,12 +17,12 @@ static_assert(sizeof(ez_stats_t) == 2120, "ez_stats_t layout");
 constexpr int kStatsLoads = 16;                             // 16-B loads per thread
 constexpr uint32_t kStatsTile = kThreads * kStatsLoads * 8;   // 32768 values
 
-// One CTA per tile of 32768 values of one shard, 6 resident CTAs per SM;
+// One CTA per tile of 32768 values of one shard, 8 resident CTAs per SM;
 // every thread keeps four 16-byte loads in flight and adds their 32 values to
 // the CTA's histogram.  Shard ci = tile / tps holds values [ci*L, ci*L + n_s)
 // of x; its CTAs fold into bins G[ci], and the last of them writes out[ci].
 // The a1 statistics of a whole tensor are the case of one shard.
-__global__ void __launch_bounds__(kThreads, 6)
+__global__ void __launch_bounds__(kThreads, 8)
 k_stats(const uint16_t* __restrict__ x, uint64_t n, uint64_t L, uint32_t first, uint32_t W,
         uint32_t tps, StatsBins* G, ez_stats_t* out, double K)
 {
@@ -36,6 +36,8 @@ k_stats(const uint16_t* __restrict__ x, uint64_t n, uint64_t L, uint32_t first, 
     const int t = threadIdx.x;
     st_begin(S, (uint32_t)(8 * t) < nv ? (uint32_t)xt[8 * t] : 0xFFFFFFFFu);
     const uint32_t elo = S.elo;
+    const uint32_t e7 = (elo << 7) * 0x10001u;
+    const uint32_t hb = (uint32_t)__cvta_generic_to_shared(S.hist);
     if (nv == kStatsTile) {
         // full tile: no per-group bounds
 #pragma unroll 1
@@ -44,48 +46,18 @@ k_stats(const uint16_t* __restrict__ x, uint64_t n, uint64_t L, uint32_t first, 
 #pragma unroll
             for (int k = 0; k < 4; k++) w[k] = ld_v4_nc(xt + 8u * (uint32_t)((g0 + k) * kThreads + t));
 #pragma unroll
-            for (int k = 0; k < 4; k++) {
-                const uint32_t ws[4] = {w[k].x, w[k].y, w[k].z, w[k].w};
-#pragma unroll
-                for (int q = 0; q < 4; q++) {
-                    st_add(ws[q] & 0xFFFFu, elo, S);
-                    st_add(ws[q] >> 16, elo, S);
-                }
-            }
+            for (int k = 0; k < 4; k++) st_add8(w[k], e7, hb, S);
         }
         if (st_end(S, G + ci, tps)) st_finalize(G + ci, n_s, K, out + ci, S);
         return;
     }
 #pragma unroll 1
-    for (int g0 = 0; g0 < kStatsLoads; g0 += 4) {
-        uint4 w[4];
-#pragma unroll
-        for (int k = 0; k < 4; k++) {
-            const uint32_t v = 8u * (uint32_t)((g0 + k) * kThreads + t);
-            if (v + 8 <= nv) {
-                w[k] = ld_v4_nc(xt + v);
-            } else {
-                uint32_t h[8];
-#pragma unroll
-                for (int i = 0; i < 8; i++) h[i] = (v + i < nv) ? (uint32_t)xt[v + i] : 0u;
-                w[k] = make_uint4(h[0] | h[1] << 16, h[2] | h[3] << 16, h[4] | h[5] << 16,
-                                  h[6] | h[7] << 16);
-            }
-        }
-#pragma unroll
-        for (int k = 0; k < 4; k++) {
-            const uint32_t v = 8u * (uint32_t)((g0 + k) * kThreads + t);
-            if (v + 8 <= nv) {
-                const uint32_t ws[4] = {w[k].x, w[k].y, w[k].z, w[k].w};
-#pragma unroll
-                for (int q = 0; q < 4; q++) {
-                    st_add(ws[q] & 0xFFFFu, elo, S);
-                    st_add(ws[q] >> 16, elo, S);
-                }
-            } else if (v < nv) {
-                for (int i = 0; i < 8; i++)
-                    if (v + i < nv) st_add(half_of(w[k], i), elo, S);
-            }
+    for (int g = 0; g < kStatsLoads; g++) {
+        const uint32_t v = 8u * (uint32_t)(g * kThreads + t);
+        if (v + 8 <= nv) {
+            st_add8(ld_v4_nc(xt + v), e7, hb, S);
+        } else if (v < nv) {
+            for (uint32_t i = v; i < nv; i++) st_add(xt[i], elo, S);
         }
     }
     if (st_end(S, G + ci, tps)) st_finalize(G + ci, n_s, K, out + ci, S);
