@@ -107,6 +107,39 @@ __device__ __forceinline__ unsigned long long insert_selected_s(unsigned long lo
     return (e8 & ~bm) | (x & bm);
 }
 
+// ---- table-free forms (integer multiplies instead of shared-memory lookups) ----
+// Bits 0..3 of n4 (n4 < 16) to bits 0, 8, 16, 24: the four shifted copies
+// n4 << 7k (k = 0..3) do not overlap, so the product has no carries and bit
+// 8k of it is bit k of n4.
+__device__ __forceinline__ uint32_t spread4(uint32_t n4) { return (n4 * 0x00204081u) & 0x01010101u; }
+
+// 3-bit codes of 8 values from one byte of each code plane: byte i of the
+// result is bit i of b0 | bit i of b1 << 1 | bit i of b2 << 2.
+__device__ __forceinline__ unsigned long long codes8(uint32_t b0, uint32_t b1, uint32_t b2)
+{
+    const uint32_t lo = spread4(b0 & 15u) | spread4(b1 & 15u) << 1 | spread4(b2 & 15u) << 2;
+    const uint32_t hi = spread4(b0 >> 4) | spread4(b1 >> 4) << 1 | spread4(b2 >> 4) << 2;
+    return (unsigned long long)hi << 32 | lo;
+}
+
+// e8 with the bytes at the set bits of m (m < 256) replaced, in order, by the
+// compact bytes (c_lo, c_hi).  Byte i takes compact byte rank(i) = the set
+// bits of m below i: the bit spreads of m's nibbles times 0x01010100 are the
+// exclusive byte prefix sums, packed to nibbles they are PRMT selectors.
+__device__ __forceinline__ unsigned long long insert_selected_a(unsigned long long e8, uint32_t m,
+                                                                uint32_t c_lo, uint32_t c_hi)
+{
+    const uint32_t bl = spread4(m & 15u), bh = spread4(m >> 4);
+    const uint32_t pl = bl * 0x01010100u;
+    const uint32_t ph = bh * 0x01010100u + (uint32_t)__popc(m & 15u) * 0x01010101u;
+    const uint32_t sel_lo = __byte_perm(pl | (pl >> 4), 0u, 0x4420u);
+    const uint32_t sel_hi = __byte_perm(ph | (ph >> 4), 0u, 0x4420u);
+    const unsigned long long x = (unsigned long long)__byte_perm(c_lo, c_hi, sel_hi) << 32 |
+                                 __byte_perm(c_lo, c_hi, sel_lo);
+    const unsigned long long bm = (unsigned long long)(bh * 255u) << 32 | (bl * 255u);
+    return (e8 & ~bm) | (x & bm);
+}
+
 __device__ __forceinline__ unsigned long long spread_bits(uint32_t b)
 {
     return __ldg(&kByteTables.spread[b]);

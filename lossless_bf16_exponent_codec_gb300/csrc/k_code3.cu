@@ -395,14 +395,9 @@ __global__ void __launch_bounds__(kThreads, 6) k_code3_decode(C3Dec a)
 {
     __shared__ uint32_t s_bad, s_E0;
     __shared__ unsigned long long s_nesc;
-    __shared__ unsigned long long s_spread[256];
-    __shared__ uint32_t s_elo[256], s_ehi[256];
     __shared__ uint32_t s_warp32[kThreads / 32];
     __shared__ __align__(16) uint32_t s_esc32[(kTile + 32) / 4];
     const int t = threadIdx.x;
-    s_spread[t] = spread_bits((uint32_t)t);
-    s_elo[t] = kByteTables.exp_lo[t];
-    s_ehi[t] = kByteTables.exp_hi[t];
     const uint32_t ci = blockIdx.x / a.tpc, lt = blockIdx.x % a.tpc;
     const uint32_t c = a.first + ci;
     const uint64_t n_c = shard_values(a.n, a.L, c);
@@ -527,14 +522,13 @@ __global__ void __launch_bounds__(kThreads, 6) k_code3_decode(C3Dec a)
 #pragma unroll
     for (int g = 0; g < 4; g++) {
         const uint32_t b0 = (p0 >> (8 * g)) & 0xFFu, b1 = (p1 >> (8 * g)) & 0xFFu, b2 = (p2 >> (8 * g)) & 0xFFu;
-        const unsigned long long c8 = s_spread[b0] | (s_spread[b1] << 1) | (s_spread[b2] << 2);
-        unsigned long long e8 = codes_to_exps(c8, E0);
+        unsigned long long e8 = codes_to_exps(codes8(b0, b1, b2), E0);
         const uint32_t m = (esc >> (8 * g)) & 0xFFu;
         if (m) {
             const uint32_t r = excl + __popc(esc & ((1u << (8 * g)) - 1u));
             uint32_t c_lo, c_hi;
             load_unaligned8(s_esc32, r + sh, c_lo, c_hi);
-            e8 = insert_selected_s(e8, m, c_lo, c_hi, s_elo, s_ehi, s_spread);
+            e8 = insert_selected_a(e8, m, c_lo, c_hi);
         }
         uint4 o4;
         merge4(smv[2 * g], (uint32_t)e8, o4.x, o4.y);

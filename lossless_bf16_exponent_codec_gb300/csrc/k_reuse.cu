@@ -569,15 +569,8 @@ __global__ void __launch_bounds__(kThreads, 6) k_reuse_decode(RuDec a)
     __shared__ unsigned long long s_hdr[4];   // n_changed, m, n_esc
     __shared__ uint32_t s_bm[32], s_pre[32], s_agg;
     __shared__ unsigned long long s_warp[kThreads / 32];
-    __shared__ unsigned long long s_spread[kCoded ? 256 : 1];
-    __shared__ uint32_t s_elo[kCoded ? 256 : 1], s_ehi[kCoded ? 256 : 1];
     __shared__ __align__(16) uint32_t s_esc32[kCoded ? (kTile + 32) / 4 : 4];
     const int t = threadIdx.x;
-    if (kCoded) {
-        s_spread[t] = spread_bits((uint32_t)t);
-        s_elo[t] = kByteTables.exp_lo[t];
-        s_ehi[t] = kByteTables.exp_hi[t];
-    }
     if (t < 32) s_bm[t] = 0;
     const uint32_t ci = blockIdx.x / a.tpc, lt = blockIdx.x % a.tpc;
     const uint32_t r = a.first + ci;
@@ -768,9 +761,7 @@ __global__ void __launch_bounds__(kThreads, 6) k_reuse_decode(RuDec a)
             const uint32_t q = gbase + (uint32_t)((excl >> (16 * g)) & 0xFFFFull);
             gbase += (uint32_t)((total >> (16 * g)) & 0xFFFFull);
             if (!chg[g]) continue;
-            const unsigned long long c8 = s_spread[pbs[g] & 0xFFu] |
-                                          (s_spread[(pbs[g] >> 8) & 0xFFu] << 1) |
-                                          (s_spread[(pbs[g] >> 16) & 0xFFu] << 2);
+            const unsigned long long c8 = codes8(pbs[g] & 0xFFu, (pbs[g] >> 8) & 0xFFu, (pbs[g] >> 16) & 0xFFu);
             unsigned long long e = (E0 == 0)
                 ? ((c8 | 0x8080808080808080ull) - 0x0101010101010101ull) & 0x7F7F7F7F7F7F7F7Full
                 : c8 + (unsigned long long)(E0 - 1) * 0x0101010101010101ull;
@@ -778,7 +769,7 @@ __global__ void __launch_bounds__(kThreads, 6) k_reuse_decode(RuDec a)
             if (mm) {
                 uint32_t c_lo, c_hi;
                 load_unaligned8(s_esc32, q + sh, c_lo, c_hi);
-                e = insert_selected_s(e, mm, c_lo, c_hi, s_elo, s_ehi, s_spread);
+                e = insert_selected_a(e, mm, c_lo, c_hi);
             }
             const uint32_t cnt = min(8u, nv - (8u * (uint32_t)(g * kThreads + t)));
             ev[g] = cnt >= 8 ? e : (e & byte_mask((1u << cnt) - 1u));
