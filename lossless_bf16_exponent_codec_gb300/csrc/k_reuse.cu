@@ -146,6 +146,19 @@ __device__ __forceinline__ void st_group8(uint8_t* p, uint32_t v, uint32_t nv, u
         for (uint32_t i = 0; v + i < nv && i < 8; i++) p[v + i] = (uint8_t)(x >> (8 * i));
     }
 }
+// The first cnt (<= 16) bytes at p as a 16-byte word, zero above; stores of
+// the first cnt bytes of w.
+__device__ __forceinline__ uint4 ld_bytes16(const uint8_t* p, uint32_t cnt)
+{
+    uint32_t w[4] = {0, 0, 0, 0};
+    for (uint32_t i = 0; i < cnt && i < 16; i++) w[i >> 2] |= (uint32_t)p[i] << (8 * (i & 3));
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+__device__ __forceinline__ void st_bytes16(uint8_t* p, const uint4& w, uint32_t cnt)
+{
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+    for (uint32_t i = 0; i < cnt && i < 16; i++) p[i] = (uint8_t)(ws[i >> 2] >> (8 * (i & 3)));
+}
 __device__ __forceinline__ uint32_t vmask_of(uint32_t v, uint32_t nv)
 {
     return v >= nv ? 0u : (nv - v >= 8 ? 0xFFu : ((1u << (nv - v)) - 1u));
@@ -562,6 +575,47 @@ __device__ __forceinline__ uint4 ld16_plain(const void* p) { return *reinterpret
 // -- so the exponents read always lie inside the EXP section.  Every thread
 // reads the payload offsets, then the bitmap slice, sign+mantissa bytes and
 // index entries are loaded before thread 0's header checks complete.
+// The oracle's checks of a reuse payload's header, in its order; 0 or the
+// first failing status.  Reads the 64 header bytes only when they lie inside
+// the payload.  *E0 and hdr[0..2] = n_changed, m, n_esc are set when it
+// returns 0.
+__device__ __forceinline__ uint32_t ru_check_header(const uint8_t* p, uint64_t off, uint64_t avail,
+                                                 bool order_bad, uint32_t B, uint32_t r, uint64_t n_s,
+                                                 uint64_t nb, bool kCoded, uint32_t* E0_out,
+                                                 unsigned long long* hdr)
+{
+    uint32_t bad = 0;
+    *E0_out = 0;
+    if (order_bad) bad = EZ_DSTAT_BAD_SIZE;
+    if (!bad && (off & 15u)) bad = EZ_DSTAT_MISALIGNED;
+    if (!bad && avail < 64) bad = EZ_DSTAT_BAD_SIZE;
+    if (!bad) {
+        const uint4 h0 = ld16_plain(p), h1 = ld16_plain(p + 16), h2 = ld16_plain(p + 32),
+                    h3 = ld16_plain(p + 48);
+        const uint32_t flags = (h0.y >> 8) & 0xFFu, E0 = (h0.y >> 16) & 0xFFu;
+        const uint64_t n_hdr = (uint64_t)h1.x | (uint64_t)h1.y << 32;
+        const uint64_t n_changed = (uint64_t)h1.z | (uint64_t)h1.w << 32;
+        const uint64_t m = (uint64_t)h2.x | (uint64_t)h2.y << 32;
+        const uint64_t n_esc = (uint64_t)h2.z | (uint64_t)h2.w << 32;
+        const uint64_t total = (uint64_t)h3.x | (uint64_t)h3.y << 32;
+        const bool coded = flags & 1u;
+        if (h0.x != 0x55525A45u || (h0.y & 0xFFu) != 2u || (flags & ~3u) || (h0.y >> 24) != 0 ||
+            h0.z != B || h0.w != r || n_hdr != n_s || coded != kCoded)
+            bad = EZ_DSTAT_BAD_HEADER;
+        else if (coded ? E0 > 249 : (E0 != 0 || n_esc != 0))
+            bad = EZ_DSTAT_BAD_HEADER;
+        else if (n_changed > nb || m > n_s || n_esc > m)
+            bad = EZ_DSTAT_BAD_COUNT;
+        else if (total != ru_bytes(n_s, B, m, coded, n_esc) || total > avail)
+            bad = EZ_DSTAT_BAD_SIZE;
+        *E0_out = E0;
+        hdr[0] = n_changed;
+        hdr[1] = m;
+        hdr[2] = n_esc;
+    }
+    return bad;
+}
+
 template <bool kCoded>
 __global__ void __launch_bounds__(kThreads, 6) k_reuse_decode(RuDec a)
 {
@@ -626,36 +680,9 @@ __global__ void __launch_bounds__(kThreads, 6) k_reuse_decode(RuDec a)
         }
     }
     if (t == 0) {
-        uint32_t bad = 0;
-        s_E0 = 0;
-        if (order_bad) bad = EZ_DSTAT_BAD_SIZE;
-        if (!bad && (off & 15u)) bad = EZ_DSTAT_MISALIGNED;
-        if (!bad && avail < 64) bad = EZ_DSTAT_BAD_SIZE;
-        if (!bad) {
-            const uint4 h0 = ld16_plain(p), h1 = ld16_plain(p + 16), h2 = ld16_plain(p + 32),
-                        h3 = ld16_plain(p + 48);
-            const uint32_t flags = (h0.y >> 8) & 0xFFu, E0 = (h0.y >> 16) & 0xFFu;
-            const uint64_t n_hdr = (uint64_t)h1.x | (uint64_t)h1.y << 32;
-            const uint64_t n_changed = (uint64_t)h1.z | (uint64_t)h1.w << 32;
-            const uint64_t m = (uint64_t)h2.x | (uint64_t)h2.y << 32;
-            const uint64_t n_esc = (uint64_t)h2.z | (uint64_t)h2.w << 32;
-            const uint64_t total = (uint64_t)h3.x | (uint64_t)h3.y << 32;
-            const bool coded = flags & 1u;
-            if (h0.x != 0x55525A45u || (h0.y & 0xFFu) != 2u || (flags & ~3u) || (h0.y >> 24) != 0 ||
-                h0.z != B || h0.w != r || n_hdr != n_s || coded != kCoded)
-                bad = EZ_DSTAT_BAD_HEADER;
-            else if (coded ? E0 > 249 : (E0 != 0 || n_esc != 0))
-                bad = EZ_DSTAT_BAD_HEADER;
-            else if (n_changed > nb || m > n_s || n_esc > m)
-                bad = EZ_DSTAT_BAD_COUNT;
-            else if (total != ru_bytes(n_s, B, m, coded, n_esc) || total > avail)
-                bad = EZ_DSTAT_BAD_SIZE;
-            s_E0 = E0;
-            s_hdr[0] = n_changed;
-            s_hdr[1] = m;
-            s_hdr[2] = n_esc;
-        }
-        s_bad = bad;
+        uint32_t e0;
+        s_bad = ru_check_header(p, off, avail, order_bad, B, r, n_s, nb, kCoded, &e0, s_hdr);
+        s_E0 = e0;
     }
     if (bmb) atomicOr(&s_bm[t >> 2], bmb << (8 * (t & 3)));
     __syncthreads();
@@ -720,41 +747,56 @@ __global__ void __launch_bounds__(kThreads, 6) k_reuse_decode(RuDec a)
         const uint64_t plane = rup(cdiv(m, 8), 16);
         const uint8_t* esc_sec = ex + 3 * plane;
         uint32_t pbs[kGroups];
-        uint32_t emasks = 0;
-        unsigned long long packed = 0;
 #pragma unroll
         for (int g = 0; g < kGroups; g++) {
             pbs[g] = 0;
             if (!chg[g]) continue;
-            const uint32_t v = 8u * (uint32_t)(g * kThreads + t);
-            const uint32_t cnt = min(8u, nv - v);
             const uint64_t pb = pos[g] >> 3;
             pbs[g] = (uint32_t)ex[pb] | (uint32_t)ex[plane + pb] << 8 | (uint32_t)ex[2 * plane + pb] << 16;
+        }
+        // stage the span's escapes while the plane bytes are in flight: the
+        // index gives their range [Q, Qn); the scan below checks it against
+        // the planes, and a range the header does not allow is not staged.
+        // The escape section starts on a 16-byte boundary (EXP section and
+        // planes are multiples of 16), so whole words up to rup(n_esc, 4)
+        // stay inside the padded payload.
+        const unsigned long long Q = lt < spans ? ie_here : n_esc;
+        const unsigned long long Qn = lt + 1 < spans ? ie_next : n_esc;
+        const uint8_t* esc_w = esc_sec + (Q & ~3ull);
+        const uint32_t sh = (uint32_t)(Q & 3ull);
+        const uint32_t words = (Q <= Qn && Qn <= n_esc && Qn - Q <= nv) ? (uint32_t)((Qn - Q + sh + 3) >> 2) : 0u;
+        {
+            const uint32_t* src = reinterpret_cast<const uint32_t*>(esc_w);
+            const uint32_t i0 = (uint32_t)t, i1 = (uint32_t)t + kThreads;
+            const uint32_t w0 = i0 < words ? __ldg(src + i0) : 0u;
+            const uint32_t w1 = i1 < words ? __ldg(src + i1) : 0u;
+            if (i0 < words) s_esc32[i0] = w0;
+            if (i1 < words) s_esc32[i1] = w1;
+            for (uint32_t i = (uint32_t)t + 2 * kThreads; i < words; i += kThreads) s_esc32[i] = __ldg(src + i);
+        }
+        uint32_t emasks = 0;
+        unsigned long long packed = 0;
+#pragma unroll
+        for (int g = 0; g < kGroups; g++) {
+            if (!chg[g]) continue;
+            const uint32_t v = 8u * (uint32_t)(g * kThreads + t);
+            const uint32_t cnt = min(8u, nv - v);
             const uint32_t vm = cnt >= 8 ? 0xFFu : ((1u << cnt) - 1u);
             const uint32_t esc = ~(pbs[g] | pbs[g] >> 8 | pbs[g] >> 16) & vm;
             emasks |= esc << (8 * g);
             packed |= (unsigned long long)__popc(esc) << (16 * g);
         }
+        // the scan's barrier also publishes the staged escapes
         unsigned long long total;
         const unsigned long long excl = block_excl_scan(packed, s_warp, &total);
         const unsigned long long agg2 = (total & 0xFFFFull) + ((total >> 16) & 0xFFFFull) +
                                         ((total >> 32) & 0xFFFFull) + (total >> 48);
-        const unsigned long long Q = lt < spans ? ie_here : n_esc;
         const bool eok = (lt != 0 || spans == 0 || Q == 0) && Q <= n_esc && agg2 <= n_esc - Q &&
-                         (lt >= spans || Q + agg2 == (lt + 1 < spans ? ie_next : n_esc));
+                         (lt >= spans || Q + agg2 == Qn);
         if (!eok) {
             if (t == 0) atomicOr(a.dstatus, EZ_DSTAT_BAD_COUNT);
             return;
         }
-        const uint8_t* esc_w = esc_sec + (Q & ~3ull);
-        const uint32_t sh = (uint32_t)(Q & 3ull);
-        const uint32_t words = (uint32_t)((agg2 + sh + 3) >> 2);
-        // the escape section starts on a 16-byte boundary (EXP section and
-        // planes are multiples of 16), so whole words up to rup(n_esc, 4)
-        // stay inside the padded payload
-        for (uint32_t i = (uint32_t)t; i < words; i += kThreads)
-            s_esc32[i] = __ldg(reinterpret_cast<const uint32_t*>(esc_w) + i);
-        __syncthreads();
         uint32_t gbase = 0;
 #pragma unroll
         for (int g = 0; g < kGroups; g++) {
@@ -789,6 +831,256 @@ __global__ void __launch_bounds__(kThreads, 6) k_reuse_decode(RuDec a)
         } else {
             const uint32_t hw[4] = {o4.x, o4.y, o4.z, o4.w};
             for (uint32_t i = 0; i < nv - v; i++) ot[v + i] = (uint16_t)(hw[i >> 1] >> (16 * (i & 1)));
+        }
+    }
+}
+
+// Block size B >= 32: thread t owns the 32 consecutive values [32t, 32t + 32)
+// of the span.  They lie in one block, so one bitmap bit says where all of
+// them come from, and a changed block's stream position is a multiple of 32:
+// the thread reads its exponents as two aligned 16-byte words (raw) or one
+// aligned 32-bit word of each code plane (coded), its sign+mantissa bytes
+// and cache bytes as 16-byte words, and writes its 32 outputs as four
+// 16-byte stores.  Checks and statuses are those of k_reuse_decode.
+template <bool kCoded>
+__global__ void __launch_bounds__(kThreads, 6) k_reuse_decode32(RuDec a)
+{
+    __shared__ uint32_t s_bad, s_E0;
+    __shared__ unsigned long long s_hdr[4];   // n_changed, m, n_esc
+    __shared__ uint32_t s_bm[32], s_pre[32], s_agg;
+    __shared__ uint32_t s_warp32[kThreads / 32];
+    __shared__ __align__(16) uint32_t s_esc32[kCoded ? (kTile + 32) / 4 : 4];
+    const int t = threadIdx.x;
+    if (t < 32) s_bm[t] = 0;
+    const uint32_t ci = blockIdx.x / a.tpc, lt = blockIdx.x % a.tpc;
+    const uint32_t r = a.first + ci;
+    const uint64_t n_s = shard_values(a.n, a.L, r);
+    const uint64_t v0 = (uint64_t)lt * kTile;
+    const uint32_t nv = v0 < n_s ? (uint32_t)umin64(kTile, n_s - v0) : 0u;
+    const uint32_t B = a.B, log2B = a.log2B;
+    const uint64_t nb = cdiv(n_s, B);
+    const uint64_t bm_bytes = cdiv(nb, 8);
+    const uint64_t spans = cdiv(n_s, kTile);
+    const uint64_t off = a.offsets ? __ldg(a.offsets + ci) : 0ull;
+    uint64_t avail = a.single_avail;
+    bool order_bad = false;
+    if (a.offsets) {
+        const uint64_t end = __ldg(a.offsets + ci + 1);
+        order_bad = end < off;
+        avail = order_bad ? 0ull : end - off;
+    }
+    const uint8_t* p = a.in + off;
+    const uint64_t off_sm = ru_off_sm(n_s, B), off_idx = ru_off_idx(n_s, B);
+    const uint64_t off_exp = ru_off_exp(n_s, B, kCoded);
+    const uint32_t stride = ru_idx_stride(kCoded);
+    const bool fixed_ok = !order_bad && (off & 15u) == 0 && avail >= off_exp;
+
+    const uint32_t nbt = (uint32_t)kTile >> log2B;
+    const uint64_t bm0 = (uint64_t)lt * (nbt / 8);
+    const uint32_t tv = 32u * (uint32_t)t;
+    const uint32_t cnt_v = tv < nv ? min(32u, nv - tv) : 0u;
+    uint32_t bmb = 0;
+    uint4 smw[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+    unsigned long long ib_here = 0, ib_next = 0, ie_here = 0, ie_next = 0;
+    if (fixed_ok) {
+        if ((uint32_t)t < nbt / 8 && bm0 + t < bm_bytes) {
+            bmb = p[64 + bm0 + t];
+            if (bm0 + t == bm_bytes - 1 && (nb & 7)) bmb &= (1u << (nb & 7)) - 1u;
+        }
+        const uint8_t* sm_t = p + off_sm + v0 + tv;
+        if (cnt_v == 32) {
+            smw[0] = ld_v4_nc(sm_t);
+            smw[1] = ld_v4_nc(sm_t + 16);
+        } else if (cnt_v) {
+            smw[0] = ld_bytes16(sm_t, cnt_v);
+            smw[1] = ld_bytes16(sm_t + 16, cnt_v > 16 ? cnt_v - 16 : 0u);
+        }
+        const unsigned long long* idx = reinterpret_cast<const unsigned long long*>(p + off_idx);
+        const uint32_t sw = stride / 8;
+        if (lt < spans) {
+            ib_here = __ldg(idx + sw * lt);
+            if (kCoded) ie_here = __ldg(idx + sw * lt + 1);
+        }
+        if (lt + 1 < spans) {
+            ib_next = __ldg(idx + sw * (lt + 1));
+            if (kCoded) ie_next = __ldg(idx + sw * (lt + 1) + 1);
+        }
+    }
+    if (t == 0) {
+        uint32_t e0;
+        s_bad = ru_check_header(p, off, avail, order_bad, B, r, n_s, nb, kCoded, &e0, s_hdr);
+        s_E0 = e0;
+    }
+    if (bmb) atomicOr(&s_bm[t >> 2], bmb << (8 * (t & 3)));
+    __syncthreads();
+    if (s_bad) {
+        if (lt == 0 && t == 0) atomicOr(a.dstatus, s_bad);
+        return;
+    }
+    if (t < 32) {
+        const uint32_t c = __popc(s_bm[t]);
+        uint32_t x = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(kFull, x, o);
+            if (t >= o) x += y;
+        }
+        s_pre[t] = x - c;
+        if (t == 31) s_agg = x;
+    }
+    __syncthreads();
+    const unsigned long long agg = s_agg;
+    const uint64_t n_changed = s_hdr[0], m = s_hdr[1], n_esc = s_hdr[2];
+    const uint32_t E0 = s_E0;
+    // index checks on the changed-block prefix
+    const unsigned long long P = lt < spans ? ib_here : n_changed;
+    bool ok = (lt != 0 || spans == 0 || P == 0) && P <= n_changed && agg <= n_changed - P &&
+              (lt >= spans || P + agg == (lt + 1 < spans ? ib_next : n_changed));
+    if (ok && lt + 1 == spans) {
+        const bool last_changed = block_changed(s_bm, (uint32_t)((n_s - 1 - v0) >> log2B));
+        ok = (P + agg) * B - (last_changed ? nb * B - n_s : 0) == m;
+    }
+    if (!ok) {
+        if (t == 0) atomicOr(a.dstatus, EZ_DSTAT_BAD_COUNT);
+        return;
+    }
+    const uint8_t* ex = p + off_exp;
+    uint8_t* ct = a.cache + (uint64_t)ci * a.L + v0 + tv;
+    uint16_t* ot = a.out + (uint64_t)ci * a.L + v0 + tv;
+
+    // this thread's block: changed (exponents from the stream) or not (cache)
+    const uint32_t k = tv >> log2B;
+    bool chg = cnt_v && block_changed(s_bm, k);
+    const uint64_t pos = (P + block_rank(s_bm, s_pre, k)) * B + (tv & (B - 1u));
+    if (chg && pos + cnt_v > m) {
+        // an m smaller than the bitmap says: never read past the section
+        atomicOr(a.dstatus, EZ_DSTAT_BAD_COUNT);
+        chg = false;
+    }
+    uint4 ew[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+    if (cnt_v && !chg) {
+        if (cnt_v == 32) {
+            ew[0] = ld_v4_nc(ct);
+            ew[1] = ld_v4_nc(ct + 16);
+        } else {
+            ew[0] = ld_bytes16(ct, cnt_v);
+            ew[1] = ld_bytes16(ct + 16, cnt_v > 16 ? cnt_v - 16 : 0u);
+        }
+    }
+    if (!kCoded && chg) {
+        if (cnt_v == 32) {
+            ew[0] = ld_v4_nc(ex + pos);
+            ew[1] = ld_v4_nc(ex + pos + 16);
+        } else {
+            ew[0] = ld_bytes16(ex + pos, cnt_v);
+            ew[1] = ld_bytes16(ex + pos + 16, cnt_v > 16 ? cnt_v - 16 : 0u);
+        }
+    }
+    if (kCoded) {
+        // one word of each plane (pos is a multiple of 32, and the plane
+        // sections are padded to 16 bytes, so the word lies inside)
+        const uint64_t plane = rup(cdiv(m, 8), 16);
+        const uint8_t* esc_sec = ex + 3 * plane;
+        uint32_t p0 = 0, p1 = 0, p2 = 0;
+        if (chg) {
+            const uint32_t* pw = reinterpret_cast<const uint32_t*>(ex + (pos >> 3));
+            p0 = __ldg(pw);
+            p1 = __ldg(pw + plane / 4);
+            p2 = __ldg(pw + plane / 2);
+        }
+        // stage the span's escapes while the plane words are in flight: the
+        // index gives their range [Q, Qn); the scan below checks it against
+        // the planes, and a range the header does not allow is not staged.
+        // The escape section starts on a 16-byte boundary, so whole words up
+        // to rup(n_esc, 4) stay inside the padded payload.
+        const unsigned long long Q = lt < spans ? ie_here : n_esc;
+        const unsigned long long Qn = lt + 1 < spans ? ie_next : n_esc;
+        const uint8_t* esc_w = esc_sec + (Q & ~3ull);
+        const uint32_t sh = (uint32_t)(Q & 3ull);
+        const uint32_t words = (Q <= Qn && Qn <= n_esc && Qn - Q <= nv) ? (uint32_t)((Qn - Q + sh + 3) >> 2) : 0u;
+        {
+            const uint32_t* src = reinterpret_cast<const uint32_t*>(esc_w);
+            const uint32_t i0 = (uint32_t)t, i1 = (uint32_t)t + kThreads;
+            const uint32_t w0 = i0 < words ? __ldg(src + i0) : 0u;
+            const uint32_t w1 = i1 < words ? __ldg(src + i1) : 0u;
+            if (i0 < words) s_esc32[i0] = w0;
+            if (i1 < words) s_esc32[i1] = w1;
+            for (uint32_t i = (uint32_t)t + 2 * kThreads; i < words; i += kThreads) s_esc32[i] = __ldg(src + i);
+        }
+        const uint32_t vmask = cnt_v >= 32 ? 0xFFFFFFFFu : ((1u << cnt_v) - 1u);
+        const uint32_t esc = chg ? (~(p0 | p1 | p2) & vmask) : 0u;
+        const uint32_t my = __popc(esc);
+        // block scan of the escape counts; its barrier also publishes the
+        // staged escapes
+        const int lane = t & 31, wid = t >> 5;
+        uint32_t x = my;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(kFull, x, o);
+            if (lane >= o) x += y;
+        }
+        if (lane == 31) s_warp32[wid] = x;
+        __syncthreads();
+        uint32_t wpre = 0, agg2 = 0;
+#pragma unroll
+        for (int i = 0; i < kThreads / 32; i++) {
+            const uint32_t v = s_warp32[i];
+            wpre += i < wid ? v : 0u;
+            agg2 += v;
+        }
+        const uint32_t excl = wpre + x - my;
+        const bool eok = (lt != 0 || spans == 0 || Q == 0) && Q <= n_esc && agg2 <= n_esc - Q &&
+                         (lt >= spans || Q + agg2 == Qn);
+        if (!eok) {
+            if (t == 0) atomicOr(a.dstatus, EZ_DSTAT_BAD_COUNT);
+            return;
+        }
+        if (chg) {
+            uint32_t ev32[8];
+#pragma unroll
+            for (int g = 0; g < 4; g++) {
+                const unsigned long long c8 = codes8((p0 >> (8 * g)) & 0xFFu, (p1 >> (8 * g)) & 0xFFu,
+                                                     (p2 >> (8 * g)) & 0xFFu);
+                unsigned long long e = (E0 == 0)
+                    ? ((c8 | 0x8080808080808080ull) - 0x0101010101010101ull) & 0x7F7F7F7F7F7F7F7Full
+                    : c8 + (unsigned long long)(E0 - 1) * 0x0101010101010101ull;
+                const uint32_t mm = (esc >> (8 * g)) & 0xFFu;
+                if (mm) {
+                    const uint32_t q = excl + __popc(esc & ((1u << (8 * g)) - 1u));
+                    uint32_t c_lo, c_hi;
+                    load_unaligned8(s_esc32, q + sh, c_lo, c_hi);
+                    e = insert_selected_a(e, mm, c_lo, c_hi);
+                }
+                ev32[2 * g] = (uint32_t)e;
+                ev32[2 * g + 1] = (uint32_t)(e >> 32);
+            }
+            ew[0] = make_uint4(ev32[0], ev32[1], ev32[2], ev32[3]);
+            ew[1] = make_uint4(ev32[4], ev32[5], ev32[6], ev32[7]);
+        }
+    }
+    if (!cnt_v) return;
+    if (chg) {
+        if (cnt_v == 32) {
+            st_v4(ct, ew[0]);
+            st_v4(ct + 16, ew[1]);
+        } else {
+            st_bytes16(ct, ew[0], cnt_v);
+            st_bytes16(ct + 16, ew[1], cnt_v > 16 ? cnt_v - 16 : 0u);
+        }
+    }
+    const uint32_t smv[8] = {smw[0].x, smw[0].y, smw[0].z, smw[0].w, smw[1].x, smw[1].y, smw[1].z, smw[1].w};
+    const uint32_t evv[8] = {ew[0].x, ew[0].y, ew[0].z, ew[0].w, ew[1].x, ew[1].y, ew[1].z, ew[1].w};
+#pragma unroll
+    for (int g = 0; g < 4; g++) {
+        uint4 o4;
+        merge4(smv[2 * g], evv[2 * g], o4.x, o4.y);
+        merge4(smv[2 * g + 1], evv[2 * g + 1], o4.z, o4.w);
+        const uint32_t v = 8u * (uint32_t)g;
+        if (v + 8 <= cnt_v) {
+            st_v4(ot + v, o4);
+        } else if (v < cnt_v) {
+            const uint32_t hw[4] = {o4.x, o4.y, o4.z, o4.w};
+            for (uint32_t i = 0; i < cnt_v - v; i++) ot[v + i] = (uint16_t)(hw[i >> 1] >> (16 * (i & 1)));
         }
     }
 }
@@ -882,8 +1174,14 @@ cudaError_t launch_reuse_decode(const ez_plan_s* p, const uint8_t* in, const uin
     a.counter = w.counters + 3;
     a.abort = w.counters + 7;
     const unsigned tiles = (unsigned)((uint64_t)count * p->tpc);
-    if (p->codec == EZ_CODEC_REUSE_CODE3) k_reuse_decode<true><<<tiles, kThreads, 0, s>>>(a);
-    else k_reuse_decode<false><<<tiles, kThreads, 0, s>>>(a);
+    const bool coded = p->codec == EZ_CODEC_REUSE_CODE3;
+    if (p->B >= 32) {
+        if (coded) k_reuse_decode32<true><<<tiles, kThreads, 0, s>>>(a);
+        else k_reuse_decode32<false><<<tiles, kThreads, 0, s>>>(a);
+    } else {
+        if (coded) k_reuse_decode<true><<<tiles, kThreads, 0, s>>>(a);
+        else k_reuse_decode<false><<<tiles, kThreads, 0, s>>>(a);
+    }
     return cudaGetLastError();
 }
 
