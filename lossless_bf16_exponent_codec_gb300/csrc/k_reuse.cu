@@ -475,6 +475,68 @@ __global__ void __launch_bounds__(kThreads, 6) k_reuse_place(RuEnc a)
     }
 }
 
+// Block size B >= 32: as k_reuse_place, with thread t on the 32 consecutive
+// values [32t, 32t + 32) of the tile, which lie in one block: a changed
+// block's 32 exponents go to a stream position that is a multiple of 32, as
+// two aligned 16-byte stores.
+__global__ void __launch_bounds__(kThreads, 6) k_reuse_place32(RuEnc a)
+{
+    __shared__ uint32_t s_bm[32], s_pre[32], s_agg;
+    const int t = threadIdx.x;
+    if (t < 32) s_bm[t] = 0;
+    const TilePos tp = tile_pos(blockIdx.x, a.count, a.tpc);
+    const uint32_t ci = tp.ci, lt = tp.lt;
+    const uint32_t r = a.first + ci;
+    const uint64_t n_s = shard_values(a.n, a.L, r);
+    const uint64_t v0 = (uint64_t)lt * kTile;
+    const uint32_t nv = v0 < n_s ? (uint32_t)umin64(kTile, n_s - v0) : 0u;
+    const uint32_t B = a.B, log2B = a.log2B;
+    const uint64_t nb = cdiv(n_s, B);
+    const uint64_t off_idx = ru_off_idx(n_s, B), off_exp = ru_off_exp(n_s, B, false);
+    const uint32_t tv = 32u * (uint32_t)t;
+    const uint32_t cnt_v = tv < nv ? min(32u, nv - tv) : 0u;
+    const uint8_t* ct = a.cache + (uint64_t)ci * a.L + v0 + tv;
+    uint8_t* o = a.out + (uint64_t)ci * a.slot;
+    const unsigned long long* sc = a.state + (uint64_t)ci * a.tpc;
+    // the thread's cache bytes, loaded with the bitmap and the prefix
+    uint4 ew[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+    if (cnt_v == 32) {
+        ew[0] = ld_v4_nc(ct);
+        ew[1] = ld_v4_nc(ct + 16);
+    } else if (cnt_v) {
+        ew[0] = ld_bytes16(ct, cnt_v);
+        ew[1] = ld_bytes16(ct + 16, cnt_v > 16 ? cnt_v - 16 : 0u);
+    }
+    const unsigned long long P = lt ? ld_relaxed(sc + lt - 1) : 0ull;
+    __syncthreads();
+    load_bitmap(o, lt, nb, log2B, s_bm, s_pre, &s_agg);
+    if (t == 0 && v0 < n_s) *reinterpret_cast<unsigned long long*>(o + off_idx + 8ull * lt) = P;
+    const uint64_t m = a.info[ci].m;
+    const uint32_t k = tv >> log2B;
+    if (cnt_v && block_changed(s_bm, k)) {
+        const uint64_t pos = (P + block_rank(s_bm, s_pre, k)) * B + (tv & (B - 1u));
+        uint8_t* dst = o + off_exp + pos;
+        if (cnt_v == 32 && pos + 32 <= m) {
+            st_v4(dst, ew[0]);
+            st_v4(dst + 16, ew[1]);
+        } else if (pos + cnt_v <= m) {
+            st_bytes16(dst, ew[0], cnt_v);
+            st_bytes16(dst + 16, ew[1], cnt_v > 16 ? cnt_v - 16 : 0u);
+        }
+    }
+    const uint32_t fin_tile = n_s ? (uint32_t)((n_s - 1) / kTile) : 0u;
+    if (lt == fin_tile) {
+        const uint64_t n_changed = a.info[ci].n_changed;
+        const uint64_t total = ru_bytes(n_s, B, m, false, 0);
+        if (t < 64)
+            o[t] = (uint8_t)ru_header_byte(t, a.cold ? 2u : 0u, 0u, B, r, n_s, n_changed, m, 0, total);
+        if (t < 128 && off_exp + m + t < total) o[off_exp + m + t] = 0;
+        const uint64_t ib = 8 * cdiv(n_s, kTile);
+        if (t < 16 && ib + t < ru_idx_bytes(n_s, false)) o[off_idx + ib + t] = 0;
+        if (t == 0) a.sizes[ci] = total;
+    }
+}
+
 // Bytes [b, b+16) of a run of `len` bytes at dst, from d (bytes past len
 // are not written).
 constexpr uint32_t kSpecBytes = 2048;
@@ -568,13 +630,6 @@ __global__ void __launch_bounds__(kThreads, 8) k_reuse_place_coded(RuEnc a)
 
 __device__ __forceinline__ uint4 ld16_plain(const void* p) { return *reinterpret_cast<const uint4*>(p); }
 
-// One CTA per kTile span of one payload, no inter-tile dependence.  The
-// span's index entry gives the changed blocks (and, coded, the escapes)
-// before it; it is checked against the span's own counts -- entry 0 must be
-// 0, entry + count must equal the next entry, the last one n_changed (n_esc)
-// -- so the exponents read always lie inside the EXP section.  Every thread
-// reads the payload offsets, then the bitmap slice, sign+mantissa bytes and
-// index entries are loaded before thread 0's header checks complete.
 // The oracle's checks of a reuse payload's header, in its order; 0 or the
 // first failing status.  Reads the 64 header bytes only when they lie inside
 // the payload.  *E0 and hdr[0..2] = n_changed, m, n_esc are set when it
@@ -616,6 +671,13 @@ __device__ __forceinline__ uint32_t ru_check_header(const uint8_t* p, uint64_t o
     return bad;
 }
 
+// One CTA per kTile span of one payload, no inter-tile dependence.  The
+// span's index entry gives the changed blocks (and, coded, the escapes)
+// before it; it is checked against the span's own counts -- entry 0 must be
+// 0, entry + count must equal the next entry, the last one n_changed (n_esc)
+// -- so the exponents read always lie inside the EXP section.  Every thread
+// reads the payload offsets, then the bitmap slice, sign+mantissa bytes and
+// index entries are loaded before thread 0's header checks complete.
 template <bool kCoded>
 __global__ void __launch_bounds__(kThreads, 6) k_reuse_decode(RuDec a)
 {
@@ -1132,7 +1194,8 @@ cudaError_t launch_reuse_encode(const ez_plan_s* p, const uint16_t* x, uint32_t 
         if (e != cudaSuccess) return e;
         e = launch_tile_scan(p, w.state_a, count, w.seg_a, w.counters + 4, w.counters + 7, dstatus, s);
         if (e != cudaSuccess) return e;
-        k_reuse_place<<<tiles, kThreads, 0, s>>>(a);
+        if (p->B >= 32) k_reuse_place32<<<tiles, kThreads, 0, s>>>(a);
+        else k_reuse_place<<<tiles, kThreads, 0, s>>>(a);
         return cudaGetLastError();
     }
     a.plbuf = w.plbuf;
