@@ -559,7 +559,10 @@ __device__ __forceinline__ void store_run16(uint8_t* dst, uint32_t b, uint32_t l
 // (prefix * B) / 8 of each plane, its staged escapes to their prefix; both
 // prefixes are the span's index entries; the tile holding the shard's last
 // value writes the header, the padding and the size.
-__global__ void __launch_bounds__(kThreads, 8) k_reuse_place_coded(RuEnc a)
+constexpr int kPlaceThreads = 64;
+static_assert(3 * (kTile / 8) == 3 * 16 * kPlaceThreads && kSpecBytes == 2 * 16 * kPlaceThreads,
+              "k_reuse_place_coded covers 3 KB of planes and the escape window with 64 threads");
+__global__ void __launch_bounds__(kPlaceThreads) k_reuse_place_coded(RuEnc a)
 {
     const int t = threadIdx.x;
     const TilePos tp = tile_pos(blockIdx.x, a.count, a.tpc);
@@ -581,10 +584,15 @@ __global__ void __launch_bounds__(kThreads, 8) k_reuse_place_coded(RuEnc a)
     // the prefixes
     const uint8_t* pst = a.plbuf + (uint64_t)tp.state * 3 * (kTile / 8);
     const uint8_t* est = a.escbuf + (uint64_t)ci * a.L + v0;
-    const uint32_t b0 = 16u * (uint32_t)t;
-    uint4 dp = make_uint4(0, 0, 0, 0), de = make_uint4(0, 0, 0, 0);
-    if (b0 < 3 * (kTile / 8)) dp = ld_v4_nc(pst + b0);
-    if (b0 < kSpecBytes && v0 + b0 + 16 <= a.L) de = ld_v4_nc(est + b0);
+    // 64 threads: 48 plane bytes and 32 speculative escape bytes each
+    uint4 dp[3], de[2];
+#pragma unroll
+    for (int j = 0; j < 3; j++) dp[j] = ld_v4_nc(pst + 16u * (uint32_t)(t + j * kPlaceThreads));
+#pragma unroll
+    for (int j = 0; j < 2; j++) {
+        const uint32_t b = 16u * (uint32_t)(t + j * kPlaceThreads);
+        de[j] = v0 + b + 16 <= a.L ? ld_v4_nc(est + b) : make_uint4(0, 0, 0, 0);
+    }
     const unsigned long long P = lt ? ld_relaxed(sa + lt - 1) : 0ull;
     const unsigned long long Pend = ld_relaxed(sa + lt);
     const unsigned long long Q = lt ? ld_relaxed(sb + lt - 1) : 0ull;
@@ -599,12 +607,15 @@ __global__ void __launch_bounds__(kThreads, 8) k_reuse_place_coded(RuEnc a)
         idx[2 * lt] = P;
         idx[2 * lt + 1] = Q;
     }
-    if (b0 < 3 * (kTile / 8)) {
-        const uint32_t p = b0 / (kTile / 8), off = b0 % (kTile / 8);
-        store_run16(pl + (uint64_t)p * plane + start / 8, off, nbytes, dp);
+#pragma unroll
+    for (int j = 0; j < 3; j++) {
+        const uint32_t b0 = 16u * (uint32_t)(t + j * kPlaceThreads);
+        const uint32_t pi = b0 / (kTile / 8), off = b0 % (kTile / 8);
+        store_run16(pl + (uint64_t)pi * plane + start / 8, off, nbytes, dp[j]);
     }
-    if (b0 < kSpecBytes) store_run16(esc_sec + Q, b0, agg2, de);
-    for (uint32_t b = kSpecBytes + (uint32_t)t; b < agg2; b += kThreads) esc_sec[Q + b] = est[b];
+#pragma unroll
+    for (int j = 0; j < 2; j++) store_run16(esc_sec + Q, 16u * (uint32_t)(t + j * kPlaceThreads), agg2, de[j]);
+    for (uint32_t b = kSpecBytes + (uint32_t)t; b < agg2; b += kPlaceThreads) esc_sec[Q + b] = est[b];
     const uint32_t fin_tile = n_s ? (uint32_t)((n_s - 1) / kTile) : 0u;
     if (lt == fin_tile) {
         uint32_t E0 = a.stats[ci].E0;
@@ -621,7 +632,8 @@ __global__ void __launch_bounds__(kThreads, 8) k_reuse_place_coded(RuEnc a)
             pl[plane + pbytes + t] = 0;
             pl[2 * plane + pbytes + t] = 0;
         }
-        if (t < 128 && off_exp + 3 * plane + n_esc + t < tot) o[off_exp + 3 * plane + n_esc + t] = 0;
+        for (uint32_t u = (uint32_t)t; u < 128; u += kPlaceThreads)
+            if (off_exp + 3 * plane + n_esc + u < tot) o[off_exp + 3 * plane + n_esc + u] = 0;
         const uint64_t ib = 16 * cdiv(n_s, kTile);
         if (t < 16 && ib + t < ru_idx_bytes(n_s, true)) o[off_idx + ib + t] = 0;
         if (t == 0) a.sizes[ci] = tot;
@@ -1208,7 +1220,7 @@ cudaError_t launch_reuse_encode(const ez_plan_s* p, const uint16_t* x, uint32_t 
     if (e != cudaSuccess) return e;
     e = launch_tile_scan(p, w.state_b, count, w.seg_b, w.counters + 5, w.counters + 7, dstatus, s);
     if (e != cudaSuccess) return e;
-    k_reuse_place_coded<<<tiles, kThreads, 0, s>>>(a);
+    k_reuse_place_coded<<<tiles, kPlaceThreads, 0, s>>>(a);
     return cudaGetLastError();
 }
 
