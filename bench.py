@@ -352,15 +352,31 @@ def pinned_inputs(args, xs):
 def run_e2e(args, world, xs, hosts, start, c3, ru, rc, s):
     """Same metric through the public calls with host inputs: each step copies
     the iteration's tensor from pinned host memory, runs the six passes and
-    reads back the three size tables and status words.  One untimed pass over
-    the K steps warms the host-to-device path (it runs far below the link's
-    rate after a stretch without host traffic); the median of the next three
+    reads back the three size tables and status words.  The copies run on
+    their own stream into two device buffers, so step k+1's input crosses the
+    link while step k's passes run (a copy waits until the passes of step
+    k-1, which read the same buffer, are done; a step's passes wait for its
+    copy); every copy lies inside the timed region.  One untimed pass over the
+    K steps warms the host-to-device path (it runs far below the link's rate
+    after a stretch without host traffic); the median of the next three
     passes is reported (the caches are re-primed before each pass)."""
     K = len(hosts)
     n = N_VALUES
-    dev = torch.empty_like(xs[0])
+    dev = [torch.empty_like(xs[0]) for _ in range(2)]
+    cs = torch.cuda.Stream()
+    copied = [torch.cuda.Event() for _ in range(2)]
+    freed = [torch.cuda.Event() for _ in range(2)]
     out_sizes = torch.empty(3 * W_CHUNKS + 3, dtype=torch.int64).pin_memory()
     times = []
+
+    def issue_copy(k):
+        j = k % 2
+        with torch.cuda.stream(cs):
+            if k >= 2:
+                cs.wait_event(freed[j])
+            dev[j].copy_(hosts[k], non_blocking=True)
+            copied[j].record(cs)
+
     for rep in range(4):   # pass 0: untimed warm-up of the host-to-device path
         # prime the caches with the iteration before
         ru.encode_reuse(xs[start])
@@ -371,15 +387,22 @@ def run_e2e(args, world, xs, hosts, start, c3, ru, rc, s):
         barrier(world)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(s)
+        cs.wait_event(e0)
+        issue_copy(0)
         for k in range(K):
-            dev.copy_(hosts[k], non_blocking=True)
-            c3.stats(dev)
-            c3.encode_code3(dev)
+            if k + 1 < K:
+                issue_copy(k + 1)
+            j = k % 2
+            s.wait_event(copied[j])
+            x = dev[j]
+            c3.stats(x)
+            c3.encode_code3(x)
             c3.gather_decode()
-            ru.encode_reuse(dev)
+            ru.encode_reuse(x)
             ru.gather_decode()
-            rc.encode_reuse(dev)
+            rc.encode_reuse(x)
             rc.gather_decode()
+            freed[j].record(s)
             res = torch.cat([c3.sizes, ru.sizes, rc.sizes, c3.status.long(), ru.status.long(),
                              rc.status.long()])
             out_sizes.copy_(res, non_blocking=True)
