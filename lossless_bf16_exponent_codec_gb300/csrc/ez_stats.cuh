@@ -315,12 +315,14 @@ __device__ __forceinline__ uint32_t window_base(double var, double K)
     return (uint32_t)lo;
 }
 
-// The last CTA finalises.  Every thread takes one exponent bin and adds its
-// terms, split into 32-bit pieces, to per-limb 64-bit accumulators of the
-// three big sums (positive and negative parts of s1, and s2) with
-// shared-memory atomics; three threads propagate the carries into 32-bit
-// limbs, and thread 0 does the rounding.  A limb accumulator receives at most
-// 3 * 256 pieces < 2^42.
+// The last CTA finalises.  Every thread takes one exponent bin and splits its
+// terms into 32-bit pieces at their limbs of the three big sums (positive and
+// negative parts of s1, and s2); the bins of one warp reach at most five
+// consecutive limbs, so each warp adds its pieces limb by limb with shuffles
+// and its lane 0 adds the five warp totals to per-limb 64-bit accumulators
+// (eight warps: no long chains of shared atomics on one limb).  Three threads
+// then propagate the carries into 32-bit limbs, and thread 0 does the
+// rounding.  A limb accumulator receives at most 3 * 256 pieces < 2^42.
 struct FinSmem {
     unsigned long long h[256];
     unsigned long long acc[3][kLimbs + 2];     // P, Q, R
@@ -329,16 +331,24 @@ struct FinSmem {
 };
 static_assert(sizeof(FinSmem) <= sizeof(StatsSmem::hist), "finalise scratch fits the histogram");
 
-// acc += v * 2^sh, as three 32-bit pieces
-__device__ __forceinline__ void acc_add_shl(unsigned long long* acc, unsigned long long v, int sh)
+// The 32-bit pieces of v * 2^sh at limbs sh/32, sh/32 + 1, sh/32 + 2, added
+// over the warp (all 32 lanes call it; lanes without a term pass v = 0).  The
+// lanes' first limbs lie within 3 of lane 0's, so five slot sums cover them.
+__device__ __forceinline__ void warp_acc_add_shl(unsigned long long* acc, unsigned long long v, int sh)
 {
     const int limb = sh >> 5, bit = sh & 31;
-    const uint32_t p0 = (uint32_t)(v << bit);
-    const uint32_t p1 = (uint32_t)(bit ? (v >> (32 - bit)) : (v >> 32));
-    const uint32_t p2 = (uint32_t)(bit ? (v >> (64 - bit)) : 0ull);
-    if (p0) atomicAdd(&acc[limb], (unsigned long long)p0);
-    if (p1) atomicAdd(&acc[limb + 1], (unsigned long long)p1);
-    if (p2) atomicAdd(&acc[limb + 2], (unsigned long long)p2);
+    const unsigned long long p0 = (uint32_t)(v << bit);
+    const unsigned long long p1 = (uint32_t)(bit ? (v >> (32 - bit)) : (v >> 32));
+    const unsigned long long p2 = (uint32_t)(bit ? (v >> (64 - bit)) : 0ull);
+    const int base = __shfl_sync(kFull, limb, 0);
+    const int k = limb - base;
+#pragma unroll
+    for (int j = 0; j < 5; j++) {
+        unsigned long long c = (j == k ? p0 : 0ull) + (j == k + 1 ? p1 : 0ull) + (j == k + 2 ? p2 : 0ull);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(kFull, c, o);
+        if ((threadIdx.x & 31) == 0 && c) atomicAdd(&acc[base + j], c);
+    }
 }
 
 static __device__ __noinline__ void st_finalize(const StatsBins* G, uint64_t n, double K, ez_stats_t* out,
@@ -356,11 +366,13 @@ static __device__ __noinline__ void st_finalize(const StatsBins* G, uint64_t n, 
     F.h[t] = h;
     out->hist[t] = h;
     __syncthreads();
-    if (t < 255 && (s1 || s2)) {
-        const int sh = (t ? t : 1) - 1;     // v * 2^133 = +-M * 2^sh
-        if (s1 > 0) acc_add_shl(F.acc[0], (unsigned long long)s1, sh);
-        else if (s1 < 0) acc_add_shl(F.acc[1], (unsigned long long)(-s1), sh);
-        if (s2) acc_add_shl(F.acc[2], s2, 2 * sh);   // v^2 * 2^266 = M^2 * 2^(2 sh)
+    {
+        // v * 2^133 = +-M * 2^sh; v^2 * 2^266 = M^2 * 2^(2 sh); bin 255 holds no terms
+        const int sh = (t ? t : 1) - 1;
+        const bool live = t < 255;
+        warp_acc_add_shl(F.acc[0], live && s1 > 0 ? (unsigned long long)s1 : 0ull, sh);
+        warp_acc_add_shl(F.acc[1], live && s1 < 0 ? (unsigned long long)(-s1) : 0ull, sh);
+        warp_acc_add_shl(F.acc[2], live ? s2 : 0ull, 2 * sh);
     }
     if (t < 255 && h) atomicAdd(&F.n_fin, h);
     __syncthreads();

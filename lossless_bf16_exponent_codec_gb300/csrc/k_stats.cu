@@ -14,10 +14,10 @@ static_assert(sizeof(StatsBins) == 3 * 256 * 8 + 256, "StatsBins layout (api.cpp
 static_assert(sizeof(ShardInfo) == 64, "ShardInfo layout (api.cpp sizes it)");
 static_assert(sizeof(ez_stats_t) == 2120, "ez_stats_t layout");
 
-constexpr int kStatsLoads = 16;                             // 16-B loads per thread
-constexpr uint32_t kStatsTile = kThreads * kStatsLoads * 8;   // 32768 values
+constexpr int kStatsLoads = 32;                             // 16-B loads per thread
+constexpr uint32_t kStatsTile = kThreads * kStatsLoads * 8;   // 65536 values
 
-// One CTA per tile of 32768 values of one shard, 8 resident CTAs per SM;
+// One CTA per tile of 65536 values of one shard, 8 resident CTAs per SM;
 // every thread keeps four 16-byte loads in flight and adds their 32 values to
 // the CTA's histogram.  Shard ci = tile / tps holds values [ci*L, ci*L + n_s)
 // of x; its CTAs fold into bins G[ci], and the last of them writes out[ci].
