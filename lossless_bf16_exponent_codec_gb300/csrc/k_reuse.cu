@@ -255,10 +255,9 @@ __global__ void __launch_bounds__(kThreads, kCoded ? 4 : 5) k_reuse_split(RuEnc 
     __shared__ unsigned long long s_warp[kCoded ? kThreads / 32 : 1];
     __shared__ __align__(16) uint32_t s_esc32[kCoded ? (kTile + 16) / 4 : 4];
     const int t = threadIdx.x, lane = t & 31, wid = t >> 5;
-    if (t < 32) {
-        s_gl[t] = 0;
-        s_bm[t] = 0;
-    }
+    // s_gl needs no clearing: lane 0 of every warp writes its entry of every
+    // group below (a clear here could land after another warp's entry)
+    if (t < 32) s_bm[t] = 0;
     const TilePos tp = tile_pos(blockIdx.x, a.count, a.tpc);
     const uint32_t ci = tp.ci, lt = tp.lt;
     if (kCoded) {
@@ -699,7 +698,10 @@ __global__ void __launch_bounds__(kThreads, 6) k_reuse_decode(RuDec a)
     __shared__ unsigned long long s_warp[kThreads / 32];
     __shared__ __align__(16) uint32_t s_esc32[kCoded ? (kTile + 32) / 4 : 4];
     const int t = threadIdx.x;
-    if (t < 32) s_bm[t] = 0;
+    if (t < 32) {
+        s_bm[t] = 0;
+        __syncwarp();   // cleared before warp 0 ORs the bitmap bytes in
+    }
     const uint32_t ci = blockIdx.x / a.tpc, lt = blockIdx.x % a.tpc;
     const uint32_t r = a.first + ci;
     const uint64_t n_s = shard_values(a.n, a.L, r);
@@ -925,7 +927,10 @@ __global__ void __launch_bounds__(kThreads, 6) k_reuse_decode32(RuDec a)
     __shared__ uint32_t s_warp32[kThreads / 32];
     __shared__ __align__(16) uint32_t s_esc32[kCoded ? (kTile + 32) / 4 : 4];
     const int t = threadIdx.x;
-    if (t < 32) s_bm[t] = 0;
+    if (t < 32) {
+        s_bm[t] = 0;
+        __syncwarp();   // cleared before warp 0 ORs the bitmap bytes in
+    }
     const uint32_t ci = blockIdx.x / a.tpc, lt = blockIdx.x % a.tpc;
     const uint32_t r = a.first + ci;
     const uint64_t n_s = shard_values(a.n, a.L, r);
