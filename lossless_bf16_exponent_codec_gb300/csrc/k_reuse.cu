@@ -563,6 +563,7 @@ static_assert(3 * (kTile / 8) == 3 * 16 * kPlaceThreads && kSpecBytes == 2 * 16 
               "k_reuse_place_coded covers 3 KB of planes and the escape window with 64 threads");
 __global__ void __launch_bounds__(kPlaceThreads) k_reuse_place_coded(RuEnc a)
 {
+    __shared__ __align__(16) uint32_t s_e[kSpecBytes / 4 + 4];
     const int t = threadIdx.x;
     const TilePos tp = tile_pos(blockIdx.x, a.count, a.tpc);
     const uint32_t ci = tp.ci, lt = tp.lt;
@@ -588,10 +589,7 @@ __global__ void __launch_bounds__(kPlaceThreads) k_reuse_place_coded(RuEnc a)
 #pragma unroll
     for (int j = 0; j < 3; j++) dp[j] = ld_v4_nc(pst + 16u * (uint32_t)(t + j * kPlaceThreads));
 #pragma unroll
-    for (int j = 0; j < 2; j++) {
-        const uint32_t b = 16u * (uint32_t)(t + j * kPlaceThreads);
-        de[j] = v0 + b + 16 <= a.L ? ld_v4_nc(est + b) : make_uint4(0, 0, 0, 0);
-    }
+    for (int j = 0; j < 2; j++) de[j] = ld_v4_nc(est + 16u * (uint32_t)(t + j * kPlaceThreads));
     const unsigned long long P = lt ? ld_relaxed(sa + lt - 1) : 0ull;
     const unsigned long long Pend = ld_relaxed(sa + lt);
     const unsigned long long Q = lt ? ld_relaxed(sb + lt - 1) : 0ull;
@@ -612,9 +610,47 @@ __global__ void __launch_bounds__(kPlaceThreads) k_reuse_place_coded(RuEnc a)
         const uint32_t pi = b0 / (kTile / 8), off = b0 % (kTile / 8);
         store_run16(pl + (uint64_t)pi * plane + start / 8, off, nbytes, dp[j]);
     }
+    // escapes: run [Q, Q + agg2) of the escape section from staged bytes
+    // [0, agg2).  The 2 KB window goes through shared memory, so that every
+    // aligned 16-byte word of the run is one store built from five words of
+    // the window; only the unaligned head and tail are byte stores.  (Staged
+    // bytes past the tile's own run are read but never stored; the staging
+    // buffer is followed by the plane staging buffer, so the reads stay in
+    // the workspace.)
 #pragma unroll
-    for (int j = 0; j < 2; j++) store_run16(esc_sec + Q, 16u * (uint32_t)(t + j * kPlaceThreads), agg2, de[j]);
-    for (uint32_t b = kSpecBytes + (uint32_t)t; b < agg2; b += kPlaceThreads) esc_sec[Q + b] = est[b];
+    for (int j = 0; j < 2; j++)
+        *reinterpret_cast<uint4*>(&s_e[4u * (uint32_t)(t + j * kPlaceThreads)]) = de[j];
+    if (t < 4) s_e[kSpecBytes / 4 + t] = 0u;
+    __syncthreads();
+    {
+        uint8_t* d = esc_sec + Q;
+        const uint32_t head = min((uint32_t)((16u - (reinterpret_cast<uintptr_t>(d) & 15u)) & 15u), agg2);
+        const uint32_t nw = (agg2 - head) / 16u;
+        const uint32_t tail0 = head + 16u * nw;
+        const uint8_t* s_b = reinterpret_cast<const uint8_t*>(s_e);
+        for (uint32_t b = (uint32_t)t; b < head; b += kPlaceThreads) d[b] = b < kSpecBytes ? s_b[b] : est[b];
+        for (uint32_t b = tail0 + (uint32_t)t; b < agg2; b += kPlaceThreads)
+            d[b] = b < kSpecBytes ? s_b[b] : est[b];
+        const uint32_t sh = 8u * (head & 3u);
+        for (uint32_t j = (uint32_t)t; j < nw; j += kPlaceThreads) {
+            const uint32_t sb = head + 16u * j, q = sb >> 2;
+            uint32_t w[5];
+            if (sb + 16u <= kSpecBytes) {   // every byte of this word is in the window
+#pragma unroll
+                for (int k = 0; k < 5; k++) w[k] = s_e[q + k];
+            } else {
+                const uint32_t* g = reinterpret_cast<const uint32_t*>(est);
+#pragma unroll
+                for (int k = 0; k < 5; k++) w[k] = __ldg(g + q + k);
+            }
+            uint4 v;
+            v.x = __funnelshift_r(w[0], w[1], sh);
+            v.y = __funnelshift_r(w[1], w[2], sh);
+            v.z = __funnelshift_r(w[2], w[3], sh);
+            v.w = __funnelshift_r(w[3], w[4], sh);
+            *reinterpret_cast<uint4*>(d + sb) = v;
+        }
+    }
     const uint32_t fin_tile = n_s ? (uint32_t)((n_s - 1) / kTile) : 0u;
     if (lt == fin_tile) {
         uint32_t E0 = a.stats[ci].E0;
@@ -698,10 +734,7 @@ __global__ void __launch_bounds__(kThreads, 6) k_reuse_decode(RuDec a)
     __shared__ unsigned long long s_warp[kThreads / 32];
     __shared__ __align__(16) uint32_t s_esc32[kCoded ? (kTile + 32) / 4 : 4];
     const int t = threadIdx.x;
-    if (t < 32) {
-        s_bm[t] = 0;
-        __syncwarp();   // cleared before warp 0 ORs the bitmap bytes in
-    }
+    if (t < 32) s_bm[t] = 0;   // warp 0, which alone ORs the bitmap bytes in below
     const uint32_t ci = blockIdx.x / a.tpc, lt = blockIdx.x % a.tpc;
     const uint32_t r = a.first + ci;
     const uint64_t n_s = shard_values(a.n, a.L, r);
@@ -927,10 +960,7 @@ __global__ void __launch_bounds__(kThreads, 6) k_reuse_decode32(RuDec a)
     __shared__ uint32_t s_warp32[kThreads / 32];
     __shared__ __align__(16) uint32_t s_esc32[kCoded ? (kTile + 32) / 4 : 4];
     const int t = threadIdx.x;
-    if (t < 32) {
-        s_bm[t] = 0;
-        __syncwarp();   // cleared before warp 0 ORs the bitmap bytes in
-    }
+    if (t < 32) s_bm[t] = 0;   // warp 0, which alone ORs the bitmap bytes in below
     const uint32_t ci = blockIdx.x / a.tpc, lt = blockIdx.x % a.tpc;
     const uint32_t r = a.first + ci;
     const uint64_t n_s = shard_values(a.n, a.L, r);
