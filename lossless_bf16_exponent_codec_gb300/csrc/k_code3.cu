@@ -343,7 +343,25 @@ __global__ void __launch_bounds__(kEncThreads, 2) k_code3_encode(C3Enc a)
         }
         if (lane == 0 && v0_of(lt) < n_c)
             *reinterpret_cast<unsigned long long*>(idx_sec + 8ull * lt) = P;
-        for (uint32_t b = (uint32_t)lane; b < agg; b += 32) esc_sec[P + b] = S.esc[s][b];
+        {
+            // the tile's escapes to [P, P + agg): every aligned 16-byte word
+            // of the run is one store assembled from five words of the slot
+            // with funnel shifts (the words read lie below agg + 4, inside
+            // the slot); the unaligned head and tail are byte stores
+            uint8_t* d = esc_sec + P;
+            const uint32_t head = min((uint32_t)((16u - (reinterpret_cast<uintptr_t>(d) & 15u)) & 15u), agg);
+            const uint32_t nw = (agg - head) / 16u, tail0 = head + 16u * nw;
+            for (uint32_t b = (uint32_t)lane; b < head; b += 32) d[b] = S.esc[s][b];
+            for (uint32_t b = tail0 + (uint32_t)lane; b < agg; b += 32) d[b] = S.esc[s][b];
+            const uint32_t* e32 = reinterpret_cast<const uint32_t*>(S.esc[s]);
+            const uint32_t sh = 8u * (head & 3u);
+            for (uint32_t j = (uint32_t)lane; j < nw; j += 32) {
+                const uint32_t sb = head + 16u * j, q = sb >> 2;
+                const uint32_t w0 = e32[q], w1 = e32[q + 1], w2 = e32[q + 2], w3 = e32[q + 3], w4 = e32[q + 4];
+                st_v4(d + sb, make_uint4(__funnelshift_r(w0, w1, sh), __funnelshift_r(w1, w2, sh),
+                                         __funnelshift_r(w2, w3, sh), __funnelshift_r(w3, w4, sh)));
+            }
+        }
         if (lt == a.tpc - 1) {
             const uint64_t n_esc = P + agg;
             const uint64_t bytes = c3_bytes(n_c, n_esc);
