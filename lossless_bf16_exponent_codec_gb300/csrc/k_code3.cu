@@ -409,7 +409,7 @@ __device__ __forceinline__ uint4 ld_v4_plain(const void* p)
 // checked against the tile's own escape count (entry 0 must be 0, each entry
 // plus the tile's count must equal the next entry, the last one n_esc), so
 // the escapes read are always inside the escape section.
-__global__ void __launch_bounds__(kThreads, 6) k_code3_decode(C3Dec a)
+__global__ void __launch_bounds__(kThreads, 5) k_code3_decode(C3Dec a)
 {
     __shared__ uint32_t s_bad, s_E0;
     __shared__ unsigned long long s_nesc;
@@ -488,6 +488,22 @@ __global__ void __launch_bounds__(kThreads, 6) k_code3_decode(C3Dec a)
         }
         s_bad = bad;
     }
+    // stage the span's escapes as soon as the index gives their range
+    // [idx_here, idx_next) (the scan below checks it against the planes):
+    // every span but the chunk's last, whose end is the header's count, when
+    // the range lies inside the payload
+    const bool early = fixed_ok && lt + 1 < n_idx && idx_next >= idx_here && idx_next - idx_here <= nv &&
+                       sec_esc + ((idx_next + 3) & ~3ull) <= avail;
+    if (early) {
+        const uint32_t* src = reinterpret_cast<const uint32_t*>(p + sec_esc + (idx_here & ~3ull));
+        const uint32_t words = (uint32_t)((idx_next - idx_here + (idx_here & 3ull) + 3) >> 2);
+        const uint32_t i0 = (uint32_t)t, i1 = (uint32_t)t + kThreads;
+        const uint32_t w0 = i0 < words ? __ldg(src + i0) : 0u;
+        const uint32_t w1 = i1 < words ? __ldg(src + i1) : 0u;
+        if (i0 < words) s_esc32[i0] = w0;
+        if (i1 < words) s_esc32[i1] = w1;
+        for (uint32_t i = (uint32_t)t + 2 * kThreads; i < words; i += kThreads) s_esc32[i] = __ldg(src + i);
+    }
     // escapes of the thread's 32 values: code 0 in all three planes
     const uint32_t vmask = cnt_v >= 32 ? 0xFFFFFFFFu : ((1u << cnt_v) - 1u);
     const uint32_t esc = ~(p0 | p1 | p2) & vmask;
@@ -501,7 +517,7 @@ __global__ void __launch_bounds__(kThreads, 6) k_code3_decode(C3Dec a)
         if (lane >= o) x += y;
     }
     if (lane == 31) s_warp32[wid] = x;
-    __syncthreads();   // also publishes s_bad
+    __syncthreads();   // also publishes s_bad and the early-staged escapes
     uint32_t wpre = 0, agg32 = 0;
 #pragma unroll
     for (int i = 0; i < kThreads / 32; i++) {
@@ -530,10 +546,12 @@ __global__ void __launch_bounds__(kThreads, 6) k_code3_decode(C3Dec a)
     // this tile's escapes as aligned words: byte q of the tile is byte q + (P & 3)
     const uint8_t* esc_w = p + sec_esc + (P & ~3ull);
     const uint32_t sh = (uint32_t)(P & 3ull);
-    const uint32_t words = (uint32_t)((agg + sh + 3) >> 2);
-    for (uint32_t i = (uint32_t)t; i < words; i += kThreads)
-        s_esc32[i] = __ldg(reinterpret_cast<const uint32_t*>(esc_w) + i);
-    __syncthreads();
+    if (!early) {   // CTA-uniform: every thread read the same index entries
+        const uint32_t words = (uint32_t)((agg + sh + 3) >> 2);
+        for (uint32_t i = (uint32_t)t; i < words; i += kThreads)
+            s_esc32[i] = __ldg(reinterpret_cast<const uint32_t*>(esc_w) + i);
+        __syncthreads();
+    }
     if (!cnt_v) return;
     uint16_t* ot = a.out + (uint64_t)ci * a.L + v0 + tv;
     const uint32_t smv[8] = {smw[0].x, smw[0].y, smw[0].z, smw[0].w, smw[1].x, smw[1].y, smw[1].z, smw[1].w};
