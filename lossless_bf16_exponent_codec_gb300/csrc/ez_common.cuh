@@ -17,6 +17,7 @@
 #pragma once
 
 #include <cstdint>
+#include <utility>
 #include <cuda_runtime.h>
 
 #include "expzip.h"
@@ -357,6 +358,36 @@ __device__ __forceinline__ unsigned long long tile_prefix(unsigned long long* st
 
 // Grid of a persistent kernel: resident CTAs per SM (from the occupancy
 // calculator) times the SM count of the current device.
+// ---- programmatic dependent launch -------------------------------------------
+// The later kernels of a multi-kernel call are launched so that their CTAs may
+// start while the kernel before them drains; each such kernel calls
+// grid_dep_wait() before it touches anything an earlier kernel of the call
+// wrote (the wait returns once those grids have completed and their memory
+// operations are visible).  Launched without the attribute, the wait returns
+// at once.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Called at the start of a kernel that has a dependent launch after it: once
+// every CTA has called it, the dependent kernel may be scheduled (its CTAs
+// then fill SMs as this kernel's CTAs finish, and wait as above).
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" :::); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_dependent(void (*kernel)(KArgs...), unsigned grid, unsigned block, size_t smem,
+                                    cudaStream_t s, Args&&... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 template <typename K>
 inline unsigned persistent_grid(K kernel, int threads, size_t dyn_smem = 0)
 {

@@ -258,16 +258,9 @@ __global__ void __launch_bounds__(kThreads, kCoded ? 4 : 5) k_reuse_split(RuEnc 
     // s_gl needs no clearing: lane 0 of every warp writes its entry of every
     // group below (a clear here could land after another warp's entry)
     if (t < 32) s_bm[t] = 0;
+    grid_dep_launch();
     const TilePos tp = tile_pos(blockIdx.x, a.count, a.tpc);
     const uint32_t ci = tp.ci, lt = tp.lt;
-    if (kCoded) {
-        uint32_t E0 = a.stats[ci].E0;
-        if (E0 > 249u) {
-            if (t == 0 && lt == 0) atomicOr(a.dstatus, EZ_DSTAT_BAD_STATS);
-            E0 = 0;
-        }
-        s_lut[t] = ru_lut_entry((uint32_t)t, E0);
-    }
     const uint32_t r = a.first + ci;
     const uint64_t n_s = shard_values(a.n, a.L, r);
     const uint64_t v0 = (uint64_t)lt * kTile;
@@ -287,6 +280,17 @@ __global__ void __launch_bounds__(kThreads, kCoded ? 4 : 5) k_reuse_split(RuEnc 
         const uint32_t v = 8u * (uint32_t)(g * kThreads + t);
         w[g] = ld_group16(xt, v, nv);
         cv[g] = (v < nv && !a.cold) ? ld_group8(ct, v, nv) : 0ull;
+    }
+    // coded: the split may start while the shard statistics finish; nothing
+    // above depends on them, everything below may
+    grid_dep_wait();
+    if (kCoded) {
+        uint32_t E0 = a.stats[ci].E0;
+        if (E0 > 249u) {
+            if (t == 0 && lt == 0) atomicOr(a.dstatus, EZ_DSTAT_BAD_STATS);
+            E0 = 0;
+        }
+        s_lut[t] = ru_lut_entry((uint32_t)t, E0);
     }
     unsigned long long e8[kGroups];
 #pragma unroll
@@ -426,6 +430,7 @@ __global__ void __launch_bounds__(kThreads, 6) k_reuse_place(RuEnc a)
 {
     __shared__ uint32_t s_bm[32], s_pre[32], s_agg;
     const int t = threadIdx.x;
+    grid_dep_wait();   // prefixes, cache and staging come from the kernels before
     if (t < 32) s_bm[t] = 0;
     const TilePos tp = tile_pos(blockIdx.x, a.count, a.tpc);
     const uint32_t ci = tp.ci, lt = tp.lt;
@@ -482,6 +487,7 @@ __global__ void __launch_bounds__(kThreads, 6) k_reuse_place32(RuEnc a)
 {
     __shared__ uint32_t s_bm[32], s_pre[32], s_agg;
     const int t = threadIdx.x;
+    grid_dep_wait();   // prefixes, cache and staging come from the kernels before
     if (t < 32) s_bm[t] = 0;
     const TilePos tp = tile_pos(blockIdx.x, a.count, a.tpc);
     const uint32_t ci = tp.ci, lt = tp.lt;
@@ -565,6 +571,7 @@ __global__ void __launch_bounds__(kPlaceThreads) k_reuse_place_coded(RuEnc a)
 {
     __shared__ __align__(16) uint32_t s_e[kSpecBytes / 4 + 4];
     const int t = threadIdx.x;
+    grid_dep_wait();   // prefixes, cache and staging come from the kernels before
     const TilePos tp = tile_pos(blockIdx.x, a.count, a.tpc);
     const uint32_t ci = tp.ci, lt = tp.lt;
     const uint32_t r = a.first + ci;
@@ -1241,22 +1248,19 @@ cudaError_t launch_reuse_encode(const ez_plan_s* p, const uint16_t* x, uint32_t 
         if (e != cudaSuccess) return e;
         e = launch_tile_scan(p, w.state_a, count, w.seg_a, w.counters + 4, w.counters + 7, dstatus, s);
         if (e != cudaSuccess) return e;
-        if (p->B >= 32) k_reuse_place32<<<tiles, kThreads, 0, s>>>(a);
-        else k_reuse_place<<<tiles, kThreads, 0, s>>>(a);
-        return cudaGetLastError();
+        return p->B >= 32 ? launch_dependent(k_reuse_place32, tiles, kThreads, 0, s, a)
+                          : launch_dependent(k_reuse_place, tiles, kThreads, 0, s, a);
     }
     a.plbuf = w.plbuf;
     a.escbuf = w.escbuf;
     a.state_b = w.state_b;
-    k_reuse_split<true><<<tiles, kThreads, 0, s>>>(a);
-    e = cudaGetLastError();
+    e = launch_dependent(k_reuse_split<true>, tiles, kThreads, 0, s, a);
     if (e != cudaSuccess) return e;
     e = launch_tile_scan(p, w.state_a, count, w.seg_a, w.counters + 4, w.counters + 7, dstatus, s);
     if (e != cudaSuccess) return e;
     e = launch_tile_scan(p, w.state_b, count, w.seg_b, w.counters + 5, w.counters + 7, dstatus, s);
     if (e != cudaSuccess) return e;
-    k_reuse_place_coded<<<tiles, kPlaceThreads, 0, s>>>(a);
-    return cudaGetLastError();
+    return launch_dependent(k_reuse_place_coded, tiles, kPlaceThreads, 0, s, a);
 }
 
 cudaError_t launch_reuse_decode(const ez_plan_s* p, const uint8_t* in, const uint64_t* offsets,

@@ -29,6 +29,8 @@ __global__ void __launch_bounds__(kThreads) k_tile_scan(unsigned long long* st, 
     __shared__ unsigned long long s_warp[kThreads / 32];
     __shared__ unsigned long long s_prefix;
     const int t = threadIdx.x;
+    grid_dep_launch();
+    grid_dep_wait();   // the counts come from the kernel before
     const uint32_t id = next_tile(counter, &s_tile);
     const uint32_t c = id / spc, sg = id % spc;   // segments of a chunk in order
     if (c >= count) return;
@@ -60,9 +62,8 @@ cudaError_t launch_tile_scan(const ez_plan_s* p, unsigned long long* st, uint32_
     const uint32_t spc = (uint32_t)cdiv(p->tpc, kScanSpan);
     const uint64_t ctas = (uint64_t)count * spc;
     if (ctas > 0x7fffffffull) return cudaErrorInvalidValue;
-    k_tile_scan<<<(unsigned)ctas, kThreads, 0, s>>>(st, count, p->tpc, spc, seg_st, counter,
-                                                    abort, dstatus);
-    return cudaGetLastError();
+    return launch_dependent(k_tile_scan, (unsigned)ctas, kThreads, 0, s, st, count, p->tpc, spc, seg_st,
+                            counter, abort, dstatus);
 }
 
 uint64_t tile_scan_segments(uint64_t tpc) { return cdiv(tpc, kScanSpan); }

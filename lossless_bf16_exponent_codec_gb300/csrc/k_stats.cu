@@ -28,6 +28,7 @@ k_stats(const uint16_t* __restrict__ x, uint64_t n, uint64_t L, uint32_t first, 
 {
     extern __shared__ __align__(16) unsigned char dyn[];
     StatsSmem& S = *reinterpret_cast<StatsSmem*>(dyn);
+    grid_dep_launch();   // a dependent launch (the coded split) may be scheduled
     const uint32_t ci = blockIdx.x / tps, lt = blockIdx.x % tps;
     const uint64_t n_s = W ? shard_values(n, L, first + ci) : n;
     const uint64_t base = (uint64_t)lt * kStatsTile;
