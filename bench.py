@@ -201,12 +201,14 @@ def run_ours(args, world, rank, local):
     rc.gather_decode()
     ops = ["stats", "code3_encode", "code3_decode", "reuse_encode", "reuse_decode",
            "reuse_code3_encode", "reuse_code3_decode"]
-    # kernels each op launches (library code; the memsets of the workspace
-    # clears are copy-engine operations, not kernels)
-    launches = {"stats": 1, "code3_encode": 1, "code3_decode": 1,
-                "reuse_encode": 3,            # split, tile scan, place
+    # kernels each op launches (library code; the encoders clear their
+    # workspace with a kernel of their own)
+    launches = {"stats": 2,                   # workspace clear, statistics
+                "code3_encode": 2,            # workspace clear, encode
+                "code3_decode": 1,
+                "reuse_encode": 4,            # workspace clear, split, tile scan, place
                 "reuse_decode": 1,
-                "reuse_code3_encode": 5,      # shard stats, split, two scans, place
+                "reuse_code3_encode": 6,      # clear, shard statistics, split, two scans, place
                 "reuse_code3_decode": 1}
 
     def step(x, evs):

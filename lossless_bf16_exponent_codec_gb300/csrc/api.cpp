@@ -23,11 +23,11 @@ bool is_reuse(const ez_plan_s* p) { return p->codec != EZ_CODEC_CODE3; }
 
 ez_status cuda_status(cudaError_t e) { return e == cudaSuccess ? EZ_OK : EZ_ERR_CUDA; }
 
-// Clear [0, bytes) of the workspace on the stream.
+// Clear [0, bytes) of the workspace on the stream (a kernel; the encode's
+// first kernel is a dependent launch after it).
 ez_status clear_ws(void* ws, uint64_t bytes, cudaStream_t s)
 {
-    if (!bytes) return EZ_OK;
-    return cuda_status(cudaMemsetAsync(ws, 0, bytes, s));
+    return cuda_status(ezk::launch_zero(ws, bytes, s));
 }
 
 ez_status check_ws(const ez_plan_s* p, const void* ws, uint64_t ws_bytes)

@@ -46,6 +46,7 @@ struct WsView {
 WsView ws_view(const ez_plan_s* p, void* ws);
 
 // Scan segments per chunk of tpc tiles (k_scan.cu).
+cudaError_t launch_zero(void* p, uint64_t bytes, cudaStream_t s);
 uint64_t tile_scan_segments(uint64_t tpc);
 
 // Inclusive prefixes, per chunk, of the per-tile counts in st[count * tpc].

@@ -160,6 +160,7 @@ __global__ void __launch_bounds__(kEncThreads, 2) k_code3_encode(C3Enc a)
     __shared__ uint32_t s_efull[kSlots], s_edone[kSlots];
     __shared__ unsigned long long s_warp[kCompute / 32];
     const int t = threadIdx.x;
+    grid_dep_wait();   // the counters were cleared by the kernel before
     uint32_t E0 = __ldg(&a.st->E0);
     if (E0 > 249u) {
         if (t == 0) atomicOr(a.dstatus, EZ_DSTAT_BAD_STATS);
@@ -603,9 +604,8 @@ cudaError_t launch_code3_encode(const ez_plan_s* p, const uint16_t* x, uint32_t 
     static const cudaError_t attr = cudaFuncSetAttribute(
         k_code3_encode, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(EncSmem));
     if (attr != cudaSuccess) return attr;
-    k_code3_encode<<<persistent_grid(k_code3_encode, kEncThreads, sizeof(EncSmem)), kEncThreads,
-                     sizeof(EncSmem), s>>>(a);
-    return cudaGetLastError();
+    return launch_dependent(k_code3_encode, persistent_grid(k_code3_encode, kEncThreads, sizeof(EncSmem)),
+                            kEncThreads, sizeof(EncSmem), s, a);
 }
 
 cudaError_t launch_code3_decode(const ez_plan_s* p, const uint8_t* in, const uint64_t* offsets,

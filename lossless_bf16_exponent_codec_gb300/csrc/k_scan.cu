@@ -68,4 +68,24 @@ cudaError_t launch_tile_scan(const ez_plan_s* p, unsigned long long* st, uint32_
 
 uint64_t tile_scan_segments(uint64_t tpc) { return cdiv(tpc, kScanSpan); }
 
+// Workspace clear before an encode: a kernel rather than a memset, so that
+// the encode's first kernel can be a dependent launch (it starts its loads
+// while this runs and waits before it touches the workspace).
+__global__ void __launch_bounds__(kThreads) k_zero(uint4* p, uint64_t n16)
+{
+    grid_dep_launch();
+    for (uint64_t i = (uint64_t)blockIdx.x * kThreads + threadIdx.x; i < n16; i += (uint64_t)gridDim.x * kThreads)
+        p[i] = make_uint4(0, 0, 0, 0);
+}
+
+cudaError_t launch_zero(void* p, uint64_t bytes, cudaStream_t s)
+{
+    if (!bytes) return cudaSuccess;
+    if ((bytes & 15u) || (reinterpret_cast<uintptr_t>(p) & 15u)) return cudaMemsetAsync(p, 0, bytes, s);
+    const uint64_t n16 = bytes / 16;
+    const unsigned grid = (unsigned)umin64(cdiv(n16, kThreads), 1024);
+    k_zero<<<grid, kThreads, 0, s>>>(reinterpret_cast<uint4*>(p), n16);
+    return cudaGetLastError();
+}
+
 }  // namespace ezk

@@ -49,6 +49,7 @@ k_stats(const uint16_t* __restrict__ x, uint64_t n, uint64_t L, uint32_t first, 
 #pragma unroll
             for (int k = 0; k < 4; k++) st_add8(w[k], e7, hb, S);
         }
+        grid_dep_wait();   // the bins were cleared by the kernel before
         if (st_end(S, G + ci, tps)) st_finalize(G + ci, n_s, K, out + ci, S);
         return;
     }
@@ -61,7 +62,8 @@ k_stats(const uint16_t* __restrict__ x, uint64_t n, uint64_t L, uint32_t first, 
             for (uint32_t i = v; i < nv; i++) st_add(xt[i], elo, S);
         }
     }
-    if (st_end(S, G + ci, tps)) st_finalize(G + ci, n_s, K, out + ci, S);
+    grid_dep_wait();   // the bins were cleared by the kernel before
+        if (st_end(S, G + ci, tps)) st_finalize(G + ci, n_s, K, out + ci, S);
 }
 
 static cudaError_t stats_launch(const uint16_t* x, uint64_t n, uint64_t L, uint32_t first,
@@ -74,9 +76,8 @@ static cudaError_t stats_launch(const uint16_t* x, uint64_t n, uint64_t L, uint3
     static const cudaError_t attr = cudaFuncSetAttribute(
         k_stats, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(StatsSmem));
     if (attr != cudaSuccess) return attr;
-    k_stats<<<(unsigned)tiles, kThreads, sizeof(StatsSmem), s>>>(x, n, L, first, W, (uint32_t)tps,
-                                                               G, out, K);
-    return cudaGetLastError();
+    return launch_dependent(k_stats, (unsigned)tiles, kThreads, sizeof(StatsSmem), s, x, n, L, first, W,
+                            (uint32_t)tps, G, out, K);
 }
 
 cudaError_t launch_stats(const ez_plan_s* p, const uint16_t* x, uint64_t n, ez_stats_t* out,
