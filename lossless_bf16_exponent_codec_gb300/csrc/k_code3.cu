@@ -127,7 +127,7 @@ __device__ __forceinline__ uint32_t byte_of(uint32_t lo, uint32_t hi, int i)
 }
 
 constexpr uint32_t kEndMark = 0xFFFFFFFFu;
-constexpr int kStages = 4;                       // input ring depth (16 KB per stage)
+constexpr int kStages = 2;                       // input ring depth (16 KB per stage)
 constexpr int kEncThreads = kCompute + 64;       // + chain warp + producer warp
 
 struct EncSmem {
@@ -149,7 +149,7 @@ __device__ __forceinline__ uint4 lds128(const uint8_t* p)
 //  * chain warp: resolves each tile's escape prefix in order (decoupled
 //    look-back), writes the escapes, and on a chunk's last tile its header,
 //    padding and size.
-__global__ void __launch_bounds__(kEncThreads, 2) k_code3_encode(C3Enc a)
+__global__ void __launch_bounds__(kEncThreads, 3) k_code3_encode(C3Enc a)
 {
     extern __shared__ __align__(128) unsigned char dyn[];
     EncSmem& S = *reinterpret_cast<EncSmem*>(dyn);
