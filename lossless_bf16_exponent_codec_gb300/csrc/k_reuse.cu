@@ -248,7 +248,7 @@ __device__ __forceinline__ uint32_t codes_of_bytes(const uint32_t* lut, uint32_t
 // aggregate.  The updated cache then holds every current exponent at its own
 // position, so the later steps read the changed exponents from it.
 template <bool kCoded>
-__global__ void __launch_bounds__(kThreads, kCoded ? 4 : 5) k_reuse_split(RuEnc a)
+__global__ void __launch_bounds__(kThreads, kCoded ? 4 : 6) k_reuse_split(RuEnc a)
 {
     __shared__ uint32_t s_gl[32], s_bm[32], s_pre[32];
     __shared__ uint32_t s_lut[kCoded ? 256 : 1];
