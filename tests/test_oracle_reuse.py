@@ -102,7 +102,7 @@ def test_reuse_rate_uniform_flips(orc, B):
     rate, nb = _reuse_rate(orc, x0, x1, B)
     p = (1 - c) ** B
     assert abs(rate - p) < 5 * math.sqrt(p * (1 - p) / nb) + 1e-9
-    # the survey values at c = 0.005
+    # (1 - c)^B at c = 0.005 to four places
     table = {64: 0.7256, 128: 0.5264, 256: 0.2771, 512: 0.0768, 1024: 0.0059}
     assert p == pytest.approx(table[B], abs=1e-4)
     # the realised element change rate is c
