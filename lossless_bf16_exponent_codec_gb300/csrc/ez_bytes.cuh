@@ -4,8 +4,9 @@
 // the escaping exponent bytes, in value order, to the tile's escape list; the
 // decoder must put the next popc(m) bytes of that list back at the set bits
 // of m.  Both are byte permutations that depend only on m, so they are done
-// with PRMT (__byte_perm) and selectors from compile-time tables indexed by m
-// instead of a per-escape loop.
+// with PRMT (__byte_perm) instead of a per-escape loop: the encoder takes its
+// selectors from a compile-time table indexed by m, the decoder computes them
+// with integer multiplies.
 #pragma once
 
 #include <cstdint>
@@ -15,36 +16,27 @@ namespace ez {
 struct ByteTables {
     uint32_t comp_lo[256];   // PRMT selector: selected bytes 0..3 of (lo, hi)
     uint32_t comp_hi[256];   // selected bytes 4..7
-    uint32_t exp_lo[256];    // PRMT selector: byte i (0..3) <- compact byte rank(i)
-    uint32_t exp_hi[256];    // byte i (4..7)
     unsigned long long bmask[256];    // 0xFF in byte i where bit i of m is set
-    unsigned long long spread[256];   // bit i of b -> bit 8i
 };
 
 constexpr ByteTables make_byte_tables()
 {
     ByteTables t{};
     for (int m = 0; m < 256; m++) {
-        uint32_t clo = 0, chi = 0, elo = 0, ehi = 0;
-        unsigned long long bm = 0, sp = 0;
+        uint32_t clo = 0, chi = 0;
+        unsigned long long bm = 0;
         int rank = 0;
         for (int i = 0; i < 8; i++) {
             if ((m >> i) & 1) {
                 if (rank < 4) clo |= (uint32_t)i << (4 * rank);
                 else chi |= (uint32_t)i << (4 * (rank - 4));
-                if (i < 4) elo |= (uint32_t)rank << (4 * i);
-                else ehi |= (uint32_t)rank << (4 * (i - 4));
                 bm |= 0xFFull << (8 * i);
-                sp |= 1ull << (8 * i);
                 rank++;
             }
         }
         t.comp_lo[m] = clo;
         t.comp_hi[m] = chi;
-        t.exp_lo[m] = elo;
-        t.exp_hi[m] = ehi;
         t.bmask[m] = bm;
-        t.spread[m] = sp;
     }
     return t;
 }
@@ -79,34 +71,6 @@ __device__ __forceinline__ void load_unaligned8(const uint32_t* s32, uint32_t r,
     hi = __byte_perm(w1, w2, sel);
 }
 
-// e8 with the bytes at the set bits of m replaced, in order, by the compact
-// bytes (c_lo, c_hi).
-__device__ __forceinline__ unsigned long long insert_selected(unsigned long long e8, uint32_t m,
-                                                              uint32_t c_lo, uint32_t c_hi)
-{
-    const unsigned long long x =
-        (unsigned long long)__byte_perm(c_lo, c_hi, __ldg(&kByteTables.exp_hi[m])) << 32 |
-        __byte_perm(c_lo, c_hi, __ldg(&kByteTables.exp_lo[m]));
-    const unsigned long long bm = __ldg(&kByteTables.bmask[m]);
-    return (e8 & ~bm) | (x & bm);
-}
-
-// insert_selected with the expansion selectors in shared memory (s_elo/s_ehi
-// = ByteTables::exp_lo/exp_hi) and the byte mask made from the bit spread
-// s_spread[m] (bit i -> bit 8i): mask = spread * 255.
-__device__ __forceinline__ unsigned long long insert_selected_s(unsigned long long e8, uint32_t m,
-                                                                uint32_t c_lo, uint32_t c_hi,
-                                                                const uint32_t* s_elo,
-                                                                const uint32_t* s_ehi,
-                                                                const unsigned long long* s_spread)
-{
-    const unsigned long long x = (unsigned long long)__byte_perm(c_lo, c_hi, s_ehi[m]) << 32 |
-                                 __byte_perm(c_lo, c_hi, s_elo[m]);
-    const unsigned long long sp = s_spread[m];
-    const unsigned long long bm = (sp << 8) - sp;
-    return (e8 & ~bm) | (x & bm);
-}
-
 // ---- table-free forms (integer multiplies instead of shared-memory lookups) ----
 // Bits 0..3 of n4 (n4 < 16) to bits 0, 8, 16, 24: the four shifted copies
 // n4 << 7k (k = 0..3) do not overlap, so the product has no carries and bit
@@ -138,11 +102,6 @@ __device__ __forceinline__ unsigned long long insert_selected_a(unsigned long lo
                                  __byte_perm(c_lo, c_hi, sel_lo);
     const unsigned long long bm = (unsigned long long)(bh * 255u) << 32 | (bl * 255u);
     return (e8 & ~bm) | (x & bm);
-}
-
-__device__ __forceinline__ unsigned long long spread_bits(uint32_t b)
-{
-    return __ldg(&kByteTables.spread[b]);
 }
 
 __device__ __forceinline__ unsigned long long byte_mask(uint32_t m)

@@ -48,17 +48,6 @@ __host__ __device__ __forceinline__ uint64_t shard_values(uint64_t n, uint64_t L
 
 // ---- BF16 fields (CIERA split; ZipCCL 3.1) ---------------------------------
 __device__ __forceinline__ uint32_t exp_of(uint32_t h) { return (h >> 7) & 0xFFu; }
-__device__ __forceinline__ uint32_t sm_of(uint32_t h) { return ((h >> 8) & 0x80u) | (h & 0x7Fu); }
-__device__ __forceinline__ uint32_t merge_of(uint32_t sm, uint32_t e)
-{
-    return ((sm & 0x80u) << 8) | (e << 7) | (sm & 0x7Fu);
-}
-// value i (0..7) of a 16-byte group held as uint4
-__device__ __forceinline__ uint32_t half_of(const uint4& w, int i)
-{
-    uint32_t word = (i < 2) ? w.x : (i < 4) ? w.y : (i < 6) ? w.z : w.w;
-    return (i & 1) ? (word >> 16) : (word & 0xFFFFu);
-}
 
 // ---- SWAR helpers: two BF16 values per 32-bit word --------------------------
 // Sign+mantissa bytes of the 4 values in words a (values 0,1) and b (2,3):
@@ -286,12 +275,6 @@ struct ShardIter {
     __device__ __forceinline__ bool valid() const { return next < count; }
     __device__ __forceinline__ void advance() { next = (step == count) ? count : next + step; }
 };
-
-// CTAs serving shard s (for the count <= G case; 1 otherwise)
-__device__ __forceinline__ uint32_t servers_of(uint32_t G, uint32_t count)
-{
-    return count <= G ? G / count : 1u;
-}
 
 // Exclusive scan over the kCompute compute threads (named barrier 1); s_warp
 // holds 8 entries and must not be reused before the next compute_sync().
