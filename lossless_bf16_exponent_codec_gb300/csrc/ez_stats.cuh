@@ -39,13 +39,15 @@ struct StatsBins {                 // per shard, in the workspace (zeroed per ca
 };
 
 // Per-CTA accumulators (dynamic shared memory).  A CTA adds at most
-// kStatsMaxValues values before it flushes, so no cell or bin can overflow:
-// counts <= 2^23, |sum +-M| <= 2^23 * 255 < 2^31, and sums of M^2 are 64-bit.
+// kStatsMaxValues values before it flushes, so no cell or bin can overflow
+// 32 bits: counts <= 2^16, |sum +-M| <= 2^16 * 255 < 2^31 and sums of M^2
+// <= 2^16 * 255^2 < 2^32 (all plain 32-bit shared atomics).
 constexpr int kStatsWin = 16;                  // binades in a CTA's window
-constexpr uint32_t kStatsMaxValues = 1u << 23;
+constexpr uint32_t kStatsMaxValues = 1u << 16;
+static_assert((unsigned long long)kStatsMaxValues * 255u * 255u < (1ull << 32), "sum of M^2 fits 32 bits");
 struct StatsSmem {
     uint32_t hist[2 * kStatsWin * 128];        // [sign][d][mantissa]
-    unsigned long long s2[256];
+    uint32_t s2[256];
     uint32_t cnt[256];
     int s1[256];
     uint32_t sample[256];
@@ -100,7 +102,7 @@ __device__ __forceinline__ void st_add_slow(uint32_t h, StatsSmem& S)
     const uint32_t M = (E ? 128u : 0u) | (h & 0x7Fu);
     if (E != 255u && M) {
         atomicAdd(&S.s1[E], (h & 0x8000u) ? -(int)M : (int)M);
-        atomicAdd(&S.s2[E], (unsigned long long)(M * M));
+        atomicAdd(&S.s2[E], M * M);
     }
 }
 
@@ -186,8 +188,7 @@ __device__ __forceinline__ bool st_end(StatsSmem& S, StatsBins* G, uint32_t expe
     {
         const uint32_t s = (uint32_t)t >> 7, d = ((uint32_t)t >> 3) & 15u, part = (uint32_t)t & 7u;
         const uint4* row = reinterpret_cast<const uint4*>(&S.hist[(s << 11) | (d << 7) | (part << 4)]);
-        uint32_t c = 0, s1 = 0;
-        unsigned long long s2 = 0;
+        uint32_t c = 0, s1 = 0, s2 = 0;
         uint32_t M = 128u + (part << 4);
 #pragma unroll
         for (int q = 0; q < 4; q++) {
@@ -197,7 +198,7 @@ __device__ __forceinline__ bool st_end(StatsSmem& S, StatsBins* G, uint32_t expe
             for (int i = 0; i < 4; i++, M++) {
                 c += xs[i];
                 s1 += xs[i] * M;
-                s2 += (unsigned long long)xs[i] * (M * M);
+                s2 += xs[i] * (M * M);
             }
         }
 #pragma unroll
@@ -217,7 +218,7 @@ __device__ __forceinline__ bool st_end(StatsSmem& S, StatsBins* G, uint32_t expe
     // per-exponent bins -> global
     if (S.cnt[t]) atomicAdd(&G->hist[t], (unsigned long long)S.cnt[t]);
     if (S.s1[t]) atomicAdd(&G->s1[t], (unsigned long long)(long long)S.s1[t]);
-    if (S.s2[t]) atomicAdd(&G->s2[t], S.s2[t]);
+    if (S.s2[t]) atomicAdd(&G->s2[t], (unsigned long long)S.s2[t]);
     // the barrier orders every thread's bin atomics before thread 0's fence
     // (fences are cumulative), which orders them before the completion count
     __syncthreads();
@@ -319,62 +320,78 @@ __device__ __forceinline__ uint32_t window_base(double var, double K)
 // terms into 32-bit pieces at their limbs of the three big sums (positive and
 // negative parts of s1, and s2); the bins of one warp reach at most five
 // consecutive limbs, so each warp adds its pieces limb by limb with shuffles
-// and its lane 0 adds the five warp totals to per-limb 64-bit accumulators
-// (eight warps: no long chains of shared atomics on one limb).  Three threads
-// then propagate the carries into 32-bit limbs, and thread 0 does the
-// rounding.  A limb accumulator receives at most 3 * 256 pieces < 2^42.
+// and stores its five slot sums with their first limb (no atomics).  One
+// thread per limb then adds the eight warps' slots, three threads propagate
+// the carries into 32-bit limbs, and two threads round s1 and s2 at the same
+// time.  A limb total is at most 8 * 5 * 32 pieces of 32 bits < 2^43.
+constexpr int kAccLimbs = kLimbs + 2;
 struct FinSmem {
     unsigned long long h[256];
-    unsigned long long acc[3][kLimbs + 2];     // P, Q, R
+    unsigned long long slot[kThreads / 32][3][5];   // per warp and sum: slot sums
+    int base[kThreads / 32][3];                     // limb of each warp's slot 0
+    unsigned long long acc[3][kAccLimbs];           // P, Q, R limb totals
     uint32_t w[3][kLimbs];
-    unsigned long long n_fin;
+    unsigned long long nw[kThreads / 32];           // finite values per warp
+    double s1d, s2d;
 };
 static_assert(sizeof(FinSmem) <= sizeof(StatsSmem::hist), "finalise scratch fits the histogram");
 
 // The 32-bit pieces of v * 2^sh at limbs sh/32, sh/32 + 1, sh/32 + 2, added
 // over the warp (all 32 lanes call it; lanes without a term pass v = 0).  The
-// lanes' first limbs lie within 3 of lane 0's, so five slot sums cover them.
-__device__ __forceinline__ void warp_acc_add_shl(unsigned long long* acc, unsigned long long v, int sh)
+// lanes' first limbs lie within 3 of lane 0's, so five slot sums cover them;
+// lane 0 stores them to slot[0..4] and lane 0's limb to *base.
+__device__ __forceinline__ void warp_slot_sums(unsigned long long* slot, int* base, unsigned long long v, int sh)
 {
     const int limb = sh >> 5, bit = sh & 31;
     const unsigned long long p0 = (uint32_t)(v << bit);
     const unsigned long long p1 = (uint32_t)(bit ? (v >> (32 - bit)) : (v >> 32));
     const unsigned long long p2 = (uint32_t)(bit ? (v >> (64 - bit)) : 0ull);
-    const int base = __shfl_sync(kFull, limb, 0);
-    const int k = limb - base;
+    const int b0 = __shfl_sync(kFull, limb, 0);
+    const int k = limb - b0;
 #pragma unroll
     for (int j = 0; j < 5; j++) {
         unsigned long long c = (j == k ? p0 : 0ull) + (j == k + 1 ? p1 : 0ull) + (j == k + 2 ? p2 : 0ull);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(kFull, c, o);
-        if ((threadIdx.x & 31) == 0 && c) atomicAdd(&acc[base + j], c);
+        if ((threadIdx.x & 31) == 0) slot[j] = c;
     }
+    if ((threadIdx.x & 31) == 0) *base = b0;
 }
 
 static __device__ __noinline__ void st_finalize(const StatsBins* G, uint64_t n, double K, ez_stats_t* out,
                                                 StatsSmem& S)
 {
-    const int t = threadIdx.x;
+    const int t = threadIdx.x, wid = t >> 5, lane = t & 31;
     FinSmem& F = *reinterpret_cast<FinSmem*>(S.hist);
     __syncthreads();
-    unsigned long long* accz = &F.acc[0][0];
-    for (int i = t; i < 3 * (kLimbs + 2); i += kThreads) accz[i] = 0;
-    if (t == 0) F.n_fin = 0;
     const unsigned long long h = __ldcg(&G->hist[t]);
     const long long s1 = (long long)__ldcg(&G->s1[t]);
     const unsigned long long s2 = __ldcg(&G->s2[t]);
     F.h[t] = h;
     out->hist[t] = h;
-    __syncthreads();
     {
         // v * 2^133 = +-M * 2^sh; v^2 * 2^266 = M^2 * 2^(2 sh); bin 255 holds no terms
         const int sh = (t ? t : 1) - 1;
         const bool live = t < 255;
-        warp_acc_add_shl(F.acc[0], live && s1 > 0 ? (unsigned long long)s1 : 0ull, sh);
-        warp_acc_add_shl(F.acc[1], live && s1 < 0 ? (unsigned long long)(-s1) : 0ull, sh);
-        warp_acc_add_shl(F.acc[2], live ? s2 : 0ull, 2 * sh);
+        warp_slot_sums(F.slot[wid][0], &F.base[wid][0], live && s1 > 0 ? (unsigned long long)s1 : 0ull, sh);
+        warp_slot_sums(F.slot[wid][1], &F.base[wid][1], live && s1 < 0 ? (unsigned long long)(-s1) : 0ull, sh);
+        warp_slot_sums(F.slot[wid][2], &F.base[wid][2], live ? s2 : 0ull, 2 * sh);
+        unsigned long long c = live ? h : 0ull;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(kFull, c, o);
+        if (lane == 0) F.nw[wid] = c;
     }
-    if (t < 255 && h) atomicAdd(&F.n_fin, h);
+    __syncthreads();
+    if (t < 3 * kAccLimbs) {
+        const int q = t / kAccLimbs, i = t % kAccLimbs;
+        unsigned long long a = 0;
+#pragma unroll
+        for (int v = 0; v < kThreads / 32; v++) {
+            const int j = i - F.base[v][q];
+            if (j >= 0 && j < 5) a += F.slot[v][q][j];
+        }
+        F.acc[q][i] = a;
+    }
     __syncthreads();
     if (t < 3) {
         unsigned long long carry = 0;
@@ -385,20 +402,25 @@ static __device__ __noinline__ void st_finalize(const StatsBins* G, uint64_t n, 
         }
     }
     __syncthreads();
-    if (t != 0) return;
-    uint32_t* P = F.w[0];
-    uint32_t* Q = F.w[1];
-    const uint32_t* R = F.w[2];
-    const unsigned long long n_fin = F.n_fin;
-    double s1d;
-    if (big_cmp(P, Q) >= 0) {
-        big_sub(P, Q);
-        s1d = big_round(P, -133);
-    } else {
-        big_sub(Q, P);
-        s1d = -big_round(Q, -133);
+    if (t == 0) {
+        uint32_t* P = F.w[0];
+        uint32_t* Q = F.w[1];
+        if (big_cmp(P, Q) >= 0) {
+            big_sub(P, Q);
+            F.s1d = big_round(P, -133);
+        } else {
+            big_sub(Q, P);
+            F.s1d = -big_round(Q, -133);
+        }
+    } else if (t == 32) {
+        F.s2d = big_round(F.w[2], -266);
     }
-    const double s2d = big_round(R, -266);
+    __syncthreads();
+    if (t != 0) return;
+    unsigned long long n_fin = 0;
+#pragma unroll
+    for (int v = 0; v < kThreads / 32; v++) n_fin += F.nw[v];
+    const double s1d = F.s1d, s2d = F.s2d;
     double var = 0.0, sigma = 0.0;
     uint32_t rule = 1, E0 = 0;
     if (n_fin >= 2) {

@@ -16,6 +16,7 @@ static_assert(sizeof(ez_stats_t) == 2120, "ez_stats_t layout");
 
 constexpr int kStatsLoads = 32;                             // 16-B loads per thread
 constexpr uint32_t kStatsTile = kThreads * kStatsLoads * 8;   // 65536 values
+static_assert(kStatsTile <= kStatsMaxValues, "a tile's sums fit the 32-bit shared bins");
 
 // One CTA per tile of 65536 values of one shard, 8 resident CTAs per SM;
 // every thread keeps four 16-byte loads in flight and adds their 32 values to
@@ -63,7 +64,7 @@ k_stats(const uint16_t* __restrict__ x, uint64_t n, uint64_t L, uint32_t first, 
         }
     }
     grid_dep_wait();   // the bins were cleared by the kernel before
-        if (st_end(S, G + ci, tps)) st_finalize(G + ci, n_s, K, out + ci, S);
+    if (st_end(S, G + ci, tps)) st_finalize(G + ci, n_s, K, out + ci, S);
 }
 
 static cudaError_t stats_launch(const uint16_t* x, uint64_t n, uint64_t L, uint32_t first,
