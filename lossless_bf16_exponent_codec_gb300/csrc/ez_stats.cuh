@@ -232,36 +232,39 @@ __device__ __forceinline__ bool st_end(StatsSmem& S, StatsBins* G, uint32_t expe
     return last;
 }
 
-// ---- exact rounding of big sums --------------------------------------------
+// ---- exact rounding of big sums ---------------------------------------------
+// A big sum is a vector of 32-bit limbs held by one warp, limb i in lane i
+// (lanes kLimbs..31 hold 0): kLimbs limbs hold every sum of at most 2^40
+// terms below 2^16 * 2^506.
 
-constexpr int kLimbs = 24;   // 768-bit non-negative integers, little-endian 32-bit limbs
+constexpr int kLimbs = 24;
 
-__device__ __forceinline__ int big_cmp(const uint32_t* a, const uint32_t* b)
+// Carry-in bits of an addition whose limbs generate a carry (mask G) or pass
+// one on (mask P, disjoint from G): the carries of the bit vectors G | P and
+// G added as integers are exactly those of the limbs.
+__device__ __forceinline__ uint32_t carry_in_mask(uint32_t G, uint32_t P) { return ((G | P) + G) ^ P; }
+
+// Lane i holds x_i < 2^48 (zero in lanes >= kLimbs); returns limb i of the
+// sum of x_i * 2^(32 i).  After adding each lane's high word into the next
+// lane, a limb that carries out holds less than 2^16, so the remaining carries
+// are single bits.
+__device__ __forceinline__ uint32_t warp_carry(unsigned long long x)
 {
-    for (int i = kLimbs - 1; i >= 0; i--)
-        if (a[i] != b[i]) return a[i] > b[i] ? 1 : -1;
-    return 0;
+    const uint32_t lane = threadIdx.x & 31u;
+    uint32_t up = __shfl_up_sync(kFull, (uint32_t)(x >> 32), 1);
+    if (lane == 0) up = 0;
+    const unsigned long long v = (x & 0xFFFFFFFFull) + up;
+    const uint32_t l = (uint32_t)v;
+    const uint32_t C = carry_in_mask(__ballot_sync(kFull, (v >> 32) != 0), __ballot_sync(kFull, l == 0xFFFFFFFFu));
+    return l + ((C >> lane) & 1u);
 }
 
-__device__ __forceinline__ void big_sub(uint32_t* a, const uint32_t* b)   // a >= b
+// Limbs of a - b (a >= b).
+__device__ __forceinline__ uint32_t warp_sub(uint32_t a, uint32_t b)
 {
-    unsigned long long borrow = 0;
-    for (int i = 0; i < kLimbs; i++) {
-        const unsigned long long bi = (unsigned long long)b[i] + borrow;
-        borrow = (unsigned long long)a[i] < bi ? 1ull : 0ull;
-        a[i] = (uint32_t)((unsigned long long)a[i] - bi);
-    }
-}
-
-__device__ __forceinline__ uint32_t limb(const uint32_t* w, int i) { return (i >= 0 && i < kLimbs) ? w[i] : 0u; }
-
-// Bits [pos, pos + 64) of the number (pos >= 0).
-__device__ __forceinline__ unsigned long long bits64(const uint32_t* w, int pos)
-{
-    const int i = pos >> 5, sh = pos & 31;
-    const unsigned long long lo = (unsigned long long)limb(w, i) | (unsigned long long)limb(w, i + 1) << 32;
-    if (!sh) return lo;
-    return (lo >> sh) | ((unsigned long long)limb(w, i + 2) << (64 - sh));
+    const uint32_t lane = threadIdx.x & 31u;
+    const uint32_t C = carry_in_mask(__ballot_sync(kFull, a < b), __ballot_sync(kFull, a == b));
+    return a - b - ((C >> lane) & 1u);
 }
 
 // 2^e as a double, e in the normal range
@@ -270,28 +273,30 @@ __device__ __forceinline__ double pow2d(int e)
     return __longlong_as_double((long long)(e + 1023) << 52);
 }
 
-// w * 2^scale to the nearest double, ties to even: the top 53 bits, the next
-// bit and whether any bit below it is set, taken a word at a time.
-static __device__ __noinline__ double big_round(const uint32_t* w, int scale)
+// (sum of w_i 2^(32 i)) * 2^scale to the nearest double, ties to even: the
+// top 53 bits, the next bit and whether any bit below it is set.
+__device__ __forceinline__ double warp_round(uint32_t w, int scale)
 {
-    int top = -1;
-    for (int i = kLimbs - 1; i >= 0; i--) {
-        if (w[i]) { top = i; break; }
-    }
-    if (top < 0) return 0.0;
-    const int L = top * 32 + (32 - __clz(w[top]));     // bit length
-    if (L <= 53)                                       // exact: at most two limbs
-        return __dmul_rn((double)((unsigned long long)w[0] | (unsigned long long)limb(w, 1) << 32),
-                         pow2d(scale));
-    unsigned long long top64;                          // bits [L-64, L), zero-filled below 0
+    const uint32_t lane = threadIdx.x & 31u;
+    const uint32_t nz = __ballot_sync(kFull, w != 0);
+    if (!nz) return 0.0;
+    const int top = 31 - __clz((int)nz);
+    const int L = top * 32 + (32 - __clz((int)__shfl_sync(kFull, w, top)));   // bit length
+    const unsigned long long low = (unsigned long long)__shfl_sync(kFull, w, 0) |
+                                   (unsigned long long)__shfl_sync(kFull, w, 1) << 32;
+    if (L <= 53) return __dmul_rn((double)low, pow2d(scale));                // exact: two limbs
+    unsigned long long top64;                                                 // bits [L-64, L)
     bool sticky = false;
     if (L >= 64) {
-        top64 = bits64(w, L - 64);
-        const int below = L - 64;                      // bits [0, below) feed the sticky bit
-        for (int i = 0; i < (below >> 5); i++) sticky |= w[i] != 0;
-        if (below & 31) sticky |= (w[below >> 5] & ((1u << (below & 31)) - 1u)) != 0;
+        const int pos = L - 64, i = pos >> 5, sh = pos & 31;                 // i + 2 <= kLimbs
+        const uint32_t w0 = __shfl_sync(kFull, w, i), w1 = __shfl_sync(kFull, w, i + 1),
+                       w2 = __shfl_sync(kFull, w, i + 2);
+        const unsigned long long lo = (unsigned long long)w0 | (unsigned long long)w1 << 32;
+        top64 = sh ? (lo >> sh) | ((unsigned long long)w2 << (64 - sh)) : lo;
+        sticky = __ballot_sync(kFull, w != 0 && (int)lane < i) != 0;         // bits [0, 32 i)
+        if (sh) sticky |= (w0 & ((1u << sh) - 1u)) != 0;                      // bits [32 i, pos)
     } else {
-        top64 = bits64(w, 0) << (64 - L);
+        top64 = low << (64 - L);
     }
     unsigned long long q = top64 >> 11;                // the top 53 bits
     const bool half = (top64 >> 10) & 1ull;
@@ -319,22 +324,26 @@ __device__ __forceinline__ uint32_t window_base(double var, double K)
 // The last CTA finalises.  Every thread takes one exponent bin and splits its
 // terms into 32-bit pieces at their limbs of the three big sums (positive and
 // negative parts of s1, and s2); the bins of one warp reach at most five
-// consecutive limbs, so each warp adds its pieces limb by limb with shuffles
-// and stores its five slot sums with their first limb (no atomics).  One
-// thread per limb then adds the eight warps' slots, three threads propagate
-// the carries into 32-bit limbs, and two threads round s1 and s2 at the same
-// time.  A limb total is at most 8 * 5 * 32 pieces of 32 bits < 2^43.
-constexpr int kAccLimbs = kLimbs + 2;
+// consecutive limbs, so each warp adds its pieces limb by limb (warp
+// reductions of the 16-bit halves) and stores its five slot sums with their
+// first limb.  Warp 0 then gathers the limbs of s1's two parts (lane i adds
+// the eight warps' slots at limb i), resolves the carries, subtracts and
+// rounds; warp 1 does the same for s2 at the same time.  A limb total is at
+// most 256 pieces of 32 bits < 2^40.
 struct FinSmem {
     unsigned long long h[256];
     unsigned long long slot[kThreads / 32][3][5];   // per warp and sum: slot sums
     int base[kThreads / 32][3];                     // limb of each warp's slot 0
-    unsigned long long acc[3][kAccLimbs];           // P, Q, R limb totals
-    uint32_t w[3][kLimbs];
     unsigned long long nw[kThreads / 32];           // finite values per warp
-    double s1d, s2d;
+    double s1d, s2d, b;
 };
 static_assert(sizeof(FinSmem) <= sizeof(StatsSmem::hist), "finalise scratch fits the histogram");
+
+// Sum over the warp of 32-bit values
+__device__ __forceinline__ unsigned long long warp_sum32(uint32_t v)
+{
+    return ((unsigned long long)__reduce_add_sync(kFull, v >> 16) << 16) + __reduce_add_sync(kFull, v & 0xFFFFu);
+}
 
 // The 32-bit pieces of v * 2^sh at limbs sh/32, sh/32 + 1, sh/32 + 2, added
 // over the warp (all 32 lanes call it; lanes without a term pass v = 0).  The
@@ -343,19 +352,30 @@ static_assert(sizeof(FinSmem) <= sizeof(StatsSmem::hist), "finalise scratch fits
 __device__ __forceinline__ void warp_slot_sums(unsigned long long* slot, int* base, unsigned long long v, int sh)
 {
     const int limb = sh >> 5, bit = sh & 31;
-    const unsigned long long p0 = (uint32_t)(v << bit);
-    const unsigned long long p1 = (uint32_t)(bit ? (v >> (32 - bit)) : (v >> 32));
-    const unsigned long long p2 = (uint32_t)(bit ? (v >> (64 - bit)) : 0ull);
+    const uint32_t p0 = (uint32_t)(v << bit);
+    const uint32_t p1 = (uint32_t)(bit ? (v >> (32 - bit)) : (v >> 32));
+    const uint32_t p2 = (uint32_t)(bit ? (v >> (64 - bit)) : 0ull);
     const int b0 = __shfl_sync(kFull, limb, 0);
     const int k = limb - b0;
 #pragma unroll
     for (int j = 0; j < 5; j++) {
-        unsigned long long c = (j == k ? p0 : 0ull) + (j == k + 1 ? p1 : 0ull) + (j == k + 2 ? p2 : 0ull);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(kFull, c, o);
+        const unsigned long long c = warp_sum32((j == k ? p0 : 0u) + (j == k + 1 ? p1 : 0u) + (j == k + 2 ? p2 : 0u));
         if ((threadIdx.x & 31) == 0) slot[j] = c;
     }
     if ((threadIdx.x & 31) == 0) *base = b0;
+}
+
+// Lane i of the calling warp: limb i of sum q, before carries.
+__device__ __forceinline__ unsigned long long gather_limb(const FinSmem& F, int q)
+{
+    const int i = (int)(threadIdx.x & 31);
+    unsigned long long a = 0;
+#pragma unroll
+    for (int v = 0; v < kThreads / 32; v++) {
+        const int j = i - F.base[v][q];
+        if (j >= 0 && j < 5) a += F.slot[v][q][j];
+    }
+    return a;
 }
 
 static __device__ __noinline__ void st_finalize(const StatsBins* G, uint64_t n, double K, ez_stats_t* out,
@@ -376,68 +396,59 @@ static __device__ __noinline__ void st_finalize(const StatsBins* G, uint64_t n, 
         warp_slot_sums(F.slot[wid][0], &F.base[wid][0], live && s1 > 0 ? (unsigned long long)s1 : 0ull, sh);
         warp_slot_sums(F.slot[wid][1], &F.base[wid][1], live && s1 < 0 ? (unsigned long long)(-s1) : 0ull, sh);
         warp_slot_sums(F.slot[wid][2], &F.base[wid][2], live ? s2 : 0ull, 2 * sh);
-        unsigned long long c = live ? h : 0ull;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(kFull, c, o);
-        if (lane == 0) F.nw[wid] = c;
+        // counts are at most 2^40: two 20-bit halves
+        const unsigned long long c = live ? h : 0ull;
+        const unsigned long long nw = ((unsigned long long)__reduce_add_sync(kFull, (uint32_t)(c >> 20)) << 20) +
+                                      __reduce_add_sync(kFull, (uint32_t)(c & 0xFFFFFu));
+        if (lane == 0) F.nw[wid] = nw;
     }
     __syncthreads();
-    if (t < 3 * kAccLimbs) {
-        const int q = t / kAccLimbs, i = t % kAccLimbs;
-        unsigned long long a = 0;
-#pragma unroll
-        for (int v = 0; v < kThreads / 32; v++) {
-            const int j = i - F.base[v][q];
-            if (j >= 0 && j < 5) a += F.slot[v][q][j];
-        }
-        F.acc[q][i] = a;
-    }
-    __syncthreads();
-    if (t < 3) {
-        unsigned long long carry = 0;
-        for (int i = 0; i < kLimbs; i++) {
-            const unsigned long long x = F.acc[t][i] + carry;
-            F.w[t][i] = (uint32_t)x;
-            carry = x >> 32;
-        }
-    }
-    __syncthreads();
-    if (t == 0) {
-        uint32_t* P = F.w[0];
-        uint32_t* Q = F.w[1];
-        if (big_cmp(P, Q) >= 0) {
-            big_sub(P, Q);
-            F.s1d = big_round(P, -133);
-        } else {
-            big_sub(Q, P);
-            F.s1d = -big_round(Q, -133);
-        }
-    } else if (t == 32) {
-        F.s2d = big_round(F.w[2], -266);
-    }
-    __syncthreads();
-    if (t != 0) return;
+    if (wid > 1) return;
     unsigned long long n_fin = 0;
 #pragma unroll
     for (int v = 0; v < kThreads / 32; v++) n_fin += F.nw[v];
-    const double s1d = F.s1d, s2d = F.s2d;
-    double var = 0.0, sigma = 0.0;
-    uint32_t rule = 1, E0 = 0;
-    if (n_fin >= 2) {
-        const double N = (double)n_fin;
-        var = __ddiv_rn(__dsub_rn(s2d, __dmul_rn(s1d, __ddiv_rn(s1d, N))), __dsub_rn(N, 1.0));
-        if (var > 0.0 && var <= 1.7976931348623157e308) {
-            sigma = __dsqrt_rn(var);
-            E0 = window_base(var, K);
-            rule = 0;
+    const double N = (double)n_fin;
+    if (wid == 0) {
+        const uint32_t P = warp_carry(gather_limb(F, 0)), Q = warp_carry(gather_limb(F, 1));
+        const uint32_t d = __ballot_sync(kFull, P != Q);
+        double s1d = 0.0;
+        if (d) {
+            const int k = 31 - __clz((int)d);
+            const bool neg = __shfl_sync(kFull, P, k) < __shfl_sync(kFull, Q, k);
+            const double m = warp_round(neg ? warp_sub(Q, P) : warp_sub(P, Q), -133);
+            s1d = neg ? -m : m;
         }
+        if (lane == 0) {
+            F.s1d = s1d;
+            if (n_fin >= 2) F.b = __dmul_rn(s1d, __ddiv_rn(s1d, N));
+        }
+    } else {
+        const double s2d = warp_round(warp_carry(gather_limb(F, 2)), -266);
+        if (lane == 0) F.s2d = s2d;
     }
-    if (rule == 1) {
+    // warps 0 and 1 only; the rest of the CTA has returned
+    asm volatile("bar.sync 1, 64;" ::: "memory");
+    if (lane != 0) return;
+    const double s1d = F.s1d, s2d = F.s2d;
+    double var = 0.0;
+    bool ok = false;
+    if (n_fin >= 2) {
+        var = __ddiv_rn(__dsub_rn(s2d, F.b), __dsub_rn(N, 1.0));
+        ok = var > 0.0 && var <= 1.7976931348623157e308;
+    }
+    if (wid == 1) {
+        out->sigma = ok ? __dsqrt_rn(var) : 0.0;
+        return;
+    }
+    uint32_t rule = 1, E0 = 0;
+    if (ok) {
+        E0 = window_base(var, K);
+        rule = 0;
+    } else {
         // the densest run of 7 exponent bins, ties to the lowest base
         unsigned long long run = 0, best = 0;
         for (int E = 0; E < 7; E++) run += F.h[E];
         best = run;
-        E0 = 0;
         for (int b = 1; b <= 249; b++) {
             run += F.h[b + 6] - F.h[b - 1];
             if (run > best) { best = run; E0 = (uint32_t)b; }
@@ -450,7 +461,6 @@ static __device__ __noinline__ void st_finalize(const StatsBins* G, uint64_t n, 
     out->s1 = s1d;
     out->s2 = s2d;
     out->var = var;
-    out->sigma = sigma;
     out->K = K;
     out->E0 = E0;
     out->rule = rule;
