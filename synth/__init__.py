@@ -42,6 +42,8 @@ import math
 from dataclasses import dataclass
 from typing import List, Sequence, Tuple
 
+import numpy as np
+
 import torch
 
 __all__ = [
@@ -49,7 +51,7 @@ __all__ = [
     "flip_exponents", "lr_update", "Segment", "olmoe_segments",
     "deepseek_layer_segments", "config1", "config2", "config3_base",
     "config3_step", "config4_layer", "config5_base", "config5_step",
-    "config5_rate_factor", "scale_drift_bench",
+    "config5_rate_factor", "scale_drift_bench", "pow2_bf16", "rounding_tie_cases",
 ]
 
 _M64 = (1 << 64) - 1
@@ -393,3 +395,33 @@ def config5_step(bits: torch.Tensor, t: int, seed: int = 5) -> torch.Tensor:
     rate = _segments_rate(olmoe_segments(), bits.numel(), f, True,
                           key_of(seed, 7), bits.device)
     return flip_exponents(bits, rate, key_of(seed, 100 + t))
+
+
+def pow2_bf16(e: int, negative: bool = False) -> int:
+    """BF16 bits of +-2^e for a normal exponent e (-126 <= e <= 127)."""
+    assert -126 <= e <= 127
+    return ((e + 127) << 7) | (0x8000 if negative else 0)
+
+
+def rounding_tie_cases() -> List[Tuple[str, np.ndarray]]:
+    """Small tensors whose exact sum or sum of squares lies exactly halfway
+    between two doubles, or a hair above it, at several scales (so that the
+    deciding bit falls at different 32-bit word boundaries of a fixed-point
+    accumulator).  Powers of two only, so the exact sums are plain to state:
+    s1 = 2^k (1 + 2^-53) is a tie, 2^k (1 + 2^-52 + 2^-53) a tie next to an
+    odd last bit, and s2 = 2^2k (1 + 2^-53) a tie of the squares."""
+    cases = []
+    for k in (-30, -16, 0, 16, 48, 100):
+        for neg in (False, True):
+            p = lambda e: pow2_bf16(e, neg)
+            s = "-" if neg else "+"
+            cases.append((f"s1 tie even k={k}{s}", [p(k), p(k - 53)]))
+            cases.append((f"s1 tie odd k={k}{s}", [p(k), p(k - 52), p(k - 53)]))
+            cases.append((f"s1 above tie k={k}{s}", [p(k), p(k - 53), p(k - 90)]))
+            cases.append((f"s1 tie from halves k={k}{s}", [p(k), p(k - 54), p(k - 54)]))
+        cases.append((f"s2 tie even k={k}", [pow2_bf16(k), pow2_bf16(k - 27), pow2_bf16(k - 27, True)]))
+        cases.append((f"s2 tie odd k={k}", [pow2_bf16(k), pow2_bf16(k - 26), pow2_bf16(k - 27),
+                                            pow2_bf16(k - 27)]))
+        cases.append((f"s2 above tie k={k}", [pow2_bf16(k), pow2_bf16(k - 27), pow2_bf16(k - 27),
+                                              pow2_bf16(k - 60)]))
+    return [(name, np.array(v, dtype=np.uint16)) for name, v in cases]

@@ -159,6 +159,21 @@ def test_stats_sigma_sweep(ez, orc):
             assert_stats_equal(c.stats_of(0), orc.stats(x))
 
 
+def test_stats_rounding_ties(ez, orc):
+    """Sums exactly halfway between two doubles, and a hair above, at
+    several scales: the one-limb-per-lane rounding agrees with the oracle
+    bit for bit (ties to even, sticky bits far below the top)."""
+    binding, codec = ez
+    c = codec.Codec(64, 1)
+    for name, x in synth.rounding_tie_cases():
+        c.stats(dev16(x), x.size)
+        torch.cuda.synchronize()
+        try:
+            assert_stats_equal(c.stats_of(0), orc.stats(x))
+        except AssertionError as e:
+            raise AssertionError((name, e)) from None
+
+
 def test_config2_small(ez, orc):
     x = synth.config2(1 << 22).numpy().view(np.uint16)
     roundtrip(ez, orc, x, 8)

@@ -173,6 +173,28 @@ def test_exact_tie_rounds_up(orc):
         assert orc.window_from_var(math.nextafter(t, math.inf)) == 127 + k
 
 
+def test_sums_round_ties_to_even(orc):
+    """Exact sums halfway between two doubles (and a hair above) round to
+    nearest, ties to even, at several scales: the stated value of each
+    constructed case, and float() of the exact Fraction."""
+    import synth
+    cases = synth.rounding_tie_cases()
+    assert len(cases) == 66
+    for name, x in cases:
+        st = orc.stats(x)
+        s1, s2, _ = exact_sums(x)
+        assert st["s1"] == float(s1), name
+        assert st["s2"] == float(s2), name
+    by = dict(cases)
+    assert orc.stats(by["s1 tie even k=0+"])["s1"] == 1.0
+    assert orc.stats(by["s1 tie odd k=0+"])["s1"] == 1.0 + 2.0 ** -51
+    assert orc.stats(by["s1 above tie k=0+"])["s1"] == 1.0 + 2.0 ** -52
+    assert orc.stats(by["s1 tie odd k=16-"])["s1"] == -(2.0 ** 16) * (1.0 + 2.0 ** -51)
+    assert orc.stats(by["s2 tie even k=0"])["s2"] == 1.0
+    assert orc.stats(by["s2 tie odd k=0"])["s2"] == 1.0 + 2.0 ** -51
+    assert orc.stats(by["s2 above tie k=0"])["s2"] == 1.0 + 2.0 ** -52
+
+
 def test_clamp(orc):
     assert orc.window_from_var(1e-300) == 0
     assert orc.window_from_var(1e300) == 249
