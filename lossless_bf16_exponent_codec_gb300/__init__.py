@@ -4,8 +4,9 @@ behind a C ABI (include/expzip.h).
 
 ``binding`` is the ctypes marshalling of that ABI, ``codec.Codec`` allocates
 the caller-owned buffers of one plan with torch, ``build`` compiles the
-library in-tree, ``breakeven`` is the host-side break-even model.
+library in-tree, ``breakeven`` is the host-side break-even model and ``bsc``
+the benefit-driven choice of the shards to send with exponent reuse.
 """
-from . import binding, breakeven  # noqa: F401
+from . import binding, breakeven, bsc  # noqa: F401
 
-__all__ = ["binding", "breakeven", "codec", "build"]
+__all__ = ["binding", "breakeven", "bsc", "codec", "build"]
