@@ -238,6 +238,18 @@ ez_status ez_encode_code3_noalloc(ez_plan p, const uint16_t* d_x, uint32_t first
                                   const ez_stats_t* d_stats, uint8_t* d_out, uint64_t out_bytes,
                                   uint64_t* d_sizes, uint32_t* d_status, void* stream);
 
+/* The local step of a compressed reduce-scatter (ZipCCL digest 3.2,
+ * zipcclReduceScatter: an all-to-all of compressed chunks, then local
+ * decompression and a sum in higher precision).  For i < n:
+ *   d_acc[i] = (first ? 0 : d_acc[i]) + (float)bf16(d_x[i])
+ * with one IEEE single-precision addition (round to nearest even) per
+ * element, so calls over the W decoded chunks in source order give the bits
+ * of a sequential float32 sum in that order.  d_acc (n floats, read and
+ * written) and d_x (n raw BF16 values) are device pointers, 16-byte aligned,
+ * owned by the caller; n = 0 does nothing.  EZ_ERR_ARG on a null or
+ * misaligned pointer, EZ_ERR_CUDA on a launch error.  Needs no plan. */
+ez_status ez_accumulate_bf16(float* d_acc, const uint16_t* d_x, uint64_t n, int first, void* stream);
+
 /* Static text for a status code. */
 const char* ez_status_str(ez_status s);
 

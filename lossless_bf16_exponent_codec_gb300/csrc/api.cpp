@@ -231,6 +231,13 @@ ez_status ez_decode_reuse(ez_plan p, const uint8_t* d_payload, uint64_t payload_
                                                 ezk::ws_view(p, d_ws), st));
 }
 
+ez_status ez_accumulate_bf16(float* d_acc, const uint16_t* d_x, uint64_t n, int first, void* stream)
+{
+    if (!n) return EZ_OK;
+    if (!d_acc || !al(d_acc, 16) || !d_x || !al(d_x, 16)) return EZ_ERR_ARG;
+    return cuda_status(ezk::launch_accumulate_bf16(d_acc, d_x, n, first, static_cast<cudaStream_t>(stream)));
+}
+
 ez_status ez_gather_decode(ez_plan p, const uint8_t* d_recv, const uint64_t* d_offsets,
                            uint8_t* d_recv_cache, uint16_t* d_full_out, uint32_t* d_status, void* d_ws,
                            uint64_t ws_bytes, void* stream)

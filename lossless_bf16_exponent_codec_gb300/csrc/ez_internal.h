@@ -46,6 +46,7 @@ struct WsView {
 WsView ws_view(const ez_plan_s* p, void* ws);
 
 // Scan segments per chunk of tpc tiles (k_scan.cu).
+cudaError_t launch_accumulate_bf16(float* acc, const uint16_t* x, uint64_t n, int first, cudaStream_t s);
 cudaError_t launch_zero(void* p, uint64_t bytes, cudaStream_t s);
 uint64_t tile_scan_segments(uint64_t tpc);
 

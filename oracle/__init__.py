@@ -62,6 +62,7 @@ def lib():
             "orc_code3_slot_bytes": (u64, [u64, u32]),
             "orc_code3_encode": (i32, [vp, u64, u32, u32, vp, u64, vp]),
             "orc_code3_decode": (u32, [vp, vp, u64, u32, vp]),
+            "orc_code3_decode_chunk": (u32, [vp, u64, u64, u32, u32, vp]),
             "orc_reuse_bytes": (u64, [u64, u32, u64, i32, u64]),
             "orc_reuse_slot_bytes": (u64, [u64, u32, u32, i32]),
             "orc_reuse_encode": (i32, [vp, u64, u32, u32, vp, i32, i32, vp, vp, u64, vp]),
@@ -159,6 +160,16 @@ def code3_decode(buf: np.ndarray, offsets: np.ndarray, n: int, W: int
     out = np.zeros(max(n, 1), dtype=np.uint16)
     st = lib().orc_code3_decode(_p(buf), _p(offsets), n, W, _p(out))
     return out[:n], int(st)
+
+
+def code3_decode_chunk(chunk: np.ndarray, n: int, W: int, c: int) -> Tuple[np.ndarray, int]:
+    """Chunk c alone (a peer's chunk of an all-to-all), all of its bytes given."""
+    chunk = np.ascontiguousarray(chunk, dtype=np.uint8)
+    n_c = shard_count(n, W, c)
+    out = np.zeros(max(n_c, 1), dtype=np.uint16)
+    buf = chunk if chunk.size else np.zeros(1, dtype=np.uint8)
+    st = lib().orc_code3_decode_chunk(_p(buf), chunk.size, n, W, c, _p(out))
+    return out[:n_c], int(st)
 
 
 def compact(slots: np.ndarray, sizes: np.ndarray, slot: int

@@ -327,57 +327,60 @@ int orc_code3_encode(const uint16_t* x, uint64_t n, uint32_t W, uint32_t E0,
     return 0;
 }
 
+/* One chunk c of an n-value tensor split W ways, at p with avail bytes,
+ * decoded to out_c (n_c values).  Returns the status bits of that chunk. */
+uint32_t orc_code3_decode_chunk(const uint8_t* p, uint64_t avail, uint64_t n, uint32_t W,
+                                uint32_t c, uint16_t* out_c)
+{
+    uint32_t status = 0;
+    uint64_t n_c = orc_shard_count(n, W, c);
+    if (avail < 128) return ORC_BAD_SIZE;
+    if (!(p[0] == 'E' && p[1] == 'Z' && p[2] == 'C' && p[3] == '3') || p[4] != 2
+        || p[5] > 249 || get_u64(p + 8) != n_c || get_u32(p + 32) != c
+        || get_u32(p + 36) != W)
+        return ORC_BAD_HEADER;
+    unsigned E0 = p[5];
+    uint64_t n_esc = get_u64(p + 16);
+    if (n_esc > n_c) return ORC_BAD_COUNT;
+    uint64_t bytes = get_u64(p + 24);
+    if (bytes != orc_code3_chunk_bytes(n_c, n_esc) || bytes > avail) return ORC_BAD_SIZE;
+    uint64_t plane = round_up(ceil_div(n_c, 8), 128);
+    const uint8_t* sm = p + 128;
+    const uint8_t* pl = sm + round_up(n_c, 128);
+    const uint8_t* idx = pl + 3 * plane;
+    const uint8_t* esc = idx + round_up(8 * ceil_div(n_c, IDX_SPAN), 128);
+    uint64_t k = 0;
+    for (uint64_t j = 0; j < n_c; j++) {
+        /* the index must hold the escape count of the values before */
+        if (j % IDX_SPAN == 0 && get_u64(idx + 8 * (j / IDX_SPAN)) != k)
+            status |= ORC_BAD_COUNT;
+        unsigned code = 0;
+        for (unsigned b = 0; b < 3; b++)
+            code |= ((pl[b * plane + j / 8] >> (j % 8)) & 1u) << b;
+        unsigned E;
+        if (code) {
+            E = E0 + code - 1;
+        } else if (k < n_esc) {
+            E = esc[k++];
+        } else {
+            status |= ORC_BAD_COUNT;
+            E = 0;
+        }
+        out_c[j] = bf16_merge(sm[j], (uint8_t)E);
+    }
+    if (k != n_esc) status |= ORC_BAD_COUNT;
+    return status;
+}
+
 uint32_t orc_code3_decode(const uint8_t* in, const uint64_t* offsets,
                           uint64_t n, uint32_t W, uint16_t* out)
 {
     uint32_t status = 0;
     uint64_t L = orc_shard_len(n, W);
     for (uint32_t c = 0; c < W; c++) {
-        uint64_t n_c = orc_shard_count(n, W, c);
         if (offsets[c + 1] < offsets[c]) { status |= ORC_BAD_SIZE; continue; }
-        uint64_t avail = offsets[c + 1] - offsets[c];
-        if (avail < 128) { status |= ORC_BAD_SIZE; continue; }
-        const uint8_t* p = in + offsets[c];
-        if (!(p[0] == 'E' && p[1] == 'Z' && p[2] == 'C' && p[3] == '3') || p[4] != 2
-            || p[5] > 249 || get_u64(p + 8) != n_c || get_u32(p + 32) != c
-            || get_u32(p + 36) != W) {
-            status |= ORC_BAD_HEADER;
-            continue;
-        }
-        unsigned E0 = p[5];
-        uint64_t n_esc = get_u64(p + 16);
-        if (n_esc > n_c) { status |= ORC_BAD_COUNT; continue; }
-        uint64_t bytes = get_u64(p + 24);
-        if (bytes != orc_code3_chunk_bytes(n_c, n_esc) || bytes > avail) {
-            status |= ORC_BAD_SIZE;
-            continue;
-        }
-        uint64_t plane = round_up(ceil_div(n_c, 8), 128);
-        const uint8_t* sm = p + 128;
-        const uint8_t* pl = sm + round_up(n_c, 128);
-        const uint8_t* idx = pl + 3 * plane;
-        const uint8_t* esc = idx + round_up(8 * ceil_div(n_c, IDX_SPAN), 128);
-        uint16_t* oc = out + (uint64_t)c * L;
-        uint64_t k = 0;
-        for (uint64_t j = 0; j < n_c; j++) {
-            /* the index must hold the escape count of the values before */
-            if (j % IDX_SPAN == 0 && get_u64(idx + 8 * (j / IDX_SPAN)) != k)
-                status |= ORC_BAD_COUNT;
-            unsigned code = 0;
-            for (unsigned b = 0; b < 3; b++)
-                code |= ((pl[b * plane + j / 8] >> (j % 8)) & 1u) << b;
-            unsigned E;
-            if (code) {
-                E = E0 + code - 1;
-            } else if (k < n_esc) {
-                E = esc[k++];
-            } else {
-                status |= ORC_BAD_COUNT;
-                E = 0;
-            }
-            oc[j] = bf16_merge(sm[j], (uint8_t)E);
-        }
-        if (k != n_esc) status |= ORC_BAD_COUNT;
+        status |= orc_code3_decode_chunk(in + offsets[c], offsets[c + 1] - offsets[c], n, W, c,
+                                         out + (uint64_t)c * L);
     }
     return status;
 }

@@ -60,6 +60,9 @@ uint64_t orc_code3_chunk_bytes(uint64_t n_c, uint64_t n_esc);
 uint64_t orc_code3_slot_bytes(uint64_t n, uint32_t W);
 int  orc_code3_encode(const uint16_t* x, uint64_t n, uint32_t W, uint32_t E0,
                       uint8_t* out, uint64_t slot_bytes, uint64_t* sizes);
+/* one chunk c (ZipCCL digest 3.2: a peer's chunk of an all-to-all) */
+uint32_t orc_code3_decode_chunk(const uint8_t* p, uint64_t avail, uint64_t n, uint32_t W,
+                                uint32_t c, uint16_t* out_c);
 uint32_t orc_code3_decode(const uint8_t* in, const uint64_t* offsets,
                           uint64_t n, uint32_t W, uint16_t* out);
 
