@@ -103,8 +103,16 @@ typedef struct {
     uint32_t W;       /* shards / per-peer chunks, 1..65536                      */
     uint32_t B;       /* reuse block size: power of two, 8..1024 (code3: ignored)*/
     uint32_t codec;   /* ez_codec                                                */
-    uint32_t flags;   /* must be 0                                               */
+    uint32_t flags;   /* 0 or EZ_FLAG_WINDOW_HIST                                */
 } ez_plan_desc;
+
+/* Plan flag: the 3-bit code window of this plan's statistics (ez_stats and
+ * the coded reuse encode's per-shard statistics) is always the densest run
+ * of 7 exponent bins (ties to the lowest base, rule = 1), the window with the
+ * fewest escapes, instead of the one placed by sigma.  sigma and var are
+ * still computed and reported.  It suits tensors far from N(0, sigma^2),
+ * e.g. norm weights near 1.0, where the sigma window misses every value. */
+#define EZ_FLAG_WINDOW_HIST 1u
 
 typedef struct ez_plan_s* ez_plan;   /* immutable after creation; may be shared */
 
@@ -134,7 +142,8 @@ typedef struct {
     double sigma;         /* sqrt(var); 0 when var <= 0                         */
     double K;             /* 16383 / (14 ln 2)                                  */
     uint32_t E0;          /* window base: codes 1..7 cover E0..E0+6             */
-    uint32_t rule;        /* 0 from sigma, 1 histogram fallback                 */
+    uint32_t rule;        /* 0 from sigma, 1 from the histogram (fallback, or   */
+                          /* always with EZ_FLAG_WINDOW_HIST)                   */
     uint64_t n_escape;    /* values outside the window                          */
 } ez_stats_t;
 

@@ -22,6 +22,7 @@ EZ_CODEC_CODE3, EZ_CODEC_REUSE, EZ_CODEC_REUSE_CODE3 = 1, 2, 3
 DSTAT_BAD_HEADER, DSTAT_BAD_SIZE, DSTAT_BAD_COUNT = 1, 2, 4
 DSTAT_TIMEOUT, DSTAT_MISALIGNED, DSTAT_BAD_STATS = 8, 16, 32
 STATS_BYTES = 2120          # sizeof(ez_stats_t)
+EZ_FLAG_WINDOW_HIST = 1     # plan flag: window from the histogram's densest 7-bin run
 NOALLOC_SCRATCH_BYTES = 4 << 20   # EZ_NOALLOC_SCRATCH_BYTES
 
 ENTRY_POINTS = ("ez_plan_create", "ez_plan_destroy", "ez_plan_sizes", "ez_stats",

@@ -13,10 +13,10 @@ from . import binding as B
 
 class Codec:
     def __init__(self, n: int, W: int, B_block: int = 0, codec: int = B.EZ_CODEC_CODE3,
-                 device: str = "cuda"):
+                 device: str = "cuda", flags: int = 0):
         self.n, self.W, self.B, self.codec = n, W, B_block, codec
         self.device = torch.device(device)
-        self.plan = B.ez_plan_create(n, W, B_block, codec)
+        self.plan = B.ez_plan_create(n, W, B_block, codec, flags)
         self.geom = B.ez_plan_sizes(self.plan)
         self.L = self.geom["shard_len"]
         self.slot = self.geom["slot_bytes"]

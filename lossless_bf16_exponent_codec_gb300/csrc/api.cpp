@@ -68,7 +68,7 @@ ez_status ez_plan_create(ez_plan* out, const ez_plan_desc* d)
 {
     if (!out || !d) return EZ_ERR_ARG;
     *out = nullptr;
-    if (d->flags != 0 || d->W == 0 || d->W > 65536 || d->n > kMaxN) return EZ_ERR_ARG;
+    if ((d->flags & ~EZ_FLAG_WINDOW_HIST) || d->W == 0 || d->W > 65536 || d->n > kMaxN) return EZ_ERR_ARG;
     if (d->codec < EZ_CODEC_CODE3 || d->codec > EZ_CODEC_REUSE_CODE3) return EZ_ERR_ARG;
     const bool reuse = d->codec != EZ_CODEC_CODE3;
     if (reuse) {
@@ -78,6 +78,7 @@ ez_status ez_plan_create(ez_plan* out, const ez_plan_desc* d)
     ez_plan_s* p = new (std::nothrow) ez_plan_s();
     if (!p) return EZ_ERR_ARG;
     p->n = d->n;
+    p->hist_window = (d->flags & EZ_FLAG_WINDOW_HIST) ? 1u : 0u;
     p->W = d->W;
     p->B = reuse ? d->B : 0;
     p->codec = d->codec;

@@ -17,6 +17,7 @@ struct ez_plan_s {
     uint64_t off_ctr, off_info, off_shard_stats, off_bins, off_state_a, off_state_b, off_seg, off_escbuf, off_plbuf;
     uint64_t zero_bytes, ws_bytes;
     uint32_t n_bins;
+    uint32_t hist_window;    // EZ_FLAG_WINDOW_HIST: window from the histogram
 };
 
 namespace ezk {

@@ -379,7 +379,7 @@ __device__ __forceinline__ unsigned long long gather_limb(const FinSmem& F, int 
 }
 
 static __device__ __noinline__ void st_finalize(const StatsBins* G, uint64_t n, double K, ez_stats_t* out,
-                                                StatsSmem& S)
+                                                StatsSmem& S, uint32_t hist_window)
 {
     const int t = threadIdx.x, wid = t >> 5, lane = t & 31;
     FinSmem& F = *reinterpret_cast<FinSmem*>(S.hist);
@@ -441,7 +441,7 @@ static __device__ __noinline__ void st_finalize(const StatsBins* G, uint64_t n, 
         return;
     }
     uint32_t rule = 1, E0 = 0;
-    if (ok) {
+    if (ok && !hist_window) {
         E0 = window_base(var, K);
         rule = 0;
     } else {

@@ -25,7 +25,7 @@ static_assert(kStatsTile <= kStatsMaxValues, "a tile's sums fit the 32-bit share
 // The a1 statistics of a whole tensor are the case of one shard.
 __global__ void __launch_bounds__(kThreads, 8)
 k_stats(const uint16_t* __restrict__ x, uint64_t n, uint64_t L, uint32_t first, uint32_t W,
-        uint32_t tps, StatsBins* G, ez_stats_t* out, double K)
+        uint32_t tps, StatsBins* G, ez_stats_t* out, double K, uint32_t hist_window)
 {
     extern __shared__ __align__(16) unsigned char dyn[];
     StatsSmem& S = *reinterpret_cast<StatsSmem*>(dyn);
@@ -51,7 +51,7 @@ k_stats(const uint16_t* __restrict__ x, uint64_t n, uint64_t L, uint32_t first, 
             for (int k = 0; k < 4; k++) st_add8(w[k], e7, hb, S);
         }
         grid_dep_wait();   // the bins were cleared by the kernel before
-        if (st_end(S, G + ci, tps)) st_finalize(G + ci, n_s, K, out + ci, S);
+        if (st_end(S, G + ci, tps)) st_finalize(G + ci, n_s, K, out + ci, S, hist_window);
         return;
     }
 #pragma unroll 1
@@ -64,12 +64,12 @@ k_stats(const uint16_t* __restrict__ x, uint64_t n, uint64_t L, uint32_t first, 
         }
     }
     grid_dep_wait();   // the bins were cleared by the kernel before
-    if (st_end(S, G + ci, tps)) st_finalize(G + ci, n_s, K, out + ci, S);
+    if (st_end(S, G + ci, tps)) st_finalize(G + ci, n_s, K, out + ci, S, hist_window);
 }
 
 static cudaError_t stats_launch(const uint16_t* x, uint64_t n, uint64_t L, uint32_t first,
                                 uint32_t W, uint32_t count, uint64_t per_shard, StatsBins* G,
-                                ez_stats_t* out, double K, cudaStream_t s)
+                                ez_stats_t* out, double K, uint32_t hist_window, cudaStream_t s)
 {
     const uint64_t tps = per_shard ? cdiv(per_shard, kStatsTile) : 1;
     const uint64_t tiles = tps * count;
@@ -78,19 +78,20 @@ static cudaError_t stats_launch(const uint16_t* x, uint64_t n, uint64_t L, uint3
         k_stats, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(StatsSmem));
     if (attr != cudaSuccess) return attr;
     return launch_dependent(k_stats, (unsigned)tiles, kThreads, sizeof(StatsSmem), s, x, n, L, first, W,
-                            (uint32_t)tps, G, out, K);
+                            (uint32_t)tps, G, out, K, hist_window);
 }
 
 cudaError_t launch_stats(const ez_plan_s* p, const uint16_t* x, uint64_t n, ez_stats_t* out,
                          const WsView& w, cudaStream_t s)
 {
-    return stats_launch(x, n, n, 0, 0, 1, n, (StatsBins*)w.bins, out, p->K, s);
+    return stats_launch(x, n, n, 0, 0, 1, n, (StatsBins*)w.bins, out, p->K, p->hist_window, s);
 }
 
 cudaError_t launch_shard_stats(const ez_plan_s* p, const uint16_t* x, uint32_t first, uint32_t count,
                                ez_stats_t* out, const WsView& w, cudaStream_t s)
 {
-    return stats_launch(x, p->n, p->L, first, p->W, count, p->L, (StatsBins*)w.bins, out, p->K, s);
+    return stats_launch(x, p->n, p->L, first, p->W, count, p->L, (StatsBins*)w.bins, out, p->K,
+                        p->hist_window, s);
 }
 
 }  // namespace ezk

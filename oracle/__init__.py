@@ -56,6 +56,7 @@ def lib():
             "orc_shard_len": (u64, [u64, u32]),
             "orc_shard_count": (u64, [u64, u32, u32]),
             "orc_stats_compute": (i32, [vp, u64, vp]),
+            "orc_stats_compute_mode": (i32, [vp, u64, i32, vp]),
             "orc_window_K": (ctypes.c_double, []),
             "orc_window_from_var": (u32, [ctypes.c_double]),
             "orc_code3_chunk_bytes": (u64, [u64, u64]),
@@ -66,6 +67,7 @@ def lib():
             "orc_reuse_bytes": (u64, [u64, u32, u64, i32, u64]),
             "orc_reuse_slot_bytes": (u64, [u64, u32, u32, i32]),
             "orc_reuse_encode": (i32, [vp, u64, u32, u32, vp, i32, i32, vp, vp, u64, vp]),
+            "orc_reuse_encode_mode": (i32, [vp, u64, u32, u32, vp, i32, i32, i32, vp, vp, u64, vp]),
             "orc_reuse_decode": (u32, [vp, u64, u64, u32, u32, vp, vp]),
             "orc_gather_decode_reuse": (u32, [vp, vp, u64, u32, u32, vp, vp]),
         }
@@ -117,10 +119,11 @@ def reuse_slot_bytes(n: int, W: int, B: int, coded: bool = False) -> int:
 
 # ----------------------------------------------------------------- stats
 
-def stats(x) -> dict:
+def stats(x, window_mode: int = 0) -> dict:
+    """window_mode 1: the window from the histogram's densest 7-bin run."""
     x = _u16(x)
     st = _Stats()
-    lib().orc_stats_compute(_p(x), x.size, ctypes.byref(st))
+    lib().orc_stats_compute_mode(_p(x), x.size, int(window_mode), ctypes.byref(st))
     return _stats_dict(st)
 
 
@@ -188,7 +191,7 @@ def compact(slots: np.ndarray, sizes: np.ndarray, slot: int
 # ----------------------------------------------------------------- reuse
 
 def reuse_encode(shard, B: int, shard_index: int, cache: np.ndarray, cold: bool = False,
-                 coded: bool = False) -> Tuple[np.ndarray, Optional[dict]]:
+                 coded: bool = False, window_mode: int = 0) -> Tuple[np.ndarray, Optional[dict]]:
     """Encode one shard; ``cache`` (u8[n_s]) is updated in place."""
     x = _u16(shard)
     assert cache.dtype == np.uint8 and cache.size >= x.size
@@ -197,9 +200,10 @@ def reuse_encode(shard, B: int, shard_index: int, cache: np.ndarray, cold: bool 
     out = np.zeros(cap, dtype=np.uint8)
     size = ctypes.c_uint64(0)
     st = _Stats()
-    rc = lib().orc_reuse_encode(_p(x), x.size, B, shard_index, _p(cache), int(cold),
-                                int(coded), ctypes.byref(st) if coded else None,
-                                _p(out), cap, ctypes.byref(size))
+    rc = lib().orc_reuse_encode_mode(_p(x), x.size, B, shard_index, _p(cache), int(cold),
+                                     int(coded), int(window_mode),
+                                     ctypes.byref(st) if coded else None,
+                                     _p(out), cap, ctypes.byref(size))
     if rc != 0:
         raise ValueError(f"orc_reuse_encode failed ({rc})")
     del nb
@@ -228,7 +232,7 @@ def gather_decode_reuse(recv: np.ndarray, offsets: np.ndarray, n: int, W: int, B
 
 
 def reuse_encode_all(x, W: int, B: int, cache: np.ndarray, cold: bool = False,
-                     coded: bool = False):
+                     coded: bool = False, window_mode: int = 0):
     """Encode all W shards of x (cache u8[n] holds every shard's sender cache).
     -> (slots u8[W*slot], sizes u64[W], slot, [stats per shard or None])"""
     x = _u16(x)
@@ -243,7 +247,7 @@ def reuse_encode_all(x, W: int, B: int, cache: np.ndarray, cold: bool = False,
         b = min(a + L, n) if a < n else n
         c = cache[a:b] if b > a else np.zeros(0, np.uint8)
         cc = np.ascontiguousarray(c)
-        pay, st = reuse_encode(x[a:b], B, r, cc, cold, coded)
+        pay, st = reuse_encode(x[a:b], B, r, cc, cold, coded, window_mode)
         if b > a:
             cache[a:b] = cc
         slots[r * slot:r * slot + pay.size] = pay

@@ -196,6 +196,14 @@ uint32_t orc_window_from_var(double var)
 
 int orc_stats_compute(const uint16_t* x, uint64_t n, orc_stats* st)
 {
+    return orc_stats_compute_mode(x, n, 0, st);
+}
+
+/* mode 0: the window from sigma, the histogram only as the fallback
+ * [ZIP 3.1]; mode 1: the window always from the histogram (the densest
+ * run of 7 exponent bins), sigma still computed and reported. */
+int orc_stats_compute_mode(const uint16_t* x, uint64_t n, int mode, orc_stats* st)
+{
     int64_t S1[256];
     uint64_t S2[256];
     memset(st, 0, sizeof(*st));
@@ -241,8 +249,10 @@ int orc_stats_compute(const uint16_t* x, uint64_t n, orc_stats* st)
         st->var = var;
         if (var > 0 && isfinite(var)) {
             st->sigma = sqrt(var);
-            st->E0 = orc_window_from_var(var);
-            st->rule = 0;
+            if (mode == 0) {
+                st->E0 = orc_window_from_var(var);
+                st->rule = 0;
+            }
         }
     }
     if (st->rule == 1) {
@@ -412,6 +422,15 @@ int orc_reuse_encode(const uint16_t* shard, uint64_t n_s, uint32_t B,
                      int coded, orc_stats* st, uint8_t* out, uint64_t cap,
                      uint64_t* size)
 {
+    return orc_reuse_encode_mode(shard, n_s, B, shard_index, send_cache, cold, coded, 0, st, out,
+                                 cap, size);
+}
+
+int orc_reuse_encode_mode(const uint16_t* shard, uint64_t n_s, uint32_t B,
+                          uint32_t shard_index, uint8_t* send_cache, int cold,
+                          int coded, int window_mode, orc_stats* st, uint8_t* out,
+                          uint64_t cap, uint64_t* size)
+{
     if (B == 0) return -1;
     uint64_t nb = ceil_div(n_s, B);
     uint8_t* changed = (uint8_t*)calloc(nb ? nb : 1, 1);
@@ -436,7 +455,7 @@ int orc_reuse_encode(const uint16_t* shard, uint64_t n_s, uint32_t B,
         /* the code window comes from this shard's sigma [ZIP 3.1] */
         orc_stats local;
         orc_stats* s = st ? st : &local;
-        orc_stats_compute(shard, n_s, s);
+        orc_stats_compute_mode(shard, n_s, window_mode, s);
         E0 = s->E0;
         for (uint64_t j = 0; j < m; j++)
             if (code_of(exps[j], E0) == 0) n_esc++;

@@ -52,6 +52,8 @@ uint64_t orc_shard_len(uint64_t n, uint32_t W);
 uint64_t orc_shard_count(uint64_t n, uint32_t W, uint32_t r);
 
 int  orc_stats_compute(const uint16_t* x, uint64_t n, orc_stats* st);
+/* mode 1: window from the histogram's densest 7-bin run (ties to the lowest) */
+int  orc_stats_compute_mode(const uint16_t* x, uint64_t n, int mode, orc_stats* st);
 double orc_window_K(void);
 uint32_t orc_window_from_var(double var);
 
@@ -74,6 +76,10 @@ int  orc_reuse_encode(const uint16_t* shard, uint64_t n_s, uint32_t B,
                       uint32_t shard_index, uint8_t* send_cache, int cold,
                       int coded, orc_stats* st /* coded: shard stats, may be NULL */,
                       uint8_t* out, uint64_t cap, uint64_t* size);
+int  orc_reuse_encode_mode(const uint16_t* shard, uint64_t n_s, uint32_t B,
+                           uint32_t shard_index, uint8_t* send_cache, int cold,
+                           int coded, int window_mode, orc_stats* st, uint8_t* out,
+                           uint64_t cap, uint64_t* size);
 uint32_t orc_reuse_decode(const uint8_t* payload, uint64_t avail, uint64_t n_s,
                           uint32_t B, uint32_t shard_index,
                           uint8_t* recv_cache, uint16_t* out);

@@ -42,11 +42,13 @@ def test_every_declared_symbol_is_exported(B):
 def test_plan_validation(B):
     E = B.EzError
     for bad in [dict(n=10, W=0), dict(n=1 << 41, W=1), dict(n=10, W=70000),
-                dict(n=10, W=1, codec=9), dict(n=10, W=1, flags=1),
+                dict(n=10, W=1, codec=9), dict(n=10, W=1, flags=2),
+                dict(n=10, W=1, flags=B.EZ_FLAG_WINDOW_HIST | 4),
                 dict(n=10, W=1, codec=B.EZ_CODEC_REUSE, B=0)]:
         with pytest.raises(E) as ei:
             B.ez_plan_create(**bad)
         assert ei.value.status == B.EZ_ERR_ARG
+    B.ez_plan_destroy(B.ez_plan_create(10, 1, 0, B.EZ_CODEC_CODE3, B.EZ_FLAG_WINDOW_HIST))
     for bb in (4, 12, 2048):
         with pytest.raises(E) as ei:
             B.ez_plan_create(1000, 2, bb, B.EZ_CODEC_REUSE)

@@ -174,6 +174,50 @@ def test_stats_rounding_ties(ez, orc):
             raise AssertionError((name, e)) from None
 
 
+def _norm_weights(n, seed):
+    rng = np.random.default_rng(seed)
+    v = (1.0 + rng.normal(0, 0.01, n)).astype(np.float32).view(np.uint32)
+    return ((v + 0x7FFF + ((v >> 16) & 1)) >> 16).astype(np.uint16)
+
+
+@pytest.mark.parametrize("kind", ["wide", "mean", "sub", "bits", "const", "naninf", "0.02"])
+@pytest.mark.parametrize("n", [0, 1, 5000, 300001])
+def test_stats_histogram_window(ez, orc, kind, n):
+    """EZ_FLAG_WINDOW_HIST: the window from the densest 7-bin run, bit for
+    bit as the oracle's window mode 1."""
+    binding, codec = ez
+    x = _dist(kind, n, hash((kind, n, 1)) % 2**31)
+    c = codec.Codec(max(n, 1), 1, flags=binding.EZ_FLAG_WINDOW_HIST)
+    xd = dev16(x) if n else torch.zeros(8, dtype=torch.int16, device="cuda")
+    c.stats(xd, n)
+    torch.cuda.synchronize()
+    assert_stats_equal(c.stats_of(0), orc.stats(x, 1))
+
+
+def test_code3_histogram_window_on_norm_weights(ez, orc):
+    """Norm weights near 1.0: every value escapes the sigma window; with the
+    histogram window none does, the chunks shrink accordingly, and the round
+    trip is exact."""
+    binding, codec = ez
+    n, W = 200_003, 4
+    x = _norm_weights(n, 9)
+    sizes = {}
+    for flags in (0, binding.EZ_FLAG_WINDOW_HIST):
+        c = codec.Codec(n, W, flags=flags)
+        c.stats(dev16(x))
+        c.encode_code3(dev16(x))
+        c.gather_decode()
+        torch.cuda.synchronize()
+        assert c.status_word() == 0
+        assert np.array_equal(host16(c.full)[:n], x)
+        st = c.stats_of(0)
+        assert_stats_equal(st, orc.stats(x, 1 if flags else 0))
+        oslots, osizes, slot = orc.code3_encode(x, W, st["E0"])
+        slots_equal(c.out.cpu().numpy(), c.sizes.cpu().numpy(), oslots, osizes, slot, W)
+        sizes[flags] = int(c.sizes.sum().item())
+    assert sizes[binding.EZ_FLAG_WINDOW_HIST] < 0.75 * sizes[0]
+
+
 def test_config2_small(ez, orc):
     x = synth.config2(1 << 22).numpy().view(np.uint16)
     roundtrip(ez, orc, x, 8)

@@ -204,3 +204,32 @@ def test_corrupt_code3_chunks_are_reported(ez, orc):
     ost = orc.code3_decode(recv, o2, x.size, 2)[1]
     g = gpu_status(recv, o2)
     assert ost and (g & ost)
+
+
+def test_coded_reuse_histogram_window(ez, orc):
+    """The coded reuse encode with EZ_FLAG_WINDOW_HIST: each shard's window
+    from its own histogram; payloads, caches and statistics as the oracle's
+    window mode 1, cold then warm."""
+    binding, codec = ez
+    rng = np.random.default_rng(4)
+    n, W, B = 150_001, 4, 256
+    v = (1.0 + rng.normal(0, 0.01, n // 2)).astype(np.float32).view(np.uint32)
+    norms = ((v + 0x7FFF + ((v >> 16) & 1)) >> 16).astype(np.uint16)
+    x0 = np.concatenate([norms, synth.config2(n - n // 2, seed=4).numpy().view(np.uint16)])
+    x1 = synth.scale_drift_bench(torch.from_numpy(x0.view(np.int16)), 1).numpy().view(np.uint16)
+    c = codec.Codec(n, W, B, binding.EZ_CODEC_REUSE_CODE3, flags=binding.EZ_FLAG_WINDOW_HIST)
+    o_send = np.zeros(n, np.uint8)
+    for it, x in enumerate((x0, x1)):
+        c.encode_reuse(dev16(x), cold=it == 0)
+        torch.cuda.synchronize()
+        assert c.status_word() == 0
+        oslots, osizes, slot, osts = orc.reuse_encode_all(x, W, B, o_send, cold=it == 0, coded=True,
+                                                          window_mode=1)
+        slots_equal(c.out.cpu().numpy(), c.sizes.cpu().numpy(), oslots, osizes, slot, W)
+        assert np.array_equal(c.send_cache.cpu().numpy()[:n], o_send)
+        for r in range(W):
+            assert_stats_equal(c.stats_of(r), osts[r])
+            assert osts[r]["rule"] == 1
+        c.gather_decode()
+        torch.cuda.synchronize()
+        assert c.status_word() == 0 and np.array_equal(host16(c.full)[:n], x)

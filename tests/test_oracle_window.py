@@ -195,6 +195,44 @@ def test_sums_round_ties_to_even(orc):
     assert orc.stats(by["s2 above tie k=0"])["s2"] == 1.0 + 2.0 ** -52
 
 
+def _norm_weights(n, seed):
+    """LayerNorm-like weights: 1.0 + N(0, 0.01), rounded to BF16."""
+    rng = np.random.default_rng(seed)
+    v = (1.0 + rng.normal(0, 0.01, n)).astype(np.float32)
+    b = v.view(np.uint32)
+    return ((b + 0x7FFF + ((b >> 16) & 1)) >> 16).astype(np.uint16)
+
+
+def test_histogram_window_is_the_fewest_escapes(orc):
+    """Window mode 1 takes the base with the fewest values outside its 7
+    bins (brute force over every base on an independent histogram), ties to
+    the lowest base, and leaves the moments as they are."""
+    rng = np.random.default_rng(11)
+    cases = [_norm_weights(5000, 1), rand_bf16(rng, 4000, "gauss"), rand_bf16(rng, 4000, "wide"),
+             rand_bf16(rng, 3000, "bits"), rand_bf16(rng, 2000, "sub"),
+             np.full(100, 0x3F80, np.uint16), np.zeros(0, np.uint16),
+             np.concatenate([np.full(5, 10 << 7), np.full(5, 100 << 7)]).astype(np.uint16)]
+    for x in cases:
+        h = np.bincount((x.astype(np.uint32) >> 7) & 0xFF, minlength=256)
+        esc = [x.size - int(h[b:b + 7].sum()) for b in range(250)]
+        best = int(np.argmin(esc))              # first minimum: the lowest base
+        s0, s1 = orc.stats(x, 0), orc.stats(x, 1)
+        assert s1["E0"] == best and s1["n_escape"] == esc[best] and s1["rule"] == 1
+        assert s1["n_escape"] <= s0["n_escape"]
+        for k in ("s1", "s2", "var", "sigma", "n_finite"):
+            assert s1[k] == s0[k] or (math.isnan(s1[k]) and math.isnan(s0[k])), k
+
+
+def test_sigma_window_misses_norm_weights(orc):
+    """The sigma-only window's weak case: weights near 1.0 with a small
+    spread put the window ~12 binades below 1.0, so every value escapes; the
+    histogram window codes all of them."""
+    x = _norm_weights(20000, 2)
+    s0, s1 = orc.stats(x, 0), orc.stats(x, 1)
+    assert s0["rule"] == 0 and s0["n_escape"] == x.size
+    assert s1["n_escape"] == 0 and s1["E0"] <= 126 <= s1["E0"] + 6
+
+
 def test_clamp(orc):
     assert orc.window_from_var(1e-300) == 0
     assert orc.window_from_var(1e300) == 249
