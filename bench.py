@@ -53,6 +53,7 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     return ap.parse_args()
 
@@ -317,6 +318,7 @@ def run_ours(args, world, rank, local):
     }
     value = world * PASSES * raw / (step_ms_max * 1e-3) / 1e9
     e2e = None if args.no_e2e else run_e2e(args, world, xs, hosts, start, c3, ru, rc, s)
+    extras = None if args.no_extras else run_extras(xs, n, W, flush, s, peak)
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
         "steps": K, "warmup": Wm, "ms_per_step": round(step_ms_max, 4),
@@ -336,7 +338,80 @@ def run_ours(args, world, rank, local):
     }
     if e2e is not None:
         line["e2e"] = e2e
+    if extras is not None:
+        line["extras"] = extras
     return line, (rank == 0)
+
+
+def run_extras(xs, n, W, flush, s, peak, reps=10):
+    """Measured beside the step, not part of it (the step is the six codec
+    passes): the local step of a compressed reduce-scatter at this workload
+    (receiver 0 decodes chunk 0 of W sources and sums them in FP32), the
+    FP32 accumulate kernel alone against HBM, and the statistics op with the
+    histogram window (EZ_FLAG_WINDOW_HIST)."""
+    from lossless_bf16_exponent_codec_gb300 import binding as Bd
+    from lossless_bf16_exponent_codec_gb300 import codec as C
+    enc = C.Codec(n, W)
+    chunks = []
+    for i in range(W):
+        x = xs[(1 + i) % len(xs)]
+        enc.stats(x)
+        enc.encode_code3(x)
+        size0 = int(enc.sizes[0].item())
+        chunks.append(enc.out[:size0].clone())
+    offs = [0]
+    for c in chunks:
+        offs.append(offs[-1] + c.numel())
+    recv = torch.cat(chunks)
+    rx = C.Codec(n, W)
+    n0 = min(rx.L, n)
+    ones = [torch.tensor([0, offs[i + 1] - offs[i]], dtype=torch.int64, device="cuda") for i in range(W)]
+    tmp = torch.zeros(max(rx.L, 8), dtype=torch.int16, device="cuda")
+    acc = torch.zeros(max(n0, 4), dtype=torch.float32, device="cuda")
+    torch.cuda.synchronize()
+
+    def local_step():
+        for i in range(W):
+            Bd.ez_decode_code3(rx.plan, recv[offs[i]:], ones[i], 0, 1, tmp, rx.status, rx.ws,
+                               rx.ws_bytes, None)
+            Bd.ez_accumulate_bf16(acc, tmp, n0, i == 0)
+
+    def accumulate_only():
+        for i in range(W):
+            Bd.ez_accumulate_bf16(acc, tmp, n0, i == 0)
+
+    hist = C.Codec(n, 1, flags=Bd.EZ_FLAG_WINDOW_HIST)
+
+    def timed(fn):
+        tot = 0.0
+        for r in range(reps + 3):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(s)
+            fn()
+            b.record(s)
+            b.synchronize()
+            if r >= 3:
+                tot += a.elapsed_time(b)
+        return tot / reps
+
+    t_local = timed(local_step)
+    ok = rx.status_word() == 0
+    t_acc = timed(accumulate_only)
+    t_hist = timed(lambda: hist.stats(xs[0]))
+    acc_bytes = n0 * (6 + 10 * (W - 1))            # BF16 in, FP32 read (not the first) and written
+    acc_gbs = acc_bytes / (t_acc * 1e-3) / 1e9
+    return {
+        "note": "timed beside the step (not in ms_per_step); L2 flushed before each",
+        "reduce_scatter_local": {
+            "what": f"receiver 0: chunk 0 of {W} sources ({n0} values each), code3 decode + FP32 sum",
+            "ms": round(t_local, 4), "uncompressed_GBs": round(W * n0 * 2 / (t_local * 1e-3) / 1e9, 1),
+            "status_ok": bool(ok), "launches": 2 * W},
+        "accumulate_bf16": {"ms": round(t_acc, 4), "launches": W, "alg_bytes": acc_bytes,
+                            "hbm_GBs": round(acc_gbs, 1), "frac": round(acc_gbs / peak, 3)},
+        "stats_hist_window": {"ms": round(t_hist, 4),
+                              "uncompressed_GBs": round(2 * n / (t_hist * 1e-3) / 1e9, 1)},
+    }
 
 
 def pinned_inputs(args, xs):
