@@ -68,6 +68,9 @@ def lib():
             "orc_reuse_slot_bytes": (u64, [u64, u32, u32, i32]),
             "orc_reuse_encode": (i32, [vp, u64, u32, u32, vp, i32, i32, vp, vp, u64, vp]),
             "orc_reuse_encode_mode": (i32, [vp, u64, u32, u32, vp, i32, i32, i32, vp, vp, u64, vp]),
+            "orc_reuse_encode_hash": (i32, [vp, u64, u32, u32, vp, i32, i32, i32, vp, vp, u64, vp]),
+            "orc_splitmix64_next": (u64, [vp]),
+            "orc_block_hash": (u64, [vp, u64, u32, u64, i32]),
             "orc_reuse_decode": (u32, [vp, u64, u64, u32, u32, vp, vp]),
             "orc_gather_decode_reuse": (u32, [vp, vp, u64, u32, u32, vp, vp]),
         }
@@ -207,6 +210,39 @@ def reuse_encode(shard, B: int, shard_index: int, cache: np.ndarray, cold: bool 
     if rc != 0:
         raise ValueError(f"orc_reuse_encode failed ({rc})")
     del nb
+    return out[:size.value].copy(), (_stats_dict(st) if coded else None)
+
+
+def splitmix64(state: int, count: int) -> list:
+    """The first `count` outputs of the SplitMix64 generator from `state`."""
+    st = ctypes.c_uint64(state)
+    return [int(lib().orc_splitmix64_next(ctypes.byref(st))) for _ in range(count)]
+
+
+def block_hash(shard, B: int, k: int, s: int) -> int:
+    x = _u16(shard)
+    buf = x if x.size else np.zeros(1, dtype=np.uint16)
+    return int(lib().orc_block_hash(_p(buf), x.size, B, k, s))
+
+
+def reuse_encode_hash(shard, B: int, shard_index: int, hash_cache: np.ndarray, cold: bool = False,
+                      coded: bool = False, window_mode: int = 0) -> Tuple[np.ndarray, Optional[dict]]:
+    """Encode one shard with hash-based change detection; ``hash_cache``
+    (u64[2 * ceil(n_s / B)]) is updated in place."""
+    x = _u16(shard)
+    nb = -(-x.size // B) if x.size else 0
+    assert hash_cache.dtype == np.uint64 and hash_cache.size >= 2 * nb
+    cap = reuse_bytes(x.size, B, x.size, coded, x.size if coded else 0)
+    out = np.zeros(cap, dtype=np.uint8)
+    size = ctypes.c_uint64(0)
+    st = _Stats()
+    buf = x if x.size else np.zeros(1, dtype=np.uint16)
+    hc = hash_cache if hash_cache.size else np.zeros(2, dtype=np.uint64)
+    rc = lib().orc_reuse_encode_hash(_p(buf), x.size, B, shard_index, _p(hc), int(cold), int(coded),
+                                     int(window_mode), ctypes.byref(st) if coded else None,
+                                     _p(out), cap, ctypes.byref(size))
+    if rc != 0:
+        raise ValueError(f"orc_reuse_encode_hash failed ({rc})")
     return out[:size.value].copy(), (_stats_dict(st) if coded else None)
 
 

@@ -426,28 +426,22 @@ int orc_reuse_encode(const uint16_t* shard, uint64_t n_s, uint32_t B,
                                  cap, size);
 }
 
-int orc_reuse_encode_mode(const uint16_t* shard, uint64_t n_s, uint32_t B,
-                          uint32_t shard_index, uint8_t* send_cache, int cold,
-                          int coded, int window_mode, orc_stats* st, uint8_t* out,
-                          uint64_t cap, uint64_t* size)
+/* The payload of one shard given its changed-block flags (CIERA exponent
+ * reuse; the coded variant codes the changed exponents with ZipCCL's 3-bit
+ * code, window from the shard's statistics). */
+static int reuse_payload(const uint16_t* shard, uint64_t n_s, uint32_t B, uint32_t shard_index,
+                         const uint8_t* changed, int cold, int coded, int window_mode,
+                         orc_stats* st, uint8_t* out, uint64_t cap, uint64_t* size)
 {
-    if (B == 0) return -1;
     uint64_t nb = ceil_div(n_s, B);
-    uint8_t* changed = (uint8_t*)calloc(nb ? nb : 1, 1);
     uint8_t* exps = (uint8_t*)malloc(n_s ? n_s : 1);
-    if (!changed || !exps) { free(changed); free(exps); return -3; }
-    /* changed_k = cold or some exponent differs from the sender's cache */
+    if (!exps) return -3;
     uint64_t n_changed = 0, m = 0;
     for (uint64_t k = 0; k < nb; k++) {
+        if (!changed[k]) continue;
         uint64_t a = k * B, b = (k + 1) * B < n_s ? (k + 1) * B : n_s;
-        int ch = cold;
-        for (uint64_t i = a; i < b; i++)
-            if (bf16_exp(shard[i]) != send_cache[i]) ch = 1;
-        changed[k] = (uint8_t)ch;
-        if (ch) {
-            n_changed++;
-            for (uint64_t i = a; i < b; i++) exps[m++] = bf16_exp(shard[i]);
-        }
+        n_changed++;
+        for (uint64_t i = a; i < b; i++) exps[m++] = bf16_exp(shard[i]);
     }
     uint32_t E0 = 0;
     uint64_t n_esc = 0;
@@ -461,7 +455,7 @@ int orc_reuse_encode_mode(const uint16_t* shard, uint64_t n_s, uint32_t B,
             if (code_of(exps[j], E0) == 0) n_esc++;
     }
     uint64_t total = orc_reuse_bytes(n_s, B, m, coded, n_esc);
-    if (total > cap) { free(changed); free(exps); return -2; }
+    if (total > cap) { free(exps); return -2; }
     memset(out, 0, total);
     out[0] = 'E'; out[1] = 'Z'; out[2] = 'R'; out[3] = 'U';
     out[4] = 2;
@@ -510,16 +504,107 @@ int orc_reuse_encode_mode(const uint16_t* shard, uint64_t n_s, uint32_t B,
             if (code == 0) out[off_e + k++] = exps[j];
         }
     }
-    /* the sender's cache now holds this iteration's exponents */
-    for (uint64_t k = 0; k < nb; k++) {
-        if (!changed[k]) continue;
-        uint64_t a = k * B, b = (k + 1) * B < n_s ? (k + 1) * B : n_s;
-        for (uint64_t i = a; i < b; i++) send_cache[i] = bf16_exp(shard[i]);
-    }
     *size = total;
-    free(changed);
     free(exps);
     return 0;
+}
+
+int orc_reuse_encode_mode(const uint16_t* shard, uint64_t n_s, uint32_t B,
+                          uint32_t shard_index, uint8_t* send_cache, int cold,
+                          int coded, int window_mode, orc_stats* st, uint8_t* out,
+                          uint64_t cap, uint64_t* size)
+{
+    if (B == 0) return -1;
+    uint64_t nb = ceil_div(n_s, B);
+    uint8_t* changed = (uint8_t*)calloc(nb ? nb : 1, 1);
+    if (!changed) return -3;
+    /* changed_k = cold or some exponent differs from the sender's cache */
+    for (uint64_t k = 0; k < nb; k++) {
+        uint64_t a = k * B, b = (k + 1) * B < n_s ? (k + 1) * B : n_s;
+        int ch = cold;
+        for (uint64_t i = a; i < b; i++)
+            if (bf16_exp(shard[i]) != send_cache[i]) ch = 1;
+        changed[k] = (uint8_t)ch;
+    }
+    int rc = reuse_payload(shard, n_s, B, shard_index, changed, cold, coded, window_mode, st, out,
+                           cap, size);
+    if (rc == 0) {
+        /* the sender's cache now holds this iteration's exponents */
+        for (uint64_t k = 0; k < nb; k++) {
+            if (!changed[k]) continue;
+            uint64_t a = k * B, b = (k + 1) * B < n_s ? (k + 1) * B : n_s;
+            for (uint64_t i = a; i < b; i++) send_cache[i] = bf16_exp(shard[i]);
+        }
+    }
+    free(changed);
+    return rc;
+}
+
+/* ---- hash-based change detection (CIERA: HashCache, two independent
+ * 64-bit SplitMix64 hashes per block) ----------------------------------- */
+
+/* The SplitMix64 generator (Steele, Lea and Flood): the state advances by
+ * the golden gamma and each output is the state passed through the mixing
+ * function below. */
+#define SM64_GAMMA 0x9E3779B97F4A7C15ull
+static uint64_t sm64_mix(uint64_t z)
+{
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    return z ^ (z >> 31);
+}
+
+uint64_t orc_splitmix64_next(uint64_t* state)
+{
+    *state += SM64_GAMMA;
+    return sm64_mix(*state);
+}
+
+/* Hash s (0 or 1) of block k: word i is the 8 exponent bytes of values
+ * kB + 8i .. kB + 8i + 7 (little-endian, 0 for values past the shard);
+ * term_i = mix(word_i + seed_s + (i + 1) * gamma), one SplitMix64 output per
+ * word; the hash is mix(sum of the B/8 terms mod 2^64).  A change in any
+ * single word changes its term (mix is a bijection) and so the sum. */
+static const uint64_t kHashSeed[2] = {0ull, 0x5851F42D4C957F2Dull};
+
+uint64_t orc_block_hash(const uint16_t* shard, uint64_t n_s, uint32_t B, uint64_t k, int s)
+{
+    uint64_t sum = 0;
+    for (uint32_t i = 0; i < B / 8; i++) {
+        uint64_t w = 0;
+        for (unsigned j = 0; j < 8; j++) {
+            uint64_t v = k * B + 8ull * i + j;
+            if (v < n_s) w |= (uint64_t)bf16_exp(shard[v]) << (8 * j);
+        }
+        sum += sm64_mix(w + kHashSeed[s] + (uint64_t)(i + 1) * SM64_GAMMA);
+    }
+    return sm64_mix(sum);
+}
+
+int orc_reuse_encode_hash(const uint16_t* shard, uint64_t n_s, uint32_t B,
+                          uint32_t shard_index, uint64_t* hash_cache, int cold,
+                          int coded, int window_mode, orc_stats* st, uint8_t* out,
+                          uint64_t cap, uint64_t* size)
+{
+    if (B < 8 || (B & 7)) return -1;
+    uint64_t nb = ceil_div(n_s, B);
+    uint8_t* changed = (uint8_t*)calloc(nb ? nb : 1, 1);
+    uint64_t* h = (uint64_t*)malloc(2 * (nb ? nb : 1) * sizeof(uint64_t));
+    if (!changed || !h) { free(changed); free(h); return -3; }
+    /* changed_k = cold or the block's hash pair differs from HashCache[k] */
+    for (uint64_t k = 0; k < nb; k++) {
+        h[2 * k] = orc_block_hash(shard, n_s, B, k, 0);
+        h[2 * k + 1] = orc_block_hash(shard, n_s, B, k, 1);
+        changed[k] = (uint8_t)(cold || h[2 * k] != hash_cache[2 * k] || h[2 * k + 1] != hash_cache[2 * k + 1]);
+    }
+    int rc = reuse_payload(shard, n_s, B, shard_index, changed, cold, coded, window_mode, st, out,
+                           cap, size);
+    if (rc == 0)
+        for (uint64_t k = 0; k < nb; k++)
+            if (changed[k]) { hash_cache[2 * k] = h[2 * k]; hash_cache[2 * k + 1] = h[2 * k + 1]; }
+    free(changed);
+    free(h);
+    return rc;
 }
 
 uint32_t orc_reuse_decode(const uint8_t* p, uint64_t avail, uint64_t n_s,

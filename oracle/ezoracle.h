@@ -80,6 +80,14 @@ int  orc_reuse_encode_mode(const uint16_t* shard, uint64_t n_s, uint32_t B,
                            uint32_t shard_index, uint8_t* send_cache, int cold,
                            int coded, int window_mode, orc_stats* st, uint8_t* out,
                            uint64_t cap, uint64_t* size);
+/* CIERA's hash-based change detection: two 64-bit SplitMix64 hashes per
+ * block in hash_cache (u64[2 * ceil(n_s / B)]); same payload as above. */
+uint64_t orc_splitmix64_next(uint64_t* state);
+uint64_t orc_block_hash(const uint16_t* shard, uint64_t n_s, uint32_t B, uint64_t k, int s);
+int  orc_reuse_encode_hash(const uint16_t* shard, uint64_t n_s, uint32_t B,
+                           uint32_t shard_index, uint64_t* hash_cache, int cold,
+                           int coded, int window_mode, orc_stats* st, uint8_t* out,
+                           uint64_t cap, uint64_t* size);
 uint32_t orc_reuse_decode(const uint8_t* payload, uint64_t avail, uint64_t n_s,
                           uint32_t B, uint32_t shard_index,
                           uint8_t* recv_cache, uint16_t* out);
