@@ -395,6 +395,24 @@ def run_extras(xs, n, W, flush, s, peak, reps=10):
                 tot += a.elapsed_time(b)
         return tot / reps
 
+    # raw reuse encode with the hash cache against the exponent cache, both
+    # alternating between two drift iterations so that every encode sees the
+    # benchmark's change rate
+    from lossless_bf16_exponent_codec_gb300 import binding as Bd2
+    encs = {"exponent_cache": C.Codec(n, W, B_BLOCK, Bd2.EZ_CODEC_REUSE),
+            "hash_cache": C.Codec(n, W, B_BLOCK, Bd2.EZ_CODEC_REUSE, flags=Bd2.EZ_FLAG_HASH_CACHE)}
+    x1, x2 = xs[1 % len(xs)], xs[2 % len(xs)]
+    t_enc = {}
+    for name, ce in encs.items():
+        ce.encode_reuse(xs[0], cold=True)
+        flip = [0]
+
+        def enc(ce=ce):
+            flip[0] ^= 1
+            ce.encode_reuse(x1 if flip[0] else x2)
+        t_enc[name] = timed(enc)
+        if ce.status_word():
+            raise RuntimeError(f"{name} encode status {ce.status_word():#x}")
     t_local = timed(local_step)
     ok = rx.status_word() == 0
     t_acc = timed(accumulate_only)
@@ -411,6 +429,9 @@ def run_extras(xs, n, W, flush, s, peak, reps=10):
                             "hbm_GBs": round(acc_gbs, 1), "frac": round(acc_gbs / peak, 3)},
         "stats_hist_window": {"ms": round(t_hist, 4),
                               "uncompressed_GBs": round(2 * n / (t_hist * 1e-3) / 1e9, 1)},
+        "reuse_encode_change_detection": {
+            k: {"ms": round(v, 4), "uncompressed_GBs": round(2 * n / (v * 1e-3) / 1e9, 1),
+                "sender_cache_bytes": encs[k].geom["send_cache_bytes"]} for k, v in t_enc.items()},
     }
 
 

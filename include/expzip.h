@@ -114,6 +114,19 @@ typedef struct {
  * e.g. norm weights near 1.0, where the sigma window misses every value. */
 #define EZ_FLAG_WINDOW_HIST 1u
 
+/* Plan flag (reuse codecs, B >= 32; EZ_ERR_UNSUPPORTED for smaller blocks,
+ * EZ_ERR_ARG with the code3 codec): CIERA's hash-based change detection.  The
+ * sender cache holds two 64-bit hashes per block (HashCache, 16 bytes per
+ * block instead of one byte per value): a block is sent when it is cold or
+ * its hash pair differs, and the pair is then replaced.  Hash s of a block:
+ * word i = the 8 exponent bytes of values 8i..8i+7 of the block (little-
+ * endian, 0 past the shard), term_i = mix(word_i + seed_s + (i+1) * gamma),
+ * hash = mix(sum of the B/8 terms mod 2^64), with mix the SplitMix64 output
+ * function, gamma = 0x9E3779B97F4A7C15, seeds 0 and 0x5851F42D4C957F2D.  The
+ * payload is the one the exponent compare gives unless a hash pair collides
+ * (about 2^-128 per block); receivers are unchanged. */
+#define EZ_FLAG_HASH_CACHE 2u
+
 typedef struct ez_plan_s* ez_plan;   /* immutable after creation; may be shared */
 
 typedef struct {
@@ -122,6 +135,8 @@ typedef struct {
     uint64_t workspace_bytes;  /* device scratch every call of this plan needs    */
     uint64_t cache_bytes;      /* exponent-cache bytes of the full tensor (reuse) */
     uint64_t tile_values;      /* values per CUDA tile (8192)                     */
+    uint64_t send_cache_bytes; /* sender cache of all W shards: cache_bytes, or   */
+                               /* W * 16 * ceil(L / B) with EZ_FLAG_HASH_CACHE    */
 } ez_sizes;
 
 /* Statistics of one tensor (ZipCCL digest 3.1: "one call of torch.std gives
@@ -192,8 +207,10 @@ ez_status ez_decode_code3(ez_plan p, const uint8_t* d_in, const uint64_t* d_offs
  * d_out + i*slot_bytes, its size to d_sizes[i].  For EZ_CODEC_REUSE_CODE3 the
  * shard's statistics are computed in the same pass and, if d_stats is not
  * NULL, written to d_stats[i]; the changed exponents are 3-bit coded with
- * that shard's window.  CIERA exponent-reuse paragraphs, Algorithm 1 sender
- * side (split, detect, pack; ANS replaced by the 3-bit code). */
+ * that shard's window.  With EZ_FLAG_HASH_CACHE, d_send_cache holds each
+ * shard's block hash pairs instead (shard first+i at byte i*16*ceil(L/B)).
+ * CIERA exponent-reuse paragraphs, Algorithm 1 sender side (split, detect,
+ * pack; ANS replaced by the 3-bit code). */
 ez_status ez_encode_reuse(ez_plan p, const uint16_t* d_x, uint32_t first, uint32_t count,
                           uint8_t* d_send_cache, int cold, uint8_t* d_out, uint64_t out_bytes,
                           uint64_t* d_sizes, ez_stats_t* d_stats, uint32_t* d_status,

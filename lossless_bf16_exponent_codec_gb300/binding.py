@@ -23,6 +23,7 @@ DSTAT_BAD_HEADER, DSTAT_BAD_SIZE, DSTAT_BAD_COUNT = 1, 2, 4
 DSTAT_TIMEOUT, DSTAT_MISALIGNED, DSTAT_BAD_STATS = 8, 16, 32
 STATS_BYTES = 2120          # sizeof(ez_stats_t)
 EZ_FLAG_WINDOW_HIST = 1     # plan flag: window from the histogram's densest 7-bin run
+EZ_FLAG_HASH_CACHE = 2      # plan flag: sender cache of block hash pairs (reuse, B >= 32)
 NOALLOC_SCRATCH_BYTES = 4 << 20   # EZ_NOALLOC_SCRATCH_BYTES
 
 ENTRY_POINTS = ("ez_plan_create", "ez_plan_destroy", "ez_plan_sizes", "ez_stats",
@@ -45,7 +46,7 @@ class PlanDesc(ctypes.Structure):
 class Sizes(ctypes.Structure):
     _fields_ = [("shard_len", ctypes.c_uint64), ("slot_bytes", ctypes.c_uint64),
                 ("workspace_bytes", ctypes.c_uint64), ("cache_bytes", ctypes.c_uint64),
-                ("tile_values", ctypes.c_uint64)]
+                ("tile_values", ctypes.c_uint64), ("send_cache_bytes", ctypes.c_uint64)]
 
 
 _lib = None

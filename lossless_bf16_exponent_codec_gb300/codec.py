@@ -30,7 +30,10 @@ class Codec:
         self.slot_offsets = (torch.arange(W + 1, dtype=torch.int64) * self.slot).to(dev)
         self.full = torch.zeros(max(n, 1), dtype=torch.int16, device=dev)
         if codec != B.EZ_CODEC_CODE3:
-            self.send_cache = torch.zeros(max(n, 8), dtype=torch.uint8, device=dev)
+            # exponent cache (1 byte per value) or, with EZ_FLAG_HASH_CACHE,
+            # two u64 hashes per block
+            self.send_cache = torch.zeros(max(self.geom["send_cache_bytes"], 16), dtype=torch.uint8,
+                                          device=dev)
             self.recv_cache = torch.zeros(max(n, 8), dtype=torch.uint8, device=dev)
 
     def __del__(self):

@@ -52,6 +52,7 @@ WsView ws_view(const ez_plan_s* p, void* ws)
     v.bins = b + p->off_bins;
     v.escbuf = p->off_escbuf ? b + p->off_escbuf : nullptr;
     v.plbuf = p->off_plbuf ? b + p->off_plbuf : nullptr;
+    v.hbm = p->hash_cache ? reinterpret_cast<uint32_t*>(b + p->off_hbm) : nullptr;
     const uint64_t segs = tile_scan_segments(p->tpc) * p->W;
     v.seg_a = reinterpret_cast<unsigned long long*>(b + p->off_seg);
     v.seg_b = v.seg_a + segs;
@@ -68,17 +69,23 @@ ez_status ez_plan_create(ez_plan* out, const ez_plan_desc* d)
 {
     if (!out || !d) return EZ_ERR_ARG;
     *out = nullptr;
-    if ((d->flags & ~EZ_FLAG_WINDOW_HIST) || d->W == 0 || d->W > 65536 || d->n > kMaxN) return EZ_ERR_ARG;
+    if ((d->flags & ~(EZ_FLAG_WINDOW_HIST | EZ_FLAG_HASH_CACHE)) || d->W == 0 || d->W > 65536 ||
+        d->n > kMaxN)
+        return EZ_ERR_ARG;
     if (d->codec < EZ_CODEC_CODE3 || d->codec > EZ_CODEC_REUSE_CODE3) return EZ_ERR_ARG;
     const bool reuse = d->codec != EZ_CODEC_CODE3;
+    const bool hash = (d->flags & EZ_FLAG_HASH_CACHE) != 0;
+    if (hash && !reuse) return EZ_ERR_ARG;
     if (reuse) {
         if (d->B == 0) return EZ_ERR_ARG;
         if (d->B < 8 || d->B > 1024 || (d->B & (d->B - 1))) return EZ_ERR_UNSUPPORTED;
+        if (hash && d->B < 32) return EZ_ERR_UNSUPPORTED;
     }
     ez_plan_s* p = new (std::nothrow) ez_plan_s();
     if (!p) return EZ_ERR_ARG;
     p->n = d->n;
     p->hist_window = (d->flags & EZ_FLAG_WINDOW_HIST) ? 1u : 0u;
+    p->hash_cache = hash ? 1u : 0u;
     p->W = d->W;
     p->B = reuse ? d->B : 0;
     p->codec = d->codec;
@@ -115,6 +122,12 @@ ez_status ez_plan_create(ez_plan* out, const ez_plan_desc* d)
     off = rup(off + (coded ? W * tpc * 8 : 0), 256);
     p->off_seg = off;                                     // two arrays of scan-segment states
     off = rup(off + 2 * W * ezk::tile_scan_segments(tpc) * 8, 256);
+    // hash mode: each shard's changed-block bits from the hash step
+    const uint64_t blocks = reuse ? cdiv(L, d->B) : 0;
+    p->hwords = hash ? (uint32_t)cdiv(blocks, 32) : 0u;
+    p->hstride = hash ? 16 * blocks : L;
+    p->off_hbm = off;
+    off = rup(off + W * p->hwords * 4ull, 256);
     p->zero_bytes = off;
     // coded reuse: each tile's escapes staged at its own offset, its planes
     // in 3 KB per tile
@@ -141,6 +154,7 @@ ez_status ez_plan_sizes(ez_plan p, ez_sizes* out)
     out->workspace_bytes = p->ws_bytes;
     out->cache_bytes = is_reuse(p) ? p->n : 0;
     out->tile_values = kTileValues;
+    out->send_cache_bytes = !is_reuse(p) ? 0 : (p->hash_cache ? p->W * p->hstride : p->n);
     return EZ_OK;
 }
 

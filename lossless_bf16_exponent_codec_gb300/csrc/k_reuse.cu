@@ -51,6 +51,13 @@ struct RuEnc {
     uint8_t* plbuf;
     uint8_t* escbuf;
     unsigned long long* state_b;
+    // hash-based change detection: `cache` holds 2 u64 hashes per block,
+    // shard first+i at byte i * hstride; the hash step leaves each shard's
+    // changed-block bits in hbm (hwords 32-bit words per shard)
+    int hash;
+    uint32_t* hbm;
+    uint32_t hwords;
+    uint64_t hstride;
 };
 
 
@@ -240,6 +247,91 @@ __device__ __forceinline__ uint32_t codes_of_bytes(const uint32_t* lut, uint32_t
     return acc;
 }
 
+// Exponent bytes of cnt (1..32) consecutive BF16 values at p, 32 bytes as
+// two 16-byte words (0 past cnt).
+__device__ __forceinline__ void ew_from_x(const uint16_t* p, uint32_t cnt, uint4* ew)
+{
+    uint32_t xw[16];
+    if (cnt == 32) {
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+            const uint4 w = ld_v4_nc(p + 8 * q);
+            xw[4 * q] = w.x; xw[4 * q + 1] = w.y; xw[4 * q + 2] = w.z; xw[4 * q + 3] = w.w;
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 16; i++) {
+            const uint32_t lo = 2u * i < cnt ? (uint32_t)p[2 * i] : 0u;
+            const uint32_t hi = 2u * i + 1 < cnt ? (uint32_t)p[2 * i + 1] : 0u;
+            xw[i] = lo | hi << 16;
+        }
+    }
+    ew[0] = make_uint4(exp4_of(xw[0], xw[1]), exp4_of(xw[2], xw[3]), exp4_of(xw[4], xw[5]),
+                       exp4_of(xw[6], xw[7]));
+    ew[1] = make_uint4(exp4_of(xw[8], xw[9]), exp4_of(xw[10], xw[11]), exp4_of(xw[12], xw[13]),
+                       exp4_of(xw[14], xw[15]));
+}
+
+// ---- hash-based change detection (CIERA: HashCache, two independent 64-bit
+// SplitMix64 hashes per block) ---------------------------------------------
+// Word i of a block is its 8 exponent bytes (little-endian; 0 past the
+// shard); term_i = mix(word + seed + (i + 1) * gamma) is one SplitMix64
+// output; the block's hash is mix(sum of its B/8 terms).  The sum makes the
+// hash a plain reduction over the block's threads.
+constexpr unsigned long long kGamma = 0x9E3779B97F4A7C15ull;
+constexpr unsigned long long kHashSeed1 = 0x5851F42D4C957F2Dull;
+__device__ __forceinline__ unsigned long long sm64_mix(unsigned long long z)
+{
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    return z ^ (z >> 31);
+}
+
+// One CTA per 8192-value tile, B >= 32: thread t hashes the four words of
+// values [32t, 32t + 32) (they lie in one block), the B/32 threads of a block
+// add their partial sums with shuffles, and the block's first thread compares
+// the pair with the cache, writes it back when it differs (or cold) and sets
+// the block's bit in the shard's bit array for the split.
+__global__ void __launch_bounds__(kThreads) k_reuse_hash(RuEnc a)
+{
+    const int t = threadIdx.x, lane = t & 31;
+    const TilePos tp = tile_pos(blockIdx.x, a.count, a.tpc);
+    const uint32_t ci = tp.ci, lt = tp.lt;
+    const uint64_t n_s = shard_values(a.n, a.L, a.first + ci);
+    const uint64_t v0 = (uint64_t)lt * kTile;
+    const uint32_t nv = v0 < n_s ? (uint32_t)umin64(kTile, n_s - v0) : 0u;
+    const uint32_t B = a.B, log2B = a.log2B;
+    const uint32_t tv = 32u * (uint32_t)t;
+    const uint32_t cnt_v = tv < nv ? min(32u, nv - tv) : 0u;
+    uint4 ew[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+    if (cnt_v) ew_from_x(a.x + (uint64_t)ci * a.L + v0 + tv, cnt_v, ew);
+    const unsigned long long w[4] = {
+        (unsigned long long)ew[0].y << 32 | ew[0].x, (unsigned long long)ew[0].w << 32 | ew[0].z,
+        (unsigned long long)ew[1].y << 32 | ew[1].x, (unsigned long long)ew[1].w << 32 | ew[1].z};
+    const unsigned long long i0 = (tv & (B - 1u)) >> 3;   // word index of w[0] in the block
+    unsigned long long s0 = 0, s1 = 0;
+#pragma unroll
+    for (int q = 0; q < 4; q++) {
+        const unsigned long long base = w[q] + (i0 + q + 1) * kGamma;
+        s0 += sm64_mix(base);
+        s1 += sm64_mix(base + kHashSeed1);
+    }
+    const uint32_t per = B >> 5;                          // threads per block, 1..32
+    for (uint32_t o = per >> 1; o; o >>= 1) {
+        s0 += __shfl_xor_sync(kFull, s0, o);
+        s1 += __shfl_xor_sync(kFull, s1, o);
+    }
+    if ((lane & (per - 1)) != 0 || v0 + tv >= n_s) return;   // the block's first thread, if the block exists
+    const uint64_t k = (v0 + tv) >> log2B;
+    unsigned long long* hc = reinterpret_cast<unsigned long long*>(a.cache + (uint64_t)ci * a.hstride) + 2 * k;
+    const unsigned long long h0 = sm64_mix(s0), h1 = sm64_mix(s1);
+    if (a.cold || hc[0] != h0 || hc[1] != h1) {
+        hc[0] = h0;
+        hc[1] = h1;
+        atomicOr(&a.hbm[(uint64_t)ci * a.hwords + (k >> 5)], 1u << (k & 31));
+    }
+}
+
 // Step A of both reuse encoders, one CTA per 8192-value tile with no
 // inter-tile dependence: compare the exponents with the sender cache, store
 // the sign+mantissa bytes, build the tile's slice of the changed-block bitmap
@@ -279,7 +371,7 @@ __global__ void __launch_bounds__(kThreads, kCoded ? 4 : 6) k_reuse_split(RuEnc 
     for (int g = 0; g < kGroups; g++) {
         const uint32_t v = 8u * (uint32_t)(g * kThreads + t);
         w[g] = ld_group16(xt, v, nv);
-        cv[g] = (v < nv && !a.cold) ? ld_group8(ct, v, nv) : 0ull;
+        cv[g] = (v < nv && !a.cold && !a.hash) ? ld_group8(ct, v, nv) : 0ull;
     }
     // coded: the split may start while the shard statistics finish; nothing
     // above depends on them, everything below may
@@ -301,7 +393,13 @@ __global__ void __launch_bounds__(kThreads, kCoded ? 4 : 6) k_reuse_split(RuEnc 
         const unsigned long long e = ((unsigned long long)exp4_of(w[g].z, w[g].w) << 32 |
                                       exp4_of(w[g].x, w[g].y)) & bmask;
         e8[g] = e;
-        const bool ch = vm && (a.cold || ((e ^ cv[g]) & bmask) != 0ull);
+        bool ch;
+        if (a.hash) {   // the hash step's decision for the group's block
+            const uint64_t kk = (v0 + v) >> log2B;
+            ch = vm && ((a.hbm[(uint64_t)ci * a.hwords + (kk >> 5)] >> (kk & 31)) & 1u);
+        } else {
+            ch = vm && (a.cold || ((e ^ cv[g]) & bmask) != 0ull);
+        }
         const uint32_t bal = __ballot_sync(kFull, ch);
         if (lane == 0) s_gl[g * (kThreads / 32) + wid] = bal;
         if (vm) {
@@ -334,7 +432,7 @@ __global__ void __launch_bounds__(kThreads, kCoded ? 4 : 6) k_reuse_split(RuEnc 
 #pragma unroll
     for (int g = 0; g < kGroups; g++) {
         const uint32_t v = 8u * (uint32_t)(g * kThreads + t);
-        if (v < nv && block_changed(s_bm, v >> log2B)) st_group8(ct, v, nv, e8[g]);
+        if (!a.hash && v < nv && block_changed(s_bm, v >> log2B)) st_group8(ct, v, nv, e8[g]);
     }
     if (lt == fin_tile) {
         if (t < 16 && rup(bm_bytes, 16) > bm_bytes + t) o[64 + bm_bytes + t] = 0;
@@ -503,9 +601,12 @@ __global__ void __launch_bounds__(kThreads, 6) k_reuse_place32(RuEnc a)
     const uint8_t* ct = a.cache + (uint64_t)ci * a.L + v0 + tv;
     uint8_t* o = a.out + (uint64_t)ci * a.slot;
     const unsigned long long* sc = a.state + (uint64_t)ci * a.tpc;
-    // the thread's cache bytes, loaded with the bitmap and the prefix
+    // the thread's exponents, loaded with the bitmap and the prefix: from the
+    // cache, or (hash-based detection: the cache holds hashes) from x
     uint4 ew[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
-    if (cnt_v == 32) {
+    if (a.hash) {
+        if (cnt_v) ew_from_x(a.x + (uint64_t)ci * a.L + v0 + tv, cnt_v, ew);
+    } else if (cnt_v == 32) {
         ew[0] = ld_v4_nc(ct);
         ew[1] = ld_v4_nc(ct + 16);
     } else if (cnt_v) {
@@ -1235,8 +1336,18 @@ cudaError_t launch_reuse_encode(const ez_plan_s* p, const uint16_t* x, uint32_t 
     a.abort = w.counters + 7;
     a.info = w.info;
     a.stats = st ? st : w.shard_stats;
+    a.hash = p->hash_cache ? 1 : 0;
+    a.hbm = w.hbm;
+    a.hwords = p->hwords;
+    a.hstride = p->hstride;
     const unsigned tiles = (unsigned)((uint64_t)count * p->tpc);
     cudaError_t e;
+    if (a.hash) {
+        // the blocks' hash pairs against the cache: changed-block bits for the split
+        k_reuse_hash<<<tiles, kThreads, 0, s>>>(a);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
     if (coded) {
         // the shards' windows (a pass over the values of their own)
         e = launch_shard_stats(p, x, first, count, a.stats, w, s);
