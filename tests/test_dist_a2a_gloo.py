@@ -31,41 +31,45 @@ def worker(rank: int, world: int, port: int, q):
     os.environ["MASTER_PORT"] = str(port)
     try:
         dist.init_process_group("gloo", rank=rank, world_size=world)
-        import oracle
-        import synth
-        from lossless_bf16_exponent_codec_gb300 import dist as zd
-        n = 50_001
-        xs = [synth.config2(n, seed=10 + s).numpy().view(np.uint16) for s in range(world)]
-        L = oracle.shard_len(n, world)
-        n_me = oracle.shard_count(n, world, rank)
-        x = xs[rank]
-        slots, sizes, slot = oracle.code3_encode(x, world, oracle.stats(x)["E0"])
-        chunks = [torch.from_numpy(slots[j * slot:j * slot + int(sizes[j])].copy()) for j in range(world)]
-        static = [zd.code3_static_bytes(oracle.shard_count(n, world, j)) for j in range(world)]
-        got = {}
-        for design in (1, 2):
-            recv, offs = zd.alltoall_payloads(chunks, design=design,
-                                              static_bytes=static if design == 2 else None)
-            r, o = recv.numpy(), offs.tolist()
-            dec = []
-            ok = True
-            for s in range(world):
-                out, st = oracle.code3_decode_chunk(r[o[s]:o[s + 1]], n, world, rank)
-                ok = ok and st == 0 and np.array_equal(out, xs[s][rank * L:rank * L + n_me])
-                dec.append(torch.from_numpy(out.view(np.int16).copy()))
-            got[design] = (ok, r[:o[-1]].copy(), dec)
-        same = np.array_equal(got[1][1], got[2][1])
-        summed = zd.reduce_decoded(got[1][2]).numpy()
-        want = np.zeros(n_me, np.float32)
-        for s in range(world):
-            want = want + _f32(xs[s][rank * L:rank * L + n_me])
-        rs_ok = np.array_equal(summed.view(np.uint32), want.view(np.uint32))
-        q.put((rank, got[1][0], got[2][0], same, rs_ok))
+        res = [_round(rank, world, n) for n in (50_001, 200)]   # 200: the last rank's chunk is empty
+        q.put((rank,) + tuple(all(r[i] for r in res) for i in range(4)))
     except Exception as e:  # report, never hang the parent
         q.put((rank, repr(e), None, None, None))
     finally:
         if dist.is_initialized():
             dist.destroy_process_group()
+
+
+def _round(rank, world, n):
+    import oracle
+    import synth
+    from lossless_bf16_exponent_codec_gb300 import dist as zd
+    xs = [synth.config2(n, seed=10 + s).numpy().view(np.uint16) for s in range(world)]
+    L = oracle.shard_len(n, world)
+    n_me = oracle.shard_count(n, world, rank)
+    x = xs[rank]
+    slots, sizes, slot = oracle.code3_encode(x, world, oracle.stats(x)["E0"])
+    chunks = [torch.from_numpy(slots[j * slot:j * slot + int(sizes[j])].copy()) for j in range(world)]
+    static = [zd.code3_static_bytes(oracle.shard_count(n, world, j)) for j in range(world)]
+    got = {}
+    for design in (1, 2):
+        recv, offs = zd.alltoall_payloads(chunks, design=design,
+                                          static_bytes=static if design == 2 else None)
+        r, o = recv.numpy(), offs.tolist()
+        dec = []
+        ok = True
+        for s in range(world):
+            out, st = oracle.code3_decode_chunk(r[o[s]:o[s + 1]], n, world, rank)
+            ok = ok and st == 0 and np.array_equal(out, xs[s][rank * L:rank * L + n_me])
+            dec.append(torch.from_numpy(out.view(np.int16).copy()))
+        got[design] = (ok, r[:o[-1]].copy(), dec)
+    same = np.array_equal(got[1][1], got[2][1])
+    summed = zd.reduce_decoded(got[1][2]).numpy()
+    want = np.zeros(n_me, np.float32)
+    for s in range(world):
+        want = want + _f32(xs[s][rank * L:rank * L + n_me])
+    rs_ok = np.array_equal(summed.view(np.uint32), want.view(np.uint32))
+    return got[1][0], got[2][0], same, rs_ok
 
 
 def test_alltoall_and_reduce_scatter_three_ranks():
