@@ -199,6 +199,18 @@ ez_status ez_decode_code3(ez_plan p, const uint8_t* d_in, const uint64_t* d_offs
                           uint32_t first, uint32_t count, uint16_t* d_out,
                           uint32_t* d_status, void* d_ws, uint64_t ws_bytes, void* stream);
 
+/* The local step of a compressed reduce-scatter fused into a6 (ZipCCL
+ * digest 3.2, zipcclReduceScatter): chunks [first, first+count) as
+ * ez_decode_code3, but chunk first+i is added into the FP32 accumulator
+ * d_acc + i*L instead of written as BF16: d_acc[j] = (first_source ? 0 :
+ * d_acc[j]) + (float)value_j, one IEEE single-precision addition each --
+ * the same bits as ez_decode_code3 followed by ez_accumulate_bf16.  d_acc is
+ * a 16-byte aligned device pointer owned by the caller.  A chunk that fails
+ * its checks leaves its part of d_acc untouched and sets d_status. */
+ez_status ez_decode_code3_accumulate(ez_plan p, const uint8_t* d_in, const uint64_t* d_offsets,
+                                     uint32_t first, uint32_t count, float* d_acc, int first_source,
+                                     uint32_t* d_status, void* d_ws, uint64_t ws_bytes, void* stream);
+
 /* a3: exponent-reuse encode of shards [first, first+count) (one sender
  * encodes count = 1).  d_x and d_send_cache hold those shards contiguously
  * (shard first+i at offset i*L values / bytes).  A block is sent when cold

@@ -28,8 +28,8 @@ NOALLOC_SCRATCH_BYTES = 4 << 20   # EZ_NOALLOC_SCRATCH_BYTES
 
 ENTRY_POINTS = ("ez_plan_create", "ez_plan_destroy", "ez_plan_sizes", "ez_stats",
                 "ez_encode_code3", "ez_decode_code3", "ez_encode_reuse", "ez_decode_reuse",
-                "ez_gather_decode", "ez_encode_code3_noalloc", "ez_accumulate_bf16", "ez_status_str",
-                "ez_version")
+                "ez_gather_decode", "ez_encode_code3_noalloc", "ez_accumulate_bf16",
+                "ez_decode_code3_accumulate", "ez_status_str", "ez_version")
 
 
 class EzError(RuntimeError):
@@ -72,6 +72,7 @@ def lib():
             "ez_gather_decode": [vp, vp, vp, vp, vp, vp, vp, u64, vp],
             "ez_encode_code3_noalloc": [vp, vp, u32, u32, vp, vp, u64, vp, vp, vp],
             "ez_accumulate_bf16": [vp, vp, u64, i32, vp],
+            "ez_decode_code3_accumulate": [vp, vp, vp, u32, u32, vp, i32, vp, vp, u64, vp],
         }
         for name, args in sig.items():
             f = getattr(L, name)
@@ -183,6 +184,14 @@ def ez_encode_code3_noalloc(plan, x, first: int, count: int, stats, out, out_byt
 def ez_accumulate_bf16(acc, x, n: int, first: bool, stream=None) -> None:
     _check("ez_accumulate_bf16", lib().ez_accumulate_bf16(_ptr(acc), _ptr(x), n, 1 if first else 0,
                                                           _stream(stream)))
+
+
+def ez_decode_code3_accumulate(plan, inp, offsets, first: int, count: int, acc, first_source: bool,
+                               status, ws, ws_bytes: int, stream=None) -> None:
+    _check("ez_decode_code3_accumulate",
+           lib().ez_decode_code3_accumulate(plan, _ptr(inp), _ptr(offsets), first, count, _ptr(acc),
+                                            1 if first_source else 0, _ptr(status), _ptr(ws), ws_bytes,
+                                            _stream(stream)))
 
 
 def ez_version() -> int:

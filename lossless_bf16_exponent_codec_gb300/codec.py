@@ -121,15 +121,14 @@ class Codec:
                         stream=None) -> torch.Tensor:
         """Decode the W code3 chunks this rank received in an all-to-all
         (chunk ``me`` of every source, back to back in source order at
-        ``offsets``) and sum them in FP32 in source order (the library's
-        accumulate kernel).  Returns the FP32 sums of chunk ``me``."""
+        ``offsets``) and sum them in FP32 in source order, the decoder adding
+        each chunk into the accumulator.  Returns the FP32 sums of chunk
+        ``me``."""
         offs = offsets.cpu().tolist()
         n_me = max(0, min(self.L, self.n - me * self.L))
-        tmp = torch.zeros(max(self.L, 8), dtype=torch.int16, device=self.device)
-        acc = torch.zeros(max(n_me, 4), dtype=torch.float32, device=self.device)
+        acc = torch.zeros(max(self.L, 4), dtype=torch.float32, device=self.device)
         for s in range(self.W):
             one = torch.tensor([0, offs[s + 1] - offs[s]], dtype=torch.int64, device=self.device)
-            B.ez_decode_code3(self.plan, recv[offs[s]:], one, me, 1, tmp, self.status, self.ws,
-                              self.ws_bytes, stream)
-            B.ez_accumulate_bf16(acc, tmp, n_me, s == 0, stream)
+            B.ez_decode_code3_accumulate(self.plan, recv[offs[s]:], one, me, 1, acc, s == 0,
+                                         self.status, self.ws, self.ws_bytes, stream)
         return acc[:n_me]

@@ -208,6 +208,22 @@ ez_status ez_decode_code3(ez_plan p, const uint8_t* d_in, const uint64_t* d_offs
                                                 ezk::ws_view(p, d_ws), st));
 }
 
+ez_status ez_decode_code3_accumulate(ez_plan p, const uint8_t* d_in, const uint64_t* d_offsets,
+                                     uint32_t first, uint32_t count, float* d_acc, int first_source,
+                                     uint32_t* d_status, void* d_ws, uint64_t ws_bytes, void* stream)
+{
+    if (!p || p->codec != EZ_CODEC_CODE3) return EZ_ERR_ARG;
+    if (count == 0 || first >= p->W || count > p->W - first) return EZ_ERR_ARG;
+    if (!d_in || !al(d_in, 16) || !d_offsets || !al(d_offsets, 8) || !d_status || !al(d_status, 4))
+        return EZ_ERR_ARG;
+    if (p->n && (!d_acc || !al(d_acc, 16))) return EZ_ERR_ARG;
+    ez_status s = check_ws(p, d_ws, ws_bytes);
+    if (s != EZ_OK) return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    return cuda_status(ezk::launch_code3_decode(p, d_in, d_offsets, first, count, nullptr, d_status,
+                                                ezk::ws_view(p, d_ws), st, d_acc, first_source ? 1 : 0));
+}
+
 ez_status ez_encode_reuse(ez_plan p, const uint16_t* d_x, uint32_t first, uint32_t count,
                           uint8_t* d_send_cache, int cold, uint8_t* d_out, uint64_t out_bytes,
                           uint64_t* d_sizes, ez_stats_t* d_stats, uint32_t* d_status, void* d_ws,

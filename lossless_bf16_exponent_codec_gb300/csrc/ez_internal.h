@@ -76,7 +76,8 @@ cudaError_t launch_code3_encode(const ez_plan_s* p, const uint16_t* x, uint32_t 
 
 cudaError_t launch_code3_decode(const ez_plan_s* p, const uint8_t* in, const uint64_t* offsets,
                                 uint32_t first, uint32_t count, uint16_t* out,
-                                uint32_t* dstatus, const WsView& w, cudaStream_t s);
+                                uint32_t* dstatus, const WsView& w, cudaStream_t s,
+                                float* acc = nullptr, int acc_first = 0);
 
 cudaError_t launch_reuse_encode(const ez_plan_s* p, const uint16_t* x, uint32_t first,
                                 uint32_t count, uint8_t* cache, int cold, uint8_t* out,

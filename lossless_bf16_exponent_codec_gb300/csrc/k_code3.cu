@@ -40,6 +40,8 @@ struct C3Dec {
     const uint8_t* in;
     const uint64_t* offsets;
     uint16_t* out;
+    float* acc;          // accumulate variant: FP32 sums instead of BF16 output
+    int acc_first;       // the first source: acc = 0 + value
     uint32_t* dstatus;
     uint64_t n, L;
     uint32_t W, first, count, tpc;
@@ -410,7 +412,11 @@ __device__ __forceinline__ uint4 ld_v4_plain(const void* p)
 // checked against the tile's own escape count (entry 0 must be 0, each entry
 // plus the tile's count must equal the next entry, the last one n_esc), so
 // the escapes read are always inside the escape section.
-__global__ void __launch_bounds__(kThreads, 5) k_code3_decode(C3Dec a)
+// kAcc: the local step of a compressed reduce-scatter fused into the decode;
+// each decoded value is converted to FP32 (exact) and added to a.acc with one
+// IEEE addition (0 + value for the first source), as ez_accumulate_bf16 does.
+template <bool kAcc>
+__global__ void __launch_bounds__(kThreads, kAcc ? 4 : 5) k_code3_decode(C3Dec a)
 {
     __shared__ uint32_t s_bad, s_E0;
     __shared__ unsigned long long s_nesc;
@@ -554,7 +560,19 @@ __global__ void __launch_bounds__(kThreads, 5) k_code3_decode(C3Dec a)
         __syncthreads();
     }
     if (!cnt_v) return;
-    uint16_t* ot = a.out + (uint64_t)ci * a.L + v0 + tv;
+    uint16_t* ot = kAcc ? nullptr : a.out + (uint64_t)ci * a.L + v0 + tv;
+    float* at = kAcc ? a.acc + (uint64_t)ci * a.L + v0 + tv : nullptr;
+    // accumulate variant: the thread's 32 sums are requested before the code
+    // expansion, so their latency overlaps it
+    float4 accv[kAcc ? 8 : 1];
+    if (kAcc) {
+#pragma unroll
+        for (int q = 0; q < 8; q++) accv[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (!a.acc_first && cnt_v == 32) {
+#pragma unroll
+            for (int q = 0; q < 8; q++) accv[q] = reinterpret_cast<const float4*>(at)[q];
+        }
+    }
     const uint32_t smv[8] = {smw[0].x, smw[0].y, smw[0].z, smw[0].w, smw[1].x, smw[1].y, smw[1].z, smw[1].w};
 #pragma unroll
     for (int g = 0; g < 4; g++) {
@@ -571,7 +589,27 @@ __global__ void __launch_bounds__(kThreads, 5) k_code3_decode(C3Dec a)
         merge4(smv[2 * g], (uint32_t)e8, o4.x, o4.y);
         merge4(smv[2 * g + 1], (uint32_t)(e8 >> 32), o4.z, o4.w);
         const uint32_t v = 8u * (uint32_t)g;
-        if (v + 8 <= cnt_v) {
+        if (kAcc) {
+            const uint32_t hw[4] = {o4.x, o4.y, o4.z, o4.w};
+            float f[8];
+#pragma unroll
+            for (int i = 0; i < 8; i++)
+                f[i] = __uint_as_float((i & 1) ? (hw[i >> 1] & 0xFFFF0000u) : (hw[i >> 1] << 16));
+            if (cnt_v == 32) {
+                float4* p4 = reinterpret_cast<float4*>(at + v);
+                float4 lo = accv[2 * g], hi = accv[2 * g + 1];
+                lo.x = __fadd_rn(lo.x, f[0]); lo.y = __fadd_rn(lo.y, f[1]);
+                lo.z = __fadd_rn(lo.z, f[2]); lo.w = __fadd_rn(lo.w, f[3]);
+                hi.x = __fadd_rn(hi.x, f[4]); hi.y = __fadd_rn(hi.y, f[5]);
+                hi.z = __fadd_rn(hi.z, f[6]); hi.w = __fadd_rn(hi.w, f[7]);
+                p4[0] = lo;
+                p4[1] = hi;
+            } else {
+#pragma unroll
+                for (uint32_t i = 0; i < 8; i++)
+                    if (v + i < cnt_v) at[v + i] = __fadd_rn(a.acc_first ? 0.f : at[v + i], f[i]);
+            }
+        } else if (v + 8 <= cnt_v) {
             st_v4(ot + v, o4);
         } else if (v < cnt_v) {
             const uint32_t hw[4] = {o4.x, o4.y, o4.z, o4.w};
@@ -610,12 +648,15 @@ cudaError_t launch_code3_encode(const ez_plan_s* p, const uint16_t* x, uint32_t 
 
 cudaError_t launch_code3_decode(const ez_plan_s* p, const uint8_t* in, const uint64_t* offsets,
                                 uint32_t first, uint32_t count, uint16_t* out,
-                                uint32_t* dstatus, const WsView& w, cudaStream_t s)
+                                uint32_t* dstatus, const WsView& w, cudaStream_t s,
+                                float* acc, int acc_first)
 {
     C3Dec a;
     a.in = in;
     a.offsets = offsets;
     a.out = out;
+    a.acc = acc;
+    a.acc_first = acc_first;
     a.dstatus = dstatus;
     a.n = p->n;
     a.L = p->L;
@@ -627,7 +668,8 @@ cudaError_t launch_code3_decode(const ez_plan_s* p, const uint8_t* in, const uin
     a.counter = w.counters + 1;
     a.abort = w.counters + 7;
     const uint64_t tiles = (uint64_t)count * p->tpc;
-    k_code3_decode<<<(unsigned)tiles, kThreads, 0, s>>>(a);
+    if (acc) k_code3_decode<true><<<(unsigned)tiles, kThreads, 0, s>>>(a);
+    else k_code3_decode<false><<<(unsigned)tiles, kThreads, 0, s>>>(a);
     return cudaGetLastError();
 }
 

@@ -57,6 +57,34 @@ def test_reduce_scatter_local_step(ez, n, W):
         assert np.array_equal(acc.cpu().numpy().view(np.uint32), want.view(np.uint32)), j
 
 
+@pytest.mark.parametrize("n,W", [((1 << 20) + 777, 4), (5_003, 2)])
+def test_fused_decode_accumulate_equals_two_kernels(ez, n, W):
+    """ez_decode_code3_accumulate gives the bits of ez_decode_code3 followed
+    by ez_accumulate_bf16, for every chunk (ragged last chunks included)."""
+    binding, codec = ez
+    xs = [synth.config2(n, seed=40 + s, device="cuda") for s in range(3)]
+    c = codec.Codec(n, W)
+    L = c.L
+    for j in range(W):
+        n_j = max(0, min(L, n - j * L))
+        fused = torch.zeros(max(L, 4), dtype=torch.float32, device="cuda")
+        two = torch.zeros(max(L, 4), dtype=torch.float32, device="cuda")
+        tmp = torch.zeros(max(L, 8), dtype=torch.int16, device="cuda")
+        for s, x in enumerate(xs):
+            c.stats(x)
+            c.encode_code3(x)
+            size = int(c.sizes[j].item())
+            chunk = c.out[j * c.slot:j * c.slot + size].clone()
+            one = torch.tensor([0, size], dtype=torch.int64, device="cuda")
+            binding.ez_decode_code3_accumulate(c.plan, chunk, one, j, 1, fused, s == 0, c.status,
+                                               c.ws, c.ws_bytes)
+            binding.ez_decode_code3(c.plan, chunk, one, j, 1, tmp, c.status, c.ws, c.ws_bytes)
+            binding.ez_accumulate_bf16(two, tmp, n_j, s == 0)
+        torch.cuda.synchronize()
+        assert c.status_word() == 0
+        assert torch.equal(fused[:n_j].view(torch.int32), two[:n_j].view(torch.int32)), j
+
+
 def test_accumulate_kernel_all_patterns(ez):
     binding, codec = ez
     pats = np.arange(65536, dtype=np.uint32).astype(np.uint16)
