@@ -291,7 +291,7 @@ def run_ours(args, world, rank, local):
     # figure is a slight underestimate), the largest time x launches of that
     # kernel per step (k_stats also runs inside the coded reuse encode)
     single = {"stats": ("k_stats", 2, True), "code3_encode": ("k_code3_encode", 1, True),
-              "code3_decode": ("k_code3_decode", 1, False),
+              "code3_decode": ("k_code3_decode<0>", 1, False),
               "reuse_decode": ("k_reuse_decode32<0>", 1, False),
               "reuse_code3_decode": ("k_reuse_decode32<1>", 1, False)}
     top = max((ops.index(o) for o in single), key=lambda i: op_ms[i] * single[ops[i]][1])
