@@ -143,3 +143,23 @@ def test_device_collectives_one_rank_nccl(ez):
             assert np.array_equal(acc.cpu().numpy().view(np.uint32), want.view(np.uint32))
     finally:
         dist.destroy_process_group()
+
+
+def test_fused_decode_leaves_sums_of_a_bad_chunk_untouched(ez):
+    """A chunk that fails its header checks adds nothing and is reported."""
+    binding, codec = ez
+    n, W = 40_000, 2
+    x = synth.config2(n, seed=50, device="cuda")
+    c = codec.Codec(n, W)
+    c.stats(x)
+    c.encode_code3(x)
+    size = int(c.sizes[1].item())
+    chunk = c.out[c.slot:c.slot + size].clone()
+    chunk[0] ^= 0xFF                                   # magic broken
+    one = torch.tensor([0, size], dtype=torch.int64, device="cuda")
+    acc = torch.full((c.L,), 3.5, dtype=torch.float32, device="cuda")
+    c.clear_status()
+    binding.ez_decode_code3_accumulate(c.plan, chunk, one, 1, 1, acc, False, c.status, c.ws, c.ws_bytes)
+    torch.cuda.synchronize()
+    assert c.status_word() & binding.DSTAT_BAD_HEADER
+    assert torch.all(acc == 3.5)
