@@ -581,6 +581,7 @@ __global__ void __launch_bounds__(kThreads, 6) k_reuse_place(RuEnc a)
 // values [32t, 32t + 32) of the tile, which lie in one block: a changed
 // block's 32 exponents go to a stream position that is a multiple of 32, as
 // two aligned 16-byte stores.
+template <bool kHash>
 __global__ void __launch_bounds__(kThreads, 6) k_reuse_place32(RuEnc a)
 {
     __shared__ uint32_t s_bm[32], s_pre[32], s_agg;
@@ -604,7 +605,7 @@ __global__ void __launch_bounds__(kThreads, 6) k_reuse_place32(RuEnc a)
     // the thread's exponents, loaded with the bitmap and the prefix: from the
     // cache, or (hash-based detection: the cache holds hashes) from x
     uint4 ew[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
-    if (a.hash) {
+    if (kHash) {
         if (cnt_v) ew_from_x(a.x + (uint64_t)ci * a.L + v0 + tv, cnt_v, ew);
     } else if (cnt_v == 32) {
         ew[0] = ld_v4_nc(ct);
@@ -1359,8 +1360,9 @@ cudaError_t launch_reuse_encode(const ez_plan_s* p, const uint16_t* x, uint32_t 
         if (e != cudaSuccess) return e;
         e = launch_tile_scan(p, w.state_a, count, w.seg_a, w.counters + 4, w.counters + 7, dstatus, s);
         if (e != cudaSuccess) return e;
-        return p->B >= 32 ? launch_dependent(k_reuse_place32, tiles, kThreads, 0, s, a)
-                          : launch_dependent(k_reuse_place, tiles, kThreads, 0, s, a);
+        if (p->B < 32) return launch_dependent(k_reuse_place, tiles, kThreads, 0, s, a);
+        return a.hash ? launch_dependent(k_reuse_place32<true>, tiles, kThreads, 0, s, a)
+                      : launch_dependent(k_reuse_place32<false>, tiles, kThreads, 0, s, a);
     }
     a.plbuf = w.plbuf;
     a.escbuf = w.escbuf;
