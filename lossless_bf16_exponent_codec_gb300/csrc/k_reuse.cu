@@ -332,6 +332,130 @@ __global__ void __launch_bounds__(kThreads) k_reuse_hash(RuEnc a)
     }
 }
 
+// Raw reuse encode with hash-based change detection, step A in one pass
+// (same outputs as k_reuse_split<false> in hash mode): thread t holds the 32
+// values [32t, 32t + 32) of the tile, stores their sign+mantissa bytes,
+// hashes their exponent words as k_reuse_hash does, and the block's first
+// thread decides and updates the cache; the block bits go into the tile's
+// bitmap (a ballot, B/32 threads per block), whose count is published for
+// the scan and added to the shard totals.  The place step then reads the
+// changed exponents from x.
+__global__ void __launch_bounds__(kThreads, 6) k_reuse_hash_split(RuEnc a)
+{
+    __shared__ uint32_t s_bm[32];
+    const int t = threadIdx.x, lane = t & 31, wid = t >> 5;
+    if (t < 32) s_bm[t] = 0;
+    const TilePos tp = tile_pos(blockIdx.x, a.count, a.tpc);
+    const uint32_t ci = tp.ci, lt = tp.lt;
+    const uint64_t n_s = shard_values(a.n, a.L, a.first + ci);
+    const uint64_t v0 = (uint64_t)lt * kTile;
+    const uint32_t nv = v0 < n_s ? (uint32_t)umin64(kTile, n_s - v0) : 0u;
+    const uint32_t B = a.B, log2B = a.log2B;
+    const uint64_t nb = cdiv(n_s, B);
+    const uint64_t bm_bytes = cdiv(nb, 8);
+    const uint64_t off_sm = ru_off_sm(n_s, B);
+    const uint32_t tv = 32u * (uint32_t)t;
+    const uint32_t cnt_v = tv < nv ? min(32u, nv - tv) : 0u;
+    const uint16_t* xt = a.x + (uint64_t)ci * a.L + v0 + tv;
+    uint8_t* o = a.out + (uint64_t)ci * a.slot;
+    uint32_t xw[16];
+    if (cnt_v == 32) {
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+            const uint4 w = ld_v4_nc(xt + 8 * q);
+            xw[4 * q] = w.x; xw[4 * q + 1] = w.y; xw[4 * q + 2] = w.z; xw[4 * q + 3] = w.w;
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 16; i++) {
+            const uint32_t lo = 2u * i < cnt_v ? (uint32_t)xt[2 * i] : 0u;
+            const uint32_t hi = 2u * i + 1 < cnt_v ? (uint32_t)xt[2 * i + 1] : 0u;
+            xw[i] = lo | hi << 16;
+        }
+    }
+    if (cnt_v) {
+        uint32_t sm[8];
+#pragma unroll
+        for (int j = 0; j < 8; j++) sm[j] = sm4_of(xw[2 * j], xw[2 * j + 1]);
+        uint8_t* dst = o + off_sm + v0 + tv;
+        if (cnt_v == 32) {
+            st_v4(dst, make_uint4(sm[0], sm[1], sm[2], sm[3]));
+            st_v4(dst + 16, make_uint4(sm[4], sm[5], sm[6], sm[7]));
+        } else {
+            st_bytes16(dst, make_uint4(sm[0], sm[1], sm[2], sm[3]), cnt_v);
+            st_bytes16(dst + 16, make_uint4(sm[4], sm[5], sm[6], sm[7]), cnt_v > 16 ? cnt_v - 16 : 0u);
+        }
+    }
+    // the block's hash pair (words of 8 exponent bytes, 0 past the shard)
+    unsigned long long s0 = 0, s1 = 0;
+    const unsigned long long i0 = (tv & (B - 1u)) >> 3;
+#pragma unroll
+    for (int q = 0; q < 4; q++) {
+        const unsigned long long w = (unsigned long long)exp4_of(xw[4 * q + 2], xw[4 * q + 3]) << 32 |
+                                     exp4_of(xw[4 * q], xw[4 * q + 1]);
+        const unsigned long long base = w + (i0 + q + 1) * kGamma;
+        s0 += sm64_mix(base);
+        s1 += sm64_mix(base + kHashSeed1);
+    }
+    const uint32_t per = B >> 5;                          // threads per block, 1..32
+    for (uint32_t o2 = per >> 1; o2; o2 >>= 1) {
+        s0 += __shfl_xor_sync(kFull, s0, o2);
+        s1 += __shfl_xor_sync(kFull, s1, o2);
+    }
+    bool ch = false;
+    if ((lane & (per - 1)) == 0 && v0 + tv < n_s) {
+        const uint64_t k = (v0 + tv) >> log2B;
+        unsigned long long* hc = reinterpret_cast<unsigned long long*>(a.cache + (uint64_t)ci * a.hstride) + 2 * k;
+        const unsigned long long h0 = sm64_mix(s0), h1 = sm64_mix(s1);
+        if (a.cold || hc[0] != h0 || hc[1] != h1) {
+            hc[0] = h0;
+            hc[1] = h1;
+            ch = true;
+        }
+    }
+    const uint32_t bal = __ballot_sync(kFull, ch);
+    __syncthreads();   // s_bm cleared
+    if (lane == 0 && bal) {
+        const uint32_t nbw = 32u / per;                   // blocks per warp
+        uint32_t bits = 0;
+        for (uint32_t j = 0; j < nbw; j++)
+            if ((bal >> (j * per)) & 1u) bits |= 1u << j;
+        const uint32_t pos = (uint32_t)wid * nbw;
+        atomicOr(&s_bm[pos >> 5], bits << (pos & 31));
+    }
+    __syncthreads();
+    const uint32_t fin_tile = n_s ? (uint32_t)((n_s - 1) / kTile) : 0u;
+    if (t < 32) {
+        const uint32_t c = __popc(s_bm[lane]);
+        uint32_t x = c;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const uint32_t y = __shfl_up_sync(kFull, x, d);
+            if (lane >= d) x += y;
+        }
+        const uint32_t agg = __shfl_sync(kFull, x, 31);
+        if (t == 0) {
+            st_relaxed(a.state + tp.state, (lt == 0 ? kFlagIncl : kFlagAgg) | agg);
+            uint64_t len = (uint64_t)agg * B;
+            if (lt == fin_tile && n_s && block_changed(s_bm, (uint32_t)((n_s - 1 - v0) >> log2B)))
+                len -= nb * B - n_s;
+            if (agg) {
+                atomicAdd(&a.info[ci].n_changed, (unsigned long long)agg);
+                atomicAdd(&a.info[ci].m, (unsigned long long)len);
+            }
+        }
+    }
+    __syncthreads();
+    const uint32_t nbt = (uint32_t)kTile >> log2B;
+    const uint64_t bm0 = (uint64_t)lt * (nbt / 8);
+    if ((uint32_t)t < nbt / 8 && bm0 + t < bm_bytes)
+        o[64 + bm0 + t] = reinterpret_cast<const uint8_t*>(s_bm)[t];
+    if (lt == fin_tile) {
+        if (t < 16 && rup(bm_bytes, 16) > bm_bytes + t) o[64 + bm_bytes + t] = 0;
+        if (t < 16 && rup(n_s, 16) > n_s + t) o[off_sm + n_s + t] = 0;
+    }
+}
+
 // Step A of both reuse encoders, one CTA per 8192-value tile with no
 // inter-tile dependence: compare the exponents with the sender cache, store
 // the sign+mantissa bytes, build the tile's slice of the changed-block bitmap
@@ -1343,7 +1467,7 @@ cudaError_t launch_reuse_encode(const ez_plan_s* p, const uint16_t* x, uint32_t 
     a.hstride = p->hstride;
     const unsigned tiles = (unsigned)((uint64_t)count * p->tpc);
     cudaError_t e;
-    if (a.hash) {
+    if (a.hash && coded) {
         // the blocks' hash pairs against the cache: changed-block bits for the split
         k_reuse_hash<<<tiles, kThreads, 0, s>>>(a);
         e = cudaGetLastError();
@@ -1355,7 +1479,8 @@ cudaError_t launch_reuse_encode(const ez_plan_s* p, const uint16_t* x, uint32_t 
         if (e != cudaSuccess) return e;
     }
     if (!coded) {
-        k_reuse_split<false><<<tiles, kThreads, 0, s>>>(a);
+        if (a.hash) k_reuse_hash_split<<<tiles, kThreads, 0, s>>>(a);
+        else k_reuse_split<false><<<tiles, kThreads, 0, s>>>(a);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
         e = launch_tile_scan(p, w.state_a, count, w.seg_a, w.counters + 4, w.counters + 7, dstatus, s);
