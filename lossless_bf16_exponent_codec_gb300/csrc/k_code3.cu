@@ -13,6 +13,10 @@
 // prefix in one pass; only the escape bytes wait for it, the sign+mantissa
 // bytes and planes are stored before the look-back.  The last tile of each
 // chunk writes the header, the zero padding and the chunk size.
+//
+// The decoder has a second variant that adds the decoded values into an FP32
+// accumulator instead of storing BF16 (the local step of a compressed
+// reduce-scatter, digest 3.2).
 #include "ez_internal.h"
 #include "ez_common.cuh"
 #include "ez_bytes.cuh"

@@ -2,16 +2,20 @@
 // ("CIERA: Cross-Iteration Exponent Reuse for Lossless Allgather in Sharded
 // MoE Training", exponent-reuse and gain-formula paragraphs).
 //
-// Sender (k_reuse_encode): per block of B values, the block is "changed" when
-// one of its exponents differs from the sender's cache of the previous
-// iteration (or the call is cold).  The payload carries a changed-block
-// bitmap, the sign+mantissa byte of every value and the exponents of the
-// changed blocks packed in block order; the cache then takes the new
-// exponents.  The pages detect changes with a 128-bit block hash compared to
-// a hash cache; comparing the cached exponents directly gives the same
-// bitmap (minus hash collisions) in one pass.  A changed block's position in
-// the exponent section is (changed blocks before it) * B: a decoupled
-// look-back gives each tile the count of changed blocks in earlier tiles.
+// Sender: per block of B values, the block is "changed" when one of its
+// exponents differs from the sender's cache of the previous iteration (or the
+// call is cold).  The payload carries a changed-block bitmap, the
+// sign+mantissa byte of every value and the exponents of the changed blocks
+// packed in block order.  Change detection compares the exponents with an
+// exponent cache (1 byte per value; same bitmap as the pages' block hash,
+// minus collisions) or, with EZ_FLAG_HASH_CACHE, compares two SplitMix64
+// hashes per block with the pages' HashCache (16 bytes per block).  Step A
+// (k_reuse_split, or k_reuse_hash_split for the raw codec in hash mode) is one
+// CTA per 8192-value tile with no inter-tile dependence and publishes the
+// tile's changed-block count; k_tile_scan turns the counts into prefixes; the
+// place step puts each tile's changed exponents at (prefix + rank) * B and
+// writes the index entry, and the tile holding the shard's last value writes
+// the header and the size.
 //
 // Coded variant (EZ_CODEC_REUSE_CODE3): the changed exponents are coded with
 // the 3-bit code of ZipCCL (research digest 3.1) instead of nvCOMP's ANS,
@@ -19,11 +23,12 @@
 // launch of its own).  The split codes each tile's changed exponents and
 // stages its planes and escapes; the place step moves them into the payload.
 //
-// Receiver (k_reuse_decode): for W payloads in one launch, each tile reads
-// its slice of the bitmap, looks back for the changed-block prefix, takes
-// unchanged exponents from its exponent cache (ExpCache) and changed ones
-// from the payload, writes them back into the cache and stores the merged
-// BF16 values straight into the gathered full buffer.
+// Receiver (k_reuse_decode32, k_reuse_decode for B < 32): for W payloads in
+// one launch, each 8192-value span reads its slice of the bitmap and its
+// prefix from the payload's index, takes unchanged exponents from its
+// exponent cache (ExpCache) and changed ones from the payload, writes them
+// back into the cache and stores the merged BF16 values straight into the
+// gathered full buffer.
 #include "ez_internal.h"
 #include "ez_common.cuh"
 #include "ez_bytes.cuh"
