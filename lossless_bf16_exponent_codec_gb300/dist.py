@@ -1,4 +1,6 @@
-"""The exchange step of a compressed all-gather across ranks.
+"""The exchange steps of the compressed collectives across ranks: all-gather,
+all-to-all (Designs 1 and 2) and reduce-scatter, and the switcher between the
+compressed and the native reduce-scatter.
 
 ZipCCL research digest 3.2 (zipcclAllGather): each rank compresses its own
 chunk, the ranks all-gather the compressed sizes, then all-gather the
