@@ -14,13 +14,17 @@ static_assert(sizeof(StatsBins) == 3 * 256 * 8 + 256, "StatsBins layout (api.cpp
 static_assert(sizeof(ShardInfo) == 64, "ShardInfo layout (api.cpp sizes it)");
 static_assert(sizeof(ez_stats_t) == 2120, "ez_stats_t layout");
 
-constexpr int kStatsLoads = 32;                             // 16-B loads per thread
-constexpr uint32_t kStatsTile = kThreads * kStatsLoads * 8;   // 65536 values
+constexpr int kStatsLoads = 27;                             // 16-B loads per thread
+constexpr int kStatsBatch = 3;                              // loads in flight per thread
+static_assert(kStatsLoads % kStatsBatch == 0, "whole batches");
+// 55296 values: 2^26 values make 1214 tiles, 8 shards of 2^23 make 1216,
+// i.e. at most 8 per SM on 152 SMs (8 resident), none left for a second wave
+constexpr uint32_t kStatsTile = kThreads * kStatsLoads * 8;
 static_assert(kStatsTile <= kStatsMaxValues, "a tile's sums fit the 32-bit shared bins");
 
-// One CTA per tile of 65536 values of one shard, 8 resident CTAs per SM;
-// every thread keeps four 16-byte loads in flight and adds their 32 values to
-// the CTA's histogram.  Shard ci = tile / tps holds values [ci*L, ci*L + n_s)
+// One CTA per tile of 55296 values of one shard, 8 resident CTAs per SM;
+// every thread keeps three 16-byte loads in flight and adds their 24 values
+// to the CTA's histogram.  Shard ci = tile / tps holds values [ci*L, ci*L + n_s)
 // of x; its CTAs fold into bins G[ci], and the last of them writes out[ci].
 // The a1 statistics of a whole tensor are the case of one shard.
 __global__ void __launch_bounds__(kThreads, 8)
@@ -43,12 +47,12 @@ k_stats(const uint16_t* __restrict__ x, uint64_t n, uint64_t L, uint32_t first, 
     if (nv == kStatsTile) {
         // full tile: no per-group bounds
 #pragma unroll 1
-        for (int g0 = 0; g0 < kStatsLoads; g0 += 4) {
-            uint4 w[4];
+        for (int g0 = 0; g0 < kStatsLoads; g0 += kStatsBatch) {
+            uint4 w[kStatsBatch];
 #pragma unroll
-            for (int k = 0; k < 4; k++) w[k] = ld_v4_nc(xt + 8u * (uint32_t)((g0 + k) * kThreads + t));
+            for (int k = 0; k < kStatsBatch; k++) w[k] = ld_v4_nc(xt + 8u * (uint32_t)((g0 + k) * kThreads + t));
 #pragma unroll
-            for (int k = 0; k < 4; k++) st_add8(w[k], e7, hb, S);
+            for (int k = 0; k < kStatsBatch; k++) st_add8(w[k], e7, hb, S);
         }
         grid_dep_wait();   // the bins were cleared by the kernel before
         if (st_end(S, G + ci, tps)) st_finalize(G + ci, n_s, K, out + ci, S, hist_window);
