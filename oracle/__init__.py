@@ -46,6 +46,18 @@ class _Stats(ctypes.Structure):
                 ("n_escape", ctypes.c_uint64)]
 
 
+class _Fp8Stats(ctypes.Structure):
+    _fields_ = [("hist", ctypes.c_uint64 * 32), ("n", ctypes.c_uint64),
+                ("n_finite", ctypes.c_uint64), ("s1", ctypes.c_double),
+                ("s2", ctypes.c_double), ("var", ctypes.c_double),
+                ("sigma", ctypes.c_double), ("K", ctypes.c_double),
+                ("E0", ctypes.c_uint32), ("rule", ctypes.c_uint32),
+                ("n_escape", ctypes.c_uint64)]
+
+
+FP8_E5M2, FP8_E4M3 = 1, 2
+
+
 def lib():
     global _lib
     if _lib is None:
@@ -70,6 +82,10 @@ def lib():
             "orc_reuse_encode_mode": (i32, [vp, u64, u32, u32, vp, i32, i32, i32, vp, vp, u64, vp]),
             "orc_reuse_encode_hash": (i32, [vp, u64, u32, u32, vp, i32, i32, i32, vp, vp, u64, vp]),
             "orc_splitmix64_next": (u64, [vp]),
+            "orc_fp8_stats": (i32, [vp, u64, i32, i32, vp]),
+            "orc_fp8_chunk_bytes": (u64, [u64, u64, i32]),
+            "orc_fp8_encode": (i32, [vp, u64, u32, i32, u32, vp, u64, vp]),
+            "orc_fp8_decode": (u32, [vp, vp, u64, u32, i32, vp]),
             "orc_block_hash": (u64, [vp, u64, u32, u64, i32]),
             "orc_reuse_decode": (u32, [vp, u64, u64, u32, u32, vp, vp]),
             "orc_gather_decode_reuse": (u32, [vp, vp, u64, u32, u32, vp, vp]),
@@ -290,3 +306,46 @@ def reuse_encode_all(x, W: int, B: int, cache: np.ndarray, cold: bool = False,
         sizes[r] = pay.size
         sts.append(st)
     return slots, sizes, slot, sts
+
+
+# ----------------------------------------------------------------- FP8
+
+def fp8_stats(x, fmt: int, window_mode: int = 0) -> dict:
+    """Statistics and window of FP8 values (uint8 bit patterns)."""
+    x = np.ascontiguousarray(x, dtype=np.uint8)
+    st = _Fp8Stats()
+    buf = x if x.size else np.zeros(1, dtype=np.uint8)
+    rc = lib().orc_fp8_stats(_p(buf), x.size, fmt, window_mode, ctypes.byref(st))
+    if rc != 0:
+        raise ValueError("bad FP8 format")
+    nb = 32 if fmt == FP8_E5M2 else 16
+    return {"hist": np.array(st.hist[:nb], dtype=np.uint64), "n": st.n, "n_finite": st.n_finite,
+            "s1": st.s1, "s2": st.s2, "var": st.var, "sigma": st.sigma, "K": st.K, "E0": st.E0,
+            "rule": st.rule, "n_escape": st.n_escape}
+
+
+def fp8_chunk_bytes(n_c: int, n_esc: int, fmt: int) -> int:
+    return int(lib().orc_fp8_chunk_bytes(n_c, n_esc, fmt))
+
+
+def fp8_encode(x, W: int, fmt: int, E0: int) -> Tuple[np.ndarray, np.ndarray, int]:
+    """-> (slots u8[W*slot], sizes u64[W], slot_bytes); slot = worst case of one chunk."""
+    x = np.ascontiguousarray(x, dtype=np.uint8)
+    L = shard_len(x.size, W)
+    slot = fp8_chunk_bytes(L, L, fmt)
+    out = np.zeros(W * slot, dtype=np.uint8)
+    sizes = np.zeros(W, dtype=np.uint64)
+    buf = x if x.size else np.zeros(1, dtype=np.uint8)
+    rc = lib().orc_fp8_encode(_p(buf), x.size, W, fmt, E0, _p(out), slot, _p(sizes))
+    if rc != 0:
+        raise ValueError(f"orc_fp8_encode failed ({rc})")
+    return out, sizes, slot
+
+
+def fp8_decode(buf: np.ndarray, offsets: np.ndarray, n: int, W: int, fmt: int) -> Tuple[np.ndarray, int]:
+    buf = np.ascontiguousarray(buf, dtype=np.uint8)
+    offsets = np.ascontiguousarray(offsets, dtype=np.uint64)
+    out = np.zeros(max(n, 1), dtype=np.uint8)
+    st = lib().orc_fp8_decode(_p(buf if buf.size else np.zeros(1, np.uint8)), _p(offsets), n, W, fmt,
+                              _p(out))
+    return out[:n], int(st)

@@ -696,3 +696,225 @@ uint32_t orc_gather_decode_reuse(const uint8_t* recv, const uint64_t* offsets,
     }
     return status;
 }
+
+/* ------------------------------------------------------------------ FP8 */
+/* The 3-bit exponent code applied to FP8 [ZIP 3.3 last paragraph: "FP8 E5M2
+ * coded to 3 bits gives e = 0.75, E4M3 gives e ~ 0.88"].  Formats as in the
+ * OCP 8-bit floating-point specification: E5M2 (bias 15, infinities and NaN
+ * at exponent field 31) and E4M3 (bias 7, no infinities, NaN only at
+ * S.1111.111).  A value keeps its sign and mantissa bits raw (1+m bits, as
+ * bit-planes); its exponent field becomes the 3-bit code of the window
+ * E0..E0+6 or escapes to the raw field.  The window follows the same Gaussian
+ * model as for BF16 (the 7-binade argument does not depend on the format):
+ * E0 = bias + x0, clamped to 0 .. (2^e - 1) - 6. */
+
+typedef struct { unsigned ebits, mbits, bias; } fp8_fmt;
+
+static int fp8_format(int fmt, fp8_fmt* f)
+{
+    if (fmt == ORC_FP8_E5M2) { f->ebits = 5; f->mbits = 2; f->bias = 15; return 0; }
+    if (fmt == ORC_FP8_E4M3) { f->ebits = 4; f->mbits = 3; f->bias = 7; return 0; }
+    return -1;
+}
+
+static unsigned fp8_exp(const fp8_fmt* f, uint8_t b) { return (b >> f->mbits) & ((1u << f->ebits) - 1u); }
+static unsigned fp8_man(const fp8_fmt* f, uint8_t b) { return b & ((1u << f->mbits) - 1u); }
+static unsigned fp8_sm(const fp8_fmt* f, uint8_t b) { return ((b >> 7) << f->mbits) | fp8_man(f, b); }
+static uint8_t fp8_merge(const fp8_fmt* f, unsigned sm, unsigned e)
+{
+    return (uint8_t)(((sm >> f->mbits) << 7) | (e << f->mbits) | (sm & ((1u << f->mbits) - 1u)));
+}
+static int fp8_finite(const fp8_fmt* f, uint8_t b)
+{
+    unsigned emax = (1u << f->ebits) - 1u;
+    if (f->ebits == 5) return fp8_exp(f, b) != emax;                          /* E5M2: Inf / NaN */
+    return !(fp8_exp(f, b) == emax && fp8_man(f, b) == (1u << f->mbits) - 1u);  /* E4M3: NaN only */
+}
+
+int orc_fp8_stats(const uint8_t* x, uint64_t n, int fmt, int window_mode, orc_fp8_stats_t* st)
+{
+    fp8_fmt f;
+    if (fp8_format(fmt, &f)) return -1;
+    memset(st, 0, sizeof(*st));
+    st->n = n;
+    const unsigned nbins = 1u << f.ebits, emax0 = nbins - 1u - 6u;
+    uint64_t cnt[256];
+    memset(cnt, 0, sizeof(cnt));
+    for (uint64_t i = 0; i < n; i++) {
+        cnt[x[i]]++;
+        st->hist[fp8_exp(&f, x[i])]++;
+    }
+    /* v * 2^U = +-M * 2^(max(E,1) - 1), M = E ? 2^m + man : man,
+     * U = bias + m - 1: exact big sums of the 256 patterns, rounded once */
+    big_t P, Q, R;
+    memset(&P, 0, sizeof(P));
+    memset(&Q, 0, sizeof(Q));
+    memset(&R, 0, sizeof(R));
+    for (unsigned b = 0; b < 256; b++) {
+        if (!cnt[b] || !fp8_finite(&f, (uint8_t)b)) continue;
+        st->n_finite += cnt[b];
+        unsigned E = fp8_exp(&f, (uint8_t)b);
+        uint64_t M = (E ? (1u << f.mbits) : 0u) + fp8_man(&f, (uint8_t)b);
+        unsigned sh = (E ? E : 1u) - 1u;
+        if (M == 0) continue;
+        if (b & 0x80u) big_add_shifted(&Q, cnt[b] * M, sh);
+        else big_add_shifted(&P, cnt[b] * M, sh);
+        big_add_shifted(&R, cnt[b] * M * M, 2 * sh);
+    }
+    int U = (int)(f.bias + f.mbits) - 1;
+    if (big_cmp(&P, &Q) >= 0) {
+        big_sub(&P, &Q);
+        st->s1 = big_round(&P, -U);
+    } else {
+        big_sub(&Q, &P);
+        st->s1 = -big_round(&Q, -U);
+    }
+    st->s2 = big_round(&R, -2 * U);
+    st->K = orc_window_K();
+    st->rule = 1;
+    if (st->n_finite >= 2) {
+        double N = (double)st->n_finite;
+        double var = (st->s2 - st->s1 * (st->s1 / N)) / (N - 1.0);
+        st->var = var;
+        if (var > 0 && isfinite(var)) {
+            st->sigma = sqrt(var);
+            if (window_mode == 0) {
+                /* the integer nearest x_opt, ties up: the largest k with
+                 * var >= K 2^(2k-1), as a field value bias + k */
+                uint32_t E0 = 0;
+                for (unsigned e = 1; e <= emax0; e++) {
+                    int k = (int)e - (int)f.bias;
+                    if (var >= ldexp(st->K, 2 * k - 1)) E0 = e;
+                }
+                st->E0 = E0;
+                st->rule = 0;
+            }
+        }
+    }
+    if (st->rule == 1) {
+        uint64_t best = 0;
+        uint32_t best_b = 0;
+        for (uint32_t b = 0; b <= emax0; b++) {
+            uint64_t c = 0;
+            for (uint32_t E = b; E <= b + 6; E++) c += st->hist[E];
+            if (c > best) { best = c; best_b = b; }
+        }
+        st->E0 = best_b;
+    }
+    uint64_t in_window = 0;
+    for (uint32_t E = st->E0; E <= st->E0 + 6; E++) in_window += st->hist[E];
+    st->n_escape = n - in_window;
+    return 0;
+}
+
+/* chunk: header 128 | 1+m sign/mantissa planes | 3 code planes | index (u64
+ * escapes before each 8192 values) | escapes (raw exponent fields, value
+ * order); every section padded to 128 bytes, plane p holding bit p of the
+ * field for value j at bit j&7 of byte j>>3. */
+uint64_t orc_fp8_chunk_bytes(uint64_t n_c, uint64_t n_esc, int fmt)
+{
+    fp8_fmt f;
+    if (fp8_format(fmt, &f)) return 0;
+    uint64_t plane = round_up(ceil_div(n_c, 8), 128);
+    return 128 + (1 + f.mbits + 3) * plane + round_up(8 * ceil_div(n_c, IDX_SPAN), 128) + round_up(n_esc, 128);
+}
+
+int orc_fp8_encode(const uint8_t* x, uint64_t n, uint32_t W, int fmt, uint32_t E0,
+                   uint8_t* out, uint64_t slot_bytes, uint64_t* sizes)
+{
+    fp8_fmt f;
+    if (fp8_format(fmt, &f) || W == 0) return -1;
+    const unsigned nsm = 1 + f.mbits, emax0 = (1u << f.ebits) - 1u - 6u;
+    if (E0 > emax0) return -1;
+    uint64_t L = orc_shard_len(n, W);
+    for (uint32_t c = 0; c < W; c++) {
+        uint64_t n_c = orc_shard_count(n, W, c);
+        const uint8_t* xc = x + (uint64_t)c * L;
+        uint64_t n_esc = 0;
+        for (uint64_t j = 0; j < n_c; j++) {
+            unsigned E = fp8_exp(&f, xc[j]);
+            if (!(E >= E0 && E <= E0 + 6)) n_esc++;
+        }
+        uint64_t bytes = orc_fp8_chunk_bytes(n_c, n_esc, fmt);
+        if (bytes > slot_bytes) return -2;
+        uint8_t* o = out + (uint64_t)c * slot_bytes;
+        memset(o, 0, bytes);
+        o[0] = 'E'; o[1] = 'Z'; o[2] = 'F'; o[3] = '8';
+        o[4] = 1;
+        o[5] = (uint8_t)fmt;
+        o[6] = (uint8_t)E0;
+        put_u64(o + 8, n_c);
+        put_u64(o + 16, n_esc);
+        put_u64(o + 24, bytes);
+        put_u32(o + 32, c);
+        put_u32(o + 36, W);
+        uint64_t plane = round_up(ceil_div(n_c, 8), 128);
+        uint8_t* pl = o + 128;
+        uint8_t* idx = pl + (nsm + 3) * plane;
+        uint8_t* esc = idx + round_up(8 * ceil_div(n_c, IDX_SPAN), 128);
+        uint64_t k = 0;
+        for (uint64_t j = 0; j < n_c; j++) {
+            if (j % IDX_SPAN == 0) put_u64(idx + 8 * (j / IDX_SPAN), k);
+            unsigned sm = fp8_sm(&f, xc[j]), E = fp8_exp(&f, xc[j]);
+            unsigned code = (E >= E0 && E <= E0 + 6) ? E - E0 + 1 : 0;
+            for (unsigned p = 0; p < nsm; p++)
+                if ((sm >> p) & 1u) pl[p * plane + j / 8] |= (uint8_t)(1u << (j % 8));
+            for (unsigned p = 0; p < 3; p++)
+                if ((code >> p) & 1u) pl[(nsm + p) * plane + j / 8] |= (uint8_t)(1u << (j % 8));
+            if (code == 0) esc[k++] = (uint8_t)E;
+        }
+        sizes[c] = bytes;
+    }
+    return 0;
+}
+
+uint32_t orc_fp8_decode(const uint8_t* in, const uint64_t* offsets, uint64_t n, uint32_t W,
+                        int fmt, uint8_t* out)
+{
+    fp8_fmt f;
+    if (fp8_format(fmt, &f) || W == 0) return ORC_BAD_HEADER;
+    const unsigned nsm = 1 + f.mbits, emax0 = (1u << f.ebits) - 1u - 6u;
+    uint32_t status = 0;
+    uint64_t L = orc_shard_len(n, W);
+    for (uint32_t c = 0; c < W; c++) {
+        uint64_t n_c = orc_shard_count(n, W, c);
+        if (offsets[c + 1] < offsets[c]) { status |= ORC_BAD_SIZE; continue; }
+        uint64_t avail = offsets[c + 1] - offsets[c];
+        if (avail < 128) { status |= ORC_BAD_SIZE; continue; }
+        const uint8_t* p = in + offsets[c];
+        if (!(p[0] == 'E' && p[1] == 'Z' && p[2] == 'F' && p[3] == '8') || p[4] != 1 || p[5] != (uint8_t)fmt
+            || p[6] > emax0 || get_u64(p + 8) != n_c || get_u32(p + 32) != c || get_u32(p + 36) != W) {
+            status |= ORC_BAD_HEADER;
+            continue;
+        }
+        unsigned E0 = p[6];
+        uint64_t n_esc = get_u64(p + 16);
+        if (n_esc > n_c) { status |= ORC_BAD_COUNT; continue; }
+        uint64_t bytes = get_u64(p + 24);
+        if (bytes != orc_fp8_chunk_bytes(n_c, n_esc, fmt) || bytes > avail) { status |= ORC_BAD_SIZE; continue; }
+        uint64_t plane = round_up(ceil_div(n_c, 8), 128);
+        const uint8_t* pl = p + 128;
+        const uint8_t* idx = pl + (nsm + 3) * plane;
+        const uint8_t* esc = idx + round_up(8 * ceil_div(n_c, IDX_SPAN), 128);
+        uint8_t* oc = out + (uint64_t)c * L;
+        uint64_t k = 0;
+        for (uint64_t j = 0; j < n_c; j++) {
+            if (j % IDX_SPAN == 0 && get_u64(idx + 8 * (j / IDX_SPAN)) != k) status |= ORC_BAD_COUNT;
+            unsigned sm = 0, code = 0;
+            for (unsigned q = 0; q < nsm; q++) sm |= ((pl[q * plane + j / 8] >> (j % 8)) & 1u) << q;
+            for (unsigned q = 0; q < 3; q++) code |= ((pl[(nsm + q) * plane + j / 8] >> (j % 8)) & 1u) << q;
+            unsigned E;
+            if (code) {
+                E = E0 + code - 1;
+            } else if (k < n_esc) {
+                E = esc[k++] & ((1u << f.ebits) - 1u);
+            } else {
+                status |= ORC_BAD_COUNT;
+                E = 0;
+            }
+            oc[j] = fp8_merge(&f, sm, E);
+        }
+        if (k != n_esc) status |= ORC_BAD_COUNT;
+    }
+    return status;
+}

@@ -97,6 +97,24 @@ uint32_t orc_gather_decode_reuse(const uint8_t* recv, const uint64_t* offsets,
                                  uint64_t n, uint32_t W, uint32_t B,
                                  uint8_t* recv_cache, uint16_t* out);
 
+/* ---- FP8 (E5M2 / E4M3) with the 3-bit exponent code [ZIP 3.3]: oracle of
+ * a format for later kernels; no library entry point yet ---- */
+#define ORC_FP8_E5M2 1
+#define ORC_FP8_E4M3 2
+typedef struct {
+    uint64_t hist[32];       /* count of each exponent field value (16 for E4M3) */
+    uint64_t n, n_finite;
+    double   s1, s2, var, sigma, K;
+    uint32_t E0, rule;
+    uint64_t n_escape;
+} orc_fp8_stats_t;
+int      orc_fp8_stats(const uint8_t* x, uint64_t n, int fmt, int window_mode, orc_fp8_stats_t* st);
+uint64_t orc_fp8_chunk_bytes(uint64_t n_c, uint64_t n_esc, int fmt);
+int      orc_fp8_encode(const uint8_t* x, uint64_t n, uint32_t W, int fmt, uint32_t E0,
+                        uint8_t* out, uint64_t slot_bytes, uint64_t* sizes);
+uint32_t orc_fp8_decode(const uint8_t* in, const uint64_t* offsets, uint64_t n, uint32_t W,
+                        int fmt, uint8_t* out);
+
 #ifdef __cplusplus
 }
 #endif
