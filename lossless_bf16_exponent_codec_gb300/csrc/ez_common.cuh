@@ -16,6 +16,7 @@
 // the caller turns into EZ_DSTAT_TIMEOUT.
 #pragma once
 
+#include <atomic>
 #include <cstdint>
 #include <utility>
 #include <cuda_runtime.h>
@@ -369,6 +370,27 @@ inline cudaError_t launch_dependent(void (*kernel)(KArgs...), unsigned grid, uns
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+// A kernel's dynamic shared-memory limit is an attribute of the kernel in one
+// device's context, so it must be raised on every device the kernel runs on.
+// One record per kernel: bit d is set once device d has it (ordinals >= 64
+// set it on every launch).
+struct PerDeviceAttr {
+    std::atomic<unsigned long long> done{0};
+};
+
+template <typename K>
+inline cudaError_t max_dyn_smem_per_device(PerDeviceAttr& rec, K kernel, int bytes)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const bool tracked = dev >= 0 && dev < 64;
+    if (tracked && ((rec.done.load(std::memory_order_acquire) >> dev) & 1ull)) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && tracked) rec.done.fetch_or(1ull << dev, std::memory_order_release);
+    return e;
 }
 
 template <typename K>

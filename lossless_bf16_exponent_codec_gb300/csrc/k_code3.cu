@@ -643,8 +643,8 @@ cudaError_t launch_code3_encode(const ez_plan_s* p, const uint16_t* x, uint32_t 
     a.counter = w.counters + 0;
     a.abort = w.counters + 7;
     a.shard_ctr = w.shard_ctr;
-    static const cudaError_t attr = cudaFuncSetAttribute(
-        k_code3_encode, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(EncSmem));
+    static PerDeviceAttr smem_attr;
+    const cudaError_t attr = max_dyn_smem_per_device(smem_attr, k_code3_encode, (int)sizeof(EncSmem));
     if (attr != cudaSuccess) return attr;
     return launch_dependent(k_code3_encode, persistent_grid(k_code3_encode, kEncThreads, sizeof(EncSmem)),
                             kEncThreads, sizeof(EncSmem), s, a);

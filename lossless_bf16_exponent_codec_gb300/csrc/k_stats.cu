@@ -78,8 +78,8 @@ static cudaError_t stats_launch(const uint16_t* x, uint64_t n, uint64_t L, uint3
     const uint64_t tps = per_shard ? cdiv(per_shard, kStatsTile) : 1;
     const uint64_t tiles = tps * count;
     if (tiles > 0x7fffffffull) return cudaErrorInvalidValue;
-    static const cudaError_t attr = cudaFuncSetAttribute(
-        k_stats, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(StatsSmem));
+    static PerDeviceAttr smem_attr;
+    const cudaError_t attr = max_dyn_smem_per_device(smem_attr, k_stats, (int)sizeof(StatsSmem));
     if (attr != cudaSuccess) return attr;
     return launch_dependent(k_stats, (unsigned)tiles, kThreads, sizeof(StatsSmem), s, x, n, L, first, W,
                             (uint32_t)tps, G, out, K, hist_window);
