@@ -267,7 +267,10 @@ ez_status ez_gather_decode(ez_plan p, const uint8_t* d_recv, const uint64_t* d_o
  * launched (4 MiB covers e.g. 2^31 values in 8 chunks).
  * The first call on a device, with that device current, looks up the
  * array's device address (cudaGetSymbolAddress); make that first call before
- * any stream capture.  Each call clears the scratch it needs on `stream`
+ * any stream capture.  The address is kept for the life of the process, so
+ * the device's primary context must live as long: do not call this entry
+ * point on a device after cudaDeviceReset on it (the array would be at a new
+ * address and the kept one would be stale).  Each call clears the scratch it needs on `stream`
  * before its launch; every call on a device shares the one array, so calls
  * whose work overlaps on the GPU (unordered streams) race and must not be
  * issued.  Devices with ordinal >= 64 give EZ_ERR_UNSUPPORTED.  Arguments

@@ -54,6 +54,37 @@ def test_noalloc_matches_workspace_encode(ez, n, W):
             assert torch.equal(o[r * c.slot:r * c.slot + k], o_ref[r * c.slot:r * c.slot + k])
 
 
+@pytest.mark.gpu
+def test_noalloc_chunk_subrange(ez):
+    """Chunks [3, 5) of 8: the scratch holds per-chunk state for the encoded
+    chunks only (indexed from `first`), so a sub-range must give the same
+    bytes as the workspace encoder on the same sub-range, twice in a row."""
+    binding, codec = ez
+    n, W, first, count = (1 << 21) + 4099, 8, 3, 2
+    c = codec.Codec(n, W)
+    x = synth.config2(n, device="cuda")
+    c.stats(x)
+    sub = x[first * c.L:]
+    c.out.zero_()
+    binding.ez_encode_code3(c.plan, sub, first, count, c.stats_buf, c.out, c.out.numel(), c.sizes,
+                            c.status, c.ws, c.ws_bytes)
+    torch.cuda.synchronize()
+    assert c.status_word() == 0
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for _ in range(2):
+        o = torch.zeros_like(c.out)
+        sz = torch.zeros_like(c.sizes)
+        binding.ez_encode_code3_noalloc(c.plan, sub, first, count, c.stats_buf, o, o.numel(), sz,
+                                        status)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        assert torch.equal(sz[:count], c.sizes[:count])
+        for i in range(count):
+            k = int(c.sizes[i].item())
+            assert k > 0
+            assert torch.equal(o[i * c.slot:i * c.slot + k], c.out[i * c.slot:i * c.slot + k])
+
+
 def test_noalloc_rejects_oversized_plans(ez):
     """Sizes beyond EZ_NOALLOC_SCRATCH_BYTES give EZ_ERR_CAPACITY before any
     device work; the pointers below are aligned placeholders that are never
