@@ -74,6 +74,7 @@ def lib():
             "orc_code3_chunk_bytes": (u64, [u64, u64]),
             "orc_code3_slot_bytes": (u64, [u64, u32]),
             "orc_code3_encode": (i32, [vp, u64, u32, u32, vp, u64, vp]),
+            "orc_code3_encode_chunk": (i32, [vp, u64, u32, u32, u32, vp, u64, vp]),
             "orc_code3_decode": (u32, [vp, vp, u64, u32, vp]),
             "orc_code3_decode_chunk": (u32, [vp, u64, u64, u32, u32, vp]),
             "orc_reuse_bytes": (u64, [u64, u32, u64, i32, u64]),
@@ -108,6 +109,17 @@ def _u16(x) -> np.ndarray:
         import torch
         x = x.detach().cpu().contiguous().view(torch.int16).numpy()
     return np.ascontiguousarray(x).view(np.uint16)
+
+
+def _map(fn, items, threads: int):
+    """fn over items, on `threads` host threads when > 1 (the C calls release
+    the GIL; every item touches disjoint parts of the arrays)."""
+    items = list(items)
+    if threads <= 1 or len(items) <= 1:
+        return [fn(i) for i in items]
+    from concurrent.futures import ThreadPoolExecutor
+    with ThreadPoolExecutor(max_workers=min(threads, len(items))) as ex:
+        return list(ex.map(fn, items))
 
 
 # ----------------------------------------------------------------- geometry
@@ -163,25 +175,59 @@ def window_from_var(var: float) -> int:
 
 # ----------------------------------------------------------------- code3
 
-def code3_encode(x, W: int, E0: int) -> Tuple[np.ndarray, np.ndarray, int]:
-    """-> (slots u8[W*slot], sizes u64[W], slot_bytes)"""
+def code3_encode(x, W: int, E0: int, threads: int = 1) -> Tuple[np.ndarray, np.ndarray, int]:
+    """-> (slots u8[W*slot], sizes u64[W], slot_bytes).  With threads > 1 the
+    chunks are encoded by separate single-threaded oracle calls, `threads`
+    at a time (same bytes)."""
     x = _u16(x)
     slot = code3_slot_bytes(x.size, W)
     out = np.zeros(W * slot, dtype=np.uint8)
     sizes = np.zeros(W, dtype=np.uint64)
-    rc = lib().orc_code3_encode(_p(x), x.size, W, E0, _p(out), slot, _p(sizes))
-    if rc != 0:
-        raise ValueError(f"orc_code3_encode failed ({rc})")
+    if threads <= 1:
+        rc = lib().orc_code3_encode(_p(x), x.size, W, E0, _p(out), slot, _p(sizes))
+        if rc != 0:
+            raise ValueError(f"orc_code3_encode failed ({rc})")
+        return out, sizes, slot
+    n, L = x.size, shard_len(x.size, W)
+    buf = x if x.size else np.zeros(1, np.uint16)
+
+    def one(c):
+        size = ctypes.c_uint64(0)
+        xc = buf[min(c * L, buf.size - 1):]
+        rc = lib().orc_code3_encode_chunk(_p(xc), n, W, c, E0, _p(out[c * slot:(c + 1) * slot]),
+                                          slot, ctypes.byref(size))
+        if rc != 0:
+            raise ValueError(f"orc_code3_encode_chunk failed ({rc})")
+        sizes[c] = size.value
+
+    _map(one, range(W), threads)
     return out, sizes, slot
 
 
-def code3_decode(buf: np.ndarray, offsets: np.ndarray, n: int, W: int
+def code3_decode(buf: np.ndarray, offsets: np.ndarray, n: int, W: int, threads: int = 1
                  ) -> Tuple[np.ndarray, int]:
+    """Decode W chunks laid at offsets (W+1 entries).  With threads > 1 each
+    chunk is a separate oracle call, `threads` at a time."""
     buf = np.ascontiguousarray(buf, dtype=np.uint8)
     offsets = np.ascontiguousarray(offsets, dtype=np.uint64)
     out = np.zeros(max(n, 1), dtype=np.uint16)
-    st = lib().orc_code3_decode(_p(buf), _p(offsets), n, W, _p(out))
-    return out[:n], int(st)
+    if threads <= 1:
+        st = lib().orc_code3_decode(_p(buf), _p(offsets), n, W, _p(out))
+        return out[:n], int(st)
+    L = shard_len(n, W)
+
+    def one(c):
+        a, b = int(offsets[c]), int(offsets[c + 1])
+        if b < a:
+            return BAD_SIZE
+        dst = out[min(c * L, out.size - 1):]
+        src = buf[min(a, buf.size - 1):]
+        return int(lib().orc_code3_decode_chunk(_p(src), b - a, n, W, c, _p(dst)))
+
+    status = 0
+    for s in _map(one, range(W), threads):
+        status |= s
+    return out[:n], status
 
 
 def code3_decode_chunk(chunk: np.ndarray, n: int, W: int, c: int) -> Tuple[np.ndarray, int]:
@@ -284,28 +330,54 @@ def gather_decode_reuse(recv: np.ndarray, offsets: np.ndarray, n: int, W: int, B
 
 
 def reuse_encode_all(x, W: int, B: int, cache: np.ndarray, cold: bool = False,
-                     coded: bool = False, window_mode: int = 0):
-    """Encode all W shards of x (cache u8[n] holds every shard's sender cache).
-    -> (slots u8[W*slot], sizes u64[W], slot, [stats per shard or None])"""
+                     coded: bool = False, window_mode: int = 0, threads: int = 1):
+    """Encode all W shards of x (cache u8[n] holds every shard's sender cache),
+    one independent single-threaded oracle call per shard, `threads` shards at
+    a time.  -> (slots u8[W*slot], sizes u64[W], slot, [stats per shard or None])"""
     x = _u16(x)
     n = x.size
     L = shard_len(n, W)
     slot = reuse_slot_bytes(n, W, B, coded)
     slots = np.zeros(W * slot, dtype=np.uint8)
     sizes = np.zeros(W, dtype=np.uint64)
-    sts = []
-    for r in range(W):
+
+    def one(r):
         a = min(r * L, n)
         b = min(a + L, n) if a < n else n
-        c = cache[a:b] if b > a else np.zeros(0, np.uint8)
-        cc = np.ascontiguousarray(c)
+        cc = cache[a:b] if b > a else np.zeros(0, np.uint8)
         pay, st = reuse_encode(x[a:b], B, r, cc, cold, coded, window_mode)
-        if b > a:
-            cache[a:b] = cc
         slots[r * slot:r * slot + pay.size] = pay
         sizes[r] = pay.size
-        sts.append(st)
+        return st
+
+    sts = _map(one, range(W), threads)
     return slots, sizes, slot, sts
+
+
+def reuse_decode_all(slots: np.ndarray, sizes, slot: int, n: int, W: int, B: int,
+                     cache: np.ndarray, threads: int = 1) -> Tuple[np.ndarray, int]:
+    """Decode payload r (at slots[r*slot], sizes[r] bytes) of every shard into
+    the full tensor against the receiver cache u8[n] (updated in place), one
+    oracle call per shard, `threads` shards at a time.  -> (values, OR of the
+    shards' status words)"""
+    L = shard_len(n, W)
+    out = np.zeros(n, dtype=np.uint16)
+
+    def one(r):
+        a = min(r * L, n)
+        b = min(a + L, n) if a < n else n
+        size = int(sizes[r])
+        pay = slots[r * slot:r * slot + size]
+        cc = cache[a:b] if b > a else np.zeros(0, np.uint8)
+        vals, st = reuse_decode(pay, b - a, B, r, cc if cc.size else np.zeros(1, np.uint8))
+        out[a:b] = vals
+        return st
+
+    sts = _map(one, range(W), threads)
+    status = 0
+    for s in sts:
+        status |= s
+    return out, status
 
 
 # ----------------------------------------------------------------- FP8

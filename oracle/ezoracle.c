@@ -293,46 +293,56 @@ uint64_t orc_code3_slot_bytes(uint64_t n, uint32_t W)
     return orc_code3_chunk_bytes(L, L);
 }
 
+/* Chunk c of an n-value tensor split W ways: its n_c values at xc, encoded
+ * into o (slot_bytes available); the chunk's size goes to *size. */
+int orc_code3_encode_chunk(const uint16_t* xc, uint64_t n, uint32_t W, uint32_t c, uint32_t E0,
+                           uint8_t* o, uint64_t slot_bytes, uint64_t* size)
+{
+    if (W == 0 || c >= W || E0 > 249) return -1;
+    uint64_t n_c = orc_shard_count(n, W, c);
+    uint64_t n_esc = 0;
+    for (uint64_t j = 0; j < n_c; j++)
+        if (code_of(bf16_exp(xc[j]), E0) == 0) n_esc++;
+    uint64_t bytes = orc_code3_chunk_bytes(n_c, n_esc);
+    if (bytes > slot_bytes) return -2;
+    memset(o, 0, bytes);
+    o[0] = 'E'; o[1] = 'Z'; o[2] = 'C'; o[3] = '3';
+    o[4] = 2;
+    o[5] = (uint8_t)E0;
+    put_u64(o + 8, n_c);
+    put_u64(o + 16, n_esc);
+    put_u64(o + 24, bytes);
+    put_u32(o + 32, c);
+    put_u32(o + 36, W);
+    uint64_t off_sm = 128;
+    uint64_t plane = round_up(ceil_div(n_c, 8), 128);
+    uint64_t off_p = off_sm + round_up(n_c, 128);
+    uint64_t off_i = off_p + 3 * plane;
+    uint64_t off_e = off_i + round_up(8 * ceil_div(n_c, IDX_SPAN), 128);
+    uint64_t k = 0;
+    for (uint64_t j = 0; j < n_c; j++) {
+        uint16_t h = xc[j];
+        if (j % IDX_SPAN == 0) put_u64(o + off_i + 8 * (j / IDX_SPAN), k);
+        unsigned E = bf16_exp(h);
+        unsigned code = code_of(E, E0);
+        o[off_sm + j] = bf16_sm(h);
+        for (unsigned p = 0; p < 3; p++)
+            if ((code >> p) & 1u) o[off_p + p * plane + j / 8] |= (uint8_t)(1u << (j % 8));
+        if (code == 0) o[off_e + k++] = (uint8_t)E;
+    }
+    *size = bytes;
+    return 0;
+}
+
 int orc_code3_encode(const uint16_t* x, uint64_t n, uint32_t W, uint32_t E0,
                      uint8_t* out, uint64_t slot_bytes, uint64_t* sizes)
 {
     if (W == 0 || E0 > 249) return -1;
     uint64_t L = orc_shard_len(n, W);
     for (uint32_t c = 0; c < W; c++) {
-        uint64_t n_c = orc_shard_count(n, W, c);
-        const uint16_t* xc = x + (uint64_t)c * L;
-        uint8_t* o = out + (uint64_t)c * slot_bytes;
-        uint64_t n_esc = 0;
-        for (uint64_t j = 0; j < n_c; j++)
-            if (code_of(bf16_exp(xc[j]), E0) == 0) n_esc++;
-        uint64_t bytes = orc_code3_chunk_bytes(n_c, n_esc);
-        if (bytes > slot_bytes) return -2;
-        memset(o, 0, bytes);
-        o[0] = 'E'; o[1] = 'Z'; o[2] = 'C'; o[3] = '3';
-        o[4] = 2;
-        o[5] = (uint8_t)E0;
-        put_u64(o + 8, n_c);
-        put_u64(o + 16, n_esc);
-        put_u64(o + 24, bytes);
-        put_u32(o + 32, c);
-        put_u32(o + 36, W);
-        uint64_t off_sm = 128;
-        uint64_t plane = round_up(ceil_div(n_c, 8), 128);
-        uint64_t off_p = off_sm + round_up(n_c, 128);
-        uint64_t off_i = off_p + 3 * plane;
-        uint64_t off_e = off_i + round_up(8 * ceil_div(n_c, IDX_SPAN), 128);
-        uint64_t k = 0;
-        for (uint64_t j = 0; j < n_c; j++) {
-            uint16_t h = xc[j];
-            if (j % IDX_SPAN == 0) put_u64(o + off_i + 8 * (j / IDX_SPAN), k);
-            unsigned E = bf16_exp(h);
-            unsigned code = code_of(E, E0);
-            o[off_sm + j] = bf16_sm(h);
-            for (unsigned p = 0; p < 3; p++)
-                if ((code >> p) & 1u) o[off_p + p * plane + j / 8] |= (uint8_t)(1u << (j % 8));
-            if (code == 0) o[off_e + k++] = (uint8_t)E;
-        }
-        sizes[c] = bytes;
+        int rc = orc_code3_encode_chunk(x + (uint64_t)c * L, n, W, c, E0,
+                                        out + (uint64_t)c * slot_bytes, slot_bytes, sizes + c);
+        if (rc) return rc;
     }
     return 0;
 }

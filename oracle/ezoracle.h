@@ -60,6 +60,8 @@ uint32_t orc_window_from_var(double var);
 /* code3: W per-peer chunks, chunk c written at out + c*slot_bytes */
 uint64_t orc_code3_chunk_bytes(uint64_t n_c, uint64_t n_esc);
 uint64_t orc_code3_slot_bytes(uint64_t n, uint32_t W);
+int  orc_code3_encode_chunk(const uint16_t* xc, uint64_t n, uint32_t W, uint32_t c, uint32_t E0,
+                            uint8_t* o, uint64_t slot_bytes, uint64_t* size);
 int  orc_code3_encode(const uint16_t* x, uint64_t n, uint32_t W, uint32_t E0,
                       uint8_t* out, uint64_t slot_bytes, uint64_t* sizes);
 /* one chunk c (ZipCCL digest 3.2: a peer's chunk of an all-to-all) */
