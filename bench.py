@@ -54,6 +54,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true")
+    ap.add_argument("--no-moe", action="store_true",
+                    help="skip the MoE-shaped configuration legs and the 2^30-value op timings")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     return ap.parse_args()
 
@@ -319,6 +321,12 @@ def run_ours(args, world, rank, local):
     value = world * PASSES * raw / (step_ms_max * 1e-3) / 1e9
     e2e = None if args.no_e2e else run_e2e(args, world, xs, hosts, start, c3, ru, rc, s)
     extras = None if args.no_extras else run_extras(xs, n, W, flush, s, peak)
+    if extras is not None and not args.no_moe:
+        del xs, c3, ru, rc
+        torch.cuda.empty_cache()
+        extras["ops_2p30"] = run_ops_2p30(flush, s, peak)
+        torch.cuda.empty_cache()
+        extras.update(run_moe_configs(flush, s, peak))
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
         "steps": K, "warmup": Wm, "ms_per_step": round(step_ms_max, 4),
@@ -443,6 +451,205 @@ def run_extras(xs, n, W, flush, s, peak, reps=10):
     }
 
 
+def time_seq(seq, s, flush, reps, warm=2):
+    """Mean CUDA-event milliseconds of each named op; seq(r) gives the ops of
+    repetition r in order.  L2 is flushed (a 512 MiB write) before every op,
+    outside its events."""
+    tot = {}
+    for r in range(warm + reps):
+        evs = []
+        for name, fn in seq(r):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(s)
+            fn()
+            b.record(s)
+            evs.append((name, a, b))
+        torch.cuda.synchronize()
+        if r >= warm:
+            for name, a, b in evs:
+                tot[name] = tot.get(name, 0.0) + a.elapsed_time(b)
+    return {k: v / reps for k, v in tot.items()}
+
+
+def reuse_header_sums(cdc):
+    """(changed blocks, changed exponents m, payload bytes) summed over the
+    W payloads of the last reuse encode (read from the payload headers)."""
+    nc = m = 0
+    for r in range(cdc.W):
+        h = cdc.out[r * cdc.slot:r * cdc.slot + 64].cpu().numpy()
+        nc += int(h[24:32].view(np.uint64)[0])
+        m += int(h[32:40].view(np.uint64)[0])
+    return nc, m, int(cdc.sizes.sum().item())
+
+
+def reuse_leg(cdc, xa, xb, s, flush, peak, reps, coded=False):
+    """Warm reuse encode and gather-decode of one plan, alternating between
+    two iterations xa and xb (each encode then sees the same changed blocks:
+    the change from xa to xb and back).  Returns timings, fractions of HBM
+    (algorithmic bytes as in the step) and the compression figures."""
+    n = cdc.n
+    cdc.encode_reuse(xb, cold=True)
+    cdc.gather_decode()
+    xs = (xa, xb)
+    t = time_seq(lambda r: [("enc", lambda: cdc.encode_reuse(xs[r % 2])),
+                            ("dec", lambda: cdc.gather_decode())], s, flush, reps)
+    last = xs[(reps + 2 - 1) % 2]
+    torch.cuda.synchronize()
+    ok = cdc.status_word() == 0 and torch.equal(cdc.full[:n], last)
+    nc, m, size = reuse_header_sums(cdc)
+    raw = 2 * n
+    a_enc = raw + n + size + m
+    a_dec = size + (n - m) + raw + m
+    nb = sum(-(-max(0, min(cdc.L, n - r * cdc.L)) // cdc.B) for r in range(cdc.W))
+    g_enc = a_enc / (t["enc"] * 1e-3) / 1e9
+    g_dec = a_dec / (t["dec"] * 1e-3) / 1e9
+    return {"encode_ms": round(t["enc"], 4), "gather_decode_ms": round(t["dec"], 4),
+            "encode_uncompressed_GBs": round(raw / (t["enc"] * 1e-3) / 1e9, 1),
+            "gather_decode_uncompressed_GBs": round(raw / (t["dec"] * 1e-3) / 1e9, 1),
+            "encode_frac": round(g_enc / peak, 3), "gather_decode_frac": round(g_dec / peak, 3),
+            "reuse_rate": round(1 - nc / max(nb, 1), 4), "exp_change_values": m,
+            "ratio": round(raw / size, 4), "verified": bool(ok)}
+
+
+def run_ops_2p30(flush, s, peak, reps=5):
+    """The step's seven ops at 2^30 values (the benchmark tensor's recipe at
+    16x the size: N(0, 0.02), 0.5% x100, 0.1% zeros, W = 8, B = 256, flips
+    at c = 0.003), alternating between two iterations."""
+    import synth
+    from lossless_bf16_exponent_codec_gb300 import binding as Bd
+    from lossless_bf16_exponent_codec_gb300.codec import Codec
+    n, W, B = 1 << 30, W_CHUNKS, B_BLOCK
+    xa = synth.config2(n, device="cuda")
+    xb = synth.scale_drift_bench(xa, 1, rate=FLIP_RATE)
+    raw = 2 * n
+    c3 = Codec(n, W)
+    res = {}
+    t = time_seq(lambda r: [("stats", lambda: c3.stats(xa)), ("enc", lambda: c3.encode_code3(xa)),
+                            ("dec", lambda: c3.gather_decode())], s, flush, reps)
+    torch.cuda.synchronize()
+    ok3 = c3.status_word() == 0 and torch.equal(c3.full[:n], xa)
+    size3 = int(c3.sizes.sum().item())
+    for name, ms, alg in (("stats", t["stats"], raw), ("code3_encode", t["enc"], raw + size3),
+                          ("code3_decode", t["dec"], size3 + raw)):
+        gbs = alg / (ms * 1e-3) / 1e9
+        res[name] = {"ms": round(ms, 4), "hbm_GBs": round(gbs, 1), "frac": round(gbs / peak, 3),
+                     "uncompressed_GBs": round(raw / (ms * 1e-3) / 1e9, 1)}
+    res["code3_ratio"] = round(raw / size3, 4)
+    del c3
+    torch.cuda.empty_cache()
+    for name, codec in (("reuse", Bd.EZ_CODEC_REUSE), ("reuse_code3", Bd.EZ_CODEC_REUSE_CODE3)):
+        cdc = Codec(n, W, B, codec)
+        leg = reuse_leg(cdc, xa, xb, s, flush, peak, reps)
+        res[name + "_encode"] = {"ms": leg["encode_ms"], "frac": leg["encode_frac"],
+                                 "uncompressed_GBs": leg["encode_uncompressed_GBs"]}
+        res[name + "_decode"] = {"ms": leg["gather_decode_ms"], "frac": leg["gather_decode_frac"],
+                                 "uncompressed_GBs": leg["gather_decode_uncompressed_GBs"]}
+        res[name + "_ratio"] = leg["ratio"]
+        ok3 = ok3 and leg["verified"]
+        del cdc
+        torch.cuda.empty_cache()
+    res["verified"] = bool(ok3)
+    res["n"] = n
+    return res
+
+
+def run_moe_configs(flush, s, peak, reps=4):
+    """Timing legs on the MoE-shaped configurations (beside the step):
+    config 3 (OLMoE-1B-7B-shaped layer set, 522,588,160 values, W = 1) per
+    block size, with the reuse rate per weight category; config 4 (one
+    DeepSeek-MoE-16B-shaped layer, 587,862,016 values, B = 128) per gather
+    width W; config 5 (2^30 values in the config-3 mix, W = 8, B = 256,
+    changed exponents 3-bit coded) over its 20 drift iterations."""
+    import synth
+    from lossless_bf16_exponent_codec_gb300 import binding as Bd
+    from lossless_bf16_exponent_codec_gb300.codec import Codec
+    out = {}
+    # ---- config 3
+    x0 = synth.config3_base(device="cuda")
+    x1 = synth.config3_step(x0)
+    n = x0.numel()
+    segs = synth.olmoe_segments()
+    cat = []
+    pos = 0
+    for sg in segs:
+        cat.append((sg.category, pos, pos + sg.numel))
+        pos += sg.numel
+    c3 = {"workload": "olmoe_1b7b_layer_set_522M_w1_clustered_flips", "n": n, "per_B": {}}
+    for B in (64, 128, 256, 512, 1024):
+        cdc = Codec(n, 1, B, Bd.EZ_CODEC_REUSE)
+        leg = reuse_leg(cdc, x0, x1, s, flush, peak, reps)
+        nb = -(-n // B)
+        bm = cdc.out[64:64 + (nb + 7) // 8]
+        bits = ((bm.to(torch.int32).unsqueeze(1) >> torch.arange(8, device="cuda")) & 1).flatten()[:nb]
+        starts = torch.arange(nb, device="cuda", dtype=torch.int64) * B
+        per = {}
+        for name in ("expert_ffn", "attention", "router", "norm", "embedding"):
+            mask = torch.zeros(nb, dtype=torch.bool, device="cuda")
+            for c, a, b in cat:
+                if c == name:
+                    mask |= (starts >= a) & (starts < b)
+            k = int(mask.sum().item())
+            per[name] = round(1 - int(bits[mask].sum().item()) / k, 4) if k else None
+        leg["reuse_rate_by_category"] = per
+        c3["per_B"][str(B)] = leg
+        del cdc
+        torch.cuda.empty_cache()
+    out["config3_block_sweep"] = c3
+    del x0, x1
+    torch.cuda.empty_cache()
+    # ---- config 4
+    x0, x1 = synth.config4_layer(0, device="cuda")
+    n = x0.numel()
+    c4 = {"workload": "deepseek_moe_16b_layer_588M_b128", "n": n, "per_W": {}}
+    for W in (4, 8, 16, 32):
+        cdc = Codec(n, W, 128, Bd.EZ_CODEC_REUSE)
+        c4["per_W"][str(W)] = reuse_leg(cdc, x0, x1, s, flush, peak, reps)
+        del cdc
+        torch.cuda.empty_cache()
+    out["config4_gather_widths"] = c4
+    del x0, x1
+    torch.cuda.empty_cache()
+    # ---- config 5
+    n, W, B = 1 << 30, 8, 256
+    cdc = Codec(n, W, B, Bd.EZ_CODEC_REUSE_CODE3)
+    x = synth.config5_base(device="cuda")
+    cdc.encode_reuse(x, cold=True)
+    cdc.gather_decode()
+    raw = 2 * n
+    its = []
+    ok = True
+    for t in range(1, 21):
+        x = synth.config5_step(x, t)
+        tm = time_seq(lambda r: [("enc", lambda: cdc.encode_reuse(x)),
+                                 ("dec", lambda: cdc.gather_decode())], s, flush, 1, warm=0)
+        torch.cuda.synchronize()
+        ok = ok and cdc.status_word() == 0 and torch.equal(cdc.full[:n], x)
+        nc, m, size = reuse_header_sums(cdc)
+        a_enc = raw + n + size + m
+        a_dec = size + (n - m) + raw + m
+        its.append({"t": t, "encode_ms": round(tm["enc"], 4), "gather_decode_ms": round(tm["dec"], 4),
+                    "GBs": round(2 * raw / ((tm["enc"] + tm["dec"]) * 1e-3) / 1e9, 1),
+                    "encode_frac": round(a_enc / (tm["enc"] * 1e-3) / 1e9 / peak, 3),
+                    "gather_decode_frac": round(a_dec / (tm["dec"] * 1e-3) / 1e9 / peak, 3),
+                    "ratio": round(raw / size, 4), "exp_change_values": m})
+    del cdc, x
+    torch.cuda.empty_cache()
+
+    def mean(key, sel):
+        v = [i[key] for i in its if sel(i["t"])]
+        return round(sum(v) / len(v), 4)
+    out["config5_sustained"] = {
+        "workload": "olmoe_mix_2p30_w8_b256_reuse_code3_20_iterations", "n": n,
+        "GBs_definition": "two codec passes (encode, gather-decode) x 2n bytes / (encode + decode time)",
+        "iterations": its, "verified": bool(ok),
+        "mean_GBs_flip_0.08pct": mean("GBs", lambda t: t <= 10),
+        "mean_GBs_flip_0.4pct": mean("GBs", lambda t: t > 10),
+        "mean_ratio_flip_0.08pct": mean("ratio", lambda t: t <= 10),
+        "mean_ratio_flip_0.4pct": mean("ratio", lambda t: t > 10)}
+    return out
+
+
 def pinned_inputs(args, xs):
     """The e2e inputs in pinned host memory, made once before any timing and
     touched twice by the device (a pipeline reuses its pinned staging
@@ -530,11 +737,40 @@ def run_e2e(args, world, xs, hosts, start, c3, ru, rc, s):
 
 # ------------------------------------------------------------------ oracle
 
-def oracle_sample(seconds: float, n_sample: int = 1 << 22):
-    """The CPU oracle, single-threaded, on the first n_sample values of the
-    workload (W = 8), through the same six passes, iteration after iteration
-    until `seconds` of oracle work.  Drawing each iteration's flips is not
-    timed.  Returns (iterations, seconds, n_sample)."""
+def cpu_desc() -> dict:
+    """CPU model and the number of host cores this process may use."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if model is None:
+        try:
+            for line in open("/proc/cpuinfo"):
+                if line.lower().startswith("model name"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+        except OSError:
+            pass
+    try:
+        nproc = len(os.sched_getaffinity(0))
+    except AttributeError:
+        nproc = os.cpu_count() or 1
+    return {"cpu_model": model or "unknown", "nproc": nproc}
+
+
+def oracle_sample(seconds: float, n_sample: int = 1 << 22, threads: int = 1):
+    """The CPU oracle on the first n_sample values of the workload (W = 8),
+    through the same six passes, iteration after iteration until `seconds`
+    of oracle work.  threads = 1: the oracle as written, one call per pass.
+    threads > 1: the per-shard and per-chunk calls of the passes run on that
+    many host threads (shards are independent); the tensor-wide statistics
+    stay one call.  Drawing each iteration's flips is not timed.  Returns
+    (iterations, seconds, n_sample)."""
     import oracle
     import synth
     oracle.build()
@@ -544,32 +780,45 @@ def oracle_sample(seconds: float, n_sample: int = 1 << 22):
     x0 = cur.numpy().view(np.uint16)
     for coded, (send, recv) in caches.items():          # cold iteration, untimed
         sl, sz, slot, _ = oracle.reuse_encode_all(x0, W, B, send, cold=True, coded=coded)
-        rb, of = oracle.compact(sl, sz, slot)
-        oracle.gather_decode_reuse(rb, of, n_sample, W, B, recv)
+        oracle.reuse_decode_all(sl, sz, slot, n_sample, W, B, recv)
     iters, busy = 0, 0.0
     while busy < seconds:
         cur = synth.scale_drift_bench(cur, iters + 1, rate=FLIP_RATE)
         xn = cur.numpy().view(np.uint16)
         t = time.perf_counter()
         st = oracle.stats(xn)
-        sl, sz, slot = oracle.code3_encode(xn, W, st["E0"])
+        sl, sz, slot = oracle.code3_encode(xn, W, st["E0"], threads=threads)
         rb, of = oracle.compact(sl, sz, slot)
-        oracle.code3_decode(rb, of, n_sample, W)
+        oracle.code3_decode(rb, of, n_sample, W, threads=threads)
         for coded, (send, recv) in caches.items():
-            sl, sz, slot, _ = oracle.reuse_encode_all(xn, W, B, send, coded=coded)
-            rb, of = oracle.compact(sl, sz, slot)
-            oracle.gather_decode_reuse(rb, of, n_sample, W, B, recv)
+            sl, sz, slot, _ = oracle.reuse_encode_all(xn, W, B, send, coded=coded, threads=threads)
+            if threads > 1:
+                oracle.reuse_decode_all(sl, sz, slot, n_sample, W, B, recv, threads=threads)
+            else:
+                rb, of = oracle.compact(sl, sz, slot)
+                oracle.gather_decode_reuse(rb, of, n_sample, W, B, recv)
         busy += time.perf_counter() - t
         iters += 1
     return iters, busy, n_sample
 
 
 def cpu_baseline(seconds: float) -> dict:
+    host = cpu_desc()
     iters, elapsed, ns = oracle_sample(seconds)
     gbs = PASSES * 2 * ns * iters / elapsed / 1e9
-    return {"value": round(gbs, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+    line = {"value": round(gbs, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
             "sample": f"first {ns} values of the workload (W=8, B=256), {iters} iterations "
-                      f"through the six passes, {elapsed:.1f} s of oracle time"}
+                      f"through the six passes, {elapsed:.1f} s of oracle time",
+            "cpu_model": host["cpu_model"], "nproc": host["nproc"]}
+    th = max(1, min(W_CHUNKS, host["nproc"]))
+    if th > 1:
+        it2, el2, ns2 = oracle_sample(seconds / 2, n_sample=1 << 23, threads=th)
+        line["cpu_shards"] = {
+            "value": round(PASSES * 2 * ns2 * it2 / el2 / 1e9, 4), "unit": UNIT, "cores": th,
+            "kind": "oracle, one call per shard or chunk on parallel host threads",
+            "sample": f"first {ns2} values of the workload (W=8, B=256), {it2} iterations through "
+                      f"the six passes, {el2:.1f} s; the tensor-wide statistics pass is one call"}
+    return line
 
 
 def run_reference(args, world, rank):
