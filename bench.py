@@ -327,6 +327,8 @@ def run_ours(args, world, rank, local):
         extras["ops_2p30"] = run_ops_2p30(flush, s, peak)
         torch.cuda.empty_cache()
         extras.update(run_moe_configs(flush, s, peak))
+        torch.cuda.empty_cache()
+        extras["fp8"] = run_fp8(flush, s, peak)
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
         "steps": K, "warmup": Wm, "ms_per_step": round(step_ms_max, 4),
@@ -648,6 +650,37 @@ def run_moe_configs(flush, s, peak, reps=4):
         "mean_ratio_flip_0.08pct": mean("ratio", lambda t: t <= 10),
         "mean_ratio_flip_0.4pct": mean("ratio", lambda t: t > 10)}
     return out
+
+
+def run_fp8(flush, s, peak, reps=5):
+    """The 3-bit exponent code on FP8 (E5M2, E4M3): statistics, encode and
+    gather-decode of 2^28 values from N(0, 1) (E5M2) and N(0, 16^2) (E4M3),
+    W = 8.  Algorithmic bytes: n read (statistics); n read + payload written
+    (encode); payload read + n written (decode)."""
+    import synth
+    from lossless_bf16_exponent_codec_gb300 import binding as Bd
+    from lossless_bf16_exponent_codec_gb300.codec import Fp8Codec
+    n, W = 1 << 28, W_CHUNKS
+    res = {"n": n, "W": W}
+    for fmt, codec, sigma in (("e5m2", Bd.EZ_CODEC_FP8_E5M2, 1.0), ("e4m3", Bd.EZ_CODEC_FP8_E4M3, 16.0)):
+        x = synth.fp8_gaussian(n, sigma, fmt, device="cuda")
+        c = Fp8Codec(n, W, codec)
+        t = time_seq(lambda r: [("stats", lambda: c.stats(x)), ("enc", lambda: c.encode(x)),
+                                ("dec", lambda: c.gather_decode())], s, flush, reps)
+        torch.cuda.synchronize()
+        ok = c.status_word() == 0 and torch.equal(c.full[:n], x)
+        size = int(c.sizes.sum().item())
+        leg = {"ratio": round(n / size, 4), "bytes_per_value": round(size / n, 4), "verified": bool(ok),
+               "E0": c.stats_of()["E0"], "escape_rate": round(c.stats_of()["n_escape"] / n, 5)}
+        for name, key, alg in (("stats", "stats", n), ("encode", "enc", n + size), ("decode", "dec", size + n)):
+            ms = t[key]
+            gbs = alg / (ms * 1e-3) / 1e9
+            leg[name] = {"ms": round(ms, 4), "hbm_GBs": round(gbs, 1), "frac": round(gbs / peak, 3),
+                         "uncompressed_GBs": round(n / (ms * 1e-3) / 1e9, 1)}
+        res[fmt] = leg
+        del c, x
+        torch.cuda.empty_cache()
+    return res
 
 
 def pinned_inputs(args, xs):

@@ -87,7 +87,9 @@ typedef enum {
 typedef enum {
     EZ_CODEC_CODE3 = 1,        /* ZipCCL 3-bit exponent code                     */
     EZ_CODEC_REUSE = 2,        /* CIERA exponent reuse, raw changed exponents    */
-    EZ_CODEC_REUSE_CODE3 = 3   /* CIERA reuse, changed exponents 3-bit coded     */
+    EZ_CODEC_REUSE_CODE3 = 3,  /* CIERA reuse, changed exponents 3-bit coded     */
+    EZ_CODEC_FP8_E5M2 = 4,     /* 3-bit exponent code on FP8 E5M2 values         */
+    EZ_CODEC_FP8_E4M3 = 5      /* 3-bit exponent code on FP8 E4M3 values         */
 } ez_codec;
 
 /* bits OR-ed into a decoder's device status word */
@@ -241,11 +243,77 @@ ez_status ez_decode_reuse(ez_plan p, const uint8_t* d_payload, uint64_t payload_
  * one launch.  Payload r occupies d_recv[d_offsets[r] .. d_offsets[r+1])
  * (W+1 device offsets).  Shard r is written to d_full_out + r*L.  For the
  * reuse codecs d_recv_cache is the receiver's full n-byte exponent cache;
- * for code3 it is ignored (may be NULL).  ZipCCL digest 3.2 zipcclAllGather
+ * for code3 and the FP8 codecs it is ignored (may be NULL); an FP8 plan
+ * writes n bytes (d_full_out is then the FP8 tensor's bytes).  ZipCCL digest 3.2 zipcclAllGather
  * ("decompress all"); CIERA Decmp (the only codec step on the critical path). */
 ez_status ez_gather_decode(ez_plan p, const uint8_t* d_recv, const uint64_t* d_offsets,
                            uint8_t* d_recv_cache, uint16_t* d_full_out, uint32_t* d_status,
                            void* d_ws, uint64_t ws_bytes, void* stream);
+
+/* ---- FP8 ----------------------------------------------------------------
+ * ZipCCL digest 3.3, last paragraph: the 3-bit exponent code applied to FP8
+ * (E5M2 coded to 3 bits gives e = 0.75, E4M3 gives e ~ 0.88).  Formats as
+ * in the OCP 8-bit floating-point specification: E5M2 (exponent bias 15,
+ * infinities and NaN at exponent field 31) and E4M3 (bias 7, no
+ * infinities, NaN only at S.1111.111).  A plan with codec EZ_CODEC_FP8_E5M2
+ * or EZ_CODEC_FP8_E4M3 describes n FP8 values (one byte each, passed as raw
+ * bit patterns) in W chunks of L = 128*ceil(ceil(n/W)/128) values; B is
+ * ignored and EZ_FLAG_WINDOW_HIST may be set.  Each value keeps its sign
+ * and m mantissa bits raw (sm = sign << m | mantissa, stored as 1 + m bit-
+ * planes, plane q = bit q of sm); its exponent field E becomes the code
+ * E - E0 + 1 for E0 <= E <= E0+6 (three code planes) or code 0 with E
+ * appended to the chunk's escape list.
+ * Chunk layout (little-endian, all padding zero): 128-byte header {"EZF8",
+ * u8 version 1, u8 format (1 = E5M2, 2 = E4M3), u8 E0, u8 0, u64 n_c,
+ * u64 n_esc, u64 chunk_bytes, u32 chunk index, u32 W, zeros}; the 1 + m
+ * sign/mantissa planes then the 3 code planes (ceil(n_c/8) bytes each,
+ * padded to 128; bit j&7 of byte j>>3 is value j); the escape index (u64
+ * per 8192 values: escapes among the values before that point, padded to
+ * 128); the escapes (raw exponent fields in value order, padded to 128). */
+
+/* Statistics of FP8 values: as ez_stats_t, with the exact sums taken over
+ * the finite values and E0 a field value in 0 .. 2^e - 7 (25 for E5M2, 9 for
+ * E4M3): the largest e with var >= K * 2^(2(e - bias) - 1) (the integer
+ * nearest x_opt, ties up), 0 if none; when N < 2, var <= 0 or with
+ * EZ_FLAG_WINDOW_HIST, the densest 7 consecutive exponent bins (ties to the
+ * lowest), rule = 1. */
+typedef struct {
+    uint64_t hist[32];    /* count of each exponent field value (16 for E4M3)   */
+    uint64_t n;           /* values                                             */
+    uint64_t n_finite;    /* values that are neither Inf nor NaN                */
+    double s1;            /* exact sum of the finite values, rounded once       */
+    double s2;            /* exact sum of their squares, rounded once           */
+    double var;           /* (s2 - s1*(s1/N)) / (N-1); 0 when N < 2             */
+    double sigma;         /* sqrt(var); 0 when var <= 0                         */
+    double K;             /* 16383 / (14 ln 2)                                  */
+    uint32_t E0;          /* window base field value                            */
+    uint32_t rule;        /* 0 from sigma, 1 from the histogram                 */
+    uint64_t n_escape;    /* values outside the window                          */
+} ez_fp8_stats_t;
+
+/* Statistics and window of n_values FP8 values at d_x (the plan's codec
+ * fixes the format; any count up to 2^40).  Writes *d_stats (8-byte
+ * aligned device memory).  EZ_ERR_ARG for a plan that is not an FP8 plan. */
+ez_status ez_fp8_stats(ez_plan p, const uint8_t* d_x, uint64_t n_values, ez_fp8_stats_t* d_stats,
+                       void* d_ws, uint64_t ws_bytes, void* stream);
+
+/* Encode FP8 chunks [first, first+count): d_x holds those chunks' values
+ * contiguously (chunk first+i at d_x + i*L), E0 is read from d_stats->E0 on
+ * the device; chunk first+i goes to the slot d_out + i*slot_bytes and its
+ * size to d_sizes[i].  d_status receives EZ_DSTAT_TIMEOUT (a look-back wait
+ * gave up) or EZ_DSTAT_BAD_STATS (E0 above 2^e - 7; encoded with E0 = 0). */
+ez_status ez_fp8_encode(ez_plan p, const uint8_t* d_x, uint32_t first, uint32_t count,
+                        const ez_fp8_stats_t* d_stats, uint8_t* d_out, uint64_t out_bytes,
+                        uint64_t* d_sizes, uint32_t* d_status, void* d_ws, uint64_t ws_bytes,
+                        void* stream);
+
+/* Decode FP8 chunks [first, first+count): chunk first+i occupies
+ * d_in[d_offsets[i] .. d_offsets[i+1]); its values go to d_out + i*L.  A
+ * chunk that fails its checks (header, sizes, index, escape count) is not
+ * written and sets d_status bits as the code3 decoder does. */
+ez_status ez_fp8_decode(ez_plan p, const uint8_t* d_in, const uint64_t* d_offsets, uint32_t first,
+                        uint32_t count, uint8_t* d_out, uint32_t* d_status, void* d_ws,
+                        uint64_t ws_bytes, void* stream);
 
 /* Bytes of the library's fixed device scratch array used by
  * ez_encode_code3_noalloc (one array per device). */

@@ -19,9 +19,11 @@ LIB_PATH = os.path.join(HERE, "libexpzip.so")
 EZ_OK, EZ_ERR_ARG, EZ_ERR_CUDA, EZ_ERR_CAPACITY = 0, 1, 2, 3
 EZ_ERR_CORRUPT, EZ_ERR_TIMEOUT, EZ_ERR_UNSUPPORTED = 4, 5, 6
 EZ_CODEC_CODE3, EZ_CODEC_REUSE, EZ_CODEC_REUSE_CODE3 = 1, 2, 3
+EZ_CODEC_FP8_E5M2, EZ_CODEC_FP8_E4M3 = 4, 5
 DSTAT_BAD_HEADER, DSTAT_BAD_SIZE, DSTAT_BAD_COUNT = 1, 2, 4
 DSTAT_TIMEOUT, DSTAT_MISALIGNED, DSTAT_BAD_STATS = 8, 16, 32
 STATS_BYTES = 2120          # sizeof(ez_stats_t)
+FP8_STATS_BYTES = 328       # sizeof(ez_fp8_stats_t)
 EZ_FLAG_WINDOW_HIST = 1     # plan flag: window from the histogram's densest 7-bin run
 EZ_FLAG_HASH_CACHE = 2      # plan flag: sender cache of block hash pairs (reuse, B >= 32)
 NOALLOC_SCRATCH_BYTES = 4 << 20   # EZ_NOALLOC_SCRATCH_BYTES
@@ -29,7 +31,8 @@ NOALLOC_SCRATCH_BYTES = 4 << 20   # EZ_NOALLOC_SCRATCH_BYTES
 ENTRY_POINTS = ("ez_plan_create", "ez_plan_destroy", "ez_plan_sizes", "ez_stats",
                 "ez_encode_code3", "ez_decode_code3", "ez_encode_reuse", "ez_decode_reuse",
                 "ez_gather_decode", "ez_encode_code3_noalloc", "ez_accumulate_bf16",
-                "ez_decode_code3_accumulate", "ez_status_str", "ez_version")
+                "ez_decode_code3_accumulate", "ez_fp8_stats", "ez_fp8_encode", "ez_fp8_decode",
+                "ez_status_str", "ez_version")
 
 
 class EzError(RuntimeError):
@@ -73,6 +76,9 @@ def lib():
             "ez_encode_code3_noalloc": [vp, vp, u32, u32, vp, vp, u64, vp, vp, vp],
             "ez_accumulate_bf16": [vp, vp, u64, i32, vp],
             "ez_decode_code3_accumulate": [vp, vp, vp, u32, u32, vp, i32, vp, vp, u64, vp],
+            "ez_fp8_stats": [vp, vp, u64, vp, vp, u64, vp],
+            "ez_fp8_encode": [vp, vp, u32, u32, vp, vp, u64, vp, vp, vp, u64, vp],
+            "ez_fp8_decode": [vp, vp, vp, u32, u32, vp, vp, vp, u64, vp],
         }
         for name, args in sig.items():
             f = getattr(L, name)
@@ -194,6 +200,24 @@ def ez_decode_code3_accumulate(plan, inp, offsets, first: int, count: int, acc, 
                                             _stream(stream)))
 
 
+def ez_fp8_stats(plan, x, n_values: int, stats, ws, ws_bytes: int, stream=None) -> None:
+    _check("ez_fp8_stats", lib().ez_fp8_stats(plan, _ptr(x), n_values, _ptr(stats), _ptr(ws), ws_bytes,
+                                              _stream(stream)))
+
+
+def ez_fp8_encode(plan, x, first: int, count: int, stats, out, out_bytes: int, sizes, status,
+                  ws, ws_bytes: int, stream=None) -> None:
+    _check("ez_fp8_encode", lib().ez_fp8_encode(plan, _ptr(x), first, count, _ptr(stats), _ptr(out),
+                                                out_bytes, _ptr(sizes), _ptr(status), _ptr(ws), ws_bytes,
+                                                _stream(stream)))
+
+
+def ez_fp8_decode(plan, inp, offsets, first: int, count: int, out, status, ws, ws_bytes: int,
+                  stream=None) -> None:
+    _check("ez_fp8_decode", lib().ez_fp8_decode(plan, _ptr(inp), _ptr(offsets), first, count, _ptr(out),
+                                                _ptr(status), _ptr(ws), ws_bytes, _stream(stream)))
+
+
 def ez_version() -> int:
     return int(lib().ez_version())
 
@@ -216,3 +240,20 @@ def parse_stats(raw) -> dict:
             "s2": float(d[1]), "var": float(d[2]), "sigma": float(d[3]), "K": float(d[4]),
             "E0": int(u32[0]), "rule": int(u32[1]),
             "n_escape": int(b[2112:2120].view(np.uint64)[0])}
+
+
+def parse_fp8_stats(raw) -> dict:
+    """Decode an ez_fp8_stats_t record (bytes / uint8 numpy / uint8 tensor)."""
+    if not isinstance(raw, np.ndarray):
+        try:
+            raw = raw.detach().cpu().numpy()
+        except AttributeError:
+            raw = np.frombuffer(bytes(raw), dtype=np.uint8)
+    b = np.ascontiguousarray(np.ascontiguousarray(raw, dtype=np.uint8)[:FP8_STATS_BYTES])
+    q = b[256:272].view(np.uint64)
+    d = b[272:312].view(np.float64)
+    u32 = b[312:320].view(np.uint32)
+    return {"hist": b[:256].view(np.uint64).copy(), "n": int(q[0]), "n_finite": int(q[1]),
+            "s1": float(d[0]), "s2": float(d[1]), "var": float(d[2]), "sigma": float(d[3]),
+            "K": float(d[4]), "E0": int(u32[0]), "rule": int(u32[1]),
+            "n_escape": int(b[320:328].view(np.uint64)[0])}

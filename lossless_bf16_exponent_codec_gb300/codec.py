@@ -132,3 +132,66 @@ class Codec:
             B.ez_decode_code3_accumulate(self.plan, recv[offs[s]:], one, me, 1, acc, s == 0,
                                          self.status, self.ws, self.ws_bytes, stream)
         return acc[:n_me]
+
+
+class Fp8Codec:
+    """Buffers and calls of one FP8 plan (EZ_CODEC_FP8_E5M2 / _E4M3): the
+    tensor is n FP8 values passed as their raw bytes (uint8)."""
+
+    def __init__(self, n: int, W: int, codec: int = B.EZ_CODEC_FP8_E5M2, device: str = "cuda",
+                 flags: int = 0):
+        self.n, self.W, self.codec = n, W, codec
+        self.device = torch.device(device)
+        self.plan = B.ez_plan_create(n, W, 0, codec, flags)
+        self.geom = B.ez_plan_sizes(self.plan)
+        self.L = self.geom["shard_len"]
+        self.slot = self.geom["slot_bytes"]
+        self.ws_bytes = self.geom["workspace_bytes"]
+        dev = self.device
+        self.ws = torch.zeros(max(self.ws_bytes, 256), dtype=torch.uint8, device=dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.stats_buf = torch.zeros(B.FP8_STATS_BYTES, dtype=torch.uint8, device=dev)
+        self.out = torch.zeros(W * self.slot, dtype=torch.uint8, device=dev)
+        self.sizes = torch.zeros(W, dtype=torch.int64, device=dev)
+        self.slot_offsets = (torch.arange(W + 1, dtype=torch.int64) * self.slot).to(dev)
+        self.full = torch.zeros(max(n, 16), dtype=torch.uint8, device=dev)
+
+    def __del__(self):
+        try:
+            B.ez_plan_destroy(self.plan)
+        except Exception:
+            pass
+
+    def stats(self, x: torch.Tensor, n_values: int | None = None, stream=None) -> None:
+        nv = x.numel() if n_values is None else n_values
+        B.ez_fp8_stats(self.plan, x, nv, self.stats_buf, self.ws, self.ws_bytes, stream)
+
+    def encode(self, x: torch.Tensor, first: int = 0, count: int | None = None, stream=None) -> None:
+        count = self.W - first if count is None else count
+        B.ez_fp8_encode(self.plan, x, first, count, self.stats_buf, self.out, self.out.numel(),
+                        self.sizes, self.status, self.ws, self.ws_bytes, stream)
+
+    def decode(self, inp: torch.Tensor, offsets: torch.Tensor, first: int = 0, count: int | None = None,
+               out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+        count = self.W - first if count is None else count
+        out = self.full if out is None else out
+        B.ez_fp8_decode(self.plan, inp, offsets, first, count, out, self.status, self.ws, self.ws_bytes,
+                        stream)
+        return out
+
+    def gather_decode(self, recv: torch.Tensor | None = None, offsets: torch.Tensor | None = None,
+                      out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+        recv = self.out if recv is None else recv
+        offsets = self.slot_offsets if offsets is None else offsets
+        out = self.full if out is None else out
+        B.ez_gather_decode(self.plan, recv, offsets, None, out, self.status, self.ws, self.ws_bytes, stream)
+        return out
+
+    def stats_of(self) -> dict:
+        return B.parse_fp8_stats(self.stats_buf)
+
+    def status_word(self) -> int:
+        return int(self.status.item())
+
+    def clear_status(self) -> None:
+        self.status.zero_()

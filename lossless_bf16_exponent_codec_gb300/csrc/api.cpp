@@ -19,7 +19,11 @@ bool al(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (
 constexpr uint64_t kShardInfoBytes = 64;
 constexpr uint64_t kStatsBinsBytes = 3 * 256 * 8 + 256;
 
-bool is_reuse(const ez_plan_s* p) { return p->codec != EZ_CODEC_CODE3; }
+bool is_reuse(const ez_plan_s* p)
+{
+    return p->codec == EZ_CODEC_REUSE || p->codec == EZ_CODEC_REUSE_CODE3;
+}
+bool is_fp8(const ez_plan_s* p) { return p->codec == EZ_CODEC_FP8_E5M2 || p->codec == EZ_CODEC_FP8_E4M3; }
 
 ez_status cuda_status(cudaError_t e) { return e == cudaSuccess ? EZ_OK : EZ_ERR_CUDA; }
 
@@ -58,6 +62,7 @@ WsView ws_view(const ez_plan_s* p, void* ws)
     v.seg_b = v.seg_a + segs;
     v.state_a = reinterpret_cast<unsigned long long*>(b + p->off_state_a);
     v.state_b = reinterpret_cast<unsigned long long*>(b + p->off_state_b);
+    v.ctot = p->off_ctot ? reinterpret_cast<unsigned long long*>(b + p->off_ctot) : nullptr;
     return v;
 }
 
@@ -72,8 +77,9 @@ ez_status ez_plan_create(ez_plan* out, const ez_plan_desc* d)
     if ((d->flags & ~(EZ_FLAG_WINDOW_HIST | EZ_FLAG_HASH_CACHE)) || d->W == 0 || d->W > 65536 ||
         d->n > kMaxN)
         return EZ_ERR_ARG;
-    if (d->codec < EZ_CODEC_CODE3 || d->codec > EZ_CODEC_REUSE_CODE3) return EZ_ERR_ARG;
-    const bool reuse = d->codec != EZ_CODEC_CODE3;
+    if (d->codec < EZ_CODEC_CODE3 || d->codec > EZ_CODEC_FP8_E4M3) return EZ_ERR_ARG;
+    const bool reuse = d->codec == EZ_CODEC_REUSE || d->codec == EZ_CODEC_REUSE_CODE3;
+    const bool fp8 = d->codec == EZ_CODEC_FP8_E5M2 || d->codec == EZ_CODEC_FP8_E4M3;
     const bool hash = (d->flags & EZ_FLAG_HASH_CACHE) != 0;
     if (hash && !reuse) return EZ_ERR_ARG;
     if (reuse) {
@@ -94,7 +100,9 @@ ez_status ez_plan_create(ez_plan* out, const ez_plan_desc* d)
     p->tpc = (uint32_t)tpc;
     const uint64_t L = p->L;
     const uint64_t spans = cdiv(L, kTileValues);   // index entries per shard
-    if (!reuse) {
+    if (fp8) {
+        p->slot_bytes = ezk::fp8_slot_bytes(d->codec, L);
+    } else if (!reuse) {
         p->slot_bytes = 128 + L + 3 * rup(cdiv(L, 8), 128) + rup(8 * spans, 128) + L;
     } else {
         const uint64_t nb = cdiv(L, p->B);
@@ -129,10 +137,17 @@ ez_status ez_plan_create(ez_plan* out, const ez_plan_desc* d)
     p->off_hbm = off;
     off = rup(off + W * p->hwords * 4ull, 256);
     p->zero_bytes = off;
+    // code3: per-CTA escape totals of the grid-barrier encoder and a staging
+    // slot of 8192 + 16 bytes per tile for escapes that do not fit the CTA's
+    // shared staging area (neither needs clearing: every entry is written
+    // before it is read)
+    const bool code3 = d->codec == EZ_CODEC_CODE3;
+    p->off_ctot = code3 ? off : 0;
+    off = rup(off + (code3 ? ezk::kMaxGridCtas * 8 : 0), 256);
     // coded reuse: each tile's escapes staged at its own offset, its planes
     // in 3 KB per tile
-    p->off_escbuf = coded ? off : 0;
-    off = rup(off + (coded ? W * L : 0), 256);
+    p->off_escbuf = (coded || code3) ? off : 0;
+    off = rup(off + (coded ? W * L : (code3 ? W * tpc * (kTileValues + 16) : 0)), 256);
     p->off_plbuf = coded ? off : 0;
     off = rup(off + (coded ? W * tpc * 3 * (kTileValues / 8) : 0), 256);
     p->ws_bytes = off;
@@ -269,6 +284,55 @@ ez_status ez_accumulate_bf16(float* d_acc, const uint16_t* d_x, uint64_t n, int 
     return cuda_status(ezk::launch_accumulate_bf16(d_acc, d_x, n, first, static_cast<cudaStream_t>(stream)));
 }
 
+ez_status ez_fp8_stats(ez_plan p, const uint8_t* d_x, uint64_t n_values, ez_fp8_stats_t* d_stats,
+                       void* d_ws, uint64_t ws_bytes, void* stream)
+{
+    if (!p || !is_fp8(p) || !d_stats || !al(d_stats, 8) || n_values > kMaxN) return EZ_ERR_ARG;
+    if (n_values && (!d_x || !al(d_x, 16))) return EZ_ERR_ARG;
+    ez_status s = check_ws(p, d_ws, ws_bytes);
+    if (s != EZ_OK) return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    s = clear_ws(d_ws, p->off_state_a, st);
+    if (s != EZ_OK) return s;
+    return cuda_status(ezk::launch_fp8_stats(p, d_x, n_values, d_stats, ezk::ws_view(p, d_ws), st));
+}
+
+ez_status ez_fp8_encode(ez_plan p, const uint8_t* d_x, uint32_t first, uint32_t count,
+                        const ez_fp8_stats_t* d_stats, uint8_t* d_out, uint64_t out_bytes,
+                        uint64_t* d_sizes, uint32_t* d_status, void* d_ws, uint64_t ws_bytes,
+                        void* stream)
+{
+    if (!p || !is_fp8(p)) return EZ_ERR_ARG;
+    if (count == 0 || first >= p->W || count > p->W - first) return EZ_ERR_ARG;
+    if (!d_stats || !al(d_stats, 8) || !d_out || !al(d_out, 16) || !d_sizes || !al(d_sizes, 8) ||
+        !d_status || !al(d_status, 4))
+        return EZ_ERR_ARG;
+    if (p->n && (!d_x || !al(d_x, 16))) return EZ_ERR_ARG;
+    if (out_bytes / p->slot_bytes < count) return EZ_ERR_CAPACITY;
+    ez_status s = check_ws(p, d_ws, ws_bytes);
+    if (s != EZ_OK) return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    s = clear_ws(d_ws, p->zero_bytes, st);
+    if (s != EZ_OK) return s;
+    return cuda_status(ezk::launch_fp8_encode(p, d_x, first, count, d_stats, d_out, d_sizes, d_status,
+                                              ezk::ws_view(p, d_ws), st));
+}
+
+ez_status ez_fp8_decode(ez_plan p, const uint8_t* d_in, const uint64_t* d_offsets, uint32_t first,
+                        uint32_t count, uint8_t* d_out, uint32_t* d_status, void* d_ws,
+                        uint64_t ws_bytes, void* stream)
+{
+    if (!p || !is_fp8(p)) return EZ_ERR_ARG;
+    if (count == 0 || first >= p->W || count > p->W - first) return EZ_ERR_ARG;
+    if (!d_in || !al(d_in, 16) || !d_offsets || !al(d_offsets, 8) || !d_status || !al(d_status, 4))
+        return EZ_ERR_ARG;
+    if (p->n && (!d_out || !al(d_out, 16))) return EZ_ERR_ARG;
+    ez_status s = check_ws(p, d_ws, ws_bytes);
+    if (s != EZ_OK) return s;
+    return cuda_status(ezk::launch_fp8_decode(p, d_in, d_offsets, first, count, d_out, d_status,
+                                              static_cast<cudaStream_t>(stream)));
+}
+
 ez_status ez_gather_decode(ez_plan p, const uint8_t* d_recv, const uint64_t* d_offsets,
                            uint8_t* d_recv_cache, uint16_t* d_full_out, uint32_t* d_status, void* d_ws,
                            uint64_t ws_bytes, void* stream)
@@ -283,6 +347,9 @@ ez_status ez_gather_decode(ez_plan p, const uint8_t* d_recv, const uint64_t* d_o
     if (s != EZ_OK) return s;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const ezk::WsView w = ezk::ws_view(p, d_ws);
+    if (is_fp8(p))
+        return cuda_status(ezk::launch_fp8_decode(p, d_recv, d_offsets, 0, p->W,
+                                                  reinterpret_cast<uint8_t*>(d_full_out), d_status, st));
     if (!is_reuse(p))
         return cuda_status(
             ezk::launch_code3_decode(p, d_recv, d_offsets, 0, p->W, d_full_out, d_status, w, st));
@@ -304,6 +371,6 @@ const char* ez_status_str(ez_status s)
     return "unknown status";
 }
 
-uint32_t ez_version(void) { return 0x000200u; }
+uint32_t ez_version(void) { return 0x000300u; }
 
 }  // extern "C"

@@ -397,6 +397,17 @@ def config5_step(bits: torch.Tensor, t: int, seed: int = 5) -> torch.Tensor:
     return flip_exponents(bits, rate, key_of(seed, 100 + t))
 
 
+def fp8_gaussian(n: int, sigma: float, fmt: str, seed: int = 6, device="cpu",
+                 mean: float = 0.0) -> torch.Tensor:
+    """n FP8 values (raw bytes, uint8) of mean + sigma*z, z the counter-based
+    normals of ``key_of(seed, 8)``, rounded to float32 and then to the FP8
+    format ('e5m2' or 'e4m3', torch's round-to-nearest-even casts; E4M3 is
+    the OCP E4M3 with no infinities)."""
+    z = normal(key_of(seed, 8), torch.arange(n, dtype=torch.int64, device=device))
+    dt = torch.float8_e5m2 if fmt == "e5m2" else torch.float8_e4m3fn
+    return (z * sigma + mean).to(torch.float32).to(dt).view(torch.uint8)
+
+
 def pow2_bf16(e: int, negative: bool = False) -> int:
     """BF16 bits of +-2^e for a normal exponent e (-126 <= e <= 127)."""
     assert -126 <= e <= 127

@@ -53,7 +53,12 @@ def test_plan_validation(B):
         with pytest.raises(E) as ei:
             B.ez_plan_create(1000, 2, bb, B.EZ_CODEC_REUSE)
         assert ei.value.status == B.EZ_ERR_UNSUPPORTED
-    assert B.ez_version() == 0x000200
+    assert B.ez_version() == 0x000300
+    for codec in (B.EZ_CODEC_FP8_E5M2, B.EZ_CODEC_FP8_E4M3):
+        with pytest.raises(E) as ei:
+            B.ez_plan_create(10, 1, 0, codec, B.EZ_FLAG_HASH_CACHE)
+        assert ei.value.status == B.EZ_ERR_ARG
+        B.ez_plan_destroy(B.ez_plan_create(10, 1, 0, codec, B.EZ_FLAG_WINDOW_HIST))
     assert B.status_str(0) == "ok"
 
 
@@ -73,6 +78,14 @@ def test_geometry_matches_oracle(B, orc, n, W):
             assert s["slot_bytes"] == orc.reuse_slot_bytes(n, W, bb, coded)
             assert s["cache_bytes"] == n
             B.ez_plan_destroy(p)
+    for codec, fmt in ((B.EZ_CODEC_FP8_E5M2, orc.FP8_E5M2), (B.EZ_CODEC_FP8_E4M3, orc.FP8_E4M3)):
+        p = B.ez_plan_create(n, W, 0, codec)
+        s = B.ez_plan_sizes(p)
+        L = orc.shard_len(n, W)
+        assert s["shard_len"] == L
+        assert s["slot_bytes"] == orc.fp8_chunk_bytes(L, L, fmt)
+        assert s["cache_bytes"] == 0 and s["send_cache_bytes"] == 0
+        B.ez_plan_destroy(p)
 
 
 def test_host_argument_checks_need_no_gpu(B):
