@@ -53,6 +53,7 @@ struct StatsSmem {
     uint32_t sample[256];
     uint32_t elo;
     uint32_t last;
+    uint32_t junk[32];     // target of the reductions of out-of-window lanes (never read)
 };
 
 // Zero the CTA's accumulators and choose Elo from one exponent per thread
@@ -147,26 +148,28 @@ __device__ __forceinline__ uint32_t st_sign_hi(uint32_t x)
     return r;
 }
 
-// hist[cell] += 1 when (y & mask) == 0 (the lane is in the window); addr is
-// the cell's shared-memory address.
-__device__ __forceinline__ void st_red_if_in(uint32_t addr, uint32_t y, uint32_t mask)
+// hist[cell] += 1 when (y & mask) == 0 (the lane is in the window), else a
+// lane-private junk word += 1: the address is selected, so the reduction
+// itself is unconditional and the hot loop has no branch per value.
+__device__ __forceinline__ void st_red_sel(uint32_t addr, uint32_t junk, uint32_t y, uint32_t mask)
 {
-    asm volatile("{ .reg .pred q; .reg .b32 t; and.b32 t, %1, %2; setp.eq.u32 q, t, 0;"
-                 " @q red.shared.add.u32 [%0], 1; }"
-                 :: "r"(addr), "r"(y), "r"(mask) : "memory");
+    asm volatile("{ .reg .pred q; .reg .b32 t, a; and.b32 t, %1, %2; setp.eq.u32 q, t, 0;"
+                 " selp.b32 a, %0, %3, q; red.shared.add.u32 [a], 1; }"
+                 :: "r"(addr), "r"(y), "r"(mask), "r"(junk) : "memory");
 }
 
 // Eight values (one 16-byte load): in-window values take their cell, the
 // others (rare) the per-exponent bins.
-__device__ __forceinline__ void st_add8(const uint4& w, uint32_t e7, uint32_t hist_base, StatsSmem& S)
+__device__ __forceinline__ void st_add8(const uint4& w, uint32_t e7, uint32_t hist_base, uint32_t junk,
+                                        StatsSmem& S)
 {
     const uint32_t xs[4] = {w.x, w.y, w.z, w.w};
     uint32_t y[4];
 #pragma unroll
     for (int q = 0; q < 4; q++) {
         y[q] = st_y(xs[q], e7);
-        st_red_if_in(hist_base + 4u * st_cell(y[q], st_sign_lo(xs[q])), y[q], 0x7800u);
-        st_red_if_in(hist_base + 4u * st_cell(y[q] >> 16, st_sign_hi(xs[q])), y[q], 0x78000000u);
+        st_red_sel(hist_base + 4u * st_cell(y[q], st_sign_lo(xs[q])), junk, y[q], 0x7800u);
+        st_red_sel(hist_base + 4u * st_cell(y[q] >> 16, st_sign_hi(xs[q])), junk, y[q], 0x78000000u);
     }
     if ((y[0] | y[1] | y[2] | y[3]) & 0x78007800u) {
 #pragma unroll

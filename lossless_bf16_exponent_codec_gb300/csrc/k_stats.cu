@@ -44,6 +44,7 @@ k_stats(const uint16_t* __restrict__ x, uint64_t n, uint64_t L, uint32_t first, 
     const uint32_t elo = S.elo;
     const uint32_t e7 = (elo << 7) * 0x10001u;
     const uint32_t hb = (uint32_t)__cvta_generic_to_shared(S.hist);
+    const uint32_t jb = (uint32_t)__cvta_generic_to_shared(S.junk) + 4u * (uint32_t)(t & 31);
     if (nv == kStatsTile) {
         // full tile: no per-group bounds
 #pragma unroll 1
@@ -52,7 +53,7 @@ k_stats(const uint16_t* __restrict__ x, uint64_t n, uint64_t L, uint32_t first, 
 #pragma unroll
             for (int k = 0; k < kStatsBatch; k++) w[k] = ld_v4_nc(xt + 8u * (uint32_t)((g0 + k) * kThreads + t));
 #pragma unroll
-            for (int k = 0; k < kStatsBatch; k++) st_add8(w[k], e7, hb, S);
+            for (int k = 0; k < kStatsBatch; k++) st_add8(w[k], e7, hb, jb, S);
         }
         grid_dep_wait();   // the bins were cleared by the kernel before
         if (st_end(S, G + ci, tps)) st_finalize(G + ci, n_s, K, out + ci, S, hist_window);
@@ -62,7 +63,7 @@ k_stats(const uint16_t* __restrict__ x, uint64_t n, uint64_t L, uint32_t first, 
     for (int g = 0; g < kStatsLoads; g++) {
         const uint32_t v = 8u * (uint32_t)(g * kThreads + t);
         if (v + 8 <= nv) {
-            st_add8(ld_v4_nc(xt + v), e7, hb, S);
+            st_add8(ld_v4_nc(xt + v), e7, hb, jb, S);
         } else if (v < nv) {
             for (uint32_t i = v; i < nv; i++) st_add(xt[i], elo, S);
         }
