@@ -62,7 +62,6 @@ WsView ws_view(const ez_plan_s* p, void* ws)
     v.seg_b = v.seg_a + segs;
     v.state_a = reinterpret_cast<unsigned long long*>(b + p->off_state_a);
     v.state_b = reinterpret_cast<unsigned long long*>(b + p->off_state_b);
-    v.ctot = p->off_ctot ? reinterpret_cast<unsigned long long*>(b + p->off_ctot) : nullptr;
     return v;
 }
 
@@ -85,7 +84,6 @@ ez_status ez_plan_create(ez_plan* out, const ez_plan_desc* d)
     if (reuse) {
         if (d->B == 0) return EZ_ERR_ARG;
         if (d->B < 8 || d->B > 1024 || (d->B & (d->B - 1))) return EZ_ERR_UNSUPPORTED;
-        if (hash && d->B < 32) return EZ_ERR_UNSUPPORTED;
     }
     ez_plan_s* p = new (std::nothrow) ez_plan_s();
     if (!p) return EZ_ERR_ARG;
@@ -137,17 +135,10 @@ ez_status ez_plan_create(ez_plan* out, const ez_plan_desc* d)
     p->off_hbm = off;
     off = rup(off + W * p->hwords * 4ull, 256);
     p->zero_bytes = off;
-    // code3: per-CTA escape totals of the grid-barrier encoder and a staging
-    // slot of 8192 + 16 bytes per tile for escapes that do not fit the CTA's
-    // shared staging area (neither needs clearing: every entry is written
-    // before it is read)
-    const bool code3 = d->codec == EZ_CODEC_CODE3;
-    p->off_ctot = code3 ? off : 0;
-    off = rup(off + (code3 ? ezk::kMaxGridCtas * 8 : 0), 256);
     // coded reuse: each tile's escapes staged at its own offset, its planes
     // in 3 KB per tile
-    p->off_escbuf = (coded || code3) ? off : 0;
-    off = rup(off + (coded ? W * L : (code3 ? W * tpc * (kTileValues + 16) : 0)), 256);
+    p->off_escbuf = coded ? off : 0;
+    off = rup(off + (coded ? W * L : 0), 256);
     p->off_plbuf = coded ? off : 0;
     off = rup(off + (coded ? W * tpc * 3 * (kTileValues / 8) : 0), 256);
     p->ws_bytes = off;

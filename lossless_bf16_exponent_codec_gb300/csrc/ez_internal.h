@@ -22,7 +22,6 @@ struct ez_plan_s {
     uint32_t hwords;         // 32-bit words of changed-block bits per shard (hash mode)
     uint64_t hstride;        // sender-cache bytes per shard (hash mode: 16 per block)
     uint64_t off_hbm;        // workspace: changed-block bits (hash mode)
-    uint64_t off_ctot;       // workspace: per-CTA totals (code3), 0 if none
 };
 
 namespace ezk {
@@ -48,7 +47,6 @@ struct WsView {
     uint8_t* plbuf;                // 3 KB of staged planes per tile (coded reuse) or NULL
     unsigned long long* seg_a;     // scan-segment states, two arrays of W * segments
     unsigned long long* seg_b;
-    unsigned long long* ctot;      // code3: per-CTA escape totals of the grid-barrier encode, or NULL
 };
 
 WsView ws_view(const ez_plan_s* p, void* ws);
@@ -71,20 +69,10 @@ cudaError_t launch_stats(const ez_plan_s* p, const uint16_t* x, uint64_t n, ez_s
 cudaError_t launch_shard_stats(const ez_plan_s* p, const uint16_t* x, uint32_t first, uint32_t count,
                                ez_stats_t* out, const WsView& w, cudaStream_t s);
 
-// The code3 encode: persistent CTAs, one grid barrier (cooperative launch);
-// needs the workspace's per-CTA totals and escape staging slots.
 cudaError_t launch_code3_encode(const ez_plan_s* p, const uint16_t* x, uint32_t first,
                                 uint32_t count, const ez_stats_t* st, uint8_t* out,
                                 uint64_t* sizes, uint32_t* dstatus, const WsView& w,
                                 cudaStream_t s);
-// The same encode with a decoupled look-back between tiles; its scratch is
-// only counters and 8 bytes of look-back state per tile (the no-alloc entry).
-cudaError_t launch_code3_encode_lookback(const ez_plan_s* p, const uint16_t* x, uint32_t first,
-                                         uint32_t count, const ez_stats_t* st, uint8_t* out,
-                                         uint64_t* sizes, uint32_t* dstatus, const WsView& w,
-                                         cudaStream_t s);
-// Largest grid of a persistent cooperative encode (sizes the per-CTA totals).
-constexpr uint64_t kMaxGridCtas = 8192;
 
 cudaError_t launch_code3_decode(const ez_plan_s* p, const uint8_t* in, const uint64_t* offsets,
                                 uint32_t first, uint32_t count, uint16_t* out,
