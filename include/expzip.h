@@ -116,8 +116,8 @@ typedef struct {
  * e.g. norm weights near 1.0, where the sigma window misses every value. */
 #define EZ_FLAG_WINDOW_HIST 1u
 
-/* Plan flag (reuse codecs, B >= 32; EZ_ERR_UNSUPPORTED for smaller blocks,
- * EZ_ERR_ARG with the code3 codec): CIERA's hash-based change detection.  The
+/* Plan flag (reuse codecs, any block size; EZ_ERR_ARG with the code3 and
+ * FP8 codecs): CIERA's hash-based change detection.  The
  * sender cache holds two 64-bit hashes per block (HashCache, 16 bytes per
  * block instead of one byte per value): a block is sent when it is cold or
  * its hash pair differs, and the pair is then replaced.  Hash s of a block:

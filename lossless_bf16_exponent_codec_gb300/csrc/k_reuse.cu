@@ -313,6 +313,35 @@ __global__ void __launch_bounds__(kThreads) k_reuse_hash(RuEnc a)
     const unsigned long long w[4] = {
         (unsigned long long)ew[0].y << 32 | ew[0].x, (unsigned long long)ew[0].w << 32 | ew[0].z,
         (unsigned long long)ew[1].y << 32 | ew[1].x, (unsigned long long)ew[1].w << 32 | ew[1].z};
+    unsigned long long* hc0 = reinterpret_cast<unsigned long long*>(a.cache + (uint64_t)ci * a.hstride);
+    if (B < 32) {
+        // the thread's 32 values are 32/B whole blocks of B/8 words each
+        unsigned long long t0[4], t1[4];
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+            const unsigned long long base = w[q] + ((B == 8 ? 0ull : (unsigned long long)(q & 1)) + 1) * kGamma;
+            t0[q] = sm64_mix(base);
+            t1[q] = sm64_mix(base + kHashSeed1);
+        }
+        const uint32_t bpt = 32u >> log2B;
+#pragma unroll
+        for (uint32_t j = 0; j < 4; j++) {
+            if (j >= bpt) break;
+            const uint64_t vb = v0 + tv + (uint64_t)j * B;
+            if (vb >= n_s) break;
+            const unsigned long long s0 = B == 8 ? t0[j] : t0[2 * j] + t0[2 * j + 1];
+            const unsigned long long s1 = B == 8 ? t1[j] : t1[2 * j] + t1[2 * j + 1];
+            const uint64_t k = vb >> log2B;
+            unsigned long long* hc = hc0 + 2 * k;
+            const unsigned long long h0 = sm64_mix(s0), h1 = sm64_mix(s1);
+            if (a.cold || hc[0] != h0 || hc[1] != h1) {
+                hc[0] = h0;
+                hc[1] = h1;
+                atomicOr(&a.hbm[(uint64_t)ci * a.hwords + (k >> 5)], 1u << (k & 31));
+            }
+        }
+        return;
+    }
     const unsigned long long i0 = (tv & (B - 1u)) >> 3;   // word index of w[0] in the block
     unsigned long long s0 = 0, s1 = 0;
 #pragma unroll
@@ -328,7 +357,7 @@ __global__ void __launch_bounds__(kThreads) k_reuse_hash(RuEnc a)
     }
     if ((lane & (per - 1)) != 0 || v0 + tv >= n_s) return;   // the block's first thread, if the block exists
     const uint64_t k = (v0 + tv) >> log2B;
-    unsigned long long* hc = reinterpret_cast<unsigned long long*>(a.cache + (uint64_t)ci * a.hstride) + 2 * k;
+    unsigned long long* hc = hc0 + 2 * k;
     const unsigned long long h0 = sm64_mix(s0), h1 = sm64_mix(s1);
     if (a.cold || hc[0] != h0 || hc[1] != h1) {
         hc[0] = h0;
@@ -392,41 +421,75 @@ __global__ void __launch_bounds__(kThreads, 6) k_reuse_hash_split(RuEnc a)
         }
     }
     // the block's hash pair (words of 8 exponent bytes, 0 past the shard)
-    unsigned long long s0 = 0, s1 = 0;
-    const unsigned long long i0 = (tv & (B - 1u)) >> 3;
+    unsigned long long ew[4];
 #pragma unroll
-    for (int q = 0; q < 4; q++) {
-        const unsigned long long w = (unsigned long long)exp4_of(xw[4 * q + 2], xw[4 * q + 3]) << 32 |
-                                     exp4_of(xw[4 * q], xw[4 * q + 1]);
-        const unsigned long long base = w + (i0 + q + 1) * kGamma;
-        s0 += sm64_mix(base);
-        s1 += sm64_mix(base + kHashSeed1);
-    }
-    const uint32_t per = B >> 5;                          // threads per block, 1..32
-    for (uint32_t o2 = per >> 1; o2; o2 >>= 1) {
-        s0 += __shfl_xor_sync(kFull, s0, o2);
-        s1 += __shfl_xor_sync(kFull, s1, o2);
-    }
-    bool ch = false;
-    if ((lane & (per - 1)) == 0 && v0 + tv < n_s) {
-        const uint64_t k = (v0 + tv) >> log2B;
-        unsigned long long* hc = reinterpret_cast<unsigned long long*>(a.cache + (uint64_t)ci * a.hstride) + 2 * k;
-        const unsigned long long h0 = sm64_mix(s0), h1 = sm64_mix(s1);
-        if (a.cold || hc[0] != h0 || hc[1] != h1) {
-            hc[0] = h0;
-            hc[1] = h1;
-            ch = true;
+    for (int q = 0; q < 4; q++)
+        ew[q] = (unsigned long long)exp4_of(xw[4 * q + 2], xw[4 * q + 3]) << 32 | exp4_of(xw[4 * q], xw[4 * q + 1]);
+    unsigned long long* hc0 = reinterpret_cast<unsigned long long*>(a.cache + (uint64_t)ci * a.hstride);
+    if (B < 32) {
+        // the thread's 32 values are 32/B whole blocks of B/8 words each: it
+        // decides them all and ORs their bits into the tile's bitmap
+        unsigned long long t0[4], t1[4];
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+            const unsigned long long base = ew[q] + ((B == 8 ? 0ull : (unsigned long long)(q & 1)) + 1) * kGamma;
+            t0[q] = sm64_mix(base);
+            t1[q] = sm64_mix(base + kHashSeed1);
         }
-    }
-    const uint32_t bal = __ballot_sync(kFull, ch);
-    __syncthreads();   // s_bm cleared
-    if (lane == 0 && bal) {
-        const uint32_t nbw = 32u / per;                   // blocks per warp
+        const uint32_t bpt = 32u >> log2B;
         uint32_t bits = 0;
-        for (uint32_t j = 0; j < nbw; j++)
-            if ((bal >> (j * per)) & 1u) bits |= 1u << j;
-        const uint32_t pos = (uint32_t)wid * nbw;
-        atomicOr(&s_bm[pos >> 5], bits << (pos & 31));
+#pragma unroll
+        for (uint32_t j = 0; j < 4; j++) {
+            if (j >= bpt) break;
+            const uint64_t vb = v0 + tv + (uint64_t)j * B;
+            if (vb >= n_s) break;
+            const unsigned long long s0 = B == 8 ? t0[j] : t0[2 * j] + t0[2 * j + 1];
+            const unsigned long long s1 = B == 8 ? t1[j] : t1[2 * j] + t1[2 * j + 1];
+            unsigned long long* hc = hc0 + 2 * (vb >> log2B);
+            const unsigned long long h0 = sm64_mix(s0), h1 = sm64_mix(s1);
+            if (a.cold || hc[0] != h0 || hc[1] != h1) {
+                hc[0] = h0;
+                hc[1] = h1;
+                bits |= 1u << j;
+            }
+        }
+        __syncthreads();   // s_bm cleared
+        const uint32_t pos = (uint32_t)t * bpt;             // the thread's first block in the tile
+        if (bits) atomicOr(&s_bm[pos >> 5], bits << (pos & 31));
+    } else {
+        unsigned long long s0 = 0, s1 = 0;
+        const unsigned long long i0 = (tv & (B - 1u)) >> 3;
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+            const unsigned long long base = ew[q] + (i0 + q + 1) * kGamma;
+            s0 += sm64_mix(base);
+            s1 += sm64_mix(base + kHashSeed1);
+        }
+        const uint32_t per = B >> 5;                      // threads per block, 1..32
+        for (uint32_t o2 = per >> 1; o2; o2 >>= 1) {
+            s0 += __shfl_xor_sync(kFull, s0, o2);
+            s1 += __shfl_xor_sync(kFull, s1, o2);
+        }
+        bool ch = false;
+        if ((lane & (per - 1)) == 0 && v0 + tv < n_s) {
+            unsigned long long* hc = hc0 + 2 * ((v0 + tv) >> log2B);
+            const unsigned long long h0 = sm64_mix(s0), h1 = sm64_mix(s1);
+            if (a.cold || hc[0] != h0 || hc[1] != h1) {
+                hc[0] = h0;
+                hc[1] = h1;
+                ch = true;
+            }
+        }
+        const uint32_t bal = __ballot_sync(kFull, ch);
+        __syncthreads();   // s_bm cleared
+        if (lane == 0 && bal) {
+            const uint32_t nbw = 32u / per;               // blocks per warp
+            uint32_t bits = 0;
+            for (uint32_t j = 0; j < nbw; j++)
+                if ((bal >> (j * per)) & 1u) bits |= 1u << j;
+            const uint32_t pos = (uint32_t)wid * nbw;
+            atomicOr(&s_bm[pos >> 5], bits << (pos & 31));
+        }
     }
     __syncthreads();
     const uint32_t fin_tile = n_s ? (uint32_t)((n_s - 1) / kTile) : 0u;
@@ -653,6 +716,7 @@ __device__ __forceinline__ uint32_t load_bitmap(const uint8_t* o, uint32_t lt, u
 // read from the cache, go to EXP at (prefix + rank) * B + offset.  The index
 // entry is the prefix; the tile holding the shard's last value writes the
 // header, the padding and the size (totals from the split's shard record).
+template <bool kHash>
 __global__ void __launch_bounds__(kThreads, 6) k_reuse_place(RuEnc a)
 {
     __shared__ uint32_t s_bm[32], s_pre[32], s_agg;
@@ -671,12 +735,20 @@ __global__ void __launch_bounds__(kThreads, 6) k_reuse_place(RuEnc a)
     const uint8_t* ct = a.cache + (uint64_t)ci * a.L + v0;
     uint8_t* o = a.out + (uint64_t)ci * a.slot;
     const unsigned long long* sc = a.state + (uint64_t)ci * a.tpc;
-    // every group's cache bytes, loaded with the bitmap and the prefix
+    // every group's exponents, loaded with the bitmap and the prefix: the
+    // cache bytes, or (hash-based detection: the cache holds hashes) the
+    // exponent fields of x
     unsigned long long ev[kGroups];
+    const uint16_t* xt = a.x + (uint64_t)ci * a.L + v0;
 #pragma unroll
     for (int g = 0; g < kGroups; g++) {
         const uint32_t v = 8u * (uint32_t)(g * kThreads + t);
-        ev[g] = v < nv ? ld_group8(ct, v, nv) : 0ull;
+        if (kHash) {
+            const uint4 xw = v < nv ? ld_group16(xt, v, nv) : make_uint4(0, 0, 0, 0);
+            ev[g] = (unsigned long long)exp4_of(xw.z, xw.w) << 32 | exp4_of(xw.x, xw.y);
+        } else {
+            ev[g] = v < nv ? ld_group8(ct, v, nv) : 0ull;
+        }
     }
     const unsigned long long P = lt ? ld_relaxed(sc + lt - 1) : 0ull;
     __syncthreads();
@@ -1490,7 +1562,9 @@ cudaError_t launch_reuse_encode(const ez_plan_s* p, const uint16_t* x, uint32_t 
         if (e != cudaSuccess) return e;
         e = launch_tile_scan(p, w.state_a, count, w.seg_a, w.counters + 4, w.counters + 7, dstatus, s);
         if (e != cudaSuccess) return e;
-        if (p->B < 32) return launch_dependent(k_reuse_place, tiles, kThreads, 0, s, a);
+        if (p->B < 32)
+            return a.hash ? launch_dependent(k_reuse_place<true>, tiles, kThreads, 0, s, a)
+                          : launch_dependent(k_reuse_place<false>, tiles, kThreads, 0, s, a);
         return a.hash ? launch_dependent(k_reuse_place32<true>, tiles, kThreads, 0, s, a)
                       : launch_dependent(k_reuse_place32<false>, tiles, kThreads, 0, s, a);
     }

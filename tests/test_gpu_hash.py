@@ -31,7 +31,7 @@ def _flip(rng, x, rate):
 
 
 @pytest.mark.parametrize("coded", [False, True])
-@pytest.mark.parametrize("B", [32, 64, 256, 1024])
+@pytest.mark.parametrize("B", [8, 16, 32, 64, 256, 1024])
 @pytest.mark.parametrize("n,W", [(50_001, 3), ((1 << 20) + 77, 8), (16_384, 1), (1000, 4)])
 def test_hash_mode_parity(ez, orc, coded, B, n, W):
     binding, codec = ez
@@ -75,9 +75,15 @@ def test_hash_mode_parity(ez, orc, coded, B, n, W):
 def test_hash_mode_plan_checks(ez):
     binding, codec = ez
     E = binding.EzError
+    for bb in (8, 16):   # every reuse block size has hash mode
+        binding.ez_plan_destroy(binding.ez_plan_create(1000, 2, bb, binding.EZ_CODEC_REUSE,
+                                                       binding.EZ_FLAG_HASH_CACHE))
     with pytest.raises(E) as ei:
-        binding.ez_plan_create(1000, 2, 16, binding.EZ_CODEC_REUSE, binding.EZ_FLAG_HASH_CACHE)
+        binding.ez_plan_create(1000, 2, 4, binding.EZ_CODEC_REUSE, binding.EZ_FLAG_HASH_CACHE)
     assert ei.value.status == binding.EZ_ERR_UNSUPPORTED
+    with pytest.raises(E) as ei:
+        binding.ez_plan_create(1000, 2, 0, binding.EZ_CODEC_FP8_E5M2, binding.EZ_FLAG_HASH_CACHE)
+    assert ei.value.status == binding.EZ_ERR_ARG
     with pytest.raises(E) as ei:
         binding.ez_plan_create(1000, 2, 0, binding.EZ_CODEC_CODE3, binding.EZ_FLAG_HASH_CACHE)
     assert ei.value.status == binding.EZ_ERR_ARG
