@@ -24,7 +24,8 @@
 // (both are their own inverses).  Codes are computed bit-sliced, 32 values
 // per operation: d = E - E0 by a ripple subtraction over the exponent
 // planes, in-window = no borrow and d <= 6, code = d + 1.  Escape offsets use
-// the decoupled look-back of ez_common.cuh (encode) or the index (decode).
+// the decoupled look-back of ez_common.cuh over tiles of 4 index spans
+// (encode) or the index (decode).
 // Statistics: every byte pattern is counted exactly (one shared-memory
 // reduction per value into lane-private copies, so no two lanes of a warp
 // share an address or a bank); the last CTA forms the exact sums of the
@@ -435,17 +436,24 @@ struct F8Enc {
     uint32_t* abort;
 };
 
-// One CTA per tile of 8192 values, tiles taken in order from a counter (dealt
-// round-robin over the chunks), so a tile's look-back only waits on tiles
-// whose CTAs already run.  Planes are stored before the look-back; only the
-// escapes (and, on a chunk's last tile, the header, padding and size) wait
-// for the tile's escape prefix.
+// One CTA per tile of kF8Spans index spans (4 x 8192 values), tiles taken in
+// order from a counter (dealt round-robin over the chunks), so a tile's
+// look-back only waits on tiles whose CTAs already run.  Span by span: the
+// planes are stored at once, a block scan places each thread's escapes in the
+// tile's shared staging area; one look-back per tile then gives the escape
+// prefix, the index entries of its spans and the place of the staged escapes
+// (on a chunk's last tile also the header, padding and size).
+constexpr uint32_t kF8Spans = 4;
+constexpr uint32_t kF8TileV = kF8Spans * kTile;
+
 template <uint32_t kCodec>
 __global__ void __launch_bounds__(kThreads) k_fp8_encode(F8Enc a)
 {
     __shared__ uint32_t s_tile;
     __shared__ unsigned long long s_warp[kThreads / 32];
     __shared__ unsigned long long s_prefix;
+    __shared__ uint32_t s_base[kF8Spans + 1];
+    __shared__ __align__(16) uint8_t s_esc[kF8TileV + 16];
     const int t = threadIdx.x;
     grid_dep_wait();   // the counters and tile states were cleared by the kernel before
     constexpr Fp8Fmt f = fp8_fmt(kCodec);
@@ -455,70 +463,80 @@ __global__ void __launch_bounds__(kThreads) k_fp8_encode(F8Enc a)
         if (t == 0) atomicOr(a.dstatus, EZ_DSTAT_BAD_STATS);
         E0 = 0;
     }
+    const uint32_t tpt = (uint32_t)cdiv(a.tpc, kF8Spans);   // tiles per chunk
     const uint32_t id = next_tile(a.counter, &s_tile);
-    const TilePos tp = tile_pos(id, a.count, a.tpc);
+    const TilePos tp = tile_pos(id, a.count, tpt);
     const uint32_t ci = tp.ci, lt = tp.lt;
     const uint32_t c = a.first + ci;
     const uint64_t n_c = shard_values(a.n, a.L, c);
-    const uint64_t v0 = (uint64_t)lt * kTile;
-    const uint32_t nv = v0 < n_c ? (uint32_t)umin64(kTile, n_c - v0) : 0u;
     uint8_t* o = a.out + (uint64_t)ci * a.slot;
     const uint64_t plane = f8_plane(n_c);
     uint8_t* pl = o + 128;
     uint8_t* idx = pl + (nsm + 3) * plane;
     uint8_t* esc = idx + f8_idx_bytes(n_c);
     const uint32_t tv = 32u * (uint32_t)t;
-    const uint32_t cnt_v = tv < nv ? min(32u, nv - tv) : 0u;
-    uint32_t escm = 0, R[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-    if (cnt_v) {
-        uint32_t w[8];
-        load32(a.x + (uint64_t)ci * a.L + v0 + tv, cnt_v, w);
-        to_planes(w, R);
-        const uint32_t vm = cnt_v == 32 ? 0xFFFFFFFFu : ((1u << cnt_v) - 1u);
-        // d = E - E0 over the exponent planes R[m .. m+ebits)
-        uint32_t d[5], br = 0;
+    uint32_t base = 0;                 // escapes of the tile's earlier spans (uniform)
+#pragma unroll 1
+    for (uint32_t sp = 0; sp < kF8Spans; sp++) {
+        const uint64_t v0 = ((uint64_t)lt * kF8Spans + sp) * kTile;
+        const uint32_t nv = v0 < n_c ? (uint32_t)umin64(kTile, n_c - v0) : 0u;
+        const uint32_t cnt_v = tv < nv ? min(32u, nv - tv) : 0u;
+        uint32_t escm = 0, e[5] = {0, 0, 0, 0, 0};
+        if (cnt_v) {
+            uint32_t w[8], R[8];
+            load32(a.x + (uint64_t)ci * a.L + v0 + tv, cnt_v, w);
+            to_planes(w, R);
+            const uint32_t vm = cnt_v == 32 ? 0xFFFFFFFFu : ((1u << cnt_v) - 1u);
+            // d = E - E0 over the exponent planes R[m .. m+ebits)
+            uint32_t d[5], br = 0;
 #pragma unroll
-        for (int j = 0; j < 5; j++) {
-            if (j < (int)f.ebits) {
-                const uint32_t e = R[f.mbits + j], k = bitmask_of(E0, j);
-                d[j] = e ^ k ^ br;
-                br = borrow3(e, k, br);
-            } else {
-                d[j] = 0;
+            for (int j = 0; j < 5; j++) {
+                if (j < (int)f.ebits) {
+                    const uint32_t ej = R[f.mbits + j], k = bitmask_of(E0, j);
+                    e[j] = ej;
+                    d[j] = ej ^ k ^ br;
+                    br = borrow3(ej, k, br);
+                } else {
+                    d[j] = 0;
+                }
             }
+            const uint32_t in = ~br & ~(d[3] | d[4]) & ~(d[0] & d[1] & d[2]) & vm;
+            escm = ~in & vm;
+            // sign/mantissa planes: mantissa bits, then the sign
+            uint8_t* pt = pl + (v0 + tv) / 8;
+#pragma unroll
+            for (uint32_t q = 0; q < 4; q++)
+                if (q < nsm) *reinterpret_cast<uint32_t*>(pt + q * plane) = (q < f.mbits ? R[q] : R[7]) & vm;
+            // code = d + 1 inside the window
+            *reinterpret_cast<uint32_t*>(pt + nsm * plane) = ~d[0] & in;
+            *reinterpret_cast<uint32_t*>(pt + (nsm + 1) * plane) = (d[1] ^ d[0]) & in;
+            *reinterpret_cast<uint32_t*>(pt + (nsm + 2) * plane) = (d[2] ^ (d[1] & d[0])) & in;
         }
-        const uint32_t in = ~br & ~(d[3] | d[4]) & ~(d[0] & d[1] & d[2]) & vm;
-        escm = ~in & vm;
-        // sign/mantissa planes: mantissa bits, then the sign
-        uint8_t* pt = pl + (v0 + tv) / 8;
+        unsigned long long tot;
+        const unsigned long long ex = block_excl_scan(__popc(escm), s_warp, &tot);
+        // the thread's escapes, in value order (raw exponent fields), staged
+        uint32_t m = escm, r = base + (uint32_t)ex;
+        while (m) {
+            const int i = __ffs(m) - 1;
+            m &= m - 1;
+            uint32_t eb = 0;
 #pragma unroll
-        for (uint32_t q = 0; q < 4; q++)
-            if (q < nsm) *reinterpret_cast<uint32_t*>(pt + q * plane) = (q < f.mbits ? R[q] : R[7]) & vm;
-        // code = d + 1 inside the window
-        *reinterpret_cast<uint32_t*>(pt + nsm * plane) = ~d[0] & in;
-        *reinterpret_cast<uint32_t*>(pt + (nsm + 1) * plane) = (d[1] ^ d[0]) & in;
-        *reinterpret_cast<uint32_t*>(pt + (nsm + 2) * plane) = (d[2] ^ (d[1] & d[0])) & in;
+            for (int j = 0; j < 5; j++) eb |= ((e[j] >> i) & 1u) << j;
+            s_esc[r++] = (uint8_t)eb;
+        }
+        if (t == 0) s_base[sp] = base;
+        base += (uint32_t)tot;
+        __syncthreads();   // s_warp is read before the next span's scan writes it
     }
-    const uint32_t my = __popc(escm);
-    unsigned long long agg;
-    const unsigned long long excl = block_excl_scan(my, s_warp, &agg);
-    const unsigned long long P = tile_prefix(a.state, ci * a.tpc + lt, ci * a.tpc, agg, &s_prefix,
+    const unsigned long long P = tile_prefix(a.state, ci * tpt + lt, ci * tpt, base, &s_prefix,
                                              a.dstatus, a.abort);
-    if (t == 0 && v0 < n_c) *reinterpret_cast<unsigned long long*>(idx + 8ull * lt) = P;
-    // this thread's escapes, in value order: the raw exponent fields
-    uint32_t m = escm;
-    uint64_t r = P + excl;
-    while (m) {
-        const int i = __ffs(m) - 1;
-        m &= m - 1;
-        uint32_t e = 0;
-#pragma unroll
-        for (int j = 0; j < 5; j++)
-            if (j < (int)f.ebits) e |= ((R[f.mbits + j] >> i) & 1u) << j;
-        esc[r++] = (uint8_t)e;
+    if ((uint32_t)t < kF8Spans) {
+        const uint64_t span = (uint64_t)lt * kF8Spans + t;
+        if (span * kTile < n_c) *reinterpret_cast<unsigned long long*>(idx + 8ull * span) = P + s_base[t];
     }
-    if (lt == a.tpc - 1) {
-        const uint64_t n_esc = P + agg;
+    for (uint32_t i = (uint32_t)t; i < base; i += kThreads) esc[P + i] = s_esc[i];
+    if (lt == tpt - 1) {
+        const uint64_t n_esc = P + base;
         const uint64_t bytes = f8_bytes(n_c, n_esc, nsm);
         const uint64_t pb = cdiv(n_c, 8), ib = 8 * cdiv(n_c, kTile), ibytes = f8_idx_bytes(n_c);
         for (int q = t; q < 128; q += kThreads) {
@@ -751,7 +769,7 @@ cudaError_t launch_fp8_encode(const ez_plan_s* p, const uint8_t* x, uint32_t fir
     a.state = w.state_a;
     a.counter = w.counters + 0;
     a.abort = w.counters + 7;
-    const uint64_t tiles = (uint64_t)count * p->tpc;
+    const uint64_t tiles = (uint64_t)count * cdiv(p->tpc, kF8Spans);
     if (tiles > 0x7fffffffull) return cudaErrorInvalidValue;
     if (p->codec == EZ_CODEC_FP8_E5M2)
         return launch_dependent(k_fp8_encode<EZ_CODEC_FP8_E5M2>, (unsigned)tiles, kThreads, 0, s, a);
