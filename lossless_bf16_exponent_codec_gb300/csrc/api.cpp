@@ -56,7 +56,6 @@ WsView ws_view(const ez_plan_s* p, void* ws)
     v.bins = b + p->off_bins;
     v.escbuf = p->off_escbuf ? b + p->off_escbuf : nullptr;
     v.plbuf = p->off_plbuf ? b + p->off_plbuf : nullptr;
-    v.hbm = p->hash_cache ? reinterpret_cast<uint32_t*>(b + p->off_hbm) : nullptr;
     const uint64_t segs = tile_scan_segments(p->tpc) * p->W;
     v.seg_a = reinterpret_cast<unsigned long long*>(b + p->off_seg);
     v.seg_b = v.seg_a + segs;
@@ -128,12 +127,9 @@ ez_status ez_plan_create(ez_plan* out, const ez_plan_desc* d)
     off = rup(off + (coded ? W * tpc * 8 : 0), 256);
     p->off_seg = off;                                     // two arrays of scan-segment states
     off = rup(off + 2 * W * ezk::tile_scan_segments(tpc) * 8, 256);
-    // hash mode: each shard's changed-block bits from the hash step
+    // hash mode: the sender cache holds 16 bytes (two hashes) per block
     const uint64_t blocks = reuse ? cdiv(L, d->B) : 0;
-    p->hwords = hash ? (uint32_t)cdiv(blocks, 32) : 0u;
     p->hstride = hash ? 16 * blocks : L;
-    p->off_hbm = off;
-    off = rup(off + W * p->hwords * 4ull, 256);
     p->zero_bytes = off;
     // coded reuse: each tile's escapes staged at its own offset, its planes
     // in 3 KB per tile

@@ -19,9 +19,7 @@ struct ez_plan_s {
     uint32_t n_bins;
     uint32_t hist_window;    // EZ_FLAG_WINDOW_HIST: window from the histogram
     uint32_t hash_cache;     // EZ_FLAG_HASH_CACHE: sender cache of block hashes
-    uint32_t hwords;         // 32-bit words of changed-block bits per shard (hash mode)
     uint64_t hstride;        // sender-cache bytes per shard (hash mode: 16 per block)
-    uint64_t off_hbm;        // workspace: changed-block bits (hash mode)
 };
 
 namespace ezk {
@@ -43,7 +41,6 @@ struct WsView {
     unsigned long long* state_b;
     void* bins;                    // StatsBins[n_bins]
     uint8_t* escbuf;               // W * L bytes of staged escapes (coded reuse) or NULL
-    uint32_t* hbm;                 // changed-block bits from the hash step (hash mode) or NULL
     uint8_t* plbuf;                // 3 KB of staged planes per tile (coded reuse) or NULL
     unsigned long long* seg_a;     // scan-segment states, two arrays of W * segments
     unsigned long long* seg_b;

@@ -57,11 +57,8 @@ struct RuEnc {
     uint8_t* escbuf;
     unsigned long long* state_b;
     // hash-based change detection: `cache` holds 2 u64 hashes per block,
-    // shard first+i at byte i * hstride; the hash step leaves each shard's
-    // changed-block bits in hbm (hwords 32-bit words per shard)
+    // shard first+i at byte i * hstride
     int hash;
-    uint32_t* hbm;
-    uint32_t hwords;
     uint64_t hstride;
 };
 
@@ -292,88 +289,77 @@ __device__ __forceinline__ unsigned long long sm64_mix(unsigned long long z)
     return z ^ (z >> 31);
 }
 
-// One CTA per 8192-value tile, B >= 32: thread t hashes the four words of
-// values [32t, 32t + 32) (they lie in one block), the B/32 threads of a block
-// add their partial sums with shuffles, and the block's first thread compares
-// the pair with the cache, writes it back when it differs (or cold) and sets
-// the block's bit in the shard's bit array for the split.
-__global__ void __launch_bounds__(kThreads) k_reuse_hash(RuEnc a)
+// Hash-based decision inside the coded split, for the block holding the
+// group at tile value v (every thread of the CTA calls it for the same
+// group): each lane's 8-value word is one term of its block; the B/8 terms of
+// a block are summed across lanes (B <= 256) or across the 2 or 4 warps of
+// the block (B = 512, 1024); the block's first lane compares the hash pair
+// with the cache and writes it back when it differs (or cold).  Returns, in
+// every lane of the block, whether the block changed.
+__device__ __forceinline__ bool hash_group_changed(const RuEnc& a, uint32_t ci, uint64_t v0, uint32_t v,
+                                                   uint64_t n_s, unsigned long long word,
+                                                   unsigned long long* s_h, uint32_t* s_ch)
 {
-    const int t = threadIdx.x, lane = t & 31;
-    const TilePos tp = tile_pos(blockIdx.x, a.count, a.tpc);
-    const uint32_t ci = tp.ci, lt = tp.lt;
-    const uint64_t n_s = shard_values(a.n, a.L, a.first + ci);
-    const uint64_t v0 = (uint64_t)lt * kTile;
-    const uint32_t nv = v0 < n_s ? (uint32_t)umin64(kTile, n_s - v0) : 0u;
-    const uint32_t B = a.B, log2B = a.log2B;
-    const uint32_t tv = 32u * (uint32_t)t;
-    const uint32_t cnt_v = tv < nv ? min(32u, nv - tv) : 0u;
-    uint4 ew[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
-    if (cnt_v) ew_from_x(a.x + (uint64_t)ci * a.L + v0 + tv, cnt_v, ew);
-    const unsigned long long w[4] = {
-        (unsigned long long)ew[0].y << 32 | ew[0].x, (unsigned long long)ew[0].w << 32 | ew[0].z,
-        (unsigned long long)ew[1].y << 32 | ew[1].x, (unsigned long long)ew[1].w << 32 | ew[1].z};
+    const uint32_t B = a.B, lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    const unsigned long long i = ((v0 + v) & (B - 1u)) >> 3;     // the word's index in its block
+    const unsigned long long base = word + (i + 1) * kGamma;
+    unsigned long long s0 = sm64_mix(base), s1 = sm64_mix(base + kHashSeed1);
+    const uint32_t per = B >> 3;                                   // words (lanes) per block
+    for (uint32_t o = (per < 32 ? per : 32) >> 1; o; o >>= 1) {
+        s0 += __shfl_xor_sync(kFull, s0, o);
+        s1 += __shfl_xor_sync(kFull, s1, o);
+    }
     unsigned long long* hc0 = reinterpret_cast<unsigned long long*>(a.cache + (uint64_t)ci * a.hstride);
-    if (B < 32) {
-        // the thread's 32 values are 32/B whole blocks of B/8 words each
-        unsigned long long t0[4], t1[4];
-#pragma unroll
-        for (int q = 0; q < 4; q++) {
-            const unsigned long long base = w[q] + ((B == 8 ? 0ull : (unsigned long long)(q & 1)) + 1) * kGamma;
-            t0[q] = sm64_mix(base);
-            t1[q] = sm64_mix(base + kHashSeed1);
-        }
-        const uint32_t bpt = 32u >> log2B;
-#pragma unroll
-        for (uint32_t j = 0; j < 4; j++) {
-            if (j >= bpt) break;
-            const uint64_t vb = v0 + tv + (uint64_t)j * B;
-            if (vb >= n_s) break;
-            const unsigned long long s0 = B == 8 ? t0[j] : t0[2 * j] + t0[2 * j + 1];
-            const unsigned long long s1 = B == 8 ? t1[j] : t1[2 * j] + t1[2 * j + 1];
-            const uint64_t k = vb >> log2B;
-            unsigned long long* hc = hc0 + 2 * k;
+    if (per <= 32) {
+        bool ch = false;
+        if ((lane & (per - 1)) == 0 && v0 + v < n_s) {
+            unsigned long long* hc = hc0 + 2 * ((v0 + v) >> a.log2B);
             const unsigned long long h0 = sm64_mix(s0), h1 = sm64_mix(s1);
             if (a.cold || hc[0] != h0 || hc[1] != h1) {
                 hc[0] = h0;
                 hc[1] = h1;
-                atomicOr(&a.hbm[(uint64_t)ci * a.hwords + (k >> 5)], 1u << (k & 31));
+                ch = true;
             }
         }
-        return;
+        return __shfl_sync(kFull, ch, lane & ~(per - 1));
     }
-    const unsigned long long i0 = (tv & (B - 1u)) >> 3;   // word index of w[0] in the block
-    unsigned long long s0 = 0, s1 = 0;
-#pragma unroll
-    for (int q = 0; q < 4; q++) {
-        const unsigned long long base = w[q] + (i0 + q + 1) * kGamma;
-        s0 += sm64_mix(base);
-        s1 += sm64_mix(base + kHashSeed1);
+    const uint32_t wpb = per >> 5;                                 // warps per block
+    if (lane == 0) {
+        s_h[wid] = s0;
+        s_h[kThreads / 32 + wid] = s1;
     }
-    const uint32_t per = B >> 5;                          // threads per block, 1..32
-    for (uint32_t o = per >> 1; o; o >>= 1) {
-        s0 += __shfl_xor_sync(kFull, s0, o);
-        s1 += __shfl_xor_sync(kFull, s1, o);
+    __syncthreads();
+    if (lane == 0 && (wid & (wpb - 1)) == 0) {
+        unsigned long long b0 = 0, b1 = 0;
+        for (uint32_t k = 0; k < wpb; k++) {
+            b0 += s_h[wid + k];
+            b1 += s_h[kThreads / 32 + wid + k];
+        }
+        bool ch = false;
+        if (v0 + v < n_s) {
+            unsigned long long* hc = hc0 + 2 * ((v0 + v) >> a.log2B);
+            const unsigned long long h0 = sm64_mix(b0), h1 = sm64_mix(b1);
+            if (a.cold || hc[0] != h0 || hc[1] != h1) {
+                hc[0] = h0;
+                hc[1] = h1;
+                ch = true;
+            }
+        }
+        s_ch[wid] = ch ? 1u : 0u;
     }
-    if ((lane & (per - 1)) != 0 || v0 + tv >= n_s) return;   // the block's first thread, if the block exists
-    const uint64_t k = (v0 + tv) >> log2B;
-    unsigned long long* hc = hc0 + 2 * k;
-    const unsigned long long h0 = sm64_mix(s0), h1 = sm64_mix(s1);
-    if (a.cold || hc[0] != h0 || hc[1] != h1) {
-        hc[0] = h0;
-        hc[1] = h1;
-        atomicOr(&a.hbm[(uint64_t)ci * a.hwords + (k >> 5)], 1u << (k & 31));
-    }
+    __syncthreads();
+    return s_ch[wid & ~(wpb - 1)] != 0;
 }
 
 // Raw reuse encode with hash-based change detection, step A in one pass
 // (same outputs as k_reuse_split<false> in hash mode): thread t holds the 32
-// values [32t, 32t + 32) of the tile, stores their sign+mantissa bytes,
-// hashes their exponent words as k_reuse_hash does, and the block's first
-// thread decides and updates the cache; the block bits go into the tile's
-// bitmap (a ballot, B/32 threads per block), whose count is published for
-// the scan and added to the shard totals.  The place step then reads the
-// changed exponents from x.
+// values [32t, 32t + 32) of the tile, stores their sign+mantissa bytes and
+// hashes their four exponent words (B >= 32: the block's B/32 threads add
+// their sums with shuffles and the block's first thread decides; B = 8, 16:
+// the thread decides its own 32/B blocks), updating the hash cache; the
+// block bits go into the tile's bitmap, whose count is published for the
+// scan and added to the shard totals.  The place step then reads the changed
+// exponents from x.
 __global__ void __launch_bounds__(kThreads, 6) k_reuse_hash_split(RuEnc a)
 {
     __shared__ uint32_t s_bm[32];
@@ -538,6 +524,8 @@ __global__ void __launch_bounds__(kThreads, kCoded ? 4 : 6) k_reuse_split(RuEnc 
     __shared__ uint32_t s_lut[kCoded ? 256 : 1];
     __shared__ unsigned long long s_warp[kCoded ? kThreads / 32 : 1];
     __shared__ __align__(16) uint32_t s_esc32[kCoded ? (kTile + 16) / 4 : 4];
+    __shared__ unsigned long long s_h[kCoded ? 2 * kThreads / 32 : 1];
+    __shared__ uint32_t s_ch[kCoded ? kThreads / 32 : 1];
     const int t = threadIdx.x, lane = t & 31, wid = t >> 5;
     // s_gl needs no clearing: lane 0 of every warp writes its entry of every
     // group below (a clear here could land after another warp's entry)
@@ -586,9 +574,9 @@ __global__ void __launch_bounds__(kThreads, kCoded ? 4 : 6) k_reuse_split(RuEnc 
                                       exp4_of(w[g].x, w[g].y)) & bmask;
         e8[g] = e;
         bool ch;
-        if (a.hash) {   // the hash step's decision for the group's block
-            const uint64_t kk = (v0 + v) >> log2B;
-            ch = vm && ((a.hbm[(uint64_t)ci * a.hwords + (kk >> 5)] >> (kk & 31)) & 1u);
+        if (kCoded && a.hash) {   // the block's hash pair against the hash cache
+            const bool hch = hash_group_changed(a, ci, v0, v, n_s, e, s_h, s_ch);
+            ch = vm && hch;
         } else {
             ch = vm && (a.cold || ((e ^ cv[g]) & bmask) != 0ull);
         }
@@ -1539,17 +1527,9 @@ cudaError_t launch_reuse_encode(const ez_plan_s* p, const uint16_t* x, uint32_t 
     a.info = w.info;
     a.stats = st ? st : w.shard_stats;
     a.hash = p->hash_cache ? 1 : 0;
-    a.hbm = w.hbm;
-    a.hwords = p->hwords;
     a.hstride = p->hstride;
     const unsigned tiles = (unsigned)((uint64_t)count * p->tpc);
     cudaError_t e;
-    if (a.hash && coded) {
-        // the blocks' hash pairs against the cache: changed-block bits for the split
-        k_reuse_hash<<<tiles, kThreads, 0, s>>>(a);
-        e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
-    }
     if (coded) {
         // the shards' windows (a pass over the values of their own)
         e = launch_shard_stats(p, x, first, count, a.stats, w, s);
