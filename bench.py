@@ -415,7 +415,10 @@ def run_extras(xs, n, W, flush, s, peak, reps=10):
     # benchmark's change rate
     from lossless_bf16_exponent_codec_gb300 import binding as Bd2
     encs = {"exponent_cache": C.Codec(n, W, B_BLOCK, Bd2.EZ_CODEC_REUSE),
-            "hash_cache": C.Codec(n, W, B_BLOCK, Bd2.EZ_CODEC_REUSE, flags=Bd2.EZ_FLAG_HASH_CACHE)}
+            "hash_cache": C.Codec(n, W, B_BLOCK, Bd2.EZ_CODEC_REUSE, flags=Bd2.EZ_FLAG_HASH_CACHE),
+            "coded_exponent_cache": C.Codec(n, W, B_BLOCK, Bd2.EZ_CODEC_REUSE_CODE3),
+            "coded_hash_cache": C.Codec(n, W, B_BLOCK, Bd2.EZ_CODEC_REUSE_CODE3,
+                                        flags=Bd2.EZ_FLAG_HASH_CACHE)}
     x1, x2 = xs[1 % len(xs)], xs[2 % len(xs)]
     t_enc = {}
     for name, ce in encs.items():
@@ -428,6 +431,38 @@ def run_extras(xs, n, W, flush, s, peak, reps=10):
         t_enc[name] = timed(enc)
         if ce.status_word():
             raise RuntimeError(f"{name} encode status {ce.status_word():#x}")
+    # the pages' premise for hashing: the sender's change detection runs off
+    # the critical path, beside the receiver's decode of the previous
+    # allgather.  A hash-mode encode on a side stream during a gather-decode,
+    # against the two one after the other.
+    side = torch.cuda.Stream()
+    ce = encs["hash_cache"]
+    dec = encs["exponent_cache"]
+    dec.gather_decode()
+    flip2 = [0]
+
+    def serial():
+        flip2[0] ^= 1
+        dec.gather_decode()
+        ce.encode_reuse(x1 if flip2[0] else x2)
+
+    def overlapped():
+        flip2[0] ^= 1
+        ev = torch.cuda.Event()
+        ev.record(s)
+        side.wait_event(ev)
+        ce.encode_reuse(x1 if flip2[0] else x2, stream=side)
+        dec.gather_decode()
+        done = torch.cuda.Event()
+        done.record(side)
+        s.wait_event(done)
+
+    t_dec_alone = timed(lambda: dec.gather_decode())
+    t_serial = timed(serial)
+    t_overlap = timed(overlapped)
+    torch.cuda.synchronize()
+    if ce.status_word() or dec.status_word():
+        raise RuntimeError("overlap legs status")
     t_local = timed(local_step)
     t_local2 = timed(local_step_two_kernels)
     ok = rx.status_word() == 0
@@ -450,6 +485,12 @@ def run_extras(xs, n, W, flush, s, peak, reps=10):
         "reuse_encode_change_detection": {
             k: {"ms": round(v, 4), "uncompressed_GBs": round(2 * n / (v * 1e-3) / 1e9, 1),
                 "sender_cache_bytes": encs[k].geom["send_cache_bytes"]} for k, v in t_enc.items()},
+        "hash_encode_overlapped_with_gather_decode": {
+            "what": "raw reuse gather-decode (critical path) with a hash-mode raw reuse encode of the next "
+                    "iteration on a side stream",
+            "gather_decode_alone_ms": round(t_dec_alone, 4), "serial_ms": round(t_serial, 4),
+            "overlapped_ms": round(t_overlap, 4),
+            "encode_hidden_frac": round((t_serial - t_overlap) / max(t_serial - t_dec_alone, 1e-9), 3)},
     }
 
 
