@@ -82,9 +82,15 @@ struct RuDec {
 // one entry per kTile (8192) values of the shard: u64 changed blocks before
 // it, and for the coded variant a second u64, the escapes among the EXP
 // exponents of those blocks.
+// Blocks of a shard of n_s values: B is a power of two, so a shift instead of
+// a 64-bit division (a software routine on the GPU, paid by every thread).
+__device__ __forceinline__ uint64_t ru_blocks(uint64_t n_s, uint32_t B)
+{
+    return (n_s + B - 1) >> (__ffs((int)B) - 1);
+}
 __device__ __forceinline__ uint64_t ru_off_sm(uint64_t n_s, uint32_t B)
 {
-    return 64 + rup(cdiv(cdiv(n_s, B), 8), 16);
+    return 64 + rup(cdiv(ru_blocks(n_s, B), 8), 16);
 }
 __device__ __forceinline__ uint64_t ru_off_idx(uint64_t n_s, uint32_t B)
 {
@@ -360,7 +366,7 @@ __device__ __forceinline__ bool hash_group_changed(const RuEnc& a, uint32_t ci, 
 // block bits go into the tile's bitmap, whose count is published for the
 // scan and added to the shard totals.  The place step then reads the changed
 // exponents from x.
-__global__ void __launch_bounds__(kThreads, 6) k_reuse_hash_split(RuEnc a)
+__global__ void __launch_bounds__(kThreads, 5) k_reuse_hash_split(RuEnc a)
 {
     __shared__ uint32_t s_bm[32];
     const int t = threadIdx.x, lane = t & 31, wid = t >> 5;
@@ -371,8 +377,6 @@ __global__ void __launch_bounds__(kThreads, 6) k_reuse_hash_split(RuEnc a)
     const uint64_t v0 = (uint64_t)lt * kTile;
     const uint32_t nv = v0 < n_s ? (uint32_t)umin64(kTile, n_s - v0) : 0u;
     const uint32_t B = a.B, log2B = a.log2B;
-    const uint64_t nb = cdiv(n_s, B);
-    const uint64_t bm_bytes = cdiv(nb, 8);
     const uint64_t off_sm = ru_off_sm(n_s, B);
     const uint32_t tv = 32u * (uint32_t)t;
     const uint32_t cnt_v = tv < nv ? min(32u, nv - tv) : 0u;
@@ -478,6 +482,9 @@ __global__ void __launch_bounds__(kThreads, 6) k_reuse_hash_split(RuEnc a)
         }
     }
     __syncthreads();
+    // the shard's block count is needed only from here on (short live range)
+    const uint64_t nb = ru_blocks(n_s, B);
+    const uint64_t bm_bytes = cdiv(nb, 8);
     const uint32_t fin_tile = n_s ? (uint32_t)((n_s - 1) / kTile) : 0u;
     if (t < 32) {
         const uint32_t c = __popc(s_bm[lane]);
@@ -517,15 +524,15 @@ __global__ void __launch_bounds__(kThreads, 6) k_reuse_hash_split(RuEnc a)
 // the cache, and publish the tile's changed-block count as its look-back
 // aggregate.  The updated cache then holds every current exponent at its own
 // position, so the later steps read the changed exponents from it.
-template <bool kCoded>
+template <bool kCoded, bool kHash>
 __global__ void __launch_bounds__(kThreads, kCoded ? 4 : 6) k_reuse_split(RuEnc a)
 {
     __shared__ uint32_t s_gl[32], s_bm[32], s_pre[32];
     __shared__ uint32_t s_lut[kCoded ? 256 : 1];
     __shared__ unsigned long long s_warp[kCoded ? kThreads / 32 : 1];
     __shared__ __align__(16) uint32_t s_esc32[kCoded ? (kTile + 16) / 4 : 4];
-    __shared__ unsigned long long s_h[kCoded ? 2 * kThreads / 32 : 1];
-    __shared__ uint32_t s_ch[kCoded ? kThreads / 32 : 1];
+    __shared__ unsigned long long s_h[kHash ? 2 * kThreads / 32 : 1];
+    __shared__ uint32_t s_ch[kHash ? kThreads / 32 : 1];
     const int t = threadIdx.x, lane = t & 31, wid = t >> 5;
     // s_gl needs no clearing: lane 0 of every warp writes its entry of every
     // group below (a clear here could land after another warp's entry)
@@ -538,7 +545,7 @@ __global__ void __launch_bounds__(kThreads, kCoded ? 4 : 6) k_reuse_split(RuEnc 
     const uint64_t v0 = (uint64_t)lt * kTile;
     const uint32_t nv = v0 < n_s ? (uint32_t)umin64(kTile, n_s - v0) : 0u;
     const uint32_t B = a.B, log2B = a.log2B;
-    const uint64_t nb = cdiv(n_s, B);
+    const uint64_t nb = ru_blocks(n_s, B);
     const uint64_t bm_bytes = cdiv(nb, 8);
     const uint64_t off_sm = ru_off_sm(n_s, B);
     const uint16_t* xt = a.x + (uint64_t)ci * a.L + v0;
@@ -551,7 +558,7 @@ __global__ void __launch_bounds__(kThreads, kCoded ? 4 : 6) k_reuse_split(RuEnc 
     for (int g = 0; g < kGroups; g++) {
         const uint32_t v = 8u * (uint32_t)(g * kThreads + t);
         w[g] = ld_group16(xt, v, nv);
-        cv[g] = (v < nv && !a.cold && !a.hash) ? ld_group8(ct, v, nv) : 0ull;
+        cv[g] = (v < nv && !a.cold && !kHash) ? ld_group8(ct, v, nv) : 0ull;
     }
     // coded: the split may start while the shard statistics finish; nothing
     // above depends on them, everything below may
@@ -574,7 +581,7 @@ __global__ void __launch_bounds__(kThreads, kCoded ? 4 : 6) k_reuse_split(RuEnc 
                                       exp4_of(w[g].x, w[g].y)) & bmask;
         e8[g] = e;
         bool ch;
-        if (kCoded && a.hash) {   // the block's hash pair against the hash cache
+        if (kHash) {   // the block's hash pair against the hash cache
             const bool hch = hash_group_changed(a, ci, v0, v, n_s, e, s_h, s_ch);
             ch = vm && hch;
         } else {
@@ -612,7 +619,7 @@ __global__ void __launch_bounds__(kThreads, kCoded ? 4 : 6) k_reuse_split(RuEnc 
 #pragma unroll
     for (int g = 0; g < kGroups; g++) {
         const uint32_t v = 8u * (uint32_t)(g * kThreads + t);
-        if (!a.hash && v < nv && block_changed(s_bm, v >> log2B)) st_group8(ct, v, nv, e8[g]);
+        if (!kHash && v < nv && block_changed(s_bm, v >> log2B)) st_group8(ct, v, nv, e8[g]);
     }
     if (lt == fin_tile) {
         if (t < 16 && rup(bm_bytes, 16) > bm_bytes + t) o[64 + bm_bytes + t] = 0;
@@ -718,7 +725,7 @@ __global__ void __launch_bounds__(kThreads, 6) k_reuse_place(RuEnc a)
     const uint64_t v0 = (uint64_t)lt * kTile;
     const uint32_t nv = v0 < n_s ? (uint32_t)umin64(kTile, n_s - v0) : 0u;
     const uint32_t B = a.B, log2B = a.log2B;
-    const uint64_t nb = cdiv(n_s, B);
+    const uint64_t nb = ru_blocks(n_s, B);
     const uint64_t off_idx = ru_off_idx(n_s, B), off_exp = ru_off_exp(n_s, B, false);
     const uint8_t* ct = a.cache + (uint64_t)ci * a.L + v0;
     uint8_t* o = a.out + (uint64_t)ci * a.slot;
@@ -784,7 +791,7 @@ __global__ void __launch_bounds__(kThreads, 6) k_reuse_place32(RuEnc a)
     const uint64_t v0 = (uint64_t)lt * kTile;
     const uint32_t nv = v0 < n_s ? (uint32_t)umin64(kTile, n_s - v0) : 0u;
     const uint32_t B = a.B, log2B = a.log2B;
-    const uint64_t nb = cdiv(n_s, B);
+    const uint64_t nb = ru_blocks(n_s, B);
     const uint64_t off_idx = ru_off_idx(n_s, B), off_exp = ru_off_exp(n_s, B, false);
     const uint32_t tv = 32u * (uint32_t)t;
     const uint32_t cnt_v = tv < nv ? min(32u, nv - tv) : 0u;
@@ -1024,7 +1031,7 @@ __device__ __forceinline__ uint32_t ru_check_header(const uint8_t* p, uint64_t o
 // reads the payload offsets, then the bitmap slice, sign+mantissa bytes and
 // index entries are loaded before thread 0's header checks complete.
 template <bool kCoded>
-__global__ void __launch_bounds__(kThreads, 6) k_reuse_decode(RuDec a)
+__global__ void __launch_bounds__(kThreads, 5) k_reuse_decode(RuDec a)
 {
     __shared__ uint32_t s_bad, s_E0;
     __shared__ unsigned long long s_hdr[4];   // n_changed, m, n_esc
@@ -1039,7 +1046,7 @@ __global__ void __launch_bounds__(kThreads, 6) k_reuse_decode(RuDec a)
     const uint64_t v0 = (uint64_t)lt * kTile;
     const uint32_t nv = v0 < n_s ? (uint32_t)umin64(kTile, n_s - v0) : 0u;
     const uint32_t B = a.B, log2B = a.log2B;
-    const uint64_t nb = cdiv(n_s, B);
+    const uint64_t nb = ru_blocks(n_s, B);
     const uint64_t bm_bytes = cdiv(nb, 8);
     const uint64_t spans = cdiv(n_s, kTile);
     const uint64_t off = a.offsets ? __ldg(a.offsets + ci) : 0ull;
@@ -1265,7 +1272,7 @@ __global__ void __launch_bounds__(kThreads, 6) k_reuse_decode32(RuDec a)
     const uint64_t v0 = (uint64_t)lt * kTile;
     const uint32_t nv = v0 < n_s ? (uint32_t)umin64(kTile, n_s - v0) : 0u;
     const uint32_t B = a.B, log2B = a.log2B;
-    const uint64_t nb = cdiv(n_s, B);
+    const uint64_t nb = ru_blocks(n_s, B);
     const uint64_t bm_bytes = cdiv(nb, 8);
     const uint64_t spans = cdiv(n_s, kTile);
     const uint64_t off = a.offsets ? __ldg(a.offsets + ci) : 0ull;
@@ -1537,7 +1544,7 @@ cudaError_t launch_reuse_encode(const ez_plan_s* p, const uint16_t* x, uint32_t 
     }
     if (!coded) {
         if (a.hash) k_reuse_hash_split<<<tiles, kThreads, 0, s>>>(a);
-        else k_reuse_split<false><<<tiles, kThreads, 0, s>>>(a);
+        else k_reuse_split<false, false><<<tiles, kThreads, 0, s>>>(a);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
         e = launch_tile_scan(p, w.state_a, count, w.seg_a, w.counters + 4, w.counters + 7, dstatus, s);
@@ -1551,7 +1558,8 @@ cudaError_t launch_reuse_encode(const ez_plan_s* p, const uint16_t* x, uint32_t 
     a.plbuf = w.plbuf;
     a.escbuf = w.escbuf;
     a.state_b = w.state_b;
-    e = launch_dependent(k_reuse_split<true>, tiles, kThreads, 0, s, a);
+    e = a.hash ? launch_dependent(k_reuse_split<true, true>, tiles, kThreads, 0, s, a)
+               : launch_dependent(k_reuse_split<true, false>, tiles, kThreads, 0, s, a);
     if (e != cudaSuccess) return e;
     e = launch_tile_scan(p, w.state_a, count, w.seg_a, w.counters + 4, w.counters + 7, dstatus, s);
     if (e != cudaSuccess) return e;
