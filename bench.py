@@ -806,7 +806,10 @@ def run_e2e(args, world, xs, hosts, start, c3, ru, rc, s):
     return {"value": round(world * PASSES * 2 * n / (ms * 1e-3) / 1e9, 1), "unit": UNIT,
             "ms_per_step": round(ms, 4), "h2d_bytes_per_step": 2 * n,
             "d2h_bytes_per_step": int(out_sizes.numel() * 8),
-            "passes_ms_per_step": [round(t, 4) for t in times]}
+            "passes_ms_per_step": [round(t, 4) for t in times],
+            "note": "each step copies its BF16 input in from pinned host memory and reads the size tables and "
+                    "status words back; payloads and decoded tensors stay in device memory, where a collective "
+                    "would take them"}
 
 
 # ------------------------------------------------------------------ oracle
