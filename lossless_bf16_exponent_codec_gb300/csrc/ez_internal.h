@@ -57,6 +57,12 @@ uint64_t tile_scan_segments(uint64_t tpc);
 cudaError_t launch_tile_scan(const ez_plan_s* p, unsigned long long* st, uint32_t count,
                              unsigned long long* seg_st, uint32_t* counter, uint32_t* abort,
                              uint32_t* dstatus, cudaStream_t s);
+// The same for two state arrays of the same geometry (own segment states and
+// counters) in one launch.
+cudaError_t launch_tile_scan2(const ez_plan_s* p, unsigned long long* st0, unsigned long long* seg0,
+                              uint32_t* counter0, unsigned long long* st1, unsigned long long* seg1,
+                              uint32_t* counter1, uint32_t count, uint32_t* abort, uint32_t* dstatus,
+                              cudaStream_t s);
 
 cudaError_t launch_stats(const ez_plan_s* p, const uint16_t* x, uint64_t n, ez_stats_t* out,
                          const WsView& w, cudaStream_t s);

@@ -1561,9 +1561,9 @@ cudaError_t launch_reuse_encode(const ez_plan_s* p, const uint16_t* x, uint32_t 
     e = a.hash ? launch_dependent(k_reuse_split<true, true>, tiles, kThreads, 0, s, a)
                : launch_dependent(k_reuse_split<true, false>, tiles, kThreads, 0, s, a);
     if (e != cudaSuccess) return e;
-    e = launch_tile_scan(p, w.state_a, count, w.seg_a, w.counters + 4, w.counters + 7, dstatus, s);
-    if (e != cudaSuccess) return e;
-    e = launch_tile_scan(p, w.state_b, count, w.seg_b, w.counters + 5, w.counters + 7, dstatus, s);
+    // changed-block and escape prefixes in one launch
+    e = launch_tile_scan2(p, w.state_a, w.seg_a, w.counters + 4, w.state_b, w.seg_b, w.counters + 5, count,
+                          w.counters + 7, dstatus, s);
     if (e != cudaSuccess) return e;
     return launch_dependent(k_reuse_place_coded, tiles, kPlaceThreads, 0, s, a);
 }

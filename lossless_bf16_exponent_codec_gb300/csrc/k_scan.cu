@@ -9,7 +9,8 @@
 // One CTA scans a segment of kScanSpan entries of one chunk (8 per thread,
 // one block scan); segments of a chunk are chained by a decoupled look-back
 // over per-segment states (ids from an atomic counter, so a segment waits
-// only on running ones; every wait bounded).
+// only on running ones; every wait bounded).  The coded reuse encoder scans
+// its changed-block and escape counts in one launch of two halves.
 #include "ez_internal.h"
 #include "ez_common.cuh"
 
@@ -19,10 +20,19 @@ using namespace ez;
 constexpr uint32_t kScanPer = 8;
 constexpr uint32_t kScanSpan = kThreads * kScanPer;   // 2048 tile entries per CTA
 
-__global__ void __launch_bounds__(kThreads) k_tile_scan(unsigned long long* st, uint32_t count,
-                                                        uint32_t tpc, uint32_t spc,
-                                                        unsigned long long* seg_st,
-                                                        uint32_t* counter, uint32_t* abort,
+// One state array to scan: per-tile counts, per-segment look-back states and
+// the ticket counter of its segments.
+struct ScanArr {
+    unsigned long long* st;
+    unsigned long long* seg_st;
+    uint32_t* counter;
+};
+
+// Scans one or two state arrays of the same geometry in one launch: CTAs
+// [0, count * spc) take the first array, the rest the second; each array has
+// its own ticket counter, so a look-back only ever waits on the same array.
+__global__ void __launch_bounds__(kThreads) k_tile_scan(ScanArr A0, ScanArr A1, uint32_t count,
+                                                        uint32_t tpc, uint32_t spc, uint32_t* abort,
                                                         uint32_t* dstatus)
 {
     __shared__ uint32_t s_tile;
@@ -31,10 +41,11 @@ __global__ void __launch_bounds__(kThreads) k_tile_scan(unsigned long long* st, 
     const int t = threadIdx.x;
     grid_dep_launch();
     grid_dep_wait();   // the counts come from the kernel before
-    const uint32_t id = next_tile(counter, &s_tile);
+    const ScanArr A = blockIdx.x < count * spc ? A0 : A1;
+    const uint32_t id = next_tile(A.counter, &s_tile);
     const uint32_t c = id / spc, sg = id % spc;   // segments of a chunk in order
     if (c >= count) return;
-    unsigned long long* sc = st + (uint64_t)c * tpc;
+    unsigned long long* sc = A.st + (uint64_t)c * tpc;
     const uint32_t base = sg * kScanSpan + (uint32_t)t * kScanPer;
     unsigned long long v[kScanPer];
     unsigned long long sum = 0;
@@ -45,7 +56,7 @@ __global__ void __launch_bounds__(kThreads) k_tile_scan(unsigned long long* st, 
     }
     unsigned long long total;
     const unsigned long long excl = block_excl_scan(sum, s_warp, &total);
-    const unsigned long long P = tile_prefix(seg_st, c * spc + sg, c * spc, total, &s_prefix,
+    const unsigned long long P = tile_prefix(A.seg_st, c * spc + sg, c * spc, total, &s_prefix,
                                              dstatus, abort);
     unsigned long long run = P + excl;
 #pragma unroll
@@ -62,8 +73,21 @@ cudaError_t launch_tile_scan(const ez_plan_s* p, unsigned long long* st, uint32_
     const uint32_t spc = (uint32_t)cdiv(p->tpc, kScanSpan);
     const uint64_t ctas = (uint64_t)count * spc;
     if (ctas > 0x7fffffffull) return cudaErrorInvalidValue;
-    return launch_dependent(k_tile_scan, (unsigned)ctas, kThreads, 0, s, st, count, p->tpc, spc, seg_st,
-                            counter, abort, dstatus);
+    const ScanArr A{st, seg_st, counter};
+    return launch_dependent(k_tile_scan, (unsigned)ctas, kThreads, 0, s, A, A, count, p->tpc, spc, abort,
+                            dstatus);
+}
+
+cudaError_t launch_tile_scan2(const ez_plan_s* p, unsigned long long* st0, unsigned long long* seg0,
+                              uint32_t* counter0, unsigned long long* st1, unsigned long long* seg1,
+                              uint32_t* counter1, uint32_t count, uint32_t* abort, uint32_t* dstatus,
+                              cudaStream_t s)
+{
+    const uint32_t spc = (uint32_t)cdiv(p->tpc, kScanSpan);
+    const uint64_t ctas = 2ull * count * spc;
+    if (ctas > 0x7fffffffull) return cudaErrorInvalidValue;
+    return launch_dependent(k_tile_scan, (unsigned)ctas, kThreads, 0, s, ScanArr{st0, seg0, counter0},
+                            ScanArr{st1, seg1, counter1}, count, p->tpc, spc, abort, dstatus);
 }
 
 uint64_t tile_scan_segments(uint64_t tpc) { return cdiv(tpc, kScanSpan); }

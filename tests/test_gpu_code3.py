@@ -120,6 +120,14 @@ def _dist(kind, n, seed):
         return rng.integers(0, 65536, n, dtype=np.uint32).astype(np.uint16)
     elif kind == "const":
         return np.full(n, 0x3F80, np.uint16)
+    elif kind in ("spiky", "spiky2"):
+        # outliers x100 and zeros: 0.5% / 0.1% (a few queued groups per tile),
+        # or 1% / 0.1% (about as many as a tile's queue holds)
+        v = rng.normal(0, 0.02, n)
+        u = rng.random(n)
+        big = 0.005 if kind == "spiky" else 0.01
+        v = np.where(u < big, v * 100.0, v)
+        v = np.where((u >= big) & (u < big + 0.001), 0.0, v)
     elif kind == "naninf":
         x = (rng.normal(0, 0.02, n).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
         x[::17] = 0x7F80
@@ -131,7 +139,7 @@ def _dist(kind, n, seed):
 
 
 @pytest.mark.parametrize("kind", ["wide", "mean", "sub", "bits", "const", "naninf",
-                                  "1.0", "1e-30", "3e30", "0.02"])
+                                  "1.0", "1e-30", "3e30", "0.02", "spiky", "spiky2"])
 @pytest.mark.parametrize("n", [0, 1, 2, 3, 5000, 40000, 300001])
 def test_stats_distributions(ez, orc, kind, n):
     binding, codec = ez
