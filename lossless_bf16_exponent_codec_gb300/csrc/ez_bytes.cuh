@@ -5,8 +5,8 @@
 // decoder must put the next popc(m) bytes of that list back at the set bits
 // of m.  Both are byte permutations that depend only on m, so they are done
 // with PRMT (__byte_perm) instead of a per-escape loop: the encoder takes its
-// selectors from a compile-time table indexed by m, the decoder computes them
-// with integer multiplies.
+// selectors from a compile-time table indexed by m (copied to shared memory
+// by each CTA), the decoder computes them with integer multiplies.
 #pragma once
 
 #include <cstdint>
@@ -43,14 +43,25 @@ constexpr ByteTables make_byte_tables()
 
 __device__ const ByteTables kByteTables = make_byte_tables();
 
+// The compaction selectors in shared memory (comp[m] = comp_lo[m],
+// comp[256 + m] = comp_hi[m]), filled by the CTA's first 256 threads before a
+// barrier: a shared load on the staging path instead of a global one.
+__device__ __forceinline__ void fill_comp_table(uint32_t* comp, int t)
+{
+    if (t < 256) {
+        comp[t] = kByteTables.comp_lo[t];
+        comp[256 + t] = kByteTables.comp_hi[t];
+    }
+}
+
 // Append the bytes of (lo, hi) selected by m to s[r ...].  kmax is the
 // largest popc(m) over the warp (warp-uniform), so the store loop does not
-// diverge.
+// diverge.  comp: the selector table of fill_comp_table.
 __device__ __forceinline__ void stage_selected(uint8_t* s, uint32_t r, uint32_t m, uint32_t lo,
-                                               uint32_t hi, uint32_t kmax)
+                                               uint32_t hi, uint32_t kmax, const uint32_t* comp)
 {
-    const uint32_t c_lo = __byte_perm(lo, hi, __ldg(&kByteTables.comp_lo[m]));
-    const uint32_t c_hi = __byte_perm(lo, hi, __ldg(&kByteTables.comp_hi[m]));
+    const uint32_t c_lo = __byte_perm(lo, hi, comp[m]);
+    const uint32_t c_hi = __byte_perm(lo, hi, comp[256 + m]);
     const uint32_t cnt = __popc(m);
 #pragma unroll
     for (uint32_t k = 0; k < 8; k++) {

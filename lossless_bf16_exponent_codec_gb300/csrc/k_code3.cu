@@ -165,6 +165,7 @@ __global__ void __launch_bounds__(kEncThreads, 3) k_code3_encode(C3Enc a)
     __shared__ uint32_t s_sci[kSlots], s_slt[kSlots], s_sagg[kSlots];
     __shared__ uint32_t s_efull[kSlots], s_edone[kSlots];
     __shared__ unsigned long long s_warp[kCompute / 32];
+    __shared__ uint32_t s_comp[2 * 256];
     const int t = threadIdx.x;
     grid_dep_wait();   // the counters were cleared by the kernel before
     uint32_t E0 = __ldg(&a.st->E0);
@@ -173,6 +174,7 @@ __global__ void __launch_bounds__(kEncThreads, 3) k_code3_encode(C3Enc a)
         E0 = 0;
     }
     if (t < 256) s_lut[t] = c3_lut_entry((uint32_t)t, E0);
+    fill_comp_table(s_comp, t);
     if (t < kStages) {
         mbar_init(&s_full[t], 1);
         s_empty[t] = 0;
@@ -292,7 +294,7 @@ __global__ void __launch_bounds__(kEncThreads, 3) k_code3_encode(C3Enc a)
                 if (kmax) {
                     const uint32_t r = gbase + (uint32_t)((excl >> (16 * g)) & 0xFFFFull);
                     stage_selected(S.esc[es], r, m, exp4_of(w[g].x, w[g].y), exp4_of(w[g].z, w[g].w),
-                                   kmax);
+                                   kmax, s_comp);
                 }
                 gbase += (uint32_t)((total >> (16 * g)) & 0xFFFFull);
             }

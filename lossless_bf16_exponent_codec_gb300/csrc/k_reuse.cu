@@ -529,6 +529,7 @@ __global__ void __launch_bounds__(kThreads, kCoded ? 4 : 6) k_reuse_split(RuEnc 
 {
     __shared__ uint32_t s_gl[32], s_bm[32], s_pre[32];
     __shared__ uint32_t s_lut[kCoded ? 256 : 1];
+    __shared__ uint32_t s_comp[kCoded ? 2 * 256 : 1];
     __shared__ unsigned long long s_warp[kCoded ? kThreads / 32 : 1];
     __shared__ __align__(16) uint32_t s_esc32[kCoded ? (kTile + 16) / 4 : 4];
     __shared__ unsigned long long s_h[kHash ? 2 * kThreads / 32 : 1];
@@ -570,6 +571,7 @@ __global__ void __launch_bounds__(kThreads, kCoded ? 4 : 6) k_reuse_split(RuEnc 
             E0 = 0;
         }
         s_lut[t] = ru_lut_entry((uint32_t)t, E0);
+        fill_comp_table(s_comp, t);
     }
     unsigned long long e8[kGroups];
 #pragma unroll
@@ -662,7 +664,7 @@ __global__ void __launch_bounds__(kThreads, kCoded ? 4 : 6) k_reuse_split(RuEnc 
         const uint32_t kmax = __reduce_max_sync(kFull, (uint32_t)__popc(mm));
         if (kmax) {
             const uint32_t q = gbase + (uint32_t)((excl >> (16 * g)) & 0xFFFFull);
-            stage_selected(s_esc, q, mm, (uint32_t)e8[g], (uint32_t)(e8[g] >> 32), kmax);
+            stage_selected(s_esc, q, mm, (uint32_t)e8[g], (uint32_t)(e8[g] >> 32), kmax, s_comp);
         }
         gbase += (uint32_t)((total >> (16 * g)) & 0xFFFFull);
     }
