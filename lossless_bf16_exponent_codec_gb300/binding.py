@@ -25,7 +25,7 @@ DSTAT_TIMEOUT, DSTAT_MISALIGNED, DSTAT_BAD_STATS = 8, 16, 32
 STATS_BYTES = 2120          # sizeof(ez_stats_t)
 FP8_STATS_BYTES = 328       # sizeof(ez_fp8_stats_t)
 EZ_FLAG_WINDOW_HIST = 1     # plan flag: window from the histogram's densest 7-bin run
-EZ_FLAG_HASH_CACHE = 2      # plan flag: sender cache of block hash pairs (reuse, B >= 32)
+EZ_FLAG_HASH_CACHE = 2      # plan flag: sender cache of block hash pairs (reuse codecs, any block size)
 NOALLOC_SCRATCH_BYTES = 4 << 20   # EZ_NOALLOC_SCRATCH_BYTES
 
 ENTRY_POINTS = ("ez_plan_create", "ez_plan_destroy", "ez_plan_sizes", "ez_stats",

@@ -523,9 +523,11 @@ __global__ void __launch_bounds__(kThreads, 5) k_reuse_hash_split(RuEnc a)
 // (one ballot per 8-value group), write the changed blocks' exponents into
 // the cache, and publish the tile's changed-block count as its look-back
 // aggregate.  The updated cache then holds every current exponent at its own
-// position, so the later steps read the changed exponents from it.
+// position, so the later steps read the changed exponents from it.  (The
+// hashing coded instance is held to 40 registers, 6 CTAs per SM: 2.4% faster
+// than at 64.)
 template <bool kCoded, bool kHash>
-__global__ void __launch_bounds__(kThreads, kCoded ? 4 : 6) k_reuse_split(RuEnc a)
+__global__ void __launch_bounds__(kThreads, (kCoded && !kHash) ? 4 : 6) k_reuse_split(RuEnc a)
 {
     __shared__ uint32_t s_gl[32], s_bm[32], s_pre[32];
     __shared__ uint32_t s_lut[kCoded ? 256 : 1];
