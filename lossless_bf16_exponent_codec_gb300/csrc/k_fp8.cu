@@ -160,7 +160,10 @@ __device__ __forceinline__ void load32(const uint8_t* p, uint32_t cnt, uint32_t*
     }
 #pragma unroll
     for (int q = 0; q < 8; q++) w[q] = 0;
-    for (uint32_t i = 0; i < cnt; i++) w[i >> 2] |= (uint32_t)p[i] << (8 * (i & 3));
+    // fixed indexes, so that w stays in registers
+#pragma unroll
+    for (uint32_t i = 0; i < 32; i++)
+        if (i < cnt) w[i >> 2] |= (uint32_t)p[i] << (8 * (i & 3));
 }
 
 // =================================================================== statistics
@@ -438,11 +441,14 @@ struct F8Enc {
 
 // One CTA per tile of kF8Spans index spans (4 x 8192 values), tiles taken in
 // order from a counter (dealt round-robin over the chunks), so a tile's
-// look-back only waits on tiles whose CTAs already run.  Span by span: the
-// planes are stored at once, a block scan places each thread's escapes in the
-// tile's shared staging area; one look-back per tile then gives the escape
-// prefix, the index entries of its spans and the place of the staged escapes
-// (on a chunk's last tile also the header, padding and size).
+// look-back only waits on tiles whose CTAs already run.  Span by span (each
+// thread's 32 bytes of the next span requested while the current one is
+// coded; the block scans alternate between two warp-total buffers, so a span
+// costs one barrier): the planes are stored at once, a block scan places each
+// thread's escapes in the tile's shared staging area; one look-back per tile
+// then gives the escape prefix, the index entries of its spans and the place
+// of the staged escapes (on a chunk's last tile also the header, padding and
+// size).
 constexpr uint32_t kF8Spans = 4;
 constexpr uint32_t kF8TileV = kF8Spans * kTile;
 
@@ -450,7 +456,7 @@ template <uint32_t kCodec>
 __global__ void __launch_bounds__(kThreads) k_fp8_encode(F8Enc a)
 {
     __shared__ uint32_t s_tile;
-    __shared__ unsigned long long s_warp[kThreads / 32];
+    __shared__ unsigned long long s_warp[2][kThreads / 32];   // by span parity
     __shared__ unsigned long long s_prefix;
     __shared__ uint32_t s_base[kF8Spans + 1];
     __shared__ __align__(16) uint8_t s_esc[kF8TileV + 16];
@@ -476,15 +482,31 @@ __global__ void __launch_bounds__(kThreads) k_fp8_encode(F8Enc a)
     uint8_t* esc = idx + f8_idx_bytes(n_c);
     const uint32_t tv = 32u * (uint32_t)t;
     uint32_t base = 0;                 // escapes of the tile's earlier spans (uniform)
+    // the next span's 32 bytes are requested while the current one is coded
+    uint4 pa = make_uint4(0, 0, 0, 0), pb = make_uint4(0, 0, 0, 0);
+    {
+        const uint64_t v0 = (uint64_t)lt * kF8Spans * kTile;
+        if (v0 + tv + 32 <= n_c) {
+            const uint8_t* q = a.x + (uint64_t)ci * a.L + v0 + tv;
+            pa = ld_v4_nc(q);
+            pb = ld_v4_nc(q + 16);
+        }
+    }
 #pragma unroll 1
     for (uint32_t sp = 0; sp < kF8Spans; sp++) {
         const uint64_t v0 = ((uint64_t)lt * kF8Spans + sp) * kTile;
         const uint32_t nv = v0 < n_c ? (uint32_t)umin64(kTile, n_c - v0) : 0u;
         const uint32_t cnt_v = tv < nv ? min(32u, nv - tv) : 0u;
+        uint32_t w[8] = {pa.x, pa.y, pa.z, pa.w, pb.x, pb.y, pb.z, pb.w};
+        if (sp + 1 < kF8Spans && v0 + kTile + tv + 32 <= n_c) {
+            const uint8_t* q = a.x + (uint64_t)ci * a.L + v0 + kTile + tv;
+            pa = ld_v4_nc(q);
+            pb = ld_v4_nc(q + 16);
+        }
         uint32_t escm = 0, e[5] = {0, 0, 0, 0, 0};
         if (cnt_v) {
-            uint32_t w[8], R[8];
-            load32(a.x + (uint64_t)ci * a.L + v0 + tv, cnt_v, w);
+            uint32_t R[8];
+            if (cnt_v < 32) load32(a.x + (uint64_t)ci * a.L + v0 + tv, cnt_v, w);
             to_planes(w, R);
             const uint32_t vm = cnt_v == 32 ? 0xFFFFFFFFu : ((1u << cnt_v) - 1u);
             // d = E - E0 over the exponent planes R[m .. m+ebits)
@@ -513,7 +535,7 @@ __global__ void __launch_bounds__(kThreads) k_fp8_encode(F8Enc a)
             *reinterpret_cast<uint32_t*>(pt + (nsm + 2) * plane) = (d[2] ^ (d[1] & d[0])) & in;
         }
         unsigned long long tot;
-        const unsigned long long ex = block_excl_scan(__popc(escm), s_warp, &tot);
+        const unsigned long long ex = block_excl_scan(__popc(escm), s_warp[sp & 1u], &tot);
         // the thread's escapes, in value order (raw exponent fields), staged
         uint32_t m = escm, r = base + (uint32_t)ex;
         while (m) {
@@ -526,7 +548,8 @@ __global__ void __launch_bounds__(kThreads) k_fp8_encode(F8Enc a)
         }
         if (t == 0) s_base[sp] = base;
         base += (uint32_t)tot;
-        __syncthreads();   // s_warp is read before the next span's scan writes it
+        // the next span's scan writes the other s_warp buffer; this one is
+        // written again two spans on, after the next scan's barrier
     }
     const unsigned long long P = tile_prefix(a.state, ci * tpt + lt, ci * tpt, base, &s_prefix,
                                              a.dstatus, a.abort);
