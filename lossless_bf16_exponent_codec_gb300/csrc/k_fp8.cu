@@ -441,22 +441,23 @@ struct F8Enc {
 
 // One CTA per tile of kF8Spans index spans (4 x 8192 values), tiles taken in
 // order from a counter (dealt round-robin over the chunks), so a tile's
-// look-back only waits on tiles whose CTAs already run.  Span by span (each
-// thread's 32 bytes of the next span requested while the current one is
-// coded; the block scans alternate between two warp-total buffers, so a span
-// costs one barrier): the planes are stored at once, a block scan places each
-// thread's escapes in the tile's shared staging area; one look-back per tile
-// then gives the escape prefix, the index entries of its spans and the place
-// of the staged escapes (on a chunk's last tile also the header, padding and
-// size).
+// look-back only waits on tiles whose CTAs already run.  Two spans at a time
+// (each thread's 32 bytes of both requested together; one block scan of the
+// pair's two escape counts, on one of two alternating warp-total buffers, so
+// a pair costs one barrier): the planes are stored at once, the scan places
+// each thread's escapes in the tile's shared staging area; one look-back per
+// tile then gives the escape prefix, the index entries of its spans and the
+// place of the staged escapes (on a chunk's last tile also the header,
+// padding and size).
 constexpr uint32_t kF8Spans = 4;
+static_assert(kF8Spans % 2 == 0, "spans are coded in pairs");
 constexpr uint32_t kF8TileV = kF8Spans * kTile;
 
 template <uint32_t kCodec>
 __global__ void __launch_bounds__(kThreads) k_fp8_encode(F8Enc a)
 {
     __shared__ uint32_t s_tile;
-    __shared__ unsigned long long s_warp[2][kThreads / 32];   // by span parity
+    __shared__ unsigned long long s_warp[2][kThreads / 32];   // by span-pair parity
     __shared__ unsigned long long s_prefix;
     __shared__ uint32_t s_base[kF8Spans + 1];
     __shared__ __align__(16) uint8_t s_esc[kF8TileV + 16];
@@ -482,74 +483,84 @@ __global__ void __launch_bounds__(kThreads) k_fp8_encode(F8Enc a)
     uint8_t* esc = idx + f8_idx_bytes(n_c);
     const uint32_t tv = 32u * (uint32_t)t;
     uint32_t base = 0;                 // escapes of the tile's earlier spans (uniform)
-    // the next span's 32 bytes are requested while the current one is coded
-    uint4 pa = make_uint4(0, 0, 0, 0), pb = make_uint4(0, 0, 0, 0);
-    {
-        const uint64_t v0 = (uint64_t)lt * kF8Spans * kTile;
-        if (v0 + tv + 32 <= n_c) {
-            const uint8_t* q = a.x + (uint64_t)ci * a.L + v0 + tv;
-            pa = ld_v4_nc(q);
-            pb = ld_v4_nc(q + 16);
-        }
-    }
+    // spans in pairs: both spans' bytes requested together, one block scan of
+    // the two escape counts (16-bit fields; a span holds at most 8192)
 #pragma unroll 1
-    for (uint32_t sp = 0; sp < kF8Spans; sp++) {
-        const uint64_t v0 = ((uint64_t)lt * kF8Spans + sp) * kTile;
-        const uint32_t nv = v0 < n_c ? (uint32_t)umin64(kTile, n_c - v0) : 0u;
-        const uint32_t cnt_v = tv < nv ? min(32u, nv - tv) : 0u;
-        uint32_t w[8] = {pa.x, pa.y, pa.z, pa.w, pb.x, pb.y, pb.z, pb.w};
-        if (sp + 1 < kF8Spans && v0 + kTile + tv + 32 <= n_c) {
-            const uint8_t* q = a.x + (uint64_t)ci * a.L + v0 + kTile + tv;
-            pa = ld_v4_nc(q);
-            pb = ld_v4_nc(q + 16);
-        }
-        uint32_t escm = 0, e[5] = {0, 0, 0, 0, 0};
-        if (cnt_v) {
-            uint32_t R[8];
-            if (cnt_v < 32) load32(a.x + (uint64_t)ci * a.L + v0 + tv, cnt_v, w);
-            to_planes(w, R);
-            const uint32_t vm = cnt_v == 32 ? 0xFFFFFFFFu : ((1u << cnt_v) - 1u);
-            // d = E - E0 over the exponent planes R[m .. m+ebits)
-            uint32_t d[5], br = 0;
+    for (uint32_t sp = 0; sp < kF8Spans; sp += 2) {
+        uint32_t w[2][8];
+        uint32_t cnt[2];
 #pragma unroll
-            for (int j = 0; j < 5; j++) {
-                if (j < (int)f.ebits) {
-                    const uint32_t ej = R[f.mbits + j], k = bitmask_of(E0, j);
-                    e[j] = ej;
-                    d[j] = ej ^ k ^ br;
-                    br = borrow3(ej, k, br);
-                } else {
-                    d[j] = 0;
-                }
+        for (int h = 0; h < 2; h++) {
+            const uint64_t v0 = ((uint64_t)lt * kF8Spans + sp + h) * kTile;
+            const uint32_t nv = v0 < n_c ? (uint32_t)umin64(kTile, n_c - v0) : 0u;
+            cnt[h] = tv < nv ? min(32u, nv - tv) : 0u;
+            if (cnt[h] == 32) {
+                const uint8_t* q = a.x + (uint64_t)ci * a.L + v0 + tv;
+                const uint4 x0 = ld_v4_nc(q), x1 = ld_v4_nc(q + 16);
+                w[h][0] = x0.x; w[h][1] = x0.y; w[h][2] = x0.z; w[h][3] = x0.w;
+                w[h][4] = x1.x; w[h][5] = x1.y; w[h][6] = x1.z; w[h][7] = x1.w;
+            } else {
+                load32(a.x + (uint64_t)ci * a.L + v0 + tv, cnt[h], w[h]);
             }
-            const uint32_t in = ~br & ~(d[3] | d[4]) & ~(d[0] & d[1] & d[2]) & vm;
-            escm = ~in & vm;
-            // sign/mantissa planes: mantissa bits, then the sign
-            uint8_t* pt = pl + (v0 + tv) / 8;
+        }
+        uint32_t escm[2] = {0, 0}, e[2][5];
 #pragma unroll
-            for (uint32_t q = 0; q < 4; q++)
-                if (q < nsm) *reinterpret_cast<uint32_t*>(pt + q * plane) = (q < f.mbits ? R[q] : R[7]) & vm;
-            // code = d + 1 inside the window
-            *reinterpret_cast<uint32_t*>(pt + nsm * plane) = ~d[0] & in;
-            *reinterpret_cast<uint32_t*>(pt + (nsm + 1) * plane) = (d[1] ^ d[0]) & in;
-            *reinterpret_cast<uint32_t*>(pt + (nsm + 2) * plane) = (d[2] ^ (d[1] & d[0])) & in;
+        for (int h = 0; h < 2; h++) {
+#pragma unroll
+            for (int j = 0; j < 5; j++) e[h][j] = 0;
+            const uint32_t cnt_v = cnt[h];
+            if (cnt_v) {
+                const uint64_t v0 = ((uint64_t)lt * kF8Spans + sp + h) * kTile;
+                uint32_t R[8];
+                to_planes(w[h], R);
+                const uint32_t vm = cnt_v == 32 ? 0xFFFFFFFFu : ((1u << cnt_v) - 1u);
+                // d = E - E0 over the exponent planes R[m .. m+ebits)
+                uint32_t d[5], br = 0;
+#pragma unroll
+                for (int j = 0; j < 5; j++) {
+                    if (j < (int)f.ebits) {
+                        const uint32_t ej = R[f.mbits + j], k = bitmask_of(E0, j);
+                        e[h][j] = ej;
+                        d[j] = ej ^ k ^ br;
+                        br = borrow3(ej, k, br);
+                    } else {
+                        d[j] = 0;
+                    }
+                }
+                const uint32_t in = ~br & ~(d[3] | d[4]) & ~(d[0] & d[1] & d[2]) & vm;
+                escm[h] = ~in & vm;
+                // sign/mantissa planes: mantissa bits, then the sign
+                uint8_t* pt = pl + (v0 + tv) / 8;
+#pragma unroll
+                for (uint32_t q = 0; q < 4; q++)
+                    if (q < nsm) *reinterpret_cast<uint32_t*>(pt + q * plane) = (q < f.mbits ? R[q] : R[7]) & vm;
+                // code = d + 1 inside the window
+                *reinterpret_cast<uint32_t*>(pt + nsm * plane) = ~d[0] & in;
+                *reinterpret_cast<uint32_t*>(pt + (nsm + 1) * plane) = (d[1] ^ d[0]) & in;
+                *reinterpret_cast<uint32_t*>(pt + (nsm + 2) * plane) = (d[2] ^ (d[1] & d[0])) & in;
+            }
         }
         unsigned long long tot;
-        const unsigned long long ex = block_excl_scan(__popc(escm), s_warp[sp & 1u], &tot);
+        const unsigned long long ex = block_excl_scan((unsigned long long)__popc(escm[0]) |
+                                                          (unsigned long long)__popc(escm[1]) << 16,
+                                                      s_warp[(sp >> 1) & 1u], &tot);
         // the thread's escapes, in value order (raw exponent fields), staged
-        uint32_t m = escm, r = base + (uint32_t)ex;
-        while (m) {
-            const int i = __ffs(m) - 1;
-            m &= m - 1;
-            uint32_t eb = 0;
 #pragma unroll
-            for (int j = 0; j < 5; j++) eb |= ((e[j] >> i) & 1u) << j;
-            s_esc[r++] = (uint8_t)eb;
+        for (int h = 0; h < 2; h++) {
+            uint32_t m = escm[h], r = base + (uint32_t)((ex >> (16 * h)) & 0xFFFFull);
+            while (m) {
+                const int i = __ffs(m) - 1;
+                m &= m - 1;
+                uint32_t eb = 0;
+#pragma unroll
+                for (int j = 0; j < 5; j++) eb |= ((e[h][j] >> i) & 1u) << j;
+                s_esc[r++] = (uint8_t)eb;
+            }
+            if (t == 0) s_base[sp + h] = base;
+            base += (uint32_t)((tot >> (16 * h)) & 0xFFFFull);
         }
-        if (t == 0) s_base[sp] = base;
-        base += (uint32_t)tot;
-        // the next span's scan writes the other s_warp buffer; this one is
-        // written again two spans on, after the next scan's barrier
+        // the next pair's scan writes the other s_warp buffer; this one is
+        // written again two pairs on, after the next scan's barrier
     }
     const unsigned long long P = tile_prefix(a.state, ci * tpt + lt, ci * tpt, base, &s_prefix,
                                              a.dstatus, a.abort);
