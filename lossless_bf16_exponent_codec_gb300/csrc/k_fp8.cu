@@ -600,7 +600,7 @@ struct F8Dec {
 // the index is checked against the span's own escape count, so the escapes
 // read always lie inside the escape section.
 // kVPT values per thread in kVPT / 32 words of 32 values (64: 128 threads per
-// span, so the per-thread setup -- offsets, header verdict, scan, index
+// span, so the per-thread setup -- offsets, header checks, scan, index
 // checks -- is spread over 64 one-byte values: 0.160 -> 0.124 ms at 2^28).
 template <uint32_t kCodec, int kVPT>
 __global__ void __launch_bounds__(kTile / kVPT) k_fp8_decode(F8Dec a)
