@@ -80,6 +80,20 @@ __device__ __forceinline__ void merge4(uint32_t sm4, uint32_t e4, uint32_t& lo, 
 // Tile ids are dealt round-robin over the `count` shards of a launch, so the
 // shards' look-back chains advance side by side; state index is
 // shard-contiguous (shard ci owns [ci*tpc, (ci+1)*tpc)).
+// n / d for 32-bit n and d >= 1 by one multiply: rcp = floor((2^64 - 1) / d)
+// + 1 (0 stands for d = 1).  With 2^64 = q d + r, n * rcp / 2^64 exceeds n / d
+// by less than n / 2^64 < 1 / d, and the fractional part of n / d is at most
+// 1 - 1 / d, so the floor is n / d exactly (for a power of two rcp = 2^64 / d).
+struct FastDiv {
+    uint32_t d, pad;
+    unsigned long long rcp;
+};
+inline FastDiv make_fastdiv(uint32_t d) { return FastDiv{d, 0u, d > 1 ? ~0ull / d + 1 : 0ull}; }
+__device__ __forceinline__ uint32_t fdiv(uint32_t n, const FastDiv& f)
+{
+    return f.rcp ? (uint32_t)__umul64hi((unsigned long long)n, f.rcp) : n;
+}
+
 struct TilePos {
     uint32_t ci, lt, state;
 };
@@ -90,6 +104,20 @@ __device__ __forceinline__ TilePos tile_pos(uint32_t id, uint32_t count, uint32_
     p.lt = id / count;
     p.state = p.ci * tpc + p.lt;
     return p;
+}
+__device__ __forceinline__ TilePos tile_pos(uint32_t id, const FastDiv& count, uint32_t tpc)
+{
+    TilePos p;
+    p.lt = fdiv(id, count);
+    p.ci = id - p.lt * count.d;
+    p.state = p.ci * tpc + p.lt;
+    return p;
+}
+// Chunk ci and tile lt of CTA id over chunks of tpc tiles.
+__device__ __forceinline__ void chunk_tile(uint32_t id, const FastDiv& tpc, uint32_t& ci, uint32_t& lt)
+{
+    ci = fdiv(id, tpc);
+    lt = id - ci * tpc.d;
 }
 
 // ---- memory helpers ----------------------------------------------------------

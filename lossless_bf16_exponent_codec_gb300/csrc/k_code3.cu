@@ -52,6 +52,9 @@ struct C3Dec {
     unsigned long long* state;
     uint32_t* counter;
     uint32_t* abort;
+    FastDiv tpcd;                 // tpc, for the CTA index split
+    unsigned long long full_plane, full_sec_pl, full_sec_idx, full_sec_esc;   // sections of an L-value chunk
+    unsigned long long full_nidx;   // its index entries, ceil(L / kTile) (tpc is at least 1, this may be 0)
 };
 
 // Escape index: one u64 per kTile (8192) values of the chunk, the number of
@@ -429,7 +432,8 @@ __global__ void __launch_bounds__(kThreads, kAcc ? 4 : 5) k_code3_decode(C3Dec a
     __shared__ uint32_t s_warp32[kThreads / 32];
     __shared__ __align__(16) uint32_t s_esc32[(kTile + 32) / 4];
     const int t = threadIdx.x;
-    const uint32_t ci = blockIdx.x / a.tpc, lt = blockIdx.x % a.tpc;
+    uint32_t ci, lt;
+    chunk_tile(blockIdx.x, a.tpcd, ci, lt);
     const uint32_t c = a.first + ci;
     const uint64_t n_c = shard_values(a.n, a.L, c);
     const uint64_t v0 = (uint64_t)lt * kTile;
@@ -437,11 +441,13 @@ __global__ void __launch_bounds__(kThreads, kAcc ? 4 : 5) k_code3_decode(C3Dec a
     const uint64_t off = __ldg(a.offsets + ci), end = __ldg(a.offsets + ci + 1);
     const uint64_t avail = end >= off ? end - off : 0ull;
     const uint8_t* p = a.in + off;
-    const uint64_t plane = rup(cdiv(n_c, 8), 128);
-    const uint64_t sec_pl = 128 + rup(n_c, 128);
-    const uint64_t sec_idx = sec_pl + 3 * plane;
-    const uint64_t sec_esc = sec_idx + c3_idx_bytes(n_c);
-    const uint64_t n_idx = cdiv(n_c, kTile);
+    // sections: precomputed for a full chunk (every chunk but a short last one)
+    const bool full = n_c == a.L;
+    const uint64_t plane = full ? a.full_plane : rup(cdiv(n_c, 8), 128);
+    const uint64_t sec_pl = full ? a.full_sec_pl : 128 + rup(n_c, 128);
+    const uint64_t sec_idx = full ? a.full_sec_idx : sec_pl + 3 * plane;
+    const uint64_t sec_esc = full ? a.full_sec_esc : sec_idx + c3_idx_bytes(n_c);
+    const uint64_t n_idx = full ? a.full_nidx : cdiv(n_c, kTile);
     // all fixed sections inside the payload: safe to read before the header
     const bool fixed_ok = (off & 15u) == 0 && end >= off && avail >= sec_esc;
     // thread t owns the 32 consecutive values [32t, 32t + 32) of the tile:
@@ -673,6 +679,12 @@ cudaError_t launch_code3_decode(const ez_plan_s* p, const uint8_t* in, const uin
     a.state = w.state_a;
     a.counter = w.counters + 1;
     a.abort = w.counters + 7;
+    a.tpcd = make_fastdiv(p->tpc);
+    a.full_plane = rup(cdiv(p->L, 8), 128);
+    a.full_sec_pl = 128 + rup(p->L, 128);
+    a.full_sec_idx = a.full_sec_pl + 3 * a.full_plane;
+    a.full_sec_esc = a.full_sec_idx + rup(8 * cdiv(p->L, kTile), 128);
+    a.full_nidx = cdiv(p->L, kTile);
     const uint64_t tiles = (uint64_t)count * p->tpc;
     if (acc) k_code3_decode<true><<<(unsigned)tiles, kThreads, 0, s>>>(a);
     else k_code3_decode<false><<<(unsigned)tiles, kThreads, 0, s>>>(a);

@@ -593,6 +593,7 @@ struct F8Dec {
     uint32_t* dstatus;
     uint64_t n, L;
     uint32_t W, first, count, tpc;
+    FastDiv tpcd;         // tpc, for the CTA index split
 };
 
 // One CTA per 8192-value span, no inter-span dependence (the span's escape
@@ -614,7 +615,8 @@ __global__ void __launch_bounds__(kTile / kVPT) k_fp8_decode(F8Dec a)
     const int t = threadIdx.x;
     constexpr Fp8Fmt f = fp8_fmt(kCodec);
     constexpr uint32_t nsm = 1 + f.mbits;
-    const uint32_t ci = blockIdx.x / a.tpc, lt = blockIdx.x % a.tpc;
+    uint32_t ci, lt;
+    chunk_tile(blockIdx.x, a.tpcd, ci, lt);
     const uint32_t c = a.first + ci;
     const uint64_t n_c = shard_values(a.n, a.L, c);
     const uint64_t v0 = (uint64_t)lt * kTile;
@@ -857,6 +859,7 @@ cudaError_t launch_fp8_decode(const ez_plan_s* p, const uint8_t* in, const uint6
     a.first = first;
     a.count = count;
     a.tpc = p->tpc;
+    a.tpcd = make_fastdiv(p->tpc);
     const uint64_t tiles = (uint64_t)count * p->tpc;
     if (tiles > 0x7fffffffull) return cudaErrorInvalidValue;
     if (p->codec == EZ_CODEC_FP8_E5M2)

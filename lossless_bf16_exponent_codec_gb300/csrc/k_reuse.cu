@@ -60,6 +60,7 @@ struct RuEnc {
     // shard first+i at byte i * hstride
     int hash;
     uint64_t hstride;
+    FastDiv countd;       // count, for the tile-position split
 };
 
 
@@ -76,6 +77,7 @@ struct RuDec {
     unsigned long long* state_b;
     uint32_t* counter;
     uint32_t* abort;
+    FastDiv tpcd;         // tpc, for the CTA index split
 };
 
 // Payload sections: header 64 | bitmap | SM | index | EXP.  The index holds
@@ -371,7 +373,7 @@ __global__ void __launch_bounds__(kThreads, 5) k_reuse_hash_split(RuEnc a)
     __shared__ uint32_t s_bm[32];
     const int t = threadIdx.x, lane = t & 31, wid = t >> 5;
     if (t < 32) s_bm[t] = 0;
-    const TilePos tp = tile_pos(blockIdx.x, a.count, a.tpc);
+    const TilePos tp = tile_pos(blockIdx.x, a.countd, a.tpc);
     const uint32_t ci = tp.ci, lt = tp.lt;
     const uint64_t n_s = shard_values(a.n, a.L, a.first + ci);
     const uint64_t v0 = (uint64_t)lt * kTile;
@@ -525,7 +527,8 @@ __global__ void __launch_bounds__(kThreads, 5) k_reuse_hash_split(RuEnc a)
 // aggregate.  The updated cache then holds every current exponent at its own
 // position, so the later steps read the changed exponents from it.  (The
 // hashing coded instance is held to 40 registers, 6 CTAs per SM: 2.4% faster
-// than at 64.)
+// than at 64.  The coding instance keeps the plain division in tile_pos: with
+// the multiply it is compiled to 56 registers, or, held to 40, runs 2% slower.)
 template <bool kCoded, bool kHash>
 __global__ void __launch_bounds__(kThreads, (kCoded && !kHash) ? 4 : 6) k_reuse_split(RuEnc a)
 {
@@ -722,7 +725,7 @@ __global__ void __launch_bounds__(kThreads, 6) k_reuse_place(RuEnc a)
     const int t = threadIdx.x;
     grid_dep_wait();   // prefixes, cache and staging come from the kernels before
     if (t < 32) s_bm[t] = 0;
-    const TilePos tp = tile_pos(blockIdx.x, a.count, a.tpc);
+    const TilePos tp = tile_pos(blockIdx.x, a.countd, a.tpc);
     const uint32_t ci = tp.ci, lt = tp.lt;
     const uint32_t r = a.first + ci;
     const uint64_t n_s = shard_values(a.n, a.L, r);
@@ -788,7 +791,7 @@ __global__ void __launch_bounds__(kThreads, 6) k_reuse_place32(RuEnc a)
     const int t = threadIdx.x;
     grid_dep_wait();   // prefixes, cache and staging come from the kernels before
     if (t < 32) s_bm[t] = 0;
-    const TilePos tp = tile_pos(blockIdx.x, a.count, a.tpc);
+    const TilePos tp = tile_pos(blockIdx.x, a.countd, a.tpc);
     const uint32_t ci = tp.ci, lt = tp.lt;
     const uint32_t r = a.first + ci;
     const uint64_t n_s = shard_values(a.n, a.L, r);
@@ -874,7 +877,7 @@ __global__ void __launch_bounds__(kPlaceThreads) k_reuse_place_coded(RuEnc a)
     __shared__ __align__(16) uint32_t s_e[kSpecBytes / 4 + 4];
     const int t = threadIdx.x;
     grid_dep_wait();   // prefixes, cache and staging come from the kernels before
-    const TilePos tp = tile_pos(blockIdx.x, a.count, a.tpc);
+    const TilePos tp = tile_pos(blockIdx.x, a.countd, a.tpc);
     const uint32_t ci = tp.ci, lt = tp.lt;
     const uint32_t r = a.first + ci;
     const uint64_t n_s = shard_values(a.n, a.L, r);
@@ -1044,7 +1047,8 @@ __global__ void __launch_bounds__(kThreads, 5) k_reuse_decode(RuDec a)
     __shared__ __align__(16) uint32_t s_esc32[kCoded ? (kTile + 32) / 4 : 4];
     const int t = threadIdx.x;
     if (t < 32) s_bm[t] = 0;   // warp 0, which alone ORs the bitmap bytes in below
-    const uint32_t ci = blockIdx.x / a.tpc, lt = blockIdx.x % a.tpc;
+    uint32_t ci, lt;
+    chunk_tile(blockIdx.x, a.tpcd, ci, lt);
     const uint32_t r = a.first + ci;
     const uint64_t n_s = shard_values(a.n, a.L, r);
     const uint64_t v0 = (uint64_t)lt * kTile;
@@ -1270,7 +1274,8 @@ __global__ void __launch_bounds__(kThreads, 6) k_reuse_decode32(RuDec a)
     __shared__ __align__(16) uint32_t s_esc32[kCoded ? (kTile + 32) / 4 : 4];
     const int t = threadIdx.x;
     if (t < 32) s_bm[t] = 0;   // warp 0, which alone ORs the bitmap bytes in below
-    const uint32_t ci = blockIdx.x / a.tpc, lt = blockIdx.x % a.tpc;
+    uint32_t ci, lt;
+    chunk_tile(blockIdx.x, a.tpcd, ci, lt);
     const uint32_t r = a.first + ci;
     const uint64_t n_s = shard_values(a.n, a.L, r);
     const uint64_t v0 = (uint64_t)lt * kTile;
@@ -1531,6 +1536,7 @@ cudaError_t launch_reuse_encode(const ez_plan_s* p, const uint16_t* x, uint32_t 
     a.first = first;
     a.count = count;
     a.tpc = p->tpc;
+    a.countd = make_fastdiv(count);
     a.cold = cold ? 1 : 0;
     a.state = w.state_a;
     a.counter = w.counters + 0;
@@ -1592,6 +1598,7 @@ cudaError_t launch_reuse_decode(const ez_plan_s* p, const uint8_t* in, const uin
     a.first = first;
     a.count = count;
     a.tpc = p->tpc;
+    a.tpcd = make_fastdiv(p->tpc);
     a.state_a = w.state_a;
     a.state_b = w.state_b;
     a.counter = w.counters + 3;
