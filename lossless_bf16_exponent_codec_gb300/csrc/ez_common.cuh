@@ -68,12 +68,14 @@ __device__ __forceinline__ uint32_t exp4_of(uint32_t a, uint32_t b)
 // exponent bytes: per value ((sm & 0x80) << 8) | (E << 7) | (sm & 0x7F).
 __device__ __forceinline__ void merge4(uint32_t sm4, uint32_t e4, uint32_t& lo, uint32_t& hi)
 {
-    // X halves = E << 8 | sm ; then pick E << 7 from X >> 1, mantissa from X,
-    // sign from X << 8
-    const uint32_t x0 = __byte_perm(sm4, e4, 0x5140);
-    const uint32_t x1 = __byte_perm(sm4, e4, 0x7362);
-    lo = ((x0 >> 1) & 0x7F807F80u) | (x0 & 0x007F007Fu) | ((x0 << 8) & 0x80008000u);
-    hi = ((x1 >> 1) & 0x7F807F80u) | (x1 & 0x007F007Fu) | ((x1 << 8) & 0x80008000u);
+    // per 16-bit lane: A = sm with its sign replicated over the high byte
+    // (bits 0..6 the mantissa, bit 15 the sign), E = exponent in the high
+    // byte; E >> 1 puts it at bits 7..14, and one LOP3 takes bits 0..6 and 15
+    // from A, the rest from E >> 1
+    const uint32_t a0 = __byte_perm(sm4, 0u, 0x9180), a1 = __byte_perm(sm4, 0u, 0xB3A2);
+    const uint32_t e0 = __byte_perm(e4, 0u, 0x1404) >> 1, e1 = __byte_perm(e4, 0u, 0x3424) >> 1;
+    asm("lop3.b32 %0, %1, %2, %3, 0xE2;" : "=r"(lo) : "r"(a0), "r"(0x807F807Fu), "r"(e0));
+    asm("lop3.b32 %0, %1, %2, %3, 0xE2;" : "=r"(hi) : "r"(a1), "r"(0x807F807Fu), "r"(e1));
 }
 
 // ---- tile order ----------------------------------------------------------------
