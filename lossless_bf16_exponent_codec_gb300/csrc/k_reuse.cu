@@ -1269,7 +1269,7 @@ __global__ void __launch_bounds__(kThreads, 6) k_reuse_decode32(RuDec a)
 {
     __shared__ uint32_t s_bad, s_E0;
     __shared__ unsigned long long s_hdr[4];   // n_changed, m, n_esc
-    __shared__ uint32_t s_bm[32], s_pre[32], s_agg;
+    __shared__ uint32_t s_bm[32];
     __shared__ uint32_t s_warp32[kThreads / 32];
     __shared__ __align__(16) uint32_t s_esc32[kCoded ? (kTile + 32) / 4 : 4];
     const int t = threadIdx.x;
@@ -1340,19 +1340,21 @@ __global__ void __launch_bounds__(kThreads, 6) k_reuse_decode32(RuDec a)
         if (lt == 0 && t == 0) atomicOr(a.dstatus, s_bad);
         return;
     }
-    if (t < 32) {
-        const uint32_t c = __popc(s_bm[t]);
-        uint32_t x = c;
+    // the span's bitmap is at most kTile / 32 = 256 bits, 8 words: every
+    // thread sums their popcounts itself (the span's changed blocks, and those
+    // before its own block) instead of waiting on a warp's scan
+    const uint32_t nbw = (uint32_t)((kTile >> log2B) + 31) >> 5;
+    const uint32_t kb = (32u * (uint32_t)t) >> log2B;   // this thread's block in the span
+    uint32_t agg32 = 0, pre32 = 0;
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t y = __shfl_up_sync(kFull, x, o);
-            if (t >= o) x += y;
+    for (uint32_t w = 0; w < kTile / 32 / 32; w++) {
+        if (w < nbw) {
+            const uint32_t bw = s_bm[w];
+            agg32 += __popc(bw);
+            pre32 += w < (kb >> 5) ? __popc(bw) : (w == (kb >> 5) ? __popc(bw & ((1u << (kb & 31)) - 1u)) : 0u);
         }
-        s_pre[t] = x - c;
-        if (t == 31) s_agg = x;
     }
-    __syncthreads();
-    const unsigned long long agg = s_agg;
+    const unsigned long long agg = agg32;
     const uint64_t n_changed = s_hdr[0], m = s_hdr[1], n_esc = s_hdr[2];
     const uint32_t E0 = s_E0;
     // index checks on the changed-block prefix
@@ -1374,7 +1376,7 @@ __global__ void __launch_bounds__(kThreads, 6) k_reuse_decode32(RuDec a)
     // this thread's block: changed (exponents from the stream) or not (cache)
     const uint32_t k = tv >> log2B;
     bool chg = cnt_v && block_changed(s_bm, k);
-    const uint64_t pos = (P + block_rank(s_bm, s_pre, k)) * B + (tv & (B - 1u));
+    const uint64_t pos = (P + pre32) * B + (tv & (B - 1u));
     if (chg && pos + cnt_v > m) {
         // an m smaller than the bitmap says: never read past the section
         atomicOr(a.dstatus, EZ_DSTAT_BAD_COUNT);
