@@ -22,6 +22,8 @@
 #include "ez_bytes.cuh"
 #include "ez_tma.cuh"
 
+#include <type_traits>
+
 namespace ezk {
 using namespace ez;
 
@@ -400,14 +402,6 @@ __global__ void __launch_bounds__(kEncThreads, 3) k_code3_encode(C3Enc a)
     }
 }
 
-// Exponent bytes of a group from its code bytes (1..7 -> E0+code-1); the
-// bytes of escapes are placeholders.
-__device__ __forceinline__ unsigned long long codes_to_exps(unsigned long long c8, uint32_t E0)
-{
-    if (E0 == 0) return ((c8 | 0x8080808080808080ull) - 0x0101010101010101ull) & 0x7F7F7F7F7F7F7F7Full;
-    return c8 + (unsigned long long)(E0 - 1) * 0x0101010101010101ull;
-}
-
 __device__ __forceinline__ uint4 ld_v4_plain(const void* p)
 {
     return *reinterpret_cast<const uint4*>(p);
@@ -586,10 +580,16 @@ __global__ void __launch_bounds__(kThreads, kAcc ? 4 : 5) k_code3_decode(C3Dec a
         }
     }
     const uint32_t smv[8] = {smw[0].x, smw[0].y, smw[0].z, smw[0].w, smw[1].x, smw[1].y, smw[1].z, smw[1].w};
+    // the window base decides the code -> exponent step once per thread, not
+    // per group: two instances of the loop
+    const unsigned long long K = (unsigned long long)(E0 - 1) * 0x0101010101010101ull;
+    auto expand = [&](auto zero) {
+    constexpr bool kZero = decltype(zero)::value;
 #pragma unroll
     for (int g = 0; g < 4; g++) {
         const uint32_t b0 = (p0 >> (8 * g)) & 0xFFu, b1 = (p1 >> (8 * g)) & 0xFFu, b2 = (p2 >> (8 * g)) & 0xFFu;
-        unsigned long long e8 = codes_to_exps(codes8(b0, b1, b2), E0);
+        unsigned long long e8 = codes8(b0, b1, b2);
+        e8 = kZero ? ((e8 | 0x8080808080808080ull) - 0x0101010101010101ull) & 0x7F7F7F7F7F7F7F7Full : e8 + K;
         const uint32_t m = (esc >> (8 * g)) & 0xFFu;
         if (m) {
             const uint32_t r = excl + __popc(esc & ((1u << (8 * g)) - 1u));
@@ -628,6 +628,9 @@ __global__ void __launch_bounds__(kThreads, kAcc ? 4 : 5) k_code3_decode(C3Dec a
             for (uint32_t i = 0; i < cnt_v - v; i++) ot[v + i] = (uint16_t)(hw[i >> 1] >> (16 * (i & 1)));
         }
     }
+    };
+    if (E0 == 0) expand(std::true_type{});
+    else expand(std::false_type{});
 }
 
 cudaError_t launch_code3_encode(const ez_plan_s* p, const uint16_t* x, uint32_t first,

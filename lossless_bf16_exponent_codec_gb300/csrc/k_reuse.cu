@@ -33,6 +33,8 @@
 #include "ez_common.cuh"
 #include "ez_bytes.cuh"
 
+#include <type_traits>
+
 namespace ezk {
 using namespace ez;
 
@@ -1220,15 +1222,20 @@ __global__ void __launch_bounds__(kThreads, 5) k_reuse_decode(RuDec a)
             return;
         }
         uint32_t gbase = 0;
+        // the window base decides the code -> exponent step once, not per
+        // group: two instances of the loop
+        const unsigned long long K = (unsigned long long)(E0 - 1) * 0x0101010101010101ull;
+        auto expand = [&](auto zero) {
+        constexpr bool kZero = decltype(zero)::value;
 #pragma unroll
         for (int g = 0; g < kGroups; g++) {
             const uint32_t q = gbase + (uint32_t)((excl >> (16 * g)) & 0xFFFFull);
             gbase += (uint32_t)((total >> (16 * g)) & 0xFFFFull);
             if (!chg[g]) continue;
             const unsigned long long c8 = codes8(pbs[g] & 0xFFu, (pbs[g] >> 8) & 0xFFu, (pbs[g] >> 16) & 0xFFu);
-            unsigned long long e = (E0 == 0)
+            unsigned long long e = kZero
                 ? ((c8 | 0x8080808080808080ull) - 0x0101010101010101ull) & 0x7F7F7F7F7F7F7F7Full
-                : c8 + (unsigned long long)(E0 - 1) * 0x0101010101010101ull;
+                : c8 + K;
             const uint32_t mm = (emasks >> (8 * g)) & 0xFFu;
             if (mm) {
                 uint32_t c_lo, c_hi;
@@ -1238,6 +1245,9 @@ __global__ void __launch_bounds__(kThreads, 5) k_reuse_decode(RuDec a)
             const uint32_t cnt = min(8u, nv - (8u * (uint32_t)(g * kThreads + t)));
             ev[g] = cnt >= 8 ? e : (e & byte_mask((1u << cnt) - 1u));
         }
+        };
+        if (E0 == 0) expand(std::true_type{});
+        else expand(std::false_type{});
     }
 
 #pragma unroll
@@ -1462,13 +1472,18 @@ __global__ void __launch_bounds__(kThreads, 6) k_reuse_decode32(RuDec a)
         }
         if (chg) {
             uint32_t ev32[8];
+            // the window base decides the code -> exponent step once, not per
+            // group: two instances of the loop
+            const unsigned long long K = (unsigned long long)(E0 - 1) * 0x0101010101010101ull;
+            auto expand = [&](auto zero) {
+            constexpr bool kZero = decltype(zero)::value;
 #pragma unroll
             for (int g = 0; g < 4; g++) {
                 const unsigned long long c8 = codes8((p0 >> (8 * g)) & 0xFFu, (p1 >> (8 * g)) & 0xFFu,
                                                      (p2 >> (8 * g)) & 0xFFu);
-                unsigned long long e = (E0 == 0)
+                unsigned long long e = kZero
                     ? ((c8 | 0x8080808080808080ull) - 0x0101010101010101ull) & 0x7F7F7F7F7F7F7F7Full
-                    : c8 + (unsigned long long)(E0 - 1) * 0x0101010101010101ull;
+                    : c8 + K;
                 const uint32_t mm = (esc >> (8 * g)) & 0xFFu;
                 if (mm) {
                     const uint32_t q = excl + __popc(esc & ((1u << (8 * g)) - 1u));
@@ -1479,6 +1494,9 @@ __global__ void __launch_bounds__(kThreads, 6) k_reuse_decode32(RuDec a)
                 ev32[2 * g] = (uint32_t)e;
                 ev32[2 * g + 1] = (uint32_t)(e >> 32);
             }
+            };
+            if (E0 == 0) expand(std::true_type{});
+            else expand(std::false_type{});
             ew[0] = make_uint4(ev32[0], ev32[1], ev32[2], ev32[3]);
             ew[1] = make_uint4(ev32[4], ev32[5], ev32[6], ev32[7]);
         }

@@ -109,6 +109,20 @@ def test_edge_shapes(ez, orc, n, W, B, coded):
     run_iterations(ez, orc, [x0, x1, x2], W, B, coded, single=(n % 2 == 0))
 
 
+@pytest.mark.parametrize("B", [32, 256])
+def test_coded_window_base_zero(ez, orc, B):
+    """Values near zero (exponent fields 0..3): the shard windows start at
+    E0 = 0, the decoders' other code -> exponent step."""
+    rng = np.random.default_rng(77 + B)
+    n, W = 3 * 8192 + 777, 4
+    x0 = ((rng.integers(0, 2, n) << 15) | (rng.integers(0, 4, n) << 7) | rng.integers(0, 128, n)).astype(np.uint16)
+    x1 = x0.copy()
+    x1[rng.random(n) < 0.01] ^= 0x0080
+    L = orc.shard_count(n, W, 0)
+    assert orc.stats(x1[:L])["E0"] == 0
+    run_iterations(ez, orc, [x0, x1], W, B, True)
+
+
 def test_empty_tensor(ez, orc):
     for coded in (False, True):
         c = codec_of(ez, 0, 4, 64, coded)
