@@ -253,21 +253,25 @@ __global__ void __launch_bounds__(kEncThreads, 3) k_code3_encode(C3Enc a)
             const uint16_t* xt = a.x + (uint64_t)ci * a.L + v0;
 
             uint4 w[kGroups];
+            uint32_t emasks = 0;
+            unsigned long long packed = 0;
+            // a full tile (every one but a chunk's short last) takes an
+            // instance of the loops without the per-group bounds
+            auto code_tile = [&](auto full_tag) {
+            constexpr bool kFullTile = decltype(full_tag)::value;
 #pragma unroll
             for (int g = 0; g < kGroups; g++) {
                 const uint32_t v = 8u * (uint32_t)(g * kCompute + t);
-                w[g] = (v + 8 <= nv) ? lds128(S.in[s] + 2 * v) : load_group(xt, v, nv);
+                w[g] = (kFullTile || v + 8 <= nv) ? lds128(S.in[s] + 2 * v) : load_group(xt, v, nv);
             }
-            uint32_t emasks = 0;
-            unsigned long long packed = 0;
 #pragma unroll
             for (int g = 0; g < kGroups; g++) {
                 const uint32_t j = (uint32_t)(g * kCompute + t);
                 const uint32_t v = 8u * j;
-                if (v >= nv) continue;
+                if (!kFullTile && v >= nv) continue;
                 uint32_t acc = group_codes(s_lut, w[g]);
                 const uint32_t sm_lo = sm4_of(w[g].x, w[g].y), sm_hi = sm4_of(w[g].z, w[g].w);
-                if (nv - v >= 8) {
+                if (kFullTile || nv - v >= 8) {
                     *reinterpret_cast<uint2*>(sm_sec + v0 + v) = make_uint2(sm_lo, sm_hi);
                 } else {
                     const uint32_t vm = (1u << (nv - v)) - 1u;
@@ -282,6 +286,9 @@ __global__ void __launch_bounds__(kEncThreads, 3) k_code3_encode(C3Enc a)
                 emasks |= esc << (8 * g);
                 packed |= (unsigned long long)__popc(esc) << (16 * g);
             }
+            };
+            if (nv == (uint32_t)kTile) code_tile(std::true_type{});
+            else code_tile(std::false_type{});
             if (t == 0 && !wait_flag(&vedone[es], eround, a.abort)) atomicOr(a.dstatus, EZ_DSTAT_TIMEOUT);
             unsigned long long total;
             const unsigned long long excl = compute_excl_scan(packed, s_warp, &total);

@@ -560,13 +560,19 @@ __global__ void __launch_bounds__(kThreads, (kCoded && !kHash) ? 4 : 6) k_reuse_
     uint8_t* ct = a.cache + (uint64_t)ci * a.L + v0;
     uint8_t* o = a.out + (uint64_t)ci * a.slot;
 
+    // a full tile (every one but a shard's short last) takes an instance
+    // without the per-group bounds
+    auto split_tile = [&](auto full_tag) {
+    constexpr bool kFullTile = decltype(full_tag)::value;
     uint4 w[kGroups];
     unsigned long long cv[kGroups];
 #pragma unroll
     for (int g = 0; g < kGroups; g++) {
         const uint32_t v = 8u * (uint32_t)(g * kThreads + t);
-        w[g] = ld_group16(xt, v, nv);
-        cv[g] = (v < nv && !a.cold && !kHash) ? ld_group8(ct, v, nv) : 0ull;
+        w[g] = kFullTile ? ld_v4_nc(xt + v) : ld_group16(xt, v, nv);
+        cv[g] = ((kFullTile || v < nv) && !a.cold && !kHash)
+                    ? (kFullTile ? __ldg(reinterpret_cast<const unsigned long long*>(ct + v)) : ld_group8(ct, v, nv))
+                    : 0ull;
     }
     // coded: the split may start while the shard statistics finish; nothing
     // above depends on them, everything below may
@@ -584,7 +590,7 @@ __global__ void __launch_bounds__(kThreads, (kCoded && !kHash) ? 4 : 6) k_reuse_
 #pragma unroll
     for (int g = 0; g < kGroups; g++) {
         const uint32_t v = 8u * (uint32_t)(g * kThreads + t);
-        const uint32_t vm = vmask_of(v, nv);
+        const uint32_t vm = kFullTile ? 0xFFu : vmask_of(v, nv);
         const unsigned long long bmask = vm == 0xFFu ? ~0ull : bytemask_of(vm);
         const unsigned long long e = ((unsigned long long)exp4_of(w[g].z, w[g].w) << 32 |
                                       exp4_of(w[g].x, w[g].y)) & bmask;
@@ -601,7 +607,8 @@ __global__ void __launch_bounds__(kThreads, (kCoded && !kHash) ? 4 : 6) k_reuse_
         if (vm) {
             const unsigned long long smw = (unsigned long long)sm4_of(w[g].z, w[g].w) << 32 |
                                            sm4_of(w[g].x, w[g].y);
-            st_group8(o + off_sm + v0, v, nv, smw);
+            if (kFullTile) *reinterpret_cast<unsigned long long*>(o + off_sm + v0 + v) = smw;
+            else st_group8(o + off_sm + v0, v, nv, smw);
         }
     }
     __syncthreads();
@@ -628,7 +635,10 @@ __global__ void __launch_bounds__(kThreads, (kCoded && !kHash) ? 4 : 6) k_reuse_
 #pragma unroll
     for (int g = 0; g < kGroups; g++) {
         const uint32_t v = 8u * (uint32_t)(g * kThreads + t);
-        if (!kHash && v < nv && block_changed(s_bm, v >> log2B)) st_group8(ct, v, nv, e8[g]);
+        if (!kHash && (kFullTile || v < nv) && block_changed(s_bm, v >> log2B)) {
+            if (kFullTile) *reinterpret_cast<unsigned long long*>(ct + v) = e8[g];
+            else st_group8(ct, v, nv, e8[g]);
+        }
     }
     if (lt == fin_tile) {
         if (t < 16 && rup(bm_bytes, 16) > bm_bytes + t) o[64 + bm_bytes + t] = 0;
@@ -644,12 +654,12 @@ __global__ void __launch_bounds__(kThreads, (kCoded && !kHash) ? 4 : 6) k_reuse_
 #pragma unroll
     for (int g = 0; g < kGroups; g++) {
         const uint32_t v = 8u * (uint32_t)(g * kThreads + t);
-        if (v >= nv) continue;
+        if (!kFullTile && v >= nv) continue;
         const uint32_t k = v >> log2B;
         if (!block_changed(s_bm, k)) continue;
         const uint32_t local = block_rank(s_bm, s_pre, k) * B + (v - (k << log2B));
         const uint32_t acc = codes_of_bytes(s_lut, (uint32_t)e8[g], (uint32_t)(e8[g] >> 32)) &
-                             (vmask_of(v, nv) * 0x01010101u);
+                             (kFullTile ? 0xFFFFFFFFu : vmask_of(v, nv) * 0x01010101u);
         const uint32_t pb = local >> 3;
         pst[pb] = (uint8_t)acc;
         pst[kTile / 8 + pb] = (uint8_t)(acc >> 8);
@@ -678,6 +688,10 @@ __global__ void __launch_bounds__(kThreads, (kCoded && !kHash) ? 4 : 6) k_reuse_
     __syncthreads();
     uint32_t* dst = reinterpret_cast<uint32_t*>(a.escbuf + (uint64_t)ci * a.L + v0);
     for (uint32_t i = (uint32_t)t; i < (agg2 + 3) / 4; i += kThreads) dst[i] = s_esc32[i];
+    };
+    if (nv == (uint32_t)kTile) split_tile(std::true_type{});
+    else split_tile(std::false_type{});
+
 }
 
 // This tile's slice of the bitmap, read back from the payload: s_bm, the
