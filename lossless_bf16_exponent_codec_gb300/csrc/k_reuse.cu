@@ -1325,7 +1325,9 @@ __global__ void __launch_bounds__(kThreads, 6) k_reuse_decode32(RuDec a)
     const uint32_t nbt = (uint32_t)kTile >> log2B;
     const uint64_t bm0 = (uint64_t)lt * (nbt / 8);
     const uint32_t tv = 32u * (uint32_t)t;
-    const uint32_t cnt_v = tv < nv ? min(32u, nv - tv) : 0u;
+    auto span_body = [&](auto full_tag) {
+    constexpr bool kFullSpan = decltype(full_tag)::value;
+    const uint32_t cnt_v = kFullSpan ? 32u : tv < nv ? min(32u, nv - tv) : 0u;
     uint32_t bmb = 0;
     uint4 smw[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
     unsigned long long ib_here = 0, ib_next = 0, ie_here = 0, ie_next = 0;
@@ -1539,6 +1541,15 @@ __global__ void __launch_bounds__(kThreads, 6) k_reuse_decode32(RuDec a)
             const uint32_t hw[4] = {o4.x, o4.y, o4.z, o4.w};
             for (uint32_t i = 0; i < cnt_v - v; i++) ot[v + i] = (uint16_t)(hw[i >> 1] >> (16 * (i & 1)));
         }
+    }
+    };
+    // the raw decoder takes an instance for a full span (every one but a
+    // shard's short last); the coded one is faster without it
+    if constexpr (!kCoded) {
+        if (nv == (uint32_t)kTile) span_body(std::true_type{});
+        else span_body(std::false_type{});
+    } else {
+        span_body(std::false_type{});
     }
 }
 
