@@ -383,7 +383,9 @@ __global__ void __launch_bounds__(kThreads, 5) k_reuse_hash_split(RuEnc a)
     const uint32_t B = a.B, log2B = a.log2B;
     const uint64_t off_sm = ru_off_sm(n_s, B);
     const uint32_t tv = 32u * (uint32_t)t;
-    const uint32_t cnt_v = tv < nv ? min(32u, nv - tv) : 0u;
+    auto span_body = [&](auto full_tag) {
+    constexpr bool kFullSpan = decltype(full_tag)::value;
+    const uint32_t cnt_v = kFullSpan ? 32u : tv < nv ? min(32u, nv - tv) : 0u;
     const uint16_t* xt = a.x + (uint64_t)ci * a.L + v0 + tv;
     uint8_t* o = a.out + (uint64_t)ci * a.slot;
     uint32_t xw[16];
@@ -519,6 +521,9 @@ __global__ void __launch_bounds__(kThreads, 5) k_reuse_hash_split(RuEnc a)
         if (t < 16 && rup(bm_bytes, 16) > bm_bytes + t) o[64 + bm_bytes + t] = 0;
         if (t < 16 && rup(n_s, 16) > n_s + t) o[off_sm + n_s + t] = 0;
     }
+    };
+    if (nv == (uint32_t)kTile) span_body(std::true_type{});
+    else span_body(std::false_type{});
 }
 
 // Step A of both reuse encoders, one CTA per 8192-value tile with no
@@ -817,7 +822,9 @@ __global__ void __launch_bounds__(kThreads, 6) k_reuse_place32(RuEnc a)
     const uint64_t nb = ru_blocks(n_s, B);
     const uint64_t off_idx = ru_off_idx(n_s, B), off_exp = ru_off_exp(n_s, B, false);
     const uint32_t tv = 32u * (uint32_t)t;
-    const uint32_t cnt_v = tv < nv ? min(32u, nv - tv) : 0u;
+    auto span_body = [&](auto full_tag) {
+    constexpr bool kFullSpan = decltype(full_tag)::value;
+    const uint32_t cnt_v = kFullSpan ? 32u : tv < nv ? min(32u, nv - tv) : 0u;
     const uint8_t* ct = a.cache + (uint64_t)ci * a.L + v0 + tv;
     uint8_t* o = a.out + (uint64_t)ci * a.slot;
     const unsigned long long* sc = a.state + (uint64_t)ci * a.tpc;
@@ -861,6 +868,9 @@ __global__ void __launch_bounds__(kThreads, 6) k_reuse_place32(RuEnc a)
         if (t < 16 && ib + t < ru_idx_bytes(n_s, false)) o[off_idx + ib + t] = 0;
         if (t == 0) a.sizes[ci] = total;
     }
+    };
+    if (nv == (uint32_t)kTile) span_body(std::true_type{});
+    else span_body(std::false_type{});
 }
 
 // Bytes [b, b+16) of a run of `len` bytes at dst, from d (bytes past len
