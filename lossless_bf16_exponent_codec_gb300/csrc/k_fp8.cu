@@ -31,6 +31,8 @@
 // share an address or a bank); the last CTA forms the exact sums of the
 // finite values and of their squares from the 256 pattern counts as 128-bit
 // integers, rounds each once to double and places the window as for BF16.
+#include <type_traits>
+
 #include "ez_internal.h"
 #include "ez_common.cuh"
 
@@ -484,84 +486,95 @@ __global__ void __launch_bounds__(kThreads) k_fp8_encode(F8Enc a)
     const uint32_t tv = 32u * (uint32_t)t;
     uint32_t base = 0;                 // escapes of the tile's earlier spans (uniform)
     // spans in pairs: both spans' bytes requested together, one block scan of
-    // the two escape counts (16-bit fields; a span holds at most 8192)
+    // the two escape counts (16-bit fields; a span holds at most 8192).  A tile
+    // whose spans are all full takes an instance without per-span counts and
+    // masks (0.147 -> 0.139 ms at 2^28 values).
+    auto code_pairs = [&](auto full_tag) {
+        constexpr bool kFullT = decltype(full_tag)::value;
 #pragma unroll 1
-    for (uint32_t sp = 0; sp < kF8Spans; sp += 2) {
-        uint32_t w[2][8];
-        uint32_t cnt[2];
+        for (uint32_t sp = 0; sp < kF8Spans; sp += 2) {
+            uint32_t w[2][8];
+            uint32_t cnt[2];
 #pragma unroll
-        for (int h = 0; h < 2; h++) {
-            const uint64_t v0 = ((uint64_t)lt * kF8Spans + sp + h) * kTile;
-            const uint32_t nv = v0 < n_c ? (uint32_t)umin64(kTile, n_c - v0) : 0u;
-            cnt[h] = tv < nv ? min(32u, nv - tv) : 0u;
-            if (cnt[h] == 32) {
-                const uint8_t* q = a.x + (uint64_t)ci * a.L + v0 + tv;
-                const uint4 x0 = ld_v4_nc(q), x1 = ld_v4_nc(q + 16);
-                w[h][0] = x0.x; w[h][1] = x0.y; w[h][2] = x0.z; w[h][3] = x0.w;
-                w[h][4] = x1.x; w[h][5] = x1.y; w[h][6] = x1.z; w[h][7] = x1.w;
-            } else {
-                load32(a.x + (uint64_t)ci * a.L + v0 + tv, cnt[h], w[h]);
-            }
-        }
-        uint32_t escm[2] = {0, 0}, e[2][5];
-#pragma unroll
-        for (int h = 0; h < 2; h++) {
-#pragma unroll
-            for (int j = 0; j < 5; j++) e[h][j] = 0;
-            const uint32_t cnt_v = cnt[h];
-            if (cnt_v) {
+            for (int h = 0; h < 2; h++) {
                 const uint64_t v0 = ((uint64_t)lt * kF8Spans + sp + h) * kTile;
-                uint32_t R[8];
-                to_planes(w[h], R);
-                const uint32_t vm = cnt_v == 32 ? 0xFFFFFFFFu : ((1u << cnt_v) - 1u);
-                // d = E - E0 over the exponent planes R[m .. m+ebits)
-                uint32_t d[5], br = 0;
-#pragma unroll
-                for (int j = 0; j < 5; j++) {
-                    if (j < (int)f.ebits) {
-                        const uint32_t ej = R[f.mbits + j], k = bitmask_of(E0, j);
-                        e[h][j] = ej;
-                        d[j] = ej ^ k ^ br;
-                        br = borrow3(ej, k, br);
-                    } else {
-                        d[j] = 0;
-                    }
+                if constexpr (kFullT) {
+                    cnt[h] = 32;
+                } else {
+                    const uint32_t nv = v0 < n_c ? (uint32_t)umin64(kTile, n_c - v0) : 0u;
+                    cnt[h] = tv < nv ? min(32u, nv - tv) : 0u;
                 }
-                const uint32_t in = ~br & ~(d[3] | d[4]) & ~(d[0] & d[1] & d[2]) & vm;
-                escm[h] = ~in & vm;
-                // sign/mantissa planes: mantissa bits, then the sign
-                uint8_t* pt = pl + (v0 + tv) / 8;
-#pragma unroll
-                for (uint32_t q = 0; q < 4; q++)
-                    if (q < nsm) *reinterpret_cast<uint32_t*>(pt + q * plane) = (q < f.mbits ? R[q] : R[7]) & vm;
-                // code = d + 1 inside the window
-                *reinterpret_cast<uint32_t*>(pt + nsm * plane) = ~d[0] & in;
-                *reinterpret_cast<uint32_t*>(pt + (nsm + 1) * plane) = (d[1] ^ d[0]) & in;
-                *reinterpret_cast<uint32_t*>(pt + (nsm + 2) * plane) = (d[2] ^ (d[1] & d[0])) & in;
+                if (kFullT || cnt[h] == 32) {
+                    const uint8_t* q = a.x + (uint64_t)ci * a.L + v0 + tv;
+                    const uint4 x0 = ld_v4_nc(q), x1 = ld_v4_nc(q + 16);
+                    w[h][0] = x0.x; w[h][1] = x0.y; w[h][2] = x0.z; w[h][3] = x0.w;
+                    w[h][4] = x1.x; w[h][5] = x1.y; w[h][6] = x1.z; w[h][7] = x1.w;
+                } else {
+                    load32(a.x + (uint64_t)ci * a.L + v0 + tv, cnt[h], w[h]);
+                }
             }
-        }
-        unsigned long long tot;
-        const unsigned long long ex = block_excl_scan((unsigned long long)__popc(escm[0]) |
-                                                          (unsigned long long)__popc(escm[1]) << 16,
-                                                      s_warp[(sp >> 1) & 1u], &tot);
-        // the thread's escapes, in value order (raw exponent fields), staged
+            uint32_t escm[2] = {0, 0}, e[2][5];
 #pragma unroll
-        for (int h = 0; h < 2; h++) {
-            uint32_t m = escm[h], r = base + (uint32_t)((ex >> (16 * h)) & 0xFFFFull);
-            while (m) {
-                const int i = __ffs(m) - 1;
-                m &= m - 1;
-                uint32_t eb = 0;
+            for (int h = 0; h < 2; h++) {
 #pragma unroll
-                for (int j = 0; j < 5; j++) eb |= ((e[h][j] >> i) & 1u) << j;
-                s_esc[r++] = (uint8_t)eb;
+                for (int j = 0; j < 5; j++) e[h][j] = 0;
+                const uint32_t cnt_v = cnt[h];
+                if (kFullT || cnt_v) {
+                    const uint64_t v0 = ((uint64_t)lt * kF8Spans + sp + h) * kTile;
+                    uint32_t R[8];
+                    to_planes(w[h], R);
+                    const uint32_t vm = (kFullT || cnt_v == 32) ? 0xFFFFFFFFu : ((1u << cnt_v) - 1u);
+                    // d = E - E0 over the exponent planes R[m .. m+ebits)
+                    uint32_t d[5], br = 0;
+#pragma unroll
+                    for (int j = 0; j < 5; j++) {
+                        if (j < (int)f.ebits) {
+                            const uint32_t ej = R[f.mbits + j], k = bitmask_of(E0, j);
+                            e[h][j] = ej;
+                            d[j] = ej ^ k ^ br;
+                            br = borrow3(ej, k, br);
+                        } else {
+                            d[j] = 0;
+                        }
+                    }
+                    const uint32_t in = ~br & ~(d[3] | d[4]) & ~(d[0] & d[1] & d[2]) & vm;
+                    escm[h] = ~in & vm;
+                    // sign/mantissa planes: mantissa bits, then the sign
+                    uint8_t* pt = pl + (v0 + tv) / 8;
+#pragma unroll
+                    for (uint32_t q = 0; q < 4; q++)
+                        if (q < nsm) *reinterpret_cast<uint32_t*>(pt + q * plane) = (q < f.mbits ? R[q] : R[7]) & vm;
+                    // code = d + 1 inside the window
+                    *reinterpret_cast<uint32_t*>(pt + nsm * plane) = ~d[0] & in;
+                    *reinterpret_cast<uint32_t*>(pt + (nsm + 1) * plane) = (d[1] ^ d[0]) & in;
+                    *reinterpret_cast<uint32_t*>(pt + (nsm + 2) * plane) = (d[2] ^ (d[1] & d[0])) & in;
+                }
             }
-            if (t == 0) s_base[sp + h] = base;
-            base += (uint32_t)((tot >> (16 * h)) & 0xFFFFull);
+            unsigned long long tot;
+            const unsigned long long ex = block_excl_scan((unsigned long long)__popc(escm[0]) |
+                                                              (unsigned long long)__popc(escm[1]) << 16,
+                                                          s_warp[(sp >> 1) & 1u], &tot);
+            // the thread's escapes, in value order (raw exponent fields), staged
+#pragma unroll
+            for (int h = 0; h < 2; h++) {
+                uint32_t m = escm[h], r = base + (uint32_t)((ex >> (16 * h)) & 0xFFFFull);
+                while (m) {
+                    const int i = __ffs(m) - 1;
+                    m &= m - 1;
+                    uint32_t eb = 0;
+#pragma unroll
+                    for (int j = 0; j < 5; j++) eb |= ((e[h][j] >> i) & 1u) << j;
+                    s_esc[r++] = (uint8_t)eb;
+                }
+                if (t == 0) s_base[sp + h] = base;
+                base += (uint32_t)((tot >> (16 * h)) & 0xFFFFull);
+            }
+            // the next pair's scan writes the other s_warp buffer; this one is
+            // written again two pairs on, after the next scan's barrier
         }
-        // the next pair's scan writes the other s_warp buffer; this one is
-        // written again two pairs on, after the next scan's barrier
-    }
+    };
+    if (((uint64_t)lt + 1) * kF8TileV <= n_c) code_pairs(std::true_type{});
+    else code_pairs(std::false_type{});
     const unsigned long long P = tile_prefix(a.state, ci * tpt + lt, ci * tpt, base, &s_prefix,
                                              a.dstatus, a.abort);
     if ((uint32_t)t < kF8Spans) {
