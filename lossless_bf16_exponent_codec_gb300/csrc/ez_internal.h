@@ -24,12 +24,15 @@ struct ez_plan_s {
 
 namespace ezk {
 
-// Per-shard totals of the reuse split, summed with atomics by its tiles.
+// Per-shard record of the reuse split, written by the tile that holds the
+// shard's last value: the values by which the shard's last block falls short
+// of B when that block changed, else 0.  The shard's changed-block count is
+// the tile scan's last inclusive prefix, so its EXP length is
+// m = n_changed * B - tail (no atomics on a per-shard total: with one shard
+// every tile of the split would add to the same two words).
 struct ShardInfo {
-    unsigned long long m;          // exponents in the changed blocks
-    unsigned long long n_changed;  // changed blocks
-    unsigned int E0;               // window of the shard
-    unsigned int pad[11];
+    unsigned long long tail;
+    unsigned int pad[14];
 };
 
 struct WsView {

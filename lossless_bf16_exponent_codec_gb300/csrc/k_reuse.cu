@@ -503,13 +503,11 @@ __global__ void __launch_bounds__(kThreads, 5) k_reuse_hash_split(RuEnc a)
         const uint32_t agg = __shfl_sync(kFull, x, 31);
         if (t == 0) {
             st_relaxed(a.state + tp.state, (lt == 0 ? kFlagIncl : kFlagAgg) | agg);
-            uint64_t len = (uint64_t)agg * B;
-            if (lt == fin_tile && n_s && block_changed(s_bm, (uint32_t)((n_s - 1 - v0) >> log2B)))
-                len -= nb * B - n_s;
-            if (agg) {
-                atomicAdd(&a.info[ci].n_changed, (unsigned long long)agg);
-                atomicAdd(&a.info[ci].m, (unsigned long long)len);
-            }
+            // the shard's tail (its changed-block total is the tile scan's
+            // last inclusive prefix)
+            if (lt == fin_tile)
+                a.info[ci].tail = (n_s && block_changed(s_bm, (uint32_t)((n_s - 1 - v0) >> log2B)))
+                                      ? nb * B - n_s : 0ull;
         }
     }
     __syncthreads();
@@ -622,14 +620,11 @@ __global__ void __launch_bounds__(kThreads, (kCoded && !kHash) ? 4 : 6) k_reuse_
         const uint32_t agg = build_bitmap(s_gl, s_bm, s_pre, log2B);
         if (t == 0) {
             st_relaxed(a.state + tp.state, (lt == 0 ? kFlagIncl : kFlagAgg) | agg);
-            // per-shard totals: changed blocks and stream length m
-            uint64_t len = (uint64_t)agg * B;
-            if (lt == fin_tile && n_s && block_changed(s_bm, (uint32_t)((n_s - 1 - v0) >> log2B)))
-                len -= nb * B - n_s;
-            if (agg) {
-                atomicAdd(&a.info[ci].n_changed, (unsigned long long)agg);
-                atomicAdd(&a.info[ci].m, (unsigned long long)len);
-            }
+            // the shard's tail (its changed-block total is the tile scan's
+            // last inclusive prefix)
+            if (lt == fin_tile)
+                a.info[ci].tail = (n_s && block_changed(s_bm, (uint32_t)((n_s - 1 - v0) >> log2B)))
+                                      ? nb * B - n_s : 0ull;
         }
     }
     __syncthreads();
@@ -697,6 +692,16 @@ __global__ void __launch_bounds__(kThreads, (kCoded && !kHash) ? 4 : 6) k_reuse_
     if (nv == (uint32_t)kTile) split_tile(std::true_type{});
     else split_tile(std::false_type{});
 
+}
+
+// Changed blocks of a shard and its EXP length, after the tile scan: the
+// scan's last inclusive prefix of the shard (sc: its state array) and
+// m = n_changed * B - the tail the split recorded.
+__device__ __forceinline__ void ru_totals(const RuEnc& a, uint32_t ci, const unsigned long long* sc,
+                                          uint64_t& n_changed, uint64_t& m)
+{
+    n_changed = ld_relaxed(sc + a.tpc - 1);
+    m = n_changed * a.B - a.info[ci].tail;
 }
 
 // This tile's slice of the bitmap, read back from the payload: s_bm, the
@@ -777,7 +782,8 @@ __global__ void __launch_bounds__(kThreads, 6) k_reuse_place(RuEnc a)
     __syncthreads();
     load_bitmap(o, lt, nb, log2B, s_bm, s_pre, &s_agg);
     if (t == 0 && v0 < n_s) *reinterpret_cast<unsigned long long*>(o + off_idx + 8ull * lt) = P;
-    const uint64_t m = a.info[ci].m;
+    uint64_t n_changed, m;
+    ru_totals(a, ci, sc, n_changed, m);
 #pragma unroll
     for (int g = 0; g < kGroups; g++) {
         const uint32_t v = 8u * (uint32_t)(g * kThreads + t);
@@ -790,7 +796,6 @@ __global__ void __launch_bounds__(kThreads, 6) k_reuse_place(RuEnc a)
     }
     const uint32_t fin_tile = n_s ? (uint32_t)((n_s - 1) / kTile) : 0u;
     if (lt == fin_tile) {
-        const uint64_t n_changed = a.info[ci].n_changed;
         const uint64_t total = ru_bytes(n_s, B, m, false, 0);
         if (t < 64)
             o[t] = (uint8_t)ru_header_byte(t, a.cold ? 2u : 0u, 0u, B, r, n_s, n_changed, m, 0, total);
@@ -844,7 +849,8 @@ __global__ void __launch_bounds__(kThreads, 6) k_reuse_place32(RuEnc a)
     __syncthreads();
     load_bitmap(o, lt, nb, log2B, s_bm, s_pre, &s_agg);
     if (t == 0 && v0 < n_s) *reinterpret_cast<unsigned long long*>(o + off_idx + 8ull * lt) = P;
-    const uint64_t m = a.info[ci].m;
+    uint64_t n_changed, m;
+    ru_totals(a, ci, sc, n_changed, m);
     const uint32_t k = tv >> log2B;
     if (cnt_v && block_changed(s_bm, k)) {
         const uint64_t pos = (P + block_rank(s_bm, s_pre, k)) * B + (tv & (B - 1u));
@@ -859,7 +865,6 @@ __global__ void __launch_bounds__(kThreads, 6) k_reuse_place32(RuEnc a)
     }
     const uint32_t fin_tile = n_s ? (uint32_t)((n_s - 1) / kTile) : 0u;
     if (lt == fin_tile) {
-        const uint64_t n_changed = a.info[ci].n_changed;
         const uint64_t total = ru_bytes(n_s, B, m, false, 0);
         if (t < 64)
             o[t] = (uint8_t)ru_header_byte(t, a.cold ? 2u : 0u, 0u, B, r, n_s, n_changed, m, 0, total);
@@ -912,12 +917,13 @@ __global__ void __launch_bounds__(kPlaceThreads) k_reuse_place_coded(RuEnc a)
     const uint64_t spans = cdiv(n_s, kTile);
     const uint64_t off_idx = ru_off_idx(n_s, B), off_exp = ru_off_exp(n_s, B, true);
     uint8_t* o = a.out + (uint64_t)ci * a.slot;
-    const uint64_t m = a.info[ci].m;
+    const unsigned long long* sa = a.state + (uint64_t)ci * a.tpc;
+    const unsigned long long* sb = a.state_b + (uint64_t)ci * a.tpc;
+    uint64_t n_changed, m;
+    ru_totals(a, ci, sa, n_changed, m);
     const uint64_t plane = rup(cdiv(m, 8), 16);
     uint8_t* pl = o + off_exp;
     uint8_t* esc_sec = pl + 3 * plane;
-    const unsigned long long* sa = a.state + (uint64_t)ci * a.tpc;
-    const unsigned long long* sb = a.state_b + (uint64_t)ci * a.tpc;
     // staged planes (3 KB) and a 2 KB window of staged escapes, loaded with
     // the prefixes
     const uint8_t* pst = a.plbuf + (uint64_t)tp.state * 3 * (kTile / 8);
@@ -994,7 +1000,6 @@ __global__ void __launch_bounds__(kPlaceThreads) k_reuse_place_coded(RuEnc a)
         uint32_t E0 = a.stats[ci].E0;
         if (E0 > 249u) E0 = 0;
         const uint64_t n_esc = ld_relaxed(sb + a.tpc - 1);
-        const uint64_t n_changed = a.info[ci].n_changed;
         const uint64_t tot = ru_bytes(n_s, B, m, true, n_esc);
         if (t < 64)
             o[t] = (uint8_t)ru_header_byte(t, 1u | (a.cold ? 2u : 0u), E0, B, r, n_s, n_changed, m,
