@@ -694,14 +694,17 @@ __global__ void __launch_bounds__(kThreads, (kCoded && !kHash) ? 4 : 6) k_reuse_
 
 }
 
-// Changed blocks of a shard and its EXP length, after the tile scan: the
-// scan's last inclusive prefix of the shard (sc: its state array) and
-// m = n_changed * B - the tail the split recorded.
+// Changed blocks of a shard of n_s values and its EXP length, after the tile
+// scan: the scan's last inclusive prefix of the shard (sc: its state array)
+// and m = n_changed * B - the tail the split recorded.  Both are clamped to
+// the shard (n_changed <= its blocks, m <= n_s), so a scan that gave up on a
+// bounded wait (and reported it) cannot move a store out of the payload.
 __device__ __forceinline__ void ru_totals(const RuEnc& a, uint32_t ci, const unsigned long long* sc,
-                                          uint64_t& n_changed, uint64_t& m)
+                                          uint64_t n_s, uint64_t& n_changed, uint64_t& m)
 {
-    n_changed = ld_relaxed(sc + a.tpc - 1);
-    m = n_changed * a.B - a.info[ci].tail;
+    n_changed = umin64(ld_relaxed(sc + a.tpc - 1), ru_blocks(n_s, a.B));
+    const uint64_t full = n_changed * a.B, tail = a.info[ci].tail;
+    m = umin64(full > tail ? full - tail : 0ull, n_s);
 }
 
 // This tile's slice of the bitmap, read back from the payload: s_bm, the
@@ -783,7 +786,7 @@ __global__ void __launch_bounds__(kThreads, 6) k_reuse_place(RuEnc a)
     load_bitmap(o, lt, nb, log2B, s_bm, s_pre, &s_agg);
     if (t == 0 && v0 < n_s) *reinterpret_cast<unsigned long long*>(o + off_idx + 8ull * lt) = P;
     uint64_t n_changed, m;
-    ru_totals(a, ci, sc, n_changed, m);
+    ru_totals(a, ci, sc, n_s, n_changed, m);
 #pragma unroll
     for (int g = 0; g < kGroups; g++) {
         const uint32_t v = 8u * (uint32_t)(g * kThreads + t);
@@ -850,7 +853,7 @@ __global__ void __launch_bounds__(kThreads, 6) k_reuse_place32(RuEnc a)
     load_bitmap(o, lt, nb, log2B, s_bm, s_pre, &s_agg);
     if (t == 0 && v0 < n_s) *reinterpret_cast<unsigned long long*>(o + off_idx + 8ull * lt) = P;
     uint64_t n_changed, m;
-    ru_totals(a, ci, sc, n_changed, m);
+    ru_totals(a, ci, sc, n_s, n_changed, m);
     const uint32_t k = tv >> log2B;
     if (cnt_v && block_changed(s_bm, k)) {
         const uint64_t pos = (P + block_rank(s_bm, s_pre, k)) * B + (tv & (B - 1u));
@@ -920,7 +923,7 @@ __global__ void __launch_bounds__(kPlaceThreads) k_reuse_place_coded(RuEnc a)
     const unsigned long long* sa = a.state + (uint64_t)ci * a.tpc;
     const unsigned long long* sb = a.state_b + (uint64_t)ci * a.tpc;
     uint64_t n_changed, m;
-    ru_totals(a, ci, sa, n_changed, m);
+    ru_totals(a, ci, sa, n_s, n_changed, m);
     const uint64_t plane = rup(cdiv(m, 8), 16);
     uint8_t* pl = o + off_exp;
     uint8_t* esc_sec = pl + 3 * plane;
