@@ -51,7 +51,7 @@ struct RuEnc {
     unsigned long long* state;
     uint32_t* counter;
     uint32_t* abort;
-    ShardInfo* info;      // per-shard totals (changed blocks, m)
+    ShardInfo* info;      // per-shard records (the tail of the EXP length)
     ez_stats_t* stats;    // per shard record (caller's or workspace), coded only
     // coded only: staged planes (3 x 1 KB per tile), staged escapes (the
     // tile's own kTile bytes of a W*L stream), escape-count tile states
@@ -368,8 +368,8 @@ __device__ __forceinline__ bool hash_group_changed(const RuEnc& a, uint32_t ci, 
 // their sums with shuffles and the block's first thread decides; B = 8, 16:
 // the thread decides its own 32/B blocks), updating the hash cache; the
 // block bits go into the tile's bitmap, whose count is published for the
-// scan and added to the shard totals.  The place step then reads the changed
-// exponents from x.
+// scan; the shard's final tile records its tail.  The place step then reads
+// the changed exponents from x.
 __global__ void __launch_bounds__(kThreads, 5) k_reuse_hash_split(RuEnc a)
 {
     __shared__ uint32_t s_bm[32];
