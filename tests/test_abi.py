@@ -24,7 +24,8 @@ def declared_entry_points():
     for h in os.listdir(os.path.join(ROOT, "include")):
         if not h.endswith(".h"):
             continue
-        text = open(os.path.join(ROOT, "include", h)).read()
+        with open(os.path.join(ROOT, "include", h)) as f:
+            text = f.read()
         text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
         names += re.findall(r"^\s*[A-Za-z_][\w\s\*]*?\b(ez_\w+)\s*\(", text, flags=re.M)
     return sorted(set(names))

@@ -28,7 +28,8 @@ def _flip(rng, x, rate):
 
 
 def test_splitmix64_published_outputs(orc):
-    want = [int(l, 16) for l in open(GOLDEN) if l.strip() and not l.startswith("#")]
+    with open(GOLDEN) as f:
+        want = [int(l, 16) for l in f if l.strip() and not l.startswith("#")]
     assert orc.splitmix64(0, 3) == want
 
 

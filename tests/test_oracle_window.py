@@ -23,7 +23,9 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 
 
 def bf16_to_f64(x):
-    return (x.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    # NaN patterns stay NaN (numpy flags the cast of a signalling NaN)
+    with np.errstate(invalid="ignore"):
+        return (x.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
 
 
 def exact_sums(x):
